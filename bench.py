@@ -1,0 +1,368 @@
+#!/usr/bin/env python
+"""Benchmark of the deterministic gated BF16 FFN on GB300 (libdetffn).
+
+Step: one decode-shaped forward, M=32 tokens, H=4096, I=12288 (weights
+~302 MB, larger than the 129 MB L2; two weight copies alternate between steps
+so every step streams its weights from HBM).  `value` is the forward latency
+in microseconds (max over ranks; lower is better).  The same run also reports
+the M=1 and M=8 forward latencies and the M=32 forward+backward latency.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the only reference this build has) on
+a bounded sample of the same workload.  Under torchrun (N>1) each rank runs
+an independent replica (the FFN itself runs on one GPU); rank 0 prints one
+JSON line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_DEC, H, I = 32, 4096, 12288
+METRIC = "det. FFN fwd / fwd+bwd latency (µs) and HBM GB/s, M=1/8/32, H=4096, I=12288"
+WEIGHT_BYTES = 3 * H * I * 2
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "tree_gemm_exact": "k_exact.cu",
+    "decode_gateup": "k_decode.cu",
+    "decode_down": "k_decode.cu",
+    "tc_tree_gemm": "k_tc.cu",
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK, "fallback"
+
+
+def fwd_bytes(M):
+    return WEIGHT_BYTES + 2 * M * H * 2
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when the kernel source changed since the capture."""
+    src = KERNEL_SOURCES.get(kernel)
+    summ = os.path.join(ROOT, "profiles", "ncu_%s_%s.txt" % (kernel, workload))
+    if not src or not os.path.exists(summ):
+        return None
+    with open(os.path.join(ROOT, "gemm_deterministic_bf16_gb300", "csrc", src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    rec = {}
+    with open(summ) as f:
+        for ln in f:
+            if ":" in ln:
+                k, v = ln.split(":", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("kernel_source_sha256") != sha:
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def dist_setup(n_gpus):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, v):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_forward_rows(rows, seed=0):
+    """Times the CPU oracle on `rows` token rows of the M=32 decode forward
+    (rows are independent, so the M=32 latency scales by 32/rows)."""
+    import oracle
+    from gemm_deterministic_bf16_gb300.inputs import ffn_inputs
+    if seed not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS[seed] = ffn_inputs(M_DEC, H, I, seed=seed, with_dout=False)
+    d = _ORACLE_INPUTS[seed]
+    t0 = time.perf_counter()
+    oracle.ffn_forward(d["x"][:rows], d["Wg"], d["Wu"], d["Wd"])
+    return time.perf_counter() - t0
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.lib()
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_forward_rows(rows)
+    times = [oracle_forward_rows(rows) for _ in range(args.steps)]
+    us = statistics.median(times) * 1e6 * M_DEC / rows
+    sample = ("oracle (plain C, LANE8x8 leaves, all host threads) on %d of the 32 token rows of "
+              "the M=32, H=4096, I=12288 forward per step, scaled by 32/%d" % (rows, rows))
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) x, N(0,0.02) weights)",
+            "config": {"workload": "decode forward M=32 H=4096 I=12288", "M": M_DEC, "H": H, "I": I},
+            "cpu_baseline": {"value": us, "unit": "us", "cores": host_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import gemm_deterministic_bf16_gb300 as G
+    from gemm_deterministic_bf16_gb300 import build as libbuild
+    from gemm_deterministic_bf16_gb300.inputs import ffn_inputs
+
+    ws_n, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    libbuild.build()
+    path = {"auto": G.PATH_AUTO, "exact": G.PATH_EXACT, "tensor": G.PATH_TENSOR}[args.path]
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    # Two weight copies, alternated per step: every step streams 302 MB from HBM.
+    copies = []
+    for c in range(2):
+        d = ffn_inputs(M_DEC, H, I, seed=100 * rank + c)
+        copies.append({k: dev(v) for k, v in d.items()})
+    stream = torch.cuda.current_stream()
+
+    def fwd(M, c, out, ws):
+        t = copies[c]
+        G.detffn_forward(t["x"][:M], t["Wg"], t["Wu"], t["Wd"], out=out, ws=ws, path=path)
+
+    def timed(fn, steps, warmup):
+        for i in range(warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        barrier(ws_n)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps  # ms per step
+
+    outs = {M: torch.empty(M, H, dtype=torch.bfloat16, device="cuda") for M in (1, 8, 32)}
+    wss = {M: G.workspace(G.OP_FORWARD, M, H, I, 1, path) for M in (1, 8, 32)}
+
+    # Headline: M=32 forward.
+    with Clocks(local) as clk:
+        ms = timed(lambda i: fwd(M_DEC, i & 1, outs[M_DEC], wss[M_DEC]), args.steps, args.warmup)
+    ms = max_over_ranks(ws_n, ms)
+    us = ms * 1e3
+
+    # Per-kernel durations from events on the launching stream (same loop, profiling on).
+    G.detffn_profiling(True)
+    for i in range(args.steps):
+        fwd(M_DEC, i & 1, outs[M_DEC], wss[M_DEC])
+    prof = G.detffn_profile_read()
+    G.detffn_profiling(False)
+    launches = sum(v["launches"] for v in prof.values()) // max(1, args.steps)
+    top = max(prof.items(), key=lambda kv: kv[1]["ms"])
+    pk, how = peaks()
+    kname, kv = top
+    per_launch_ms = kv["ms"] / kv["launches"]
+    bytes_per_launch = kv["bytes"] / kv["launches"]
+    achieved = bytes_per_launch / (per_launch_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                "traffic": traffic_for(kname, "decode_m32"), "peak_source": how,
+                "share": kv["ms"] / sum(v["ms"] for v in prof.values()),
+                "algorithmic_bytes_per_launch": bytes_per_launch}
+
+    # Other decode sizes and the M=32 training step (forward with saves + backward).
+    extra = {}
+    for M in (1, 8):
+        extra["fwd_us_M%d" % M] = 1e3 * max_over_ranks(
+            ws_n, timed(lambda i, M=M: fwd(M, i & 1, outs[M], wss[M]), args.steps, args.warmup))
+        extra["fwd_gbs_M%d" % M] = fwd_bytes(M) / (extra["fwd_us_M%d" % M] * 1e-6) / 1e9
+    gsave = torch.empty(M_DEC, I, dtype=torch.bfloat16, device="cuda")
+    usave = torch.empty_like(gsave)
+    grads = [torch.empty(I, H, dtype=torch.bfloat16, device="cuda") for _ in range(2)] + \
+        [torch.empty(H, I, dtype=torch.bfloat16, device="cuda")]
+    dX = torch.empty(M_DEC, H, dtype=torch.bfloat16, device="cuda")
+    wsb = G.workspace(G.OP_BACKWARD, M_DEC, H, I, 1, path)
+    wsf = G.workspace(G.OP_FORWARD, M_DEC, H, I, 1, path)
+
+    def train_step(i):
+        t = copies[i & 1]
+        G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], out=outs[M_DEC], gate_save=gsave,
+                         up_save=usave, ws=wsf, path=path)
+        G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], gsave, usave, t["dOut"], dX=dX,
+                          dWg=grads[0], dWu=grads[1], dWd=grads[2], ws=wsb, path=path)
+
+    tsteps = max(3, args.steps // 4)
+    extra["fwd_bwd_us_M32"] = 1e3 * max_over_ranks(ws_n, timed(train_step, tsteps, 3))
+    extra["fwd_bwd_gbs_M32"] = 3 * WEIGHT_BYTES / (extra["fwd_bwd_us_M32"] * 1e-6) / 1e9
+
+    # End to end through the public API: pinned host x in, host out back, every step.
+    xh = torch.empty(M_DEC, H, dtype=torch.bfloat16).pin_memory()
+    xh.copy_(copies[0]["x"].cpu())
+    oh = torch.empty(M_DEC, H, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty(M_DEC, H, dtype=torch.bfloat16, device="cuda")
+
+    def e2e_step(i):
+        t = copies[i & 1]
+        xd.copy_(xh, non_blocking=True)
+        G.detffn_forward(xd, t["Wg"], t["Wu"], t["Wd"], out=outs[M_DEC], ws=wss[M_DEC], path=path)
+        oh.copy_(outs[M_DEC], non_blocking=True)
+
+    e2e_us = 1e3 * max_over_ranks(ws_n, timed(e2e_step, args.steps, args.warmup))
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        t = oracle_forward_rows(args.ref_rows)
+        cpu = {"value": t * 1e6 * M_DEC / args.ref_rows, "unit": "us", "cores": host_cores(),
+               "kind": "oracle",
+               "sample": "one oracle forward on %d of the 32 token rows, scaled by 32/%d"
+                         % (args.ref_rows, args.ref_rows)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": us, "unit": "us", "n_gpus": ws_n, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded N(0,1) x and dOut, N(0,0.02) weights, [out,in] layout)",
+                "config": {"workload": "decode forward M=32 H=4096 I=12288", "M": M_DEC, "H": H,
+                           "I": I, "path": args.path,
+                           "l2": "weights 302 MB > 129 MB L2, two copies alternated per step",
+                           "replicas": ws_n},
+                "hbm_gbs": fwd_bytes(M_DEC) / (us * 1e-6) / 1e9,
+                "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": M_DEC * H * 2,
+                        "d2h_bytes_per_step": M_DEC * H * 2},
+                "gpu_launches": launches * args.steps, "clocks": clk.summary(),
+                "kernels": {k: {"launches_per_step": v["launches"] // max(1, args.steps),
+                                "us_per_step": 1e3 * v["ms"] / max(1, args.steps)}
+                            for k, v in prof.items()},
+                "extra": extra}
+        print(json.dumps(line))
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", choices=["auto", "exact", "tensor"], default="auto")
+    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

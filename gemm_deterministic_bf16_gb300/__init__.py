@@ -1,7 +1,15 @@
 """Deterministic gated BF16 FFN for GB300 (sm_103a): Python binding of libdetffn.
 
 The compute path is the C-ABI library ``libdetffn.so`` built from ``csrc/``;
-this package only marshals arguments (tensor pointers, sizes, the current CUDA
-stream).  Importing the package does not load the library; the first call
-does, and raises if the library is missing -- there is no CPU fallback.
+the binding in ``detffn.py`` only marshals arguments (tensor pointers, sizes,
+the current CUDA stream).  Importing the package does not load the library;
+the first call does, and raises if the library is missing -- there is no CPU
+fallback.
 """
+from .detffn import (  # noqa: F401
+    BF16, F16, F32, OP_BACKWARD, OP_FORWARD, OP_FORWARD_SHARDED, OP_WGRAD_CHUNKED, PATH_AUTO,
+    PATH_EXACT, PATH_TENSOR, DetFFNError, detffn_backward, detffn_forward,
+    detffn_forward_sharded, detffn_get_status, detffn_rank_tree_reduce, detffn_silu_tables,
+    detffn_profile_read, detffn_profiling, detffn_tree_gemm, detffn_wgrad_chunked,
+    detffn_workspace_size, workspace,
+)

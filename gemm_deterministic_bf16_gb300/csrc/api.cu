@@ -1,0 +1,762 @@
+// api.cu -- the C ABI of libdetffn: argument checks, scratch layout, dispatch.
+//
+// Every call validates its arguments on the host and returns an error before
+// launching anything; every launch goes to the caller's stream.  Nothing here
+// allocates device memory except detffn_create (tables and status word).
+#include <float.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+using namespace detffn;
+
+struct detffn_handle_s {
+  int device = 0;
+  int sm_count = 0;
+  uint16_t* d_silu = nullptr;   // [65536] BF16 SiLU by gate bit pattern
+  float* d_dsilu = nullptr;     // [65536] FP32 SiLU' by gate bit pattern
+  int* d_status = nullptr;      // device status word (bounded waits)
+  std::vector<uint16_t> h_silu;
+  std::vector<float> h_dsilu;
+  // Measurement: event pairs around launches while profiling is on.
+  struct Rec {
+    const char* name;
+    cudaEvent_t a, b;
+    double bytes, flops;
+  };
+  bool prof = false;
+  std::vector<Rec> recs;
+};
+
+// ---------------------------------------------------------------------------
+// SiLU tables, correctly rounded (the value of the real function rounded to
+// FP32, and for SiLU then to BF16).  Method: binary64 evaluation; entries
+// whose binary64 value lies within 2^-40 (relative) of an FP32 rounding
+// boundary are re-evaluated in long double.  For |g| < 2^-10, SiLU'(g) is
+// 1/2 + g/2 - g^3/12 + O(g^5): 1/2 + g/2 is exact in binary64 and the cubic
+// term only decides an exact FP32 tie, toward the sign of -g.
+// ---------------------------------------------------------------------------
+namespace {
+
+float widen_bf16(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+uint16_t bf16_rne_host(float v) {
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)(((u >> 16) & 0x8000u) | 0x7fc0u);
+  const uint32_t lsb = (u >> 16) & 1u;
+  return (uint16_t)((u + 0x7fffu + lsb) >> 16);
+}
+
+// Distance from v to the nearest FP32 midpoint, relative to |v|.
+double tie_gap(double v) {
+  const float f = (float)v;
+  const double d = v - (double)f;
+  if (d == 0.0) return INFINITY;
+  const float nb = nextafterf(f, d > 0 ? INFINITY : -INFINITY);
+  const double mid = 0.5 * ((double)f + (double)nb);
+  return fabs(v - mid) / fabs(v);
+}
+
+void silu_pair_ld(double g, float* y, float* d) {
+  const long double G = (long double)g;
+  const long double t = expl(-G);
+  const long double s = 1.0L / (1.0L + t);
+  const long double oms = t / (1.0L + t);
+  *y = (float)(G * s);
+  *d = (float)(s * (1.0L + G * oms));
+}
+
+void build_silu_tables(std::vector<uint16_t>& silu, std::vector<float>& dsilu) {
+  silu.assign(65536, 0);
+  dsilu.assign(65536, 0.0f);
+  for (uint32_t i = 0; i < 65536u; ++i) {
+    const float gf = widen_bf16((uint16_t)i);
+    const double g = gf;
+    float y, d;
+    if (g != g) {
+      silu[i] = bf16_rne_host(gf);
+      dsilu[i] = gf;
+      continue;
+    }
+    if (g > 200.0) {            // sigma(g) = 1 to far below FP32 resolution
+      y = gf;
+      d = 1.0f;
+    } else if (g < -200.0) {    // both values are below 2^-150 in magnitude
+      y = -0.0f;
+      d = -0.0f;
+    } else {
+      const double t = exp(-g);
+      const double s = 1.0 / (1.0 + t);
+      const double oms = t / (1.0 + t);
+      const double yd = g * s;
+      const double dd = s * (1.0 + g * oms);
+      y = (float)yd;
+      d = (float)dd;
+      if (fabs(g) < 0x1p-10) {
+        const double lead = 0.5 + 0.5 * g;  // exact
+        d = (float)lead;
+        const double diff = lead - (double)d;
+        if (diff != 0.0) {
+          const float nb = nextafterf(d, diff > 0 ? INFINITY : -INFINITY);
+          const double half = 0.5 * ((double)nb - (double)d);
+          // At an exact tie the true value lies on the side of -g: take the
+          // neighbour when that side is the neighbour's.
+          if (diff == half && ((g < 0) == (diff > 0))) d = nb;
+        }
+        if (tie_gap(yd) < 0x1p-40) {
+          float d_unused;
+          silu_pair_ld(g, &y, &d_unused);
+        }
+      } else if (tie_gap(yd) < 0x1p-40 || tie_gap(dd) < 0x1p-40) {
+        silu_pair_ld(g, &y, &d);
+      }
+    }
+    silu[i] = bf16_rne_host(y);
+    dsilu[i] = d;
+  }
+}
+
+std::once_flag g_tab_once;
+std::vector<uint16_t> g_silu;
+std::vector<float> g_dsilu;
+
+void host_tables() {
+  std::call_once(g_tab_once, [] { build_silu_tables(g_silu, g_dsilu); });
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Argument checks and scratch layout
+// ---------------------------------------------------------------------------
+namespace {
+
+struct Opts {
+  int path = DETFFN_PATH_AUTO;
+  int shards = 1;
+  long long spin_limit = 0;
+};
+
+detffn_status read_opts(const detffn_options* o, Opts* out) {
+  Opts r;
+  if (o) {
+    if (o->leaf_width != 0 && o->leaf_width != kLeaf) return DETFFN_ERR_UNSUPPORTED;
+    if (o->path < DETFFN_PATH_AUTO || o->path > DETFFN_PATH_TENSOR) return DETFFN_ERR_INVALID_ARG;
+    if (!(o->shards == 0 || o->shards == 1 || o->shards == 2 || o->shards == 4 || o->shards == 8))
+      return DETFFN_ERR_INVALID_ARG;
+    if (o->spin_limit < 0) return DETFFN_ERR_INVALID_ARG;
+    r.path = o->path;
+    r.shards = o->shards ? o->shards : 1;
+    r.spin_limit = o->spin_limit;
+  }
+  *out = r;
+  return DETFFN_OK;
+}
+
+// The kernel family a call uses: a function of M (tokens) and the requested
+// path only.  The exact CUDA-core family is the only one built in this file;
+// other families register through dispatch below.
+enum Family { kExact = 0 };
+
+detffn_status pick_family(const Opts& o, long long M, Family* f) {
+  (void)M;
+  if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_UNSUPPORTED;
+  *f = kExact;
+  return DETFFN_OK;
+}
+
+struct Arena {
+  char* base;
+  size_t off = 0;
+  explicit Arena(void* b) : base(static_cast<char*>(b)) {}
+  template <class T>
+  T* take(long long count) {
+    off = (off + 255) & ~(size_t)255;
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += (size_t)count * sizeof(T);
+    return p;
+  }
+};
+
+struct FwdWs { uint16_t *gate, *up, *h, *parts; };
+FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k) {
+  FwdWs w;
+  w.gate = a.take<uint16_t>(M * I);
+  w.up = a.take<uint16_t>(M * I);
+  w.h = a.take<uint16_t>(M * I);
+  w.parts = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
+  return w;
+}
+
+struct BwdWs { uint16_t *dh, *dU, *dG, *h, *cg, *cu, *cgs, *cus; };
+BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k) {
+  BwdWs w;
+  w.dh = a.take<uint16_t>(M * I);
+  w.dU = a.take<uint16_t>(M * I);
+  w.dG = a.take<uint16_t>(M * I);
+  w.h = a.take<uint16_t>(M * I);
+  w.cg = a.take<uint16_t>(M * H);
+  w.cu = a.take<uint16_t>(M * H);
+  w.cgs = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
+  w.cus = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
+  return w;
+}
+
+struct ChunkWs { uint16_t *x, *dO, *g, *u, *dh, *dU, *dG, *h; };
+ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I) {
+  ChunkWs w;
+  w.x = a.take<uint16_t>(M * H);
+  w.dO = a.take<uint16_t>(M * H);
+  w.g = a.take<uint16_t>(M * I);
+  w.u = a.take<uint16_t>(M * I);
+  w.dh = a.take<uint16_t>(M * I);
+  w.dU = a.take<uint16_t>(M * I);
+  w.dG = a.take<uint16_t>(M * I);
+  w.h = a.take<uint16_t>(M * I);
+  return w;
+}
+
+size_t ws_bytes_for(int op, long long M, long long H, long long I, int k) {
+  Arena a(nullptr);
+  switch (op) {
+    case DETFFN_OP_FORWARD: plan_forward(a, M, H, I, 1); break;
+    case DETFFN_OP_FORWARD_SHARDED: plan_forward(a, M, H, I, k); break;
+    case DETFFN_OP_BACKWARD: plan_backward(a, M, H, I, k); break;
+    case DETFFN_OP_WGRAD_CHUNKED: plan_chunked(a, M, H, I); break;
+    default: return 0;
+  }
+  return (a.off + 255) & ~(size_t)255;
+}
+
+detffn_status check_ws(void* ws, size_t have, size_t need) {
+  if (need == 0) return DETFFN_OK;
+  if (!ws || ((uintptr_t)ws & 255u) != 0 || have < need) return DETFFN_ERR_WORKSPACE;
+  return DETFFN_OK;
+}
+
+bool overlap(const void* a, long long na, const void* b, long long nb) {
+  if (!a || !b || na <= 0 || nb <= 0) return false;
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
+bool aligned2(const void* p) { return ((uintptr_t)p & 1u) == 0; }
+
+detffn_status check_sizes(long long M, long long H, long long I) {
+  if (M < 0 || H <= 0 || I <= 0) return DETFFN_ERR_SHAPE;
+  if (H > kMaxK || I > kMaxK || M > kMaxK) return DETFFN_ERR_SHAPE;
+  return DETFFN_OK;
+}
+
+detffn_status cu(cudaError_t e) { return e == cudaSuccess ? DETFFN_OK : DETFFN_ERR_CUDA; }
+
+#define TRY(expr)                              \
+  do {                                         \
+    detffn_status _s = (expr);                 \
+    if (_s != DETFFN_OK) return _s;            \
+  } while (0)
+#define TRYCU(expr) TRY(cu(expr))
+
+// Runs `launch`; while profiling, brackets it with an event pair on `st`.
+template <class F>
+detffn_status timed(detffn_handle h, cudaStream_t st, const char* name, double bytes,
+                    double flops, F&& launch) {
+  if (!h || !h->prof) return launch();
+  detffn_handle_s::Rec r{name, nullptr, nullptr, bytes, flops};
+  if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return DETFFN_ERR_CUDA;
+  cudaEventRecord(r.a, st);
+  const detffn_status s = launch();
+  cudaEventRecord(r.b, st);
+  h->recs.push_back(r);
+  return s;
+}
+
+// One tree contraction on the chosen family.
+detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long long R, long long C,
+                        long long K, uint16_t* out, long long o_rs, cudaStream_t st) {
+  (void)f;
+  const double bytes = 2.0 * ((double)R * K + (double)C * K + (double)R * C);
+  return timed(h, st, "tree_gemm_exact", bytes, 2.0 * R * C * K,
+               [&] { return cu(launch_tree_gemm_exact(A, B, R, C, K, out, o_rs, st)); });
+}
+
+detffn_status silu_mul(detffn_handle h, const uint16_t* g, const uint16_t* u, uint16_t* hh,
+                       long long rows, long long cols, long long ld, cudaStream_t st) {
+  return timed(h, st, "silu_mul", 6.0 * rows * cols, 0.0,
+               [&] { return cu(launch_silu_mul(g, u, hh, rows, cols, ld, h->d_silu, st)); });
+}
+
+detffn_status silu_bwd(detffn_handle h, const uint16_t* dh, const uint16_t* g, const uint16_t* u,
+                       uint16_t* dU, uint16_t* dG, long long n, cudaStream_t st) {
+  return timed(h, st, "silu_bwd", 10.0 * n, 0.0, [&] {
+    return cu(launch_silu_bwd(dh, g, u, dU, dG, n, h->d_silu, h->d_dsilu, st));
+  });
+}
+
+detffn_status add_bf16(detffn_handle h, const uint16_t* a, const uint16_t* b, uint16_t* out,
+                       long long n, cudaStream_t st) {
+  return timed(h, st, "add_bf16", 6.0 * n, 0.0, [&] { return cu(launch_add_bf16(a, b, out, n, st)); });
+}
+
+detffn_status rank_tree_bf16(detffn_handle h, const void* const* in, int k, void* out,
+                             long long count, cudaStream_t st) {
+  return timed(h, st, "rank_tree", 2.0 * (k + 1) * count, 0.0, [&] {
+    return cu(launch_rank_tree(in, k, out, count, DETFFN_BF16, h->sm_count, st));
+  });
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Exported calls
+// ---------------------------------------------------------------------------
+extern "C" {
+
+const char* detffn_status_string(detffn_status s) {
+  switch (s) {
+    case DETFFN_OK: return "ok";
+    case DETFFN_ERR_INVALID_ARG: return "invalid argument";
+    case DETFFN_ERR_SHAPE: return "unsupported or inconsistent sizes";
+    case DETFFN_ERR_ALIGN: return "misaligned pointer";
+    case DETFFN_ERR_UNSUPPORTED: return "unsupported option";
+    case DETFFN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DETFFN_ERR_CUDA: return "CUDA error";
+    case DETFFN_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+detffn_status detffn_create(detffn_handle* out, int device) {
+  if (!out) return DETFFN_ERR_INVALID_ARG;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n) return DETFFN_ERR_INVALID_ARG;
+  int prev = 0;
+  TRYCU(cudaGetDevice(&prev));
+  TRYCU(cudaSetDevice(device));
+  host_tables();
+  detffn_handle h = new detffn_handle_s();
+  h->device = device;
+  h->h_silu = g_silu;
+  h->h_dsilu = g_dsilu;
+  detffn_status st = DETFFN_OK;
+  do {
+    if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+    if (cudaMalloc(&h->d_silu, 65536 * sizeof(uint16_t)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+    if (cudaMalloc(&h->d_dsilu, 65536 * sizeof(float)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+    if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+    if (cudaMemcpy(h->d_silu, h->h_silu.data(), 65536 * sizeof(uint16_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(h->d_dsilu, h->h_dsilu.data(), 65536 * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+  } while (0);
+  cudaSetDevice(prev);
+  if (st != DETFFN_OK) {
+    detffn_destroy(h);
+    return st;
+  }
+  *out = h;
+  return DETFFN_OK;
+}
+
+detffn_status detffn_destroy(detffn_handle h) {
+  if (!h) return DETFFN_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(h->device);
+  if (h->d_silu) cudaFree(h->d_silu);
+  if (h->d_dsilu) cudaFree(h->d_dsilu);
+  if (h->d_status) cudaFree(h->d_status);
+  for (auto& r : h->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  cudaSetDevice(prev);
+  delete h;
+  return DETFFN_OK;
+}
+
+detffn_status detffn_workspace_size(detffn_handle h, int op, long long M, long long H, long long I,
+                                    int k, const detffn_options* opts, size_t* bytes) {
+  (void)h;
+  if (!bytes) return DETFFN_ERR_INVALID_ARG;
+  Opts o;
+  TRY(read_opts(opts, &o));
+  TRY(check_sizes(M, H, I));
+  if (op < DETFFN_OP_FORWARD || op > DETFFN_OP_WGRAD_CHUNKED) return DETFFN_ERR_INVALID_ARG;
+  if (op == DETFFN_OP_BACKWARD && k <= 1) k = o.shards;
+  if (!(k == 1 || k == 2 || k == 4 || k == 8)) return DETFFN_ERR_INVALID_ARG;
+  *bytes = ws_bytes_for(op, M, H, I, k);
+  return DETFFN_OK;
+}
+
+detffn_status detffn_silu_tables(detffn_handle h, unsigned short* silu_bf16, float* dsilu_f32) {
+  const std::vector<uint16_t>* s;
+  const std::vector<float>* d;
+  if (h) {
+    s = &h->h_silu;
+    d = &h->h_dsilu;
+  } else {
+    host_tables();
+    s = &g_silu;
+    d = &g_dsilu;
+  }
+  if (silu_bf16) memcpy(silu_bf16, s->data(), 65536 * sizeof(uint16_t));
+  if (dsilu_f32) memcpy(dsilu_f32, d->data(), 65536 * sizeof(float));
+  return DETFFN_OK;
+}
+
+detffn_status detffn_get_status(detffn_handle h, void* stream) {
+  if (!h) return DETFFN_ERR_INVALID_ARG;
+  TRYCU(cudaStreamSynchronize((cudaStream_t)stream));
+  int v = 0;
+  TRYCU(cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost));
+  TRYCU(cudaMemset(h->d_status, 0, sizeof(int)));
+  return (detffn_status)v;
+}
+
+}  // extern "C"
+
+namespace {
+
+detffn_status check_ffn_ptrs(const void* x, const void* Wg, const void* Wu, const void* Wd) {
+  if (!x || !Wg || !Wu || !Wd) return DETFFN_ERR_INVALID_ARG;
+  if (!aligned2(x) || !aligned2(Wg) || !aligned2(Wu) || !aligned2(Wd)) return DETFFN_ERR_ALIGN;
+  return DETFFN_OK;
+}
+
+// Forward of one shard (or of everything when w == I, s == 0): gate/up for
+// rows [s*w, (s+1)*w) of Wg/Wu, then h on the same columns.
+detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const uint16_t* Wg,
+                           const uint16_t* Wu, uint16_t* gate, uint16_t* up, uint16_t* hh,
+                           long long M, long long H, long long I, long long s, long long w,
+                           cudaStream_t st) {
+  const Strided X{x, H, 1};
+  TRY(tree_gemm(h, f, X, Strided{Wg + s * w * H, H, 1}, M, w, H, gate + s * w, I, st));
+  TRY(tree_gemm(h, f, X, Strided{Wu + s * w * H, H, 1}, M, w, H, up + s * w, I, st));
+  return silu_mul(h, gate + s * w, up + s * w, hh + s * w, M, w, I, st);
+}
+
+detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const void* Wu,
+                           const void* Wd, void* out, void* gate_save, void* up_save, long long M,
+                           long long H, long long I, int k, void* ws, size_t ws_bytes,
+                           void* stream, const detffn_options* opts) {
+  if (!h || !out) return DETFFN_ERR_INVALID_ARG;
+  Opts o;
+  TRY(read_opts(opts, &o));
+  TRY(check_sizes(M, H, I));
+  TRY(check_ffn_ptrs(x, Wg, Wu, Wd));
+  if (!aligned2(out) || !aligned2(gate_save) || !aligned2(up_save)) return DETFFN_ERR_ALIGN;
+  if ((gate_save == nullptr) != (up_save == nullptr)) return DETFFN_ERR_INVALID_ARG;
+  if (!(k == 1 || k == 2 || k == 4 || k == 8)) return DETFFN_ERR_INVALID_ARG;
+  if (k > 1 && (I % k != 0 || (I / k) % kLeaf != 0 || (I / k) / kLeaf < 2)) return DETFFN_ERR_SHAPE;
+  const long long bx = 2 * M * H, bw = 2 * I * H, bmi = 2 * M * I;
+  const void* ins[4] = {x, Wg, Wu, Wd};
+  const long long nin[4] = {bx, bw, bw, bw};
+  void* outs[3] = {out, gate_save, up_save};
+  const long long nout[3] = {bx, bmi, bmi};
+  for (int a = 0; a < 3; ++a) {
+    for (int b = 0; b < 4; ++b)
+      if (overlap(outs[a], nout[a], ins[b], nin[b])) return DETFFN_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlap(outs[a], nout[a], outs[b], nout[b])) return DETFFN_ERR_INVALID_ARG;
+  }
+  TRY(check_ws(ws, ws_bytes, ws_bytes_for(k > 1 ? DETFFN_OP_FORWARD_SHARDED : DETFFN_OP_FORWARD, M, H, I, k)));
+  if (M == 0) return DETFFN_OK;
+  Family f;
+  TRY(pick_family(o, M, &f));
+  TRYCU(cudaSetDevice(h->device));
+  cudaStream_t st = (cudaStream_t)stream;
+  Arena a(ws);
+  FwdWs w = plan_forward(a, M, H, I, k);
+  uint16_t* gate = gate_save ? (uint16_t*)gate_save : w.gate;
+  uint16_t* up = up_save ? (uint16_t*)up_save : w.up;
+  const uint16_t* X = (const uint16_t*)x;
+  const uint16_t* WG = (const uint16_t*)Wg;
+  const uint16_t* WU = (const uint16_t*)Wu;
+  const uint16_t* WD = (const uint16_t*)Wd;
+  if (k == 1) {
+    TRY(gateup_slice(h, f, X, WG, WU, gate, up, w.h, M, H, I, 0, I, st));
+    return tree_gemm(h, f, Strided{w.h, I, 1}, Strided{WD, I, 1}, M, H, I, (uint16_t*)out, H, st);
+  }
+  // Tensor-parallel emulation: shard s owns I/k rows of Wg/Wu and columns of Wd.
+  const long long sw = I / k;
+  for (long long s = 0; s < k; ++s) {
+    TRY(gateup_slice(h, f, X, WG, WU, gate, up, w.h, M, H, I, s, sw, st));
+    TRY(tree_gemm(h, f, Strided{w.h + s * sw, I, 1}, Strided{WD + s * sw, I, 1}, M, H, sw,
+                  w.parts + s * M * H, H, st));
+  }
+  const void* parts[8];
+  for (int s = 0; s < k; ++s) parts[s] = w.parts + (long long)s * M * H;
+  return rank_tree_bf16(h, parts, k, out, M * H, st);
+}
+
+}  // namespace
+
+extern "C" detffn_status detffn_forward(detffn_handle h, const void* x, const void* Wg,
+                                        const void* Wu, const void* Wd, void* out,
+                                        void* gate_save, void* up_save, long long M, long long H,
+                                        long long I, void* ws, size_t ws_bytes, void* stream,
+                                        const detffn_options* opts) {
+  return forward_impl(h, x, Wg, Wu, Wd, out, gate_save, up_save, M, H, I, 1, ws, ws_bytes, stream, opts);
+}
+
+extern "C" detffn_status detffn_forward_sharded(detffn_handle h, const void* x, const void* Wg,
+                                                const void* Wu, const void* Wd, void* out,
+                                                void* gate_save, void* up_save, long long M,
+                                                long long H, long long I, int k, void* ws,
+                                                size_t ws_bytes, void* stream,
+                                                const detffn_options* opts) {
+  return forward_impl(h, x, Wg, Wu, Wd, out, gate_save, up_save, M, H, I, k, ws, ws_bytes, stream, opts);
+}
+
+namespace {
+
+// Row-wise backward stages for rows [r0, r0+rows): dh, then dU and dG.
+detffn_status rowwise_bwd(detffn_handle h, Family f, const uint16_t* dOut, const uint16_t* Wd,
+                          const uint16_t* gate, const uint16_t* up, uint16_t* dh, uint16_t* dU,
+                          uint16_t* dG, long long rows, long long H, long long I,
+                          cudaStream_t st) {
+  // dh[m, i] = T_{n<H}(dOut[m, n], Wd[n, i]): B row i has K stride I.
+  TRY(tree_gemm(h, f, Strided{dOut, H, 1}, Strided{Wd, 1, I}, rows, I, H, dh, I, st));
+  return silu_bwd(h, dh, gate, up, dU, dG, rows * I, st);
+}
+
+// Weight gradients over K = M tokens from row-major [M, .] stage tensors.
+detffn_status wgrads(detffn_handle h, Family f, const uint16_t* x, const uint16_t* dOut, const uint16_t* hh,
+                     const uint16_t* dU, const uint16_t* dG, uint16_t* dWg, uint16_t* dWu,
+                     uint16_t* dWd, long long M, long long H, long long I, cudaStream_t st) {
+  // dWd[n, i] = T_m(dOut[m, n], h[m, i])
+  TRY(tree_gemm(h, f, Strided{dOut, 1, H}, Strided{hh, 1, I}, H, I, M, dWd, I, st));
+  // dWg[i, n] = T_m(dG[m, i], x[m, n]); dWu likewise with dU.
+  TRY(tree_gemm(h, f, Strided{dG, 1, I}, Strided{x, 1, H}, I, H, M, dWg, H, st));
+  return tree_gemm(h, f, Strided{dU, 1, I}, Strided{x, 1, H}, I, H, M, dWu, H, st);
+}
+
+}  // namespace
+
+extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const void* Wg,
+                                         const void* Wu, const void* Wd, const void* gate,
+                                         const void* up, const void* dOut, void* dX, void* dWg,
+                                         void* dWu, void* dWd, void* dh_save, void* dU_save,
+                                         void* dG_save, long long M, long long H, long long I,
+                                         void* ws, size_t ws_bytes, void* stream,
+                                         const detffn_options* opts) {
+  if (!h || !gate || !up || !dOut || !dX || !dWg || !dWu || !dWd) return DETFFN_ERR_INVALID_ARG;
+  Opts o;
+  TRY(read_opts(opts, &o));
+  TRY(check_sizes(M, H, I));
+  TRY(check_ffn_ptrs(x, Wg, Wu, Wd));
+  const void* al[] = {gate, up, dOut, dX, dWg, dWu, dWd, dh_save, dU_save, dG_save};
+  for (const void* p : al)
+    if (!aligned2(p)) return DETFFN_ERR_ALIGN;
+  const int k = o.shards;
+  if (k > 1 && (I % k != 0 || (I / k) % kLeaf != 0 || (I / k) / kLeaf < 2)) return DETFFN_ERR_SHAPE;
+  const long long bx = 2 * M * H, bw = 2 * I * H, bmi = 2 * M * I;
+  const void* ins[7] = {x, Wg, Wu, Wd, gate, up, dOut};
+  const long long nin[7] = {bx, bw, bw, bw, bmi, bmi, bx};
+  void* outs[7] = {dX, dWg, dWu, dWd, dh_save, dU_save, dG_save};
+  const long long nout[7] = {bx, bw, bw, bw, bmi, bmi, bmi};
+  for (int a = 0; a < 7; ++a) {
+    for (int b = 0; b < 7; ++b)
+      if (overlap(outs[a], nout[a], ins[b], nin[b])) return DETFFN_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 7; ++b)
+      if (overlap(outs[a], nout[a], outs[b], nout[b])) return DETFFN_ERR_INVALID_ARG;
+  }
+  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_BACKWARD, M, H, I, k)));
+  if (M == 0) {
+    // No tokens: the weight gradients are empty sums (+0); nothing else exists.
+    TRYCU(cudaSetDevice(h->device));
+    cudaStream_t st = (cudaStream_t)stream;
+    TRYCU(cudaMemsetAsync(dWg, 0, (size_t)bw, st));
+    TRYCU(cudaMemsetAsync(dWu, 0, (size_t)bw, st));
+    return cu(cudaMemsetAsync(dWd, 0, (size_t)bw, st));
+  }
+  Family f;
+  TRY(pick_family(o, M, &f));
+  TRYCU(cudaSetDevice(h->device));
+  cudaStream_t st = (cudaStream_t)stream;
+  Arena a(ws);
+  BwdWs w = plan_backward(a, M, H, I, k);
+  uint16_t* dh = dh_save ? (uint16_t*)dh_save : w.dh;
+  uint16_t* dU = dU_save ? (uint16_t*)dU_save : w.dU;
+  uint16_t* dG = dG_save ? (uint16_t*)dG_save : w.dG;
+  const uint16_t* G = (const uint16_t*)gate;
+  const uint16_t* U = (const uint16_t*)up;
+  const uint16_t* WG = (const uint16_t*)Wg;
+  const uint16_t* WU = (const uint16_t*)Wu;
+  TRY(rowwise_bwd(h, f, (const uint16_t*)dOut, (const uint16_t*)Wd, G, U, dh, dU, dG, M, H, I, st));
+  // dHidden: cg = T_i(dG[m, i], Wg[i, n]), cu = T_i(dU[m, i], Wu[i, n]); the two
+  // trees stay separate until the final gate-then-up addition.
+  if (k == 1) {
+    TRY(tree_gemm(h, f, Strided{dG, I, 1}, Strided{WG, 1, H}, M, H, I, w.cg, H, st));
+    TRY(tree_gemm(h, f, Strided{dU, I, 1}, Strided{WU, 1, H}, M, H, I, w.cu, H, st));
+  } else {
+    const long long sw = I / k;
+    for (long long s = 0; s < k; ++s) {
+      TRY(tree_gemm(h, f, Strided{dG + s * sw, I, 1}, Strided{WG + s * sw * H, 1, H}, M, H, sw,
+                    w.cgs + s * M * H, H, st));
+      TRY(tree_gemm(h, f, Strided{dU + s * sw, I, 1}, Strided{WU + s * sw * H, 1, H}, M, H, sw,
+                    w.cus + s * M * H, H, st));
+    }
+    const void *pg[8], *pu[8];
+    for (int s = 0; s < k; ++s) {
+      pg[s] = w.cgs + (long long)s * M * H;
+      pu[s] = w.cus + (long long)s * M * H;
+    }
+    TRY(rank_tree_bf16(h, pg, k, w.cg, M * H, st));
+    TRY(rank_tree_bf16(h, pu, k, w.cu, M * H, st));
+  }
+  TRY(add_bf16(h, w.cg, w.cu, (uint16_t*)dX, M * H, st));
+  TRY(silu_mul(h, G, U, w.h, M, I, I, st));
+  return wgrads(h, f, (const uint16_t*)x, (const uint16_t*)dOut, w.h, dU, dG, (uint16_t*)dWg,
+                (uint16_t*)dWu, (uint16_t*)dWd, M, H, I, st);
+}
+
+extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
+                                              const long long* chunk_tokens,
+                                              const void* const* x_chunks,
+                                              const void* const* gate_chunks,
+                                              const void* const* up_chunks,
+                                              const void* const* dOut_chunks, const void* Wd,
+                                              void* dWg, void* dWu, void* dWd, long long H,
+                                              long long I, void* ws, size_t ws_bytes,
+                                              void* stream, const detffn_options* opts) {
+  if (!h || n_chunks < 1 || !chunk_tokens || !x_chunks || !gate_chunks || !up_chunks ||
+      !dOut_chunks || !Wd || !dWg || !dWu || !dWd)
+    return DETFFN_ERR_INVALID_ARG;
+  Opts o;
+  TRY(read_opts(opts, &o));
+  long long M = 0;
+  for (int c = 0; c < n_chunks; ++c) {
+    if (chunk_tokens[c] < 0) return DETFFN_ERR_SHAPE;
+    if (chunk_tokens[c] > 0 && (!x_chunks[c] || !gate_chunks[c] || !up_chunks[c] || !dOut_chunks[c]))
+      return DETFFN_ERR_INVALID_ARG;
+    if (!aligned2(x_chunks[c]) || !aligned2(gate_chunks[c]) || !aligned2(up_chunks[c]) ||
+        !aligned2(dOut_chunks[c]))
+      return DETFFN_ERR_ALIGN;
+    M += chunk_tokens[c];
+  }
+  TRY(check_sizes(M, H, I));
+  if (!aligned2(Wd) || !aligned2(dWg) || !aligned2(dWu) || !aligned2(dWd)) return DETFFN_ERR_ALIGN;
+  const long long bw = 2 * I * H;
+  if (overlap(dWg, bw, dWu, bw) || overlap(dWg, bw, dWd, bw) || overlap(dWu, bw, dWd, bw) ||
+      overlap(dWg, bw, Wd, bw) || overlap(dWu, bw, Wd, bw) || overlap(dWd, bw, Wd, bw))
+    return DETFFN_ERR_INVALID_ARG;
+  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_WGRAD_CHUNKED, M, H, I, 1)));
+  TRYCU(cudaSetDevice(h->device));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (M == 0) {
+    TRYCU(cudaMemsetAsync(dWg, 0, (size_t)bw, st));
+    TRYCU(cudaMemsetAsync(dWu, 0, (size_t)bw, st));
+    return cu(cudaMemsetAsync(dWd, 0, (size_t)bw, st));
+  }
+  Family f;
+  TRY(pick_family(o, M, &f));  // by the total token count
+  Arena a(ws);
+  ChunkWs w = plan_chunked(a, M, H, I);
+  // Gather the chunks in logical token order, then run the row-wise stages
+  // chunk by chunk on their own rows.
+  long long r0 = 0;
+  for (int c = 0; c < n_chunks; ++c) {
+    const long long t = chunk_tokens[c];
+    if (t == 0) continue;
+    TRYCU(cudaMemcpyAsync(w.x + r0 * H, x_chunks[c], (size_t)(2 * t * H), cudaMemcpyDeviceToDevice, st));
+    TRYCU(cudaMemcpyAsync(w.dO + r0 * H, dOut_chunks[c], (size_t)(2 * t * H), cudaMemcpyDeviceToDevice, st));
+    TRYCU(cudaMemcpyAsync(w.g + r0 * I, gate_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
+    TRYCU(cudaMemcpyAsync(w.u + r0 * I, up_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
+    TRY(rowwise_bwd(h, f, w.dO + r0 * H, (const uint16_t*)Wd, w.g + r0 * I, w.u + r0 * I,
+                    w.dh + r0 * I, w.dU + r0 * I, w.dG + r0 * I, t, H, I, st));
+    TRY(silu_mul(h, w.g + r0 * I, w.u + r0 * I, w.h + r0 * I, t, I, I, st));
+    r0 += t;
+  }
+  return wgrads(h, f, w.x, w.dO, w.h, w.dU, w.dG, (uint16_t*)dWg, (uint16_t*)dWu, (uint16_t*)dWd,
+                M, H, I, st);
+}
+
+extern "C" detffn_status detffn_rank_tree_reduce(const void* const* inputs, int n, void* out,
+                                                 long long count, int dtype, void* stream) {
+  if (!inputs || !out || count < 0) return DETFFN_ERR_INVALID_ARG;
+  if (!(n == 1 || n == 2 || n == 4 || n == 8)) return DETFFN_ERR_INVALID_ARG;
+  if (dtype < DETFFN_F32 || dtype > DETFFN_BF16) return DETFFN_ERR_INVALID_ARG;
+  const long long esz = dtype == DETFFN_F32 ? 4 : 2;
+  if (((uintptr_t)out % (uintptr_t)esz) != 0) return DETFFN_ERR_ALIGN;
+  for (int s = 0; s < n; ++s) {
+    if (!inputs[s]) return DETFFN_ERR_INVALID_ARG;
+    if (((uintptr_t)inputs[s] % (uintptr_t)esz) != 0) return DETFFN_ERR_ALIGN;
+    // In place is allowed only at exactly the same address.
+    if (inputs[s] != out && overlap(inputs[s], count * esz, out, count * esz)) return DETFFN_ERR_INVALID_ARG;
+  }
+  if (count == 0) return DETFFN_OK;
+  int dev = 0, sms = 0;
+  TRYCU(cudaGetDevice(&dev));
+  TRYCU(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  return cu(launch_rank_tree(inputs, n, out, count, dtype, sms, (cudaStream_t)stream));
+}
+
+extern "C" detffn_status detffn_tree_gemm(detffn_handle h, const void* A, long long a_rs,
+                                          long long a_ks, const void* B, long long b_rs,
+                                          long long b_ks, long long R, long long C, long long K,
+                                          void* out, long long o_rs, void* stream,
+                                          const detffn_options* opts) {
+  if (!h || !out || R < 0 || C < 0 || K < 0 || K > kMaxK) return DETFFN_ERR_INVALID_ARG;
+  if (K > 0 && (!A || !B)) return DETFFN_ERR_INVALID_ARG;
+  if (!aligned2(A) || !aligned2(B) || !aligned2(out)) return DETFFN_ERR_ALIGN;
+  if (R > 1 && o_rs < C) return DETFFN_ERR_INVALID_ARG;
+  Opts o;
+  TRY(read_opts(opts, &o));
+  if (R == 0 || C == 0) return DETFFN_OK;
+  Family f;
+  TRY(pick_family(o, R, &f));
+  TRYCU(cudaSetDevice(h->device));
+  return tree_gemm(h, f, Strided{(const uint16_t*)A, a_rs, a_ks}, Strided{(const uint16_t*)B, b_rs, b_ks},
+                   R, C, K, (uint16_t*)out, o_rs, (cudaStream_t)stream);
+}
+
+extern "C" detffn_status detffn_profiling(detffn_handle h, int enable) {
+  if (!h) return DETFFN_ERR_INVALID_ARG;
+  for (auto& r : h->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  h->recs.clear();
+  h->prof = enable != 0;
+  return DETFFN_OK;
+}
+
+extern "C" detffn_status detffn_profile_read(detffn_handle h, int max, detffn_kernel_time* out, int* n) {
+  if (!h || !n || max < 0 || (max > 0 && !out)) return DETFFN_ERR_INVALID_ARG;
+  TRYCU(cudaSetDevice(h->device));
+  TRYCU(cudaDeviceSynchronize());
+  std::vector<detffn_kernel_time> agg;
+  for (auto& r : h->recs) {
+    float ms = 0.0f;
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    size_t j = 0;
+    while (j < agg.size() && strcmp(agg[j].name, r.name) != 0) ++j;
+    if (j == agg.size()) {
+      detffn_kernel_time t{};
+      strncpy(t.name, r.name, sizeof(t.name) - 1);
+      agg.push_back(t);
+    }
+    agg[j].launches += 1;
+    agg[j].ms += ms;
+    agg[j].bytes += r.bytes;
+    agg[j].flops += r.flops;
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  h->recs.clear();
+  *n = (int)(agg.size() < (size_t)max ? agg.size() : (size_t)max);
+  for (int j = 0; j < *n; ++j) out[j] = agg[j];
+  return DETFFN_OK;
+}

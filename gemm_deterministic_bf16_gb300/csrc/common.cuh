@@ -1,0 +1,74 @@
+// common.cuh -- device helpers and internal launcher declarations of libdetffn.
+//
+// The canonical tree (RL-Kernel PR #325, "Design": FP32-leaf / BF16-node
+// midpoint reduction tree): leaves of 64 contiguous K positions; internal
+// node = rne_bf16(fp32(left) + fp32(right)); the left child of a node over n
+// leaves takes floor(n/2) of them.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/detffn.h"
+
+namespace detffn {
+
+constexpr int kLeaf = 64;        // leaf width (K positions per FP32 leaf)
+constexpr int kMaxDepth = 24;    // stack entries; enough for < 2^22 leaves
+constexpr long long kMaxK = 1ll << 27;
+
+// ---------------------------------------------------------------------------
+// Element arithmetic
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+__device__ __forceinline__ uint16_t f2bf(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));  // cvt.rn.bf16.f32
+}
+// Tree node: one FP32 add (round to nearest even), then round to BF16.
+__device__ __forceinline__ float node(float l, float r) { return bf2f(f2bf(__fadd_rn(l, r))); }
+
+// Number of internal nodes that end at leaf j in the midpoint tree over L
+// leaves, i.e. how many combines follow the push of leaf j in a left-to-right
+// post-order evaluation.
+__host__ __device__ __forceinline__ int combines_after(int j, int L) {
+  int lo = 0, hi = L, cnt = 0;
+  while (hi - lo > 1) {
+    if (hi - 1 == j) cnt++;
+    int mid = lo + (hi - lo) / 2;
+    if (j < mid) hi = mid; else lo = mid;
+  }
+  return cnt;
+}
+
+__host__ __device__ __forceinline__ long long n_leaves(long long K) { return (K + kLeaf - 1) / kLeaf; }
+
+// ---------------------------------------------------------------------------
+// Internal launchers (all asynchronous on `st`; they return cudaGetLastError)
+// ---------------------------------------------------------------------------
+struct Strided {
+  const uint16_t* p;
+  long long rs, ks;  // element strides of a row and of a K position
+};
+
+// out[r*o_rs + c] = T_K(A[r,:], B[c,:]) on CUDA cores, LANE8x8 leaves.
+cudaError_t launch_tree_gemm_exact(Strided A, Strided B, long long R, long long C, long long K,
+                                   uint16_t* out, long long o_rs, cudaStream_t st);
+
+// h = rne(silu[g] * u) on rows x cols elements at r*ld + c.
+cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* h, long long rows,
+                            long long cols, long long ld, const uint16_t* silu_tab,
+                            cudaStream_t st);
+// dU = rne(dh*a), dG = rne(rne_f32(rne(dh*u) * dsilu[g])).
+cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u,
+                            uint16_t* dU, uint16_t* dG, long long n, const uint16_t* silu_tab,
+                            const float* dsilu_tab, cudaStream_t st);
+// out = rne(a + b).
+cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out, long long n,
+                            cudaStream_t st);
+// Balanced rank tree over n in {1,2,4,8} buffers.
+cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long count, int dtype,
+                             int sm_count, cudaStream_t st);
+
+}  // namespace detffn

@@ -1,0 +1,241 @@
+// k_elem.cu -- BF16 stage boundaries and the balanced rank-tree reduction.
+//
+// Stage boundaries (RL-Kernel PR #325, "Design": "preserve BF16 stage
+// boundaries in forward and backward"):
+//   h  = rne_bf16(silu_bf16(g) * u)
+//   dU = rne_bf16(dh * a), dA = rne_bf16(dh * u), dG = rne_bf16(rne_f32(dA * silu'(g)))
+//   dX = rne_bf16(cg + cu)        (gate contribution first; PR #325,
+//                                  "Communication overlap assessment")
+// Products of two BF16 values are exact in FP32, so h, dU and dA round once.
+//
+// Rank tree (PR #357, "Design"; PR #356, "Design"):
+//   ((b0 + b1) + (b2 + b3)) + ((b4 + b5) + (b6 + b7)), every node an FP32 add
+//   rounded to the buffers' dtype.  It streams n inputs and one output once:
+//   16-byte vectors when every pointer is 16-byte aligned, two-element words
+//   for 16-bit data on 4-byte-aligned pointers, scalars otherwise; the part of
+//   the count that does not fill a vector is done by scalar lanes.
+#include "common.cuh"
+
+namespace detffn {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Rows x cols elements at r*ld + c in all three arrays.
+__global__ void k_silu_mul(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
+                           uint16_t* __restrict__ h, long long rows, long long cols, long long ld,
+                           const uint16_t* __restrict__ silu) {
+  const long long n = rows * cols;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
+       t += (long long)gridDim.x * blockDim.x) {
+    const long long i = (t / cols) * ld + (t % cols);
+    const float a = bf2f(__ldg(silu + g[i]));
+    h[i] = f2bf(__fmul_rn(a, bf2f(u[i])));
+  }
+}
+
+__global__ void k_silu_bwd(const uint16_t* __restrict__ dh, const uint16_t* __restrict__ g,
+                           const uint16_t* __restrict__ u, uint16_t* __restrict__ dU,
+                           uint16_t* __restrict__ dG, long long n,
+                           const uint16_t* __restrict__ silu, const float* __restrict__ dsilu) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint16_t gi = g[i];
+    const float d = bf2f(dh[i]);
+    const float a = bf2f(__ldg(silu + gi));
+    dU[i] = f2bf(__fmul_rn(d, a));
+    const float dA = bf2f(f2bf(__fmul_rn(d, bf2f(u[i]))));
+    dG[i] = f2bf(__fmul_rn(dA, __ldg(dsilu + gi)));
+  }
+}
+
+__global__ void k_add_bf16(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
+                           uint16_t* __restrict__ out, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    out[i] = f2bf(__fadd_rn(bf2f(a[i]), bf2f(b[i])));
+}
+
+// ----------------------------- rank tree ---------------------------------
+
+struct Bufs {
+  const unsigned char* in[8];
+  unsigned char* out;
+};
+
+template <int DT> struct Elt;
+template <> struct Elt<DETFFN_F32> {
+  static constexpr int kBytes = 4;
+  __device__ static float ld(const unsigned char* p, long long i) { return reinterpret_cast<const float*>(p)[i]; }
+  __device__ static float rnd(float v) { return v; }
+  __device__ static void st(unsigned char* p, long long i, float v) { reinterpret_cast<float*>(p)[i] = v; }
+  __device__ static float from_bits(uint32_t b) { return __uint_as_float(b); }
+  __device__ static uint32_t to_bits(float v) { return __float_as_uint(v); }
+};
+template <> struct Elt<DETFFN_F16> {
+  static constexpr int kBytes = 2;
+  __device__ static float from_bits(uint32_t b) { return __half2float(__ushort_as_half((unsigned short)b)); }
+  __device__ static uint32_t to_bits(float v) { return __half_as_ushort(__float2half_rn(v)); }
+  __device__ static float ld(const unsigned char* p, long long i) { return from_bits(reinterpret_cast<const uint16_t*>(p)[i]); }
+  __device__ static float rnd(float v) { return from_bits(to_bits(v)); }
+  __device__ static void st(unsigned char* p, long long i, float v) { reinterpret_cast<uint16_t*>(p)[i] = (uint16_t)to_bits(v); }
+};
+template <> struct Elt<DETFFN_BF16> {
+  static constexpr int kBytes = 2;
+  __device__ static float from_bits(uint32_t b) { return bf2f((uint16_t)b); }
+  __device__ static uint32_t to_bits(float v) { return f2bf(v); }
+  __device__ static float ld(const unsigned char* p, long long i) { return bf2f(reinterpret_cast<const uint16_t*>(p)[i]); }
+  __device__ static float rnd(float v) { return bf2f(f2bf(v)); }
+  __device__ static void st(unsigned char* p, long long i, float v) { reinterpret_cast<uint16_t*>(p)[i] = f2bf(v); }
+};
+
+// The balanced tree over v[0..N): N in {1,2,4,8}; each node rounded to DT.
+template <int DT, int N>
+__device__ __forceinline__ float rank_tree(const float* v) {
+  if (N == 1) return v[0];
+  const float a = Elt<DT>::rnd(__fadd_rn(v[0], v[1]));
+  if (N == 2) return a;
+  const float b = Elt<DT>::rnd(__fadd_rn(v[2], v[3]));
+  const float ab = Elt<DT>::rnd(__fadd_rn(a, b));
+  if (N == 4) return ab;
+  const float c = Elt<DT>::rnd(__fadd_rn(v[4], v[5]));
+  const float d = Elt<DT>::rnd(__fadd_rn(v[6], v[7]));
+  const float cd = Elt<DT>::rnd(__fadd_rn(c, d));
+  return Elt<DT>::rnd(__fadd_rn(ab, cd));
+}
+
+// VEC = bytes moved per input per step (16, 4 or the element size).
+template <int DT, int N, int VEC>
+__global__ void __launch_bounds__(kThreads) k_rank_tree(Bufs B, long long count) {
+  constexpr int E = Elt<DT>::kBytes;
+  constexpr int PER = VEC / E;  // elements per step
+  constexpr bool kScalar = (VEC == E);
+  const long long nvec = kScalar ? 0 : count / PER;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long t0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  for (long long v = t0; v < nvec; v += stride) {
+    uint32_t w[N][VEC / 4 > 0 ? VEC / 4 : 1];
+#pragma unroll
+    for (int s = 0; s < N; ++s) {
+      if (VEC == 16) {
+        const uint4 q = __ldcs(reinterpret_cast<const uint4*>(B.in[s]) + v);
+        w[s][0] = q.x; w[s][1] = q.y; w[s][2] = q.z; w[s][3] = q.w;
+      } else {
+        w[s][0] = reinterpret_cast<const uint32_t*>(B.in[s])[v];
+      }
+    }
+    uint32_t o[VEC / 4 > 0 ? VEC / 4 : 1];
+#pragma unroll
+    for (int q = 0; q < (VEC / 4 > 0 ? VEC / 4 : 1); ++q) {
+      if (E == 4) {
+        float x[N];
+#pragma unroll
+        for (int s = 0; s < N; ++s) x[s] = Elt<DT>::from_bits(w[s][q]);
+        o[q] = Elt<DT>::to_bits(rank_tree<DT, N>(x));
+      } else {
+        float lo[N], hi[N];
+#pragma unroll
+        for (int s = 0; s < N; ++s) {
+          lo[s] = Elt<DT>::from_bits(w[s][q] & 0xFFFFu);
+          hi[s] = Elt<DT>::from_bits(w[s][q] >> 16);
+        }
+        o[q] = (Elt<DT>::to_bits(rank_tree<DT, N>(lo)) & 0xFFFFu) |
+               (Elt<DT>::to_bits(rank_tree<DT, N>(hi)) << 16);
+      }
+    }
+    if (VEC == 16)
+      reinterpret_cast<uint4*>(B.out)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    else
+      reinterpret_cast<uint32_t*>(B.out)[v] = o[0];
+  }
+  // Scalar tail (all of it when PER == 1).
+  for (long long i = nvec * PER + t0; i < count; i += stride) {
+    float x[N];
+#pragma unroll
+    for (int s = 0; s < N; ++s) x[s] = Elt<DT>::ld(B.in[s], i);
+    Elt<DT>::st(B.out, i, rank_tree<DT, N>(x));
+  }
+}
+
+template <int DT, int N>
+cudaError_t launch_rt_n(const Bufs& B, long long count, int align_all, int sm_count, cudaStream_t st) {
+  constexpr int E = Elt<DT>::kBytes;
+  int vec = E;
+  if (align_all % 16 == 0) vec = 16;
+  else if (E == 2 && align_all % 4 == 0) vec = 4;
+  const long long per = vec / E;
+  long long work = count / per + (count % per);
+  long long blocks = (work + kThreads - 1) / kThreads;
+  const long long cap = (long long)sm_count * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (vec == 16) k_rank_tree<DT, N, 16><<<(unsigned)blocks, kThreads, 0, st>>>(B, count);
+  else if (vec == 4) k_rank_tree<DT, N, 4><<<(unsigned)blocks, kThreads, 0, st>>>(B, count);
+  else k_rank_tree<DT, N, E><<<(unsigned)blocks, kThreads, 0, st>>>(B, count);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_rt_dt(const Bufs& B, int n, long long count, int align_all, int sm_count, cudaStream_t st) {
+  switch (n) {
+    case 1: return launch_rt_n<DT, 1>(B, count, align_all, sm_count, st);
+    case 2: return launch_rt_n<DT, 2>(B, count, align_all, sm_count, st);
+    case 4: return launch_rt_n<DT, 4>(B, count, align_all, sm_count, st);
+    case 8: return launch_rt_n<DT, 8>(B, count, align_all, sm_count, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+unsigned grid_for(long long n, int cap_blocks) {
+  long long b = (n + kThreads - 1) / kThreads;
+  if (b > cap_blocks) b = cap_blocks;
+  return (unsigned)(b < 1 ? 1 : b);
+}
+
+}  // namespace
+
+cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* h, long long rows,
+                            long long cols, long long ld, const uint16_t* silu_tab,
+                            cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  k_silu_mul<<<grid_for(rows * cols, 4096), kThreads, 0, st>>>(g, u, h, rows, cols, ld, silu_tab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u,
+                            uint16_t* dU, uint16_t* dG, long long n, const uint16_t* silu_tab,
+                            const float* dsilu_tab, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  k_silu_bwd<<<grid_for(n, 4096), kThreads, 0, st>>>(dh, g, u, dU, dG, n, silu_tab, dsilu_tab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out, long long n,
+                            cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  k_add_bf16<<<grid_for(n, 4096), kThreads, 0, st>>>(a, b, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long count, int dtype,
+                             int sm_count, cudaStream_t st) {
+  if (count <= 0) return cudaSuccess;
+  Bufs B{};
+  uintptr_t acc = (uintptr_t)out;
+  for (int s = 0; s < n; ++s) {
+    B.in[s] = static_cast<const unsigned char*>(in[s]);
+    acc |= (uintptr_t)in[s];
+  }
+  B.out = static_cast<unsigned char*>(out);
+  // Largest power of two (<= 16) dividing every address.
+  int align_all = 16;
+  while (align_all > 1 && (acc % (uintptr_t)align_all) != 0) align_all >>= 1;
+  switch (dtype) {
+    case DETFFN_F32: return launch_rt_dt<DETFFN_F32>(B, n, count, align_all, sm_count, st);
+    case DETFFN_F16: return launch_rt_dt<DETFFN_F16>(B, n, count, align_all, sm_count, st);
+    case DETFFN_BF16: return launch_rt_dt<DETFFN_BF16>(B, n, count, align_all, sm_count, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace detffn

@@ -8,10 +8,12 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
 #include "common.cuh"
+#include "decode.h"
 
 using namespace detffn;
 
@@ -189,13 +191,19 @@ struct Arena {
   }
 };
 
-struct FwdWs { uint16_t *gate, *up, *h, *parts; };
+struct FwdWs { uint16_t *gate, *up, *h, *parts, *dec_part; unsigned* dec_cnt; };
+// Decode scratch: block-root planes (at most 8 blocks x 8 tokens x rows) and
+// one ticket per row tile (at most one tile per row).
+constexpr long long kDecPlanes = 64;
 FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k) {
   FwdWs w;
   w.gate = a.take<uint16_t>(M * I);
   w.up = a.take<uint16_t>(M * I);
   w.h = a.take<uint16_t>(M * I);
   w.parts = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
+  const long long rows = 2 * I > H ? 2 * I : H;
+  w.dec_part = M <= 32 ? a.take<uint16_t>(kDecPlanes * rows) : nullptr;
+  w.dec_cnt = M <= 32 ? a.take<unsigned>(rows + 1) : nullptr;
   return w;
 }
 
@@ -313,6 +321,63 @@ detffn_status rank_tree_bf16(detffn_handle h, const void* const* in, int k, void
                              long long count, cudaStream_t st) {
   return timed(h, st, "rank_tree", 2.0 * (k + 1) * count, 0.0, [&] {
     return cu(launch_rank_tree(in, k, out, count, DETFFN_BF16, h->sm_count, st));
+  });
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// True when the exact weight-streaming decode kernels cover a forward of M
+// tokens with gate/up contraction length Kg over Ng rows and down contraction
+// length Kd (same bits as the general exact kernel either way).
+bool decode_covers(long long M, long long Kg, long long Kd, std::initializer_list<const void*> ptrs) {
+  int S, NB;
+  if (M < 1 || M > 32 || !decode_geometry(Kg, &S, &NB) || !decode_geometry(Kd, &S, &NB)) return false;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return false;
+  return true;
+}
+
+// gate/up rows [0, N) of Wg/Wu (row stride ldw), K = Kg; h (and the optional
+// saves) get columns [0, N) with row stride ldo.  Token passes of 8.
+detffn_status decode_gateup(detffn_handle h, const uint16_t* x, long long ldx, const uint16_t* Wg,
+                            const uint16_t* Wu, long long ldw, long long N, long long Kg,
+                            long long M, uint16_t* hh, uint16_t* gsave, uint16_t* usave,
+                            long long ldo, uint16_t* part, unsigned* cnt, cudaStream_t st) {
+  const double bytes = 2.0 * (2.0 * N * Kg + (double)M * Kg + 3.0 * M * N);
+  return timed(h, st, "decode_gateup", bytes, 4.0 * M * N * Kg, [&] {
+    for (long long p = 0; p < M; p += 8) {
+      DecArgs a{};
+      a.x = x + p * ldx; a.ldx = ldx; a.w0 = Wg; a.w1 = Wu; a.ldw = ldw; a.N = N; a.K = Kg;
+      a.M = (int)(M - p < 8 ? M - p : 8);
+      a.part = part; a.cnt = cnt;
+      a.out = hh + p * ldo; a.ldo = ldo;
+      a.gsave = gsave ? gsave + p * ldo : nullptr;
+      a.usave = usave ? usave + p * ldo : nullptr;
+      a.silu = h->d_silu; a.status = h->d_status; a.spin_limit = 0;
+      const cudaError_t e = launch_decode_exact(a, h->sm_count, st);
+      if (e != cudaSuccess) return DETFFN_ERR_CUDA;
+    }
+    return DETFFN_OK;
+  });
+}
+
+// out[:, 0:N) = T_K(x, W rows) with W row stride ldw, x row stride ldx.
+detffn_status decode_plain(detffn_handle h, const uint16_t* x, long long ldx, const uint16_t* W,
+                           long long ldw, long long N, long long K, long long M, uint16_t* out,
+                           long long ldo, uint16_t* part, unsigned* cnt, cudaStream_t st) {
+  const double bytes = 2.0 * ((double)N * K + (double)M * K + (double)M * N);
+  return timed(h, st, "decode_down", bytes, 2.0 * M * N * K, [&] {
+    for (long long p = 0; p < M; p += 8) {
+      DecArgs a{};
+      a.x = x + p * ldx; a.ldx = ldx; a.w0 = W; a.w1 = nullptr; a.ldw = ldw; a.N = N; a.K = K;
+      a.M = (int)(M - p < 8 ? M - p : 8);
+      a.part = part; a.cnt = cnt;
+      a.out = out + p * ldo; a.ldo = ldo;
+      a.silu = h->d_silu; a.status = h->d_status; a.spin_limit = 0;
+      const cudaError_t e = launch_decode_exact(a, h->sm_count, st);
+      if (e != cudaSuccess) return DETFFN_ERR_CUDA;
+    }
+    return DETFFN_OK;
   });
 }
 
@@ -484,17 +549,24 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
   const uint16_t* WG = (const uint16_t*)Wg;
   const uint16_t* WU = (const uint16_t*)Wu;
   const uint16_t* WD = (const uint16_t*)Wd;
-  if (k == 1) {
-    TRY(gateup_slice(h, f, X, WG, WU, gate, up, w.h, M, H, I, 0, I, st));
-    return tree_gemm(h, f, Strided{w.h, I, 1}, Strided{WD, I, 1}, M, H, I, (uint16_t*)out, H, st);
-  }
-  // Tensor-parallel emulation: shard s owns I/k rows of Wg/Wu and columns of Wd.
-  const long long sw = I / k;
+  const long long sw = I / k;  // I-slice of one shard (all of I when k == 1)
+  const bool dec = f == kExact &&
+                   decode_covers(M, H, sw, {x, Wg, Wu, Wd, w.h, (const void*)(w.h + sw)});
+  const bool saves = gate_save != nullptr;
+  if (dec) TRYCU(cudaMemsetAsync(w.dec_cnt, 0, sizeof(unsigned) * (size_t)((2 * I > H ? 2 * I : H) + 1), st));
   for (long long s = 0; s < k; ++s) {
-    TRY(gateup_slice(h, f, X, WG, WU, gate, up, w.h, M, H, I, s, sw, st));
-    TRY(tree_gemm(h, f, Strided{w.h + s * sw, I, 1}, Strided{WD + s * sw, I, 1}, M, H, sw,
-                  w.parts + s * M * H, H, st));
+    uint16_t* dst = k == 1 ? (uint16_t*)out : w.parts + s * M * H;
+    if (dec) {
+      TRY(decode_gateup(h, X, H, WG + s * sw * H, WU + s * sw * H, H, sw, H, M, w.h + s * sw,
+                        saves ? gate + s * sw : nullptr, saves ? up + s * sw : nullptr, I,
+                        w.dec_part, w.dec_cnt, st));
+      TRY(decode_plain(h, w.h + s * sw, I, WD + s * sw, I, H, sw, M, dst, H, w.dec_part, w.dec_cnt, st));
+    } else {
+      TRY(gateup_slice(h, f, X, WG, WU, gate, up, w.h, M, H, I, s, sw, st));
+      TRY(tree_gemm(h, f, Strided{w.h + s * sw, I, 1}, Strided{WD + s * sw, I, 1}, M, H, sw, dst, H, st));
+    }
   }
+  if (k == 1) return DETFFN_OK;
   const void* parts[8];
   for (int s = 0; s < k; ++s) parts[s] = w.parts + (long long)s * M * H;
   return rank_tree_bf16(h, parts, k, out, M * H, st);
@@ -685,9 +757,11 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
 
 extern "C" detffn_status detffn_rank_tree_reduce(const void* const* inputs, int n, void* out,
                                                  long long count, int dtype, void* stream) {
-  if (!inputs || !out || count < 0) return DETFFN_ERR_INVALID_ARG;
+  if (!inputs || count < 0) return DETFFN_ERR_INVALID_ARG;
   if (!(n == 1 || n == 2 || n == 4 || n == 8)) return DETFFN_ERR_INVALID_ARG;
   if (dtype < DETFFN_F32 || dtype > DETFFN_BF16) return DETFFN_ERR_INVALID_ARG;
+  if (count == 0) return DETFFN_OK;  // empty buffers may have null addresses
+  if (!out) return DETFFN_ERR_INVALID_ARG;
   const long long esz = dtype == DETFFN_F32 ? 4 : 2;
   if (((uintptr_t)out % (uintptr_t)esz) != 0) return DETFFN_ERR_ALIGN;
   for (int s = 0; s < n; ++s) {
@@ -696,7 +770,6 @@ extern "C" detffn_status detffn_rank_tree_reduce(const void* const* inputs, int 
     // In place is allowed only at exactly the same address.
     if (inputs[s] != out && overlap(inputs[s], count * esz, out, count * esz)) return DETFFN_ERR_INVALID_ARG;
   }
-  if (count == 0) return DETFFN_OK;
   int dev = 0, sms = 0;
   TRYCU(cudaGetDevice(&dev));
   TRYCU(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));

@@ -174,3 +174,36 @@ def test_tree_gemm_layouts(G, oracle_mod):
 
 def test_status_word_ok(G):
     assert G.detffn_get_status() == 0
+
+
+@pytest.mark.parametrize("M,H,I", [(2, 1024, 3072), (3, 256, 768), (5, 1024, 3072), (7, 512, 1536),
+                                   (13, 1024, 3072), (24, 256, 768), (1, 4096, 1536)])
+def test_decode_kernel_shapes_bit_exact(G, oracle_mod, M, H, I):
+    """The weight-streaming decode kernel (leaf blocks of 4, 8, 12 and 24
+    leaves, 1 to 4 token passes) against the oracle, forward and sharded."""
+    d = ffn_inputs(M, H, I, seed=M * 7 + H, with_dout=False)
+    t = {n: dev(v) for n, v in d.items()}
+    gate, up = empty_bf16(M, I), empty_bf16(M, I)
+    out = G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], gate_save=gate, up_save=up, path=EXACT)
+    ref = oracle_mod.ffn_forward(d["x"], d["Wg"], d["Wu"], d["Wd"])
+    assert mismatches(host(gate), ref["gate"]) == 0
+    assert mismatches(host(up), ref["up"]) == 0
+    assert mismatches(host(out), ref["out"]) == 0
+    for k in [2, 4]:
+        if (I // k) % 64 == 0 and (I // k) // 64 >= 2:
+            o2 = G.detffn_forward_sharded(t["x"], t["Wg"], t["Wu"], t["Wd"], k, path=EXACT)
+            assert mismatches(host(o2), ref["out"]) == 0, k
+
+
+def test_decode_repeat_and_stream(G):
+    """Repeated decode forwards on a side stream are bitwise identical."""
+    d = ffn_inputs(8, 4096, 12288, seed=11, with_dout=False)
+    t = {n: dev(v) for n, v in d.items()}
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            outs.append(G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], path=EXACT).clone())
+    s.synchronize()
+    assert mismatches(host(outs[0]), host(outs[1])) == 0
+    assert mismatches(host(outs[0]), host(outs[2])) == 0

@@ -347,6 +347,32 @@ def run_ours(args):
     return 0
 
 
+def run_profile_case(args):
+    """A few forwards of one size and nothing else: the command ncu captures."""
+    import numpy as np
+    import torch
+
+    import gemm_deterministic_bf16_gb300 as G
+    from gemm_deterministic_bf16_gb300 import build as libbuild
+    from gemm_deterministic_bf16_gb300.inputs import ffn_inputs
+    libbuild.build()
+    kind, M = args.profile_case[:3], int(args.profile_case[3:])
+    path = {"auto": G.PATH_AUTO, "exact": G.PATH_EXACT, "tensor": G.PATH_TENSOR}[args.path]
+    d = ffn_inputs(M, H, I, seed=0, with_dout=(kind == "trn"))
+    t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in d.items()}
+    for _ in range(args.steps):
+        if kind == "fwd":
+            G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], path=path)
+        else:
+            g = torch.empty(M, I, dtype=torch.bfloat16, device="cuda")
+            u = torch.empty_like(g)
+            G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], gate_save=g, up_save=u, path=path)
+            G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], g, u, t["dOut"], path=path)
+    torch.cuda.synchronize()
+    print("profile case %s done" % args.profile_case)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -356,9 +382,14 @@ def main():
     ap.add_argument("--path", choices=["auto", "exact", "tensor"], default="auto")
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None,
+                    help="fwdM or trnM (e.g. fwd8): run --steps forwards (or training steps) "
+                         "of M tokens only, for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.profile_case:
+        return run_profile_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

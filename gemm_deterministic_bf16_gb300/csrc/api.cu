@@ -30,6 +30,7 @@ struct detffn_handle_s {
     const char* name;
     cudaEvent_t a, b;
     double bytes, flops;
+    int launches;
   };
   bool prof = false;
   std::vector<Rec> recs;
@@ -279,9 +280,9 @@ detffn_status cu(cudaError_t e) { return e == cudaSuccess ? DETFFN_OK : DETFFN_E
 // Runs `launch`; while profiling, brackets it with an event pair on `st`.
 template <class F>
 detffn_status timed(detffn_handle h, cudaStream_t st, const char* name, double bytes,
-                    double flops, F&& launch) {
+                    double flops, F&& launch, int launches = 1) {
   if (!h || !h->prof) return launch();
-  detffn_handle_s::Rec r{name, nullptr, nullptr, bytes, flops};
+  detffn_handle_s::Rec r{name, nullptr, nullptr, bytes, flops, launches};
   if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return DETFFN_ERR_CUDA;
   cudaEventRecord(r.a, st);
   const detffn_status s = launch();
@@ -358,7 +359,7 @@ detffn_status decode_gateup(detffn_handle h, const uint16_t* x, long long ldx, c
       if (e != cudaSuccess) return DETFFN_ERR_CUDA;
     }
     return DETFFN_OK;
-  });
+  }, (int)((M + 7) / 8));
 }
 
 // out[:, 0:N) = T_K(x, W rows) with W row stride ldw, x row stride ldx.
@@ -378,7 +379,7 @@ detffn_status decode_plain(detffn_handle h, const uint16_t* x, long long ldx, co
       if (e != cudaSuccess) return DETFFN_ERR_CUDA;
     }
     return DETFFN_OK;
-  });
+  }, (int)((M + 7) / 8));
 }
 
 }  // namespace
@@ -821,7 +822,7 @@ extern "C" detffn_status detffn_profile_read(detffn_handle h, int max, detffn_ke
       strncpy(t.name, r.name, sizeof(t.name) - 1);
       agg.push_back(t);
     }
-    agg[j].launches += 1;
+    agg[j].launches += r.launches;
     agg[j].ms += ms;
     agg[j].bytes += r.bytes;
     agg[j].flops += r.flops;

@@ -15,7 +15,7 @@
 //     ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)) while spreading tokens over lanes;
 //   * after a batch of rows, each (row, token) block subtree root is formed
 //     from the S leaves in shared memory and written (BF16) to a partial plane.
-// The weight rows stream through a 4-stage ring of 1-D bulk (TMA) copies
+// The weight rows stream through a 3-stage ring of 1-D bulk (TMA) copies
 // completing on mbarriers.  The last CTA of a row tile to finish (an atomic
 // ticket; nothing waits on another CTA) applies the top of the tree over the
 // block roots and the epilogue: a plain BF16 store, or for the gate/up pair
@@ -27,12 +27,12 @@
 namespace detffn {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 
 template <int S> struct Geo {
   static constexpr int B = (S % 3 == 0) ? 3 : 1;  // bottom subtree size
   static constexpr int P = S / B;                 // bottom subtrees per block (power of 2)
-  static constexpr int RB = (S <= 8) ? 8 : 4;     // rows per batch
+  static constexpr int RB = (S <= 8) ? 4 : 2;     // rows per batch
   static constexpr int ROWB = S * 128;            // bytes of one row's block slice
   static constexpr int STAGEB = RB * ROWB;
   static constexpr int LVB = RB * 8 * (S + 1) * 4;
@@ -342,7 +342,7 @@ int decode_tiles(long long K, long long N, bool gate_up, int sm_count, int* RT) 
   int per_sm = (227 * 1024) / (smem + 1024);
   const int by_threads = 2048 / (8 * S);
   if (per_sm > by_threads) per_sm = by_threads;
-  if (per_sm > 24) per_sm = 24;
+  if (per_sm > 32) per_sm = 32;
   if (per_sm < 1) per_sm = 1;
   long long tiles = ((long long)sm_count * per_sm) / NB;
   if (tiles < 1) tiles = 1;

@@ -140,6 +140,13 @@ void host_tables() {
 
 }  // namespace
 
+namespace detffn {
+const uint16_t* host_silu_table() {
+  host_tables();
+  return g_silu.data();
+}
+}  // namespace detffn
+
 // ---------------------------------------------------------------------------
 // Argument checks and scratch layout
 // ---------------------------------------------------------------------------

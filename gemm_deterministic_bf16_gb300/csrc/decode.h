@@ -40,4 +40,7 @@ int decode_tiles(long long K, long long N, bool gate_up, int sm_count, int* RT);
 // geometry is not covered.
 cudaError_t launch_decode_exact(DecArgs a, int sm_count, cudaStream_t st);
 
+// The library's host copy of the BF16 SiLU table (65536 entries, built once).
+const uint16_t* host_silu_table();
+
 }  // namespace detffn

@@ -296,3 +296,24 @@ def detffn_profile_read(device=None):
     _check(L.detffn_profile_read(handle(device), 64, buf, ctypes.byref(n)), "detffn_profile_read")
     return {buf[i].name.decode(): dict(launches=buf[i].launches, ms=buf[i].ms, bytes=buf[i].bytes,
                                        flops=buf[i].flops) for i in range(n.value)}
+
+
+def detffn_forward_decode_noalloc(x, Wg, Wu, Wd, out=None, stream=None):
+    """The decode forward (1 <= M <= 8) for callers that cannot allocate device
+    memory: the library uses its own fixed scratch, so this call makes no
+    allocation of its own (pass `out` to avoid the one for the result).
+    Same bits as detffn_forward(path=PATH_EXACT).  Calls must not overlap on
+    the GPU; the first call on a device does a one-time set-up."""
+    _bf16(x, Wg, Wu, Wd, out)
+    M, H = x.shape
+    I = Wg.shape[0]
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    L = lib()
+    L.detffn_forward_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _ll, _ll, _ll, _vp]
+    L.detffn_forward_decode_noalloc.restype = ctypes.c_int
+    with torch.cuda.device(x.device):
+        _check(L.detffn_forward_decode_noalloc(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(out),
+                                               M, H, I, _stream(x.device, stream)),
+               "detffn_forward_decode_noalloc")
+    return out

@@ -213,6 +213,31 @@ typedef struct {
 DETFFN_API detffn_status detffn_profiling(detffn_handle h, int enable);
 DETFFN_API detffn_status detffn_profile_read(detffn_handle h, int max, detffn_kernel_time *out, int *n);
 
+/* Decode forward that allocates nothing (the pages have no counterpart to
+ * this call; it exists for callers that cannot call cudaMalloc, such as a
+ * process whose device memory is already owned by a caching allocator's
+ * pool, or a runtime that only hands out buffers reserved in advance).
+ * It computes exactly what detffn_forward computes on the EXACT path -- the
+ * same bits -- for 1 <= M <= 8 tokens, H <= 8192, I <= 16384, where H and I
+ * are 64 times 2^d or 3 * 2^d leaves (e.g. 4096 and 12288).  Inputs x [M,H]
+ * and the weights must be 16-byte aligned; out [M,H] is written.  Larger or
+ * unsupported sizes return DETFFN_ERR_SHAPE, misaligned pointers
+ * DETFFN_ERR_ALIGN, and nothing is launched.
+ * Its scratch (h, the kernels' block-root planes and tickets, about 4.4 MiB)
+ * and its SiLU table are fixed-size arrays inside the library, held by every
+ * GPU that loads it until the process exits.  The first call on a device
+ * performs a one-time set-up there (it resolves those arrays' device
+ * addresses and copies the SiLU table with a synchronous cudaMemcpy); make
+ * that first call before any stream capture.  Every call uses the same
+ * arrays and clears what must start at zero, so calls that overlap on the
+ * GPU (on different streams, or from different host threads) race and must
+ * not be issued; calls in order on one stream are fine.  It uses the current
+ * device and runs on `stream` (a cudaStream_t). */
+DETFFN_API detffn_status detffn_forward_decode_noalloc(const void *x, const void *Wg,
+                                                       const void *Wu, const void *Wd, void *out,
+                                                       long long M, long long H, long long I,
+                                                       void *stream);
+
 /* Synchronises `stream`, then returns and clears the handle's device status
  * word (DETFFN_OK or DETFFN_ERR_TIMEOUT from a bounded wait). */
 DETFFN_API detffn_status detffn_get_status(detffn_handle h, void *stream);

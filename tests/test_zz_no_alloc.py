@@ -1,0 +1,54 @@
+"""The allocation-free decode forward, checked against detffn_forward.
+
+detffn_forward_decode_noalloc serves callers that cannot call cudaMalloc (for
+example when a caching allocator's pool already holds the device's memory):
+it keeps its scratch in fixed arrays inside the library instead of a
+caller-provided workspace.  This file is collected last, so that a run that
+stops at the first failure has already run every other test.  It checks, on
+two calls in a row, that the output equals detffn_forward's on the exact path
+bit for bit (the tolerance of the exact path is 0 mismatching elements), and
+that sizes beyond its limits are refused before anything is launched.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gemm_deterministic_bf16_gb300.inputs import ffn_inputs
+from tests.gpu_util import dev, host, mismatches
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def G():
+    import gemm_deterministic_bf16_gb300 as G
+    from gemm_deterministic_bf16_gb300 import build
+    build.build()
+    return G
+
+
+@pytest.mark.parametrize("M,H,I", [(8, 4096, 12288), (1, 4096, 12288), (5, 1024, 3072)])
+def test_noalloc_matches_forward_twice(G, M, H, I):
+    d = ffn_inputs(M, H, I, seed=40 + M, with_dout=False)
+    t = {n: dev(v) for n, v in d.items()}
+    ref = host(G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], path=G.PATH_EXACT))
+    out = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):
+        out.fill_(0)
+        G.detffn_forward_decode_noalloc(t["x"], t["Wg"], t["Wu"], t["Wd"], out=out)
+        torch.cuda.synchronize()
+        assert mismatches(host(out), ref) == 0
+
+
+def test_noalloc_rejects_sizes_beyond_limits(G):
+    x = torch.zeros(9, 256, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(768, 256, dtype=torch.bfloat16, device="cuda")
+    wd = torch.zeros(256, 768, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(G.DetFFNError) as e:
+        G.detffn_forward_decode_noalloc(x, w, w, wd)   # M = 9 > 8
+    assert e.value.status == 2
+    big = torch.zeros(32768, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(G.DetFFNError) as e:
+        G.detffn_forward_decode_noalloc(x[:1, :64], big, big,
+                                        torch.zeros(64, 32768, dtype=torch.bfloat16, device="cuda"))
+    assert e.value.status == 2                           # I = 32768 > 16384

@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "decode.h"
+#include "tc.h"
 
 using namespace detffn;
 
@@ -174,15 +175,34 @@ detffn_status read_opts(const detffn_options* o, Opts* out) {
   return DETFFN_OK;
 }
 
-// The kernel family a call uses: a function of M (tokens) and the requested
-// path only.  The exact CUDA-core family is the only one built in this file;
-// other families register through dispatch below.
-enum Family { kExact = 0 };
+// The kernel family a call uses.  EXACT: CUDA-core kernels with LANE8x8
+// leaves (bit-identical to the oracle).  TENSOR: tcgen05 leaves.  AUTO takes
+// TENSOR for M > 32 tokens when the tensor kernel covers every contraction
+// length of the call (H, I, I/k and M leaves of the form 1, 2^d or 3*2^d, and
+// H, I multiples of 8), else EXACT.  It never depends on the shard count or
+// the chunking: a shard of I has the same leaf-count form as I.
+enum Family { kExact = 0, kTensor = 1 };
 
-detffn_status pick_family(const Opts& o, long long M, Family* f) {
-  (void)M;
-  if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_UNSUPPORTED;
-  *f = kExact;
+bool tc_len_ok(long long K) {
+  int G, E;
+  return K > 0 && tc_tree_shape((K + kLeaf - 1) / kLeaf, &G, &E);
+}
+
+bool tc_covers(long long M, long long H, long long I, bool backward) {
+  if (H % 8 || I % 8) return false;
+  if (!tc_len_ok(H) || !tc_len_ok(I)) return false;
+  return !backward || tc_len_ok(M);
+}
+
+detffn_status pick_family(const Opts& o, long long M, long long H, long long I, bool backward, Family* f) {
+  if (o.path == DETFFN_PATH_EXACT) {
+    *f = kExact;
+  } else if (o.path == DETFFN_PATH_TENSOR) {
+    if (!tc_covers(M, H, I, backward)) return DETFFN_ERR_UNSUPPORTED;
+    *f = kTensor;
+  } else {
+    *f = (M > 32 && tc_covers(M, H, I, backward)) ? kTensor : kExact;
+  }
   return DETFFN_OK;
 }
 
@@ -215,9 +235,12 @@ FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k) {
   return w;
 }
 
-struct BwdWs { uint16_t *dh, *dU, *dG, *h, *cg, *cu, *cgs, *cus; };
-BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k) {
-  BwdWs w;
+struct BwdWs {
+  uint16_t *dh, *dU, *dG, *h, *cg, *cu, *cgs, *cus;
+  uint16_t *WdT, *WgT, *WuT, *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only
+};
+BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool tensor) {
+  BwdWs w{};
   w.dh = a.take<uint16_t>(M * I);
   w.dU = a.take<uint16_t>(M * I);
   w.dG = a.take<uint16_t>(M * I);
@@ -226,12 +249,25 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k) {
   w.cu = a.take<uint16_t>(M * H);
   w.cgs = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
   w.cus = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
+  if (tensor) {
+    w.WdT = a.take<uint16_t>(I * H);
+    w.WgT = a.take<uint16_t>(H * I);
+    w.WuT = a.take<uint16_t>(H * I);
+    w.dOT = a.take<uint16_t>(H * M);
+    w.xT = a.take<uint16_t>(H * M);
+    w.hT = a.take<uint16_t>(I * M);
+    w.dGT = a.take<uint16_t>(I * M);
+    w.dUT = a.take<uint16_t>(I * M);
+  }
   return w;
 }
 
-struct ChunkWs { uint16_t *x, *dO, *g, *u, *dh, *dU, *dG, *h; };
-ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I) {
-  ChunkWs w;
+struct ChunkWs {
+  uint16_t *x, *dO, *g, *u, *dh, *dU, *dG, *h;
+  uint16_t *WdT, *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only
+};
+ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tensor) {
+  ChunkWs w{};
   w.x = a.take<uint16_t>(M * H);
   w.dO = a.take<uint16_t>(M * H);
   w.g = a.take<uint16_t>(M * I);
@@ -240,16 +276,24 @@ ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I) {
   w.dU = a.take<uint16_t>(M * I);
   w.dG = a.take<uint16_t>(M * I);
   w.h = a.take<uint16_t>(M * I);
+  if (tensor) {
+    w.WdT = a.take<uint16_t>(I * H);
+    w.dOT = a.take<uint16_t>(H * M);
+    w.xT = a.take<uint16_t>(H * M);
+    w.hT = a.take<uint16_t>(I * M);
+    w.dGT = a.take<uint16_t>(I * M);
+    w.dUT = a.take<uint16_t>(I * M);
+  }
   return w;
 }
 
-size_t ws_bytes_for(int op, long long M, long long H, long long I, int k) {
+size_t ws_bytes_for(int op, long long M, long long H, long long I, int k, bool tensor) {
   Arena a(nullptr);
   switch (op) {
     case DETFFN_OP_FORWARD: plan_forward(a, M, H, I, 1); break;
     case DETFFN_OP_FORWARD_SHARDED: plan_forward(a, M, H, I, k); break;
-    case DETFFN_OP_BACKWARD: plan_backward(a, M, H, I, k); break;
-    case DETFFN_OP_WGRAD_CHUNKED: plan_chunked(a, M, H, I); break;
+    case DETFFN_OP_BACKWARD: plan_backward(a, M, H, I, k, tensor); break;
+    case DETFFN_OP_WGRAD_CHUNKED: plan_chunked(a, M, H, I, tensor); break;
     default: return 0;
   }
   return (a.off + 255) & ~(size_t)255;
@@ -299,12 +343,34 @@ detffn_status timed(detffn_handle h, cudaStream_t st, const char* name, double b
 }
 
 // One tree contraction on the chosen family.
+// Tensor family: both operands K-contiguous with 16-byte-aligned rows.  For
+// R <= 32 (few tokens) the operands swap roles (weights fill the 128-row MMA
+// side, tokens the 32-column side) and the result is stored transposed.
+bool tc_operands_ok(const Strided& X) {
+  return X.ks == 1 && (X.rs % 8) == 0 && (((uintptr_t)X.p) & 15u) == 0;
+}
+
 detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long long R, long long C,
                         long long K, uint16_t* out, long long o_rs, cudaStream_t st) {
-  (void)f;
   const double bytes = 2.0 * ((double)R * K + (double)C * K + (double)R * C);
+  if (f == kTensor) {
+    if (!tc_operands_ok(A) || !tc_operands_ok(B)) return DETFFN_ERR_ALIGN;
+    return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
+      if (R <= 32)
+        return cu(launch_tc_gemm(B.p, B.rs, A.p, A.rs, C, R, K, out, 1, o_rs, 32, h->d_status, 0,
+                                 h->sm_count, st));
+      return cu(launch_tc_gemm(A.p, A.rs, B.p, B.rs, R, C, K, out, o_rs, 1, 128, h->d_status, 0,
+                               h->sm_count, st));
+    });
+  }
   return timed(h, st, "tree_gemm_exact", bytes, 2.0 * R * C * K,
                [&] { return cu(launch_tree_gemm_exact(A, B, R, C, K, out, o_rs, st)); });
+}
+
+detffn_status transpose(detffn_handle h, const uint16_t* in, long long rows, long long cols,
+                        long long ld_in, uint16_t* out, cudaStream_t st) {
+  return timed(h, st, "transpose", 4.0 * rows * cols, 0.0,
+               [&] { return cu(launch_transpose(in, rows, cols, ld_in, out, rows, st)); });
 }
 
 detffn_status silu_mul(detffn_handle h, const uint16_t* g, const uint16_t* u, uint16_t* hh,
@@ -468,7 +534,10 @@ detffn_status detffn_workspace_size(detffn_handle h, int op, long long M, long l
   if (op < DETFFN_OP_FORWARD || op > DETFFN_OP_WGRAD_CHUNKED) return DETFFN_ERR_INVALID_ARG;
   if (op == DETFFN_OP_BACKWARD && k <= 1) k = o.shards;
   if (!(k == 1 || k == 2 || k == 4 || k == 8)) return DETFFN_ERR_INVALID_ARG;
-  *bytes = ws_bytes_for(op, M, H, I, k);
+  Family f;
+  const bool bwd = op == DETFFN_OP_BACKWARD || op == DETFFN_OP_WGRAD_CHUNKED;
+  TRY(pick_family(o, M, H, I, bwd, &f));
+  *bytes = ws_bytes_for(op, M, H, I, k, f == kTensor);
   return DETFFN_OK;
 }
 
@@ -543,10 +612,14 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
     for (int b = a + 1; b < 3; ++b)
       if (overlap(outs[a], nout[a], outs[b], nout[b])) return DETFFN_ERR_INVALID_ARG;
   }
-  TRY(check_ws(ws, ws_bytes, ws_bytes_for(k > 1 ? DETFFN_OP_FORWARD_SHARDED : DETFFN_OP_FORWARD, M, H, I, k)));
-  if (M == 0) return DETFFN_OK;
   Family f;
-  TRY(pick_family(o, M, &f));
+  TRY(pick_family(o, M, H, I, false, &f));
+  if (f == kTensor && (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))) {
+    if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_ALIGN;
+    f = kExact;
+  }
+  TRY(check_ws(ws, ws_bytes, ws_bytes_for(k > 1 ? DETFFN_OP_FORWARD_SHARDED : DETFFN_OP_FORWARD, M, H, I, k, false)));
+  if (M == 0) return DETFFN_OK;
   TRYCU(cudaSetDevice(h->device));
   cudaStream_t st = (cudaStream_t)stream;
   Arena a(ws);
@@ -603,18 +676,34 @@ namespace {
 
 // Row-wise backward stages for rows [r0, r0+rows): dh, then dU and dG.
 detffn_status rowwise_bwd(detffn_handle h, Family f, const uint16_t* dOut, const uint16_t* Wd,
-                          const uint16_t* gate, const uint16_t* up, uint16_t* dh, uint16_t* dU,
-                          uint16_t* dG, long long rows, long long H, long long I,
-                          cudaStream_t st) {
-  // dh[m, i] = T_{n<H}(dOut[m, n], Wd[n, i]): B row i has K stride I.
-  TRY(tree_gemm(h, f, Strided{dOut, H, 1}, Strided{Wd, 1, I}, rows, I, H, dh, I, st));
+                          const uint16_t* WdT, const uint16_t* gate, const uint16_t* up,
+                          uint16_t* dh, uint16_t* dU, uint16_t* dG, long long rows, long long H,
+                          long long I, cudaStream_t st) {
+  // dh[m, i] = T_{n<H}(dOut[m, n], Wd[n, i]): B row i is column i of Wd (K stride I),
+  // or row i of the transposed copy WdT [I, H] for the tensor family.
+  const Strided B = f == kTensor ? Strided{WdT, H, 1} : Strided{Wd, 1, I};
+  TRY(tree_gemm(h, f, Strided{dOut, H, 1}, B, rows, I, H, dh, I, st));
   return silu_bwd(h, dh, gate, up, dU, dG, rows * I, st);
 }
 
+// Transposed [., M] copies of the token-major stage tensors (tensor family).
+struct TokT { uint16_t *dOT, *xT, *hT, *dGT, *dUT; };
+
 // Weight gradients over K = M tokens from row-major [M, .] stage tensors.
-detffn_status wgrads(detffn_handle h, Family f, const uint16_t* x, const uint16_t* dOut, const uint16_t* hh,
-                     const uint16_t* dU, const uint16_t* dG, uint16_t* dWg, uint16_t* dWu,
-                     uint16_t* dWd, long long M, long long H, long long I, cudaStream_t st) {
+detffn_status wgrads(detffn_handle h, Family f, const uint16_t* x, const uint16_t* dOut,
+                     const uint16_t* hh, const uint16_t* dU, const uint16_t* dG, uint16_t* dWg,
+                     uint16_t* dWu, uint16_t* dWd, long long M, long long H, long long I,
+                     const TokT& tt, cudaStream_t st) {
+  if (f == kTensor) {
+    TRY(transpose(h, dOut, M, H, H, tt.dOT, st));
+    TRY(transpose(h, x, M, H, H, tt.xT, st));
+    TRY(transpose(h, hh, M, I, I, tt.hT, st));
+    TRY(transpose(h, dG, M, I, I, tt.dGT, st));
+    TRY(transpose(h, dU, M, I, I, tt.dUT, st));
+    TRY(tree_gemm(h, f, Strided{tt.dOT, M, 1}, Strided{tt.hT, M, 1}, H, I, M, dWd, I, st));
+    TRY(tree_gemm(h, f, Strided{tt.dGT, M, 1}, Strided{tt.xT, M, 1}, I, H, M, dWg, H, st));
+    return tree_gemm(h, f, Strided{tt.dUT, M, 1}, Strided{tt.xT, M, 1}, I, H, M, dWu, H, st);
+  }
   // dWd[n, i] = T_m(dOut[m, n], h[m, i])
   TRY(tree_gemm(h, f, Strided{dOut, 1, H}, Strided{hh, 1, I}, H, I, M, dWd, I, st));
   // dWg[i, n] = T_m(dG[m, i], x[m, n]); dWu likewise with dU.
@@ -652,7 +741,18 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
     for (int b = a + 1; b < 7; ++b)
       if (overlap(outs[a], nout[a], outs[b], nout[b])) return DETFFN_ERR_INVALID_ARG;
   }
-  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_BACKWARD, M, H, I, k)));
+  Family f;
+  TRY(pick_family(o, M, H, I, true, &f));
+  if (f == kTensor) {
+    const void* ps[] = {x, Wg, Wu, Wd, gate, up, dOut, dh_save, dU_save, dG_save};
+    bool al = true;
+    for (const void* p : ps) al = al && aligned16(p);
+    if (!al) {
+      if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_ALIGN;
+      f = kExact;
+    }
+  }
+  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_BACKWARD, M, H, I, k, f == kTensor)));
   if (M == 0) {
     // No tokens: the weight gradients are empty sums (+0); nothing else exists.
     TRYCU(cudaSetDevice(h->device));
@@ -661,12 +761,10 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
     TRYCU(cudaMemsetAsync(dWu, 0, (size_t)bw, st));
     return cu(cudaMemsetAsync(dWd, 0, (size_t)bw, st));
   }
-  Family f;
-  TRY(pick_family(o, M, &f));
   TRYCU(cudaSetDevice(h->device));
   cudaStream_t st = (cudaStream_t)stream;
   Arena a(ws);
-  BwdWs w = plan_backward(a, M, H, I, k);
+  BwdWs w = plan_backward(a, M, H, I, k, f == kTensor);
   uint16_t* dh = dh_save ? (uint16_t*)dh_save : w.dh;
   uint16_t* dU = dU_save ? (uint16_t*)dU_save : w.dU;
   uint16_t* dG = dG_save ? (uint16_t*)dG_save : w.dG;
@@ -674,20 +772,26 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   const uint16_t* U = (const uint16_t*)up;
   const uint16_t* WG = (const uint16_t*)Wg;
   const uint16_t* WU = (const uint16_t*)Wu;
-  TRY(rowwise_bwd(h, f, (const uint16_t*)dOut, (const uint16_t*)Wd, G, U, dh, dU, dG, M, H, I, st));
+  if (f == kTensor) {  // K-contiguous copies of the weights for the NN contractions
+    TRY(transpose(h, (const uint16_t*)Wd, H, I, I, w.WdT, st));
+    TRY(transpose(h, WG, I, H, H, w.WgT, st));
+    TRY(transpose(h, WU, I, H, H, w.WuT, st));
+  }
+  TRY(rowwise_bwd(h, f, (const uint16_t*)dOut, (const uint16_t*)Wd, w.WdT, G, U, dh, dU, dG, M, H, I, st));
   // dHidden: cg = T_i(dG[m, i], Wg[i, n]), cu = T_i(dU[m, i], Wu[i, n]); the two
-  // trees stay separate until the final gate-then-up addition.
-  if (k == 1) {
-    TRY(tree_gemm(h, f, Strided{dG, I, 1}, Strided{WG, 1, H}, M, H, I, w.cg, H, st));
-    TRY(tree_gemm(h, f, Strided{dU, I, 1}, Strided{WU, 1, H}, M, H, I, w.cu, H, st));
-  } else {
-    const long long sw = I / k;
-    for (long long s = 0; s < k; ++s) {
-      TRY(tree_gemm(h, f, Strided{dG + s * sw, I, 1}, Strided{WG + s * sw * H, 1, H}, M, H, sw,
-                    w.cgs + s * M * H, H, st));
-      TRY(tree_gemm(h, f, Strided{dU + s * sw, I, 1}, Strided{WU + s * sw * H, 1, H}, M, H, sw,
-                    w.cus + s * M * H, H, st));
-    }
+  // trees stay separate until the final gate-then-up addition.  B row n is
+  // column n of Wg (K stride H), or row n of WgT [H, I] for the tensor family.
+  auto wcol = [&](const uint16_t* W, const uint16_t* WT, long long s0) {
+    return f == kTensor ? Strided{WT + s0, I, 1} : Strided{W + s0 * H, 1, H};
+  };
+  const long long sw = I / k;
+  for (long long s = 0; s < k; ++s) {
+    uint16_t* cg = k == 1 ? w.cg : w.cgs + s * M * H;
+    uint16_t* cu = k == 1 ? w.cu : w.cus + s * M * H;
+    TRY(tree_gemm(h, f, Strided{dG + s * sw, I, 1}, wcol(WG, w.WgT, s * sw), M, H, sw, cg, H, st));
+    TRY(tree_gemm(h, f, Strided{dU + s * sw, I, 1}, wcol(WU, w.WuT, s * sw), M, H, sw, cu, H, st));
+  }
+  if (k > 1) {
     const void *pg[8], *pu[8];
     for (int s = 0; s < k; ++s) {
       pg[s] = w.cgs + (long long)s * M * H;
@@ -699,7 +803,7 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   TRY(add_bf16(h, w.cg, w.cu, (uint16_t*)dX, M * H, st));
   TRY(silu_mul(h, G, U, w.h, M, I, I, st));
   return wgrads(h, f, (const uint16_t*)x, (const uint16_t*)dOut, w.h, dU, dG, (uint16_t*)dWg,
-                (uint16_t*)dWu, (uint16_t*)dWd, M, H, I, st);
+                (uint16_t*)dWu, (uint16_t*)dWd, M, H, I, TokT{w.dOT, w.xT, w.hT, w.dGT, w.dUT}, st);
 }
 
 extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
@@ -732,7 +836,13 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
   if (overlap(dWg, bw, dWu, bw) || overlap(dWg, bw, dWd, bw) || overlap(dWu, bw, dWd, bw) ||
       overlap(dWg, bw, Wd, bw) || overlap(dWu, bw, Wd, bw) || overlap(dWd, bw, Wd, bw))
     return DETFFN_ERR_INVALID_ARG;
-  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_WGRAD_CHUNKED, M, H, I, 1)));
+  Family f;
+  TRY(pick_family(o, M, H, I, true, &f));  // by the total token count
+  if (f == kTensor && !aligned16(Wd)) {
+    if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_ALIGN;
+    f = kExact;
+  }
+  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_WGRAD_CHUNKED, M, H, I, 1, f == kTensor)));
   TRYCU(cudaSetDevice(h->device));
   cudaStream_t st = (cudaStream_t)stream;
   if (M == 0) {
@@ -740,10 +850,9 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
     TRYCU(cudaMemsetAsync(dWu, 0, (size_t)bw, st));
     return cu(cudaMemsetAsync(dWd, 0, (size_t)bw, st));
   }
-  Family f;
-  TRY(pick_family(o, M, &f));  // by the total token count
   Arena a(ws);
-  ChunkWs w = plan_chunked(a, M, H, I);
+  ChunkWs w = plan_chunked(a, M, H, I, f == kTensor);
+  if (f == kTensor) TRY(transpose(h, (const uint16_t*)Wd, H, I, I, w.WdT, st));
   // Gather the chunks in logical token order, then run the row-wise stages
   // chunk by chunk on their own rows.
   long long r0 = 0;
@@ -754,13 +863,13 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
     TRYCU(cudaMemcpyAsync(w.dO + r0 * H, dOut_chunks[c], (size_t)(2 * t * H), cudaMemcpyDeviceToDevice, st));
     TRYCU(cudaMemcpyAsync(w.g + r0 * I, gate_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
     TRYCU(cudaMemcpyAsync(w.u + r0 * I, up_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
-    TRY(rowwise_bwd(h, f, w.dO + r0 * H, (const uint16_t*)Wd, w.g + r0 * I, w.u + r0 * I,
+    TRY(rowwise_bwd(h, f, w.dO + r0 * H, (const uint16_t*)Wd, w.WdT, w.g + r0 * I, w.u + r0 * I,
                     w.dh + r0 * I, w.dU + r0 * I, w.dG + r0 * I, t, H, I, st));
     TRY(silu_mul(h, w.g + r0 * I, w.u + r0 * I, w.h + r0 * I, t, I, I, st));
     r0 += t;
   }
   return wgrads(h, f, w.x, w.dO, w.h, w.dU, w.dG, (uint16_t*)dWg, (uint16_t*)dWu, (uint16_t*)dWd,
-                M, H, I, st);
+                M, H, I, TokT{w.dOT, w.xT, w.hT, w.dGT, w.dUT}, st);
 }
 
 extern "C" detffn_status detffn_rank_tree_reduce(const void* const* inputs, int n, void* out,
@@ -796,8 +905,13 @@ extern "C" detffn_status detffn_tree_gemm(detffn_handle h, const void* A, long l
   Opts o;
   TRY(read_opts(opts, &o));
   if (R == 0 || C == 0) return DETFFN_OK;
-  Family f;
-  TRY(pick_family(o, R, &f));
+  Family f = kExact;
+  const Strided SA{(const uint16_t*)A, a_rs, a_ks}, SB{(const uint16_t*)B, b_rs, b_ks};
+  if (o.path == DETFFN_PATH_TENSOR || (o.path == DETFFN_PATH_AUTO && R > 32)) {
+    const bool ok = tc_len_ok(K) && tc_operands_ok(SA) && tc_operands_ok(SB);
+    if (ok) f = kTensor;
+    else if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_UNSUPPORTED;
+  }
   TRYCU(cudaSetDevice(h->device));
   return tree_gemm(h, f, Strided{(const uint16_t*)A, a_rs, a_ks}, Strided{(const uint16_t*)B, b_rs, b_ks},
                    R, C, K, (uint16_t*)out, o_rs, (cudaStream_t)stream);

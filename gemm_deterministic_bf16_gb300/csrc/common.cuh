@@ -67,6 +67,9 @@ cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_
 // out = rne(a + b).
 cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out, long long n,
                             cudaStream_t st);
+// out[c*ld_out + r] = in[r*ld_in + c] (a copy).
+cudaError_t launch_transpose(const uint16_t* in, long long rows, long long cols, long long ld_in,
+                             uint16_t* out, long long ld_out, cudaStream_t st);
 // Balanced rank tree over n in {1,2,4,8} buffers.
 cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long count, int dtype,
                              int sm_count, cudaStream_t st);

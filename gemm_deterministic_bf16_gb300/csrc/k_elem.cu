@@ -239,3 +239,35 @@ cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long 
 }
 
 }  // namespace detffn
+
+// ----------------------------- transpose ----------------------------------
+// out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols (BF16, a pure
+// copy: no arithmetic).  32x32 tiles through shared memory.
+namespace detffn {
+namespace {
+__global__ void k_transpose(const uint16_t* __restrict__ in, long long rows, long long cols, long long ld_in,
+                            uint16_t* __restrict__ out, long long ld_out) {
+  __shared__ uint16_t tile[32][34];
+  const long long r0 = (long long)blockIdx.y * 32, c0 = (long long)blockIdx.x * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  for (int i = ty; i < 32; i += 8) {
+    const long long r = r0 + i, c = c0 + tx;
+    if (r < rows && c < cols) tile[i][tx] = in[r * ld_in + c];
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const long long c = c0 + i, r = r0 + tx;
+    if (r < rows && c < cols) out[c * ld_out + r] = tile[tx][i];
+  }
+}
+}  // namespace
+
+cudaError_t launch_transpose(const uint16_t* in, long long rows, long long cols, long long ld_in,
+                             uint16_t* out, long long ld_out, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const long long gy = (rows + 31) / 32, gx = (cols + 31) / 32;
+  if (gy > 65535 || gx > 2147483647ll) return cudaErrorInvalidValue;
+  k_transpose<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, st>>>(in, rows, cols, ld_in, out, ld_out);
+  return cudaGetLastError();
+}
+}  // namespace detffn

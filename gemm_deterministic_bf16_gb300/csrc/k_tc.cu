@@ -1,0 +1,413 @@
+// k_tc.cu -- tensor-core (tcgen05 / TMEM) tree contraction.
+//
+// out[r, c] = T_K(A[r, :], B[c, :]) for K-major BF16 A [R, K] and B [C, K],
+// with the canonical FP32-leaf / BF16-node midpoint tree (RL-Kernel PR #325,
+// "Design").  Each 64-wide leaf is one FP32 accumulation on the tensor core
+// (4 MMAs of K = 16 into a fresh TMEM buffer; the hardware's in-leaf order),
+// and the tree over the leaves is applied exactly by the epilogue warps.
+//
+// Tree shape.  The kernel covers L = 1, 2^d and 3 * 2^d leaves: the midpoint
+// tree is then a perfect binary tree over Q = 2^E bottom groups of G leaves
+// (G = 2: leaf pairs; G = 3: leaf0 + (leaf1 + leaf2); G = 1: a lone leaf).
+//
+// Roles (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      TMA producer: A and B tiles of one leaf per pipeline stage
+//               (128-byte swizzle, K-major), NSTAGE stages on mbarriers;
+//   warp 1      allocates TMEM (4 leaf buffers of BN columns) and issues the
+//               MMAs, one leaf per buffer, committing to the stage's "empty"
+//               barrier and the buffer's "full" barrier;
+//   warps 2-9   epilogue: each thread owns one row (TMEM lane) and BN/2
+//               columns; it reads a group's leaves from TMEM, forms the
+//               group root, returns the buffers, and folds the root into a
+//               binary-counter stack of BF16 nodes (low levels in registers,
+//               high levels in shared memory); the last fold is the output.
+// Every wait is bounded; on a timeout the CTA records DETFFN_ERR_TIMEOUT,
+// stops, drains its own copies and MMAs (bounded) and frees its TMEM.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tc.h"
+
+namespace detffn {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kAccBufs = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kTcThreads = 32 * (2 + kEpiWarps);
+constexpr int kMaxLv = 6;  // up to Q = 64 bottom groups
+
+template <int BN> struct TcGeo {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int COLS = BN / 2;    // columns per epilogue thread
+  static constexpr int WORDS = COLS / 2;  // packed BF16 pairs per stack level per thread
+  static constexpr int REG_LV = BN >= 128 ? 3 : kMaxLv;
+  static constexpr int SMEM_LV = kMaxLv - REG_LV;
+  static constexpr int NSTAGE = BN >= 128 ? 4 : 6;
+  static constexpr int STACK_BYTES = SMEM_LV * BM * COLS * 2 * 2;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = 1024 + NSTAGE * STAGE + STACK_BYTES + BAR_BYTES;
+  static constexpr int TMEM_COLS = kAccBufs * BN;
+};
+
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Tree node on packed pairs: rne_bf16(fp32(a) + fp32(b)) per half.
+__device__ __forceinline__ uint32_t node2(uint32_t a, uint32_t b) {
+  return pack_bf16x2(__fadd_rn(lo_f(a), lo_f(b)), __fadd_rn(hi_f(a), hi_f(b)));
+}
+
+struct Bars {
+  uint64_t full[8], empty[8], accf[kAccBufs], acce[kAccBufs], fin;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
+                                              volatile int* abort_flag, int* status) {
+  for (long long i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  if (status) atomicExch(status, (int)DETFFN_ERR_TIMEOUT);
+  return false;
+}
+
+}  // namespace
+}  // namespace detffn
+
+namespace detffn {
+namespace {
+
+struct TcArgs {
+  int R, C, L, G, E;
+  int num_m, num_n;
+  uint16_t* out;
+  long long ld_r, ld_c;
+  int* status;
+  long long spin;
+};
+
+// Stack level m >= REG_LV lives in shared memory as [level][half][word][row].
+template <int BN>
+__device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int w, int row) {
+  using T = TcGeo<BN>;
+  return stk + (((m - T::REG_LV) * 2 + half) * T::WORDS + w) * BM + row;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+         const TcArgs a) {
+  using T = TcGeo<BN>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* stages = smem;
+  uint32_t* stk = reinterpret_cast<uint32_t*>(smem + T::NSTAGE * T::STAGE);
+  Bars* bars = reinterpret_cast<Bars*>(smem + T::NSTAGE * T::STAGE + T::STACK_BYTES);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = a.num_m * a.num_n;
+  const long long limit = a.spin > 0 ? a.spin : kDefaultSpin;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < T::NSTAGE; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(&bars->accf[b], 1);
+      mbar_init(&bars->acce[b], kEpiWarps);
+    }
+    mbar_init(&bars->fin, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_slot, T::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      long long it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int tm = t % a.num_m, tn = t / a.num_m;
+        for (int j = 0; j < a.L; ++j, ++it) {
+          const int s = (int)(it % T::NSTAGE);
+          if (!wait_or_abort(&bars->empty[s], (uint32_t)(((it / T::NSTAGE) & 1) ^ 1), limit, abort_flag,
+                             a.status)) {
+            ok = false;
+            break;
+          }
+          unsigned char* st = stages + s * T::STAGE;
+          mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
+          tma_load_2d(st, &tmA, j * BK, tm * BM, &bars->full[s]);
+          tma_load_2d(st + T::A_BYTES, &tmB, j * BK, tn * BN, &bars->full[s]);
+        }
+      }
+      // Drain: the last loads issued into each stage have landed.
+      for (long long i = (it > T::NSTAGE ? it - T::NSTAGE : 0); i < it; ++i)
+        mbar_wait(&bars->full[i % T::NSTAGE], (uint32_t)((i / T::NSTAGE) & 1), limit, nullptr);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, BN);
+      long long it = 0, lc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int j = 0; j < a.L; ++j, ++it, ++lc) {
+          const int b = (int)(lc % kAccBufs);
+          if (!wait_or_abort(&bars->acce[b], (uint32_t)(((lc / kAccBufs) & 1) ^ 1), limit, abort_flag,
+                             a.status)) {
+            ok = false;
+            break;
+          }
+          const int s = (int)(it % T::NSTAGE);
+          if (!wait_or_abort(&bars->full[s], (uint32_t)((it / T::NSTAGE) & 1), limit, abort_flag,
+                             a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da = smem_desc_sw128(stages + s * T::STAGE);
+          const uint64_t db = smem_desc_sw128(stages + s * T::STAGE + T::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
+            tc_mma_bf16(tmem + (uint32_t)(b * BN), da + 2 * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+          tc_commit(&bars->empty[s]);
+          tc_commit(&bars->accf[b]);
+        }
+      }
+      tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
+      mbar_wait(&bars->fin, 0, limit, nullptr);
+    }
+  } else {
+    // ---------------- epilogue: leaves -> tree ----------------
+    const int ew = warp - 2;
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = ew >> 2;
+    const int row = quarter * 32 + lane;
+    const int col0 = half * T::COLS;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const int Q = 1 << a.E;
+    long long lc = 0;
+    bool ok = true;
+    uint32_t reg_lv[T::REG_LV][T::WORDS];
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      const int tm = t % a.num_m, tn = t / a.num_m;
+      const long long r = (long long)tm * BM + row;
+      for (int q = 0; q < Q; ++q) {
+        for (int g = 0; g < a.G; ++g)
+          if (!wait_or_abort(&bars->accf[(lc + g) % kAccBufs], (uint32_t)(((lc + g) / kAccBufs) & 1),
+                             limit, abort_flag, a.status))
+            ok = false;
+        if (__any_sync(0xffffffffu, !ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t b0 = (uint32_t)((lc % kAccBufs) * BN), b1 = (uint32_t)(((lc + 1) % kAccBufs) * BN),
+                       b2 = (uint32_t)(((lc + 2) % kAccBufs) * BN);
+#pragma unroll
+        for (int c = 0; c < T::COLS / 16; ++c) {
+          uint32_t v0[16], v1[16], v2[16];
+          const uint32_t col = (uint32_t)(col0 + 16 * c);
+          tmem_ld16(tmem + lane_addr + b0 + col, v0);
+          if (a.G >= 2) tmem_ld16(tmem + lane_addr + b1 + col, v1);
+          if (a.G >= 3) tmem_ld16(tmem + lane_addr + b2 + col, v2);
+          tmem_wait_ld();
+          uint32_t carry[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float x = __uint_as_float(v0[2 * i]), y = __uint_as_float(v0[2 * i + 1]);
+            if (a.G == 2) {
+              x = __fadd_rn(x, __uint_as_float(v1[2 * i]));
+              y = __fadd_rn(y, __uint_as_float(v1[2 * i + 1]));
+            } else if (a.G == 3) {
+              const uint32_t n12 = pack_bf16x2(__fadd_rn(__uint_as_float(v1[2 * i]), __uint_as_float(v2[2 * i])),
+                                               __fadd_rn(__uint_as_float(v1[2 * i + 1]), __uint_as_float(v2[2 * i + 1])));
+              x = __fadd_rn(x, lo_f(n12));
+              y = __fadd_rn(y, hi_f(n12));
+            }
+            carry[i] = pack_bf16x2(x, y);  // the group root (a lone leaf is rounded once)
+          }
+          // Fold the 16 roots of this chunk into the stack (elementwise binary counter).
+          int l = 0;
+#pragma unroll
+          for (int m = 0; m < kMaxLv; ++m) {
+            if (m >= a.E || !((q >> m) & 1)) break;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t left = (m < T::REG_LV) ? reg_lv[m < T::REG_LV ? m : 0][c * 8 + i]
+                                                    : *stk_at<BN>(stk, m, half, c * 8 + i, row);
+              carry[i] = node2(left, carry[i]);
+            }
+            l = m + 1;
+          }
+          if (q != Q - 1) {
+#pragma unroll
+            for (int m = 0; m < kMaxLv; ++m)
+              if (m == l) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  if (m < T::REG_LV) reg_lv[m < T::REG_LV ? m : 0][c * 8 + i] = carry[i];
+                  else *stk_at<BN>(stk, m, half, c * 8 + i, row) = carry[i];
+                }
+              }
+          } else if (r < a.R) {
+            // The root: 16 output columns of row r.
+            const long long c0 = (long long)tn * BN + col;
+            uint16_t* o = a.out + r * a.ld_r + c0 * a.ld_c;
+            if (a.ld_c == 1 && c0 + 16 <= a.C && ((uintptr_t)o & 15u) == 0) {
+              reinterpret_cast<uint4*>(o)[0] = make_uint4(carry[0], carry[1], carry[2], carry[3]);
+              reinterpret_cast<uint4*>(o)[1] = make_uint4(carry[4], carry[5], carry[6], carry[7]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (c0 + i < a.C) o[i * a.ld_c] = (uint16_t)(carry[i >> 1] >> (16 * (i & 1)));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+          for (int g = 0; g < a.G; ++g) mbar_arrive(&bars->acce[(lc + g) % kAccBufs]);
+        lc += a.G;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, T::TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long K, long long ld, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int sm_count,
+                      cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(k_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<BN>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int tiles = a.num_m * a.num_n;
+  const int grid = tiles < sm_count ? tiles : sm_count;
+  k_tc<BN><<<grid, kTcThreads, TcGeo<BN>::SMEM, st>>>(ta, tb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_tree_shape(long long L, int* G, int* E) {
+  if (L == 1) {
+    *G = 1;
+    *E = 0;
+    return true;
+  }
+  long long q;
+  int g;
+  if ((L & (L - 1)) == 0) {
+    g = 2;
+    q = L / 2;
+  } else if (L % 3 == 0 && ((L / 3) & (L / 3 - 1)) == 0) {
+    g = 3;
+    q = L / 3;
+  } else {
+    return false;
+  }
+  int e = 0;
+  while ((1ll << e) < q) ++e;
+  if (e > kMaxLv) return false;
+  *G = g;
+  *E = e;
+  return true;
+}
+
+cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
+                           long long R, long long C, long long K, uint16_t* out, long long ld_r,
+                           long long ld_c, int bn, int* status, long long spin_limit,
+                           int sm_count, cudaStream_t st) {
+  if (R <= 0 || C <= 0) return cudaSuccess;
+  const long long L = (K + BK - 1) / BK;
+  int G, E;
+  if (K <= 0 || !tc_tree_shape(L, &G, &E)) return cudaErrorInvalidValue;
+  if ((lda % 8) || (ldb % 8) || ((uintptr_t)A & 15u) || ((uintptr_t)B & 15u)) return cudaErrorInvalidValue;
+  if (R > (1ll << 31) || C > (1ll << 31)) return cudaErrorInvalidValue;
+  TcArgs a;
+  a.R = (int)R;
+  a.C = (int)C;
+  a.L = (int)L;
+  a.G = G;
+  a.E = E;
+  a.num_m = (int)((R + BM - 1) / BM);
+  a.num_n = (int)((C + bn - 1) / bn);
+  a.out = out;
+  a.ld_r = ld_r;
+  a.ld_c = ld_c;
+  a.status = status;
+  a.spin = spin_limit;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, R, K, lda, BM) || !make_map(&tb, B, C, K, ldb, bn)) return cudaErrorInvalidValue;
+  switch (bn) {
+    case 32: return launch_bn<32>(ta, tb, a, sm_count, st);
+    case 64: return launch_bn<64>(ta, tb, a, sm_count, st);
+    case 128: return launch_bn<128>(ta, tb, a, sm_count, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace detffn

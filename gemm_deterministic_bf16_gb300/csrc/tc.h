@@ -1,0 +1,21 @@
+// tc.h -- launcher of the tensor-core (tcgen05) tree contraction.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace detffn {
+
+// Bottom-group size G and number of upper levels E such that L = G * 2^E with
+// G in {1, 2, 3}; false when the tensor-core kernel does not cover L leaves.
+bool tc_tree_shape(long long L, int* G, int* E);
+
+// out[r*ld_r + c*ld_c] = T_K(A[r, :], B[c, :]) for r < R, c < C; A and B are
+// K-contiguous BF16 with row strides lda, ldb (elements, multiples of 8) and
+// 16-byte-aligned bases.  bn in {32, 64, 128} is the tile width over C.
+cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
+                           long long R, long long C, long long K, uint16_t* out, long long ld_r,
+                           long long ld_c, int bn, int* status, long long spin_limit,
+                           int sm_count, cudaStream_t st);
+
+}  // namespace detffn

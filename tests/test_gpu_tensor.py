@@ -1,0 +1,149 @@
+"""GPU parity of the tensor-core (tcgen05) path.
+
+Each 64-wide leaf is summed by the tensor core in the hardware's own order,
+so on general data the leaves (and through them the outputs) may differ from
+the oracle's LANE8x8 leaves; that is the tolerance branch of the contract.
+Two kinds of checks:
+
+* Integer-valued operands (entries in {-2, ..., 2}): every leaf is an exact
+  integer below 2^24 whatever the summation order, so the tensor path must
+  equal the oracle bit for bit.  This pins the TMA/descriptor layout, the
+  leaf boundaries, the tree shapes (G = 1, 2, 3 bottom groups) and the
+  stores, including partial leaves and ragged tiles.
+* Random data: relative L2 <= 1e-3 against the oracle and the distribution
+  of BF16 ulp distances, plus bitwise determinism and shard/chunk invariance
+  within the tensor path (RL-Kernel PR #325, "Design"; "Correctness results").
+"""
+import numpy as np
+import pytest
+import torch
+
+from gemm_deterministic_bf16_gb300.inputs import ffn_inputs, to_bf16_bits
+from oracle.fp64 import rel_l2
+from tests.gpu_util import dev, empty_bf16, host, mismatches, ulp_dist
+
+pytestmark = pytest.mark.gpu
+TENSOR = 2
+
+
+@pytest.fixture(scope="module")
+def G():
+    import gemm_deterministic_bf16_gb300 as G
+    from gemm_deterministic_bf16_gb300 import build
+    build.build()
+    return G
+
+
+def _ints(shape, seed):
+    rng = np.random.default_rng(seed)
+    return to_bf16_bits(rng.integers(-2, 3, shape).astype(np.float32))
+
+
+@pytest.mark.parametrize("R,C,K", [(128, 128, 64), (256, 128, 128), (128, 256, 256), (200, 300, 100),
+                                   (130, 129, 192), (256, 256, 768), (128, 128, 4096),
+                                   (256, 128, 12288), (384, 384, 3072)])
+def test_tc_integer_inputs_bit_exact(G, oracle_mod, R, C, K):
+    A, B = _ints((R, K), R + K), _ints((C, K), C + 7 * K)
+    got = host(G.detffn_tree_gemm(dev(A), dev(B), path=TENSOR))
+    assert mismatches(got, oracle_mod.tree_gemm(A, B)) == 0
+
+
+@pytest.mark.parametrize("R,C,K", [(1, 256, 4096), (8, 384, 768), (32, 1024, 12288), (17, 200, 256)])
+def test_tc_few_rows_swapped_bit_exact(G, oracle_mod, R, C, K):
+    """R <= 32: weights on the 128-row MMA side, tokens as the 32-wide tile."""
+    A, B = _ints((R, K), R + K + 1), _ints((C, K), C + K + 2)
+    got = host(G.detffn_tree_gemm(dev(A), dev(B), path=TENSOR))
+    assert mismatches(got, oracle_mod.tree_gemm(A, B)) == 0
+
+
+def _stats(got, ref):
+    f = lambda u: (np.asarray(u, np.uint32) << 16).view(np.float32)  # noqa: E731
+    d = ulp_dist(got, ref)
+    return rel_l2(f(got), f(ref)), float(np.mean(d <= 1)), int(d.max())
+
+
+@pytest.mark.parametrize("R,C,K", [(256, 256, 4096), (256, 128, 12288)])
+def test_tc_random_within_tolerance(G, oracle_mod, R, C, K):
+    rng = np.random.default_rng(R + C + K)
+    A = to_bf16_bits(rng.standard_normal((R, K)).astype(np.float32))
+    B = to_bf16_bits((0.02 * rng.standard_normal((C, K))).astype(np.float32))
+    got = host(G.detffn_tree_gemm(dev(A), dev(B), path=TENSOR))
+    rl2, within1, mx = _stats(got, oracle_mod.tree_gemm(A, B))
+    print("tensor vs oracle: rel-L2 %.3g, within 1 ulp %.6f, max ulp %d" % (rl2, within1, mx))
+    assert rl2 <= 1e-3
+    assert within1 >= 0.999
+
+
+def _fwd_bwd(G, t, path, k=1):
+    M, H = t["x"].shape
+    I = t["Wg"].shape[0]
+    g, u = empty_bf16(M, I), empty_bf16(M, I)
+    if k == 1:
+        out = G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], gate_save=g, up_save=u, path=path)
+    else:
+        out = G.detffn_forward_sharded(t["x"], t["Wg"], t["Wu"], t["Wd"], k, gate_save=g, up_save=u, path=path)
+    dh = empty_bf16(M, I)
+    dX, dWg, dWu, dWd = G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], g, u, t["dOut"],
+                                          dh_save=dh, shards=k, path=path)
+    torch.cuda.synchronize()
+    return {n: host(v) for n, v in dict(out=out, gate=g, up=u, dh=dh, dX=dX, dWg=dWg, dWu=dWu,
+                                        dWd=dWd).items()}
+
+
+def test_tc_ffn_integer_inputs_bit_exact(G, oracle_mod):
+    """Forward+backward on the tensor path with integer-valued x, dOut and
+    weights: the contractions whose operands are integers (gate, up, dh) have
+    exact leaves and must equal the oracle bit for bit; h and everything after
+    it are not integers, so those stages are checked with the tolerance."""
+    M, H, I = 128, 256, 768
+    d = {"x": _ints((M, H), 1), "Wg": _ints((I, H), 2), "Wu": _ints((I, H), 3),
+         "Wd": _ints((H, I), 4), "dOut": _ints((M, H), 5)}
+    got = _fwd_bwd(G, {n: dev(v) for n, v in d.items()}, TENSOR)
+    f = oracle_mod.ffn_forward(d["x"], d["Wg"], d["Wu"], d["Wd"])
+    assert mismatches(got["gate"], f["gate"]) == 0
+    assert mismatches(got["up"], f["up"]) == 0
+    b = oracle_mod.ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], got["gate"], got["up"], d["dOut"])
+    assert mismatches(got["dh"], b["dh"]) == 0
+    for n in ["out"]:
+        assert _stats(got[n], f[n])[0] <= 1e-3, n
+    for n in ["dX", "dWg", "dWu", "dWd"]:
+        assert _stats(got[n], b[n])[0] <= 1e-3, n
+
+
+def test_tc_ffn_random_tolerance_and_invariance(G, oracle_mod):
+    M, H, I = 256, 512, 1536
+    d = ffn_inputs(M, H, I, seed=21)
+    t = {n: dev(v) for n, v in d.items()}
+    base = _fwd_bwd(G, t, TENSOR)
+    again = _fwd_bwd(G, t, TENSOR)
+    for n in base:
+        assert mismatches(base[n], again[n]) == 0, n            # repeat: bitwise
+    for k in [2, 4, 8]:
+        sh = _fwd_bwd(G, t, TENSOR, k)
+        for n in ["out", "dX", "dWg", "dWu", "dWd"]:
+            assert mismatches(base[n], sh[n]) == 0, (k, n)      # shards: bitwise
+    f = oracle_mod.ffn_forward(d["x"], d["Wg"], d["Wu"], d["Wd"])
+    b = oracle_mod.ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], f["gate"], f["up"], d["dOut"])
+    for n, ref in [("out", f["out"]), ("dX", b["dX"]), ("dWg", b["dWg"]), ("dWu", b["dWu"]), ("dWd", b["dWd"])]:
+        rl2, within1, mx = _stats(base[n], ref)
+        print("%s: rel-L2 %.3g, within 1 ulp %.5f, max ulp %d" % (n, rl2, within1, mx))
+        assert rl2 <= 1e-3, n
+
+
+def test_tc_chunked_wgrad_invariance(G):
+    M, H, I = 512, 256, 768
+    d = ffn_inputs(M, H, I, seed=22)
+    t = {n: dev(v) for n, v in d.items()}
+    base = _fwd_bwd(G, t, TENSOR)
+    g, u = dev(base["gate"]), dev(base["up"])
+    for sizes in ([256, 256], [128, 128, 128, 128], [100, 412]):
+        e = np.cumsum([0] + sizes)
+        sl = [slice(int(a), int(b)) for a, b in zip(e[:-1], e[1:])]
+        dWg, dWu, dWd = G.detffn_wgrad_chunked([t["x"][s].contiguous() for s in sl],
+                                               [g[s].contiguous() for s in sl],
+                                               [u[s].contiguous() for s in sl],
+                                               [t["dOut"][s].contiguous() for s in sl], t["Wd"],
+                                               path=TENSOR)
+        assert mismatches(host(dWg), base["dWg"]) == 0
+        assert mismatches(host(dWu), base["dWu"]) == 0
+        assert mismatches(host(dWd), base["dWd"]) == 0

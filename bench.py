@@ -207,6 +207,47 @@ def run_reference(args):
     return 0
 
 
+def large_training(G, args, ws_n, timed):
+    """M=4096 (2 x 2048 tokens) forward and forward+backward on the default
+    (tensor-core) family: TFLOP/s against 6*M*H*I and 18*M*H*I."""
+    import numpy as np
+    import torch
+    from gemm_deterministic_bf16_gb300.inputs import ffn_inputs
+    M = 4096
+    d = ffn_inputs(M, H, I, seed=7)
+    t = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in d.items()}
+    e = lambda *s: torch.empty(s, dtype=torch.bfloat16, device="cuda")  # noqa: E731
+    out, g, u, dX = e(M, H), e(M, I), e(M, I), e(M, H)
+    dWg, dWu, dWd = e(I, H), e(I, H), e(H, I)
+    wsf = G.workspace(G.OP_FORWARD, M, H, I)
+    wsb = G.workspace(G.OP_BACKWARD, M, H, I)
+
+    def fwd(i):
+        G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], out=out, gate_save=g, up_save=u, ws=wsf)
+
+    def train(i):
+        fwd(i)
+        G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], g, u, t["dOut"], dX=dX, dWg=dWg, dWu=dWu,
+                          dWd=dWd, ws=wsb)
+
+    steps = max(3, args.steps // 4)
+    fwd_ms = max_over_ranks(ws_n, timed(fwd, steps, 3))
+    trn_ms = max_over_ranks(ws_n, timed(train, steps, 3))
+    G.detffn_profiling(True)
+    train(0)
+    prof = G.detffn_profile_read()
+    G.detffn_profiling(False)
+    res = {"fwd_ms_M4096": fwd_ms, "fwd_tflops_M4096": 6 * M * H * I / (fwd_ms * 1e-3) / 1e12,
+           "fwd_bwd_ms_M4096": trn_ms, "fwd_bwd_tflops_M4096": 18 * M * H * I / (trn_ms * 1e-3) / 1e12,
+           "kernels_M4096": {k: {"launches": v["launches"], "ms": v["ms"],
+                                 "tflops": (v["flops"] / (v["ms"] * 1e-3) / 1e12) if v["flops"] else None,
+                                 "gbs": v["bytes"] / (v["ms"] * 1e-3) / 1e9}
+                             for k, v in prof.items()}}
+    del t, out, g, u, dX, dWg, dWu, dWd, wsf, wsb
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -300,6 +341,18 @@ def run_ours(args):
     extra["fwd_bwd_us_M32"] = 1e3 * max_over_ranks(ws_n, timed(train_step, tsteps, 3))
     extra["fwd_bwd_gbs_M32"] = 3 * WEIGHT_BYTES / (extra["fwd_bwd_us_M32"] * 1e-6) / 1e9
 
+    # The M=32 forward on the tensor-core family (leaves in the hardware's order).
+    wst = G.workspace(G.OP_FORWARD, M_DEC, H, I, 1, G.PATH_TENSOR)
+
+    def fwd_tc(i):
+        t = copies[i & 1]
+        G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], out=outs[M_DEC], ws=wst, path=G.PATH_TENSOR)
+
+    extra["fwd_us_M32_tensor"] = 1e3 * max_over_ranks(ws_n, timed(fwd_tc, args.steps, args.warmup))
+    extra["fwd_gbs_M32_tensor"] = fwd_bytes(M_DEC) / (extra["fwd_us_M32_tensor"] * 1e-6) / 1e9
+    if not args.no_large:
+        extra.update(large_training(G, args, ws_n, timed))
+
     # End to end through the public API: pinned host x in, host out back, every step.
     xh = torch.empty(M_DEC, H, dtype=torch.bfloat16).pin_memory()
     xh.copy_(copies[0]["x"].cpu())
@@ -382,6 +435,7 @@ def main():
     ap.add_argument("--path", choices=["auto", "exact", "tensor"], default="auto")
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-large", action="store_true", help="skip the M=4096 training measurement")
     ap.add_argument("--profile-case", default=None,
                     help="fwdM or trnM (e.g. fwd8): run --steps forwards (or training steps) "
                          "of M tokens only, for profiler captures")

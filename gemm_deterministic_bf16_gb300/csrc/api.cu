@@ -955,3 +955,18 @@ extern "C" detffn_status detffn_profile_read(detffn_handle h, int max, detffn_ke
   for (int j = 0; j < *n; ++j) out[j] = agg[j];
   return DETFFN_OK;
 }
+
+extern "C" detffn_status detffn_selfcheck_node_add(detffn_handle h, unsigned long long* mismatches) {
+  if (!h || !mismatches) return DETFFN_ERR_INVALID_ARG;
+  TRYCU(cudaSetDevice(h->device));
+  // A diagnostic call: an 8-byte device counter, one pass over all 2^32 pairs,
+  // then a device synchronisation.
+  unsigned long long* d = nullptr;
+  TRYCU(cudaMalloc(&d, sizeof(unsigned long long)));
+  detffn_status s = cu(cudaMemset(d, 0, sizeof(unsigned long long)));
+  if (s == DETFFN_OK) s = cu(launch_check_node_add(0, 1ull << 32, d, h->sm_count, 0));
+  if (s == DETFFN_OK) s = cu(cudaDeviceSynchronize());
+  if (s == DETFFN_OK) s = cu(cudaMemcpy(mismatches, d, sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+  cudaFree(d);
+  return s;
+}

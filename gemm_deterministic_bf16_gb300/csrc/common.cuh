@@ -70,6 +70,9 @@ cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out,
 // out[c*ld_out + r] = in[r*ld_in + c] (a copy).
 cudaError_t launch_transpose(const uint16_t* in, long long rows, long long cols, long long ld_in,
                              uint16_t* out, long long ld_out, cudaStream_t st);
+// Self-check: counts pairs where add.rn.bf16x2 differs from the tree node.
+cudaError_t launch_check_node_add(unsigned long long begin, unsigned long long end, unsigned long long* bad,
+                                  int sm_count, cudaStream_t st);
 // Balanced rank tree over n in {1,2,4,8} buffers.
 cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long count, int dtype,
                              int sm_count, cudaStream_t st);

@@ -271,3 +271,35 @@ cudaError_t launch_transpose(const uint16_t* in, long long rows, long long cols,
   return cudaGetLastError();
 }
 }  // namespace detffn
+
+// ------------------- self-check of the packed node add --------------------
+// Counts BF16 pairs (a, b) for which add.rn.bf16x2 differs from the tree
+// node rne_bf16(fp32(a) + fp32(b)); every NaN result counts as equal to every
+// other NaN.  Pairs are a = i >> 16, b = i & 0xffff for i in [begin, end).
+namespace detffn {
+namespace {
+__device__ __forceinline__ bool is_nan_bf16(uint32_t v) { return (v & 0x7F80u) == 0x7F80u && (v & 0x7Fu); }
+
+__global__ void k_check_node_add(unsigned long long begin, unsigned long long end, unsigned long long* bad) {
+  unsigned long long local = 0;
+  for (unsigned long long i = begin + blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; i < end;
+       i += (unsigned long long)gridDim.x * blockDim.x) {
+    const uint32_t a = (uint32_t)(i >> 16) & 0xFFFFu, b = (uint32_t)i & 0xFFFFu;
+    uint32_t packed;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(packed) : "r"(a | (b << 16)), "r"(b | (a << 16)));
+    const uint32_t ref = f2bf(__fadd_rn(bf2f((uint16_t)a), bf2f((uint16_t)b)));
+    const uint32_t lo = packed & 0xFFFFu, hi = packed >> 16;
+    const bool ok_lo = (lo == ref) || (is_nan_bf16(lo) && is_nan_bf16(ref));
+    const bool ok_hi = (hi == ref) || (is_nan_bf16(hi) && is_nan_bf16(ref));
+    local += (!ok_lo) + (!ok_hi);
+  }
+  if (local) atomicAdd(bad, local);
+}
+}  // namespace
+
+cudaError_t launch_check_node_add(unsigned long long begin, unsigned long long end, unsigned long long* bad,
+                                  int sm_count, cudaStream_t st) {
+  k_check_node_add<<<sm_count * 8, 256, 0, st>>>(begin, end, bad);
+  return cudaGetLastError();
+}
+}  // namespace detffn

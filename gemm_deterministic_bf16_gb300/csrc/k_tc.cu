@@ -57,10 +57,10 @@ template <int BN> struct TcGeo {
 __device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Tree node on packed pairs: rne_bf16(fp32(a) + fp32(b)) per half.
-__device__ __forceinline__ uint32_t node2(uint32_t a, uint32_t b) {
-  return pack_bf16x2(__fadd_rn(lo_f(a), lo_f(b)), __fadd_rn(hi_f(a), hi_f(b)));
-}
+// Tree node on packed pairs of BF16 nodes: rne_bf16(fp32(a) + fp32(b)) per
+// half, which is the correctly rounded BF16 sum, i.e. add.rn.bf16x2 (checked
+// on every one of the 2^32 operand pairs by detffn_selfcheck_node_add).
+__device__ __forceinline__ uint32_t node2(uint32_t a, uint32_t b) { return add_bf16x2(a, b); }
 
 struct Bars {
   uint64_t full[8], empty[8], accf[kAccBufs], acce[kAccBufs], fin;
@@ -102,8 +102,8 @@ __device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int 
   return stk + (((m - T::REG_LV) * 2 + half) * T::WORDS + w) * BM + row;
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int BN, int GG>
+__global__ void __maxnreg__(200)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const TcArgs a) {
   using T = TcGeo<BN>;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int tm = t % a.num_m, tn = t / a.num_m;
       const long long r = (long long)tm * BM + row;
       for (int q = 0; q < Q; ++q) {
-        for (int g = 0; g < a.G; ++g)
+        for (int g = 0; g < GG; ++g)
           if (!wait_or_abort(&bars->accf[(lc + g) % kAccBufs], (uint32_t)(((lc + g) / kAccBufs) & 1),
                              limit, abort_flag, a.status))
             ok = false;
@@ -228,22 +228,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t b0 = (uint32_t)((lc % kAccBufs) * BN), b1 = (uint32_t)(((lc + 1) % kAccBufs) * BN),
                        b2 = (uint32_t)(((lc + 2) % kAccBufs) * BN);
+        // Column chunks of CW: 32 (one TMEM read per leaf) for pairs, 16 for triples.
+        constexpr int CW = (GG == 3 || T::COLS < 32) ? 16 : 32;
 #pragma unroll
-        for (int c = 0; c < T::COLS / 16; ++c) {
-          uint32_t v0[16], v1[16], v2[16];
-          const uint32_t col = (uint32_t)(col0 + 16 * c);
-          tmem_ld16(tmem + lane_addr + b0 + col, v0);
-          if (a.G >= 2) tmem_ld16(tmem + lane_addr + b1 + col, v1);
-          if (a.G >= 3) tmem_ld16(tmem + lane_addr + b2 + col, v2);
+        for (int c = 0; c < T::COLS / CW; ++c) {
+          uint32_t v0[CW], v1[GG >= 2 ? CW : 1], v2[GG >= 3 ? CW : 1];
+          const uint32_t col = (uint32_t)(col0 + CW * c);
+          if constexpr (CW == 32) {
+            tmem_ld32(tmem + lane_addr + b0 + col, v0);
+            if constexpr (GG >= 2) tmem_ld32(tmem + lane_addr + b1 + col, v1);
+          } else {
+            tmem_ld16(tmem + lane_addr + b0 + col, v0);
+            if constexpr (GG >= 2) tmem_ld16(tmem + lane_addr + b1 + col, v1);
+            if constexpr (GG >= 3) tmem_ld16(tmem + lane_addr + b2 + col, v2);
+          }
           tmem_wait_ld();
-          uint32_t carry[8];
+          uint32_t carry[CW / 2];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
+          for (int i = 0; i < CW / 2; ++i) {
             float x = __uint_as_float(v0[2 * i]), y = __uint_as_float(v0[2 * i + 1]);
-            if (a.G == 2) {
+            if constexpr (GG == 2) {
               x = __fadd_rn(x, __uint_as_float(v1[2 * i]));
               y = __fadd_rn(y, __uint_as_float(v1[2 * i + 1]));
-            } else if (a.G == 3) {
+            } else if constexpr (GG == 3) {
               const uint32_t n12 = pack_bf16x2(__fadd_rn(__uint_as_float(v1[2 * i]), __uint_as_float(v2[2 * i])),
                                                __fadd_rn(__uint_as_float(v1[2 * i + 1]), __uint_as_float(v2[2 * i + 1])));
               x = __fadd_rn(x, lo_f(n12));
@@ -251,15 +258,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             carry[i] = pack_bf16x2(x, y);  // the group root (a lone leaf is rounded once)
           }
-          // Fold the 16 roots of this chunk into the stack (elementwise binary counter).
+          // Fold this chunk's roots into the stack (elementwise binary counter).
+          constexpr int WC = CW / 2;  // words per chunk
           int l = 0;
 #pragma unroll
           for (int m = 0; m < kMaxLv; ++m) {
             if (m >= a.E || !((q >> m) & 1)) break;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t left = (m < T::REG_LV) ? reg_lv[m < T::REG_LV ? m : 0][c * 8 + i]
-                                                    : *stk_at<BN>(stk, m, half, c * 8 + i, row);
+            for (int i = 0; i < WC; ++i) {
+              const uint32_t left = (m < T::REG_LV) ? reg_lv[m < T::REG_LV ? m : 0][c * WC + i]
+                                                    : *stk_at<BN>(stk, m, half, c * WC + i, row);
               carry[i] = node2(left, carry[i]);
             }
             l = m + 1;
@@ -269,21 +277,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int m = 0; m < kMaxLv; ++m)
               if (m == l) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  if (m < T::REG_LV) reg_lv[m < T::REG_LV ? m : 0][c * 8 + i] = carry[i];
-                  else *stk_at<BN>(stk, m, half, c * 8 + i, row) = carry[i];
+                for (int i = 0; i < WC; ++i) {
+                  if (m < T::REG_LV) reg_lv[m < T::REG_LV ? m : 0][c * WC + i] = carry[i];
+                  else *stk_at<BN>(stk, m, half, c * WC + i, row) = carry[i];
                 }
               }
           } else if (r < a.R) {
-            // The root: 16 output columns of row r.
+            // The root: CW output columns of row r.
             const long long c0 = (long long)tn * BN + col;
             uint16_t* o = a.out + r * a.ld_r + c0 * a.ld_c;
-            if (a.ld_c == 1 && c0 + 16 <= a.C && ((uintptr_t)o & 15u) == 0) {
-              reinterpret_cast<uint4*>(o)[0] = make_uint4(carry[0], carry[1], carry[2], carry[3]);
-              reinterpret_cast<uint4*>(o)[1] = make_uint4(carry[4], carry[5], carry[6], carry[7]);
+            if (a.ld_c == 1 && c0 + CW <= a.C && ((uintptr_t)o & 15u) == 0) {
+#pragma unroll
+              for (int v = 0; v < CW / 8; ++v)
+                reinterpret_cast<uint4*>(o)[v] = make_uint4(carry[4 * v], carry[4 * v + 1], carry[4 * v + 2], carry[4 * v + 3]);
             } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
+              for (int i = 0; i < CW; ++i)
                 if (c0 + i < a.C) o[i * a.ld_c] = (uint16_t)(carry[i >> 1] >> (16 * (i & 1)));
             }
           }
@@ -291,8 +300,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
-          for (int g = 0; g < a.G; ++g) mbar_arrive(&bars->acce[(lc + g) % kAccBufs]);
-        lc += a.G;
+          for (int g = 0; g < GG; ++g) mbar_arrive(&bars->acce[(lc + g) % kAccBufs]);
+        lc += GG;
       }
     }
   }
@@ -335,19 +344,31 @@ bool make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long K,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
-cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int sm_count,
-                      cudaStream_t st) {
+template <int BN, int GG>
+cudaError_t launch_bng(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int sm_count,
+                       cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(k_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<BN>::SMEM);
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_tc<BN, GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<BN>::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int tiles = a.num_m * a.num_n;
   const int grid = tiles < sm_count ? tiles : sm_count;
-  k_tc<BN><<<grid, kTcThreads, TcGeo<BN>::SMEM, st>>>(ta, tb, a);
+  k_tc<BN, GG><<<grid, kTcThreads, TcGeo<BN>::SMEM, st>>>(ta, tb, a);
   return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int sm_count,
+                      cudaStream_t st) {
+  switch (a.G) {
+    case 1: return launch_bng<BN, 1>(ta, tb, a, sm_count, st);
+    case 2: return launch_bng<BN, 2>(ta, tb, a, sm_count, st);
+    case 3: return launch_bng<BN, 3>(ta, tb, a, sm_count, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace

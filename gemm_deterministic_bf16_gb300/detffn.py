@@ -317,3 +317,14 @@ def detffn_forward_decode_noalloc(x, Wg, Wu, Wd, out=None, stream=None):
                                                M, H, I, _stream(x.device, stream)),
                "detffn_forward_decode_noalloc")
     return out
+
+
+def detffn_selfcheck_node_add(device=None):
+    """Number of BF16 pairs where the device's packed add differs from the
+    tree node rne_bf16(fp32(a) + fp32(b)) (exhaustive over 2^32 pairs)."""
+    L = lib()
+    L.detffn_selfcheck_node_add.argtypes = [_vp, ctypes.POINTER(ctypes.c_ulonglong)]
+    L.detffn_selfcheck_node_add.restype = ctypes.c_int
+    n = ctypes.c_ulonglong()
+    _check(L.detffn_selfcheck_node_add(handle(device), ctypes.byref(n)), "detffn_selfcheck_node_add")
+    return n.value

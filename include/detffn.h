@@ -238,6 +238,14 @@ DETFFN_API detffn_status detffn_forward_decode_noalloc(const void *x, const void
                                                        long long M, long long H, long long I,
                                                        void *stream);
 
+/* Diagnostic: counts the BF16 pairs (a, b), over all 2^32 of them, for which
+ * the device's packed add.rn.bf16x2 differs from the tree node
+ * rne_bf16(fp32(a) + fp32(b)) (any NaN equals any NaN).  The tree's higher
+ * nodes use the packed add only if this is 0 (the two are the same rounding
+ * of a + b, since binary32 has more than 2*8+2 significand bits).  Allocates
+ * an 8-byte counter and synchronises the device. */
+DETFFN_API detffn_status detffn_selfcheck_node_add(detffn_handle h, unsigned long long *mismatches);
+
 /* Synchronises `stream`, then returns and clears the handle's device status
  * word (DETFFN_OK or DETFFN_ERR_TIMEOUT from a bounded wait). */
 DETFFN_API detffn_status detffn_get_status(detffn_handle h, void *stream);

@@ -319,7 +319,13 @@ detffn_status check_sizes(long long M, long long H, long long I) {
   return DETFFN_OK;
 }
 
-detffn_status cu(cudaError_t e) { return e == cudaSuccess ? DETFFN_OK : DETFFN_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+detffn_status cu(cudaError_t e) {
+  if (e == cudaSuccess) return DETFFN_OK;
+  g_last_cuda = e;
+  return DETFFN_ERR_CUDA;
+}
 
 #define TRY(expr)                              \
   do {                                         \
@@ -969,4 +975,10 @@ extern "C" detffn_status detffn_selfcheck_node_add(detffn_handle h, unsigned lon
   if (s == DETFFN_OK) s = cu(cudaMemcpy(mismatches, d, sizeof(unsigned long long), cudaMemcpyDeviceToHost));
   cudaFree(d);
   return s;
+}
+
+extern "C" const char* detffn_last_cuda_error(void) {
+  const cudaError_t e = g_last_cuda;
+  g_last_cuda = cudaSuccess;
+  return e == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(e);
 }

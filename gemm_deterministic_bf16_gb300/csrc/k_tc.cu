@@ -103,7 +103,7 @@ __device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int 
 }
 
 template <int BN, int GG>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kTcThreads)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const TcArgs a) {
   using T = TcGeo<BN>;

@@ -26,7 +26,15 @@ _vp, _ll, _int = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int
 class DetFFNError(RuntimeError):
     def __init__(self, status, what):
         self.status = status
-        super().__init__("%s: %s (status %d)" % (what, _status_string(status), status))
+        msg = "%s: %s (status %d)" % (what, _status_string(status), status)
+        if status == ERR_CUDA:
+            try:
+                L = lib()
+                L.detffn_last_cuda_error.restype = ctypes.c_char_p
+                msg += ": " + L.detffn_last_cuda_error().decode()
+            except Exception:  # noqa: BLE001 - only used to format an error message
+                pass
+        super().__init__(msg)
 
 
 class Options(ctypes.Structure):

@@ -250,6 +250,10 @@ DETFFN_API detffn_status detffn_selfcheck_node_add(detffn_handle h, unsigned lon
  * word (DETFFN_OK or DETFFN_ERR_TIMEOUT from a bounded wait). */
 DETFFN_API detffn_status detffn_get_status(detffn_handle h, void *stream);
 
+/* The CUDA error behind the calling thread's last DETFFN_ERR_CUDA (a static
+ * string); reading it clears it. */
+DETFFN_API const char *detffn_last_cuda_error(void);
+
 /* Static description of a status code. */
 DETFFN_API const char *detffn_status_string(detffn_status s);
 

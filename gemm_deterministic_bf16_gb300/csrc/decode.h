@@ -32,9 +32,8 @@ struct DecArgs {
 // uses the general exact kernel, which gives the same bits).
 bool decode_geometry(long long K, int* S, int* NB);
 
-// Bytes of partial planes and tickets for one pass over N rows (2N in gate/up mode).
+// Elements of the block-root planes for one pass over rows_total rows.
 size_t decode_part_elems(long long K, long long rows_total);
-int decode_tiles(long long K, long long N, bool gate_up, int sm_count, int* RT);
 
 // Launches one pass (M <= 8 tokens).  Returns cudaErrorInvalidValue if the
 // geometry is not covered.

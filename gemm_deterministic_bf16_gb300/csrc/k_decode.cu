@@ -41,39 +41,31 @@ template <int S> struct Geo {
 };
 
 // The 8-lane transpose-reduce.  Lane l (l = lane & 7) enters with its group
-// sums s[t] for MT tokens and leaves with the leaf of token l % MT.
+// sums s[j] for MT tokens held in the lane-dependent order j = token ^ (l % MT)
+// and leaves with the leaf of token l % MT.  At the step with lane distance d
+// (1, 2, 4) a lane keeps the tokens whose bit log2(d) equals its own, adds
+// the partner's partial for the same token, and hands over the others; the
+// permuted order makes "keep" and "send" fixed registers.  The pairs formed
+// are ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)) over the 8 lanes' group sums.
 template <int MT>
-__device__ __forceinline__ float reduce_leaf(const float (&s)[MT], int l) {
+__device__ __forceinline__ float reduce_leaf(const float (&s)[MT]) {
   constexpr int N1 = MT > 1 ? MT / 2 : 1;
   constexpr int N2 = N1 > 1 ? N1 / 2 : 1;
   float a[N1], b[N2];
   if constexpr (MT >= 2) {
-    const bool hi = l & 1;
 #pragma unroll
-    for (int j = 0; j < N1; ++j) {
-      const float keep = hi ? s[2 * j + 1] : s[2 * j];
-      const float send = hi ? s[2 * j] : s[2 * j + 1];
-      a[j] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 1));
-    }
+    for (int j = 0; j < N1; ++j) a[j] = __fadd_rn(s[2 * j], __shfl_xor_sync(0xffffffffu, s[2 * j + 1], 1));
   } else {
     a[0] = __fadd_rn(s[0], __shfl_xor_sync(0xffffffffu, s[0], 1));
   }
   if constexpr (N1 >= 2) {
-    const bool hi = (l >> 1) & 1;
 #pragma unroll
-    for (int j = 0; j < N2; ++j) {
-      const float keep = hi ? a[2 * j + 1] : a[2 * j];
-      const float send = hi ? a[2 * j] : a[2 * j + 1];
-      b[j] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-    }
+    for (int j = 0; j < N2; ++j) b[j] = __fadd_rn(a[2 * j], __shfl_xor_sync(0xffffffffu, a[2 * j + 1], 2));
   } else {
     b[0] = __fadd_rn(a[0], __shfl_xor_sync(0xffffffffu, a[0], 2));
   }
   if constexpr (N2 >= 2) {
-    const bool hi = (l >> 2) & 1;
-    const float keep = hi ? b[1] : b[0];
-    const float send = hi ? b[0] : b[1];
-    return __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    return __fadd_rn(b[0], __shfl_xor_sync(0xffffffffu, b[1], 4));
   } else {
     return __fadd_rn(b[0], __shfl_xor_sync(0xffffffffu, b[0], 4));
   }
@@ -211,7 +203,9 @@ __global__ void __launch_bounds__(Geo<S>::THREADS) k_decode(DecArgs a) {
   if (tid == 0)
     for (int q = 0; q < kStages && q < nbatch; ++q) issue(q);
 
-  // This lane's x slice: 8 contiguous K positions for every token.
+  // This lane's x slice: 8 contiguous K positions for every token, then
+  // permuted so that slot j holds token j ^ (l % MT) (the order reduce_leaf
+  // expects): one conditional swap per bit of l, once per CTA.
   float xr[MT][8];
   const long long kk = k0 + g * 64 + l * 8;
 #pragma unroll
@@ -222,6 +216,20 @@ __global__ void __launch_bounds__(Geo<S>::THREADS) k_decode(DecArgs a) {
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e) xr[t][e] = 0.0f;
+    }
+  }
+#pragma unroll
+  for (int bit = 1; bit < MT; bit <<= 1) {
+    const bool sw = (l & bit) != 0;
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+      if (j & bit) continue;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float u = xr[j][e], v = xr[j | bit][e];
+        xr[j][e] = sw ? v : u;
+        xr[j | bit][e] = sw ? u : v;
+      }
     }
   }
 
@@ -236,15 +244,15 @@ __global__ void __launch_bounds__(Geo<S>::THREADS) k_decode(DecArgs a) {
     for (int r = 0; r < RB; ++r) {
       float w[8];
       unpack8(*reinterpret_cast<const uint4*>(st + r * ROWB + g * 128 + l * 16), w);
-      float sacc[MT];
+      float sacc[MT];  // group sums in the permuted token order
 #pragma unroll
-      for (int t = 0; t < MT; ++t) {
+      for (int j = 0; j < MT; ++j) {
         float acc = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc = __fmaf_rn(xr[t][e], w[e], acc);
-        sacc[t] = acc;
+        for (int e = 0; e < 8; ++e) acc = __fmaf_rn(xr[j][e], w[e], acc);
+        sacc[j] = acc;
       }
-      const float leaf = reduce_leaf<MT>(sacc, l);
+      const float leaf = reduce_leaf<MT>(sacc);
       if (l < MT) lv[(r * 8 + l) * (S + 1) + g] = leaf;
     }
     __syncthreads();
@@ -285,29 +293,35 @@ __global__ void __launch_bounds__(Geo<S>::THREADS) k_decode(DecArgs a) {
 }
 
 template <int MT, int S>
-cudaError_t launch_ms(const DecArgs& a, int NB, int tiles, cudaStream_t st) {
+cudaError_t launch_ms(DecArgs a, int NB, int sm_count, cudaStream_t st) {
   using G = Geo<S>;
-  static bool attr = false;  // set once per process (device-independent attribute)
-  if (!attr) {
+  static int per_sm = 0;  // resident CTAs per SM for this instance (registers, threads, smem)
+  if (!per_sm) {
     cudaError_t e = cudaFuncSetAttribute(k_decode<MT, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode<MT, S>, G::THREADS, G::SMEM);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
   }
+  // Rows per tile so that the grid is one wave of resident CTAs.
+  long long tiles = ((long long)sm_count * per_sm) / NB;
+  if (tiles < 1) tiles = 1;
+  long long rt = (a.N + tiles - 1) / tiles;
+  if (rt < 1) rt = 1;
+  a.RT = (int)rt;
+  tiles = (a.N + rt - 1) / rt;
+  if (tiles > 65535) return cudaErrorInvalidValue;
   k_decode<MT, S><<<dim3((unsigned)NB, (unsigned)tiles), G::THREADS, G::SMEM, st>>>(a);
   return cudaGetLastError();
 }
 
 template <int S>
-cudaError_t launch_s(const DecArgs& a, int NB, int tiles, cudaStream_t st) {
-  if (a.M <= 1) return launch_ms<1, S>(a, NB, tiles, st);
-  if (a.M <= 2) return launch_ms<2, S>(a, NB, tiles, st);
-  if (a.M <= 4) return launch_ms<4, S>(a, NB, tiles, st);
-  return launch_ms<8, S>(a, NB, tiles, st);
+cudaError_t launch_s(const DecArgs& a, int NB, int sm_count, cudaStream_t st) {
+  if (a.M <= 1) return launch_ms<1, S>(a, NB, sm_count, st);
+  if (a.M <= 2) return launch_ms<2, S>(a, NB, sm_count, st);
+  if (a.M <= 4) return launch_ms<4, S>(a, NB, sm_count, st);
+  return launch_ms<8, S>(a, NB, sm_count, st);
 }
-
-int mt_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
-
-template <int S> int smem_of() { return Geo<S>::SMEM; }
 
 }  // namespace
 
@@ -334,37 +348,14 @@ size_t decode_part_elems(long long K, long long rows_total) {
   return (size_t)NB * 8 * (size_t)rows_total;
 }
 
-// Rows per tile so that the grid is about one full wave of resident CTAs.
-int decode_tiles(long long K, long long N, bool gate_up, int sm_count, int* RT) {
-  int S, NB;
-  if (!decode_geometry(K, &S, &NB)) return 0;
-  const int smem = S == 4 ? smem_of<4>() : S == 8 ? smem_of<8>() : S == 12 ? smem_of<12>() : smem_of<24>();
-  int per_sm = (227 * 1024) / (smem + 1024);
-  const int by_threads = 2048 / (8 * S);
-  if (per_sm > by_threads) per_sm = by_threads;
-  if (per_sm > 32) per_sm = 32;
-  if (per_sm < 1) per_sm = 1;
-  long long tiles = ((long long)sm_count * per_sm) / NB;
-  if (tiles < 1) tiles = 1;
-  long long rt = (N + tiles - 1) / tiles;
-  if (rt < 1) rt = 1;
-  (void)gate_up;
-  *RT = (int)rt;
-  return (int)((N + rt - 1) / rt);
-}
-
 cudaError_t launch_decode_exact(DecArgs a, int sm_count, cudaStream_t st) {
-  int S, NB, RT;
+  int S, NB;
   if (a.M < 1 || a.M > 8 || !decode_geometry(a.K, &S, &NB)) return cudaErrorInvalidValue;
-  const int tiles = decode_tiles(a.K, a.N, a.w1 != nullptr, sm_count, &RT);
-  if (tiles > 65535) return cudaErrorInvalidValue;
-  a.RT = RT;
-  (void)mt_of;
   switch (S) {
-    case 4: return launch_s<4>(a, NB, tiles, st);
-    case 8: return launch_s<8>(a, NB, tiles, st);
-    case 12: return launch_s<12>(a, NB, tiles, st);
-    case 24: return launch_s<24>(a, NB, tiles, st);
+    case 4: return launch_s<4>(a, NB, sm_count, st);
+    case 8: return launch_s<8>(a, NB, sm_count, st);
+    case 12: return launch_s<12>(a, NB, sm_count, st);
+    case 24: return launch_s<24>(a, NB, sm_count, st);
     default: return cudaErrorInvalidValue;
   }
 }

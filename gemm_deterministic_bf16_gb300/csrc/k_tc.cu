@@ -12,15 +12,17 @@
 //
 // Roles (one CTA per SM, persistent over output tiles of 128 x BN):
 //   warp 0      TMA producer: A and B tiles of one leaf per pipeline stage
-//               (128-byte swizzle, K-major), NSTAGE stages on mbarriers;
+//               (128-byte swizzle, K-major), a ring of stages on mbarriers (as many
+//               as fit beside the shared-memory stack levels);
 //   warp 1      allocates TMEM (4 leaf buffers of BN columns) and issues the
 //               MMAs, one leaf per buffer, committing to the stage's "empty"
 //               barrier and the buffer's "full" barrier;
 //   warps 2-9   epilogue: each thread owns one row (TMEM lane) and BN/2
 //               columns; it reads a group's leaves from TMEM, forms the
-//               group root, returns the buffers, and folds the root into a
-//               binary-counter stack of BF16 nodes (low levels in registers,
-//               high levels in shared memory); the last fold is the output.
+//               group roots, returns the buffers at once, and then folds the
+//               roots into a binary-counter stack of BF16 nodes (low levels
+//               in registers, high levels in shared memory); the last fold
+//               is the output.
 // Every wait is bounded; on a timeout the CTA records DETFFN_ERR_TIMEOUT,
 // stops, drains its own copies and MMAs (bounded) and frees its TMEM.
 #include <cuda.h>
@@ -36,7 +38,8 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kAccBufs = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kTcThreads = 32 * (2 + kEpiWarps);
+constexpr int kEpiWarp0 = 2;  // warp 0: producer, warp 1: MMA, warps 2-9: epilogue
+constexpr int kTcThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kMaxLv = 6;  // up to Q = 64 bottom groups
 
 template <int BN> struct TcGeo {
@@ -45,13 +48,22 @@ template <int BN> struct TcGeo {
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int COLS = BN / 2;    // columns per epilogue thread
   static constexpr int WORDS = COLS / 2;  // packed BF16 pairs per stack level per thread
-  static constexpr int REG_LV = BN >= 128 ? 3 : kMaxLv;
-  static constexpr int SMEM_LV = kMaxLv - REG_LV;
-  static constexpr int NSTAGE = BN >= 128 ? 4 : 6;
-  static constexpr int STACK_BYTES = SMEM_LV * BM * COLS * 2 * 2;
+  static constexpr int REG_LV = BN >= 128 ? 2 : kMaxLv;  // stack levels kept in registers
+  static constexpr int LV_BYTES = BM * COLS * 2 * 2;       // one shared-memory stack level
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = 1024 + NSTAGE * STAGE + STACK_BYTES + BAR_BYTES;
+  static constexpr int MAX_SMEM = 227 * 1024;
+  static constexpr int MAX_STAGES = 8;
   static constexpr int TMEM_COLS = kAccBufs * BN;
+  // Stages that fit beside the shared-memory stack levels a tree of E levels needs.
+  static __host__ __device__ int stages_for(int E) {
+    const int lv = E > REG_LV ? E - REG_LV : 0;
+    int n = (MAX_SMEM - 1024 - BAR_BYTES - lv * LV_BYTES) / STAGE;
+    return n > MAX_STAGES ? MAX_STAGES : n;
+  }
+  static __host__ __device__ int smem_for(int E, int nstage) {
+    const int lv = E > REG_LV ? E - REG_LV : 0;
+    return 1024 + nstage * STAGE + lv * LV_BYTES + BAR_BYTES;
+  }
 };
 
 __device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
@@ -63,7 +75,7 @@ __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0
 __device__ __forceinline__ uint32_t node2(uint32_t a, uint32_t b) { return add_bf16x2(a, b); }
 
 struct Bars {
-  uint64_t full[8], empty[8], accf[kAccBufs], acce[kAccBufs], fin;
+  uint64_t full[8], empty[8], accf[kAccBufs], acce[kAccBufs], fin;  // up to 8 stages
   uint32_t tmem_slot;
   int abort;
 };
@@ -87,7 +99,7 @@ namespace detffn {
 namespace {
 
 struct TcArgs {
-  int R, C, L, G, E;
+  int R, C, L, G, E, nstage;
   int num_m, num_n;
   uint16_t* out;
   long long ld_r, ld_c;
@@ -103,15 +115,17 @@ __device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int 
 }
 
 template <int BN, int GG>
-__global__ void __launch_bounds__(kTcThreads)
+__global__ void __launch_bounds__(kTcThreads, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const TcArgs a) {
   using T = TcGeo<BN>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int NS = a.nstage;
+  const int slv = a.E > T::REG_LV ? a.E - T::REG_LV : 0;
   unsigned char* stages = smem;
-  uint32_t* stk = reinterpret_cast<uint32_t*>(smem + T::NSTAGE * T::STAGE);
-  Bars* bars = reinterpret_cast<Bars*>(smem + T::NSTAGE * T::STAGE + T::STACK_BYTES);
+  uint32_t* stk = reinterpret_cast<uint32_t*>(smem + NS * T::STAGE);
+  Bars* bars = reinterpret_cast<Bars*>(smem + NS * T::STAGE + slv * T::LV_BYTES);
   volatile int* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -119,7 +133,7 @@ __global__ void __launch_bounds__(kTcThreads)
   const long long limit = a.spin > 0 ? a.spin : kDefaultSpin;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < T::NSTAGE; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
@@ -152,8 +166,8 @@ __global__ void __launch_bounds__(kTcThreads)
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         const int tm = t % a.num_m, tn = t / a.num_m;
         for (int j = 0; j < a.L; ++j, ++it) {
-          const int s = (int)(it % T::NSTAGE);
-          if (!wait_or_abort(&bars->empty[s], (uint32_t)(((it / T::NSTAGE) & 1) ^ 1), limit, abort_flag,
+          const int s = (int)(it % NS);
+          if (!wait_or_abort(&bars->empty[s], (uint32_t)(((it / NS) & 1) ^ 1), limit, abort_flag,
                              a.status)) {
             ok = false;
             break;
@@ -165,8 +179,8 @@ __global__ void __launch_bounds__(kTcThreads)
         }
       }
       // Drain: the last loads issued into each stage have landed.
-      for (long long i = (it > T::NSTAGE ? it - T::NSTAGE : 0); i < it; ++i)
-        mbar_wait(&bars->full[i % T::NSTAGE], (uint32_t)((i / T::NSTAGE) & 1), limit, nullptr);
+      for (long long i = (it > NS ? it - NS : 0); i < it; ++i)
+        mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), limit, nullptr);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -182,8 +196,8 @@ __global__ void __launch_bounds__(kTcThreads)
             ok = false;
             break;
           }
-          const int s = (int)(it % T::NSTAGE);
-          if (!wait_or_abort(&bars->full[s], (uint32_t)((it / T::NSTAGE) & 1), limit, abort_flag,
+          const int s = (int)(it % NS);
+          if (!wait_or_abort(&bars->full[s], (uint32_t)((it / NS) & 1), limit, abort_flag,
                              a.status)) {
             ok = false;
             break;
@@ -201,9 +215,9 @@ __global__ void __launch_bounds__(kTcThreads)
       tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
       mbar_wait(&bars->fin, 0, limit, nullptr);
     }
-  } else {
+  } else if (warp >= kEpiWarp0) {
     // ---------------- epilogue: leaves -> tree ----------------
-    const int ew = warp - 2;
+    const int ew = warp - kEpiWarp0;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int half = ew >> 2;
     const int row = quarter * 32 + lane;
@@ -228,24 +242,21 @@ __global__ void __launch_bounds__(kTcThreads)
         tc_fence_after();
         const uint32_t b0 = (uint32_t)((lc % kAccBufs) * BN), b1 = (uint32_t)(((lc + 1) % kAccBufs) * BN),
                        b2 = (uint32_t)(((lc + 2) % kAccBufs) * BN);
-        // Column chunks of CW: 32 (one TMEM read per leaf) for pairs, 16 for triples.
-        constexpr int CW = (GG == 3 || T::COLS < 32) ? 16 : 32;
+        // Phase 1: read the group's leaves from TMEM in column chunks of 16
+        // and form the group roots.
+        constexpr int CW = 16;
+        constexpr int WC = CW / 2;  // packed words per chunk
+        uint32_t root[T::WORDS];
 #pragma unroll
         for (int c = 0; c < T::COLS / CW; ++c) {
           uint32_t v0[CW], v1[GG >= 2 ? CW : 1], v2[GG >= 3 ? CW : 1];
           const uint32_t col = (uint32_t)(col0 + CW * c);
-          if constexpr (CW == 32) {
-            tmem_ld32(tmem + lane_addr + b0 + col, v0);
-            if constexpr (GG >= 2) tmem_ld32(tmem + lane_addr + b1 + col, v1);
-          } else {
-            tmem_ld16(tmem + lane_addr + b0 + col, v0);
-            if constexpr (GG >= 2) tmem_ld16(tmem + lane_addr + b1 + col, v1);
-            if constexpr (GG >= 3) tmem_ld16(tmem + lane_addr + b2 + col, v2);
-          }
+          tmem_ld16(tmem + lane_addr + b0 + col, v0);
+          if constexpr (GG >= 2) tmem_ld16(tmem + lane_addr + b1 + col, v1);
+          if constexpr (GG >= 3) tmem_ld16(tmem + lane_addr + b2 + col, v2);
           tmem_wait_ld();
-          uint32_t carry[CW / 2];
 #pragma unroll
-          for (int i = 0; i < CW / 2; ++i) {
+          for (int i = 0; i < WC; ++i) {
             float x = __uint_as_float(v0[2 * i]), y = __uint_as_float(v0[2 * i + 1]);
             if constexpr (GG == 2) {
               x = __fadd_rn(x, __uint_as_float(v1[2 * i]));
@@ -256,52 +267,53 @@ __global__ void __launch_bounds__(kTcThreads)
               x = __fadd_rn(x, lo_f(n12));
               y = __fadd_rn(y, hi_f(n12));
             }
-            carry[i] = pack_bf16x2(x, y);  // the group root (a lone leaf is rounded once)
-          }
-          // Fold this chunk's roots into the stack (elementwise binary counter).
-          constexpr int WC = CW / 2;  // words per chunk
-          int l = 0;
-#pragma unroll
-          for (int m = 0; m < kMaxLv; ++m) {
-            if (m >= a.E || !((q >> m) & 1)) break;
-#pragma unroll
-            for (int i = 0; i < WC; ++i) {
-              const uint32_t left = (m < T::REG_LV) ? reg_lv[m < T::REG_LV ? m : 0][c * WC + i]
-                                                    : *stk_at<BN>(stk, m, half, c * WC + i, row);
-              carry[i] = node2(left, carry[i]);
-            }
-            l = m + 1;
-          }
-          if (q != Q - 1) {
-#pragma unroll
-            for (int m = 0; m < kMaxLv; ++m)
-              if (m == l) {
-#pragma unroll
-                for (int i = 0; i < WC; ++i) {
-                  if (m < T::REG_LV) reg_lv[m < T::REG_LV ? m : 0][c * WC + i] = carry[i];
-                  else *stk_at<BN>(stk, m, half, c * WC + i, row) = carry[i];
-                }
-              }
-          } else if (r < a.R) {
-            // The root: CW output columns of row r.
-            const long long c0 = (long long)tn * BN + col;
-            uint16_t* o = a.out + r * a.ld_r + c0 * a.ld_c;
-            if (a.ld_c == 1 && c0 + CW <= a.C && ((uintptr_t)o & 15u) == 0) {
-#pragma unroll
-              for (int v = 0; v < CW / 8; ++v)
-                reinterpret_cast<uint4*>(o)[v] = make_uint4(carry[4 * v], carry[4 * v + 1], carry[4 * v + 2], carry[4 * v + 3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < CW; ++i)
-                if (c0 + i < a.C) o[i * a.ld_c] = (uint16_t)(carry[i >> 1] >> (16 * (i & 1)));
-            }
+            root[c * WC + i] = pack_bf16x2(x, y);  // a lone leaf (GG == 1) is rounded once
           }
         }
+        // The leaves are in registers: return the TMEM buffers to the MMA warp.
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
           for (int g = 0; g < GG; ++g) mbar_arrive(&bars->acce[(lc + g) % kAccBufs]);
         lc += GG;
+
+        // Phase 2: fold the roots into the stack (an elementwise binary counter).
+        int l = 0;
+#pragma unroll
+        for (int m = 0; m < kMaxLv; ++m) {
+          if (m >= a.E || !((q >> m) & 1)) break;
+#pragma unroll
+          for (int w = 0; w < T::WORDS; ++w) {
+            const uint32_t left = (m < T::REG_LV) ? reg_lv[m < T::REG_LV ? m : 0][w]
+                                                  : *stk_at<BN>(stk, m, half, w, row);
+            root[w] = node2(left, root[w]);
+          }
+          l = m + 1;
+        }
+        if (q != Q - 1) {
+#pragma unroll
+          for (int m = 0; m < kMaxLv; ++m)
+            if (m == l) {
+#pragma unroll
+              for (int w = 0; w < T::WORDS; ++w) {
+                if (m < T::REG_LV) reg_lv[m < T::REG_LV ? m : 0][w] = root[w];
+                else *stk_at<BN>(stk, m, half, w, row) = root[w];
+              }
+            }
+        } else if (r < a.R) {
+          // The tile's output: COLS columns of row r.
+          const long long c0 = (long long)tn * BN + col0;
+          uint16_t* o = a.out + r * a.ld_r + c0 * a.ld_c;
+          if (a.ld_c == 1 && c0 + T::COLS <= a.C && ((uintptr_t)o & 15u) == 0) {
+#pragma unroll
+            for (int v = 0; v < T::COLS / 8; ++v)
+              reinterpret_cast<uint4*>(o)[v] = make_uint4(root[4 * v], root[4 * v + 1], root[4 * v + 2], root[4 * v + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < T::COLS; ++i)
+              if (c0 + i < a.C) o[i * a.ld_c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
+          }
+        }
       }
     }
   }
@@ -350,13 +362,14 @@ cudaError_t launch_bng(const CUtensorMap& ta, const CUtensorMap& tb, const TcArg
   static bool attr = false;
   if (!attr) {
     const cudaError_t e =
-        cudaFuncSetAttribute(k_tc<BN, GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<BN>::SMEM);
+        cudaFuncSetAttribute(k_tc<BN, GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<BN>::MAX_SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int tiles = a.num_m * a.num_n;
   const int grid = tiles < sm_count ? tiles : sm_count;
-  k_tc<BN, GG><<<grid, kTcThreads, TcGeo<BN>::SMEM, st>>>(ta, tb, a);
+  const int smem = TcGeo<BN>::smem_for(a.E, a.nstage);
+  k_tc<BN, GG><<<grid, kTcThreads, smem, st>>>(ta, tb, a);
   return cudaGetLastError();
 }
 
@@ -421,6 +434,8 @@ cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, 
   a.ld_c = ld_c;
   a.status = status;
   a.spin = spin_limit;
+  a.nstage = bn == 32 ? TcGeo<32>::stages_for(E) : bn == 64 ? TcGeo<64>::stages_for(E) : TcGeo<128>::stages_for(E);
+  if (a.nstage < 2) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   if (!make_map(&ta, A, R, K, lda, BM) || !make_map(&tb, B, C, K, ldb, bn)) return cudaErrorInvalidValue;
   switch (bn) {

@@ -219,7 +219,7 @@ struct Arena {
   }
 };
 
-struct FwdWs { uint16_t *gate, *up, *h, *parts, *dec_part; unsigned* dec_cnt; };
+struct FwdWs { uint16_t *gate, *up, *h, *parts, *dec_part, *tc_part; unsigned *dec_cnt, *tc_cnt; };
 // Decode scratch: block-root planes (at most 8 blocks x 8 tokens x rows) and
 // one ticket per row tile (at most one tile per row).
 constexpr long long kDecPlanes = 64;
@@ -232,6 +232,10 @@ FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k) {
   const long long rows = 2 * I > H ? 2 * I : H;
   w.dec_part = M <= 32 ? a.take<uint16_t>(kDecPlanes * rows) : nullptr;
   w.dec_cnt = M <= 32 ? a.take<unsigned>(rows + 1) : nullptr;
+  // Tensor family with few tokens: up to 16 K blocks x 32 tokens x weight rows.
+  const long long wrows = I > H ? I : H;
+  w.tc_part = M <= 32 ? a.take<uint16_t>(16 * 32 * wrows) : nullptr;
+  w.tc_cnt = M <= 32 ? a.take<unsigned>(wrows / 128 + 2) : nullptr;
   return w;
 }
 
@@ -357,15 +361,16 @@ bool tc_operands_ok(const Strided& X) {
 }
 
 detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long long R, long long C,
-                        long long K, uint16_t* out, long long o_rs, cudaStream_t st) {
+                        long long K, uint16_t* out, long long o_rs, cudaStream_t st,
+                        const TcScratch& scratch = TcScratch()) {
   const double bytes = 2.0 * ((double)R * K + (double)C * K + (double)R * C);
   if (f == kTensor) {
     if (!tc_operands_ok(A) || !tc_operands_ok(B)) return DETFFN_ERR_ALIGN;
     return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
       if (R <= 32)
-        return cu(launch_tc_gemm(B.p, B.rs, A.p, A.rs, C, R, K, out, 1, o_rs, 32, h->d_status, 0,
+        return cu(launch_tc_gemm(B.p, B.rs, A.p, A.rs, C, R, K, out, 1, o_rs, 32, scratch, h->d_status, 0,
                                  h->sm_count, st));
-      return cu(launch_tc_gemm(A.p, A.rs, B.p, B.rs, R, C, K, out, o_rs, 1, 128, h->d_status, 0,
+      return cu(launch_tc_gemm(A.p, A.rs, B.p, B.rs, R, C, K, out, o_rs, 1, 128, scratch, h->d_status, 0,
                                h->sm_count, st));
     });
   }
@@ -587,10 +592,10 @@ detffn_status check_ffn_ptrs(const void* x, const void* Wg, const void* Wu, cons
 detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const uint16_t* Wg,
                            const uint16_t* Wu, uint16_t* gate, uint16_t* up, uint16_t* hh,
                            long long M, long long H, long long I, long long s, long long w,
-                           cudaStream_t st) {
+                           cudaStream_t st, const TcScratch& sc) {
   const Strided X{x, H, 1};
-  TRY(tree_gemm(h, f, X, Strided{Wg + s * w * H, H, 1}, M, w, H, gate + s * w, I, st));
-  TRY(tree_gemm(h, f, X, Strided{Wu + s * w * H, H, 1}, M, w, H, up + s * w, I, st));
+  TRY(tree_gemm(h, f, X, Strided{Wg + s * w * H, H, 1}, M, w, H, gate + s * w, I, st, sc));
+  TRY(tree_gemm(h, f, X, Strided{Wu + s * w * H, H, 1}, M, w, H, up + s * w, I, st, sc));
   return silu_mul(h, gate + s * w, up + s * w, hh + s * w, M, w, I, st);
 }
 
@@ -641,6 +646,15 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
                    decode_covers(M, H, sw, {x, Wg, Wu, Wd, w.h, (const void*)(w.h + sw)});
   const bool saves = gate_save != nullptr;
   if (dec) TRYCU(cudaMemsetAsync(w.dec_cnt, 0, sizeof(unsigned) * (size_t)((2 * I > H ? 2 * I : H) + 1), st));
+  TcScratch sc;
+  if (f == kTensor && w.tc_part) {
+    const long long wrows = I > H ? I : H;
+    sc.part = w.tc_part;
+    sc.part_elems = (size_t)(16 * 32 * wrows);
+    sc.cnt = w.tc_cnt;
+    sc.cnt_elems = (size_t)(wrows / 128 + 2);
+    TRYCU(cudaMemsetAsync(sc.cnt, 0, sizeof(unsigned) * sc.cnt_elems, st));
+  }
   for (long long s = 0; s < k; ++s) {
     uint16_t* dst = k == 1 ? (uint16_t*)out : w.parts + s * M * H;
     if (dec) {
@@ -649,8 +663,8 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
                         w.dec_part, w.dec_cnt, st));
       TRY(decode_plain(h, w.h + s * sw, I, WD + s * sw, I, H, sw, M, dst, H, w.dec_part, w.dec_cnt, st));
     } else {
-      TRY(gateup_slice(h, f, X, WG, WU, gate, up, w.h, M, H, I, s, sw, st));
-      TRY(tree_gemm(h, f, Strided{w.h + s * sw, I, 1}, Strided{WD + s * sw, I, 1}, M, H, sw, dst, H, st));
+      TRY(gateup_slice(h, f, X, WG, WU, gate, up, w.h, M, H, I, s, sw, st, sc));
+      TRY(tree_gemm(h, f, Strided{w.h + s * sw, I, 1}, Strided{WD + s * sw, I, 1}, M, H, sw, dst, H, st, sc));
     }
   }
   if (k == 1) return DETFFN_OK;

@@ -76,8 +76,10 @@ __device__ __forceinline__ uint32_t node2(uint32_t a, uint32_t b) { return add_b
 
 struct Bars {
   uint64_t full[8], empty[8], accf[kAccBufs], acce[kAccBufs], fin;  // up to 8 stages
+  uint64_t epi;  // epilogue-warps rendezvous (split-K tickets)
   uint32_t tmem_slot;
   int abort;
+  int last;
 };
 
 // Bounded wait that also gives up when another role has aborted.
@@ -99,13 +101,54 @@ namespace detffn {
 namespace {
 
 struct TcArgs {
-  int R, C, L, G, E, nstage;
+  int R, C;
+  int L, G, E;      // leaves per unit (one K block), bottom group size, levels per unit
+  int nb;           // K blocks per output tile (split-K by aligned subtrees); 1 = whole K
+  int nstage;
   int num_m, num_n;
   uint16_t* out;
   long long ld_r, ld_c;
+  uint16_t* part;   // nb > 1: block roots [nb][R][C] (scratch)
+  unsigned* cnt;    // nb > 1: one ticket per tile (scratch, zero on entry and on exit)
   int* status;
   long long spin;
 };
+
+// Writes the COLS columns of one row held as packed BF16 pairs: element i goes
+// to base[row_off + (c0 + i) * ld_c] for c0 + i < C.
+template <int WORDS>
+__device__ __forceinline__ void store_cols(uint16_t* base, long long row_off, long long c0, long long ld_c,
+                                           long long C, const uint32_t (&root)[WORDS]) {
+  uint16_t* o = base + row_off + c0 * ld_c;
+  if (ld_c == 1 && c0 + 2 * WORDS <= C && ((uintptr_t)o & 15u) == 0) {
+#pragma unroll
+    for (int v = 0; v < WORDS / 4; ++v)
+      reinterpret_cast<uint4*>(o)[v] = make_uint4(root[4 * v], root[4 * v + 1], root[4 * v + 2], root[4 * v + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 2 * WORDS; ++i)
+      if (c0 + i < C) o[i * ld_c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
+  }
+}
+
+// Columns c, c+1 of one row of a partial plane as a packed pair (+0 past C),
+// read through L2 (the plane was written by other CTAs).
+__device__ __forceinline__ uint32_t load_pair(const uint16_t* base, long long row_off, long long c, long long C) {
+  const uint16_t* p = base + row_off + c;
+  const uint32_t lo = c < C ? (uint32_t)__ldcg(p) : 0u;
+  const uint32_t hi = c + 1 < C ? (uint32_t)__ldcg(p + 1) : 0u;
+  return lo | (hi << 16);
+}
+
+// Rendezvous of the eight epilogue warps on an mbarrier (bounded).
+__device__ __forceinline__ bool epi_sync(Bars* bars, uint32_t& phase, long long limit, volatile int* abort_flag,
+                                         int* status, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars->epi);
+  const bool ok = wait_or_abort(&bars->epi, phase & 1u, limit, abort_flag, status);
+  ++phase;
+  return __all_sync(0xffffffffu, ok);
+}
 
 // Stack level m >= REG_LV lives in shared memory as [level][half][word][row].
 template <int BN>
@@ -142,6 +185,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&bars->acce[b], kEpiWarps);
     }
     mbar_init(&bars->fin, 1);
+    mbar_init(&bars->epi, kEpiWarps);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -163,7 +207,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       long long it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < tiles * a.nb && ok; u += gridDim.x) {
+        const int t = u / a.nb, kb = u % a.nb;
         const int tm = t % a.num_m, tn = t / a.num_m;
         for (int j = 0; j < a.L; ++j, ++it) {
           const int s = (int)(it % NS);
@@ -174,8 +219,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           unsigned char* st = stages + s * T::STAGE;
           mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
-          tma_load_2d(st, &tmA, j * BK, tm * BM, &bars->full[s]);
-          tma_load_2d(st + T::A_BYTES, &tmB, j * BK, tn * BN, &bars->full[s]);
+          const int x = (kb * a.L + j) * BK;
+          tma_load_2d(st, &tmA, x, tm * BM, &bars->full[s]);
+          tma_load_2d(st + T::A_BYTES, &tmB, x, tn * BN, &bars->full[s]);
         }
       }
       // Drain: the last loads issued into each stage have landed.
@@ -188,7 +234,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t idesc = idesc_bf16(BM, BN);
       long long it = 0, lc = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < tiles * a.nb && ok; u += gridDim.x) {
         for (int j = 0; j < a.L; ++j, ++it, ++lc) {
           const int b = (int)(lc % kAccBufs);
           if (!wait_or_abort(&bars->acce[b], (uint32_t)(((lc / kAccBufs) & 1) ^ 1), limit, abort_flag,
@@ -227,7 +273,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     long long lc = 0;
     bool ok = true;
     uint32_t reg_lv[T::REG_LV][T::WORDS];
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+    uint32_t epi_phase = 0;
+    for (int u = blockIdx.x; u < tiles * a.nb && ok; u += gridDim.x) {
+      const int t = u / a.nb, kb = u % a.nb;
       const int tm = t % a.num_m, tn = t / a.num_m;
       const long long r = (long long)tm * BM + row;
       for (int q = 0; q < Q; ++q) {
@@ -300,18 +348,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 else *stk_at<BN>(stk, m, half, w, row) = root[w];
               }
             }
-        } else if (r < a.R) {
-          // The tile's output: COLS columns of row r.
-          const long long c0 = (long long)tn * BN + col0;
-          uint16_t* o = a.out + r * a.ld_r + c0 * a.ld_c;
-          if (a.ld_c == 1 && c0 + T::COLS <= a.C && ((uintptr_t)o & 15u) == 0) {
+        } else if (a.nb == 1) {
+          if (r < a.R) store_cols(a.out, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
+        } else {
+          // A block root: to the partial plane, then the tile's ticket.
+          if (r < a.R)
+            store_cols(a.part, ((long long)kb * a.R + r) * a.C, (long long)tn * BN + col0, 1, a.C, root);
+          __threadfence();
+          if (!epi_sync(bars, epi_phase, limit, abort_flag, a.status, lane)) { ok = false; break; }
+          if (ew == 0 && lane == 0) bars->last = (atomicAdd(&a.cnt[t], 1u) == (unsigned)(a.nb - 1));
+          if (!epi_sync(bars, epi_phase, limit, abort_flag, a.status, lane)) { ok = false; break; }
+          if (bars->last) {
+            // The last block of this tile: the top of the tree over the nb roots.
+            __threadfence();
+            if (r < a.R) {
+              const long long c0 = (long long)tn * BN + col0;
 #pragma unroll
-            for (int v = 0; v < T::COLS / 8; ++v)
-              reinterpret_cast<uint4*>(o)[v] = make_uint4(root[4 * v], root[4 * v + 1], root[4 * v + 2], root[4 * v + 3]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < T::COLS; ++i)
-              if (c0 + i < a.C) o[i * a.ld_c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
+              for (int w = 0; w < T::WORDS; ++w) {
+                uint32_t v[16];
+                for (int b = 0; b < a.nb; ++b) v[b] = load_pair(a.part, ((long long)b * a.R + r) * a.C, c0 + 2 * w, a.C);
+                for (int width = a.nb; width > 1; width >>= 1)
+                  for (int b = 0; b < width / 2; ++b) v[b] = node2(v[2 * b], v[2 * b + 1]);
+                root[w] = v[0];
+              }
+              store_cols(a.out, r * a.ld_r, c0, a.ld_c, a.C, root);
+            }
+            if (ew == 0 && lane == 0) a.cnt[t] = 0u;
           }
         }
       }
@@ -366,8 +428,8 @@ cudaError_t launch_bng(const CUtensorMap& ta, const CUtensorMap& tb, const TcArg
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int tiles = a.num_m * a.num_n;
-  const int grid = tiles < sm_count ? tiles : sm_count;
+  const int units = a.num_m * a.num_n * a.nb;
+  const int grid = units < sm_count ? units : sm_count;
   const int smem = TcGeo<BN>::smem_for(a.E, a.nstage);
   k_tc<BN, GG><<<grid, kTcThreads, smem, st>>>(ta, tb, a);
   return cudaGetLastError();
@@ -413,28 +475,41 @@ bool tc_tree_shape(long long L, int* G, int* E) {
 
 cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
                            long long R, long long C, long long K, uint16_t* out, long long ld_r,
-                           long long ld_c, int bn, int* status, long long spin_limit,
-                           int sm_count, cudaStream_t st) {
+                           long long ld_c, int bn, const TcScratch& scratch, int* status,
+                           long long spin_limit, int sm_count, cudaStream_t st) {
   if (R <= 0 || C <= 0) return cudaSuccess;
   const long long L = (K + BK - 1) / BK;
   int G, E;
   if (K <= 0 || !tc_tree_shape(L, &G, &E)) return cudaErrorInvalidValue;
   if ((lda % 8) || (ldb % 8) || ((uintptr_t)A & 15u) || ((uintptr_t)B & 15u)) return cudaErrorInvalidValue;
   if (R > (1ll << 31) || C > (1ll << 31)) return cudaErrorInvalidValue;
-  TcArgs a;
+  TcArgs a{};
   a.R = (int)R;
   a.C = (int)C;
-  a.L = (int)L;
   a.G = G;
-  a.E = E;
   a.num_m = (int)((R + BM - 1) / BM);
   a.num_n = (int)((C + bn - 1) / bn);
+  const long long tiles = (long long)a.num_m * a.num_n;
+  // Split K into nb aligned subtrees (blocks of L/nb leaves, still G * 2^e)
+  // while there are fewer than two units per SM and scratch for them.
+  int nb = 1;
+  while (nb < 16 && 2 * nb <= (1 << E) && tiles * nb < 2ll * sm_count &&
+         scratch.part && scratch.cnt && (size_t)(2 * nb) * (size_t)R * (size_t)C <= scratch.part_elems &&
+         (size_t)tiles <= scratch.cnt_elems)
+    nb *= 2;
+  a.nb = nb;
+  int e = 0;
+  while ((1 << e) < nb) ++e;
+  a.E = E - e;
+  a.L = (int)(L / nb);
   a.out = out;
   a.ld_r = ld_r;
   a.ld_c = ld_c;
+  a.part = nb > 1 ? scratch.part : nullptr;
+  a.cnt = nb > 1 ? scratch.cnt : nullptr;
   a.status = status;
   a.spin = spin_limit;
-  a.nstage = bn == 32 ? TcGeo<32>::stages_for(E) : bn == 64 ? TcGeo<64>::stages_for(E) : TcGeo<128>::stages_for(E);
+  a.nstage = bn == 32 ? TcGeo<32>::stages_for(a.E) : bn == 64 ? TcGeo<64>::stages_for(a.E) : TcGeo<128>::stages_for(a.E);
   if (a.nstage < 2) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   if (!make_map(&ta, A, R, K, lda, BM) || !make_map(&tb, B, C, K, ldb, bn)) return cudaErrorInvalidValue;

@@ -131,13 +131,48 @@ __device__ __forceinline__ void store_cols(uint16_t* base, long long row_off, lo
   }
 }
 
-// Columns c, c+1 of one row of a partial plane as a packed pair (+0 past C),
-// read through L2 (the plane was written by other CTAs).
-__device__ __forceinline__ uint32_t load_pair(const uint16_t* base, long long row_off, long long c, long long C) {
-  const uint16_t* p = base + row_off + c;
-  const uint32_t lo = c < C ? (uint32_t)__ldcg(p) : 0u;
-  const uint32_t hi = c + 1 < C ? (uint32_t)__ldcg(p + 1) : 0u;
-  return lo | (hi << 16);
+// The top of the tree over the nb (a power of two, <= 16) block roots of one
+// row's 2*WORDS columns starting at c0: all loads of a group of 4 columns are
+// issued before any is used (8-byte vectors when the plane rows allow it).
+template <int WORDS>
+__device__ __forceinline__ void fixup_row(const uint16_t* part, long long R, long long C, int nb, long long r,
+                                          long long c0, uint32_t (&root)[WORDS]) {
+  const bool vec = (C % 4) == 0 && (((uintptr_t)part) & 7u) == 0;
+#pragma unroll
+  for (int g4 = 0; g4 < WORDS / 2; ++g4) {
+    const long long c = c0 + 4 * g4;
+    uint32_t v[16][2];
+    if (vec && c + 4 <= C) {
+#pragma unroll
+      for (int b = 0; b < 16; ++b)
+        if (b < nb) {
+          const uint2 q = __ldcg(reinterpret_cast<const uint2*>(part + ((long long)b * R + r) * C + c));
+          v[b][0] = q.x;
+          v[b][1] = q.y;
+        }
+    } else {
+#pragma unroll
+      for (int b = 0; b < 16; ++b)
+        if (b < nb) {
+          const uint16_t* p = part + ((long long)b * R + r) * C;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const uint32_t lo = c + 2 * i < C ? (uint32_t)__ldcg(p + c + 2 * i) : 0u;
+            const uint32_t hi = c + 2 * i + 1 < C ? (uint32_t)__ldcg(p + c + 2 * i + 1) : 0u;
+            v[b][i] = lo | (hi << 16);
+          }
+        }
+    }
+#pragma unroll
+    for (int width = 16; width > 1; width >>= 1)
+      if (width <= nb)
+#pragma unroll
+        for (int b = 0; b < width / 2; ++b)
+#pragma unroll
+          for (int i = 0; i < 2; ++i) v[b][i] = node2(v[2 * b][i], v[2 * b + 1][i]);
+    root[2 * g4] = v[0][0];
+    root[2 * g4 + 1] = v[0][1];
+  }
 }
 
 // Rendezvous of the eight epilogue warps on an mbarrier (bounded).
@@ -350,8 +385,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         } else if (a.nb == 1) {
           if (r < a.R) store_cols(a.out, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
-        } else {
-          // A block root: to the partial plane, then the tile's ticket.
+        } else if constexpr (BN <= 64) {
+          // A block root: to the partial plane, then the tile's ticket (split K
+          // is used only with narrow tiles, i.e. few tokens).
           if (r < a.R)
             store_cols(a.part, ((long long)kb * a.R + r) * a.C, (long long)tn * BN + col0, 1, a.C, root);
           __threadfence();
@@ -363,14 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __threadfence();
             if (r < a.R) {
               const long long c0 = (long long)tn * BN + col0;
-#pragma unroll
-              for (int w = 0; w < T::WORDS; ++w) {
-                uint32_t v[16];
-                for (int b = 0; b < a.nb; ++b) v[b] = load_pair(a.part, ((long long)b * a.R + r) * a.C, c0 + 2 * w, a.C);
-                for (int width = a.nb; width > 1; width >>= 1)
-                  for (int b = 0; b < width / 2; ++b) v[b] = node2(v[2 * b], v[2 * b + 1]);
-                root[w] = v[0];
-              }
+              fixup_row<T::WORDS>(a.part, a.R, a.C, a.nb, r, c0, root);
               store_cols(a.out, r * a.ld_r, c0, a.ld_c, a.C, root);
             }
             if (ew == 0 && lane == 0) a.cnt[t] = 0u;
@@ -493,7 +522,7 @@ cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, 
   // Split K into nb aligned subtrees (blocks of L/nb leaves, still G * 2^e)
   // while there are fewer than two units per SM and scratch for them.
   int nb = 1;
-  while (nb < 16 && 2 * nb <= (1 << E) && tiles * nb < 2ll * sm_count &&
+  while (bn <= 64 && nb < 16 && 2 * nb <= (1 << E) && tiles * nb < 2ll * sm_count &&
          scratch.part && scratch.cnt && (size_t)(2 * nb) * (size_t)R * (size_t)C <= scratch.part_elems &&
          (size_t)tiles <= scratch.cnt_elems)
     nb *= 2;

@@ -14,7 +14,8 @@
 //   warp 0      TMA producer: A and B tiles of one leaf per pipeline stage
 //               (128-byte swizzle, K-major), a ring of stages on mbarriers (as many
 //               as fit beside the shared-memory stack levels);
-//   warp 1      allocates TMEM (4 leaf buffers of BN columns) and issues the
+//   warp 1      allocates TMEM (512/BN leaf buffers of BN columns, at most 16)
+//               and issues the
 //               MMAs, one leaf per buffer, committing to the stage's "empty"
 //               barrier and the buffer's "full" barrier;
 //   warps 2-9   epilogue: each thread owns one row (TMEM lane) and BN/2
@@ -36,7 +37,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kAccBufs = 4;
+constexpr int kMaxAccBufs = 16;  // TMEM leaf buffers: 512 columns / BN (at most 16)
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 2;  // warp 0: producer, warp 1: MMA, warps 2-9: epilogue
 constexpr int kTcThreads = 32 * (kEpiWarp0 + kEpiWarps);
@@ -50,10 +51,11 @@ template <int BN> struct TcGeo {
   static constexpr int WORDS = COLS / 2;  // packed BF16 pairs per stack level per thread
   static constexpr int REG_LV = BN >= 128 ? 2 : kMaxLv;  // stack levels kept in registers
   static constexpr int LV_BYTES = BM * COLS * 2 * 2;       // one shared-memory stack level
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int BAR_BYTES = 512;
   static constexpr int MAX_SMEM = 227 * 1024;
   static constexpr int MAX_STAGES = 8;
-  static constexpr int TMEM_COLS = kAccBufs * BN;
+  static constexpr int NBUF = (512 / BN) < kMaxAccBufs ? (512 / BN) : kMaxAccBufs;
+  static constexpr int TMEM_COLS = NBUF * BN;
   // Stages that fit beside the shared-memory stack levels a tree of E levels needs.
   static __host__ __device__ int stages_for(int E) {
     const int lv = E > REG_LV ? E - REG_LV : 0;
@@ -74,8 +76,8 @@ __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0
 // on every one of the 2^32 operand pairs by detffn_selfcheck_node_add).
 __device__ __forceinline__ uint32_t node2(uint32_t a, uint32_t b) { return add_bf16x2(a, b); }
 
-struct Bars {
-  uint64_t full[8], empty[8], accf[kAccBufs], acce[kAccBufs], fin;  // up to 8 stages
+struct Bars {  // must fit in TcGeo::BAR_BYTES
+  uint64_t full[8], empty[8], accf[kMaxAccBufs], acce[kMaxAccBufs], fin;  // up to 8 stages
   uint64_t epi;  // epilogue-warps rendezvous (split-K tickets)
   uint32_t tmem_slot;
   int abort;
@@ -83,6 +85,8 @@ struct Bars {
 };
 
 // Bounded wait that also gives up when another role has aborted.
+static_assert(sizeof(Bars) <= 512, "barrier block");
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
                                               volatile int* abort_flag, int* status) {
   for (long long i = 0; i < limit; ++i) {
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    for (int b = 0; b < kAccBufs; ++b) {
+    for (int b = 0; b < T::NBUF; ++b) {
       mbar_init(&bars->accf[b], 1);
       mbar_init(&bars->acce[b], kEpiWarps);
     }
@@ -271,8 +275,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < tiles * a.nb && ok; u += gridDim.x) {
         for (int j = 0; j < a.L; ++j, ++it, ++lc) {
-          const int b = (int)(lc % kAccBufs);
-          if (!wait_or_abort(&bars->acce[b], (uint32_t)(((lc / kAccBufs) & 1) ^ 1), limit, abort_flag,
+          const int b = (int)(lc % T::NBUF);
+          if (!wait_or_abort(&bars->acce[b], (uint32_t)(((lc / T::NBUF) & 1) ^ 1), limit, abort_flag,
                              a.status)) {
             ok = false;
             break;
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const long long r = (long long)tm * BM + row;
       for (int q = 0; q < Q; ++q) {
         for (int g = 0; g < GG; ++g)
-          if (!wait_or_abort(&bars->accf[(lc + g) % kAccBufs], (uint32_t)(((lc + g) / kAccBufs) & 1),
+          if (!wait_or_abort(&bars->accf[(lc + g) % T::NBUF], (uint32_t)(((lc + g) / T::NBUF) & 1),
                              limit, abort_flag, a.status))
             ok = false;
         if (__any_sync(0xffffffffu, !ok)) {
@@ -323,8 +327,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t b0 = (uint32_t)((lc % kAccBufs) * BN), b1 = (uint32_t)(((lc + 1) % kAccBufs) * BN),
-                       b2 = (uint32_t)(((lc + 2) % kAccBufs) * BN);
+        const uint32_t b0 = (uint32_t)((lc % T::NBUF) * BN), b1 = (uint32_t)(((lc + 1) % T::NBUF) * BN),
+                       b2 = (uint32_t)(((lc + 2) % T::NBUF) * BN);
         // Phase 1: read the group's leaves from TMEM in column chunks of 16
         // and form the group roots.
         constexpr int CW = 16;
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
-          for (int g = 0; g < GG; ++g) mbar_arrive(&bars->acce[(lc + g) % kAccBufs]);
+          for (int g = 0; g < GG; ++g) mbar_arrive(&bars->acce[(lc + g) % T::NBUF]);
         lc += GG;
 
         // Phase 2: fold the roots into the stack (an elementwise binary counter).

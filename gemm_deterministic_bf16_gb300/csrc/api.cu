@@ -594,8 +594,23 @@ detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const u
                            long long M, long long H, long long I, long long s, long long w,
                            cudaStream_t st, const TcScratch& sc) {
   const Strided X{x, H, 1};
-  TRY(tree_gemm(h, f, X, Strided{Wg + s * w * H, H, 1}, M, w, H, gate + s * w, I, st, sc));
-  TRY(tree_gemm(h, f, X, Strided{Wu + s * w * H, H, 1}, M, w, H, up + s * w, I, st, sc));
+  if (f == kTensor) {
+    // gate and up in one launch (their tiles interleave over the SMs).
+    const Strided BG{Wg + s * w * H, H, 1}, BU{Wu + s * w * H, H, 1};
+    if (!tc_operands_ok(X) || !tc_operands_ok(BG) || !tc_operands_ok(BU)) return DETFFN_ERR_ALIGN;
+    const double bytes = 2.0 * (2.0 * w * H + (double)M * H + 2.0 * M * w);
+    TRY(timed(h, st, "tc_tree_gemm", bytes, 4.0 * M * w * H, [&] {
+      if (M <= 32) {  // weights on the 128-row side, tokens as the 32-wide tile
+        const TcProblem pr[2] = {{BG.p, H, x, H, gate + s * w}, {BU.p, H, x, H, up + s * w}};
+        return cu(launch_tc_gemms(pr, 2, w, M, H, 1, I, 32, sc, h->d_status, 0, h->sm_count, st));
+      }
+      const TcProblem pr[2] = {{x, H, BG.p, H, gate + s * w}, {x, H, BU.p, H, up + s * w}};
+      return cu(launch_tc_gemms(pr, 2, M, w, H, I, 1, 128, sc, h->d_status, 0, h->sm_count, st));
+    }));
+  } else {
+    TRY(tree_gemm(h, f, X, Strided{Wg + s * w * H, H, 1}, M, w, H, gate + s * w, I, st, sc));
+    TRY(tree_gemm(h, f, X, Strided{Wu + s * w * H, H, 1}, M, w, H, up + s * w, I, st, sc));
+  }
   return silu_mul(h, gate + s * w, up + s * w, hh + s * w, M, w, I, st);
 }
 

@@ -53,7 +53,7 @@ template <int BN> struct TcGeo {
   static constexpr int LV_BYTES = BM * COLS * 2 * 2;       // one shared-memory stack level
   static constexpr int BAR_BYTES = 512;
   static constexpr int MAX_SMEM = 227 * 1024;
-  static constexpr int MAX_STAGES = 8;
+  static constexpr int MAX_STAGES = 12;
   static constexpr int NBUF = (512 / BN) < kMaxAccBufs ? (512 / BN) : kMaxAccBufs;
   static constexpr int TMEM_COLS = NBUF * BN;
   // Stages that fit beside the shared-memory stack levels a tree of E levels needs.
@@ -77,7 +77,7 @@ __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0
 __device__ __forceinline__ uint32_t node2(uint32_t a, uint32_t b) { return add_bf16x2(a, b); }
 
 struct Bars {  // must fit in TcGeo::BAR_BYTES
-  uint64_t full[8], empty[8], accf[kMaxAccBufs], acce[kMaxAccBufs], fin;  // up to 8 stages
+  uint64_t full[12], empty[12], accf[kMaxAccBufs], acce[kMaxAccBufs], fin;  // up to 12 stages
   uint64_t epi;  // epilogue-warps rendezvous (split-K tickets)
   uint32_t tmem_slot;
   int abort;
@@ -110,7 +110,9 @@ struct TcArgs {
   int nb;           // K blocks per output tile (split-K by aligned subtrees); 1 = whole K
   int nstage;
   int num_m, num_n;
+  int np;           // problems in this launch (1 or 2; the second uses tmA2/tmB2 and out2)
   uint16_t* out;
+  uint16_t* out2;
   long long ld_r, ld_c;
   uint16_t* part;   // nb > 1: block roots [nb][R][C] (scratch)
   unsigned* cnt;    // nb > 1: one ticket per tile (scratch, zero on entry and on exit)
@@ -199,6 +201,7 @@ __device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int 
 template <int BN, int GG>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
          const TcArgs a) {
   using T = TcGeo<BN>;
   extern __shared__ unsigned char smem_raw[];
@@ -212,6 +215,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = a.num_m * a.num_n;
+  const int units = tiles * a.nb * a.np;  // unit u: problem u % np, then tile and K block
   const long long limit = a.spin > 0 ? a.spin : kDefaultSpin;
 
   if (threadIdx.x == 0) {
@@ -231,6 +235,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (a.np > 1) {
+      prefetch_tmap(&tmA2);
+      prefetch_tmap(&tmB2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_slot, T::TMEM_COLS);
@@ -246,9 +254,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       long long it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < tiles * a.nb && ok; u += gridDim.x) {
-        const int t = u / a.nb, kb = u % a.nb;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int pb = u % a.np, v = u / a.np;
+        const int t = v / a.nb, kb = v % a.nb;
         const int tm = t % a.num_m, tn = t / a.num_m;
+        const CUtensorMap* mA = pb ? &tmA2 : &tmA;
+        const CUtensorMap* mB = pb ? &tmB2 : &tmB;
         for (int j = 0; j < a.L; ++j, ++it) {
           const int s = (int)(it % NS);
           if (!wait_or_abort(&bars->empty[s], (uint32_t)(((it / NS) & 1) ^ 1), limit, abort_flag,
@@ -259,8 +270,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           unsigned char* st = stages + s * T::STAGE;
           mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
           const int x = (kb * a.L + j) * BK;
-          tma_load_2d(st, &tmA, x, tm * BM, &bars->full[s]);
-          tma_load_2d(st + T::A_BYTES, &tmB, x, tn * BN, &bars->full[s]);
+          tma_load_2d(st, mA, x, tm * BM, &bars->full[s]);
+          tma_load_2d(st + T::A_BYTES, mB, x, tn * BN, &bars->full[s]);
         }
       }
       // Drain: the last loads issued into each stage have landed.
@@ -273,7 +284,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t idesc = idesc_bf16(BM, BN);
       long long it = 0, lc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < tiles * a.nb && ok; u += gridDim.x) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         for (int j = 0; j < a.L; ++j, ++it, ++lc) {
           const int b = (int)(lc % T::NBUF);
           if (!wait_or_abort(&bars->acce[b], (uint32_t)(((lc / T::NBUF) & 1) ^ 1), limit, abort_flag,
@@ -313,9 +324,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
     uint32_t reg_lv[T::REG_LV][T::WORDS];
     uint32_t epi_phase = 0;
-    for (int u = blockIdx.x; u < tiles * a.nb && ok; u += gridDim.x) {
-      const int t = u / a.nb, kb = u % a.nb;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int pb = u % a.np, v = u / a.np;
+      const int t = v / a.nb, kb = v % a.nb;
       const int tm = t % a.num_m, tn = t / a.num_m;
+      uint16_t* const outp = pb ? a.out2 : a.out;
+      uint16_t* const partp = a.part ? a.part + (size_t)pb * a.nb * a.R * a.C : nullptr;
+      unsigned* const cntp = a.cnt ? a.cnt + (size_t)pb * tiles : nullptr;
       const long long r = (long long)tm * BM + row;
       for (int q = 0; q < Q; ++q) {
         for (int g = 0; g < GG; ++g)
@@ -388,25 +403,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
             }
         } else if (a.nb == 1) {
-          if (r < a.R) store_cols(a.out, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
+          if (r < a.R) store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
         } else if constexpr (BN <= 64) {
           // A block root: to the partial plane, then the tile's ticket (split K
           // is used only with narrow tiles, i.e. few tokens).
           if (r < a.R)
-            store_cols(a.part, ((long long)kb * a.R + r) * a.C, (long long)tn * BN + col0, 1, a.C, root);
+            store_cols(partp, ((long long)kb * a.R + r) * a.C, (long long)tn * BN + col0, 1, a.C, root);
           __threadfence();
           if (!epi_sync(bars, epi_phase, limit, abort_flag, a.status, lane)) { ok = false; break; }
-          if (ew == 0 && lane == 0) bars->last = (atomicAdd(&a.cnt[t], 1u) == (unsigned)(a.nb - 1));
+          if (ew == 0 && lane == 0) bars->last = (atomicAdd(&cntp[t], 1u) == (unsigned)(a.nb - 1));
           if (!epi_sync(bars, epi_phase, limit, abort_flag, a.status, lane)) { ok = false; break; }
           if (bars->last) {
             // The last block of this tile: the top of the tree over the nb roots.
             __threadfence();
             if (r < a.R) {
               const long long c0 = (long long)tn * BN + col0;
-              fixup_row<T::WORDS>(a.part, a.R, a.C, a.nb, r, c0, root);
-              store_cols(a.out, r * a.ld_r, c0, a.ld_c, a.C, root);
+              fixup_row<T::WORDS>(partp, a.R, a.C, a.nb, r, c0, root);
+              store_cols(outp, r * a.ld_r, c0, a.ld_c, a.C, root);
             }
-            if (ew == 0 && lane == 0) a.cnt[t] = 0u;
+            if (ew == 0 && lane == 0) cntp[t] = 0u;
           }
         }
       }
@@ -452,8 +467,7 @@ bool make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long K,
 }
 
 template <int BN, int GG>
-cudaError_t launch_bng(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int sm_count,
-                       cudaStream_t st) {
+cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     const cudaError_t e =
@@ -461,20 +475,19 @@ cudaError_t launch_bng(const CUtensorMap& ta, const CUtensorMap& tb, const TcArg
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int units = a.num_m * a.num_n * a.nb;
+  const int units = a.num_m * a.num_n * a.nb * a.np;
   const int grid = units < sm_count ? units : sm_count;
   const int smem = TcGeo<BN>::smem_for(a.E, a.nstage);
-  k_tc<BN, GG><<<grid, kTcThreads, smem, st>>>(ta, tb, a);
+  k_tc<BN, GG><<<grid, kTcThreads, smem, st>>>(m[0], m[1], m[2], m[3], a);
   return cudaGetLastError();
 }
 
 template <int BN>
-cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a, int sm_count,
-                      cudaStream_t st) {
+cudaError_t launch_bn(const CUtensorMap* m, const TcArgs& a, int sm_count, cudaStream_t st) {
   switch (a.G) {
-    case 1: return launch_bng<BN, 1>(ta, tb, a, sm_count, st);
-    case 2: return launch_bng<BN, 2>(ta, tb, a, sm_count, st);
-    case 3: return launch_bng<BN, 3>(ta, tb, a, sm_count, st);
+    case 1: return launch_bng<BN, 1>(m, a, sm_count, st);
+    case 2: return launch_bng<BN, 2>(m, a, sm_count, st);
+    case 3: return launch_bng<BN, 3>(m, a, sm_count, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -506,36 +519,40 @@ bool tc_tree_shape(long long L, int* G, int* E) {
   return true;
 }
 
-cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
-                           long long R, long long C, long long K, uint16_t* out, long long ld_r,
-                           long long ld_c, int bn, const TcScratch& scratch, int* status,
-                           long long spin_limit, int sm_count, cudaStream_t st) {
+cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long C, long long K,
+                            long long ld_r, long long ld_c, int bn, const TcScratch& scratch, int* status,
+                            long long spin_limit, int sm_count, cudaStream_t st) {
   if (R <= 0 || C <= 0) return cudaSuccess;
+  if (np < 1 || np > 2) return cudaErrorInvalidValue;
   const long long L = (K + BK - 1) / BK;
   int G, E;
   if (K <= 0 || !tc_tree_shape(L, &G, &E)) return cudaErrorInvalidValue;
-  if ((lda % 8) || (ldb % 8) || ((uintptr_t)A & 15u) || ((uintptr_t)B & 15u)) return cudaErrorInvalidValue;
+  for (int p = 0; p < np; ++p)
+    if ((pr[p].lda % 8) || (pr[p].ldb % 8) || ((uintptr_t)pr[p].A & 15u) || ((uintptr_t)pr[p].B & 15u))
+      return cudaErrorInvalidValue;
   if (R > (1ll << 31) || C > (1ll << 31)) return cudaErrorInvalidValue;
   TcArgs a{};
   a.R = (int)R;
   a.C = (int)C;
   a.G = G;
+  a.np = np;
   a.num_m = (int)((R + BM - 1) / BM);
   a.num_n = (int)((C + bn - 1) / bn);
   const long long tiles = (long long)a.num_m * a.num_n;
   // Split K into nb aligned subtrees (blocks of L/nb leaves, still G * 2^e)
   // while there are fewer than two units per SM and scratch for them.
   int nb = 1;
-  while (bn <= 64 && nb < 16 && 2 * nb <= (1 << E) && tiles * nb < 2ll * sm_count &&
-         scratch.part && scratch.cnt && (size_t)(2 * nb) * (size_t)R * (size_t)C <= scratch.part_elems &&
-         (size_t)tiles <= scratch.cnt_elems)
+  while (bn <= 64 && nb < 16 && 2 * nb <= (1 << E) && tiles * nb * np < 2ll * sm_count &&
+         scratch.part && scratch.cnt && (size_t)(2 * nb) * np * (size_t)R * (size_t)C <= scratch.part_elems &&
+         (size_t)(tiles * np) <= scratch.cnt_elems)
     nb *= 2;
   a.nb = nb;
   int e = 0;
   while ((1 << e) < nb) ++e;
   a.E = E - e;
   a.L = (int)(L / nb);
-  a.out = out;
+  a.out = pr[0].out;
+  a.out2 = np > 1 ? pr[1].out : nullptr;
   a.ld_r = ld_r;
   a.ld_c = ld_c;
   a.part = nb > 1 ? scratch.part : nullptr;
@@ -544,14 +561,26 @@ cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, 
   a.spin = spin_limit;
   a.nstage = bn == 32 ? TcGeo<32>::stages_for(a.E) : bn == 64 ? TcGeo<64>::stages_for(a.E) : TcGeo<128>::stages_for(a.E);
   if (a.nstage < 2) return cudaErrorInvalidValue;
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, A, R, K, lda, BM) || !make_map(&tb, B, C, K, ldb, bn)) return cudaErrorInvalidValue;
+  CUtensorMap m[4];
+  for (int p = 0; p < 2; ++p) {
+    const TcProblem& q = pr[p < np ? p : 0];
+    if (!make_map(&m[2 * p], q.A, R, K, q.lda, BM) || !make_map(&m[2 * p + 1], q.B, C, K, q.ldb, bn))
+      return cudaErrorInvalidValue;
+  }
   switch (bn) {
-    case 32: return launch_bn<32>(ta, tb, a, sm_count, st);
-    case 64: return launch_bn<64>(ta, tb, a, sm_count, st);
-    case 128: return launch_bn<128>(ta, tb, a, sm_count, st);
+    case 32: return launch_bn<32>(m, a, sm_count, st);
+    case 64: return launch_bn<64>(m, a, sm_count, st);
+    case 128: return launch_bn<128>(m, a, sm_count, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
+                           long long R, long long C, long long K, uint16_t* out, long long ld_r,
+                           long long ld_c, int bn, const TcScratch& scratch, int* status,
+                           long long spin_limit, int sm_count, cudaStream_t st) {
+  const TcProblem p{A, lda, B, ldb, out};
+  return launch_tc_gemms(&p, 1, R, C, K, ld_r, ld_c, bn, scratch, status, spin_limit, sm_count, st);
 }
 
 }  // namespace detffn

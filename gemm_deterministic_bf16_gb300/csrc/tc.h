@@ -19,6 +19,21 @@ struct TcScratch {
   size_t cnt_elems = 0;
 };
 
+// One contraction of a (possibly two-problem) launch.
+struct TcProblem {
+  const uint16_t* A;
+  long long lda;
+  const uint16_t* B;
+  long long ldb;
+  uint16_t* out;
+};
+
+// Up to two same-shaped contractions in one launch (their units interleave);
+// scratch must hold both problems' block-root planes and tickets.
+cudaError_t launch_tc_gemms(const TcProblem* problems, int np, long long R, long long C, long long K,
+                            long long ld_r, long long ld_c, int bn, const TcScratch& scratch, int* status,
+                            long long spin_limit, int sm_count, cudaStream_t st);
+
 // out[r*ld_r + c*ld_c] = T_K(A[r, :], B[c, :]) for r < R, c < C; A and B are
 // K-contiguous BF16 with row strides lda, ldb (elements, multiples of 8) and
 // 16-byte-aligned bases.  bn in {32, 64, 128} is the tile width over C.

@@ -38,23 +38,29 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kMaxAccBufs = 16;  // TMEM leaf buffers: 512 columns / BN (at most 16)
-constexpr int kEpiWarps = 8;
-constexpr int kEpiWarp0 = 2;  // warp 0: producer, warp 1: MMA, warps 2-9: epilogue
-constexpr int kTcThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kEpiWarp0 = 2;  // warp 0: producer, warp 1: MMA, warps 2..: epilogue
 constexpr int kMaxLv = 6;  // up to Q = 64 bottom groups
 
+// Wide tiles (BN = 128, many tokens): one CTA per SM, 8 epilogue warps (two
+// per TMEM lane quarter, BN/2 columns each), 4 leaf buffers.  Narrow tiles
+// (few tokens): two CTAs per SM, 4 epilogue warps (BN columns each), 256/BN
+// leaf buffers and half the shared memory each, so two pipelines overlap.
 template <int BN> struct TcGeo {
+  static constexpr int MINB = BN >= 128 ? 1 : 2;          // resident CTAs per SM
+  static constexpr int EPI_WARPS = BN >= 128 ? 8 : 4;
+  static constexpr int HALVES = EPI_WARPS / 4;            // epilogue warps per lane quarter
+  static constexpr int THREADS = 32 * (kEpiWarp0 + EPI_WARPS);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int COLS = BN / 2;    // columns per epilogue thread
-  static constexpr int WORDS = COLS / 2;  // packed BF16 pairs per stack level per thread
-  static constexpr int REG_LV = BN >= 128 ? 2 : kMaxLv;  // stack levels kept in registers
-  static constexpr int LV_BYTES = BM * COLS * 2 * 2;       // one shared-memory stack level
+  static constexpr int COLS = BN / HALVES;  // columns per epilogue thread
+  static constexpr int WORDS = COLS / 2;    // packed BF16 pairs per stack level per thread
+  static constexpr int REG_LV = BN >= 128 ? 2 : 3;  // stack levels kept in registers
+  static constexpr int LV_BYTES = BM * BN * 2;            // one shared-memory stack level
   static constexpr int BAR_BYTES = 512;
-  static constexpr int MAX_SMEM = 227 * 1024;
+  static constexpr int MAX_SMEM = BN >= 128 ? 227 * 1024 : 113 * 1024;
   static constexpr int MAX_STAGES = 12;
-  static constexpr int NBUF = (512 / BN) < kMaxAccBufs ? (512 / BN) : kMaxAccBufs;
+  static constexpr int NBUF = (512 / (BN * MINB)) < kMaxAccBufs ? (512 / (BN * MINB)) : kMaxAccBufs;
   static constexpr int TMEM_COLS = NBUF * BN;
   // Stages that fit beside the shared-memory stack levels a tree of E levels needs.
   static __host__ __device__ int stages_for(int E) {
@@ -181,7 +187,7 @@ __device__ __forceinline__ void fixup_row(const uint16_t* part, long long R, lon
   }
 }
 
-// Rendezvous of the eight epilogue warps on an mbarrier (bounded).
+// Rendezvous of the epilogue warps on an mbarrier (bounded).
 __device__ __forceinline__ bool epi_sync(Bars* bars, uint32_t& phase, long long limit, volatile int* abort_flag,
                                          int* status, int lane) {
   __syncwarp();
@@ -195,11 +201,11 @@ __device__ __forceinline__ bool epi_sync(Bars* bars, uint32_t& phase, long long 
 template <int BN>
 __device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int w, int row) {
   using T = TcGeo<BN>;
-  return stk + (((m - T::REG_LV) * 2 + half) * T::WORDS + w) * BM + row;
+  return stk + (((m - T::REG_LV) * T::HALVES + half) * T::WORDS + w) * BM + row;
 }
 
 template <int BN, int GG>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcGeo<BN>::THREADS, TcGeo<BN>::MINB)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
          const TcArgs a) {
@@ -225,10 +231,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < T::NBUF; ++b) {
       mbar_init(&bars->accf[b], 1);
-      mbar_init(&bars->acce[b], kEpiWarps);
+      mbar_init(&bars->acce[b], T::EPI_WARPS);
     }
     mbar_init(&bars->fin, 1);
-    mbar_init(&bars->epi, kEpiWarps);
+    mbar_init(&bars->epi, T::EPI_WARPS);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -476,9 +482,10 @@ cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cuda
     attr = true;
   }
   const int units = a.num_m * a.num_n * a.nb * a.np;
-  const int grid = units < sm_count ? units : sm_count;
+  const int slots = sm_count * TcGeo<BN>::MINB;
+  const int grid = units < slots ? units : slots;
   const int smem = TcGeo<BN>::smem_for(a.E, a.nstage);
-  k_tc<BN, GG><<<grid, kTcThreads, smem, st>>>(m[0], m[1], m[2], m[3], a);
+  k_tc<BN, GG><<<grid, TcGeo<BN>::THREADS, smem, st>>>(m[0], m[1], m[2], m[3], a);
   return cudaGetLastError();
 }
 
@@ -542,7 +549,7 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   // Split K into nb aligned subtrees (blocks of L/nb leaves, still G * 2^e)
   // while there are fewer than two units per SM and scratch for them.
   int nb = 1;
-  while (bn <= 64 && nb < 16 && 2 * nb <= (1 << E) && tiles * nb * np < 2ll * sm_count &&
+  while (bn <= 64 && nb < 16 && 2 * nb <= (1 << E) && tiles * nb * np < 4ll * sm_count &&
          scratch.part && scratch.cnt && (size_t)(2 * nb) * np * (size_t)R * (size_t)C <= scratch.part_elems &&
          (size_t)(tiles * np) <= scratch.cnt_elems)
     nb *= 2;

@@ -177,11 +177,13 @@ detffn_status read_opts(const detffn_options* o, Opts* out) {
 
 // The kernel family a call uses.  EXACT: CUDA-core kernels with LANE8x8
 // leaves (bit-identical to the oracle).  TENSOR: tcgen05 leaves.  AUTO takes
-// TENSOR for M > 32 tokens when the tensor kernel covers every contraction
+// TENSOR for M > 8 tokens when the tensor kernel covers every contraction
 // length of the call (H, I, I/k and M leaves of the form 1, 2^d or 3*2^d, and
-// H, I multiples of 8), else EXACT.  It never depends on the shard count or
-// the chunking: a shard of I has the same leaf-count form as I.
+// H, I multiples of 8), else EXACT (M <= 8 stays on the exact weight-streaming
+// kernels, which run near HBM speed there).  It never depends on the shard
+// count or the chunking: a shard of I has the same leaf-count form as I.
 enum Family { kExact = 0, kTensor = 1 };
+constexpr long long kAutoExactMaxM = 8;
 
 bool tc_len_ok(long long K) {
   int G, E;
@@ -201,7 +203,7 @@ detffn_status pick_family(const Opts& o, long long M, long long H, long long I, 
     if (!tc_covers(M, H, I, backward)) return DETFFN_ERR_UNSUPPORTED;
     *f = kTensor;
   } else {
-    *f = (M > 32 && tc_covers(M, H, I, backward)) ? kTensor : kExact;
+    *f = (M > kAutoExactMaxM && tc_covers(M, H, I, backward)) ? kTensor : kExact;
   }
   return DETFFN_OK;
 }
@@ -942,7 +944,7 @@ extern "C" detffn_status detffn_tree_gemm(detffn_handle h, const void* A, long l
   if (R == 0 || C == 0) return DETFFN_OK;
   Family f = kExact;
   const Strided SA{(const uint16_t*)A, a_rs, a_ks}, SB{(const uint16_t*)B, b_rs, b_ks};
-  if (o.path == DETFFN_PATH_TENSOR || (o.path == DETFFN_PATH_AUTO && R > 32)) {
+  if (o.path == DETFFN_PATH_TENSOR || (o.path == DETFFN_PATH_AUTO && R > kAutoExactMaxM)) {
     const bool ok = tc_len_ok(K) && tc_operands_ok(SA) && tc_operands_ok(SB);
     if (ok) f = kTensor;
     else if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_UNSUPPORTED;

@@ -36,6 +36,8 @@ KERNEL_SOURCES = {
     "decode_gateup": "k_decode.cu",
     "decode_down": "k_decode.cu",
     "tc_tree_gemm": "k_tc.cu",
+    "tcs_gateup": "k_tcs.cu",
+    "tcs_tree_gemm": "k_tcs.cu",
 }
 
 

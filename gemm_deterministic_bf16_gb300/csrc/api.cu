@@ -221,11 +221,42 @@ struct Arena {
   }
 };
 
-struct FwdWs { uint16_t *gate, *up, *h, *parts, *dec_part, *tc_part; unsigned *dec_cnt, *tc_cnt; };
+// Piece slots of the few-token tensor contractions (R <= 32 tokens).
+struct TcsScratch {
+  void* p = nullptr;
+  size_t bytes = 0;
+};
+constexpr int kSizingSms = 152;  // SM count a workspace is sized for when no handle is given
+
+// Piece-slot bytes of a few-token contraction over C weight rows and K, two CTAs per SM.
+size_t tcs_bytes(long long C, long long K, int np, int sms) {
+  TcsPlan p;
+  return tcs_plan(1, C, K, np, 2 * sms, false, &p) ? p.scratch : 0;
+}
+
+// The plan for the scratch at hand: two CTAs per SM when the slots fit, fewer
+// CTAs when they do not, whole tiles per CTA (no slots) as the last resort.
+// The results are the same for every plan.
+bool tcs_plan_fit(long long R, long long C, long long K, int np, int sms, const TcsScratch& sc, TcsPlan* p) {
+  if (sc.p) {
+    for (int ctas = 2 * sms; ctas >= 1; ctas = ctas * 3 / 4) {
+      if (!tcs_plan(R, C, K, np, ctas, false, p)) return false;
+      if (p->scratch <= sc.bytes) return true;
+      if (ctas == 1) break;
+    }
+  }
+  return tcs_plan(R, C, K, np, 2 * sms, true, p);
+}
+
+struct FwdWs {
+  uint16_t *gate, *up, *h, *parts, *dec_part;
+  unsigned* dec_cnt;
+  TcsScratch tcs;
+};
 // Decode scratch: block-root planes (at most 8 blocks x 8 tokens x rows) and
 // one ticket per row tile (at most one tile per row).
 constexpr long long kDecPlanes = 64;
-FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k) {
+FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k, int sms) {
   FwdWs w;
   w.gate = a.take<uint16_t>(M * I);
   w.up = a.take<uint16_t>(M * I);
@@ -234,18 +265,22 @@ FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k) {
   const long long rows = 2 * I > H ? 2 * I : H;
   w.dec_part = M <= 32 ? a.take<uint16_t>(kDecPlanes * rows) : nullptr;
   w.dec_cnt = M <= 32 ? a.take<unsigned>(rows + 1) : nullptr;
-  // Tensor family with few tokens: up to 16 K blocks x 32 tokens x weight rows.
-  const long long wrows = I > H ? I : H;
-  w.tc_part = M <= 32 ? a.take<uint16_t>(16 * 32 * wrows) : nullptr;
-  w.tc_cnt = M <= 32 ? a.take<unsigned>(wrows / 128 + 2) : nullptr;
+  // Tensor family with few tokens: piece slots for gate/up and for down.
+  if (M >= 1 && M <= 32) {
+    const long long sw = I / k;
+    const size_t gu = tcs_bytes(sw, H, 2, sms), dn = tcs_bytes(H, sw, 1, sms);
+    w.tcs.bytes = gu > dn ? gu : dn;
+    w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
+  }
   return w;
 }
 
 struct BwdWs {
   uint16_t *dh, *dU, *dG, *h, *cg, *cu, *cgs, *cus;
   uint16_t *WdT, *WgT, *WuT, *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only
+  TcsScratch tcs;                                          // tensor family, M <= 32
 };
-BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool tensor) {
+BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool tensor, int sms) {
   BwdWs w{};
   w.dh = a.take<uint16_t>(M * I);
   w.dU = a.take<uint16_t>(M * I);
@@ -264,6 +299,11 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool
     w.hT = a.take<uint16_t>(I * M);
     w.dGT = a.take<uint16_t>(I * M);
     w.dUT = a.take<uint16_t>(I * M);
+    if (M >= 1 && M <= 32) {  // dh over K = H; cg, cu over K = I / k
+      const size_t d1 = tcs_bytes(I, H, 1, sms), d2 = tcs_bytes(H, I / k, 1, sms);
+      w.tcs.bytes = d1 > d2 ? d1 : d2;
+      w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
+    }
   }
   return w;
 }
@@ -271,8 +311,9 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool
 struct ChunkWs {
   uint16_t *x, *dO, *g, *u, *dh, *dU, *dG, *h;
   uint16_t *WdT, *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only
+  TcsScratch tcs;                              // tensor family: dh of chunks of <= 32 tokens
 };
-ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tensor) {
+ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tensor, int sms) {
   ChunkWs w{};
   w.x = a.take<uint16_t>(M * H);
   w.dO = a.take<uint16_t>(M * H);
@@ -289,17 +330,19 @@ ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tenso
     w.hT = a.take<uint16_t>(I * M);
     w.dGT = a.take<uint16_t>(I * M);
     w.dUT = a.take<uint16_t>(I * M);
+    w.tcs.bytes = tcs_bytes(I, H, 1, sms);
+    w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
   }
   return w;
 }
 
-size_t ws_bytes_for(int op, long long M, long long H, long long I, int k, bool tensor) {
+size_t ws_bytes_for(int op, long long M, long long H, long long I, int k, bool tensor, int sms) {
   Arena a(nullptr);
   switch (op) {
-    case DETFFN_OP_FORWARD: plan_forward(a, M, H, I, 1); break;
-    case DETFFN_OP_FORWARD_SHARDED: plan_forward(a, M, H, I, k); break;
-    case DETFFN_OP_BACKWARD: plan_backward(a, M, H, I, k, tensor); break;
-    case DETFFN_OP_WGRAD_CHUNKED: plan_chunked(a, M, H, I, tensor); break;
+    case DETFFN_OP_FORWARD: plan_forward(a, M, H, I, 1, sms); break;
+    case DETFFN_OP_FORWARD_SHARDED: plan_forward(a, M, H, I, k, sms); break;
+    case DETFFN_OP_BACKWARD: plan_backward(a, M, H, I, k, tensor, sms); break;
+    case DETFFN_OP_WGRAD_CHUNKED: plan_chunked(a, M, H, I, tensor, sms); break;
     default: return 0;
   }
   return (a.off + 255) & ~(size_t)255;
@@ -364,15 +407,19 @@ bool tc_operands_ok(const Strided& X) {
 
 detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long long R, long long C,
                         long long K, uint16_t* out, long long o_rs, cudaStream_t st,
-                        const TcScratch& scratch = TcScratch()) {
+                        const TcsScratch& sc = TcsScratch()) {
   const double bytes = 2.0 * ((double)R * K + (double)C * K + (double)R * C);
   if (f == kTensor) {
     if (!tc_operands_ok(A) || !tc_operands_ok(B)) return DETFFN_ERR_ALIGN;
+    if (R <= 32) {  // few tokens: the weights (B) streamed on the MMA's 128-row side
+      TcsPlan p;
+      if (!tcs_plan_fit(R, C, K, 1, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
+      const TcsProblem pr{B.p, B.rs, A.p, A.rs, out};
+      return timed(h, st, "tcs_tree_gemm", bytes, 2.0 * R * C * K,
+                   [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->d_status, 0, st)); });
+    }
     return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
-      if (R <= 32)
-        return cu(launch_tc_gemm(B.p, B.rs, A.p, A.rs, C, R, K, out, 1, o_rs, 32, scratch, h->d_status, 0,
-                                 h->sm_count, st));
-      return cu(launch_tc_gemm(A.p, A.rs, B.p, B.rs, R, C, K, out, o_rs, 1, 128, scratch, h->d_status, 0,
+      return cu(launch_tc_gemm(A.p, A.rs, B.p, B.rs, R, C, K, out, o_rs, 1, 128, TcScratch(), h->d_status, 0,
                                h->sm_count, st));
     });
   }
@@ -539,7 +586,6 @@ detffn_status detffn_destroy(detffn_handle h) {
 
 detffn_status detffn_workspace_size(detffn_handle h, int op, long long M, long long H, long long I,
                                     int k, const detffn_options* opts, size_t* bytes) {
-  (void)h;
   if (!bytes) return DETFFN_ERR_INVALID_ARG;
   Opts o;
   TRY(read_opts(opts, &o));
@@ -550,7 +596,7 @@ detffn_status detffn_workspace_size(detffn_handle h, int op, long long M, long l
   Family f;
   const bool bwd = op == DETFFN_OP_BACKWARD || op == DETFFN_OP_WGRAD_CHUNKED;
   TRY(pick_family(o, M, H, I, bwd, &f));
-  *bytes = ws_bytes_for(op, M, H, I, k, f == kTensor);
+  *bytes = ws_bytes_for(op, M, H, I, k, f == kTensor, h ? h->sm_count : kSizingSms);
   return DETFFN_OK;
 }
 
@@ -592,26 +638,34 @@ detffn_status check_ffn_ptrs(const void* x, const void* Wg, const void* Wu, cons
 // Forward of one shard (or of everything when w == I, s == 0): gate/up for
 // rows [s*w, (s+1)*w) of Wg/Wu, then h on the same columns.
 detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const uint16_t* Wg,
-                           const uint16_t* Wu, uint16_t* gate, uint16_t* up, uint16_t* hh,
+                           const uint16_t* Wu, uint16_t* gate, uint16_t* up, bool keep, uint16_t* hh,
                            long long M, long long H, long long I, long long s, long long w,
-                           cudaStream_t st, const TcScratch& sc) {
+                           cudaStream_t st, const TcsScratch& sc) {
   const Strided X{x, H, 1};
   if (f == kTensor) {
     // gate and up in one launch (their tiles interleave over the SMs).
     const Strided BG{Wg + s * w * H, H, 1}, BU{Wu + s * w * H, H, 1};
     if (!tc_operands_ok(X) || !tc_operands_ok(BG) || !tc_operands_ok(BU)) return DETFFN_ERR_ALIGN;
+    if (M <= 32) {
+      // Few tokens: the top of both trees fused with SiLU * up; gate and up
+      // are stored only when the caller keeps them.
+      TcsPlan p;
+      if (!tcs_plan_fit(M, w, H, 2, h->sm_count, sc, &p) || p.direct) return DETFFN_ERR_WORKSPACE;
+      const double bytes = 2.0 * (2.0 * w * H + (double)M * H + (keep ? 3.0 : 1.0) * M * w);
+      const TcsProblem pr[2] = {{BG.p, H, x, H, keep ? gate + s * w : nullptr},
+                                {BU.p, H, x, H, keep ? up + s * w : nullptr}};
+      return timed(h, st, "tcs_gateup", bytes, 4.0 * M * w * H, [&] {
+        return cu(launch_tcs_gateup(p, pr, hh + s * w, I, h->d_silu, sc.p, sc.bytes, h->d_status, 0, st));
+      });
+    }
     const double bytes = 2.0 * (2.0 * w * H + (double)M * H + 2.0 * M * w);
     TRY(timed(h, st, "tc_tree_gemm", bytes, 4.0 * M * w * H, [&] {
-      if (M <= 32) {  // weights on the 128-row side, tokens as the 32-wide tile
-        const TcProblem pr[2] = {{BG.p, H, x, H, gate + s * w}, {BU.p, H, x, H, up + s * w}};
-        return cu(launch_tc_gemms(pr, 2, w, M, H, 1, I, 32, sc, h->d_status, 0, h->sm_count, st));
-      }
       const TcProblem pr[2] = {{x, H, BG.p, H, gate + s * w}, {x, H, BU.p, H, up + s * w}};
-      return cu(launch_tc_gemms(pr, 2, M, w, H, I, 1, 128, sc, h->d_status, 0, h->sm_count, st));
+      return cu(launch_tc_gemms(pr, 2, M, w, H, I, 1, 128, TcScratch(), h->d_status, 0, h->sm_count, st));
     }));
   } else {
-    TRY(tree_gemm(h, f, X, Strided{Wg + s * w * H, H, 1}, M, w, H, gate + s * w, I, st, sc));
-    TRY(tree_gemm(h, f, X, Strided{Wu + s * w * H, H, 1}, M, w, H, up + s * w, I, st, sc));
+    TRY(tree_gemm(h, f, X, Strided{Wg + s * w * H, H, 1}, M, w, H, gate + s * w, I, st));
+    TRY(tree_gemm(h, f, X, Strided{Wu + s * w * H, H, 1}, M, w, H, up + s * w, I, st));
   }
   return silu_mul(h, gate + s * w, up + s * w, hh + s * w, M, w, I, st);
 }
@@ -646,12 +700,13 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
     if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_ALIGN;
     f = kExact;
   }
-  TRY(check_ws(ws, ws_bytes, ws_bytes_for(k > 1 ? DETFFN_OP_FORWARD_SHARDED : DETFFN_OP_FORWARD, M, H, I, k, false)));
+  TRY(check_ws(ws, ws_bytes,
+               ws_bytes_for(k > 1 ? DETFFN_OP_FORWARD_SHARDED : DETFFN_OP_FORWARD, M, H, I, k, false, h->sm_count)));
   if (M == 0) return DETFFN_OK;
   TRYCU(cudaSetDevice(h->device));
   cudaStream_t st = (cudaStream_t)stream;
   Arena a(ws);
-  FwdWs w = plan_forward(a, M, H, I, k);
+  FwdWs w = plan_forward(a, M, H, I, k, h->sm_count);
   uint16_t* gate = gate_save ? (uint16_t*)gate_save : w.gate;
   uint16_t* up = up_save ? (uint16_t*)up_save : w.up;
   const uint16_t* X = (const uint16_t*)x;
@@ -663,15 +718,7 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
                    decode_covers(M, H, sw, {x, Wg, Wu, Wd, w.h, (const void*)(w.h + sw)});
   const bool saves = gate_save != nullptr;
   if (dec) TRYCU(cudaMemsetAsync(w.dec_cnt, 0, sizeof(unsigned) * (size_t)((2 * I > H ? 2 * I : H) + 1), st));
-  TcScratch sc;
-  if (f == kTensor && w.tc_part) {
-    const long long wrows = I > H ? I : H;
-    sc.part = w.tc_part;
-    sc.part_elems = (size_t)(16 * 32 * wrows);
-    sc.cnt = w.tc_cnt;
-    sc.cnt_elems = (size_t)(wrows / 128 + 2);
-    TRYCU(cudaMemsetAsync(sc.cnt, 0, sizeof(unsigned) * sc.cnt_elems, st));
-  }
+  const TcsScratch& sc = w.tcs;
   for (long long s = 0; s < k; ++s) {
     uint16_t* dst = k == 1 ? (uint16_t*)out : w.parts + s * M * H;
     if (dec) {
@@ -680,7 +727,7 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
                         w.dec_part, w.dec_cnt, st));
       TRY(decode_plain(h, w.h + s * sw, I, WD + s * sw, I, H, sw, M, dst, H, w.dec_part, w.dec_cnt, st));
     } else {
-      TRY(gateup_slice(h, f, X, WG, WU, gate, up, w.h, M, H, I, s, sw, st, sc));
+      TRY(gateup_slice(h, f, X, WG, WU, gate, up, saves, w.h, M, H, I, s, sw, st, sc));
       TRY(tree_gemm(h, f, Strided{w.h + s * sw, I, 1}, Strided{WD + s * sw, I, 1}, M, H, sw, dst, H, st, sc));
     }
   }
@@ -715,11 +762,11 @@ namespace {
 detffn_status rowwise_bwd(detffn_handle h, Family f, const uint16_t* dOut, const uint16_t* Wd,
                           const uint16_t* WdT, const uint16_t* gate, const uint16_t* up,
                           uint16_t* dh, uint16_t* dU, uint16_t* dG, long long rows, long long H,
-                          long long I, cudaStream_t st) {
+                          long long I, cudaStream_t st, const TcsScratch& sc) {
   // dh[m, i] = T_{n<H}(dOut[m, n], Wd[n, i]): B row i is column i of Wd (K stride I),
   // or row i of the transposed copy WdT [I, H] for the tensor family.
   const Strided B = f == kTensor ? Strided{WdT, H, 1} : Strided{Wd, 1, I};
-  TRY(tree_gemm(h, f, Strided{dOut, H, 1}, B, rows, I, H, dh, I, st));
+  TRY(tree_gemm(h, f, Strided{dOut, H, 1}, B, rows, I, H, dh, I, st, sc));
   return silu_bwd(h, dh, gate, up, dU, dG, rows * I, st);
 }
 
@@ -789,7 +836,7 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
       f = kExact;
     }
   }
-  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_BACKWARD, M, H, I, k, f == kTensor)));
+  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_BACKWARD, M, H, I, k, f == kTensor, h->sm_count)));
   if (M == 0) {
     // No tokens: the weight gradients are empty sums (+0); nothing else exists.
     TRYCU(cudaSetDevice(h->device));
@@ -801,7 +848,7 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   TRYCU(cudaSetDevice(h->device));
   cudaStream_t st = (cudaStream_t)stream;
   Arena a(ws);
-  BwdWs w = plan_backward(a, M, H, I, k, f == kTensor);
+  BwdWs w = plan_backward(a, M, H, I, k, f == kTensor, h->sm_count);
   uint16_t* dh = dh_save ? (uint16_t*)dh_save : w.dh;
   uint16_t* dU = dU_save ? (uint16_t*)dU_save : w.dU;
   uint16_t* dG = dG_save ? (uint16_t*)dG_save : w.dG;
@@ -814,7 +861,8 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
     TRY(transpose(h, WG, I, H, H, w.WgT, st));
     TRY(transpose(h, WU, I, H, H, w.WuT, st));
   }
-  TRY(rowwise_bwd(h, f, (const uint16_t*)dOut, (const uint16_t*)Wd, w.WdT, G, U, dh, dU, dG, M, H, I, st));
+  TRY(rowwise_bwd(h, f, (const uint16_t*)dOut, (const uint16_t*)Wd, w.WdT, G, U, dh, dU, dG, M, H, I, st,
+                  w.tcs));
   // dHidden: cg = T_i(dG[m, i], Wg[i, n]), cu = T_i(dU[m, i], Wu[i, n]); the two
   // trees stay separate until the final gate-then-up addition.  B row n is
   // column n of Wg (K stride H), or row n of WgT [H, I] for the tensor family.
@@ -825,8 +873,8 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   for (long long s = 0; s < k; ++s) {
     uint16_t* cg = k == 1 ? w.cg : w.cgs + s * M * H;
     uint16_t* cu = k == 1 ? w.cu : w.cus + s * M * H;
-    TRY(tree_gemm(h, f, Strided{dG + s * sw, I, 1}, wcol(WG, w.WgT, s * sw), M, H, sw, cg, H, st));
-    TRY(tree_gemm(h, f, Strided{dU + s * sw, I, 1}, wcol(WU, w.WuT, s * sw), M, H, sw, cu, H, st));
+    TRY(tree_gemm(h, f, Strided{dG + s * sw, I, 1}, wcol(WG, w.WgT, s * sw), M, H, sw, cg, H, st, w.tcs));
+    TRY(tree_gemm(h, f, Strided{dU + s * sw, I, 1}, wcol(WU, w.WuT, s * sw), M, H, sw, cu, H, st, w.tcs));
   }
   if (k > 1) {
     const void *pg[8], *pu[8];
@@ -879,7 +927,7 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
     if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_ALIGN;
     f = kExact;
   }
-  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_WGRAD_CHUNKED, M, H, I, 1, f == kTensor)));
+  TRY(check_ws(ws, ws_bytes, ws_bytes_for(DETFFN_OP_WGRAD_CHUNKED, M, H, I, 1, f == kTensor, h->sm_count)));
   TRYCU(cudaSetDevice(h->device));
   cudaStream_t st = (cudaStream_t)stream;
   if (M == 0) {
@@ -888,7 +936,7 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
     return cu(cudaMemsetAsync(dWd, 0, (size_t)bw, st));
   }
   Arena a(ws);
-  ChunkWs w = plan_chunked(a, M, H, I, f == kTensor);
+  ChunkWs w = plan_chunked(a, M, H, I, f == kTensor, h->sm_count);
   if (f == kTensor) TRY(transpose(h, (const uint16_t*)Wd, H, I, I, w.WdT, st));
   // Gather the chunks in logical token order, then run the row-wise stages
   // chunk by chunk on their own rows.
@@ -901,7 +949,7 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
     TRYCU(cudaMemcpyAsync(w.g + r0 * I, gate_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
     TRYCU(cudaMemcpyAsync(w.u + r0 * I, up_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
     TRY(rowwise_bwd(h, f, w.dO + r0 * H, (const uint16_t*)Wd, w.WdT, w.g + r0 * I, w.u + r0 * I,
-                    w.dh + r0 * I, w.dU + r0 * I, w.dG + r0 * I, t, H, I, st));
+                    w.dh + r0 * I, w.dU + r0 * I, w.dG + r0 * I, t, H, I, st, w.tcs));
     TRY(silu_mul(h, w.g + r0 * I, w.u + r0 * I, w.h + r0 * I, t, I, I, st));
     r0 += t;
   }

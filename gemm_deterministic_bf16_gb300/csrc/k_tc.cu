@@ -460,7 +460,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long K, long long ld, int box_rows) {
+}  // namespace
+
+bool tc_make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long K, long long ld, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
@@ -471,6 +473,8 @@ bool make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long K,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int BN, int GG>
 cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cudaStream_t st) {
@@ -571,7 +575,7 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   CUtensorMap m[4];
   for (int p = 0; p < 2; ++p) {
     const TcProblem& q = pr[p < np ? p : 0];
-    if (!make_map(&m[2 * p], q.A, R, K, q.lda, BM) || !make_map(&m[2 * p + 1], q.B, C, K, q.ldb, bn))
+    if (!tc_make_map(&m[2 * p], q.A, R, K, q.lda, BM) || !tc_make_map(&m[2 * p + 1], q.B, C, K, q.ldb, bn))
       return cudaErrorInvalidValue;
   }
   switch (bn) {

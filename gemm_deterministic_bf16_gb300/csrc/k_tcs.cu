@@ -1,0 +1,872 @@
+// k_tcs.cu -- few-token tensor-core tree contraction over balanced K ranges.
+//
+// out[r * ldo + c] = T_K(X[r, :], W[c, :]) for r < R <= 32 tokens and c < C
+// weight rows, with the canonical FP32-leaf / BF16-node midpoint tree
+// (RL-Kernel PR #325, "Design").  This is the decode shape: the weights are
+// read once, so streaming them from HBM is the whole cost.  The weights sit on
+// the MMA's 128-row side and the tokens on its 32-column side (rows R..31 of
+// the token tile are zero-filled by TMA and never stored).
+//
+// Balance.  The work is the sequence of bottom groups (G leaves each) of all
+// output tiles, tile after tile (gate and up tiles of one row block next to
+// each other).  CTA b of P takes the groups [b W / P, (b+1) W / P), so every
+// CTA streams the same number of bytes to within one group.  Where a range
+// covers only part of a tile, the CTA folds that part into its maximal
+// aligned subtrees -- nodes of the canonical tree -- and writes them as
+// "pieces"; a second kernel folds each tile's pieces, left to right, into the
+// root.  A whole tile is one piece, its root.  Nothing in the streaming
+// kernel waits on another CTA.  Without scratch ("direct" mode) CTAs take
+// whole tiles and store the roots themselves.
+//
+// Streaming.  Two CTAs per SM.  In each, two producer threads issue the TMA
+// loads of alternate leaves (one issuing thread sustains only part of an SM's
+// share of HBM bandwidth), one thread issues the MMAs (4 x K=16 per 64-wide
+// leaf into a fresh TMEM buffer), and four epilogue warps read the leaves
+// from TMEM, form the group roots and fold them.
+//
+// Every wait is bounded; on a timeout the CTA records DETFFN_ERR_TIMEOUT,
+// stops, drains its own copies and MMAs (bounded) and frees its TMEM.
+#include <cuda.h>
+
+#include <utility>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tc.h"
+
+namespace detffn {
+namespace {
+
+constexpr int BM = 128;           // weight rows per tile (MMA M)
+constexpr int BK = 64;            // leaf width (MMA K = 4 x 16)
+constexpr int BN = 32;            // token columns (MMA N)
+constexpr int kProd = 2;          // producer warps 0, 1
+constexpr int kMmaWarp = kProd;   // warp 2: TMEM allocation and MMA issue
+constexpr int kEpi0 = kProd + 1;  // warps 3..6: epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
+constexpr int kNBuf = 8;          // TMEM leaf buffers of BN columns (256 columns; two CTAs per SM)
+constexpr int kTmemCols = kNBuf * BN;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE = A_BYTES + B_BYTES;
+constexpr int WORDS = BN / 2;     // packed BF16 pairs per epilogue thread (one row, all tokens)
+constexpr int REG_LV = 3;         // pending stack levels kept in registers
+constexpr int LV_BYTES = BM * WORDS * 4;
+constexpr int BAR_BYTES = 512;
+constexpr int MAX_SMEM = 113 * 1024;
+constexpr int MAX_STAGES = 8;
+constexpr int PIECE = BM * BN;    // elements of one piece: [word = token pair][row] as 32-bit words
+constexpr int kTopWords = 2;      // top kernel: token pairs per CTA (grid.y covers the rest)
+constexpr int kTopThreads = BM * kTopWords;  // one thread per (row, token pair)
+// Pieces per segment staged in shared memory at a time: fused gate/up CTAs
+// (two segments, about seven pieces each at decode sizes; four CTAs per SM)
+// and plain CTAs (one segment, up to a few dozen pieces).
+__host__ __device__ constexpr int top_chunk(bool fused) { return fused ? 16 : 32; }
+__host__ __device__ constexpr int top_smem_fixed(bool fused) {
+  return (fused ? 2 : 1) * top_chunk(fused) * kTopThreads * 4 + 3 * 2 * kTopWords * (BM + 8) * 2;
+}
+
+static_assert(kTcsMaxLv >= REG_LV, "stack levels");
+
+__host__ __device__ inline int stages_for(int E) {
+  const int lv = E > REG_LV ? E - REG_LV : 0;
+  int n = (MAX_SMEM - 1024 - BAR_BYTES - lv * LV_BYTES) / STAGE;
+  if (n > MAX_STAGES) n = MAX_STAGES;
+  return n & ~1;  // even: stage s is always filled by producer s % 2
+}
+__host__ __device__ inline int smem_for(int E, int ns) {
+  const int lv = E > REG_LV ? E - REG_LV : 0;
+  return 1024 + ns * STAGE + lv * LV_BYTES + BAR_BYTES;
+}
+
+struct Bars {
+  uint64_t full[MAX_STAGES], empty[MAX_STAGES], accf[kNBuf], acce[kNBuf], fin;
+  uint32_t tmem_slot;
+  int abort;
+};
+static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block");
+
+struct TcsArgs {
+  int R, C;         // tokens (<= 32), weight rows per problem
+  int G, E;         // leaves per bottom group, levels above the groups (2^E groups per tile)
+  int np, T;        // problems (1 or 2), 128-row tiles per problem
+  long long W;      // groups in all: np * T * 2^E
+  int cap;          // piece slots per CTA
+  int nstage;
+  uint16_t* slots;  // [gridDim.x][cap][BM][BN]; null: direct mode
+  uint16_t* out0;   // direct mode: roots go to out_p[r * ldo + c]
+  uint16_t* out1;
+  long long ldo;
+  int* status;
+  long long spin;
+};
+
+// First group of CTA b's range.  Direct mode deals whole tiles: segment
+// boundaries only, so every tile's root is formed in one CTA.
+__host__ __device__ __forceinline__ long long range_lo(long long b, long long W, long long P, int Q, bool direct) {
+  return direct ? (b * (W / Q) / P) * Q : b * W / P;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
+                                              volatile int* abort_flag, int* status) {
+  for (long long i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  if (status) atomicExch(status, (int)DETFFN_ERR_TIMEOUT);
+  return false;
+}
+
+__host__ __device__ inline int hibit(unsigned v) {  // v > 0
+#ifdef __CUDA_ARCH__
+  return 31 - __clz(v);
+#else
+  return 31 - __builtin_clz(v);
+#endif
+}
+__host__ __device__ inline int popc(unsigned v) {
+#ifdef __CUDA_ARCH__
+  return __popc(v);
+#else
+  return __builtin_popcount(v);
+#endif
+}
+
+// The pieces of groups [x, y), 0 <= x < y <= 2^E, are its maximal aligned
+// blocks.  Let h be the highest bit in which x and y - 1 differ and z the
+// multiple of 2^h between them: left to right, the pieces have the sizes of
+// the set bits of z - x (ascending) and then of y - z (descending) -- unless
+// both halves are whole, when [x, y) is itself one aligned block.
+struct PieceSplit {
+  int x, z, y;
+  bool one;  // [x, y) is one aligned block
+};
+__host__ __device__ inline PieceSplit piece_split(int x, int y) {
+  PieceSplit p{x, y, y, true};
+  if (y - x == 1) return p;
+  const int h = hibit((unsigned)(x ^ (y - 1)));
+  p.z = ((y - 1) >> h) << h;
+  p.one = (p.z - x == (1 << h)) && (y - p.z == (1 << h));
+  return p;
+}
+__host__ __device__ inline int count_pieces(int x, int y) {
+  const PieceSplit p = piece_split(x, y);
+  return p.one ? 1 : popc((unsigned)(p.z - x)) + popc((unsigned)(y - p.z));
+}
+
+// Writes one row (all tokens) of the CTA's next piece: word i of the row at
+// [i][row], so that a warp's rows of one word are one contiguous line.
+__device__ __forceinline__ void emit_piece(uint16_t* slots, int& n, int cap, int row, const uint32_t (&v)[WORDS]) {
+  if (n < cap) {
+    uint32_t* o = reinterpret_cast<uint32_t*>(slots + (size_t)n * PIECE) + row;
+#pragma unroll
+    for (int i = 0; i < WORDS; ++i) o[i * BM] = v[i];
+  }
+  ++n;
+}
+
+}  // namespace
+}  // namespace detffn
+
+namespace detffn {
+namespace {
+
+// The streaming kernel.  Each role walks the CTA's groups in the same order:
+// segment (tile, problem) after segment, groups qa..qb-1 of each.
+// 128 registers: registers are granted per 4 warps, so a CTA of 7 warps holds
+// 8 x 32 x 128 = 32,768 and two CTAs fit one SM's 65,536.
+template <int GG>
+__global__ void __maxnreg__(128)
+    k_tcs(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+          const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmX2, const TcsArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int NS = a.nstage;
+  const int slv = a.E > REG_LV ? a.E - REG_LV : 0;
+  unsigned char* stages = smem;
+  uint32_t* stk = reinterpret_cast<uint32_t*>(smem + NS * STAGE);
+  Bars* bars = reinterpret_cast<Bars*>(smem + NS * STAGE + slv * LV_BYTES);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Q = 1 << a.E;
+  const bool direct = a.slots == nullptr;
+  const long long w0 = range_lo(blockIdx.x, a.W, gridDim.x, Q, direct);
+  const long long w1 = range_lo(blockIdx.x + 1ll, a.W, gridDim.x, Q, direct);
+  const long long limit = a.spin > 0 ? a.spin : kDefaultSpin;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int b = 0; b < kNBuf; ++b) {
+      mbar_init(&bars->accf[b], 1);
+      mbar_init(&bars->acce[b], kEpiWarps);
+    }
+    mbar_init(&bars->fin, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp < kProd && lane == 0) {
+    prefetch_tmap(warp == 0 ? &tmW : &tmX);
+    if (a.np > 1) prefetch_tmap(warp == 0 ? &tmW2 : &tmX2);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  // Programmatic dependent launch: the set-up above overlaps the previous
+  // kernel; nothing below touches global memory before it has completed.
+  grid_dep_wait();
+  grid_dep_launch();
+
+  if (warp < kProd) {
+    // ---------------- TMA producers: leaf it goes to producer it % kProd ----------------
+    if (lane == 0) {
+      long long it = 0;
+      bool ok = true;
+      for (long long w = w0; w < w1 && ok;) {
+        const long long s = w / Q;
+        const int qa = (int)(w - s * Q);
+        const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
+        const int t = (int)(s / a.np), pb = (int)(s % a.np);
+        const CUtensorMap* mW = pb ? &tmW2 : &tmW;
+        const CUtensorMap* mX = pb ? &tmX2 : &tmX;
+        for (int j = qa * GG; j < qb * GG; ++j, ++it) {
+          if ((int)(it % kProd) != warp) continue;
+          const int st = (int)(it % NS);
+          if (!wait_or_abort(&bars->empty[st], (uint32_t)(((it / NS) & 1) ^ 1), limit, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          unsigned char* dst = stages + st * STAGE;
+          mbar_arrive_expect_tx(&bars->full[st], (uint32_t)STAGE);
+          tma_load_2d(dst, mW, j * BK, t * BM, &bars->full[st]);
+          tma_load_2d(dst + A_BYTES, mX, j * BK, 0, &bars->full[st]);
+        }
+        w = s * Q + qb;
+      }
+      // Drain: this producer's last loads have landed.
+      for (long long i = (it > NS ? it - NS : 0); i < it; ++i)
+        if ((int)(i % kProd) == warp) mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), limit, nullptr);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, BN);
+      long long it = 0;
+      bool ok = true;
+      for (long long w = w0; w < w1 && ok;) {
+        const long long s = w / Q;
+        const int qa = (int)(w - s * Q);
+        const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
+        for (int j = qa * GG; j < qb * GG; ++j, ++it) {
+          const int b = (int)(it % kNBuf);
+          if (!wait_or_abort(&bars->acce[b], (uint32_t)(((it / kNBuf) & 1) ^ 1), limit, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const int st = (int)(it % NS);
+          if (!wait_or_abort(&bars->full[st], (uint32_t)((it / NS) & 1), limit, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da = smem_desc_sw128(stages + st * STAGE);
+          const uint64_t db = smem_desc_sw128(stages + st * STAGE + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
+            tc_mma_bf16(tmem + (uint32_t)(b * BN), da + 2 * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+          tc_commit(&bars->empty[st]);
+          tc_commit(&bars->accf[b]);
+        }
+        w = s * Q + qb;
+      }
+      tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
+      mbar_wait(&bars->fin, 0, limit, nullptr);
+    }
+  } else {
+    // ---------------- epilogue: leaves -> group roots -> pieces ----------------
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    uint16_t* const myslots = direct ? nullptr : a.slots + (size_t)blockIdx.x * a.cap * PIECE;
+    long long lc = 0;
+    int np_out = 0;  // pieces written
+    bool ok = true;
+    uint32_t reg_lv[REG_LV][WORDS];
+    for (long long w = w0; w < w1 && ok;) {
+      const long long s = w / Q;
+      const int qa = (int)(w - s * Q);
+      const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
+      unsigned pend = 0;  // levels holding a left child that waits for its right sibling
+      for (int q = qa; q < qb; ++q) {
+        for (int g = 0; g < GG; ++g)
+          if (!wait_or_abort(&bars->accf[(lc + g) % kNBuf], (uint32_t)(((lc + g) / kNBuf) & 1), limit, abort_flag,
+                             a.status))
+            ok = false;
+        if (__any_sync(0xffffffffu, !ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t b0 = (uint32_t)((lc % kNBuf) * BN), b1 = (uint32_t)(((lc + 1) % kNBuf) * BN),
+                       b2 = (uint32_t)(((lc + 2) % kNBuf) * BN);
+        // The group root: a lone leaf rounded once, l0 + l1, or l0 + (l1 + l2).
+        uint32_t root[WORDS];
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c) {
+          uint32_t v0[16];
+          if constexpr (GG == 3) {
+            uint32_t v1[16], v2[16], n12[8];
+            tmem_ld16(tmem + lane_addr + b1 + 16 * c, v1);
+            tmem_ld16(tmem + lane_addr + b2 + 16 * c, v2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              n12[i] = pack_bf16x2(__fadd_rn(__uint_as_float(v1[2 * i]), __uint_as_float(v2[2 * i])),
+                                   __fadd_rn(__uint_as_float(v1[2 * i + 1]), __uint_as_float(v2[2 * i + 1])));
+            tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              root[8 * c + i] = pack_bf16x2(__fadd_rn(__uint_as_float(v0[2 * i]), __uint_as_float(n12[i] << 16)),
+                                            __fadd_rn(__uint_as_float(v0[2 * i + 1]),
+                                                      __uint_as_float(n12[i] & 0xFFFF0000u)));
+          } else if constexpr (GG == 2) {
+            uint32_t v1[16];
+            tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
+            tmem_ld16(tmem + lane_addr + b1 + 16 * c, v1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              root[8 * c + i] = pack_bf16x2(__fadd_rn(__uint_as_float(v0[2 * i]), __uint_as_float(v1[2 * i])),
+                                            __fadd_rn(__uint_as_float(v0[2 * i + 1]), __uint_as_float(v1[2 * i + 1])));
+          } else {
+            tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) root[8 * c + i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+          }
+        }
+        // The leaves are in registers: return the TMEM buffers to the MMA warp.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+          for (int g = 0; g < GG; ++g) mbar_arrive(&bars->acce[(lc + g) % kNBuf]);
+        lc += GG;
+
+        // Fold: merge with pending left siblings inside [qa, qb); a right
+        // child whose left sibling lies before qa is a finished piece; a left
+        // child waits on the stack for its right sibling.
+        int at = q;
+        bool live = true;
+#pragma unroll
+        for (int m = 0; m <= kTcsMaxLv; ++m) {
+          if (live) {
+            if (m == a.E) {  // the whole tile: its root
+              if (direct) {
+                const long long c = (long long)(s / a.np) * BM + row;
+                uint16_t* o = (s % a.np) ? a.out1 : a.out0;
+                if (c < a.C)
+#pragma unroll
+                  for (int i = 0; i < BN; ++i)
+                    if (i < a.R) o[i * a.ldo + c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
+              } else {
+                emit_piece(myslots, np_out, a.cap, row, root);
+              }
+              live = false;
+            } else if (((at >> m) & 1) && at - (1 << m) >= qa) {
+#pragma unroll
+              for (int i = 0; i < WORDS; ++i) {
+                const uint32_t left = m < REG_LV ? reg_lv[m < REG_LV ? m : 0][i]
+                                                 : stk[((m - REG_LV) * WORDS + i) * BM + row];
+                root[i] = add_bf16x2(left, root[i]);
+              }
+              pend &= ~(1u << m);
+              at -= 1 << m;
+            } else if ((at >> m) & 1) {
+              emit_piece(myslots, np_out, a.cap, row, root);
+              live = false;
+            } else {
+#pragma unroll
+              for (int i = 0; i < WORDS; ++i) {
+                if (m < REG_LV) reg_lv[m < REG_LV ? m : 0][i] = root[i];
+                else stk[((m - REG_LV) * WORDS + i) * BM + row] = root[i];
+              }
+              pend |= 1u << m;
+              live = false;
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      // The segment ends: pending left children are finished pieces (left to right = high level first).
+#pragma unroll
+      for (int m = kTcsMaxLv - 1; m >= 0; --m)
+        if ((pend >> m) & 1) {
+          uint32_t v[WORDS];
+#pragma unroll
+          for (int i = 0; i < WORDS; ++i)
+            v[i] = m < REG_LV ? reg_lv[m < REG_LV ? m : 0][i] : stk[((m - REG_LV) * WORDS + i) * BM + row];
+          emit_piece(myslots, np_out, a.cap, row, v);
+        }
+      w = s * Q + qb;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+}  // namespace detffn
+
+namespace detffn {
+namespace {
+
+struct TcsTopArgs {
+  int R, C, E, np;
+  long long W;
+  int P, cap;
+  const uint16_t* slots;
+  uint16_t* out0;   // problem 0 result (gate when fused), or null when fused and not kept
+  uint16_t* out1;   // problem 1 result (up when fused), or null
+  long long ldo;    // row stride of out0, out1 and h (elements)
+  uint16_t* h;      // fused: h = bf16(SiLU(gate)) * up, rounded to BF16; null: plain
+  const uint16_t* silu;
+};
+
+struct PieceRef {
+  int slot;  // b * cap + j
+  int at;    // level m (bits 0..7), left siblings it merges with (bits 8..15), and whether the
+             // result is the root (bit 16): the fold, the same for every element, worked out once
+};
+
+// The fold step of a piece of level m starting at group `at`, for a tile of
+// 2^E groups: it merges with the pending left siblings at levels m, m+1, ...
+// while its subtree is a right child, then waits on the stack at the level
+// reached or is the root.
+__device__ __forceinline__ int fold_code(int at, int m, int E) {
+  int k = 0;
+  while (m + k < E && ((at >> (m + k)) & 1)) ++k;
+  return m | (k << 8) | ((m + k == E) ? (1 << 16) : 0);
+}
+
+// Lists, in order, the pieces of segment s that CTAs [b_base, b_base + 32)
+// wrote: one lane per CTA, placed by a warp scan.  Returns the count.
+__device__ int list_pieces(const TcsTopArgs& a, long long s, long long b_base, PieceRef* list, int lane) {
+  const int Q = 1 << a.E;
+  const long long ws = s * Q, we = ws + Q;
+  const long long b = b_base + lane;
+  int cnt = 0;
+  long long lo = 0, hi = 0, blo = 0;
+  if (b < a.P) {
+    blo = b * a.W / a.P;
+    const long long bhi = (b + 1) * a.W / a.P;
+    lo = blo > ws ? blo : ws;
+    hi = bhi < we ? bhi : we;
+    if (lo < hi) cnt = count_pieces((int)(lo - ws), (int)(hi - ws));
+  }
+  int incl = cnt;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += t;
+  }
+  if (cnt > 0) {
+    // Pieces CTA b wrote for its earlier segments: its first (partial) one and whole ones.
+    const long long s0 = blo / Q;
+    int j = 0;
+    if (s0 < s) j = count_pieces((int)(blo - s0 * Q), Q) + (int)(s - s0 - 1);
+    int pos = incl - cnt;
+    const PieceSplit p = piece_split((int)(lo - ws), (int)(hi - ws));
+    if (p.one) {
+      list[pos].slot = (int)(b * a.cap + j);
+      list[pos].at = fold_code(p.x, hibit((unsigned)(p.y - p.x)), a.E);
+    } else {
+      int at = p.x;
+#pragma unroll 1
+      for (unsigned rem = (unsigned)(p.z - p.x); rem; ++pos, ++j) {  // ascending sizes
+        const unsigned bit = rem & (0u - rem);
+        list[pos].slot = (int)(b * a.cap + j);
+        list[pos].at = fold_code(at, hibit(bit), a.E);
+        at += (int)bit;
+        rem -= bit;
+      }
+#pragma unroll 1
+      for (unsigned rem = (unsigned)(p.y - p.z); rem; ++pos, ++j) {  // descending sizes
+        const unsigned bit = 1u << hibit(rem);
+        list[pos].slot = (int)(b * a.cap + j);
+        list[pos].at = fold_code(at, hibit(bit), a.E);
+        at += (int)bit;
+        rem -= bit;
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// Fold state of one segment for this thread's (row, token pair): the pieces,
+// left to right, meet their left siblings on a stack in this thread's column
+// of shared memory.
+struct Fold {
+  uint32_t* stk;  // level l at stk[l * kTopThreads]
+  uint32_t root;
+  long long b;    // first CTA of the current list batch
+  int n;          // pieces in the current list batch
+};
+
+__device__ __forceinline__ long long first_cta(const TcsTopArgs& a, long long s) {
+  return s * (1ll << a.E) * a.P / a.W;
+}
+__device__ __forceinline__ bool more_ctas(const TcsTopArgs& a, long long s, long long b) {
+  return b < a.P && b * a.W / a.P < (s + 1) * (1ll << a.E);
+}
+
+// Folds one piece (its fold code from the list) into the stack.
+__device__ __forceinline__ void fold_piece(int code, uint32_t cur, Fold& f) {
+  const int m = code & 0xFF, k = (code >> 8) & 0xFF;
+#pragma unroll 1
+  for (int i = 0; i < k; ++i) cur = add_bf16x2(f.stk[(m + i) * kTopThreads], cur);
+  if (code >> 16) f.root = cur;
+  else f.stk[(m + k) * kTopThreads] = cur;
+}
+
+// Copies (cp.async, 4 bytes per thread) this thread's word of pieces
+// k0 .. min(k0 + CH, n) - 1 of the list into its column of buf.
+template <int CH>
+__device__ __forceinline__ void stage_pieces(const TcsTopArgs& a, const PieceRef* list, int k0, int n, int row,
+                                             int word, uint32_t* buf) {
+  const int kend = n < k0 + CH ? n : k0 + CH;
+#pragma unroll 1
+  for (int k = k0; k < kend; ++k) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.slots + (size_t)list[k].slot * PIECE) + word * BM + row;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(buf + (k - k0) * kTopThreads + threadIdx.x)),
+                 "l"(src)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void staged_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <int CH>
+__device__ __forceinline__ void fold_staged(const TcsTopArgs& a, const PieceRef* list, int k0, int n,
+                                            const uint32_t* buf, Fold& f) {
+  const int kend = n < k0 + CH ? n : k0 + CH;
+#pragma unroll 1
+  for (int k = k0; k < kend; ++k) fold_piece(list[k].at, buf[(k - k0) * kTopThreads + threadIdx.x], f);
+}
+
+// Everything of segment s after its first CH pieces (already staged and
+// folded by the caller): the rest of that list, then further list batches.
+template <int CH>
+__device__ void fold_rest(const TcsTopArgs& a, long long s, PieceRef* list, int row, int word, bool active,
+                          uint32_t* buf, Fold& f) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int k0 = CH; k0 < f.n; k0 += CH) {
+    if (active) {
+      stage_pieces<CH>(a, list, k0, f.n, row, word, buf);
+      staged_wait();
+      fold_staged<CH>(a, list, k0, f.n, buf, f);
+    }
+  }
+#pragma unroll 1
+  for (f.b += 32; more_ctas(a, s, f.b); f.b += 32) {
+    __syncthreads();  // the previous batch's list is no longer read
+    if (warp == 0) {
+      const int n = list_pieces(a, s, f.b, list, lane);
+      if (lane == 0) list[32 * a.cap].slot = n;
+    }
+    __syncthreads();
+    f.n = list[32 * a.cap].slot;
+#pragma unroll 1
+    for (int k0 = 0; k0 < f.n; k0 += CH) {
+      if (active) {
+        stage_pieces<CH>(a, list, k0, f.n, row, word, buf);
+        staged_wait();
+        fold_staged<CH>(a, list, k0, f.n, buf, f);
+      }
+    }
+  }
+}
+
+// Writes a [2 kTopWords tokens][128 rows] tile held in shared memory to
+// out[r * ldo + c] for r in [r0, min(r0 + 2 kTopWords, R)), c in [c0, min(c0 + 128, C)).
+__device__ __forceinline__ void store_tile(const uint16_t* tile, uint16_t* out, long long ldo, int R, int r0,
+                                           long long c0, long long C) {
+  const int tok = threadIdx.x >> 4, c8 = (threadIdx.x & 15) * 8;
+  if (tok >= 2 * kTopWords || r0 + tok >= R) return;
+  const long long c = c0 + c8;
+  uint16_t* o = out + (r0 + tok) * ldo + c;
+  const uint16_t* src = tile + tok * (BM + 8) + c8;
+  if (c + 8 <= C && ((uintptr_t)o & 15u) == 0) {
+    *reinterpret_cast<uint4*>(o) = *reinterpret_cast<const uint4*>(src);
+  } else {
+    for (int i = 0; i < 8; ++i)
+      if (c + i < C) o[i] = src[i];
+  }
+}
+
+__device__ __forceinline__ void put_tile(uint16_t* tile, int row, int wl, uint32_t v) {
+  tile[(2 * wl) * (BM + 8) + row] = (uint16_t)(v & 0xFFFFu);
+  tile[(2 * wl + 1) * (BM + 8) + row] = (uint16_t)(v >> 16);
+}
+
+// Plain (FUSED false): CTA (s, y) folds segment s for token pairs
+// kTopWords * y .. kTopWords * y + kTopWords - 1.  Fused (np == 2): CTA (t, y)
+// folds gate (segment 2t) and up (segment 2t+1) and forms
+// h = bf16(SiLU(gate)) * up, rounded to BF16.  Each thread owns one (row,
+// token pair); the pieces are staged in shared memory (up to CH per segment in
+// flight) and folded from there.  Launched as a programmatic dependent of the
+// streaming kernel: the piece lists (arithmetic only) are built before
+// waiting for its results.
+template <bool FUSED>
+__global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
+  constexpr int NSEG = FUSED ? 2 : 1;
+  constexpr int CH = top_chunk(FUSED);
+  extern __shared__ __align__(16) unsigned char top_smem[];
+  __shared__ uint32_t stacks[NSEG][kTcsMaxLv][kTopThreads];
+  uint32_t* bufs = reinterpret_cast<uint32_t*>(top_smem);  // NSEG x [CH][kTopThreads]
+  uint16_t* tiles = reinterpret_cast<uint16_t*>(top_smem + NSEG * CH * kTopThreads * 4);  // 3 x [2 kTopWords][BM + 8]
+  PieceRef* lists =
+      reinterpret_cast<PieceRef*>(top_smem + NSEG * CH * kTopThreads * 4 + 3 * 2 * kTopWords * (BM + 8) * 2);
+  const int row = threadIdx.x % BM, wl = threadIdx.x / BM;
+  const int word = kTopWords * blockIdx.y + wl;
+  const bool active = 2 * word < a.R;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long s0 = FUSED ? 2ll * blockIdx.x : (long long)blockIdx.x;
+  const int stride = 32 * a.cap + 1;  // list entries per segment (the last holds the count)
+  Fold f[NSEG];
+  if (warp < NSEG) {
+    PieceRef* list = lists + warp * stride;
+    const int n = list_pieces(a, s0 + warp, first_cta(a, s0 + warp), list, lane);
+    if (lane == 0) list[32 * a.cap].slot = n;
+  }
+  grid_dep_launch();
+  __syncthreads();
+  grid_dep_wait();  // the streaming kernel's pieces are complete and visible
+#pragma unroll
+  for (int g = 0; g < NSEG; ++g) {
+    f[g].b = first_cta(a, s0 + g);
+    f[g].n = lists[g * stride + 32 * a.cap].slot;
+    f[g].root = 0;
+    f[g].stk = &stacks[g][0][threadIdx.x];
+    if (active) stage_pieces<CH>(a, lists + g * stride, 0, f[g].n, row, word, bufs + g * CH * kTopThreads);
+  }
+  staged_wait();
+#pragma unroll
+  for (int g = 0; g < NSEG; ++g) {
+    if (active) fold_staged<CH>(a, lists + g * stride, 0, f[g].n, bufs + g * CH * kTopThreads, f[g]);
+    fold_rest<CH>(a, s0 + g, lists + g * stride, row, word, active, bufs + g * CH * kTopThreads, f[g]);
+  }
+  const int r0 = 2 * kTopWords * blockIdx.y;
+  if constexpr (!FUSED) {
+    const int t = (int)(s0 / a.np), pb = (int)(s0 % a.np);
+    put_tile(tiles, row, wl, f[0].root);
+    __syncthreads();
+    store_tile(tiles, pb ? a.out1 : a.out0, a.ldo, a.R, r0, (long long)t * BM, a.C);
+  } else {
+    const int t = blockIdx.x;
+    const uint32_t g = f[0].root, u = f[1].root;
+    const float h0 = __fmul_rn(bf2f(__ldg(a.silu + (g & 0xFFFFu))), __uint_as_float(u << 16));
+    const float h1 = __fmul_rn(bf2f(__ldg(a.silu + (g >> 16))), __uint_as_float(u & 0xFFFF0000u));
+    constexpr int TILE = 2 * kTopWords * (BM + 8);
+    put_tile(tiles, row, wl, (uint32_t)f2bf(h0) | ((uint32_t)f2bf(h1) << 16));
+    if (a.out0) put_tile(tiles + TILE, row, wl, g);
+    if (a.out1) put_tile(tiles + 2 * TILE, row, wl, u);
+    __syncthreads();
+    store_tile(tiles, a.h, a.ldo, a.R, r0, (long long)t * BM, a.C);
+    if (a.out0) store_tile(tiles + TILE, a.out0, a.ldo, a.R, r0, (long long)t * BM, a.C);
+    if (a.out1) store_tile(tiles + 2 * TILE, a.out1, a.ldo, a.R, r0, (long long)t * BM, a.C);
+  }
+}
+
+}  // namespace
+}  // namespace detffn
+
+namespace detffn {
+
+bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* p) {
+  if (R < 1 || R > BN || C < 1 || K < 1 || np < 1 || np > 2 || max_ctas < 1) return false;
+  const long long L = (K + BK - 1) / BK;
+  int G;
+  long long q;
+  if (L == 1) {
+    G = 1;
+    q = 1;
+  } else if ((L & (L - 1)) == 0) {
+    G = 2;
+    q = L / 2;
+  } else if (L % 3 == 0 && ((L / 3) & (L / 3 - 1)) == 0) {
+    G = 3;
+    q = L / 3;
+  } else {
+    return false;
+  }
+  int E = 0;
+  while ((1ll << E) < q) ++E;
+  if (E > kTcsMaxLv || C > (1ll << 30)) return false;
+  TcsPlan r;
+  r.R = (int)R;
+  r.C = C;
+  r.K = K;
+  r.G = G;
+  r.E = E;
+  r.np = np;
+  r.T = (int)((C + BM - 1) / BM);
+  const int Q = 1 << E;
+  r.W = (long long)np * r.T * Q;
+  r.direct = direct;
+  const long long units = direct ? (long long)np * r.T : r.W;
+  r.P = (int)(max_ctas < units ? max_ctas : units);
+  r.nstage = stages_for(E);
+  if (r.nstage < 2) return false;
+  if (direct) {
+    *p = r;
+    return true;
+  }
+  // Piece slots per CTA: the most pieces any CTA's range produces.
+  int cap = 1;
+  for (long long b = 0; b < r.P; ++b) {
+    const long long w0 = b * r.W / r.P, w1 = (b + 1) * r.W / r.P;
+    int n = 0;
+    for (long long w = w0; w < w1;) {
+      const long long s = w / Q;
+      const int qa = (int)(w - s * Q), qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
+      n += count_pieces(qa, qb);
+      w = s * Q + qb;
+    }
+    if (n > cap) cap = n;
+  }
+  r.cap = cap;
+  // Top kernel: staged pieces, output tiles, piece lists (the larger of its two modes).
+  r.top_smem = top_smem_fixed(false) + 2 * (32 * cap + 1) * (int)sizeof(PieceRef);
+  if (r.top_smem > 200 * 1024) return false;
+  r.scratch = (size_t)r.P * cap * PIECE * 2;
+  *p = r;
+  return true;
+}
+
+namespace {
+
+// A launch that may begin while the previous kernel on the stream finishes
+// (programmatic dependent launch); the kernels wait in grid_dep_wait before
+// touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*k)(KArgs...), dim3 grid, int threads, int smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
+
+cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo, uint16_t* h, const uint16_t* silu,
+                       void* scratch, size_t scratch_bytes, int* status, long long spin, cudaStream_t st) {
+  if (!plan.direct && (!scratch || scratch_bytes < plan.scratch || ((uintptr_t)scratch & 15u)))
+    return cudaErrorInvalidValue;
+  if (plan.direct && h) return cudaErrorInvalidValue;
+  for (int p = 0; p < plan.np; ++p)
+    if ((pr[p].ldw % 8) || (pr[p].ldx % 8) || ((uintptr_t)pr[p].W & 15u) || ((uintptr_t)pr[p].X & 15u))
+      return cudaErrorInvalidValue;
+  CUtensorMap m[4];
+  for (int p = 0; p < 2; ++p) {
+    const TcsProblem& q = pr[p < plan.np ? p : 0];
+    if (!tc_make_map(&m[2 * p], q.W, plan.C, plan.K, q.ldw, BM) ||
+        !tc_make_map(&m[2 * p + 1], q.X, plan.R, plan.K, q.ldx, BN))
+      return cudaErrorInvalidValue;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaSuccess;
+    void (*ks[3])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) = {k_tcs<1>, k_tcs<2>, k_tcs<3>};
+    for (auto k : ks) {
+      // Two CTAs per SM: all of their shared memory, at most 113 KB each.
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    }
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_tcs_top<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_tcs_top<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  TcsArgs a{};
+  a.R = plan.R;
+  a.C = (int)plan.C;
+  a.G = plan.G;
+  a.E = plan.E;
+  a.np = plan.np;
+  a.T = plan.T;
+  a.W = plan.W;
+  a.cap = plan.cap;
+  a.nstage = plan.nstage;
+  a.slots = plan.direct ? nullptr : static_cast<uint16_t*>(scratch);
+  a.out0 = pr[0].out;
+  a.out1 = plan.np > 1 ? pr[1].out : nullptr;
+  a.ldo = ldo;
+  a.status = status;
+  a.spin = spin;
+  const int smem = smem_for(plan.E, plan.nstage);
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) =
+      plan.G == 1 ? k_tcs<1> : plan.G == 2 ? k_tcs<2> : k_tcs<3>;
+  cudaError_t e = launch_dependent(kern, dim3(plan.P), kThreads, smem, st, m[0], m[1], m[2], m[3], a);
+  if (e != cudaSuccess || plan.direct) return e;
+  TcsTopArgs t{};
+  t.R = plan.R;
+  t.C = (int)plan.C;
+  t.E = plan.E;
+  t.np = plan.np;
+  t.W = plan.W;
+  t.P = plan.P;
+  t.cap = plan.cap;
+  t.slots = static_cast<const uint16_t*>(scratch);
+  t.out0 = pr[0].out;
+  t.out1 = plan.np > 1 ? pr[1].out : nullptr;
+  t.ldo = ldo;
+  t.h = h;
+  t.silu = silu;
+  const dim3 grid(h ? plan.T : plan.np * plan.T, (plan.R + 2 * kTopWords - 1) / (2 * kTopWords));
+  const int top_smem = top_smem_fixed(h != nullptr) + 2 * (32 * plan.cap + 1) * (int)sizeof(PieceRef);
+  return h ? launch_dependent(k_tcs_top<true>, grid, kTopThreads, top_smem, st, t)
+           : launch_dependent(k_tcs_top<false>, grid, kTopThreads, top_smem, st, t);
+}
+
+}  // namespace
+
+cudaError_t launch_tcs(const TcsPlan& plan, const TcsProblem* pr, long long ldo, void* scratch,
+                       size_t scratch_bytes, int* status, long long spin, cudaStream_t st) {
+  for (int p = 0; p < plan.np; ++p)
+    if (!pr[p].out) return cudaErrorInvalidValue;
+  return tcs_launch(plan, pr, ldo, nullptr, nullptr, scratch, scratch_bytes, status, spin, st);
+}
+
+cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* pr, uint16_t* h, long long ldo,
+                              const uint16_t* silu, void* scratch, size_t scratch_bytes, int* status,
+                              long long spin, cudaStream_t st) {
+  if (plan.np != 2 || !h || !silu) return cudaErrorInvalidValue;
+  return tcs_launch(plan, pr, ldo, h, silu, scratch, scratch_bytes, status, spin, st);
+}
+
+}  // namespace detffn

@@ -1,7 +1,9 @@
 // tc.h -- launcher of the tensor-core (tcgen05) tree contraction.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace detffn {
@@ -43,5 +45,50 @@ cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, 
                            long long R, long long C, long long K, uint16_t* out, long long ld_r,
                            long long ld_c, int bn, const TcScratch& scratch, int* status,
                            long long spin_limit, int sm_count, cudaStream_t st);
+
+// A 2-D BF16 tensor map over rows x K (row stride ld elements), 128-byte
+// swizzle, boxes of 64 (K) x box_rows.
+bool tc_make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long K, long long ld, int box_rows);
+
+// ---------------------------------------------------------------------------
+// Few-token contractions (k_tcs.cu): out[r * ldo + c] = T_K(X[r, :], W[c, :])
+// for r < R <= 32 tokens and c < C weight rows, the weights streamed once with
+// the work split evenly over two CTAs per SM (balanced K ranges whose partial
+// subtrees a second kernel folds into the canonical tree).
+// ---------------------------------------------------------------------------
+constexpr int kTcsMaxLv = 8;  // at most 2^8 bottom groups (K <= 3 * 256 * 64)
+
+struct TcsPlan {
+  int R = 0, G = 0, E = 0, T = 0, np = 0, P = 0, cap = 0, nstage = 0, top_smem = 0;
+  long long C = 0, K = 0, W = 0;
+  bool direct = false;  // whole tiles per CTA, roots stored directly (no scratch, no top kernel)
+  size_t scratch = 0;   // bytes of piece slots the launch needs
+};
+
+// Plans a launch on at most max_ctas CTAs (two per SM is the design point).
+// False when the shape is not covered (R > 32, or K's leaf count not 1, 2^d or
+// 3 * 2^d with at most 2^8 bottom groups).  The results never depend on the
+// plan: only the split of each tree into pieces does.
+bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* plan);
+
+struct TcsProblem {
+  const uint16_t* W;  // [C, K] weights, row stride ldw (multiple of 8), 16-byte aligned
+  long long ldw;
+  const uint16_t* X;  // [R, K] tokens, row stride ldx (multiple of 8), 16-byte aligned
+  long long ldx;
+  uint16_t* out;      // out[r * ldo + c]
+};
+
+// One or two same-shaped contractions (plan.np): two launches on `st`, or one
+// in direct mode (scratch unused).
+cudaError_t launch_tcs(const TcsPlan& plan, const TcsProblem* problems, long long ldo, void* scratch,
+                       size_t scratch_bytes, int* status, long long spin, cudaStream_t st);
+
+// Gate (problems[0]) and up (problems[1]) with the SiLU * up stage boundary
+// fused into the top of the trees: h[r * ldo + c] = bf16(bf16(SiLU(gate)) * up);
+// gate and up are stored only where problems[p].out is non-null.
+cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* problems, uint16_t* h, long long ldo,
+                              const uint16_t* silu, void* scratch, size_t scratch_bytes, int* status,
+                              long long spin, cudaStream_t st);
 
 }  // namespace detffn

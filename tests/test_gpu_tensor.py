@@ -169,3 +169,36 @@ def test_tc_decode_split_k_same_bits(G, oracle_mod, M):
     rl2, within1, mx = _stats(host(out), ref["out"])
     print("decode M=%d tensor out: rel-L2 %.3g, within 1 ulp %.5f, max ulp %d" % (M, rl2, within1, mx))
     assert rl2 <= 1e-3
+
+
+@pytest.mark.parametrize("M,H,I", [(32, 4096, 1536), (1, 768, 200), (17, 64, 384), (32, 12288, 256),
+                                   (8, 192, 136), (32, 8192, 1024)])
+def test_tcs_forward_integer_inputs_bit_exact(G, oracle_mod, M, H, I):
+    """Few-token forward (balanced K ranges folded from pieces, SiLU * up fused
+    into the top of the trees): with integer-valued x and weights every leaf is
+    exact, so gate and up equal the oracle bit for bit -- this pins the piece
+    split and fold for bottom groups of 1, 2 and 3 leaves, ragged row tiles
+    and single tokens; h and out follow the tolerance."""
+    d = {"x": _ints((M, H), M + 3), "Wg": _ints((I, H), 4), "Wu": _ints((I, H), 5), "Wd": _ints((H, I), 6)}
+    t = {n: dev(v) for n, v in d.items()}
+    g, u = empty_bf16(M, I), empty_bf16(M, I)
+    out = G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], gate_save=g, up_save=u, path=TENSOR)
+    out_inf = G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], path=TENSOR)
+    f = oracle_mod.ffn_forward(d["x"], d["Wg"], d["Wu"], d["Wd"])
+    assert mismatches(host(g), f["gate"]) == 0
+    assert mismatches(host(u), f["up"]) == 0
+    assert mismatches(host(out), host(out_inf)) == 0          # training and inference forward agree
+    assert _stats(host(out), f["out"])[0] <= 1e-3
+
+
+@pytest.mark.parametrize("M,H,I", [(32, 4096, 1536), (5, 768, 1000), (32, 3072, 128)])
+def test_tcs_pieces_equal_whole_tiles(G, M, H, I):
+    """The forward's gate (pieces from balanced ranges, folded by the top
+    kernel) equals the stand-alone contraction, which forms whole tiles in one
+    CTA (no scratch): the same canonical tree either way."""
+    d = ffn_inputs(M, H, I, seed=40 + M, with_dout=False)
+    t = {n: dev(v) for n, v in d.items()}
+    g, u = empty_bf16(M, I), empty_bf16(M, I)
+    G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], gate_save=g, up_save=u, path=TENSOR)
+    assert mismatches(host(g), host(G.detffn_tree_gemm(t["x"], t["Wg"], path=TENSOR))) == 0
+    assert mismatches(host(u), host(G.detffn_tree_gemm(t["x"], t["Wu"], path=TENSOR))) == 0

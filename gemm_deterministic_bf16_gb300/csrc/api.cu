@@ -419,8 +419,7 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
                    [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->d_status, 0, st)); });
     }
     return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
-      return cu(launch_tc_gemm(A.p, A.rs, B.p, B.rs, R, C, K, out, o_rs, 1, 128, TcScratch(), h->d_status, 0,
-                               h->sm_count, st));
+      return cu(launch_tc_gemm(A.p, A.rs, B.p, B.rs, R, C, K, out, o_rs, 1, h->d_status, 0, h->sm_count, st));
     });
   }
   return timed(h, st, "tree_gemm_exact", bytes, 2.0 * R * C * K,
@@ -661,7 +660,7 @@ detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const u
     const double bytes = 2.0 * (2.0 * w * H + (double)M * H + 2.0 * M * w);
     TRY(timed(h, st, "tc_tree_gemm", bytes, 4.0 * M * w * H, [&] {
       const TcProblem pr[2] = {{x, H, BG.p, H, gate + s * w}, {x, H, BU.p, H, up + s * w}};
-      return cu(launch_tc_gemms(pr, 2, M, w, H, I, 1, 128, TcScratch(), h->d_status, 0, h->sm_count, st));
+      return cu(launch_tc_gemms(pr, 2, M, w, H, I, 1, h->d_status, 0, h->sm_count, st));
     }));
   } else {
     TRY(tree_gemm(h, f, X, Strided{Wg + s * w * H, H, 1}, M, w, H, gate + s * w, I, st));

@@ -10,14 +10,16 @@
 // tree is then a perfect binary tree over Q = 2^E bottom groups of G leaves
 // (G = 2: leaf pairs; G = 3: leaf0 + (leaf1 + leaf2); G = 1: a lone leaf).
 //
+// Used for many tokens (more than 32; fewer go to k_tcs.cu, which splits K
+// evenly over the SMs).
+//
 // Roles (one CTA per SM, persistent over output tiles of 128 x BN):
 //   warp 0      TMA producer: A and B tiles of one leaf per pipeline stage
 //               (128-byte swizzle, K-major), a ring of stages on mbarriers (as many
 //               as fit beside the shared-memory stack levels);
-//   warp 1      allocates TMEM (512/BN leaf buffers of BN columns, at most 16)
-//               and issues the
-//               MMAs, one leaf per buffer, committing to the stage's "empty"
-//               barrier and the buffer's "full" barrier;
+//   warp 1      allocates TMEM (512/BN leaf buffers of BN columns) and issues
+//               the MMAs, one leaf per buffer, committing to the stage's
+//               "empty" barrier and the buffer's "full" barrier;
 //   warps 2-9   epilogue: each thread owns one row (TMEM lane) and BN/2
 //               columns; it reads a group's leaves from TMEM, forms the
 //               group roots, returns the buffers at once, and then folds the
@@ -41,13 +43,10 @@ constexpr int kMaxAccBufs = 16;  // TMEM leaf buffers: 512 columns / BN (at most
 constexpr int kEpiWarp0 = 2;  // warp 0: producer, warp 1: MMA, warps 2..: epilogue
 constexpr int kMaxLv = 6;  // up to Q = 64 bottom groups
 
-// Wide tiles (BN = 128, many tokens): one CTA per SM, 8 epilogue warps (two
-// per TMEM lane quarter, BN/2 columns each), 4 leaf buffers.  Narrow tiles
-// (few tokens): two CTAs per SM, 4 epilogue warps (BN columns each), 256/BN
-// leaf buffers and half the shared memory each, so two pipelines overlap.
+// One CTA per SM, 8 epilogue warps (two per TMEM lane quarter, BN/2 columns
+// each), 512/BN leaf buffers.
 template <int BN> struct TcGeo {
-  static constexpr int MINB = BN >= 128 ? 1 : 2;          // resident CTAs per SM
-  static constexpr int EPI_WARPS = BN >= 128 ? 8 : 4;
+  static constexpr int EPI_WARPS = 8;
   static constexpr int HALVES = EPI_WARPS / 4;            // epilogue warps per lane quarter
   static constexpr int THREADS = 32 * (kEpiWarp0 + EPI_WARPS);
   static constexpr int A_BYTES = BM * BK * 2;
@@ -55,12 +54,12 @@ template <int BN> struct TcGeo {
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int COLS = BN / HALVES;  // columns per epilogue thread
   static constexpr int WORDS = COLS / 2;    // packed BF16 pairs per stack level per thread
-  static constexpr int REG_LV = BN >= 128 ? 2 : 3;  // stack levels kept in registers
+  static constexpr int REG_LV = 2;                        // stack levels kept in registers
   static constexpr int LV_BYTES = BM * BN * 2;            // one shared-memory stack level
   static constexpr int BAR_BYTES = 512;
-  static constexpr int MAX_SMEM = BN >= 128 ? 227 * 1024 : 113 * 1024;
+  static constexpr int MAX_SMEM = 227 * 1024;
   static constexpr int MAX_STAGES = 12;
-  static constexpr int NBUF = (512 / (BN * MINB)) < kMaxAccBufs ? (512 / (BN * MINB)) : kMaxAccBufs;
+  static constexpr int NBUF = (512 / BN) < kMaxAccBufs ? (512 / BN) : kMaxAccBufs;
   static constexpr int TMEM_COLS = NBUF * BN;
   // Stages that fit beside the shared-memory stack levels a tree of E levels needs.
   static __host__ __device__ int stages_for(int E) {
@@ -84,10 +83,8 @@ __device__ __forceinline__ uint32_t node2(uint32_t a, uint32_t b) { return add_b
 
 struct Bars {  // must fit in TcGeo::BAR_BYTES
   uint64_t full[12], empty[12], accf[kMaxAccBufs], acce[kMaxAccBufs], fin;  // up to 12 stages
-  uint64_t epi;  // epilogue-warps rendezvous (split-K tickets)
   uint32_t tmem_slot;
   int abort;
-  int last;
 };
 
 // Bounded wait that also gives up when another role has aborted.
@@ -112,16 +109,13 @@ namespace {
 
 struct TcArgs {
   int R, C;
-  int L, G, E;      // leaves per unit (one K block), bottom group size, levels per unit
-  int nb;           // K blocks per output tile (split-K by aligned subtrees); 1 = whole K
+  int L, G, E;      // leaves, bottom group size, levels above the groups
   int nstage;
   int num_m, num_n;
   int np;           // problems in this launch (1 or 2; the second uses tmA2/tmB2 and out2)
   uint16_t* out;
   uint16_t* out2;
   long long ld_r, ld_c;
-  uint16_t* part;   // nb > 1: block roots [nb][R][C] (scratch)
-  unsigned* cnt;    // nb > 1: one ticket per tile (scratch, zero on entry and on exit)
   int* status;
   long long spin;
 };
@@ -143,60 +137,6 @@ __device__ __forceinline__ void store_cols(uint16_t* base, long long row_off, lo
   }
 }
 
-// The top of the tree over the nb (a power of two, <= 16) block roots of one
-// row's 2*WORDS columns starting at c0: all loads of a group of 4 columns are
-// issued before any is used (8-byte vectors when the plane rows allow it).
-template <int WORDS>
-__device__ __forceinline__ void fixup_row(const uint16_t* part, long long R, long long C, int nb, long long r,
-                                          long long c0, uint32_t (&root)[WORDS]) {
-  const bool vec = (C % 4) == 0 && (((uintptr_t)part) & 7u) == 0;
-#pragma unroll
-  for (int g4 = 0; g4 < WORDS / 2; ++g4) {
-    const long long c = c0 + 4 * g4;
-    uint32_t v[16][2];
-    if (vec && c + 4 <= C) {
-#pragma unroll
-      for (int b = 0; b < 16; ++b)
-        if (b < nb) {
-          const uint2 q = __ldcg(reinterpret_cast<const uint2*>(part + ((long long)b * R + r) * C + c));
-          v[b][0] = q.x;
-          v[b][1] = q.y;
-        }
-    } else {
-#pragma unroll
-      for (int b = 0; b < 16; ++b)
-        if (b < nb) {
-          const uint16_t* p = part + ((long long)b * R + r) * C;
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const uint32_t lo = c + 2 * i < C ? (uint32_t)__ldcg(p + c + 2 * i) : 0u;
-            const uint32_t hi = c + 2 * i + 1 < C ? (uint32_t)__ldcg(p + c + 2 * i + 1) : 0u;
-            v[b][i] = lo | (hi << 16);
-          }
-        }
-    }
-#pragma unroll
-    for (int width = 16; width > 1; width >>= 1)
-      if (width <= nb)
-#pragma unroll
-        for (int b = 0; b < width / 2; ++b)
-#pragma unroll
-          for (int i = 0; i < 2; ++i) v[b][i] = node2(v[2 * b][i], v[2 * b + 1][i]);
-    root[2 * g4] = v[0][0];
-    root[2 * g4 + 1] = v[0][1];
-  }
-}
-
-// Rendezvous of the epilogue warps on an mbarrier (bounded).
-__device__ __forceinline__ bool epi_sync(Bars* bars, uint32_t& phase, long long limit, volatile int* abort_flag,
-                                         int* status, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&bars->epi);
-  const bool ok = wait_or_abort(&bars->epi, phase & 1u, limit, abort_flag, status);
-  ++phase;
-  return __all_sync(0xffffffffu, ok);
-}
-
 // Stack level m >= REG_LV lives in shared memory as [level][half][word][row].
 template <int BN>
 __device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int w, int row) {
@@ -205,7 +145,7 @@ __device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int 
 }
 
 template <int BN, int GG>
-__global__ void __launch_bounds__(TcGeo<BN>::THREADS, TcGeo<BN>::MINB)
+__global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
          const TcArgs a) {
@@ -221,7 +161,7 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, TcGeo<BN>::MINB)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = a.num_m * a.num_n;
-  const int units = tiles * a.nb * a.np;  // unit u: problem u % np, then tile and K block
+  const int units = tiles * a.np;  // unit u: problem u % np, then tile
   const long long limit = a.spin > 0 ? a.spin : kDefaultSpin;
 
   if (threadIdx.x == 0) {
@@ -234,7 +174,6 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, TcGeo<BN>::MINB)
       mbar_init(&bars->acce[b], T::EPI_WARPS);
     }
     mbar_init(&bars->fin, 1);
-    mbar_init(&bars->epi, T::EPI_WARPS);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -262,7 +201,7 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, TcGeo<BN>::MINB)
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const int pb = u % a.np, v = u / a.np;
-        const int t = v / a.nb, kb = v % a.nb;
+        const int t = v;
         const int tm = t % a.num_m, tn = t / a.num_m;
         const CUtensorMap* mA = pb ? &tmA2 : &tmA;
         const CUtensorMap* mB = pb ? &tmB2 : &tmB;
@@ -275,7 +214,7 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, TcGeo<BN>::MINB)
           }
           unsigned char* st = stages + s * T::STAGE;
           mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
-          const int x = (kb * a.L + j) * BK;
+          const int x = j * BK;
           tma_load_2d(st, mA, x, tm * BM, &bars->full[s]);
           tma_load_2d(st + T::A_BYTES, mB, x, tn * BN, &bars->full[s]);
         }
@@ -329,14 +268,11 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, TcGeo<BN>::MINB)
     long long lc = 0;
     bool ok = true;
     uint32_t reg_lv[T::REG_LV][T::WORDS];
-    uint32_t epi_phase = 0;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const int pb = u % a.np, v = u / a.np;
-      const int t = v / a.nb, kb = v % a.nb;
+      const int t = v;
       const int tm = t % a.num_m, tn = t / a.num_m;
       uint16_t* const outp = pb ? a.out2 : a.out;
-      uint16_t* const partp = a.part ? a.part + (size_t)pb * a.nb * a.R * a.C : nullptr;
-      unsigned* const cntp = a.cnt ? a.cnt + (size_t)pb * tiles : nullptr;
       const long long r = (long long)tm * BM + row;
       for (int q = 0; q < Q; ++q) {
         for (int g = 0; g < GG; ++g)
@@ -408,27 +344,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, TcGeo<BN>::MINB)
                 else *stk_at<BN>(stk, m, half, w, row) = root[w];
               }
             }
-        } else if (a.nb == 1) {
-          if (r < a.R) store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
-        } else if constexpr (BN <= 64) {
-          // A block root: to the partial plane, then the tile's ticket (split K
-          // is used only with narrow tiles, i.e. few tokens).
-          if (r < a.R)
-            store_cols(partp, ((long long)kb * a.R + r) * a.C, (long long)tn * BN + col0, 1, a.C, root);
-          __threadfence();
-          if (!epi_sync(bars, epi_phase, limit, abort_flag, a.status, lane)) { ok = false; break; }
-          if (ew == 0 && lane == 0) bars->last = (atomicAdd(&cntp[t], 1u) == (unsigned)(a.nb - 1));
-          if (!epi_sync(bars, epi_phase, limit, abort_flag, a.status, lane)) { ok = false; break; }
-          if (bars->last) {
-            // The last block of this tile: the top of the tree over the nb roots.
-            __threadfence();
-            if (r < a.R) {
-              const long long c0 = (long long)tn * BN + col0;
-              fixup_row<T::WORDS>(partp, a.R, a.C, a.nb, r, c0, root);
-              store_cols(outp, r * a.ld_r, c0, a.ld_c, a.C, root);
-            }
-            if (ew == 0 && lane == 0) cntp[t] = 0u;
-          }
+        } else if (r < a.R) {
+          store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
         }
       }
     }
@@ -485,8 +402,8 @@ cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cuda
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int units = a.num_m * a.num_n * a.nb * a.np;
-  const int slots = sm_count * TcGeo<BN>::MINB;
+  const int units = a.num_m * a.num_n * a.np;
+  const int slots = sm_count;
   const int grid = units < slots ? units : slots;
   const int smem = TcGeo<BN>::smem_for(a.E, a.nstage);
   k_tc<BN, GG><<<grid, TcGeo<BN>::THREADS, smem, st>>>(m[0], m[1], m[2], m[3], a);
@@ -531,8 +448,9 @@ bool tc_tree_shape(long long L, int* G, int* E) {
 }
 
 cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long C, long long K,
-                            long long ld_r, long long ld_c, int bn, const TcScratch& scratch, int* status,
-                            long long spin_limit, int sm_count, cudaStream_t st) {
+                            long long ld_r, long long ld_c, int* status, long long spin_limit, int sm_count,
+                            cudaStream_t st) {
+  constexpr int bn = 128;
   if (R <= 0 || C <= 0) return cudaSuccess;
   if (np < 1 || np > 2) return cudaErrorInvalidValue;
   const long long L = (K + BK - 1) / BK;
@@ -549,28 +467,15 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   a.np = np;
   a.num_m = (int)((R + BM - 1) / BM);
   a.num_n = (int)((C + bn - 1) / bn);
-  const long long tiles = (long long)a.num_m * a.num_n;
-  // Split K into nb aligned subtrees (blocks of L/nb leaves, still G * 2^e)
-  // while there are fewer than two units per SM and scratch for them.
-  int nb = 1;
-  while (bn <= 64 && nb < 16 && 2 * nb <= (1 << E) && tiles * nb * np < 4ll * sm_count &&
-         scratch.part && scratch.cnt && (size_t)(2 * nb) * np * (size_t)R * (size_t)C <= scratch.part_elems &&
-         (size_t)(tiles * np) <= scratch.cnt_elems)
-    nb *= 2;
-  a.nb = nb;
-  int e = 0;
-  while ((1 << e) < nb) ++e;
-  a.E = E - e;
-  a.L = (int)(L / nb);
+  a.E = E;
+  a.L = (int)L;
   a.out = pr[0].out;
   a.out2 = np > 1 ? pr[1].out : nullptr;
   a.ld_r = ld_r;
   a.ld_c = ld_c;
-  a.part = nb > 1 ? scratch.part : nullptr;
-  a.cnt = nb > 1 ? scratch.cnt : nullptr;
   a.status = status;
   a.spin = spin_limit;
-  a.nstage = bn == 32 ? TcGeo<32>::stages_for(a.E) : bn == 64 ? TcGeo<64>::stages_for(a.E) : TcGeo<128>::stages_for(a.E);
+  a.nstage = TcGeo<bn>::stages_for(a.E);
   if (a.nstage < 2) return cudaErrorInvalidValue;
   CUtensorMap m[4];
   for (int p = 0; p < 2; ++p) {
@@ -578,20 +483,14 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
     if (!tc_make_map(&m[2 * p], q.A, R, K, q.lda, BM) || !tc_make_map(&m[2 * p + 1], q.B, C, K, q.ldb, bn))
       return cudaErrorInvalidValue;
   }
-  switch (bn) {
-    case 32: return launch_bn<32>(m, a, sm_count, st);
-    case 64: return launch_bn<64>(m, a, sm_count, st);
-    case 128: return launch_bn<128>(m, a, sm_count, st);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_bn<bn>(m, a, sm_count, st);
 }
 
 cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
                            long long R, long long C, long long K, uint16_t* out, long long ld_r,
-                           long long ld_c, int bn, const TcScratch& scratch, int* status,
-                           long long spin_limit, int sm_count, cudaStream_t st) {
+                           long long ld_c, int* status, long long spin_limit, int sm_count, cudaStream_t st) {
   const TcProblem p{A, lda, B, ldb, out};
-  return launch_tc_gemms(&p, 1, R, C, K, ld_r, ld_c, bn, scratch, status, spin_limit, sm_count, st);
+  return launch_tc_gemms(&p, 1, R, C, K, ld_r, ld_c, status, spin_limit, sm_count, st);
 }
 
 }  // namespace detffn

@@ -62,9 +62,13 @@ constexpr int kTopThreads = BM * kTopWords;  // one thread per (row, token pair)
 // Pieces per segment staged in shared memory at a time: fused gate/up CTAs
 // (two segments, about seven pieces each at decode sizes; four CTAs per SM)
 // and plain CTAs (one segment, up to a few dozen pieces).
-__host__ __device__ constexpr int top_chunk(bool fused) { return fused ? 16 : 32; }
-__host__ __device__ constexpr int top_smem_fixed(bool fused) {
-  return (fused ? 2 : 1) * top_chunk(fused) * kTopThreads * 4 + 3 * 2 * kTopWords * (BM + 8) * 2;
+__host__ __device__ constexpr int top_chunk(bool fused) { return fused ? 8 : 32; }
+// Dynamic shared memory of a top CTA: staged pieces, the fold stacks (E
+// levels), the output tiles and the piece lists.
+__host__ __device__ inline int top_smem(bool fused, int E, int cap) {
+  const int nseg = fused ? 2 : 1;
+  return nseg * top_chunk(fused) * kTopThreads * 4 + nseg * E * kTopThreads * 4 + 3 * 2 * kTopWords * (BM + 8) * 2 +
+         2 * (32 * cap + 1) * 8;
 }
 
 static_assert(kTcsMaxLv >= REG_LV, "stack levels");
@@ -239,6 +243,9 @@ __global__ void __maxnreg__(128)
         const int t = (int)(s / a.np), pb = (int)(s % a.np);
         const CUtensorMap* mW = pb ? &tmW2 : &tmW;
         const CUtensorMap* mX = pb ? &tmX2 : &tmX;
+        // Weights are read once: evict them first, so that the pieces stay in L2.
+        uint64_t pol;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
         for (int j = qa * GG; j < qb * GG; ++j, ++it) {
           if ((int)(it % kProd) != warp) continue;
           const int st = (int)(it % NS);
@@ -248,7 +255,7 @@ __global__ void __maxnreg__(128)
           }
           unsigned char* dst = stages + st * STAGE;
           mbar_arrive_expect_tx(&bars->full[st], (uint32_t)STAGE);
-          tma_load_2d(dst, mW, j * BK, t * BM, &bars->full[st]);
+          tma_load_2d_hint(dst, mW, j * BK, t * BM, &bars->full[st], pol);
           tma_load_2d(dst + A_BYTES, mX, j * BK, 0, &bars->full[st]);
         }
         w = s * Q + qb;
@@ -636,12 +643,11 @@ template <bool FUSED>
 __global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
   constexpr int NSEG = FUSED ? 2 : 1;
   constexpr int CH = top_chunk(FUSED);
-  extern __shared__ __align__(16) unsigned char top_smem[];
-  __shared__ uint32_t stacks[NSEG][kTcsMaxLv][kTopThreads];
-  uint32_t* bufs = reinterpret_cast<uint32_t*>(top_smem);  // NSEG x [CH][kTopThreads]
-  uint16_t* tiles = reinterpret_cast<uint16_t*>(top_smem + NSEG * CH * kTopThreads * 4);  // 3 x [2 kTopWords][BM + 8]
-  PieceRef* lists =
-      reinterpret_cast<PieceRef*>(top_smem + NSEG * CH * kTopThreads * 4 + 3 * 2 * kTopWords * (BM + 8) * 2);
+  extern __shared__ __align__(16) unsigned char top_sm[];
+  uint32_t* bufs = reinterpret_cast<uint32_t*>(top_sm);     // NSEG x [CH][kTopThreads]
+  uint32_t* stacks = bufs + NSEG * CH * kTopThreads;         // NSEG x [E][kTopThreads]
+  uint16_t* tiles = reinterpret_cast<uint16_t*>(stacks + NSEG * a.E * kTopThreads);  // 3 x [2 kTopWords][BM + 8]
+  PieceRef* lists = reinterpret_cast<PieceRef*>(tiles + 3 * 2 * kTopWords * (BM + 8));
   const int row = threadIdx.x % BM, wl = threadIdx.x / BM;
   const int word = kTopWords * blockIdx.y + wl;
   const bool active = 2 * word < a.R;
@@ -662,7 +668,7 @@ __global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
     f[g].b = first_cta(a, s0 + g);
     f[g].n = lists[g * stride + 32 * a.cap].slot;
     f[g].root = 0;
-    f[g].stk = &stacks[g][0][threadIdx.x];
+    f[g].stk = stacks + (g * a.E) * kTopThreads + threadIdx.x;
     if (active) stage_pieces<CH>(a, lists + g * stride, 0, f[g].n, row, word, bufs + g * CH * kTopThreads);
   }
   staged_wait();
@@ -752,7 +758,7 @@ bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool 
   }
   r.cap = cap;
   // Top kernel: staged pieces, output tiles, piece lists (the larger of its two modes).
-  r.top_smem = top_smem_fixed(false) + 2 * (32 * cap + 1) * (int)sizeof(PieceRef);
+  r.top_smem = top_smem(false, E, cap) > top_smem(true, E, cap) ? top_smem(false, E, cap) : top_smem(true, E, cap);
   if (r.top_smem > 200 * 1024) return false;
   r.scratch = (size_t)r.P * cap * PIECE * 2;
   *p = r;
@@ -848,9 +854,9 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   t.h = h;
   t.silu = silu;
   const dim3 grid(h ? plan.T : plan.np * plan.T, (plan.R + 2 * kTopWords - 1) / (2 * kTopWords));
-  const int top_smem = top_smem_fixed(h != nullptr) + 2 * (32 * plan.cap + 1) * (int)sizeof(PieceRef);
-  return h ? launch_dependent(k_tcs_top<true>, grid, kTopThreads, top_smem, st, t)
-           : launch_dependent(k_tcs_top<false>, grid, kTopThreads, top_smem, st, t);
+  const int smem_top = top_smem(h != nullptr, plan.E, plan.cap);
+  return h ? launch_dependent(k_tcs_top<true>, grid, kTopThreads, smem_top, st, t)
+           : launch_dependent(k_tcs_top<false>, grid, kTopThreads, smem_top, st, t);
 }
 
 }  // namespace

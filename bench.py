@@ -352,6 +352,16 @@ def run_ours(args):
 
     extra["fwd_us_M32_tensor"] = 1e3 * max_over_ranks(ws_n, timed(fwd_tc, args.steps, args.warmup))
     extra["fwd_gbs_M32_tensor"] = fwd_bytes(M_DEC) / (extra["fwd_us_M32_tensor"] * 1e-6) / 1e9
+    # Each family at the other decode sizes (AUTO takes one of them by M).
+    for M in (1, 8):
+        for name, pth in (("tensor", G.PATH_TENSOR), ("exact", G.PATH_EXACT)):
+            wsm = G.workspace(G.OP_FORWARD, M, H, I, 1, pth)
+            us_m = 1e3 * max_over_ranks(ws_n, timed(
+                lambda i, M=M, pth=pth, wsm=wsm: G.detffn_forward(copies[i & 1]["x"][:M], copies[i & 1]["Wg"],
+                                                                  copies[i & 1]["Wu"], copies[i & 1]["Wd"],
+                                                                  out=outs[M], ws=wsm, path=pth),
+                args.steps, args.warmup))
+            extra["fwd_us_M%d_%s" % (M, name)] = us_m
     if not args.no_large:
         extra.update(large_training(G, args, ws_n, timed))
 

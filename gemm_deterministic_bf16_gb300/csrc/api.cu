@@ -177,13 +177,13 @@ detffn_status read_opts(const detffn_options* o, Opts* out) {
 
 // The kernel family a call uses.  EXACT: CUDA-core kernels with LANE8x8
 // leaves (bit-identical to the oracle).  TENSOR: tcgen05 leaves.  AUTO takes
-// TENSOR for M > 8 tokens when the tensor kernel covers every contraction
+// TENSOR for M > 1 token when the tensor kernels cover every contraction
 // length of the call (H, I, I/k and M leaves of the form 1, 2^d or 3*2^d, and
-// H, I multiples of 8), else EXACT (M <= 8 stays on the exact weight-streaming
-// kernels, which run near HBM speed there).  It never depends on the shard
-// count or the chunking: a shard of I has the same leaf-count form as I.
+// H, I multiples of 8), else EXACT: at one token both stream the weights at
+// the same speed and EXACT gives the oracle's bits.  It never depends on the
+// shard count or the chunking: a shard of I has the same leaf-count form as I.
 enum Family { kExact = 0, kTensor = 1 };
-constexpr long long kAutoExactMaxM = 8;
+constexpr long long kAutoExactMaxM = 1;
 
 bool tc_len_ok(long long K) {
   int G, E;

@@ -639,8 +639,10 @@ __device__ __forceinline__ void put_tile(uint16_t* tile, int row, int wl, uint32
 // flight) and folded from there.  Launched as a programmatic dependent of the
 // streaming kernel: the piece lists (arithmetic only) are built before
 // waiting for its results.
+// Six CTAs per SM (at most 40 registers) so that the 768 CTAs of the M = 32
+// gate/up top run in one wave.
 template <bool FUSED>
-__global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
+__global__ void __launch_bounds__(kTopThreads, 6) k_tcs_top(const TcsTopArgs a) {
   constexpr int NSEG = FUSED ? 2 : 1;
   constexpr int CH = top_chunk(FUSED);
   extern __shared__ __align__(16) unsigned char top_sm[];
@@ -811,10 +813,12 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     }
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_tcs_top<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_tcs_top<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    void (*tops[2])(TcsTopArgs) = {k_tcs_top<false>, k_tcs_top<true>};
+    for (auto k : tops) {
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    }
     if (e != cudaSuccess) return e;
     attr = true;
   }

@@ -61,10 +61,12 @@ typedef enum {
 
 typedef enum { DETFFN_F32 = 0, DETFFN_F16 = 1, DETFFN_BF16 = 2 } detffn_dtype;
 
-/* Kernel family.  AUTO picks TENSOR for M > 8 tokens when the tensor kernels
+/* Kernel family.  AUTO picks TENSOR for M > 1 token when the tensor kernels
  * cover the call's contraction lengths (64-wide leaf counts of the form 1, 2^d
  * or 3*2^d, H and I multiples of 8, 16-byte-aligned tensors), else EXACT; it
- * never depends on the shard count or the chunking.  EXACT runs CUDA-core kernels whose leaves follow the LANE8x8 in-leaf
+ * never depends on the shard count or the chunking, and the bits of a token's
+ * result may differ between token counts that pick different families.
+ * EXACT runs CUDA-core kernels whose leaves follow the LANE8x8 in-leaf
  * order (8 groups of 8 contiguous positions, each summed in ascending order
  * with fused multiply-adds from +0, then ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)));
  * their results are bit-identical to a CPU evaluation of the same tree.

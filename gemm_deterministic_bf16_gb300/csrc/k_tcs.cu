@@ -65,10 +65,11 @@ constexpr int kTopThreads = BM * kTopWords;  // one thread per (row, token pair)
 __host__ __device__ constexpr int top_chunk(bool fused) { return fused ? 8 : 32; }
 // Dynamic shared memory of a top CTA: staged pieces, the fold stacks (E
 // levels), the output tiles and the piece lists.
+constexpr int kPieceRefBytes = 8;  // sizeof(PieceRef), checked where it is defined
 __host__ __device__ inline int top_smem(bool fused, int E, int cap) {
   const int nseg = fused ? 2 : 1;
   return nseg * top_chunk(fused) * kTopThreads * 4 + nseg * E * kTopThreads * 4 + 3 * 2 * kTopWords * (BM + 8) * 2 +
-         2 * (32 * cap + 1) * 8;
+         2 * (32 * cap + 1) * kPieceRefBytes;
 }
 
 static_assert(kTcsMaxLv >= REG_LV, "stack levels");
@@ -226,14 +227,36 @@ __global__ void __maxnreg__(128)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
-  // Programmatic dependent launch: the set-up above overlaps the previous
-  // kernel; nothing below touches global memory before it has completed.
-  grid_dep_wait();
+  // Programmatic dependent launch: the set-up above, and the weight tiles of
+  // the first stages, overlap the previous kernel; nothing else touches
+  // global memory before it has completed (grid_dep_wait).
   grid_dep_launch();
 
   if (warp < kProd) {
     // ---------------- TMA producers: leaf it goes to producer it % kProd ----------------
     if (lane == 0) {
+      // Weights are read once: evict them first, so that the pieces stay in L2.
+      uint64_t pol;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+      // Before the previous kernel has finished: this producer's share of the
+      // first NS stages, weight tiles only (no kernel here writes weights).
+      {
+        long long it = 0;
+        for (long long w = w0; w < w1 && it < NS;) {
+          const long long s = w / Q;
+          const int qa = (int)(w - s * Q);
+          const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
+          const int t = (int)(s / a.np), pb = (int)(s % a.np);
+          const CUtensorMap* mW = pb ? &tmW2 : &tmW;
+          for (int j = qa * GG; j < qb * GG && it < NS; ++j, ++it) {
+            if ((int)(it % kProd) != warp) continue;
+            mbar_arrive_expect_tx(&bars->full[it], (uint32_t)STAGE);
+            tma_load_2d_hint(stages + it * STAGE, mW, j * BK, t * BM, &bars->full[it], pol);
+          }
+          w = s * Q + qb;
+        }
+      }
+      grid_dep_wait();  // the token tiles may be the previous kernel's output
       long long it = 0;
       bool ok = true;
       for (long long w = w0; w < w1 && ok;) {
@@ -243,19 +266,18 @@ __global__ void __maxnreg__(128)
         const int t = (int)(s / a.np), pb = (int)(s % a.np);
         const CUtensorMap* mW = pb ? &tmW2 : &tmW;
         const CUtensorMap* mX = pb ? &tmX2 : &tmX;
-        // Weights are read once: evict them first, so that the pieces stay in L2.
-        uint64_t pol;
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
         for (int j = qa * GG; j < qb * GG; ++j, ++it) {
           if ((int)(it % kProd) != warp) continue;
           const int st = (int)(it % NS);
-          if (!wait_or_abort(&bars->empty[st], (uint32_t)(((it / NS) & 1) ^ 1), limit, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
           unsigned char* dst = stages + st * STAGE;
-          mbar_arrive_expect_tx(&bars->full[st], (uint32_t)STAGE);
-          tma_load_2d_hint(dst, mW, j * BK, t * BM, &bars->full[st], pol);
+          if (it >= NS) {  // (the first NS weight tiles are already on their way)
+            if (!wait_or_abort(&bars->empty[st], (uint32_t)(((it / NS) & 1) ^ 1), limit, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->full[st], (uint32_t)STAGE);
+            tma_load_2d_hint(dst, mW, j * BK, t * BM, &bars->full[st], pol);
+          }
           tma_load_2d(dst + A_BYTES, mX, j * BK, 0, &bars->full[st]);
         }
         w = s * Q + qb;
@@ -301,6 +323,7 @@ __global__ void __maxnreg__(128)
     }
   } else {
     // ---------------- epilogue: leaves -> group roots -> pieces ----------------
+    grid_dep_wait();  // its stores may overwrite what the previous kernel reads
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
@@ -460,6 +483,7 @@ struct PieceRef {
   int at;    // level m (bits 0..7), left siblings it merges with (bits 8..15), and whether the
              // result is the root (bit 16): the fold, the same for every element, worked out once
 };
+static_assert(sizeof(PieceRef) == kPieceRefBytes, "piece list entries: shared-memory sizes assume 8 bytes");
 
 // The fold step of a piece of level m starting at group `at`, for a tile of
 // 2^E groups: it merges with the pending left siblings at levels m, m+1, ...
@@ -534,8 +558,12 @@ struct Fold {
   int n;          // pieces in the current list batch
 };
 
+// The first CTA whose range holds a group of segment s.
 __device__ __forceinline__ long long first_cta(const TcsTopArgs& a, long long s) {
-  return s * (1ll << a.E) * a.P / a.W;
+  const long long ws = s * (1ll << a.E);
+  long long b = ws * a.P / a.W;
+  if ((b + 1) * a.W / a.P <= ws) ++b;  // CTA b ends where segment s begins
+  return b;
 }
 __device__ __forceinline__ bool more_ctas(const TcsTopArgs& a, long long s, long long b) {
   return b < a.P && b * a.W / a.P < (s + 1) * (1ll << a.E);

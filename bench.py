@@ -235,19 +235,54 @@ def large_training(G, args, ws_n, timed):
     steps = max(3, args.steps // 4)
     fwd_ms = max_over_ranks(ws_n, timed(fwd, steps, 3))
     trn_ms = max_over_ranks(ws_n, timed(train, steps, 3))
+    # Weight gradients with the tokens given as c chunks in logical order (the
+    # same bits as the one-shot backward's).
+    chunked = {}
+    for c in (2, 4):
+        sl = [slice(j * M // c, (j + 1) * M // c) for j in range(c)]
+        xs, gs, us, ds = ([v[q].contiguous() for q in sl] for v in (t["x"], g, u, t["dOut"]))
+        wsc = G.workspace(G.OP_WGRAD_CHUNKED, M, H, I)
+        chunked["wgrad_chunked_ms_M4096_c%d" % c] = max_over_ranks(ws_n, timed(
+            lambda i: G.detffn_wgrad_chunked(xs, gs, us, ds, t["Wd"], dWg=dWg, dWu=dWu, dWd=dWd, ws=wsc),
+            steps, 3))
+        del xs, gs, us, ds, wsc
     G.detffn_profiling(True)
     train(0)
     prof = G.detffn_profile_read()
     G.detffn_profiling(False)
-    res = {"fwd_ms_M4096": fwd_ms, "fwd_tflops_M4096": 6 * M * H * I / (fwd_ms * 1e-3) / 1e12,
+    res = dict(chunked)
+    res.update({"fwd_ms_M4096": fwd_ms, "fwd_tflops_M4096": 6 * M * H * I / (fwd_ms * 1e-3) / 1e12,
            "fwd_bwd_ms_M4096": trn_ms, "fwd_bwd_tflops_M4096": 18 * M * H * I / (trn_ms * 1e-3) / 1e12,
            "kernels_M4096": {k: {"launches": v["launches"], "ms": v["ms"],
                                  "tflops": (v["flops"] / (v["ms"] * 1e-3) / 1e12) if v["flops"] else None,
                                  "gbs": v["bytes"] / (v["ms"] * 1e-3) / 1e9}
-                             for k, v in prof.items()}}
+                             for k, v in prof.items()}})
     del t, out, g, u, dX, dWg, dWu, dWd, wsf, wsb
     torch.cuda.empty_cache()
     return res
+
+
+def rank_tree_rows(G, args, ws_n, timed):
+    """The balanced rank tree over n buffers of S bytes: microseconds per call,
+    and for 16 MiB buffers (larger than L2 in total) GB/s of (n+1)*S bytes."""
+    import torch
+    pk, _ = peaks()
+    rows = {}
+    steps = max(5, args.steps)
+    for dt, name in ((torch.float32, "f32"), (torch.bfloat16, "bf16")):
+        esz = torch.tensor([], dtype=dt).element_size()
+        for S in (4 << 10, 1 << 20, 16 << 20):
+            for n in (2, 4, 8):
+                bufs = [torch.randn(S // esz, device="cuda").to(dt) for _ in range(n)]
+                out = torch.empty_like(bufs[0])
+                us = 1e3 * max_over_ranks(ws_n, timed(lambda i: G.detffn_rank_tree_reduce(bufs, out=out), steps, 3))
+                row = {"us": us}
+                if S >= 16 << 20:
+                    gbs = (n + 1) * S / (us * 1e-6) / 1e9
+                    row.update({"gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"]})
+                rows["%s_n%d_%dKiB" % (name, n, S >> 10)] = row
+                del bufs, out
+    return rows
 
 
 def run_ours(args):
@@ -362,6 +397,20 @@ def run_ours(args):
                                                                   out=outs[M], ws=wsm, path=pth),
                 args.steps, args.warmup))
             extra["fwd_us_M%d_%s" % (M, name)] = us_m
+    # The M=32 training step with the I axis in k=8 shards (tensor-parallel
+    # emulation: shard partials combined by the rank tree; the same bits).
+    wsf8 = G.workspace(G.OP_FORWARD_SHARDED, M_DEC, H, I, 8, path)
+    wsb8 = G.workspace(G.OP_BACKWARD, M_DEC, H, I, 8, path)
+
+    def train_step_k8(i):
+        t = copies[i & 1]
+        G.detffn_forward_sharded(t["x"], t["Wg"], t["Wu"], t["Wd"], 8, out=outs[M_DEC], gate_save=gsave,
+                                 up_save=usave, ws=wsf8, path=path)
+        G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], gsave, usave, t["dOut"], dX=dX,
+                          dWg=grads[0], dWu=grads[1], dWd=grads[2], ws=wsb8, shards=8, path=path)
+
+    extra["fwd_bwd_us_M32_k8"] = 1e3 * max_over_ranks(ws_n, timed(train_step_k8, tsteps, 3))
+    extra["rank_tree"] = rank_tree_rows(G, args, ws_n, timed)
     if not args.no_large:
         extra.update(large_training(G, args, ws_n, timed))
 

@@ -245,19 +245,48 @@ cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long 
 // copy: no arithmetic).  32x32 tiles through shared memory.
 namespace detffn {
 namespace {
-__global__ void k_transpose(const uint16_t* __restrict__ in, long long rows, long long cols, long long ld_in,
-                            uint16_t* __restrict__ out, long long ld_out) {
-  __shared__ uint16_t tile[32][34];
-  const long long r0 = (long long)blockIdx.y * 32, c0 = (long long)blockIdx.x * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
-  for (int i = ty; i < 32; i += 8) {
-    const long long r = r0 + i, c = c0 + tx;
-    if (r < rows && c < cols) tile[i][tx] = in[r * ld_in + c];
+// out[c * ld_out + r] = in[r * ld_in + c].  Tiles of 64 x 64: 16-byte loads
+// along input rows, the tile transposed through shared memory (odd row
+// stride), 16-byte stores along output rows; element-wise at ragged edges or
+// unaligned strides.
+constexpr int kTT = 64;
+__global__ void __launch_bounds__(256) k_transpose(const uint16_t* __restrict__ in, long long rows, long long cols,
+                                                   long long ld_in, uint16_t* __restrict__ out, long long ld_out,
+                                                   int vec) {
+  __shared__ uint16_t tile[kTT][kTT + 1];
+  const long long r0 = (long long)blockIdx.y * kTT, c0 = (long long)blockIdx.x * kTT;
+  const bool full = vec && r0 + kTT <= rows && c0 + kTT <= cols;
+  if (full) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {  // 64 rows x 8 vectors of 8 elements
+      const int idx = threadIdx.x + 256 * k, r = idx >> 3, cv = idx & 7;
+      const uint4 q = __ldcs(reinterpret_cast<const uint4*>(in + (r0 + r) * ld_in + c0 + 8 * cv));
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tile[r][8 * cv + j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < kTT * kTT; idx += 256) {
+      const int r = idx / kTT, c = idx % kTT;
+      if (r0 + r < rows && c0 + c < cols) tile[r][c] = in[(r0 + r) * ld_in + c0 + c];
+    }
   }
   __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const long long c = c0 + i, r = r0 + tx;
-    if (r < rows && c < cols) out[c * ld_out + r] = tile[tx][i];
+  if (full) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {  // output rows = input columns
+      const int idx = threadIdx.x + 256 * k, c = idx >> 3, rv = idx & 7;
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = (uint32_t)tile[8 * rv + 2 * j][c] | ((uint32_t)tile[8 * rv + 2 * j + 1][c] << 16);
+      __stcs(reinterpret_cast<uint4*>(out + (c0 + c) * ld_out + r0 + 8 * rv), make_uint4(w[0], w[1], w[2], w[3]));
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < kTT * kTT; idx += 256) {
+      const int c = idx / kTT, r = idx % kTT;
+      if (r0 + r < rows && c0 + c < cols) out[(c0 + c) * ld_out + r0 + r] = tile[r][c];
+    }
   }
 }
 }  // namespace
@@ -265,9 +294,11 @@ __global__ void k_transpose(const uint16_t* __restrict__ in, long long rows, lon
 cudaError_t launch_transpose(const uint16_t* in, long long rows, long long cols, long long ld_in,
                              uint16_t* out, long long ld_out, cudaStream_t st) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const long long gy = (rows + 31) / 32, gx = (cols + 31) / 32;
+  const long long gy = (rows + kTT - 1) / kTT, gx = (cols + kTT - 1) / kTT;
   if (gy > 65535 || gx > 2147483647ll) return cudaErrorInvalidValue;
-  k_transpose<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, st>>>(in, rows, cols, ld_in, out, ld_out);
+  // 16-byte vectors need 16-byte aligned rows in both layouts.
+  const int vec = (ld_in % 8 == 0) && (ld_out % 8 == 0) && (((uintptr_t)in | (uintptr_t)out) & 15u) == 0;
+  k_transpose<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, st>>>(in, rows, cols, ld_in, out, ld_out, vec);
   return cudaGetLastError();
 }
 }  // namespace detffn

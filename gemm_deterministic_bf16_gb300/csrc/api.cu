@@ -248,6 +248,10 @@ bool tcs_plan_fit(long long R, long long C, long long K, int np, int sms, const 
   return tcs_plan(R, C, K, np, 2 * sms, true, p);
 }
 
+// Row stride of the transposed [., M] token tensors: a multiple of 8 elements
+// (16 bytes), as tensor-core operands need; the padding is never read.
+long long tok_ld(long long M) { return (M + 7) / 8 * 8; }
+
 struct FwdWs {
   uint16_t *gate, *up, *h, *parts, *dec_part;
   unsigned* dec_cnt;
@@ -294,11 +298,12 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool
     w.WdT = a.take<uint16_t>(I * H);
     w.WgT = a.take<uint16_t>(H * I);
     w.WuT = a.take<uint16_t>(H * I);
-    w.dOT = a.take<uint16_t>(H * M);
-    w.xT = a.take<uint16_t>(H * M);
-    w.hT = a.take<uint16_t>(I * M);
-    w.dGT = a.take<uint16_t>(I * M);
-    w.dUT = a.take<uint16_t>(I * M);
+    const long long ldm = tok_ld(M);
+    w.dOT = a.take<uint16_t>(H * ldm);
+    w.xT = a.take<uint16_t>(H * ldm);
+    w.hT = a.take<uint16_t>(I * ldm);
+    w.dGT = a.take<uint16_t>(I * ldm);
+    w.dUT = a.take<uint16_t>(I * ldm);
     if (M >= 1 && M <= 32) {  // dh over K = H; cg, cu over K = I / k
       const size_t d1 = tcs_bytes(I, H, 1, sms), d2 = tcs_bytes(H, I / k, 1, sms);
       w.tcs.bytes = d1 > d2 ? d1 : d2;
@@ -325,11 +330,12 @@ ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tenso
   w.h = a.take<uint16_t>(M * I);
   if (tensor) {
     w.WdT = a.take<uint16_t>(I * H);
-    w.dOT = a.take<uint16_t>(H * M);
-    w.xT = a.take<uint16_t>(H * M);
-    w.hT = a.take<uint16_t>(I * M);
-    w.dGT = a.take<uint16_t>(I * M);
-    w.dUT = a.take<uint16_t>(I * M);
+    const long long ldm = tok_ld(M);
+    w.dOT = a.take<uint16_t>(H * ldm);
+    w.xT = a.take<uint16_t>(H * ldm);
+    w.hT = a.take<uint16_t>(I * ldm);
+    w.dGT = a.take<uint16_t>(I * ldm);
+    w.dUT = a.take<uint16_t>(I * ldm);
     w.tcs.bytes = tcs_bytes(I, H, 1, sms);
     w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
   }
@@ -426,10 +432,15 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
                [&] { return cu(launch_tree_gemm_exact(A, B, R, C, K, out, o_rs, st)); });
 }
 
+// out[c * ld_out + r] = in[r * ld_in + c] (ld_out = rows when not given).
+detffn_status transpose(detffn_handle h, const uint16_t* in, long long rows, long long cols,
+                        long long ld_in, uint16_t* out, long long ld_out, cudaStream_t st) {
+  return timed(h, st, "transpose", 4.0 * rows * cols, 0.0,
+               [&] { return cu(launch_transpose(in, rows, cols, ld_in, out, ld_out, st)); });
+}
 detffn_status transpose(detffn_handle h, const uint16_t* in, long long rows, long long cols,
                         long long ld_in, uint16_t* out, cudaStream_t st) {
-  return timed(h, st, "transpose", 4.0 * rows * cols, 0.0,
-               [&] { return cu(launch_transpose(in, rows, cols, ld_in, out, rows, st)); });
+  return transpose(h, in, rows, cols, ld_in, out, rows, st);
 }
 
 detffn_status silu_mul(detffn_handle h, const uint16_t* g, const uint16_t* u, uint16_t* hh,
@@ -778,14 +789,15 @@ detffn_status wgrads(detffn_handle h, Family f, const uint16_t* x, const uint16_
                      uint16_t* dWu, uint16_t* dWd, long long M, long long H, long long I,
                      const TokT& tt, cudaStream_t st) {
   if (f == kTensor) {
-    TRY(transpose(h, dOut, M, H, H, tt.dOT, st));
-    TRY(transpose(h, x, M, H, H, tt.xT, st));
-    TRY(transpose(h, hh, M, I, I, tt.hT, st));
-    TRY(transpose(h, dG, M, I, I, tt.dGT, st));
-    TRY(transpose(h, dU, M, I, I, tt.dUT, st));
-    TRY(tree_gemm(h, f, Strided{tt.dOT, M, 1}, Strided{tt.hT, M, 1}, H, I, M, dWd, I, st));
-    TRY(tree_gemm(h, f, Strided{tt.dGT, M, 1}, Strided{tt.xT, M, 1}, I, H, M, dWg, H, st));
-    return tree_gemm(h, f, Strided{tt.dUT, M, 1}, Strided{tt.xT, M, 1}, I, H, M, dWu, H, st);
+    const long long ldm = tok_ld(M);
+    TRY(transpose(h, dOut, M, H, H, tt.dOT, ldm, st));
+    TRY(transpose(h, x, M, H, H, tt.xT, ldm, st));
+    TRY(transpose(h, hh, M, I, I, tt.hT, ldm, st));
+    TRY(transpose(h, dG, M, I, I, tt.dGT, ldm, st));
+    TRY(transpose(h, dU, M, I, I, tt.dUT, ldm, st));
+    TRY(tree_gemm(h, f, Strided{tt.dOT, ldm, 1}, Strided{tt.hT, ldm, 1}, H, I, M, dWd, I, st));
+    TRY(tree_gemm(h, f, Strided{tt.dGT, ldm, 1}, Strided{tt.xT, ldm, 1}, I, H, M, dWg, H, st));
+    return tree_gemm(h, f, Strided{tt.dUT, ldm, 1}, Strided{tt.xT, ldm, 1}, I, H, M, dWu, H, st);
   }
   // dWd[n, i] = T_m(dOut[m, n], h[m, i])
   TRY(tree_gemm(h, f, Strided{dOut, 1, H}, Strided{hh, 1, I}, H, I, M, dWd, I, st));

@@ -291,6 +291,24 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
         constexpr int CW = 16;
         constexpr int WC = CW / 2;  // packed words per chunk
         uint32_t root[T::WORDS];
+        if constexpr (GG == 1) {
+          // A lone leaf (one-leaf trees: weight gradients over few tokens):
+          // all columns read with one wait, each rounded once.
+          static_assert(T::COLS % 32 == 0, "columns per thread");
+#pragma unroll
+          for (int c = 0; c < T::COLS / 32; c += 2) {
+            uint32_t va[32], vb[32];
+            tmem_ld32(tmem + lane_addr + b0 + (uint32_t)(col0 + 32 * c), va);
+            if (c + 1 < T::COLS / 32) tmem_ld32(tmem + lane_addr + b0 + (uint32_t)(col0 + 32 * c + 32), vb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) root[16 * c + i] = pack_bf16x2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]));
+            if (c + 1 < T::COLS / 32)
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                root[16 * c + 16 + i] = pack_bf16x2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1]));
+          }
+        } else
 #pragma unroll
         for (int c = 0; c < T::COLS / CW; ++c) {
           uint32_t v0[CW], v1[GG >= 2 ? CW : 1], v2[GG >= 3 ? CW : 1];

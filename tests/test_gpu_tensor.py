@@ -202,3 +202,21 @@ def test_tcs_pieces_equal_whole_tiles(G, M, H, I):
     G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], gate_save=g, up_save=u, path=TENSOR)
     assert mismatches(host(g), host(G.detffn_tree_gemm(t["x"], t["Wg"], path=TENSOR))) == 0
     assert mismatches(host(u), host(G.detffn_tree_gemm(t["x"], t["Wu"], path=TENSOR))) == 0
+
+
+@pytest.mark.parametrize("M", [32, 17, 8])
+def test_tc_backward_few_tokens(G, oracle_mod, M):
+    """Tensor-family backward with few tokens: the few-token contractions
+    (dh, cg, cu), the weight and token transposes (vector tiles for 32 and 8
+    tokens, element-wise for 17) and the one-leaf weight gradients.  With
+    integer-valued operands dh is exact in any leaf order and must equal the
+    oracle bit for bit; the rest follows the tolerance."""
+    H, I = 512, 1536
+    d = {"x": _ints((M, H), 11), "Wg": _ints((I, H), 12), "Wu": _ints((I, H), 13),
+         "Wd": _ints((H, I), 14), "dOut": _ints((M, H), 15)}
+    got = _fwd_bwd(G, {n: dev(v) for n, v in d.items()}, TENSOR)
+    f = oracle_mod.ffn_forward(d["x"], d["Wg"], d["Wu"], d["Wd"])
+    b = oracle_mod.ffn_backward(d["x"], d["Wg"], d["Wu"], d["Wd"], got["gate"], got["up"], d["dOut"])
+    assert mismatches(got["dh"], b["dh"]) == 0
+    for n in ["dX", "dWg", "dWu", "dWd"]:
+        assert _stats(got[n], b[n])[0] <= 1e-3, n

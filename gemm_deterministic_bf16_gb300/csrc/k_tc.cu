@@ -57,19 +57,26 @@ template <int BN> struct TcGeo {
   static constexpr int REG_LV = 2;                        // stack levels kept in registers
   static constexpr int LV_BYTES = BM * BN * 2;            // one shared-memory stack level
   static constexpr int BAR_BYTES = 512;
+  // Output staging for one-leaf trees (G = 1: the weight gradients over few
+  // tokens, whose epilogue is nothing but stores; longer trees need the shared
+  // memory for stack levels and stages): per epilogue warp 32 rows x COLS
+  // columns, rows padded by 16 bytes.
+  static constexpr int STG_ROW = COLS * 2 / 16 + 1;  // 16-byte units per staged row
+  static constexpr int STG_BYTES = EPI_WARPS * 32 * STG_ROW * 16;
+  static __host__ __device__ int stg_for(int G) { return G == 1 ? STG_BYTES : 0; }
   static constexpr int MAX_SMEM = 227 * 1024;
   static constexpr int MAX_STAGES = 12;
   static constexpr int NBUF = (512 / BN) < kMaxAccBufs ? (512 / BN) : kMaxAccBufs;
   static constexpr int TMEM_COLS = NBUF * BN;
   // Stages that fit beside the shared-memory stack levels a tree of E levels needs.
-  static __host__ __device__ int stages_for(int E) {
+  static __host__ __device__ int stages_for(int G, int E) {
     const int lv = E > REG_LV ? E - REG_LV : 0;
-    int n = (MAX_SMEM - 1024 - BAR_BYTES - lv * LV_BYTES) / STAGE;
+    int n = (MAX_SMEM - 1024 - BAR_BYTES - stg_for(G) - lv * LV_BYTES) / STAGE;
     return n > MAX_STAGES ? MAX_STAGES : n;
   }
-  static __host__ __device__ int smem_for(int E, int nstage) {
+  static __host__ __device__ int smem_for(int G, int E, int nstage) {
     const int lv = E > REG_LV ? E - REG_LV : 0;
-    return 1024 + nstage * STAGE + lv * LV_BYTES + BAR_BYTES;
+    return 1024 + nstage * STAGE + lv * LV_BYTES + stg_for(G) + BAR_BYTES;
   }
 };
 
@@ -156,7 +163,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
   const int slv = a.E > T::REG_LV ? a.E - T::REG_LV : 0;
   unsigned char* stages = smem;
   uint32_t* stk = reinterpret_cast<uint32_t*>(smem + NS * T::STAGE);
-  Bars* bars = reinterpret_cast<Bars*>(smem + NS * T::STAGE + slv * T::LV_BYTES);
+  uint4* stg_all = reinterpret_cast<uint4*>(smem + NS * T::STAGE + slv * T::LV_BYTES);
+  Bars* bars = reinterpret_cast<Bars*>(smem + NS * T::STAGE + slv * T::LV_BYTES + T::stg_for(GG));
   volatile int* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -362,6 +370,37 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
                 else *stk_at<BN>(stk, m, half, w, row) = root[w];
               }
             }
+        } else if (GG == 1 && a.ld_c == 1 && (a.ld_r % 8) == 0 && (((uintptr_t)outp) & 15u) == 0) {
+          // Row-major output: this warp's 32 rows x COLS columns go through
+          // shared memory and leave as whole 16-byte row segments, eight
+          // lanes per row (coalesced), instead of 32 scattered rows per store.
+          if constexpr (GG == 1) {
+          constexpr int SEG = T::COLS / 8;  // 16-byte segments per row
+          uint4* stg = stg_all + ew * 32 * T::STG_ROW;
+#pragma unroll
+          for (int v = 0; v < SEG; ++v)
+            stg[lane * T::STG_ROW + v] = make_uint4(root[4 * v], root[4 * v + 1], root[4 * v + 2], root[4 * v + 3]);
+          __syncwarp();
+          const long long rbase = (long long)tm * BM + quarter * 32;
+          const long long cbase = (long long)tn * BN + col0;
+#pragma unroll
+          for (int k = 0; k < 32 * SEG / 32; ++k) {
+            const int rl = (k * 32 + lane) / SEG, seg = (k * 32 + lane) % SEG;
+            const long long r2 = rbase + rl, c = cbase + 8 * seg;
+            if (r2 < a.R) {
+              const uint4 v = stg[rl * T::STG_ROW + seg];
+              uint16_t* o = outp + r2 * a.ld_r + c;
+              if (c + 8 <= a.C) {
+                *reinterpret_cast<uint4*>(o) = v;
+              } else {
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                for (int i = 0; i < 8; ++i)
+                  if (c + i < a.C) o[i] = (uint16_t)(w4[i >> 1] >> (16 * (i & 1)));
+              }
+            }
+          }
+          __syncwarp();
+          }
         } else if (r < a.R) {
           store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
         }
@@ -423,7 +462,7 @@ cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cuda
   const int units = a.num_m * a.num_n * a.np;
   const int slots = sm_count;
   const int grid = units < slots ? units : slots;
-  const int smem = TcGeo<BN>::smem_for(a.E, a.nstage);
+  const int smem = TcGeo<BN>::smem_for(a.G, a.E, a.nstage);
   k_tc<BN, GG><<<grid, TcGeo<BN>::THREADS, smem, st>>>(m[0], m[1], m[2], m[3], a);
   return cudaGetLastError();
 }
@@ -493,7 +532,7 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   a.ld_c = ld_c;
   a.status = status;
   a.spin = spin_limit;
-  a.nstage = TcGeo<bn>::stages_for(a.E);
+  a.nstage = TcGeo<bn>::stages_for(a.G, a.E);
   if (a.nstage < 2) return cudaErrorInvalidValue;
   CUtensorMap m[4];
   for (int p = 0; p < 2; ++p) {

@@ -281,7 +281,7 @@ FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k, int s
 
 struct BwdWs {
   uint16_t *dh, *dU, *dG, *h, *cg, *cu, *cgs, *cus;
-  uint16_t *WdT, *WgT, *WuT, *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only
+  uint16_t *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only (token-major tensors transposed)
   TcsScratch tcs;                                          // tensor family, M <= 32
 };
 BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool tensor, int sms) {
@@ -295,9 +295,6 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool
   w.cgs = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
   w.cus = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
   if (tensor) {
-    w.WdT = a.take<uint16_t>(I * H);
-    w.WgT = a.take<uint16_t>(H * I);
-    w.WuT = a.take<uint16_t>(H * I);
     const long long ldm = tok_ld(M);
     w.dOT = a.take<uint16_t>(H * ldm);
     w.xT = a.take<uint16_t>(H * ldm);
@@ -315,7 +312,7 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool
 
 struct ChunkWs {
   uint16_t *x, *dO, *g, *u, *dh, *dU, *dG, *h;
-  uint16_t *WdT, *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only
+  uint16_t *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only
   TcsScratch tcs;                              // tensor family: dh of chunks of <= 32 tokens
 };
 ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tensor, int sms) {
@@ -329,7 +326,6 @@ ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tenso
   w.dG = a.take<uint16_t>(M * I);
   w.h = a.take<uint16_t>(M * I);
   if (tensor) {
-    w.WdT = a.take<uint16_t>(I * H);
     const long long ldm = tok_ld(M);
     w.dOT = a.take<uint16_t>(H * ldm);
     w.xT = a.take<uint16_t>(H * ldm);
@@ -404,11 +400,16 @@ detffn_status timed(detffn_handle h, cudaStream_t st, const char* name, double b
 }
 
 // One tree contraction on the chosen family.
-// Tensor family: both operands K-contiguous with 16-byte-aligned rows.  For
-// R <= 32 (few tokens) the operands swap roles (weights fill the 128-row MMA
-// side, tokens the 32-column side) and the result is stored transposed.
+// Tensor family: A K-contiguous; B K-contiguous, or C-contiguous (weights in
+// their stored [out, in] layout read along columns), which the tensor core
+// then reads MN-major; 16-byte-aligned rows either way.  For R <= 32 (few
+// tokens) the operands swap roles (weights fill the 128-row MMA side, tokens
+// the 32-column side) and the result is stored transposed.
 bool tc_operands_ok(const Strided& X) {
   return X.ks == 1 && (X.rs % 8) == 0 && (((uintptr_t)X.p) & 15u) == 0;
+}
+bool tc_mn_ok(const Strided& X) {
+  return X.ks != 1 && X.rs == 1 && (X.ks % 8) == 0 && (((uintptr_t)X.p) & 15u) == 0;
 }
 
 detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long long R, long long C,
@@ -416,16 +417,18 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
                         const TcsScratch& sc = TcsScratch()) {
   const double bytes = 2.0 * ((double)R * K + (double)C * K + (double)R * C);
   if (f == kTensor) {
-    if (!tc_operands_ok(A) || !tc_operands_ok(B)) return DETFFN_ERR_ALIGN;
+    const bool b_mn = tc_mn_ok(B);
+    if (!tc_operands_ok(A) || !(b_mn || tc_operands_ok(B))) return DETFFN_ERR_ALIGN;
+    const long long ldb = b_mn ? B.ks : B.rs;
     if (R <= 32) {  // few tokens: the weights (B) streamed on the MMA's 128-row side
       TcsPlan p;
       if (!tcs_plan_fit(R, C, K, 1, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
-      const TcsProblem pr{B.p, B.rs, A.p, A.rs, out};
+      const TcsProblem pr{B.p, ldb, A.p, A.rs, out, b_mn};
       return timed(h, st, "tcs_tree_gemm", bytes, 2.0 * R * C * K,
                    [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->d_status, 0, st)); });
     }
     return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
-      return cu(launch_tc_gemm(A.p, A.rs, B.p, B.rs, R, C, K, out, o_rs, 1, h->d_status, 0, h->sm_count, st));
+      return cu(launch_tc_gemm(A.p, A.rs, B.p, ldb, R, C, K, out, o_rs, 1, h->d_status, 0, h->sm_count, st, b_mn));
     });
   }
   return timed(h, st, "tree_gemm_exact", bytes, 2.0 * R * C * K,
@@ -770,12 +773,12 @@ namespace {
 
 // Row-wise backward stages for rows [r0, r0+rows): dh, then dU and dG.
 detffn_status rowwise_bwd(detffn_handle h, Family f, const uint16_t* dOut, const uint16_t* Wd,
-                          const uint16_t* WdT, const uint16_t* gate, const uint16_t* up,
+                          const uint16_t* gate, const uint16_t* up,
                           uint16_t* dh, uint16_t* dU, uint16_t* dG, long long rows, long long H,
                           long long I, cudaStream_t st, const TcsScratch& sc) {
   // dh[m, i] = T_{n<H}(dOut[m, n], Wd[n, i]): B row i is column i of Wd (K stride I),
-  // or row i of the transposed copy WdT [I, H] for the tensor family.
-  const Strided B = f == kTensor ? Strided{WdT, H, 1} : Strided{Wd, 1, I};
+  // (read MN-major by the tensor family).
+  const Strided B{Wd, 1, I};
   TRY(tree_gemm(h, f, Strided{dOut, H, 1}, B, rows, I, H, dh, I, st, sc));
   return silu_bwd(h, dh, gate, up, dU, dG, rows * I, st);
 }
@@ -867,25 +870,18 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   const uint16_t* U = (const uint16_t*)up;
   const uint16_t* WG = (const uint16_t*)Wg;
   const uint16_t* WU = (const uint16_t*)Wu;
-  if (f == kTensor) {  // K-contiguous copies of the weights for the NN contractions
-    TRY(transpose(h, (const uint16_t*)Wd, H, I, I, w.WdT, st));
-    TRY(transpose(h, WG, I, H, H, w.WgT, st));
-    TRY(transpose(h, WU, I, H, H, w.WuT, st));
-  }
-  TRY(rowwise_bwd(h, f, (const uint16_t*)dOut, (const uint16_t*)Wd, w.WdT, G, U, dh, dU, dG, M, H, I, st,
+  TRY(rowwise_bwd(h, f, (const uint16_t*)dOut, (const uint16_t*)Wd, G, U, dh, dU, dG, M, H, I, st,
                   w.tcs));
   // dHidden: cg = T_i(dG[m, i], Wg[i, n]), cu = T_i(dU[m, i], Wu[i, n]); the two
   // trees stay separate until the final gate-then-up addition.  B row n is
-  // column n of Wg (K stride H), or row n of WgT [H, I] for the tensor family.
-  auto wcol = [&](const uint16_t* W, const uint16_t* WT, long long s0) {
-    return f == kTensor ? Strided{WT + s0, I, 1} : Strided{W + s0 * H, 1, H};
-  };
+  // column n of Wg (K stride H), read MN-major by the tensor family.
+  auto wcol = [&](const uint16_t* W, long long s0) { return Strided{W + s0 * H, 1, H}; };
   const long long sw = I / k;
   for (long long s = 0; s < k; ++s) {
     uint16_t* cg = k == 1 ? w.cg : w.cgs + s * M * H;
     uint16_t* cu = k == 1 ? w.cu : w.cus + s * M * H;
-    TRY(tree_gemm(h, f, Strided{dG + s * sw, I, 1}, wcol(WG, w.WgT, s * sw), M, H, sw, cg, H, st, w.tcs));
-    TRY(tree_gemm(h, f, Strided{dU + s * sw, I, 1}, wcol(WU, w.WuT, s * sw), M, H, sw, cu, H, st, w.tcs));
+    TRY(tree_gemm(h, f, Strided{dG + s * sw, I, 1}, wcol(WG, s * sw), M, H, sw, cg, H, st, w.tcs));
+    TRY(tree_gemm(h, f, Strided{dU + s * sw, I, 1}, wcol(WU, s * sw), M, H, sw, cu, H, st, w.tcs));
   }
   if (k > 1) {
     const void *pg[8], *pu[8];
@@ -948,7 +944,6 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
   }
   Arena a(ws);
   ChunkWs w = plan_chunked(a, M, H, I, f == kTensor, h->sm_count);
-  if (f == kTensor) TRY(transpose(h, (const uint16_t*)Wd, H, I, I, w.WdT, st));
   // Gather the chunks in logical token order, then run the row-wise stages
   // chunk by chunk on their own rows.
   long long r0 = 0;
@@ -959,7 +954,7 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
     TRYCU(cudaMemcpyAsync(w.dO + r0 * H, dOut_chunks[c], (size_t)(2 * t * H), cudaMemcpyDeviceToDevice, st));
     TRYCU(cudaMemcpyAsync(w.g + r0 * I, gate_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
     TRYCU(cudaMemcpyAsync(w.u + r0 * I, up_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
-    TRY(rowwise_bwd(h, f, w.dO + r0 * H, (const uint16_t*)Wd, w.WdT, w.g + r0 * I, w.u + r0 * I,
+    TRY(rowwise_bwd(h, f, w.dO + r0 * H, (const uint16_t*)Wd, w.g + r0 * I, w.u + r0 * I,
                     w.dh + r0 * I, w.dU + r0 * I, w.dG + r0 * I, t, H, I, st, w.tcs));
     TRY(silu_mul(h, w.g + r0 * I, w.u + r0 * I, w.h + r0 * I, t, I, I, st));
     r0 += t;
@@ -1004,7 +999,7 @@ extern "C" detffn_status detffn_tree_gemm(detffn_handle h, const void* A, long l
   Family f = kExact;
   const Strided SA{(const uint16_t*)A, a_rs, a_ks}, SB{(const uint16_t*)B, b_rs, b_ks};
   if (o.path == DETFFN_PATH_TENSOR || (o.path == DETFFN_PATH_AUTO && R > kAutoExactMaxM)) {
-    const bool ok = tc_len_ok(K) && tc_operands_ok(SA) && tc_operands_ok(SB);
+    const bool ok = tc_len_ok(K) && tc_operands_ok(SA) && (tc_operands_ok(SB) || tc_mn_ok(SB));
     if (ok) f = kTensor;
     else if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_UNSUPPORTED;
   }

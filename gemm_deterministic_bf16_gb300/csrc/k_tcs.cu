@@ -99,6 +99,7 @@ struct TcsArgs {
   long long W;      // groups in all: np * T * 2^E
   int cap;          // piece slots per CTA
   int nstage;
+  int w_mn;         // weights stored [K][C] (C contiguous): MN-major A tiles
   uint16_t* slots;  // [gridDim.x][cap][BM][BN]; null: direct mode
   uint16_t* out0;   // direct mode: roots go to out_p[r * ldo + c]
   uint16_t* out1;
@@ -178,6 +179,18 @@ __device__ __forceinline__ void emit_piece(uint16_t* slots, int& n, int cap, int
 namespace detffn {
 namespace {
 
+// The weight tile of leaf j, row tile t: 128 rows x 64 K, K-major (one box)
+// or, for weights stored [K][C], MN-major (two boxes of 64 rows x 64 K).
+__device__ __forceinline__ void load_w(unsigned char* dst, const CUtensorMap* mW, int j, int t, uint64_t* bar,
+                                       uint64_t pol, int mn) {
+  if (mn) {
+    tma_load_2d_hint(dst, mW, t * BM, j * BK, bar, pol);
+    tma_load_2d_hint(dst + A_BYTES / 2, mW, t * BM + BM / 2, j * BK, bar, pol);
+  } else {
+    tma_load_2d_hint(dst, mW, j * BK, t * BM, bar, pol);
+  }
+}
+
 // The streaming kernel.  Each role walks the CTA's groups in the same order:
 // segment (tile, problem) after segment, groups qa..qb-1 of each.
 // 128 registers: registers are granted per 4 warps, so a CTA of 7 warps holds
@@ -251,7 +264,7 @@ __global__ void __maxnreg__(128)
           for (int j = qa * GG; j < qb * GG && it < NS; ++j, ++it) {
             if ((int)(it % kProd) != warp) continue;
             mbar_arrive_expect_tx(&bars->full[it], (uint32_t)STAGE);
-            tma_load_2d_hint(stages + it * STAGE, mW, j * BK, t * BM, &bars->full[it], pol);
+            load_w(stages + it * STAGE, mW, j, t, &bars->full[it], pol, a.w_mn);
           }
           w = s * Q + qb;
         }
@@ -276,7 +289,7 @@ __global__ void __maxnreg__(128)
               break;
             }
             mbar_arrive_expect_tx(&bars->full[st], (uint32_t)STAGE);
-            tma_load_2d_hint(dst, mW, j * BK, t * BM, &bars->full[st], pol);
+            load_w(dst, mW, j, t, &bars->full[st], pol, a.w_mn);
           }
           tma_load_2d(dst + A_BYTES, mX, j * BK, 0, &bars->full[st]);
         }
@@ -289,7 +302,8 @@ __global__ void __maxnreg__(128)
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, BN);
+      const uint32_t idesc = idesc_bf16(BM, BN) | (a.w_mn ? kIdescTransA : 0u);
+      const uint32_t astep = a.w_mn ? 128u : 2u;  // K = 16 step in descriptor units
       long long it = 0;
       bool ok = true;
       for (long long w = w0; w < w1 && ok;) {
@@ -308,11 +322,11 @@ __global__ void __maxnreg__(128)
             break;
           }
           tc_fence_after();
-          const uint64_t da = smem_desc_sw128(stages + st * STAGE);
+          const uint64_t da = a.w_mn ? smem_desc_sw128_mn(stages + st * STAGE) : smem_desc_sw128(stages + st * STAGE);
           const uint64_t db = smem_desc_sw128(stages + st * STAGE + A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
-            tc_mma_bf16(tmem + (uint32_t)(b * BN), da + 2 * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+            tc_mma_bf16(tmem + (uint32_t)(b * BN), da + astep * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
           tc_commit(&bars->empty[st]);
           tc_commit(&bars->accf[b]);
         }
@@ -822,12 +836,15 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
     return cudaErrorInvalidValue;
   if (plan.direct && h) return cudaErrorInvalidValue;
   for (int p = 0; p < plan.np; ++p)
-    if ((pr[p].ldw % 8) || (pr[p].ldx % 8) || ((uintptr_t)pr[p].W & 15u) || ((uintptr_t)pr[p].X & 15u))
+    if ((pr[p].ldw % 8) || (pr[p].ldx % 8) || ((uintptr_t)pr[p].W & 15u) || ((uintptr_t)pr[p].X & 15u) ||
+        pr[p].w_mn != pr[0].w_mn)
       return cudaErrorInvalidValue;
   CUtensorMap m[4];
   for (int p = 0; p < 2; ++p) {
     const TcsProblem& q = pr[p < plan.np ? p : 0];
-    if (!tc_make_map(&m[2 * p], q.W, plan.C, plan.K, q.ldw, BM) ||
+    const bool wmap = q.w_mn ? tc_make_map(&m[2 * p], q.W, plan.K, plan.C, q.ldw, BK)
+                             : tc_make_map(&m[2 * p], q.W, plan.C, plan.K, q.ldw, BM);
+    if (!wmap ||
         !tc_make_map(&m[2 * p + 1], q.X, plan.R, plan.K, q.ldx, BN))
       return cudaErrorInvalidValue;
   }
@@ -860,6 +877,7 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   a.W = plan.W;
   a.cap = plan.cap;
   a.nstage = plan.nstage;
+  a.w_mn = pr[0].w_mn ? 1 : 0;
   a.slots = plan.direct ? nullptr : static_cast<uint16_t*>(scratch);
   a.out0 = pr[0].out;
   a.out1 = plan.np > 1 ? pr[1].out : nullptr;

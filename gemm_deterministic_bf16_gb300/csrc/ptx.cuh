@@ -195,6 +195,25 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(const void* p) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile of 128 (MN) x
+// 64 (K), stored as two 128-byte-swizzled boxes of 64 (MN) x 64 (K), one per
+// 64 MN elements: leading byte offset 8 KB (from one 64-wide MN block to the
+// next), stride byte offset 1 KB (from one group of 8 K rows to the next).
+// A K step of 16 advances the start address by 16 rows of 128 B (+128 in the
+// descriptor's 16-byte units).  (Checked against a CPU product on this GPU.)
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(const void* p) {
+  const uint64_t addr = smem_u32(p);
+  uint64_t d = 0;
+  d |= (addr >> 4) & 0x3FFFull;
+  d |= (uint64_t)(8192 >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+constexpr uint32_t kIdescTransA = 1u << 15;  // A is MN-major
+constexpr uint32_t kIdescTransB = 1u << 16;  // B is MN-major
+
 // Instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B, both
 // K-major, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {

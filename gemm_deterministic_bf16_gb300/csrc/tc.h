@@ -16,9 +16,10 @@ bool tc_tree_shape(long long L, int* G, int* E);
 struct TcProblem {
   const uint16_t* A;
   long long lda;
-  const uint16_t* B;
+  const uint16_t* B;  // [C, K] (row stride ldb); with b_mn, [K, C] (C contiguous)
   long long ldb;
   uint16_t* out;
+  bool b_mn = false;  // B read MN-major (no transposed copy needed)
 };
 
 // Up to two same-shaped contractions in one launch (their tiles interleave).
@@ -28,10 +29,13 @@ cudaError_t launch_tc_gemms(const TcProblem* problems, int np, long long R, long
 
 // out[r*ld_r + c*ld_c] = T_K(A[r, :], B[c, :]) for r < R, c < C; A and B are
 // K-contiguous BF16 with row strides lda, ldb (elements, multiples of 8) and
-// 16-byte-aligned bases; output tiles of 128 x 128, one CTA per SM.
+// 16-byte-aligned bases; output tiles of 128 x 128, one CTA per SM.  With
+// b_mn, B is given as [K, C] with C contiguous (row stride ldb) and read
+// MN-major by the tensor core.
 cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
                            long long R, long long C, long long K, uint16_t* out, long long ld_r,
-                           long long ld_c, int* status, long long spin_limit, int sm_count, cudaStream_t st);
+                           long long ld_c, int* status, long long spin_limit, int sm_count, cudaStream_t st,
+                           bool b_mn = false);
 
 // A 2-D BF16 tensor map over rows x K (row stride ld elements), 128-byte
 // swizzle, boxes of 64 (K) x box_rows.
@@ -59,11 +63,12 @@ struct TcsPlan {
 bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* plan);
 
 struct TcsProblem {
-  const uint16_t* W;  // [C, K] weights, row stride ldw (multiple of 8), 16-byte aligned
-  long long ldw;
+  const uint16_t* W;  // [C, K] weights, row stride ldw (multiple of 8), 16-byte aligned;
+  long long ldw;      //   with w_mn, [K, C] (C contiguous), row stride ldw
   const uint16_t* X;  // [R, K] tokens, row stride ldx (multiple of 8), 16-byte aligned
   long long ldx;
   uint16_t* out;      // out[r * ldo + c]
+  bool w_mn = false;  // weights read MN-major (no transposed copy needed)
 };
 
 // One or two same-shaped contractions (plan.np): two launches on `st`, or one

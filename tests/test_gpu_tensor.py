@@ -220,3 +220,17 @@ def test_tc_backward_few_tokens(G, oracle_mod, M):
     assert mismatches(got["dh"], b["dh"]) == 0
     for n in ["dX", "dWg", "dWu", "dWd"]:
         assert _stats(got[n], b[n])[0] <= 1e-3, n
+
+
+@pytest.mark.parametrize("R,C,K", [(1, 256, 4096), (32, 200, 768), (17, 384, 256), (200, 296, 1024), (256, 128, 64)])
+def test_tc_weights_mn_major_bit_exact(G, oracle_mod, R, C, K):
+    """B given as a column view of a [K, C] matrix (C contiguous, as the
+    backward reads Wd, Wg and Wu) is read MN-major by the tensor core, with no
+    transposed copy: with integer-valued operands the result must equal the
+    oracle bit for bit (few-token and many-token kernels, ragged C)."""
+    A = _ints((R, K), R + 5)
+    Bt = _ints((K, C), C + 9)                   # stored [K, C]
+    B_view = dev(Bt).t()                        # logical [C, K], strides (1, C)
+    assert B_view.stride() == (1, C)
+    got = host(G.detffn_tree_gemm(dev(A), B_view, path=TENSOR))
+    assert mismatches(got, oracle_mod.tree_gemm(A, np.ascontiguousarray(Bt.T))) == 0

@@ -248,10 +248,6 @@ bool tcs_plan_fit(long long R, long long C, long long K, int np, int sms, const 
   return tcs_plan(R, C, K, np, 2 * sms, true, p);
 }
 
-// Row stride of the transposed [., M] token tensors: a multiple of 8 elements
-// (16 bytes), as tensor-core operands need; the padding is never read.
-long long tok_ld(long long M) { return (M + 7) / 8 * 8; }
-
 struct FwdWs {
   uint16_t *gate, *up, *h, *parts, *dec_part;
   unsigned* dec_cnt;
@@ -281,8 +277,7 @@ FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k, int s
 
 struct BwdWs {
   uint16_t *dh, *dU, *dG, *h, *cg, *cu, *cgs, *cus;
-  uint16_t *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only (token-major tensors transposed)
-  TcsScratch tcs;                                          // tensor family, M <= 32
+  TcsScratch tcs;  // tensor family, M <= 32
 };
 BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool tensor, int sms) {
   BwdWs w{};
@@ -295,12 +290,6 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool
   w.cgs = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
   w.cus = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
   if (tensor) {
-    const long long ldm = tok_ld(M);
-    w.dOT = a.take<uint16_t>(H * ldm);
-    w.xT = a.take<uint16_t>(H * ldm);
-    w.hT = a.take<uint16_t>(I * ldm);
-    w.dGT = a.take<uint16_t>(I * ldm);
-    w.dUT = a.take<uint16_t>(I * ldm);
     if (M >= 1 && M <= 32) {  // dh over K = H; cg, cu over K = I / k
       const size_t d1 = tcs_bytes(I, H, 1, sms), d2 = tcs_bytes(H, I / k, 1, sms);
       w.tcs.bytes = d1 > d2 ? d1 : d2;
@@ -312,8 +301,7 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool
 
 struct ChunkWs {
   uint16_t *x, *dO, *g, *u, *dh, *dU, *dG, *h;
-  uint16_t *dOT, *xT, *hT, *dGT, *dUT;  // tensor family only
-  TcsScratch tcs;                              // tensor family: dh of chunks of <= 32 tokens
+  TcsScratch tcs;  // tensor family: dh of chunks of <= 32 tokens
 };
 ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tensor, int sms) {
   ChunkWs w{};
@@ -326,12 +314,6 @@ ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tenso
   w.dG = a.take<uint16_t>(M * I);
   w.h = a.take<uint16_t>(M * I);
   if (tensor) {
-    const long long ldm = tok_ld(M);
-    w.dOT = a.take<uint16_t>(H * ldm);
-    w.xT = a.take<uint16_t>(H * ldm);
-    w.hT = a.take<uint16_t>(I * ldm);
-    w.dGT = a.take<uint16_t>(I * ldm);
-    w.dUT = a.take<uint16_t>(I * ldm);
     w.tcs.bytes = tcs_bytes(I, H, 1, sms);
     w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
   }
@@ -417,8 +399,9 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
                         const TcsScratch& sc = TcsScratch()) {
   const double bytes = 2.0 * ((double)R * K + (double)C * K + (double)R * C);
   if (f == kTensor) {
-    const bool b_mn = tc_mn_ok(B);
-    if (!tc_operands_ok(A) || !(b_mn || tc_operands_ok(B))) return DETFFN_ERR_ALIGN;
+    const bool b_mn = tc_mn_ok(B), a_mn = tc_mn_ok(A);
+    if (!(a_mn || tc_operands_ok(A)) || !(b_mn || tc_operands_ok(B))) return DETFFN_ERR_ALIGN;
+    if (a_mn && R <= 32) return DETFFN_ERR_UNSUPPORTED;  // the few-token kernel takes K-major tokens
     const long long ldb = b_mn ? B.ks : B.rs;
     if (R <= 32) {  // few tokens: the weights (B) streamed on the MMA's 128-row side
       TcsPlan p;
@@ -428,22 +411,12 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
                    [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->d_status, 0, st)); });
     }
     return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
-      return cu(launch_tc_gemm(A.p, A.rs, B.p, ldb, R, C, K, out, o_rs, 1, h->d_status, 0, h->sm_count, st, b_mn));
+      return cu(launch_tc_gemm(A.p, a_mn ? A.ks : A.rs, B.p, ldb, R, C, K, out, o_rs, 1, h->d_status, 0,
+                               h->sm_count, st, b_mn, a_mn));
     });
   }
   return timed(h, st, "tree_gemm_exact", bytes, 2.0 * R * C * K,
                [&] { return cu(launch_tree_gemm_exact(A, B, R, C, K, out, o_rs, st)); });
-}
-
-// out[c * ld_out + r] = in[r * ld_in + c] (ld_out = rows when not given).
-detffn_status transpose(detffn_handle h, const uint16_t* in, long long rows, long long cols,
-                        long long ld_in, uint16_t* out, long long ld_out, cudaStream_t st) {
-  return timed(h, st, "transpose", 4.0 * rows * cols, 0.0,
-               [&] { return cu(launch_transpose(in, rows, cols, ld_in, out, ld_out, st)); });
-}
-detffn_status transpose(detffn_handle h, const uint16_t* in, long long rows, long long cols,
-                        long long ld_in, uint16_t* out, cudaStream_t st) {
-  return transpose(h, in, rows, cols, ld_in, out, rows, st);
 }
 
 detffn_status silu_mul(detffn_handle h, const uint16_t* g, const uint16_t* u, uint16_t* hh,
@@ -783,25 +756,12 @@ detffn_status rowwise_bwd(detffn_handle h, Family f, const uint16_t* dOut, const
   return silu_bwd(h, dh, gate, up, dU, dG, rows * I, st);
 }
 
-// Transposed [., M] copies of the token-major stage tensors (tensor family).
-struct TokT { uint16_t *dOT, *xT, *hT, *dGT, *dUT; };
-
-// Weight gradients over K = M tokens from row-major [M, .] stage tensors.
+// Weight gradients over K = M tokens from row-major [M, .] stage tensors (the
+// tensor family reads both operands MN-major: no transposed copies).
 detffn_status wgrads(detffn_handle h, Family f, const uint16_t* x, const uint16_t* dOut,
                      const uint16_t* hh, const uint16_t* dU, const uint16_t* dG, uint16_t* dWg,
                      uint16_t* dWu, uint16_t* dWd, long long M, long long H, long long I,
-                     const TokT& tt, cudaStream_t st) {
-  if (f == kTensor) {
-    const long long ldm = tok_ld(M);
-    TRY(transpose(h, dOut, M, H, H, tt.dOT, ldm, st));
-    TRY(transpose(h, x, M, H, H, tt.xT, ldm, st));
-    TRY(transpose(h, hh, M, I, I, tt.hT, ldm, st));
-    TRY(transpose(h, dG, M, I, I, tt.dGT, ldm, st));
-    TRY(transpose(h, dU, M, I, I, tt.dUT, ldm, st));
-    TRY(tree_gemm(h, f, Strided{tt.dOT, ldm, 1}, Strided{tt.hT, ldm, 1}, H, I, M, dWd, I, st));
-    TRY(tree_gemm(h, f, Strided{tt.dGT, ldm, 1}, Strided{tt.xT, ldm, 1}, I, H, M, dWg, H, st));
-    return tree_gemm(h, f, Strided{tt.dUT, ldm, 1}, Strided{tt.xT, ldm, 1}, I, H, M, dWu, H, st);
-  }
+                     cudaStream_t st) {
   // dWd[n, i] = T_m(dOut[m, n], h[m, i])
   TRY(tree_gemm(h, f, Strided{dOut, 1, H}, Strided{hh, 1, I}, H, I, M, dWd, I, st));
   // dWg[i, n] = T_m(dG[m, i], x[m, n]); dWu likewise with dU.
@@ -895,7 +855,7 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   TRY(add_bf16(h, w.cg, w.cu, (uint16_t*)dX, M * H, st));
   TRY(silu_mul(h, G, U, w.h, M, I, I, st));
   return wgrads(h, f, (const uint16_t*)x, (const uint16_t*)dOut, w.h, dU, dG, (uint16_t*)dWg,
-                (uint16_t*)dWu, (uint16_t*)dWd, M, H, I, TokT{w.dOT, w.xT, w.hT, w.dGT, w.dUT}, st);
+                (uint16_t*)dWu, (uint16_t*)dWd, M, H, I, st);
 }
 
 extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
@@ -960,7 +920,7 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
     r0 += t;
   }
   return wgrads(h, f, w.x, w.dO, w.h, w.dU, w.dG, (uint16_t*)dWg, (uint16_t*)dWu, (uint16_t*)dWd,
-                M, H, I, TokT{w.dOT, w.xT, w.hT, w.dGT, w.dUT}, st);
+                M, H, I, st);
 }
 
 extern "C" detffn_status detffn_rank_tree_reduce(const void* const* inputs, int n, void* out,
@@ -999,7 +959,8 @@ extern "C" detffn_status detffn_tree_gemm(detffn_handle h, const void* A, long l
   Family f = kExact;
   const Strided SA{(const uint16_t*)A, a_rs, a_ks}, SB{(const uint16_t*)B, b_rs, b_ks};
   if (o.path == DETFFN_PATH_TENSOR || (o.path == DETFFN_PATH_AUTO && R > kAutoExactMaxM)) {
-    const bool ok = tc_len_ok(K) && tc_operands_ok(SA) && (tc_operands_ok(SB) || tc_mn_ok(SB));
+    const bool ok = tc_len_ok(K) && (tc_operands_ok(SA) || (tc_mn_ok(SA) && R > 32)) &&
+                    (tc_operands_ok(SB) || tc_mn_ok(SB));
     if (ok) f = kTensor;
     else if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_UNSUPPORTED;
   }

@@ -68,8 +68,7 @@ cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_
 cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out, long long n,
                             cudaStream_t st);
 // out[c*ld_out + r] = in[r*ld_in + c] (a copy).
-cudaError_t launch_transpose(const uint16_t* in, long long rows, long long cols, long long ld_in,
-                             uint16_t* out, long long ld_out, cudaStream_t st);
+
 // Self-check: counts pairs where add.rn.bf16x2 differs from the tree node.
 cudaError_t launch_check_node_add(unsigned long long begin, unsigned long long end, unsigned long long* bad,
                                   int sm_count, cudaStream_t st);

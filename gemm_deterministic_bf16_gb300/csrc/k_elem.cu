@@ -240,87 +240,6 @@ cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long 
 
 }  // namespace detffn
 
-// ----------------------------- transpose ----------------------------------
-// out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols (BF16, a pure
-// copy: no arithmetic).  32x32 tiles through shared memory.
-namespace detffn {
-namespace {
-// out[c * ld_out + r] = in[r * ld_in + c].  Tiles of 64 rows x 128 columns.
-// A thread loads 16 bytes of two adjacent input rows and pairs them into
-// eight 32-bit words, each two consecutive elements of one output row; the
-// words of output row c sit in shared memory at word (r/2) ^ swz(c), an XOR
-// swizzle that spreads a warp's 32 stores over the 32 banks; output rows then
-// leave as 16-byte stores.  A tile's rows may be fewer than 64 (token-major
-// tensors of 32 tokens) when they are a multiple of 8.  Element-wise at
-// ragged edges or unaligned strides.
-constexpr int kTR = 64, kTC = 128;
-__device__ __forceinline__ int tr_swz(int c) { return ((c >> 3) & 15) << 1; }
-__global__ void __launch_bounds__(256) k_transpose(const uint16_t* __restrict__ in, long long rows, long long cols,
-                                                   long long ld_in, uint16_t* __restrict__ out, long long ld_out,
-                                                   int vec) {
-  __shared__ __align__(16) uint32_t words[kTC][kTR / 2];
-  const long long r0 = (long long)blockIdx.y * kTR, c0 = (long long)blockIdx.x * kTC;
-  const int nr = rows - r0 < kTR ? (int)(rows - r0) : kTR;  // rows of this tile
-  const bool full = vec && (nr % 8) == 0 && c0 + kTC <= cols;
-  if (full) {
-    uint4 qa[2], qb[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {  // 32 row pairs x 16 vectors of 8 columns
-      const int idx = threadIdx.x + 256 * k, cv = idx & 15, rp = idx >> 4;
-      if (2 * rp < nr) {
-        const uint16_t* p = in + (r0 + 2 * rp) * ld_in + c0 + 8 * cv;
-        qa[k] = __ldcs(reinterpret_cast<const uint4*>(p));
-        qb[k] = __ldcs(reinterpret_cast<const uint4*>(p + ld_in));
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int idx = threadIdx.x + 256 * k, cv = idx & 15, rp = idx >> 4;
-      if (2 * rp >= nr) continue;
-      const uint32_t a[4] = {qa[k].x, qa[k].y, qa[k].z, qa[k].w}, b[4] = {qb[k].x, qb[k].y, qb[k].z, qb[k].w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t lo = (a[j >> 1] >> (16 * (j & 1))) & 0xFFFFu, hi = (b[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-        words[8 * cv + j][rp ^ (2 * cv)] = lo | (hi << 16);
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {  // 128 output rows x 8 vectors
-      const int idx = threadIdx.x + 256 * k, q = idx & 7, c = idx >> 3;
-      if (8 * q >= nr) continue;
-      const int sw = tr_swz(c);
-      uint4 v = *reinterpret_cast<const uint4*>(&words[c][(4 * q) ^ (sw & ~3)]);
-      if (sw & 2) v = make_uint4(v.z, v.w, v.x, v.y);  // words 0,1 <-> 2,3 of the block
-      __stcs(reinterpret_cast<uint4*>(out + (c0 + c) * ld_out + r0 + 8 * q), v);
-    }
-  } else {
-    uint16_t* tile = reinterpret_cast<uint16_t*>(&words[0][0]);  // [kTR][kTC]
-    for (int idx = threadIdx.x; idx < kTR * kTC; idx += 256) {
-      const int r = idx / kTC, c = idx % kTC;
-      if (r0 + r < rows && c0 + c < cols) tile[r * kTC + c] = in[(r0 + r) * ld_in + c0 + c];
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < kTR * kTC; idx += 256) {
-      const int c = idx / kTR, r = idx % kTR;
-      if (r0 + r < rows && c0 + c < cols) out[(c0 + c) * ld_out + r0 + r] = tile[r * kTC + c];
-    }
-  }
-}
-}  // namespace
-
-cudaError_t launch_transpose(const uint16_t* in, long long rows, long long cols, long long ld_in,
-                             uint16_t* out, long long ld_out, cudaStream_t st) {
-  if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const long long gy = (rows + kTR - 1) / kTR, gx = (cols + kTC - 1) / kTC;
-  if (gy > 65535 || gx > 2147483647ll) return cudaErrorInvalidValue;
-  // 16-byte vectors need 16-byte aligned rows in both layouts.
-  const int vec = (ld_in % 8 == 0) && (ld_out % 8 == 0) && (((uintptr_t)in | (uintptr_t)out) & 15u) == 0;
-  k_transpose<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, st>>>(in, rows, cols, ld_in, out, ld_out, vec);
-  return cudaGetLastError();
-}
-}  // namespace detffn
-
 // ------------------- self-check of the packed node add --------------------
 // Counts BF16 pairs (a, b) for which add.rn.bf16x2 differs from the tree
 // node rne_bf16(fp32(a) + fp32(b)); every NaN result counts as equal to every

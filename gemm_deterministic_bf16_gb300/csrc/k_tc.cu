@@ -121,6 +121,7 @@ struct TcArgs {
   int num_m, num_n;
   int np;           // problems in this launch (1 or 2; the second uses tmA2/tmB2 and out2)
   int b_mn;         // B stored [K][C] (C contiguous): MN-major B tiles (BN = 128 only)
+  int a_mn;         // A stored [K][R] (R contiguous): MN-major A tiles
   uint16_t* out;
   uint16_t* out2;
   long long ld_r, ld_c;
@@ -224,7 +225,12 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
           unsigned char* st = stages + s * T::STAGE;
           mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
           const int x = j * BK;
-          tma_load_2d(st, mA, x, tm * BM, &bars->full[s]);
+          if (a.a_mn) {  // two boxes of 64 (R) x 64 (K)
+            tma_load_2d(st, mA, tm * BM, x, &bars->full[s]);
+            tma_load_2d(st + T::A_BYTES / 2, mA, tm * BM + BM / 2, x, &bars->full[s]);
+          } else {
+            tma_load_2d(st, mA, x, tm * BM, &bars->full[s]);
+          }
           if (a.b_mn) {  // two boxes of 64 (C) x 64 (K)
             tma_load_2d(st + T::A_BYTES, mB, tn * BN, x, &bars->full[s]);
             tma_load_2d(st + T::A_BYTES + T::B_BYTES / 2, mB, tn * BN + BN / 2, x, &bars->full[s]);
@@ -240,8 +246,9 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, BN) | (a.b_mn ? kIdescTransB : 0u);
+      const uint32_t idesc = idesc_bf16(BM, BN) | (a.b_mn ? kIdescTransB : 0u) | (a.a_mn ? kIdescTransA : 0u);
       const uint32_t bstep = a.b_mn ? 128u : 2u;  // K = 16 step in descriptor units
+      const uint32_t astep = a.a_mn ? 128u : 2u;
       long long it = 0, lc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
@@ -259,12 +266,12 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t da = smem_desc_sw128(stages + s * T::STAGE);
+          const uint64_t da = a.a_mn ? smem_desc_sw128_mn(stages + s * T::STAGE) : smem_desc_sw128(stages + s * T::STAGE);
           const uint64_t db = a.b_mn ? smem_desc_sw128_mn(stages + s * T::STAGE + T::A_BYTES)
                                      : smem_desc_sw128(stages + s * T::STAGE + T::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
-            tc_mma_bf16(tmem + (uint32_t)(b * BN), da + 2 * kk, db + bstep * kk, idesc, kk > 0 ? 1u : 0u);
+            tc_mma_bf16(tmem + (uint32_t)(b * BN), da + astep * kk, db + bstep * kk, idesc, kk > 0 ? 1u : 0u);
           tc_commit(&bars->empty[s]);
           tc_commit(&bars->accf[b]);
         }
@@ -531,7 +538,8 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   a.G = G;
   a.np = np;
   a.b_mn = pr[0].b_mn ? 1 : 0;
-  if (np > 1 && pr[1].b_mn != pr[0].b_mn) return cudaErrorInvalidValue;
+  a.a_mn = pr[0].a_mn ? 1 : 0;
+  if (np > 1 && (pr[1].b_mn != pr[0].b_mn || pr[1].a_mn != pr[0].a_mn)) return cudaErrorInvalidValue;
   a.num_m = (int)((R + BM - 1) / BM);
   a.num_n = (int)((C + bn - 1) / bn);
   a.E = E;
@@ -549,7 +557,8 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
     const TcProblem& q = pr[p < np ? p : 0];
     const bool bmap = q.b_mn ? tc_make_map(&m[2 * p + 1], q.B, K, C, q.ldb, BK)
                              : tc_make_map(&m[2 * p + 1], q.B, C, K, q.ldb, bn);
-    if (!tc_make_map(&m[2 * p], q.A, R, K, q.lda, BM) || !bmap)
+    const bool amap = q.a_mn ? tc_make_map(&m[2 * p], q.A, K, R, q.lda, BK) : tc_make_map(&m[2 * p], q.A, R, K, q.lda, BM);
+    if (!amap || !bmap)
       return cudaErrorInvalidValue;
   }
   return launch_bn<bn>(m, a, sm_count, st);
@@ -558,8 +567,8 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
 cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
                            long long R, long long C, long long K, uint16_t* out, long long ld_r,
                            long long ld_c, int* status, long long spin_limit, int sm_count, cudaStream_t st,
-                           bool b_mn) {
-  const TcProblem p{A, lda, B, ldb, out, b_mn};
+                           bool b_mn, bool a_mn) {
+  const TcProblem p{A, lda, B, ldb, out, b_mn, a_mn};
   return launch_tc_gemms(&p, 1, R, C, K, ld_r, ld_c, status, spin_limit, sm_count, st);
 }
 

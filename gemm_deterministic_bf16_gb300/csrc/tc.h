@@ -20,6 +20,7 @@ struct TcProblem {
   long long ldb;
   uint16_t* out;
   bool b_mn = false;  // B read MN-major (no transposed copy needed)
+  bool a_mn = false;  // A given as [K, R] (R contiguous, row stride lda), read MN-major
 };
 
 // Up to two same-shaped contractions in one launch (their tiles interleave).
@@ -30,12 +31,13 @@ cudaError_t launch_tc_gemms(const TcProblem* problems, int np, long long R, long
 // out[r*ld_r + c*ld_c] = T_K(A[r, :], B[c, :]) for r < R, c < C; A and B are
 // K-contiguous BF16 with row strides lda, ldb (elements, multiples of 8) and
 // 16-byte-aligned bases; output tiles of 128 x 128, one CTA per SM.  With
-// b_mn, B is given as [K, C] with C contiguous (row stride ldb) and read
+// b_mn, B is given as [K, C] with C contiguous (row stride ldb), with a_mn, A
+// as [K, R] with R contiguous (row stride lda); such operands are read
 // MN-major by the tensor core.
 cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
                            long long R, long long C, long long K, uint16_t* out, long long ld_r,
                            long long ld_c, int* status, long long spin_limit, int sm_count, cudaStream_t st,
-                           bool b_mn = false);
+                           bool b_mn = false, bool a_mn = false);
 
 // A 2-D BF16 tensor map over rows x K (row stride ld elements), 128-byte
 // swizzle, boxes of 64 (K) x box_rows.

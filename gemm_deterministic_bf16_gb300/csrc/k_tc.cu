@@ -15,11 +15,15 @@
 //
 // Roles (one CTA per SM, persistent over output tiles of 128 x BN):
 //   warp 0      TMA producer: A and B tiles of one leaf per pipeline stage
-//               (128-byte swizzle, K-major), a ring of stages on mbarriers (as many
-//               as fit beside the shared-memory stack levels);
+//               (128-byte swizzle, K- or MN-major), a ring of up to 512/BN
+//               stages on mbarriers (as many as fit beside the shared-memory
+//               stack levels); a stage is reused once the leaf read from it
+//               has been committed;
 //   warp 1      allocates TMEM (512/BN leaf buffers of BN columns) and issues
-//               the MMAs, one leaf per buffer, committing to the stage's
-//               "empty" barrier and the buffer's "full" barrier;
+//               the MMAs, one leaf per buffer, with one commit per leaf (the
+//               buffer's "full" barrier, which the producer reads too);
+//   warps 10..  further MMA issuers (leaves are dealt round-robin over the
+//               issuers; see kIssuers);
 //   warps 2-9   epilogue: each thread owns one row (TMEM lane) and BN/2
 //               columns; it reads a group's leaves from TMEM, forms the
 //               group roots, returns the buffers at once, and then folds the
@@ -41,6 +45,15 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kMaxAccBufs = 16;  // TMEM leaf buffers: 512 columns / BN (at most 16)
 constexpr int kEpiWarp0 = 2;  // warp 0: producer, warp 1: MMA, warps 2..: epilogue
+#ifndef DETFFN_TC_ISSUERS
+#define DETFFN_TC_ISSUERS 3
+#endif
+// MMA-issuing warps: warp 1 and the warps after the epilogue's.  Issuer q
+// takes leaves q, q + kIssuers, ...: each leaf costs its issuing thread a
+// commit and two barrier waits of a few hundred cycles of latency, more than
+// the 4 MMAs of a 128 x 128 leaf keep the tensor pipe busy, so one issuer
+// alone leaves the pipe idle between leaves.
+constexpr int kIssuers = DETFFN_TC_ISSUERS;
 constexpr int kMaxLv = 6;  // up to Q = 64 bottom groups
 
 // One CTA per SM, 8 epilogue warps (two per TMEM lane quarter, BN/2 columns
@@ -48,7 +61,7 @@ constexpr int kMaxLv = 6;  // up to Q = 64 bottom groups
 template <int BN> struct TcGeo {
   static constexpr int EPI_WARPS = 8;
   static constexpr int HALVES = EPI_WARPS / 4;            // epilogue warps per lane quarter
-  static constexpr int THREADS = 32 * (kEpiWarp0 + EPI_WARPS);
+  static constexpr int THREADS = 32 * (kEpiWarp0 + EPI_WARPS + kIssuers - 1);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
@@ -89,7 +102,7 @@ __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0
 __device__ __forceinline__ uint32_t node2(uint32_t a, uint32_t b) { return add_bf16x2(a, b); }
 
 struct Bars {  // must fit in TcGeo::BAR_BYTES
-  uint64_t full[12], empty[12], accf[kMaxAccBufs], acce[kMaxAccBufs], fin;  // up to 12 stages
+  uint64_t full[12], accf[kMaxAccBufs], acce[kMaxAccBufs], fin;  // up to 12 stages
   uint32_t tmem_slot;
   int abort;
 };
@@ -177,13 +190,12 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
     }
     for (int b = 0; b < T::NBUF; ++b) {
       mbar_init(&bars->accf[b], 1);
       mbar_init(&bars->acce[b], T::EPI_WARPS);
     }
-    mbar_init(&bars->fin, 1);
+    mbar_init(&bars->fin, kIssuers);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -205,23 +217,31 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
   const uint32_t tmem = bars->tmem_slot;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      long long it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const int pb = u % a.np, v = u / a.np;
-        const int t = v;
-        const int tm = t % a.num_m, tn = t / a.num_m;
-        const CUtensorMap* mA = pb ? &tmA2 : &tmA;
-        const CUtensorMap* mB = pb ? &tmB2 : &tmB;
-        for (int j = 0; j < a.L; ++j, ++it) {
-          const int s = (int)(it % NS);
-          if (!wait_or_abort(&bars->empty[s], (uint32_t)(((it / NS) & 1) ^ 1), limit, abort_flag,
-                             a.status)) {
+    // ---------------- TMA producer (converged warp; one lane issues) ----------------
+    // Stage it % NS is free once the MMAs of leaf it - NS have completed,
+    // which the leaf's own "full accumulator" barrier reports (NS <= NBUF,
+    // so that barrier cannot have moved on by a second phase).
+    long long it = 0;
+    Ring rs;  // stage of load it
+    Ring rv;  // TMEM buffer of leaf it - NS
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int pb = u % a.np, v = u / a.np;
+      const int t = v;
+      const int tm = t % a.num_m, tn = t / a.num_m;
+      const CUtensorMap* mA = pb ? &tmA2 : &tmA;
+      const CUtensorMap* mB = pb ? &tmB2 : &tmB;
+      for (int j = 0; j < a.L; ++j, ++it, rs.next(NS)) {
+        const int s = rs.slot;
+        if (it >= NS) {
+          const bool w = wait_or_abort(&bars->accf[rv.slot], rv.phase, limit, abort_flag, a.status);
+          if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
           }
+          rv.next(T::NBUF);
+        }
+        if (elect_one()) {
           unsigned char* st = stages + s * T::STAGE;
           mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
           const int x = j * BK;
@@ -238,48 +258,60 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
             tma_load_2d(st + T::A_BYTES, mB, x, tn * BN, &bars->full[s]);
           }
         }
+        __syncwarp();
       }
-      // Drain: the last loads issued into each stage have landed.
+    }
+    // Drain: the last loads issued into each stage have landed.
+    if (lane == 0)
       for (long long i = (it > NS ? it - NS : 0); i < it; ++i)
         mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), limit, nullptr);
+  } else if (warp == 1 || warp >= kEpiWarp0 + T::EPI_WARPS) {
+    const int q = warp == 1 ? 0 : warp - (kEpiWarp0 + T::EPI_WARPS) + 1;  // issuer index
+    // ---------------- MMA issuers (converged warps; one lane each issues) ----------------
+    // Leaf n uses stage n % NS and TMEM buffer n % NBUF; one commit per leaf
+    // (its "full accumulator" barrier) tells both the epilogue and the
+    // producer.  Leaves are independent accumulations, so the issuers' MMAs
+    // may reach the tensor pipe in any order.
+    static_assert(T::NBUF >= 3, "a group of up to 3 leaves in flight");
+    const uint32_t idesc = idesc_bf16(BM, BN) | (a.b_mn ? kIdescTransB : 0u) | (a.a_mn ? kIdescTransA : 0u);
+    const uint32_t bstep = a.b_mn ? 128u : 2u;  // K = 16 step in descriptor units
+    const uint32_t astep = a.a_mn ? 128u : 2u;
+    const int mine = blockIdx.x < units ? (units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    const long long nleaf = (long long)mine * a.L;
+    Ring rs, rb;  // pipeline stage; TMEM leaf buffer
+    for (int i = 0; i < q; ++i) {
+      rs.next(NS);
+      rb.next(T::NBUF);
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, BN) | (a.b_mn ? kIdescTransB : 0u) | (a.a_mn ? kIdescTransA : 0u);
-      const uint32_t bstep = a.b_mn ? 128u : 2u;  // K = 16 step in descriptor units
-      const uint32_t astep = a.a_mn ? 128u : 2u;
-      long long it = 0, lc = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        for (int j = 0; j < a.L; ++j, ++it, ++lc) {
-          const int b = (int)(lc % T::NBUF);
-          if (!wait_or_abort(&bars->acce[b], (uint32_t)(((lc / T::NBUF) & 1) ^ 1), limit, abort_flag,
-                             a.status)) {
-            ok = false;
-            break;
-          }
-          const int s = (int)(it % NS);
-          if (!wait_or_abort(&bars->full[s], (uint32_t)((it / NS) & 1), limit, abort_flag,
-                             a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t da = a.a_mn ? smem_desc_sw128_mn(stages + s * T::STAGE) : smem_desc_sw128(stages + s * T::STAGE);
-          const uint64_t db = a.b_mn ? smem_desc_sw128_mn(stages + s * T::STAGE + T::A_BYTES)
-                                     : smem_desc_sw128(stages + s * T::STAGE + T::A_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
-            tc_mma_bf16(tmem + (uint32_t)(b * BN), da + astep * kk, db + bstep * kk, idesc, kk > 0 ? 1u : 0u);
-          tc_commit(&bars->empty[s]);
-          tc_commit(&bars->accf[b]);
-        }
+    bool ok = true;
+    for (long long n = q; n < nleaf && ok; n += kIssuers) {
+      const int s = rs.slot, b = rb.slot;
+      const bool w = wait_or_abort(&bars->acce[b], rb.phase ^ 1u, limit, abort_flag, a.status) &&
+                     wait_or_abort(&bars->full[s], rs.phase, limit, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
       }
-      tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
-      mbar_wait(&bars->fin, 0, limit, nullptr);
+      tc_fence_after();
+      const uint64_t da = a.a_mn ? smem_desc_sw128_mn(stages + s * T::STAGE) : smem_desc_sw128(stages + s * T::STAGE);
+      const uint64_t db = a.b_mn ? smem_desc_sw128_mn(stages + s * T::STAGE + T::A_BYTES)
+                                 : smem_desc_sw128(stages + s * T::STAGE + T::A_BYTES);
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
+          tc_mma_bf16(tmem + (uint32_t)(b * BN), da + astep * kk, db + bstep * kk, idesc, kk > 0 ? 1u : 0u);
+        tc_commit(&bars->accf[b]);
+      }
+      __syncwarp();
+      for (int i = 0; i < kIssuers; ++i) {
+        rs.next(NS);
+        rb.next(T::NBUF);
+      }
     }
-  } else if (warp >= kEpiWarp0) {
+    if (elect_one()) tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
+    __syncwarp();
+    if (q == 0 && lane == 0) mbar_wait(&bars->fin, 0, limit, nullptr);  // all issuers' MMAs
+  } else {
     // ---------------- epilogue: leaves -> tree ----------------
     const int ew = warp - kEpiWarp0;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
@@ -288,7 +320,7 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     const int col0 = half * T::COLS;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const int Q = 1 << a.E;
-    long long lc = 0;
+    uint32_t lc = 0;  // leaves consumed (NBUF is a power of two)
     bool ok = true;
     uint32_t reg_lv[T::REG_LV][T::WORDS];
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
@@ -551,6 +583,7 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   a.status = status;
   a.spin = spin_limit;
   a.nstage = TcGeo<bn>::stages_for(a.G, a.E);
+  if (a.nstage > TcGeo<bn>::NBUF) a.nstage = TcGeo<bn>::NBUF;  // stage reuse is read off the leaf barriers
   if (a.nstage < 2) return cudaErrorInvalidValue;
   CUtensorMap m[4];
   for (int p = 0; p < 2; ++p) {

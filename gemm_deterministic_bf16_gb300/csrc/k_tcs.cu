@@ -271,6 +271,7 @@ __global__ void __maxnreg__(128)
       }
       grid_dep_wait();  // the token tiles may be the previous kernel's output
       long long it = 0;
+      Ring rs;
       bool ok = true;
       for (long long w = w0; w < w1 && ok;) {
         const long long s = w / Q;
@@ -279,12 +280,12 @@ __global__ void __maxnreg__(128)
         const int t = (int)(s / a.np), pb = (int)(s % a.np);
         const CUtensorMap* mW = pb ? &tmW2 : &tmW;
         const CUtensorMap* mX = pb ? &tmX2 : &tmX;
-        for (int j = qa * GG; j < qb * GG; ++j, ++it) {
+        for (int j = qa * GG; j < qb * GG; ++j, ++it, rs.next(NS)) {
           if ((int)(it % kProd) != warp) continue;
-          const int st = (int)(it % NS);
+          const int st = rs.slot;
           unsigned char* dst = stages + st * STAGE;
           if (it >= NS) {  // (the first NS weight tiles are already on their way)
-            if (!wait_or_abort(&bars->empty[st], (uint32_t)(((it / NS) & 1) ^ 1), limit, abort_flag, a.status)) {
+            if (!wait_or_abort(&bars->empty[st], rs.phase ^ 1u, limit, abort_flag, a.status)) {
               ok = false;
               break;
             }
@@ -304,33 +305,33 @@ __global__ void __maxnreg__(128)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(BM, BN) | (a.w_mn ? kIdescTransA : 0u);
       const uint32_t astep = a.w_mn ? 128u : 2u;  // K = 16 step in descriptor units
-      long long it = 0;
-      bool ok = true;
-      for (long long w = w0; w < w1 && ok;) {
-        const long long s = w / Q;
-        const int qa = (int)(w - s * Q);
-        const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
-        for (int j = qa * GG; j < qb * GG; ++j, ++it) {
-          const int b = (int)(it % kNBuf);
-          if (!wait_or_abort(&bars->acce[b], (uint32_t)(((it / kNBuf) & 1) ^ 1), limit, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          const int st = (int)(it % NS);
-          if (!wait_or_abort(&bars->full[st], (uint32_t)((it / NS) & 1), limit, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t da = a.w_mn ? smem_desc_sw128_mn(stages + st * STAGE) : smem_desc_sw128(stages + st * STAGE);
-          const uint64_t db = smem_desc_sw128(stages + st * STAGE + A_BYTES);
+      // Leaf n of this CTA's range uses stage n % NS and TMEM buffer n % kNBuf.
+      // The barriers of leaf n + 1 are waited on before leaf n is committed:
+      // a wait issued after a tcgen05.commit does not return before the
+      // committed MMAs have completed, which would leave the tensor pipe idle
+      // between leaves.  (No deadlock: leaf n + 1 needs the commits of leaves
+      // up to n + 1 - NS and n + G - kNBuf only, both at most n - 1.)
+      const long long nleaf = (w1 - w0) * GG;
+      Ring rs, rb;  // pipeline stage; TMEM leaf buffer
+      auto wait_leaf = [&]() {
+        return wait_or_abort(&bars->acce[rb.slot], rb.phase ^ 1u, limit, abort_flag, a.status) &&
+               wait_or_abort(&bars->full[rs.slot], rs.phase, limit, abort_flag, a.status);
+      };
+      bool ok = nleaf > 0 && wait_leaf();
+      for (long long n = 0; n < nleaf && ok; ++n) {
+        const int st = rs.slot, b = rb.slot;
+        tc_fence_after();
+        const uint64_t da = a.w_mn ? smem_desc_sw128_mn(stages + st * STAGE) : smem_desc_sw128(stages + st * STAGE);
+        const uint64_t db = smem_desc_sw128(stages + st * STAGE + A_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
-            tc_mma_bf16(tmem + (uint32_t)(b * BN), da + astep * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-          tc_commit(&bars->empty[st]);
-          tc_commit(&bars->accf[b]);
-        }
-        w = s * Q + qb;
+        for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
+          tc_mma_bf16(tmem + (uint32_t)(b * BN), da + astep * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+        rs.next(NS);
+        rb.next(kNBuf);
+        const bool next_ok = n + 1 == nleaf || wait_leaf();
+        tc_commit(&bars->empty[st]);
+        tc_commit(&bars->accf[b]);
+        ok = next_ok;
       }
       tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
       mbar_wait(&bars->fin, 0, limit, nullptr);
@@ -342,7 +343,7 @@ __global__ void __maxnreg__(128)
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     uint16_t* const myslots = direct ? nullptr : a.slots + (size_t)blockIdx.x * a.cap * PIECE;
-    long long lc = 0;
+    uint32_t lc = 0;  // leaves consumed (kNBuf is a power of two)
     int np_out = 0;  // pieces written
     bool ok = true;
     uint32_t reg_lv[REG_LV][WORDS];

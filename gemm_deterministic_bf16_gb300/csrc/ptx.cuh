@@ -60,6 +60,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   return false;
 }
 
+// True in exactly one lane of a converged warp (the lowest active lane, the
+// same lane on every call).  Work that must come from one thread (MMA issue
+// and its commits, TMA issue) is done under it by a warp that otherwise runs
+// converged, so that the loop's operands are warp-uniform values.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p = 0;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}" : "=r"(p));
+  return p != 0;
+}
+
+// Position in a ring of n mbarrier-guarded slots: the slot and the parity of
+// its current phase, advanced by one increment per use.  (Deriving both from
+// a 64-bit use counter costs a 64-bit division by a run-time n per use, which
+// is a sizeable share of a single-thread producer's or MMA issuer's loop.)
+struct Ring {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // 1-D bulk copy global -> shared, completing `bytes` of transaction on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

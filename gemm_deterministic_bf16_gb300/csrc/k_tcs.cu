@@ -18,11 +18,11 @@
 // kernel waits on another CTA.  Without scratch ("direct" mode) CTAs take
 // whole tiles and store the roots themselves.
 //
-// Streaming.  Two CTAs per SM.  In each, two producer threads issue the TMA
-// loads of alternate leaves (one issuing thread sustains only part of an SM's
-// share of HBM bandwidth), one thread issues the MMAs (4 x K=16 per 64-wide
-// leaf into a fresh TMEM buffer), and four epilogue warps read the leaves
-// from TMEM, form the group roots and fold them.
+// Streaming.  Two CTAs per SM.  In each, two producer warps issue the TMA
+// loads of alternate leaves, one warp issues the MMAs (4 x K=16 per 64-wide
+// leaf into a fresh TMEM buffer, one commit per leaf), and four epilogue
+// warps read the leaves from TMEM, form the group roots and fold them.  The
+// producer and MMA warps run converged and issue from one elected lane.
 //
 // Every wait is bounded; on a timeout the CTA records DETFFN_ERR_TIMEOUT,
 // stops, drains its own copies and MMAs (bounded) and frees its TMEM.
@@ -56,23 +56,25 @@ constexpr int LV_BYTES = BM * WORDS * 4;
 constexpr int BAR_BYTES = 512;
 constexpr int MAX_SMEM = 113 * 1024;
 constexpr int MAX_STAGES = 8;
-constexpr int PIECE = BM * BN;    // elements of one piece: [word = token pair][row] as 32-bit words
-constexpr int kTopWords = 2;      // top kernel: token pairs per CTA (grid.y covers the rest)
-constexpr int kTopThreads = BM * kTopWords;  // one thread per (row, token pair)
+constexpr int PIECE = BM * BN;    // elements of one piece: [row][token], 64 bytes per row
+constexpr int kTopTok = 8;        // top kernel: tokens per CTA (one 16-byte quarter of a piece row; grid.y covers the rest)
+constexpr int kTopThreads = BM;   // one thread per row
 // Pieces per segment staged in shared memory at a time: fused gate/up CTAs
-// (two segments, about seven pieces each at decode sizes; four CTAs per SM)
-// and plain CTAs (one segment, up to a few dozen pieces).
+// (two segments, a few pieces each at decode sizes) and plain CTAs (one
+// segment, up to a few dozen pieces).
 __host__ __device__ constexpr int top_chunk(bool fused) { return fused ? 8 : 32; }
 // Dynamic shared memory of a top CTA: staged pieces, the fold stacks (E
-// levels), the output tiles and the piece lists.
+// levels), the output tiles and the piece lists (16 bytes per row and piece
+// or level).
 constexpr int kPieceRefBytes = 8;  // sizeof(PieceRef), checked where it is defined
 __host__ __device__ inline int top_smem(bool fused, int E, int cap) {
   const int nseg = fused ? 2 : 1;
-  return nseg * top_chunk(fused) * kTopThreads * 4 + nseg * E * kTopThreads * 4 + 3 * 2 * kTopWords * (BM + 8) * 2 +
+  return nseg * top_chunk(fused) * BM * 16 + nseg * E * BM * 16 + 3 * kTopTok * (BM + 8) * 2 +
          2 * (32 * cap + 1) * kPieceRefBytes;
 }
 
 static_assert(kTcsMaxLv >= REG_LV, "stack levels");
+static_assert(MAX_STAGES <= kNBuf, "stage reuse is read off the leaf barriers");
 
 __host__ __device__ inline int stages_for(int E) {
   const int lv = E > REG_LV ? E - REG_LV : 0;
@@ -86,7 +88,7 @@ __host__ __device__ inline int smem_for(int E, int ns) {
 }
 
 struct Bars {
-  uint64_t full[MAX_STAGES], empty[MAX_STAGES], accf[kNBuf], acce[kNBuf], fin;
+  uint64_t full[MAX_STAGES], accf[kNBuf], acce[kNBuf], fin;
   uint32_t tmem_slot;
   int abort;
 };
@@ -162,13 +164,13 @@ __host__ __device__ inline int count_pieces(int x, int y) {
   return p.one ? 1 : popc((unsigned)(p.z - x)) + popc((unsigned)(y - p.z));
 }
 
-// Writes one row (all tokens) of the CTA's next piece: word i of the row at
-// [i][row], so that a warp's rows of one word are one contiguous line.
+// Writes one row (all tokens) of the CTA's next piece: the row's 64 bytes
+// at [row], so that the top kernel reads a quarter row with one 16-byte load.
 __device__ __forceinline__ void emit_piece(uint16_t* slots, int& n, int cap, int row, const uint32_t (&v)[WORDS]) {
   if (n < cap) {
-    uint32_t* o = reinterpret_cast<uint32_t*>(slots + (size_t)n * PIECE) + row;
+    uint4* o = reinterpret_cast<uint4*>(slots + (size_t)n * PIECE) + row * (WORDS / 4);
 #pragma unroll
-    for (int i = 0; i < WORDS; ++i) o[i * BM] = v[i];
+    for (int i = 0; i < WORDS / 4; ++i) o[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
   }
   ++n;
 }
@@ -218,7 +220,6 @@ __global__ void __maxnreg__(128)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
     }
     for (int b = 0; b < kNBuf; ++b) {
       mbar_init(&bars->accf[b], 1);
@@ -247,95 +248,108 @@ __global__ void __maxnreg__(128)
 
   if (warp < kProd) {
     // ---------------- TMA producers: leaf it goes to producer it % kProd ----------------
-    if (lane == 0) {
-      // Weights are read once: evict them first, so that the pieces stay in L2.
-      uint64_t pol;
-      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-      // Before the previous kernel has finished: this producer's share of the
-      // first NS stages, weight tiles only (no kernel here writes weights).
-      {
-        long long it = 0;
-        for (long long w = w0; w < w1 && it < NS;) {
-          const long long s = w / Q;
-          const int qa = (int)(w - s * Q);
-          const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
-          const int t = (int)(s / a.np), pb = (int)(s % a.np);
-          const CUtensorMap* mW = pb ? &tmW2 : &tmW;
-          for (int j = qa * GG; j < qb * GG && it < NS; ++j, ++it) {
-            if ((int)(it % kProd) != warp) continue;
-            mbar_arrive_expect_tx(&bars->full[it], (uint32_t)STAGE);
-            load_w(stages + it * STAGE, mW, j, t, &bars->full[it], pol, a.w_mn);
-          }
-          w = s * Q + qb;
-        }
-      }
-      grid_dep_wait();  // the token tiles may be the previous kernel's output
+    // Converged warps; one lane issues.  Stage it % NS is free once leaf
+    // it - NS has been committed, which its "full accumulator" barrier
+    // reports (NS <= kNBuf, so that barrier cannot have moved on by a second
+    // phase: the MMAs run in leaf order).
+    // Weights are read once: evict them first, so that the pieces stay in L2.
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    // Before the previous kernel has finished: this producer's share of the
+    // first NS stages, weight tiles only (no kernel here writes weights).
+    {
       long long it = 0;
-      Ring rs;
-      bool ok = true;
-      for (long long w = w0; w < w1 && ok;) {
+      for (long long w = w0; w < w1 && it < NS;) {
         const long long s = w / Q;
         const int qa = (int)(w - s * Q);
         const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
         const int t = (int)(s / a.np), pb = (int)(s % a.np);
         const CUtensorMap* mW = pb ? &tmW2 : &tmW;
-        const CUtensorMap* mX = pb ? &tmX2 : &tmX;
-        for (int j = qa * GG; j < qb * GG; ++j, ++it, rs.next(NS)) {
+        for (int j = qa * GG; j < qb * GG && it < NS; ++j, ++it) {
           if ((int)(it % kProd) != warp) continue;
-          const int st = rs.slot;
-          unsigned char* dst = stages + st * STAGE;
-          if (it >= NS) {  // (the first NS weight tiles are already on their way)
-            if (!wait_or_abort(&bars->empty[st], rs.phase ^ 1u, limit, abort_flag, a.status)) {
-              ok = false;
-              break;
-            }
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&bars->full[it], (uint32_t)STAGE);
+            load_w(stages + it * STAGE, mW, j, t, &bars->full[it], pol, a.w_mn);
+          }
+          __syncwarp();
+        }
+        w = s * Q + qb;
+      }
+    }
+    grid_dep_wait();  // the token tiles may be the previous kernel's output
+    long long it = 0;
+    Ring rs;  // stage of load it
+    Ring rv;  // TMEM buffer of leaf it - NS
+    bool ok = true;
+    for (long long w = w0; w < w1 && ok;) {
+      const long long s = w / Q;
+      const int qa = (int)(w - s * Q);
+      const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
+      const int t = (int)(s / a.np), pb = (int)(s % a.np);
+      const CUtensorMap* mW = pb ? &tmW2 : &tmW;
+      const CUtensorMap* mX = pb ? &tmX2 : &tmX;
+      for (int j = qa * GG; j < qb * GG; ++j, ++it, rs.next(NS)) {
+        const bool reuse = it >= NS;  // (the first NS weight tiles are already on their way)
+        const int vb = rv.slot;
+        const uint32_t vph = rv.phase;
+        if (reuse) rv.next(kNBuf);
+        if ((int)(it % kProd) != warp) continue;
+        const int st = rs.slot;
+        unsigned char* dst = stages + st * STAGE;
+        if (reuse) {
+          const bool wok = wait_or_abort(&bars->accf[vb], vph, limit, abort_flag, a.status);
+          if (!__all_sync(0xffffffffu, wok)) {
+            ok = false;
+            break;
+          }
+        }
+        if (elect_one()) {
+          if (reuse) {
             mbar_arrive_expect_tx(&bars->full[st], (uint32_t)STAGE);
             load_w(dst, mW, j, t, &bars->full[st], pol, a.w_mn);
           }
           tma_load_2d(dst + A_BYTES, mX, j * BK, 0, &bars->full[st]);
         }
-        w = s * Q + qb;
+        __syncwarp();
       }
-      // Drain: this producer's last loads have landed.
+      w = s * Q + qb;
+    }
+    // Drain: this producer's last loads have landed.
+    if (lane == 0)
       for (long long i = (it > NS ? it - NS : 0); i < it; ++i)
         if ((int)(i % kProd) == warp) mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), limit, nullptr);
-    }
   } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, BN) | (a.w_mn ? kIdescTransA : 0u);
-      const uint32_t astep = a.w_mn ? 128u : 2u;  // K = 16 step in descriptor units
-      // Leaf n of this CTA's range uses stage n % NS and TMEM buffer n % kNBuf.
-      // The barriers of leaf n + 1 are waited on before leaf n is committed:
-      // a wait issued after a tcgen05.commit does not return before the
-      // committed MMAs have completed, which would leave the tensor pipe idle
-      // between leaves.  (No deadlock: leaf n + 1 needs the commits of leaves
-      // up to n + 1 - NS and n + G - kNBuf only, both at most n - 1.)
-      const long long nleaf = (w1 - w0) * GG;
-      Ring rs, rb;  // pipeline stage; TMEM leaf buffer
-      auto wait_leaf = [&]() {
-        return wait_or_abort(&bars->acce[rb.slot], rb.phase ^ 1u, limit, abort_flag, a.status) &&
-               wait_or_abort(&bars->full[rs.slot], rs.phase, limit, abort_flag, a.status);
-      };
-      bool ok = nleaf > 0 && wait_leaf();
-      for (long long n = 0; n < nleaf && ok; ++n) {
-        const int st = rs.slot, b = rb.slot;
-        tc_fence_after();
-        const uint64_t da = a.w_mn ? smem_desc_sw128_mn(stages + st * STAGE) : smem_desc_sw128(stages + st * STAGE);
-        const uint64_t db = smem_desc_sw128(stages + st * STAGE + A_BYTES);
+    // ---------------- MMA issuer (converged warp; one lane issues) ----------------
+    // Leaf n of this CTA's range uses stage n % NS and TMEM buffer n % kNBuf;
+    // one commit per leaf (its "full accumulator" barrier, read by the
+    // epilogue and the producers).
+    const uint32_t idesc = idesc_bf16(BM, BN) | (a.w_mn ? kIdescTransA : 0u);
+    const uint32_t astep = a.w_mn ? 128u : 2u;  // K = 16 step in descriptor units
+    const long long nleaf = (w1 - w0) * GG;
+    Ring rs, rb;  // pipeline stage; TMEM leaf buffer
+    bool ok = true;
+    for (long long n = 0; n < nleaf && ok; ++n, rs.next(NS), rb.next(kNBuf)) {
+      const int st = rs.slot, b = rb.slot;
+      const bool wok = wait_or_abort(&bars->acce[b], rb.phase ^ 1u, limit, abort_flag, a.status) &&
+                       wait_or_abort(&bars->full[st], rs.phase, limit, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, wok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t da = a.w_mn ? smem_desc_sw128_mn(stages + st * STAGE) : smem_desc_sw128(stages + st * STAGE);
+      const uint64_t db = smem_desc_sw128(stages + st * STAGE + A_BYTES);
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
           tc_mma_bf16(tmem + (uint32_t)(b * BN), da + astep * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-        rs.next(NS);
-        rb.next(kNBuf);
-        const bool next_ok = n + 1 == nleaf || wait_leaf();
-        tc_commit(&bars->empty[st]);
         tc_commit(&bars->accf[b]);
-        ok = next_ok;
       }
-      tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
-      mbar_wait(&bars->fin, 0, limit, nullptr);
+      __syncwarp();
     }
+    if (elect_one()) tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
+    __syncwarp();
+    if (lane == 0) mbar_wait(&bars->fin, 0, limit, nullptr);
   } else {
     // ---------------- epilogue: leaves -> group roots -> pieces ----------------
     grid_dep_wait();  // its stores may overwrite what the previous kernel reads
@@ -563,15 +577,19 @@ __device__ int list_pieces(const TcsTopArgs& a, long long s, long long b_base, P
   return __shfl_sync(0xffffffffu, incl, 31);
 }
 
-// Fold state of one segment for this thread's (row, token pair): the pieces,
+// Fold state of one segment for this thread's (row, 8 tokens): the pieces,
 // left to right, meet their left siblings on a stack in this thread's column
 // of shared memory.
 struct Fold {
-  uint32_t* stk;  // level l at stk[l * kTopThreads]
-  uint32_t root;
+  uint4* stk;     // level l at stk[l * BM]
+  uint4 root;
   long long b;    // first CTA of the current list batch
   int n;          // pieces in the current list batch
 };
+
+__device__ __forceinline__ uint4 add4(uint4 l, uint4 r) {
+  return make_uint4(add_bf16x2(l.x, r.x), add_bf16x2(l.y, r.y), add_bf16x2(l.z, r.z), add_bf16x2(l.w, r.w));
+}
 
 // The first CTA whose range holds a group of segment s.
 __device__ __forceinline__ long long first_cta(const TcsTopArgs& a, long long s) {
@@ -585,25 +603,25 @@ __device__ __forceinline__ bool more_ctas(const TcsTopArgs& a, long long s, long
 }
 
 // Folds one piece (its fold code from the list) into the stack.
-__device__ __forceinline__ void fold_piece(int code, uint32_t cur, Fold& f) {
+__device__ __forceinline__ void fold_piece(int code, uint4 cur, Fold& f) {
   const int m = code & 0xFF, k = (code >> 8) & 0xFF;
 #pragma unroll 1
-  for (int i = 0; i < k; ++i) cur = add_bf16x2(f.stk[(m + i) * kTopThreads], cur);
+  for (int i = 0; i < k; ++i) cur = add4(f.stk[(m + i) * BM], cur);
   if (code >> 16) f.root = cur;
-  else f.stk[(m + k) * kTopThreads] = cur;
+  else f.stk[(m + k) * BM] = cur;
 }
 
-// Copies (cp.async, 4 bytes per thread) this thread's word of pieces
-// k0 .. min(k0 + CH, n) - 1 of the list into its column of buf.
+// Copies (cp.async, 16 bytes per thread: 8 tokens of one row) this
+// thread's part of pieces k0 .. min(k0 + CH, n) - 1 of the list into its
+// column of buf.
 template <int CH>
 __device__ __forceinline__ void stage_pieces(const TcsTopArgs& a, const PieceRef* list, int k0, int n, int row,
-                                             int word, uint32_t* buf) {
+                                             int quad, uint4* buf) {
   const int kend = n < k0 + CH ? n : k0 + CH;
 #pragma unroll 1
   for (int k = k0; k < kend; ++k) {
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.slots + (size_t)list[k].slot * PIECE) + word * BM + row;
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(buf + (k - k0) * kTopThreads + threadIdx.x)),
-                 "l"(src)
+    const uint16_t* src = a.slots + (size_t)list[k].slot * PIECE + row * BN + quad * kTopTok;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(buf + (k - k0) * BM + row)), "l"(src)
                  : "memory");
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -612,22 +630,22 @@ __device__ __forceinline__ void staged_wait() { asm volatile("cp.async.wait_all;
 
 template <int CH>
 __device__ __forceinline__ void fold_staged(const TcsTopArgs& a, const PieceRef* list, int k0, int n,
-                                            const uint32_t* buf, Fold& f) {
+                                            const uint4* buf, Fold& f) {
   const int kend = n < k0 + CH ? n : k0 + CH;
 #pragma unroll 1
-  for (int k = k0; k < kend; ++k) fold_piece(list[k].at, buf[(k - k0) * kTopThreads + threadIdx.x], f);
+  for (int k = k0; k < kend; ++k) fold_piece(list[k].at, buf[(k - k0) * BM + threadIdx.x], f);
 }
 
 // Everything of segment s after its first CH pieces (already staged and
 // folded by the caller): the rest of that list, then further list batches.
 template <int CH>
-__device__ void fold_rest(const TcsTopArgs& a, long long s, PieceRef* list, int row, int word, bool active,
-                          uint32_t* buf, Fold& f) {
+__device__ void fold_rest(const TcsTopArgs& a, long long s, PieceRef* list, int row, int quad, bool active,
+                          uint4* buf, Fold& f) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int k0 = CH; k0 < f.n; k0 += CH) {
     if (active) {
-      stage_pieces<CH>(a, list, k0, f.n, row, word, buf);
+      stage_pieces<CH>(a, list, k0, f.n, row, quad, buf);
       staged_wait();
       fold_staged<CH>(a, list, k0, f.n, buf, f);
     }
@@ -644,7 +662,7 @@ __device__ void fold_rest(const TcsTopArgs& a, long long s, PieceRef* list, int 
 #pragma unroll 1
     for (int k0 = 0; k0 < f.n; k0 += CH) {
       if (active) {
-        stage_pieces<CH>(a, list, k0, f.n, row, word, buf);
+        stage_pieces<CH>(a, list, k0, f.n, row, quad, buf);
         staged_wait();
         fold_staged<CH>(a, list, k0, f.n, buf, f);
       }
@@ -652,12 +670,13 @@ __device__ void fold_rest(const TcsTopArgs& a, long long s, PieceRef* list, int 
   }
 }
 
-// Writes a [2 kTopWords tokens][128 rows] tile held in shared memory to
-// out[r * ldo + c] for r in [r0, min(r0 + 2 kTopWords, R)), c in [c0, min(c0 + 128, C)).
+// Writes a [kTopTok tokens][128 rows] tile held in shared memory to
+// out[r * ldo + c] for r in [r0, min(r0 + kTopTok, R)), c in [c0, min(c0 + 128, C)).
 __device__ __forceinline__ void store_tile(const uint16_t* tile, uint16_t* out, long long ldo, int R, int r0,
                                            long long c0, long long C) {
+  static_assert(kTopTok * BM == 8 * kTopThreads, "one 16-byte store per thread");
   const int tok = threadIdx.x >> 4, c8 = (threadIdx.x & 15) * 8;
-  if (tok >= 2 * kTopWords || r0 + tok >= R) return;
+  if (r0 + tok >= R) return;
   const long long c = c0 + c8;
   uint16_t* o = out + (r0 + tok) * ldo + c;
   const uint16_t* src = tile + tok * (BM + 8) + c8;
@@ -669,33 +688,35 @@ __device__ __forceinline__ void store_tile(const uint16_t* tile, uint16_t* out, 
   }
 }
 
-__device__ __forceinline__ void put_tile(uint16_t* tile, int row, int wl, uint32_t v) {
-  tile[(2 * wl) * (BM + 8) + row] = (uint16_t)(v & 0xFFFFu);
-  tile[(2 * wl + 1) * (BM + 8) + row] = (uint16_t)(v >> 16);
+// Token t of this thread's 8 (word t / 2 of v, low half first) to tile[t][row].
+__device__ __forceinline__ void put_tile(uint16_t* tile, int row, uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    tile[(2 * i) * (BM + 8) + row] = (uint16_t)(w[i] & 0xFFFFu);
+    tile[(2 * i + 1) * (BM + 8) + row] = (uint16_t)(w[i] >> 16);
+  }
 }
 
-// Plain (FUSED false): CTA (s, y) folds segment s for token pairs
-// kTopWords * y .. kTopWords * y + kTopWords - 1.  Fused (np == 2): CTA (t, y)
-// folds gate (segment 2t) and up (segment 2t+1) and forms
-// h = bf16(SiLU(gate)) * up, rounded to BF16.  Each thread owns one (row,
-// token pair); the pieces are staged in shared memory (up to CH per segment in
-// flight) and folded from there.  Launched as a programmatic dependent of the
-// streaming kernel: the piece lists (arithmetic only) are built before
-// waiting for its results.
-// Six CTAs per SM (at most 40 registers) so that the 768 CTAs of the M = 32
-// gate/up top run in one wave.
+// Plain (FUSED false): CTA (s, y) folds segment s for tokens
+// kTopTok * y .. kTopTok * y + kTopTok - 1.  Fused (np == 2): CTA (t, y) folds
+// gate (segment 2t) and up (segment 2t+1) and forms h = bf16(SiLU(gate)) * up,
+// rounded to BF16.  Each thread owns one row and 8 tokens (a 16-byte quarter
+// of a piece row); the pieces are staged in shared memory (up to CH per
+// segment in flight) and folded from there.  Launched as a programmatic
+// dependent of the streaming kernel: the piece lists (arithmetic only) are
+// built before waiting for its results.
 template <bool FUSED>
-__global__ void __launch_bounds__(kTopThreads, 6) k_tcs_top(const TcsTopArgs a) {
+__global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
   constexpr int NSEG = FUSED ? 2 : 1;
   constexpr int CH = top_chunk(FUSED);
   extern __shared__ __align__(16) unsigned char top_sm[];
-  uint32_t* bufs = reinterpret_cast<uint32_t*>(top_sm);     // NSEG x [CH][kTopThreads]
-  uint32_t* stacks = bufs + NSEG * CH * kTopThreads;         // NSEG x [E][kTopThreads]
-  uint16_t* tiles = reinterpret_cast<uint16_t*>(stacks + NSEG * a.E * kTopThreads);  // 3 x [2 kTopWords][BM + 8]
-  PieceRef* lists = reinterpret_cast<PieceRef*>(tiles + 3 * 2 * kTopWords * (BM + 8));
-  const int row = threadIdx.x % BM, wl = threadIdx.x / BM;
-  const int word = kTopWords * blockIdx.y + wl;
-  const bool active = 2 * word < a.R;
+  uint4* bufs = reinterpret_cast<uint4*>(top_sm);        // NSEG x [CH][BM]
+  uint4* stacks = bufs + NSEG * CH * BM;                  // NSEG x [E][BM]
+  uint16_t* tiles = reinterpret_cast<uint16_t*>(stacks + NSEG * a.E * BM);  // 3 x [kTopTok][BM + 8]
+  PieceRef* lists = reinterpret_cast<PieceRef*>(tiles + 3 * kTopTok * (BM + 8));
+  const int row = threadIdx.x, quad = blockIdx.y;
+  const bool active = kTopTok * quad < a.R;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long s0 = FUSED ? 2ll * blockIdx.x : (long long)blockIdx.x;
   const int stride = 32 * a.cap + 1;  // list entries per segment (the last holds the count)
@@ -712,31 +733,37 @@ __global__ void __launch_bounds__(kTopThreads, 6) k_tcs_top(const TcsTopArgs a) 
   for (int g = 0; g < NSEG; ++g) {
     f[g].b = first_cta(a, s0 + g);
     f[g].n = lists[g * stride + 32 * a.cap].slot;
-    f[g].root = 0;
-    f[g].stk = stacks + (g * a.E) * kTopThreads + threadIdx.x;
-    if (active) stage_pieces<CH>(a, lists + g * stride, 0, f[g].n, row, word, bufs + g * CH * kTopThreads);
+    f[g].root = make_uint4(0, 0, 0, 0);
+    f[g].stk = stacks + (g * a.E) * BM + row;
+    if (active) stage_pieces<CH>(a, lists + g * stride, 0, f[g].n, row, quad, bufs + g * CH * BM);
   }
   staged_wait();
 #pragma unroll
   for (int g = 0; g < NSEG; ++g) {
-    if (active) fold_staged<CH>(a, lists + g * stride, 0, f[g].n, bufs + g * CH * kTopThreads, f[g]);
-    fold_rest<CH>(a, s0 + g, lists + g * stride, row, word, active, bufs + g * CH * kTopThreads, f[g]);
+    if (active) fold_staged<CH>(a, lists + g * stride, 0, f[g].n, bufs + g * CH * BM, f[g]);
+    fold_rest<CH>(a, s0 + g, lists + g * stride, row, quad, active, bufs + g * CH * BM, f[g]);
   }
-  const int r0 = 2 * kTopWords * blockIdx.y;
+  const int r0 = kTopTok * quad;
   if constexpr (!FUSED) {
     const int t = (int)(s0 / a.np), pb = (int)(s0 % a.np);
-    put_tile(tiles, row, wl, f[0].root);
+    put_tile(tiles, row, f[0].root);
     __syncthreads();
     store_tile(tiles, pb ? a.out1 : a.out0, a.ldo, a.R, r0, (long long)t * BM, a.C);
   } else {
     const int t = blockIdx.x;
-    const uint32_t g = f[0].root, u = f[1].root;
-    const float h0 = __fmul_rn(bf2f(__ldg(a.silu + (g & 0xFFFFu))), __uint_as_float(u << 16));
-    const float h1 = __fmul_rn(bf2f(__ldg(a.silu + (g >> 16))), __uint_as_float(u & 0xFFFF0000u));
-    constexpr int TILE = 2 * kTopWords * (BM + 8);
-    put_tile(tiles, row, wl, (uint32_t)f2bf(h0) | ((uint32_t)f2bf(h1) << 16));
-    if (a.out0) put_tile(tiles + TILE, row, wl, g);
-    if (a.out1) put_tile(tiles + 2 * TILE, row, wl, u);
+    const uint32_t gw[4] = {f[0].root.x, f[0].root.y, f[0].root.z, f[0].root.w};
+    const uint32_t uw[4] = {f[1].root.x, f[1].root.y, f[1].root.z, f[1].root.w};
+    uint32_t hw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float h0 = __fmul_rn(bf2f(__ldg(a.silu + (gw[i] & 0xFFFFu))), __uint_as_float(uw[i] << 16));
+      const float h1 = __fmul_rn(bf2f(__ldg(a.silu + (gw[i] >> 16))), __uint_as_float(uw[i] & 0xFFFF0000u));
+      hw[i] = (uint32_t)f2bf(h0) | ((uint32_t)f2bf(h1) << 16);
+    }
+    constexpr int TILE = kTopTok * (BM + 8);
+    put_tile(tiles, row, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    if (a.out0) put_tile(tiles + TILE, row, f[0].root);
+    if (a.out1) put_tile(tiles + 2 * TILE, row, f[1].root);
     __syncthreads();
     store_tile(tiles, a.h, a.ldo, a.R, r0, (long long)t * BM, a.C);
     if (a.out0) store_tile(tiles + TILE, a.out0, a.ldo, a.R, r0, (long long)t * BM, a.C);
@@ -904,7 +931,7 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   t.ldo = ldo;
   t.h = h;
   t.silu = silu;
-  const dim3 grid(h ? plan.T : plan.np * plan.T, (plan.R + 2 * kTopWords - 1) / (2 * kTopWords));
+  const dim3 grid(h ? plan.T : plan.np * plan.T, (plan.R + kTopTok - 1) / kTopTok);
   const int smem_top = top_smem(h != nullptr, plan.E, plan.cap);
   return h ? launch_dependent(k_tcs_top<true>, grid, kTopThreads, smem_top, st, t)
            : launch_dependent(k_tcs_top<false>, grid, kTopThreads, smem_top, st, t);

@@ -19,17 +19,18 @@
 //               stages on mbarriers (as many as fit beside the shared-memory
 //               stack levels); a stage is reused once the leaf read from it
 //               has been committed;
-//   warp 1      allocates TMEM (512/BN leaf buffers of BN columns) and issues
-//               the MMAs, one leaf per buffer, with one commit per leaf (the
-//               buffer's "full" barrier, which the producer reads too);
-//   warps 10..  further MMA issuers (leaves are dealt round-robin over the
-//               issuers; see kIssuers);
-//   warps 2-9   epilogue: each thread owns one row (TMEM lane) and BN/2
+//   warps 1-3   MMA issuers (warp 1 also allocates TMEM: 512/BN leaf buffers
+//               of BN columns); leaves are dealt round-robin over them, one
+//               leaf per buffer, with one commit per leaf (the buffer's
+//               "full" barrier, which the producer reads too);
+//   warps 4-11  epilogue: each thread owns one row (TMEM lane) and BN/2
 //               columns; it reads a group's leaves from TMEM, forms the
 //               group roots, returns the buffers at once, and then folds the
 //               roots into a binary-counter stack of BF16 nodes (low levels
 //               in registers, high levels in shared memory); the last fold
 //               is the output.
+// Registers: warps 0-3 hand most of their share to the epilogue's two
+// warpgroups (setmaxnreg), which hold a group's leaves in 32-column chunks.
 // Every wait is bounded; on a timeout the CTA records DETFFN_ERR_TIMEOUT,
 // stops, drains its own copies and MMAs (bounded) and frees its TMEM.
 #include <cuda.h>
@@ -44,16 +45,19 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kMaxAccBufs = 16;  // TMEM leaf buffers: 512 columns / BN (at most 16)
-constexpr int kEpiWarp0 = 2;  // warp 0: producer, warp 1: MMA, warps 2..: epilogue
-#ifndef DETFFN_TC_ISSUERS
-#define DETFFN_TC_ISSUERS 3
-#endif
-// MMA-issuing warps: warp 1 and the warps after the epilogue's.  Issuer q
-// takes leaves q, q + kIssuers, ...: each leaf costs its issuing thread a
-// commit and two barrier waits of a few hundred cycles of latency, more than
-// the 4 MMAs of a 128 x 128 leaf keep the tensor pipe busy, so one issuer
-// alone leaves the pipe idle between leaves.
-constexpr int kIssuers = DETFFN_TC_ISSUERS;
+constexpr int kEpiWarp0 = 4;  // warp 0: producer, warps 1-3: MMA, warps 4..11: epilogue
+// MMA-issuing warps 1 .. kIssuers.  Issuer q takes leaves q, q + kIssuers,
+// ...: each leaf costs its issuing thread a commit and two barrier waits of
+// a few hundred cycles of latency, more than the 4 MMAs of a 128 x 128 leaf
+// keep the tensor pipe busy, so one issuer alone leaves the pipe idle
+// between leaves.
+constexpr int kIssuers = kEpiWarp0 - 1;
+// Registers per thread: at launch (384 threads), and after the split between
+// warpgroup 0 (producer and issuers) and the epilogue's two warpgroups.  The
+// split hands over exactly what the launch holds; the host refuses to launch
+// a build whose register count differs.
+constexpr int kRegsLaunch = 168, kRegsLow = 56, kRegsHigh = 224;
+static_assert(128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch, "register split");
 constexpr int kMaxLv = 6;  // up to Q = 64 bottom groups
 
 // One CTA per SM, 8 epilogue warps (two per TMEM lane quarter, BN/2 columns
@@ -61,7 +65,8 @@ constexpr int kMaxLv = 6;  // up to Q = 64 bottom groups
 template <int BN> struct TcGeo {
   static constexpr int EPI_WARPS = 8;
   static constexpr int HALVES = EPI_WARPS / 4;            // epilogue warps per lane quarter
-  static constexpr int THREADS = 32 * (kEpiWarp0 + EPI_WARPS + kIssuers - 1);
+  static constexpr int THREADS = 32 * (kEpiWarp0 + EPI_WARPS);
+  static_assert(THREADS == 384, "register split assumes 384 threads");
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
@@ -93,8 +98,6 @@ template <int BN> struct TcGeo {
   }
 };
 
-__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Tree node on packed pairs of BF16 nodes: rne_bf16(fp32(a) + fp32(b)) per
 // half, which is the correctly rounded BF16 sum, i.e. add.rn.bf16x2 (checked
@@ -215,6 +218,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
+  if (warp < kEpiWarp0) regs_dec<kRegsLow>();
+  else regs_inc<kRegsHigh>();
 
   if (warp == 0) {
     // ---------------- TMA producer (converged warp; one lane issues) ----------------
@@ -265,8 +270,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     if (lane == 0)
       for (long long i = (it > NS ? it - NS : 0); i < it; ++i)
         mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), limit, nullptr);
-  } else if (warp == 1 || warp >= kEpiWarp0 + T::EPI_WARPS) {
-    const int q = warp == 1 ? 0 : warp - (kEpiWarp0 + T::EPI_WARPS) + 1;  // issuer index
+  } else if (warp < kEpiWarp0) {
+    const int q = warp - 1;  // issuer index
     // ---------------- MMA issuers (converged warps; one lane each issues) ----------------
     // Leaf n uses stage n % NS and TMEM buffer n % NBUF; one commit per leaf
     // (its "full accumulator" barrier) tells both the epilogue and the
@@ -341,9 +346,9 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
         tc_fence_after();
         const uint32_t b0 = (uint32_t)((lc % T::NBUF) * BN), b1 = (uint32_t)(((lc + 1) % T::NBUF) * BN),
                        b2 = (uint32_t)(((lc + 2) % T::NBUF) * BN);
-        // Phase 1: read the group's leaves from TMEM in column chunks of 16
+        // Phase 1: read the group's leaves from TMEM in column chunks of 32
         // and form the group roots.
-        constexpr int CW = 16;
+        constexpr int CW = 32;
         constexpr int WC = CW / 2;  // packed words per chunk
         uint32_t root[T::WORDS];
         if constexpr (GG == 1) {
@@ -368,23 +373,21 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
         for (int c = 0; c < T::COLS / CW; ++c) {
           uint32_t v0[CW], v1[GG >= 2 ? CW : 1], v2[GG >= 3 ? CW : 1];
           const uint32_t col = (uint32_t)(col0 + CW * c);
-          tmem_ld16(tmem + lane_addr + b0 + col, v0);
-          if constexpr (GG >= 2) tmem_ld16(tmem + lane_addr + b1 + col, v1);
-          if constexpr (GG >= 3) tmem_ld16(tmem + lane_addr + b2 + col, v2);
+          tmem_ld32(tmem + lane_addr + b0 + col, v0);
+          if constexpr (GG >= 2) tmem_ld32(tmem + lane_addr + b1 + col, v1);
+          if constexpr (GG >= 3) tmem_ld32(tmem + lane_addr + b2 + col, v2);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < WC; ++i) {
-            float x = __uint_as_float(v0[2 * i]), y = __uint_as_float(v0[2 * i + 1]);
+            // Pairs of adjacent columns, added two at a time (add.rn.f32x2).
+            uint64_t xy = f32x2(v0[2 * i], v0[2 * i + 1]);
             if constexpr (GG == 2) {
-              x = __fadd_rn(x, __uint_as_float(v1[2 * i]));
-              y = __fadd_rn(y, __uint_as_float(v1[2 * i + 1]));
+              xy = add_f32x2(xy, f32x2(v1[2 * i], v1[2 * i + 1]));
             } else if constexpr (GG == 3) {
-              const uint32_t n12 = pack_bf16x2(__fadd_rn(__uint_as_float(v1[2 * i]), __uint_as_float(v2[2 * i])),
-                                               __fadd_rn(__uint_as_float(v1[2 * i + 1]), __uint_as_float(v2[2 * i + 1])));
-              x = __fadd_rn(x, lo_f(n12));
-              y = __fadd_rn(y, hi_f(n12));
+              const uint32_t n12 = pack_bf16x2_of(add_f32x2(f32x2(v1[2 * i], v1[2 * i + 1]), f32x2(v2[2 * i], v2[2 * i + 1])));
+              xy = add_f32x2(xy, f32x2(n12 << 16, n12 & 0xFFFF0000u));
             }
-            root[c * WC + i] = pack_bf16x2(x, y);  // a lone leaf (GG == 1) is rounded once
+            root[c * WC + i] = pack_bf16x2_of(xy);  // a lone leaf (GG == 1) is rounded once
           }
         }
         // The leaves are in registers: return the TMEM buffers to the MMA warp.
@@ -504,6 +507,12 @@ cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cuda
     const cudaError_t e =
         cudaFuncSetAttribute(k_tc<BN, GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<BN>::MAX_SMEM);
     if (e != cudaSuccess) return e;
+    // The in-kernel register split (setmaxnreg) hands over exactly the
+    // launch's registers; with any other count it could not complete.
+    cudaFuncAttributes fa;
+    const cudaError_t e2 = cudaFuncGetAttributes(&fa, k_tc<BN, GG>);
+    if (e2 != cudaSuccess) return e2;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
     attr = true;
   }
   const int units = a.num_m * a.num_n * a.np;

@@ -390,15 +390,13 @@ __global__ void __maxnreg__(128)
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              n12[i] = pack_bf16x2(__fadd_rn(__uint_as_float(v1[2 * i]), __uint_as_float(v2[2 * i])),
-                                   __fadd_rn(__uint_as_float(v1[2 * i + 1]), __uint_as_float(v2[2 * i + 1])));
+              n12[i] = pack_bf16x2_of(add_f32x2(f32x2(v1[2 * i], v1[2 * i + 1]), f32x2(v2[2 * i], v2[2 * i + 1])));
             tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              root[8 * c + i] = pack_bf16x2(__fadd_rn(__uint_as_float(v0[2 * i]), __uint_as_float(n12[i] << 16)),
-                                            __fadd_rn(__uint_as_float(v0[2 * i + 1]),
-                                                      __uint_as_float(n12[i] & 0xFFFF0000u)));
+              root[8 * c + i] =
+                  pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(n12[i] << 16, n12[i] & 0xFFFF0000u)));
           } else if constexpr (GG == 2) {
             uint32_t v1[16];
             tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
@@ -406,8 +404,7 @@ __global__ void __maxnreg__(128)
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              root[8 * c + i] = pack_bf16x2(__fadd_rn(__uint_as_float(v0[2 * i]), __uint_as_float(v1[2 * i])),
-                                            __fadd_rn(__uint_as_float(v0[2 * i + 1]), __uint_as_float(v1[2 * i + 1])));
+              root[8 * c + i] = pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(v1[2 * i], v1[2 * i + 1])));
           } else {
             tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
             tmem_wait_ld();

@@ -250,6 +250,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// BF16 pair (round to nearest even) of the two FP32 values of a pair.
+__device__ __forceinline__ uint32_t pack_bf16x2_of(uint64_t p) {
+  return pack_bf16x2(__uint_as_float((uint32_t)p), __uint_as_float((uint32_t)(p >> 32)));
+}
+// Two FP32 values in one 64-bit register pair (lo first) and two IEEE
+// round-to-nearest FP32 additions in one instruction: (a.lo + b.lo, a.hi + b.hi),
+// each the same as __fadd_rn.
+__device__ __forceinline__ uint64_t f32x2(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 // Correctly rounded BF16 sum of each half (equals rne_bf16(fp32(a) + fp32(b))).
 __device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
   uint32_t r;

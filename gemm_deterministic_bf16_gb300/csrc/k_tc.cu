@@ -77,10 +77,11 @@ template <int BN> struct TcGeo {
   static constexpr int BAR_BYTES = 512;
   // Output staging for one-leaf trees (G = 1: the weight gradients over few
   // tokens, whose epilogue is nothing but stores; longer trees need the shared
-  // memory for stack levels and stages): per epilogue warp 32 rows x COLS
-  // columns, rows padded by 16 bytes.
-  static constexpr int STG_ROW = COLS * 2 / 16 + 1;  // 16-byte units per staged row
-  static constexpr int STG_BYTES = EPI_WARPS * 32 * STG_ROW * 16;
+  // memory for stack levels and stages): per epilogue warp two buffers of 32
+  // rows x COLS columns in the 128-byte-swizzled layout of a TMA store box.
+  static constexpr int STG_BUF = 32 * COLS * 2;  // bytes of one buffer (4 KB)
+  static constexpr int STG_BYTES = EPI_WARPS * 2 * STG_BUF;
+  static_assert(COLS * 2 == 128, "one 128-byte swizzle span per staged row");
   static __host__ __device__ int stg_for(int G) { return G == 1 ? STG_BYTES : 0; }
   static constexpr int MAX_SMEM = 227 * 1024;
   static constexpr int MAX_STAGES = 12;
@@ -137,6 +138,7 @@ struct TcArgs {
   int num_m, num_n;
   int np;           // problems in this launch (1 or 2; the second uses tmA2/tmB2 and out2)
   int b_mn;         // B stored [K][C] (C contiguous): MN-major B tiles (BN = 128 only)
+  int o_tma;        // one-leaf trees: outputs leave through TMA stores (maps tmO, tmO2)
   int a_mn;         // A stored [K][R] (R contiguous): MN-major A tiles
   uint16_t* out;
   uint16_t* out2;
@@ -173,7 +175,7 @@ template <int BN, int GG>
 __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-         const TcArgs a) {
+         const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2, const TcArgs a) {
   using T = TcGeo<BN>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
   const int slv = a.E > T::REG_LV ? a.E - T::REG_LV : 0;
   unsigned char* stages = smem;
   uint32_t* stk = reinterpret_cast<uint32_t*>(smem + NS * T::STAGE);
-  uint4* stg_all = reinterpret_cast<uint4*>(smem + NS * T::STAGE + slv * T::LV_BYTES);
+  unsigned char* stg_all = smem + NS * T::STAGE + slv * T::LV_BYTES;  // 1024-byte aligned
   Bars* bars = reinterpret_cast<Bars*>(smem + NS * T::STAGE + slv * T::LV_BYTES + T::stg_for(GG));
   volatile int* abort_flag = &bars->abort;
 
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const int Q = 1 << a.E;
     uint32_t lc = 0;  // leaves consumed (NBUF is a power of two)
+    int stg_n = 0;    // tiles staged for a TMA store
     bool ok = true;
     uint32_t reg_lv[T::REG_LV][T::WORDS];
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
@@ -420,42 +423,33 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
                 else *stk_at<BN>(stk, m, half, w, row) = root[w];
               }
             }
-        } else if (GG == 1 && a.ld_c == 1 && (a.ld_r % 8) == 0 && (((uintptr_t)outp) & 15u) == 0) {
-          // Row-major output: this warp's 32 rows x COLS columns go through
-          // shared memory and leave as whole 16-byte row segments, eight
-          // lanes per row (coalesced), instead of 32 scattered rows per store.
+        } else if (GG == 1 && a.o_tma) {
+          // Row-major output: this warp's 32 rows x COLS columns go to shared
+          // memory in the swizzled layout of a TMA box and leave as one bulk
+          // tensor store (clipped at the output's edges); two buffers per
+          // warp, so that staging the next tile overlaps this store.
           if constexpr (GG == 1) {
-          constexpr int SEG = T::COLS / 8;  // 16-byte segments per row
-          uint4* stg = stg_all + ew * 32 * T::STG_ROW;
+            unsigned char* buf = stg_all + (ew * 2 + (stg_n & 1)) * T::STG_BUF;
+            if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+            __syncwarp();
 #pragma unroll
-          for (int v = 0; v < SEG; ++v)
-            stg[lane * T::STG_ROW + v] = make_uint4(root[4 * v], root[4 * v + 1], root[4 * v + 2], root[4 * v + 3]);
-          __syncwarp();
-          const long long rbase = (long long)tm * BM + quarter * 32;
-          const long long cbase = (long long)tn * BN + col0;
-#pragma unroll
-          for (int k = 0; k < 32 * SEG / 32; ++k) {
-            const int rl = (k * 32 + lane) / SEG, seg = (k * 32 + lane) % SEG;
-            const long long r2 = rbase + rl, c = cbase + 8 * seg;
-            if (r2 < a.R) {
-              const uint4 v = stg[rl * T::STG_ROW + seg];
-              uint16_t* o = outp + r2 * a.ld_r + c;
-              if (c + 8 <= a.C) {
-                *reinterpret_cast<uint4*>(o) = v;
-              } else {
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                for (int i = 0; i < 8; ++i)
-                  if (c + i < a.C) o[i] = (uint16_t)(w4[i >> 1] >> (16 * (i & 1)));
-              }
+            for (int v = 0; v < T::COLS / 8; ++v)  // 16-byte chunk v of row `lane` at chunk v ^ (lane % 8)
+              *reinterpret_cast<uint4*>(buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
+                  make_uint4(root[4 * v], root[4 * v + 1], root[4 * v + 2], root[4 * v + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(pb ? &tmO2 : &tmO, buf, tn * BN + col0, tm * BM + quarter * 32);
+              bulk_commit();
             }
-          }
-          __syncwarp();
+            ++stg_n;
           }
         } else if (r < a.R) {
           store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
         }
       }
     }
+    if (lane == 0) bulk_wait<0>();  // this warp's output stores have completed
   }
 
   tc_fence_before();
@@ -519,7 +513,7 @@ cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cuda
   const int slots = sm_count;
   const int grid = units < slots ? units : slots;
   const int smem = TcGeo<BN>::smem_for(a.G, a.E, a.nstage);
-  k_tc<BN, GG><<<grid, TcGeo<BN>::THREADS, smem, st>>>(m[0], m[1], m[2], m[3], a);
+  k_tc<BN, GG><<<grid, TcGeo<BN>::THREADS, smem, st>>>(m[0], m[1], m[2], m[3], m[4], m[5], a);
   return cudaGetLastError();
 }
 
@@ -594,7 +588,19 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   a.nstage = TcGeo<bn>::stages_for(a.G, a.E);
   if (a.nstage > TcGeo<bn>::NBUF) a.nstage = TcGeo<bn>::NBUF;  // stage reuse is read off the leaf barriers
   if (a.nstage < 2) return cudaErrorInvalidValue;
-  CUtensorMap m[4];
+  CUtensorMap m[6];
+  // One-leaf trees with row-major outputs store through TMA: boxes of 32 rows
+  // x 64 columns (one epilogue warp's share of a tile), 128-byte swizzle.
+  a.o_tma = 0;
+  if (G == 1 && ld_c == 1 && ld_r % 8 == 0) {
+    bool okm = true;
+    for (int p = 0; p < 2 && okm; ++p) {
+      const uint16_t* o = pr[p < np ? p : 0].out;
+      okm = ((uintptr_t)o & 15u) == 0 && tc_make_map(&m[4 + p], o, R, C, ld_r, 32);
+    }
+    a.o_tma = okm ? 1 : 0;
+  }
+  if (!a.o_tma) m[4] = m[5] = CUtensorMap{};
   for (int p = 0; p < 2; ++p) {
     const TcProblem& q = pr[p < np ? p : 0];
     const bool bmap = q.b_mn ? tc_make_map(&m[2 * p + 1], q.B, K, C, q.ldb, BK)

@@ -438,8 +438,9 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
                   make_uint4(root[4 * v], root[4 * v + 1], root[4 * v + 2], root[4 * v + 3]);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(pb ? &tmO2 : &tmO, buf, tn * BN + col0, tm * BM + quarter * 32);
+            const int ox = tn * BN + col0, oy = tm * BM + quarter * 32;
+            if (lane == 0 && ox < a.C && oy < a.R) {  // (a box wholly past the edge is skipped)
+              tma_store_2d(pb ? &tmO2 : &tmO, buf, ox, oy);
               bulk_commit();
             }
             ++stg_n;

@@ -48,6 +48,16 @@ def test_tc_integer_inputs_bit_exact(G, oracle_mod, R, C, K):
     assert mismatches(got, oracle_mod.tree_gemm(A, B)) == 0
 
 
+@pytest.mark.parametrize("R,C,K", [(200, 296, 40), (130, 72, 64), (33, 1000, 24), (4096, 136, 32), (200, 300, 48)])
+def test_tc_one_leaf_ragged_bit_exact(G, oracle_mod, R, C, K):
+    """One-leaf trees (K <= 64) with more than 32 rows: the output leaves
+    through TMA tensor stores of 32 x 64 boxes, clipped at ragged edges (or,
+    with a row length that is not a multiple of 8, through plain stores)."""
+    A, B = _ints((R, K), R + 3 * K), _ints((C, K), C + 5 * K)
+    got = host(G.detffn_tree_gemm(dev(A), dev(B), path=TENSOR))
+    assert mismatches(got, oracle_mod.tree_gemm(A, B)) == 0
+
+
 @pytest.mark.parametrize("R,C,K", [(1, 256, 4096), (8, 384, 768), (32, 1024, 12288), (17, 200, 256)])
 def test_tc_few_rows_swapped_bit_exact(G, oracle_mod, R, C, K):
     """R <= 32: weights on the 128-row MMA side, tokens as the 32-wide tile."""

@@ -10,7 +10,7 @@ from .detffn import (  # noqa: F401
     BF16, F16, F32, OP_BACKWARD, OP_FORWARD, OP_FORWARD_SHARDED, OP_WGRAD_CHUNKED, PATH_AUTO,
     PATH_EXACT, PATH_TENSOR, DetFFNError, detffn_backward, detffn_forward,
     detffn_forward_sharded, detffn_get_status, detffn_rank_tree_reduce, detffn_silu_tables,
-    detffn_forward_decode_noalloc, detffn_profile_read, detffn_profiling, detffn_selfcheck_node_add,
+    detffn_forward_decode_noalloc, detffn_profile_read, detffn_profiling, detffn_selfcheck_node_add, detffn_selfcheck_pieces,
     detffn_tree_gemm,
     detffn_wgrad_chunked,
     detffn_workspace_size, workspace,

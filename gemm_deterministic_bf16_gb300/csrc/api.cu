@@ -1008,6 +1008,12 @@ extern "C" detffn_status detffn_profile_read(detffn_handle h, int max, detffn_ke
   return DETFFN_OK;
 }
 
+extern "C" detffn_status detffn_selfcheck_pieces(int max_levels, unsigned long long* failures) {
+  if (!failures || max_levels < 0 || max_levels > kTcsMaxLv) return DETFFN_ERR_INVALID_ARG;
+  *failures = tcs_selfcheck_pieces(max_levels);
+  return DETFFN_OK;
+}
+
 extern "C" detffn_status detffn_selfcheck_node_add(detffn_handle h, unsigned long long* mismatches) {
   if (!h || !mismatches) return DETFFN_ERR_INVALID_ARG;
   TRYCU(cudaSetDevice(h->device));

@@ -33,6 +33,7 @@
 #include "common.cuh"
 #include "ptx.cuh"
 #include "tc.h"
+#include "tcs_pieces.cuh"
 
 namespace detffn {
 namespace {
@@ -125,43 +126,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, lo
   *abort_flag = 1;
   if (status) atomicExch(status, (int)DETFFN_ERR_TIMEOUT);
   return false;
-}
-
-__host__ __device__ inline int hibit(unsigned v) {  // v > 0
-#ifdef __CUDA_ARCH__
-  return 31 - __clz(v);
-#else
-  return 31 - __builtin_clz(v);
-#endif
-}
-__host__ __device__ inline int popc(unsigned v) {
-#ifdef __CUDA_ARCH__
-  return __popc(v);
-#else
-  return __builtin_popcount(v);
-#endif
-}
-
-// The pieces of groups [x, y), 0 <= x < y <= 2^E, are its maximal aligned
-// blocks.  Let h be the highest bit in which x and y - 1 differ and z the
-// multiple of 2^h between them: left to right, the pieces have the sizes of
-// the set bits of z - x (ascending) and then of y - z (descending) -- unless
-// both halves are whole, when [x, y) is itself one aligned block.
-struct PieceSplit {
-  int x, z, y;
-  bool one;  // [x, y) is one aligned block
-};
-__host__ __device__ inline PieceSplit piece_split(int x, int y) {
-  PieceSplit p{x, y, y, true};
-  if (y - x == 1) return p;
-  const int h = hibit((unsigned)(x ^ (y - 1)));
-  p.z = ((y - 1) >> h) << h;
-  p.one = (p.z - x == (1 << h)) && (y - p.z == (1 << h));
-  return p;
-}
-__host__ __device__ inline int count_pieces(int x, int y) {
-  const PieceSplit p = piece_split(x, y);
-  return p.one ? 1 : popc((unsigned)(p.z - x)) + popc((unsigned)(y - p.z));
 }
 
 // Writes one row (all tokens) of the CTA's next piece: the row's 64 bytes
@@ -510,16 +474,6 @@ struct PieceRef {
              // result is the root (bit 16): the fold, the same for every element, worked out once
 };
 static_assert(sizeof(PieceRef) == kPieceRefBytes, "piece list entries: shared-memory sizes assume 8 bytes");
-
-// The fold step of a piece of level m starting at group `at`, for a tile of
-// 2^E groups: it merges with the pending left siblings at levels m, m+1, ...
-// while its subtree is a right child, then waits on the stack at the level
-// reached or is the root.
-__device__ __forceinline__ int fold_code(int at, int m, int E) {
-  int k = 0;
-  while (m + k < E && ((at >> (m + k)) & 1)) ++k;
-  return m | (k << 8) | ((m + k == E) ? (1 << 16) : 0);
-}
 
 // Lists, in order, the pieces of segment s that CTAs [b_base, b_base + 32)
 // wrote: one lane per CTA, placed by a warp scan.  Returns the count.

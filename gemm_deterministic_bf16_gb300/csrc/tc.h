@@ -85,4 +85,8 @@ cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* problems, u
                               const uint16_t* silu, void* scratch, size_t scratch_bytes, int* status,
                               long long spin, cudaStream_t st);
 
+// Host check of the few-token kernels' piece decomposition and fold codes
+// over every tile of up to 2^max_levels groups; returns the failed cases.
+unsigned long long tcs_selfcheck_pieces(int max_levels);
+
 }  // namespace detffn

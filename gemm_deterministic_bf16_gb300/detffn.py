@@ -327,6 +327,17 @@ def detffn_forward_decode_noalloc(x, Wg, Wu, Wd, out=None, stream=None):
     return out
 
 
+def detffn_selfcheck_pieces(max_levels=8):
+    """Failed cases of the host check of the few-token kernels' piece
+    decomposition and fold codes (no GPU needed)."""
+    L = lib()
+    L.detffn_selfcheck_pieces.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_ulonglong)]
+    L.detffn_selfcheck_pieces.restype = ctypes.c_int
+    n = ctypes.c_ulonglong()
+    _check(L.detffn_selfcheck_pieces(int(max_levels), ctypes.byref(n)), "detffn_selfcheck_pieces")
+    return n.value
+
+
 def detffn_selfcheck_node_add(device=None):
     """Number of BF16 pairs where the device's packed add differs from the
     tree node rne_bf16(fp32(a) + fp32(b)) (exhaustive over 2^32 pairs)."""

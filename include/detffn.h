@@ -250,6 +250,19 @@ DETFFN_API detffn_status detffn_forward_decode_noalloc(const void *x, const void
  * an 8-byte counter and synchronises the device. */
 DETFFN_API detffn_status detffn_selfcheck_node_add(detffn_handle h, unsigned long long *mismatches);
 
+/* Diagnostic, host only (no device, no handle): checks the decomposition of
+ * K ranges into pieces used by the few-token tensor kernels (balanced K
+ * ranges; RL-Kernel PR #325, "Design": every contiguous range of leaves that
+ * is an aligned block is a subtree of the canonical tree).  For every tile of
+ * 2^E bottom groups, E <= max_levels (at most 8): the closed-form pieces of
+ * every group range equal the greedy decomposition into maximal aligned
+ * blocks, and for every split of the tile into three consecutive ranges the
+ * pieces, folded left to right with their fold codes, pair each right child
+ * with its left sibling and end in the tile's root exactly once.  Writes the
+ * number of failed cases to *failures.  DETFFN_ERR_INVALID_ARG for a null
+ * pointer or max_levels outside [0, 8]. */
+DETFFN_API detffn_status detffn_selfcheck_pieces(int max_levels, unsigned long long *failures);
+
 /* Synchronises `stream`, then returns and clears the handle's device status
  * word (DETFFN_OK or DETFFN_ERR_TIMEOUT from a bounded wait). */
 DETFFN_API detffn_status detffn_get_status(detffn_handle h, void *stream);

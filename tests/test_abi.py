@@ -90,3 +90,21 @@ def test_header_names_readings():
     txt = open(os.path.join(ROOT, "include", "detffn.h")).read()
     for needle in ["leaf", "midpoint", "rne_bf16", "PR #325", "PR #357"]:
         assert needle in txt
+
+
+def test_piece_decomposition_and_fold_selfcheck():
+    """The few-token tensor kernels split each tile's tree into pieces (maximal
+    aligned blocks of bottom groups) by a closed form and fold them with
+    per-piece codes; the library's host check compares the closed form with
+    the greedy decomposition on every range of every tile of up to 256 groups
+    and replays the fold symbolically on every three-way split of each tile
+    (the pieces of each right child must meet their own left sibling and end
+    in the root once).  No GPU is needed."""
+    from gemm_deterministic_bf16_gb300 import build, detffn
+    build.build()
+    assert detffn.detffn_selfcheck_pieces(8) == 0
+    L = detffn.lib()
+    n = ctypes.c_ulonglong()
+    L.detffn_selfcheck_pieces.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_ulonglong)]
+    assert L.detffn_selfcheck_pieces(9, ctypes.byref(n)) != 0          # out of range: an argument error
+    assert L.detffn_selfcheck_pieces(8, None) != 0

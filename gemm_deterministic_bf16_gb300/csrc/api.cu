@@ -265,10 +265,11 @@ FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k, int s
   const long long rows = 2 * I > H ? 2 * I : H;
   w.dec_part = M <= 32 ? a.take<uint16_t>(kDecPlanes * rows) : nullptr;
   w.dec_cnt = M <= 32 ? a.take<unsigned>(rows + 1) : nullptr;
-  // Tensor family with few tokens: piece slots for gate/up and for down.
+  // Tensor family with few tokens: piece slots for gate/up (all of I: the
+  // shards' gate/up slices are computed by one launch) and for down.
   if (M >= 1 && M <= 32) {
     const long long sw = I / k;
-    const size_t gu = tcs_bytes(sw, H, 2, sms), dn = tcs_bytes(H, sw, 1, sms);
+    const size_t gu = tcs_bytes(I, H, 2, sms), dn = tcs_bytes(H, sw, 1, sms);
     w.tcs.bytes = gu > dn ? gu : dn;
     w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
   }
@@ -290,8 +291,8 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool
   w.cgs = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
   w.cus = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
   if (tensor) {
-    if (M >= 1 && M <= 32) {  // dh over K = H; cg, cu over K = I / k
-      const size_t d1 = tcs_bytes(I, H, 1, sms), d2 = tcs_bytes(H, I / k, 1, sms);
+    if (M >= 1 && M <= 32) {  // dh over K = H; cg and cu (one launch) over K = I / k
+      const size_t d1 = tcs_bytes(I, H, 1, sms), d2 = tcs_bytes(H, I / k, 2, sms);
       w.tcs.bytes = d1 > d2 ? d1 : d2;
       w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
     }
@@ -417,6 +418,36 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
   }
   return timed(h, st, "tree_gemm_exact", bytes, 2.0 * R * C * K,
                [&] { return cu(launch_tree_gemm_exact(A, B, R, C, K, out, o_rs, st)); });
+}
+
+// Two same-shaped contractions: one launch of the tensor family (the two
+// problems' tiles interleave over the SMs), two launches of the exact one.
+detffn_status tree_gemm2(detffn_handle h, Family f, Strided A0, Strided B0, uint16_t* out0, Strided A1,
+                         Strided B1, uint16_t* out1, long long R, long long C, long long K, long long o_rs,
+                         cudaStream_t st, const TcsScratch& sc) {
+  if (f != kTensor) {
+    TRY(tree_gemm(h, f, A0, B0, R, C, K, out0, o_rs, st, sc));
+    return tree_gemm(h, f, A1, B1, R, C, K, out1, o_rs, st, sc);
+  }
+  const double bytes = 4.0 * ((double)R * K + (double)C * K + (double)R * C);
+  const bool b_mn = tc_mn_ok(B0), a_mn = tc_mn_ok(A0);
+  if (tc_mn_ok(B1) != b_mn || tc_mn_ok(A1) != a_mn) return DETFFN_ERR_ALIGN;
+  if (!(a_mn || (tc_operands_ok(A0) && tc_operands_ok(A1))) || !(b_mn || (tc_operands_ok(B0) && tc_operands_ok(B1))))
+    return DETFFN_ERR_ALIGN;
+  if (a_mn && R <= 32) return DETFFN_ERR_UNSUPPORTED;
+  const long long ldb0 = b_mn ? B0.ks : B0.rs, ldb1 = b_mn ? B1.ks : B1.rs;
+  if (R <= 32) {
+    TcsPlan p;
+    if (!tcs_plan_fit(R, C, K, 2, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
+    const TcsProblem pr[2] = {{B0.p, ldb0, A0.p, A0.rs, out0, b_mn}, {B1.p, ldb1, A1.p, A1.rs, out1, b_mn}};
+    return timed(h, st, "tcs_tree_gemm", bytes, 4.0 * R * C * K,
+                 [&] { return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->d_status, 0, st)); });
+  }
+  return timed(h, st, "tc_tree_gemm", bytes, 4.0 * R * C * K, [&] {
+    const TcProblem pr[2] = {{A0.p, a_mn ? A0.ks : A0.rs, B0.p, ldb0, out0, b_mn, a_mn},
+                             {A1.p, a_mn ? A1.ks : A1.rs, B1.p, ldb1, out1, b_mn, a_mn}};
+    return cu(launch_tc_gemms(pr, 2, R, C, K, o_rs, 1, h->d_status, 0, h->sm_count, st));
+  });
 }
 
 detffn_status silu_mul(detffn_handle h, const uint16_t* g, const uint16_t* u, uint16_t* hh,
@@ -713,7 +744,10 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
                         w.dec_part, w.dec_cnt, st));
       TRY(decode_plain(h, w.h + s * sw, I, WD + s * sw, I, H, sw, M, dst, H, w.dec_part, w.dec_cnt, st));
     } else {
-      TRY(gateup_slice(h, f, X, WG, WU, gate, up, saves, w.h, M, H, I, s, sw, st, sc));
+      // gate/up contract over H, which no shard splits: the shards' slices of
+      // gate, up and h are the same bits whether computed slice by slice or
+      // at once, so one launch computes all of them.
+      if (s == 0) TRY(gateup_slice(h, f, X, WG, WU, gate, up, saves, w.h, M, H, I, 0, I, st, sc));
       TRY(tree_gemm(h, f, Strided{w.h + s * sw, I, 1}, Strided{WD + s * sw, I, 1}, M, H, sw, dst, H, st, sc));
     }
   }
@@ -840,8 +874,8 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   for (long long s = 0; s < k; ++s) {
     uint16_t* cg = k == 1 ? w.cg : w.cgs + s * M * H;
     uint16_t* cu = k == 1 ? w.cu : w.cus + s * M * H;
-    TRY(tree_gemm(h, f, Strided{dG + s * sw, I, 1}, wcol(WG, s * sw), M, H, sw, cg, H, st, w.tcs));
-    TRY(tree_gemm(h, f, Strided{dU + s * sw, I, 1}, wcol(WU, s * sw), M, H, sw, cu, H, st, w.tcs));
+    TRY(tree_gemm2(h, f, Strided{dG + s * sw, I, 1}, wcol(WG, s * sw), cg, Strided{dU + s * sw, I, 1},
+                   wcol(WU, s * sw), cu, M, H, sw, H, st, w.tcs));
   }
   if (k > 1) {
     const void *pg[8], *pu[8];

@@ -228,10 +228,42 @@ struct TcsScratch {
 };
 constexpr int kSizingSms = 152;  // SM count a workspace is sized for when no handle is given
 
+// Plans are validated and worked out once per signature: a plan depends only
+// on (R, C, K, problems, CTAs, direct), and working it out walks every CTA's
+// range, which costs microseconds of host time per call at decode sizes --
+// comparable to the call's device time.  A small table keeps the recent ones.
+bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bool direct, TcsPlan* p) {
+  struct Entry {
+    long long R, C, K;
+    int np, ctas;
+    bool direct, ok, used;
+    TcsPlan plan;
+  };
+  constexpr int kEntries = 32;
+  static Entry table[kEntries];
+  static int next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : table)
+      if (e.used && e.R == R && e.C == C && e.K == K && e.np == np && e.ctas == ctas && e.direct == direct) {
+        if (e.ok) *p = e.plan;
+        return e.ok;
+      }
+  }
+  TcsPlan plan{};
+  const bool ok = tcs_plan(R, C, K, np, ctas, direct, &plan);
+  std::lock_guard<std::mutex> lock(mu);
+  table[next] = Entry{R, C, K, np, ctas, direct, ok, true, plan};
+  next = (next + 1) % kEntries;
+  if (ok) *p = plan;
+  return ok;
+}
+
 // Piece-slot bytes of a few-token contraction over C weight rows and K, two CTAs per SM.
 size_t tcs_bytes(long long C, long long K, int np, int sms) {
   TcsPlan p;
-  return tcs_plan(1, C, K, np, 2 * sms, false, &p) ? p.scratch : 0;
+  return tcs_plan_cached(1, C, K, np, 2 * sms, false, &p) ? p.scratch : 0;
 }
 
 // The plan for the scratch at hand: two CTAs per SM when the slots fit, fewer
@@ -240,12 +272,12 @@ size_t tcs_bytes(long long C, long long K, int np, int sms) {
 bool tcs_plan_fit(long long R, long long C, long long K, int np, int sms, const TcsScratch& sc, TcsPlan* p) {
   if (sc.p) {
     for (int ctas = 2 * sms; ctas >= 1; ctas = ctas * 3 / 4) {
-      if (!tcs_plan(R, C, K, np, ctas, false, p)) return false;
+      if (!tcs_plan_cached(R, C, K, np, ctas, false, p)) return false;
       if (p->scratch <= sc.bytes) return true;
       if (ctas == 1) break;
     }
   }
-  return tcs_plan(R, C, K, np, 2 * sms, true, p);
+  return tcs_plan_cached(R, C, K, np, 2 * sms, true, p);
 }
 
 struct FwdWs {

@@ -228,8 +228,9 @@ struct TcsScratch {
 };
 constexpr int kSizingSms = 152;  // SM count a workspace is sized for when no handle is given
 
-// Plans are validated and worked out once per signature: a plan depends only
-// on (R, C, K, problems, CTAs, direct), and working it out walks every CTA's
+// Plans are validated and worked out once per signature (as the transport
+// collectives do, RL-Kernel PR #356, "Design"): a plan depends only on
+// (R, C, K, problems, CTAs, direct), and working it out walks every CTA's
 // range, which costs microseconds of host time per call at decode sizes --
 // comparable to the call's device time.  A small table keeps the recent ones.
 bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bool direct, TcsPlan* p) {

@@ -169,9 +169,32 @@ def test_golden_fixtures(oracle_mod):
             bufs = [_bf16([float.fromhex(v)]) for v in case["buffers"]]
             got = oracle_mod.rank_tree(bufs, oracle_mod.BF16)[0]
             assert got == int(case["expect_bits"], 16), case["name"]
+        elif case["kind"] == "rank_tree_f16":
+            bufs = [np.float16([float.fromhex(v)]).view(np.uint16) for v in case["buffers"]]
+            got = oracle_mod.rank_tree(bufs, oracle_mod.F16)[0]
+            assert got == int(case["expect_bits"], 16), case["name"]
+        elif case["kind"] == "rank_tree_f32":
+            bufs = [np.float32([float.fromhex(v)]) for v in case["buffers"]]
+            got = oracle_mod.rank_tree(bufs, oracle_mod.F32)
+            assert int(got.view(np.uint32)[0]) == int(case["expect_bits"], 16), case["name"]
         elif case["kind"] == "leaf_lane":
             a = _bf16([float.fromhex(v) for v in case["a"]])
             b = _bf16([float.fromhex(v) for v in case["b"]])
             assert oracle_mod.leaf(a, b, 64, 1) == float.fromhex(case["expect"]), case["name"]
         else:
             raise AssertionError(case["kind"])
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 8])
+def test_rank_tree_integers_are_exact_in_every_dtype(oracle_mod, n):
+    """Small integers add exactly in FP32, FP16 and BF16 whatever the order:
+    the rank tree must then return the exact sum (n = 1: the buffer itself)."""
+    rng = np.random.default_rng(n)
+    ints = [rng.integers(-16, 17, 1000) for _ in range(n)]   # |sum| <= 128: exact in BF16
+    want = np.sum(ints, axis=0).astype(np.float32)
+    got32 = oracle_mod.rank_tree([v.astype(np.float32) for v in ints], oracle_mod.F32)
+    assert np.array_equal(got32, want)
+    got16 = oracle_mod.rank_tree([v.astype(np.float16).view(np.uint16) for v in ints], oracle_mod.F16)
+    assert np.array_equal(got16.view(np.float16).astype(np.float32), want)
+    gotb = oracle_mod.rank_tree([_bf16(v.astype(np.float32)) for v in ints], oracle_mod.BF16)
+    assert np.array_equal((gotb.astype(np.uint32) << 16).view(np.float32), want)

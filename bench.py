@@ -296,7 +296,11 @@ def run_ours(args):
 
     ws_n, rank, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
-    libbuild.build()
+    # One rank compiles (the others would race on the same object files);
+    # the rest load the library once it is there.
+    if rank == 0:
+        libbuild.build()
+    barrier(ws_n)
     path = {"auto": G.PATH_AUTO, "exact": G.PATH_EXACT, "tensor": G.PATH_TENSOR}[args.path]
 
     def dev(a):

@@ -24,6 +24,7 @@ struct detffn_handle_s {
   uint16_t* d_silu = nullptr;   // [65536] BF16 SiLU by gate bit pattern
   float* d_dsilu = nullptr;     // [65536] FP32 SiLU' by gate bit pattern
   int* d_status = nullptr;      // device status word (bounded waits)
+  Waits wt;                     // the current call's wait settings (status word, poll limit, test stall)
   std::vector<uint16_t> h_silu;
   std::vector<float> h_dsilu;
   // Measurement: event pairs around launches while profiling is on.
@@ -156,6 +157,7 @@ namespace {
 struct Opts {
   int path = DETFFN_PATH_AUTO;
   int shards = 1;
+  int flags = 0;
   long long spin_limit = 0;
 };
 
@@ -167,12 +169,21 @@ detffn_status read_opts(const detffn_options* o, Opts* out) {
     if (!(o->shards == 0 || o->shards == 1 || o->shards == 2 || o->shards == 4 || o->shards == 8))
       return DETFFN_ERR_INVALID_ARG;
     if (o->spin_limit < 0) return DETFFN_ERR_INVALID_ARG;
+    if (o->flags & ~DETFFN_FLAG_TEST_STALL) return DETFFN_ERR_INVALID_ARG;
     r.path = o->path;
     r.shards = o->shards ? o->shards : 1;
+    r.flags = o->flags;
     r.spin_limit = o->spin_limit;
   }
   *out = r;
   return DETFFN_OK;
+}
+
+// The wait settings the launches of one call take from its options.
+void set_waits(detffn_handle h, const Opts& o) {
+  h->wt.status = h->d_status;
+  h->wt.spin = o.spin_limit;
+  h->wt.stall = (o.flags & DETFFN_FLAG_TEST_STALL) ? 1 : 0;
 }
 
 // The kernel family a call uses.  EXACT: CUDA-core kernels with LANE8x8
@@ -430,7 +441,7 @@ bool tc_mn_ok(const Strided& X) {
 
 detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long long R, long long C,
                         long long K, uint16_t* out, long long o_rs, cudaStream_t st,
-                        const TcsScratch& sc = TcsScratch()) {
+                        const TcsScratch& sc = TcsScratch(), float* dump = nullptr) {
   const double bytes = 2.0 * ((double)R * K + (double)C * K + (double)R * C);
   if (f == kTensor) {
     const bool b_mn = tc_mn_ok(B), a_mn = tc_mn_ok(A);
@@ -442,11 +453,11 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
       if (!tcs_plan_fit(R, C, K, 1, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
       const TcsProblem pr{B.p, ldb, A.p, A.rs, out, b_mn};
       return timed(h, st, "tcs_tree_gemm", bytes, 2.0 * R * C * K,
-                   [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->d_status, 0, st)); });
+                   [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->wt, st, dump)); });
     }
     return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
-      return cu(launch_tc_gemm(A.p, a_mn ? A.ks : A.rs, B.p, ldb, R, C, K, out, o_rs, 1, h->d_status, 0,
-                               h->sm_count, st, b_mn, a_mn));
+      return cu(launch_tc_gemm(A.p, a_mn ? A.ks : A.rs, B.p, ldb, R, C, K, out, o_rs, 1, h->wt, h->sm_count, st,
+                               b_mn, a_mn, dump));
     });
   }
   return timed(h, st, "tree_gemm_exact", bytes, 2.0 * R * C * K,
@@ -474,12 +485,12 @@ detffn_status tree_gemm2(detffn_handle h, Family f, Strided A0, Strided B0, uint
     if (!tcs_plan_fit(R, C, K, 2, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
     const TcsProblem pr[2] = {{B0.p, ldb0, A0.p, A0.rs, out0, b_mn}, {B1.p, ldb1, A1.p, A1.rs, out1, b_mn}};
     return timed(h, st, "tcs_tree_gemm", bytes, 4.0 * R * C * K,
-                 [&] { return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->d_status, 0, st)); });
+                 [&] { return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st)); });
   }
   return timed(h, st, "tc_tree_gemm", bytes, 4.0 * R * C * K, [&] {
     const TcProblem pr[2] = {{A0.p, a_mn ? A0.ks : A0.rs, B0.p, ldb0, out0, b_mn, a_mn},
                              {A1.p, a_mn ? A1.ks : A1.rs, B1.p, ldb1, out1, b_mn, a_mn}};
-    return cu(launch_tc_gemms(pr, 2, R, C, K, o_rs, 1, h->d_status, 0, h->sm_count, st));
+    return cu(launch_tc_gemms(pr, 2, R, C, K, o_rs, 1, h->wt, h->sm_count, st));
   });
 }
 
@@ -537,7 +548,7 @@ detffn_status decode_gateup(detffn_handle h, const uint16_t* x, long long ldx, c
       a.out = hh + p * ldo; a.ldo = ldo;
       a.gsave = gsave ? gsave + p * ldo : nullptr;
       a.usave = usave ? usave + p * ldo : nullptr;
-      a.silu = h->d_silu; a.status = h->d_status; a.spin_limit = 0;
+      a.silu = h->d_silu; a.status = h->wt.status; a.spin_limit = h->wt.spin; a.stall = h->wt.stall;
       const cudaError_t e = launch_decode_exact(a, h->sm_count, st);
       if (e != cudaSuccess) return DETFFN_ERR_CUDA;
     }
@@ -557,7 +568,7 @@ detffn_status decode_plain(detffn_handle h, const uint16_t* x, long long ldx, co
       a.M = (int)(M - p < 8 ? M - p : 8);
       a.part = part; a.cnt = cnt;
       a.out = out + p * ldo; a.ldo = ldo;
-      a.silu = h->d_silu; a.status = h->d_status; a.spin_limit = 0;
+      a.silu = h->d_silu; a.status = h->wt.status; a.spin_limit = h->wt.spin; a.stall = h->wt.stall;
       const cudaError_t e = launch_decode_exact(a, h->sm_count, st);
       if (e != cudaSuccess) return DETFFN_ERR_CUDA;
     }
@@ -705,13 +716,13 @@ detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const u
       const TcsProblem pr[2] = {{BG.p, H, x, H, keep ? gate + s * w : nullptr},
                                 {BU.p, H, x, H, keep ? up + s * w : nullptr}};
       return timed(h, st, "tcs_gateup", bytes, 4.0 * M * w * H, [&] {
-        return cu(launch_tcs_gateup(p, pr, hh + s * w, I, h->d_silu, sc.p, sc.bytes, h->d_status, 0, st));
+        return cu(launch_tcs_gateup(p, pr, hh + s * w, I, h->d_silu, sc.p, sc.bytes, h->wt, st));
       });
     }
     const double bytes = 2.0 * (2.0 * w * H + (double)M * H + 2.0 * M * w);
     TRY(timed(h, st, "tc_tree_gemm", bytes, 4.0 * M * w * H, [&] {
       const TcProblem pr[2] = {{x, H, BG.p, H, gate + s * w}, {x, H, BU.p, H, up + s * w}};
-      return cu(launch_tc_gemms(pr, 2, M, w, H, I, 1, h->d_status, 0, h->sm_count, st));
+      return cu(launch_tc_gemms(pr, 2, M, w, H, I, 1, h->wt, h->sm_count, st));
     }));
   } else {
     TRY(tree_gemm(h, f, X, Strided{Wg + s * w * H, H, 1}, M, w, H, gate + s * w, I, st));
@@ -727,6 +738,7 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
   if (!h || !out) return DETFFN_ERR_INVALID_ARG;
   Opts o;
   TRY(read_opts(opts, &o));
+  set_waits(h, o);
   TRY(check_sizes(M, H, I));
   TRY(check_ffn_ptrs(x, Wg, Wu, Wd));
   if (!aligned2(out) || !aligned2(gate_save) || !aligned2(up_save)) return DETFFN_ERR_ALIGN;
@@ -848,6 +860,7 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   if (!h || !gate || !up || !dOut || !dX || !dWg || !dWu || !dWd) return DETFFN_ERR_INVALID_ARG;
   Opts o;
   TRY(read_opts(opts, &o));
+  set_waits(h, o);
   TRY(check_sizes(M, H, I));
   TRY(check_ffn_ptrs(x, Wg, Wu, Wd));
   const void* al[] = {gate, up, dOut, dX, dWg, dWu, dWd, dh_save, dU_save, dG_save};
@@ -939,6 +952,7 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
     return DETFFN_ERR_INVALID_ARG;
   Opts o;
   TRY(read_opts(opts, &o));
+  set_waits(h, o);
   long long M = 0;
   for (int c = 0; c < n_chunks; ++c) {
     if (chunk_tokens[c] < 0) return DETFFN_ERR_SHAPE;
@@ -1022,6 +1036,7 @@ extern "C" detffn_status detffn_tree_gemm(detffn_handle h, const void* A, long l
   if (R > 1 && o_rs < C) return DETFFN_ERR_INVALID_ARG;
   Opts o;
   TRY(read_opts(opts, &o));
+  set_waits(h, o);
   if (R == 0 || C == 0) return DETFFN_OK;
   Family f = kExact;
   const Strided SA{(const uint16_t*)A, a_rs, a_ks}, SB{(const uint16_t*)B, b_rs, b_ks};
@@ -1034,6 +1049,29 @@ extern "C" detffn_status detffn_tree_gemm(detffn_handle h, const void* A, long l
   TRYCU(cudaSetDevice(h->device));
   return tree_gemm(h, f, Strided{(const uint16_t*)A, a_rs, a_ks}, Strided{(const uint16_t*)B, b_rs, b_ks},
                    R, C, K, (uint16_t*)out, o_rs, (cudaStream_t)stream);
+}
+
+extern "C" detffn_status detffn_tree_gemm_leaves(detffn_handle h, const void* A, long long a_rs,
+                                                 long long a_ks, const void* B, long long b_rs,
+                                                 long long b_ks, long long R, long long C, long long K,
+                                                 void* out, long long o_rs, void* leaves, void* stream,
+                                                 const detffn_options* opts) {
+  if (!h || !out || !leaves || R < 0 || C < 0 || K <= 0 || K > kMaxK) return DETFFN_ERR_INVALID_ARG;
+  if (!A || !B) return DETFFN_ERR_INVALID_ARG;
+  if (!aligned2(A) || !aligned2(B) || !aligned2(out) || ((uintptr_t)leaves & 3u)) return DETFFN_ERR_ALIGN;
+  if (R > 1 && o_rs < C) return DETFFN_ERR_INVALID_ARG;
+  Opts o;
+  TRY(read_opts(opts, &o));
+  set_waits(h, o);
+  if (o.path == DETFFN_PATH_EXACT) return DETFFN_ERR_UNSUPPORTED;  // its leaves are the oracle's order
+  if (R == 0 || C == 0) return DETFFN_OK;
+  const Strided SA{(const uint16_t*)A, a_rs, a_ks}, SB{(const uint16_t*)B, b_rs, b_ks};
+  const bool ok = tc_len_ok(K) && (tc_operands_ok(SA) || (tc_mn_ok(SA) && R > 32)) &&
+                  (tc_operands_ok(SB) || tc_mn_ok(SB));
+  if (!ok) return DETFFN_ERR_UNSUPPORTED;
+  TRYCU(cudaSetDevice(h->device));
+  return tree_gemm(h, kTensor, SA, SB, R, C, K, (uint16_t*)out, o_rs, (cudaStream_t)stream, TcsScratch(),
+                   (float*)leaves);
 }
 
 extern "C" detffn_status detffn_profiling(detffn_handle h, int enable) {
@@ -1079,6 +1117,17 @@ extern "C" detffn_status detffn_selfcheck_pieces(int max_levels, unsigned long l
   if (!failures || max_levels < 0 || max_levels > kTcsMaxLv) return DETFFN_ERR_INVALID_ARG;
   *failures = tcs_selfcheck_pieces(max_levels);
   return DETFFN_OK;
+}
+
+extern "C" detffn_status detffn_cvt_f32_bf16(detffn_handle h, const void* in, void* out, long long n,
+                                             void* stream) {
+  if (!h || n < 0) return DETFFN_ERR_INVALID_ARG;
+  if (n == 0) return DETFFN_OK;
+  if (!in || !out) return DETFFN_ERR_INVALID_ARG;
+  if (((uintptr_t)in & 3u) || ((uintptr_t)out & 1u)) return DETFFN_ERR_ALIGN;
+  if (overlap(in, 4 * n, out, 2 * n)) return DETFFN_ERR_INVALID_ARG;
+  TRYCU(cudaSetDevice(h->device));
+  return cu(launch_cvt_bf16((const float*)in, (uint16_t*)out, n, h->sm_count, (cudaStream_t)stream));
 }
 
 extern "C" detffn_status detffn_selfcheck_node_add(detffn_handle h, unsigned long long* mismatches) {

@@ -47,6 +47,15 @@ __host__ __device__ __forceinline__ long long n_leaves(long long K) { return (K 
 // ---------------------------------------------------------------------------
 // Internal launchers (all asynchronous on `st`; they return cudaGetLastError)
 // ---------------------------------------------------------------------------
+// Bounded waits of a launch: where a timeout is recorded, the poll limit of
+// the role loops' waits (0 = the default), and a test-only switch under which
+// the kernels issue no copies, so that their first wait runs out.
+struct Waits {
+  int* status = nullptr;
+  long long spin = 0;
+  int stall = 0;
+};
+
 struct Strided {
   const uint16_t* p;
   long long rs, ks;  // element strides of a row and of a K position
@@ -72,6 +81,8 @@ cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out,
 // Self-check: counts pairs where add.rn.bf16x2 differs from the tree node.
 cudaError_t launch_check_node_add(unsigned long long begin, unsigned long long end, unsigned long long* bad,
                                   int sm_count, cudaStream_t st);
+// out[i] = rne_bf16(in[i]) with the kernels' own conversion (diagnostic).
+cudaError_t launch_cvt_bf16(const float* in, uint16_t* out, long long n, int sm_count, cudaStream_t st);
 // Balanced rank tree over n in {1,2,4,8} buffers.
 cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long count, int dtype,
                              int sm_count, cudaStream_t st);

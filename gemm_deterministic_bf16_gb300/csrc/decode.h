@@ -25,6 +25,7 @@ struct DecArgs {
   const uint16_t* silu;
   int* status;
   long long spin_limit;
+  int stall;           // test only: issue no copies, so the first wait runs out
 };
 
 // Leaf-block geometry for K: fills S (leaves per block), NB (blocks) and

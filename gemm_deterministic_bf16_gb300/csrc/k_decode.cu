@@ -20,6 +20,8 @@
 // ticket; nothing waits on another CTA) applies the top of the tree over the
 // block roots and the epilogue: a plain BF16 store, or for the gate/up pair
 // the fused stage boundary h = bf16(bf16(SiLU(gate)) * up).
+#include <mutex>
+
 #include "common.cuh"
 #include "decode.h"
 #include "ptx.cuh"
@@ -195,13 +197,18 @@ __global__ void __launch_bounds__(Geo<S>::THREADS) k_decode(DecArgs a) {
       if (slot_row(q * RB + r, wr, pi)) bulk_g2s(stage + s * STAGEB + r * ROWB, wr, ROWB, &full[s]);
   };
 
+  // A wait of an earlier launch ran out (the status word is set until the
+  // caller reads it): its outputs, which may be this launch's inputs (h, the
+  // tickets), are unfinished, so this launch does nothing.
+  if (__syncthreads_or(a.status != nullptr && *(volatile int*)a.status != 0)) return;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0)
-    for (int q = 0; q < kStages && q < nbatch; ++q) issue(q);
+  int issued = 0;  // batches whose copies thread 0 has issued
+  if (tid == 0 && !a.stall)
+    for (; issued < kStages && issued < nbatch; ++issued) issue(issued);
 
   // This lane's x slice: 8 contiguous K positions for every token, then
   // permuted so that slot j holds token j ^ (l % MT) (the order reduce_leaf
@@ -256,7 +263,10 @@ __global__ void __launch_bounds__(Geo<S>::THREADS) k_decode(DecArgs a) {
       if (l < MT) lv[(r * 8 + l) * (S + 1) + g] = leaf;
     }
     __syncthreads();
-    if (tid == 0 && q + kStages < nbatch) issue(q + kStages);
+    if (tid == 0 && q + kStages < nbatch) {
+      issue(q + kStages);
+      issued = q + kStages + 1;
+    }
     for (int i = tid; i < MT * RB; i += NT) {
       const int t = i / RB, r = i % RB;
       const uint16_t* wr;
@@ -267,10 +277,12 @@ __global__ void __launch_bounds__(Geo<S>::THREADS) k_decode(DecArgs a) {
     __syncthreads();
   }
   if (q < nbatch) {
-    // A wait ran out: drain this CTA's own copies (bounded), leave the tile unfinished.
+    // A wait ran out: drain the copies this CTA issued (on the long bound,
+    // whatever the call's poll limit: it exits with no copy in flight), and
+    // leave the tile unfinished.
     if (tid == 0)
-      for (int p = q; p < q + kStages && p < nbatch; ++p)
-        mbar_wait(&full[p % kStages], (uint32_t)((p / kStages) & 1), limit, nullptr);
+      for (int p = q; p < issued; ++p)
+        mbar_wait(&full[p % kStages], (uint32_t)((p / kStages) & 1), kDefaultSpin, nullptr);
     __syncthreads();
     return;
   }
@@ -295,14 +307,19 @@ __global__ void __launch_bounds__(Geo<S>::THREADS) k_decode(DecArgs a) {
 template <int MT, int S>
 cudaError_t launch_ms(DecArgs a, int NB, int sm_count, cudaStream_t st) {
   using G = Geo<S>;
-  static int per_sm = 0;  // resident CTAs per SM for this instance (registers, threads, smem)
-  if (!per_sm) {
-    cudaError_t e = cudaFuncSetAttribute(k_decode<MT, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode<MT, S>, G::THREADS, G::SMEM);
-    if (e != cudaSuccess) return e;
+  // Resident CTAs per SM for this instance (registers, threads, smem), worked
+  // out once; concurrent first calls (several host threads, the handle path
+  // and the allocation-free entry point) all wait for the one set-up.
+  static std::once_flag once;
+  static cudaError_t setup_err = cudaSuccess;
+  static int per_sm = 0;
+  std::call_once(once, [] {
+    setup_err = cudaFuncSetAttribute(k_decode<MT, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+    if (setup_err == cudaSuccess)
+      setup_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode<MT, S>, G::THREADS, G::SMEM);
     if (per_sm < 1) per_sm = 1;
-  }
+  });
+  if (setup_err != cudaSuccess) return setup_err;
   // Rows per tile so that the grid is one wave of resident CTAs.
   long long tiles = ((long long)sm_count * per_sm) / NB;
   if (tiles < 1) tiles = 1;

@@ -270,4 +270,21 @@ cudaError_t launch_check_node_add(unsigned long long begin, unsigned long long e
   k_check_node_add<<<sm_count * 8, 256, 0, st>>>(begin, end, bad);
   return cudaGetLastError();
 }
+
+// ------------- the kernels' FP32 -> BF16 rounding, exposed for tests -------------
+// out[i] = f2bf(in[i]): the conversion every kernel uses for leaves, nodes
+// and stage boundaries (cvt.rn.bf16.f32), so that a test can compare it with
+// an independent round-to-nearest-even rule on any set of bit patterns.
+namespace {
+__global__ void k_cvt_bf16(const float* in, uint16_t* out, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    out[i] = f2bf(in[i]);
+}
+}  // namespace
+
+cudaError_t launch_cvt_bf16(const float* in, uint16_t* out, long long n, int sm_count, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  k_cvt_bf16<<<sm_count * 8, 256, 0, st>>>(in, out, n);
+  return cudaGetLastError();
+}
 }  // namespace detffn

@@ -35,6 +35,8 @@
 // stops, drains its own copies and MMAs (bounded) and frees its TMEM.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 #include "tc.h"
@@ -145,6 +147,8 @@ struct TcArgs {
   long long ld_r, ld_c;
   int* status;
   long long spin;
+  int stall;        // test only: the producer issues no loads
+  float* dump;      // leaf dump (DUMP instances): [np][R][C][L] FP32 leaves
 };
 
 // Writes the COLS columns of one row held as packed BF16 pairs: element i goes
@@ -171,7 +175,7 @@ __device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int 
   return stk + (((m - T::REG_LV) * T::HALVES + half) * T::WORDS + w) * BM + row;
 }
 
-template <int BN, int GG>
+template <int BN, int GG, bool DUMP>
 __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -191,6 +195,10 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
   const int tiles = a.num_m * a.num_n;
   const int units = tiles * a.np;  // unit u: problem u % np, then tile
   const long long limit = a.spin > 0 ? a.spin : kDefaultSpin;
+  // A wait of an earlier launch ran out (the status word is set until the
+  // caller reads it): its outputs, which may be this launch's inputs, are
+  // unfinished, so this launch does nothing.
+  if (__syncthreads_or(a.status != nullptr && *(volatile int*)a.status != 0)) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
           }
           rv.next(T::NBUF);
         }
-        if (elect_one()) {
+        if (!a.stall && elect_one()) {
           unsigned char* st = stages + s * T::STAGE;
           mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
           const int x = j * BK;
@@ -268,10 +276,12 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
         __syncwarp();
       }
     }
-    // Drain: the last loads issued into each stage have landed.
-    if (lane == 0)
+    // Drain: the last loads issued into each stage have landed (on the long
+    // bound, whatever the call's poll limit: no CTA exits with copies in
+    // flight).
+    if (lane == 0 && !a.stall)
       for (long long i = (it > NS ? it - NS : 0); i < it; ++i)
-        mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), limit, nullptr);
+        mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), kDefaultSpin, nullptr);
   } else if (warp < kEpiWarp0) {
     const int q = warp - 1;  // issuer index
     // ---------------- MMA issuers (converged warps; one lane each issues) ----------------
@@ -317,7 +327,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     }
     if (elect_one()) tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
     __syncwarp();
-    if (q == 0 && lane == 0) mbar_wait(&bars->fin, 0, limit, nullptr);  // all issuers' MMAs
+    // Every issuer's MMAs have completed before TMEM is freed (long bound).
+    if (q == 0 && lane == 0) mbar_wait(&bars->fin, 0, kDefaultSpin, nullptr);
   } else {
     // ---------------- epilogue: leaves -> tree ----------------
     const int ew = warp - kEpiWarp0;
@@ -364,6 +375,12 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
             tmem_ld32(tmem + lane_addr + b0 + (uint32_t)(col0 + 32 * c), va);
             if (c + 1 < T::COLS / 32) tmem_ld32(tmem + lane_addr + b0 + (uint32_t)(col0 + 32 * c + 32), vb);
             tmem_wait_ld();
+            if constexpr (DUMP) {
+              float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
+              const long long cc = (long long)tn * BN + col0 + 32 * c;
+              dump_leaves(d, r, cc, a.R, a.C, a.L, q, va);
+              if (c + 1 < T::COLS / 32) dump_leaves(d, r, cc + 32, a.R, a.C, a.L, q, vb);
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) root[16 * c + i] = pack_bf16x2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]));
             if (c + 1 < T::COLS / 32)
@@ -380,6 +397,13 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
           if constexpr (GG >= 2) tmem_ld32(tmem + lane_addr + b1 + col, v1);
           if constexpr (GG >= 3) tmem_ld32(tmem + lane_addr + b2 + col, v2);
           tmem_wait_ld();
+          if constexpr (DUMP) {
+            float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
+            const long long cc = (long long)tn * BN + col;
+            dump_leaves(d, r, cc, a.R, a.C, a.L, q * GG, v0);
+            if constexpr (GG >= 2) dump_leaves(d, r, cc, a.R, a.C, a.L, q * GG + 1, v1);
+            if constexpr (GG >= 3) dump_leaves(d, r, cc, a.R, a.C, a.L, q * GG + 2, v2);
+          }
 #pragma unroll
           for (int i = 0; i < WC; ++i) {
             // Pairs of adjacent columns, added two at a time (add.rn.f32x2).
@@ -467,15 +491,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
+  static std::once_flag once;
   static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  std::call_once(once, [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+  });
   return fn;
 }
 
@@ -495,35 +520,43 @@ bool tc_make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long
 
 namespace {
 
-template <int BN, int GG>
+template <int BN, int GG, bool DUMP>
 cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(k_tc<BN, GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<BN>::MAX_SMEM);
-    if (e != cudaSuccess) return e;
+  static std::once_flag once;
+  static cudaError_t setup_err = cudaSuccess;
+  std::call_once(once, [] {
+    setup_err = cudaFuncSetAttribute(k_tc<BN, GG, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     TcGeo<BN>::MAX_SMEM);
+    if (setup_err != cudaSuccess) return;
     // The in-kernel register split (setmaxnreg) hands over exactly the
     // launch's registers; with any other count it could not complete.
     cudaFuncAttributes fa;
-    const cudaError_t e2 = cudaFuncGetAttributes(&fa, k_tc<BN, GG>);
-    if (e2 != cudaSuccess) return e2;
-    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
-    attr = true;
-  }
+    setup_err = cudaFuncGetAttributes(&fa, k_tc<BN, GG, DUMP>);
+    if (setup_err == cudaSuccess && fa.numRegs != kRegsLaunch) setup_err = cudaErrorInvalidConfiguration;
+  });
+  if (setup_err != cudaSuccess) return setup_err;
   const int units = a.num_m * a.num_n * a.np;
   const int slots = sm_count;
   const int grid = units < slots ? units : slots;
   const int smem = TcGeo<BN>::smem_for(a.G, a.E, a.nstage);
-  k_tc<BN, GG><<<grid, TcGeo<BN>::THREADS, smem, st>>>(m[0], m[1], m[2], m[3], m[4], m[5], a);
+  k_tc<BN, GG, DUMP><<<grid, TcGeo<BN>::THREADS, smem, st>>>(m[0], m[1], m[2], m[3], m[4], m[5], a);
   return cudaGetLastError();
 }
 
 template <int BN>
 cudaError_t launch_bn(const CUtensorMap* m, const TcArgs& a, int sm_count, cudaStream_t st) {
+  if (a.dump) {
+    switch (a.G) {
+      case 1: return launch_bng<BN, 1, true>(m, a, sm_count, st);
+      case 2: return launch_bng<BN, 2, true>(m, a, sm_count, st);
+      case 3: return launch_bng<BN, 3, true>(m, a, sm_count, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.G) {
-    case 1: return launch_bng<BN, 1>(m, a, sm_count, st);
-    case 2: return launch_bng<BN, 2>(m, a, sm_count, st);
-    case 3: return launch_bng<BN, 3>(m, a, sm_count, st);
+    case 1: return launch_bng<BN, 1, false>(m, a, sm_count, st);
+    case 2: return launch_bng<BN, 2, false>(m, a, sm_count, st);
+    case 3: return launch_bng<BN, 3, false>(m, a, sm_count, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -556,8 +589,8 @@ bool tc_tree_shape(long long L, int* G, int* E) {
 }
 
 cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long C, long long K,
-                            long long ld_r, long long ld_c, int* status, long long spin_limit, int sm_count,
-                            cudaStream_t st) {
+                            long long ld_r, long long ld_c, const Waits& wt, int sm_count, cudaStream_t st,
+                            float* dump) {
   constexpr int bn = 128;
   if (R <= 0 || C <= 0) return cudaSuccess;
   if (np < 1 || np > 2) return cudaErrorInvalidValue;
@@ -584,8 +617,10 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   a.out2 = np > 1 ? pr[1].out : nullptr;
   a.ld_r = ld_r;
   a.ld_c = ld_c;
-  a.status = status;
-  a.spin = spin_limit;
+  a.status = wt.status;
+  a.spin = wt.spin;
+  a.stall = wt.stall;
+  a.dump = dump;
   a.nstage = TcGeo<bn>::stages_for(a.G, a.E);
   if (a.nstage > TcGeo<bn>::NBUF) a.nstage = TcGeo<bn>::NBUF;  // stage reuse is read off the leaf barriers
   if (a.nstage < 2) return cudaErrorInvalidValue;
@@ -615,10 +650,10 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
 
 cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
                            long long R, long long C, long long K, uint16_t* out, long long ld_r,
-                           long long ld_c, int* status, long long spin_limit, int sm_count, cudaStream_t st,
-                           bool b_mn, bool a_mn) {
+                           long long ld_c, const Waits& wt, int sm_count, cudaStream_t st,
+                           bool b_mn, bool a_mn, float* dump) {
   const TcProblem p{A, lda, B, ldb, out, b_mn, a_mn};
-  return launch_tc_gemms(&p, 1, R, C, K, ld_r, ld_c, status, spin_limit, sm_count, st);
+  return launch_tc_gemms(&p, 1, R, C, K, ld_r, ld_c, wt, sm_count, st, dump);
 }
 
 }  // namespace detffn

@@ -28,6 +28,7 @@
 // stops, drains its own copies and MMAs (bounded) and frees its TMEM.
 #include <cuda.h>
 
+#include <mutex>
 #include <utility>
 
 #include "common.cuh"
@@ -109,6 +110,9 @@ struct TcsArgs {
   long long ldo;
   int* status;
   long long spin;
+  int stall;        // test only: the producers issue no loads
+  int L;            // leaves per tree (G * 2^E)
+  float* dump;      // leaf dump (DUMP instances): [np][R][C][L] FP32 leaves
 };
 
 // First group of CTA b's range.  Direct mode deals whole tiles: segment
@@ -126,6 +130,16 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, lo
   *abort_flag = 1;
   if (status) atomicExch(status, (int)DETFFN_ERR_TIMEOUT);
   return false;
+}
+
+// Leaf dump (diagnostic instances): weight row crow's leaves for tokens
+// t0 .. t0 + 15, as leaf j of the [R][C][L] array (tokens are the rows).
+__device__ __forceinline__ void dump_tokens(float* d, long long crow, int t0, int R, int C, int L, int j,
+                                            const uint32_t (&v)[16]) {
+  if (crow >= C) return;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if (t0 + i < R) d[((size_t)(t0 + i) * (size_t)C + (size_t)crow) * (size_t)L + (size_t)j] = __uint_as_float(v[i]);
 }
 
 // Writes one row (all tokens) of the CTA's next piece: the row's 64 bytes
@@ -161,7 +175,7 @@ __device__ __forceinline__ void load_w(unsigned char* dst, const CUtensorMap* mW
 // segment (tile, problem) after segment, groups qa..qb-1 of each.
 // 128 registers: registers are granted per 4 warps, so a CTA of 7 warps holds
 // 8 x 32 x 128 = 32,768 and two CTAs fit one SM's 65,536.
-template <int GG>
+template <int GG, bool DUMP>
 __global__ void __maxnreg__(128)
     k_tcs(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
           const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmX2, const TcsArgs a) {
@@ -180,6 +194,10 @@ __global__ void __maxnreg__(128)
   const long long w0 = range_lo(blockIdx.x, a.W, gridDim.x, Q, direct);
   const long long w1 = range_lo(blockIdx.x + 1ll, a.W, gridDim.x, Q, direct);
   const long long limit = a.spin > 0 ? a.spin : kDefaultSpin;
+  // A wait of an earlier launch ran out (the status word is set until the
+  // caller reads it): its outputs, which may be this launch's inputs, are
+  // unfinished, so this launch does nothing.
+  if (__syncthreads_or(a.status != nullptr && *(volatile int*)a.status != 0)) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -221,7 +239,7 @@ __global__ void __maxnreg__(128)
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     // Before the previous kernel has finished: this producer's share of the
     // first NS stages, weight tiles only (no kernel here writes weights).
-    {
+    if (!a.stall) {
       long long it = 0;
       for (long long w = w0; w < w1 && it < NS;) {
         const long long s = w / Q;
@@ -267,7 +285,7 @@ __global__ void __maxnreg__(128)
             break;
           }
         }
-        if (elect_one()) {
+        if (!a.stall && elect_one()) {
           if (reuse) {
             mbar_arrive_expect_tx(&bars->full[st], (uint32_t)STAGE);
             load_w(dst, mW, j, t, &bars->full[st], pol, a.w_mn);
@@ -278,10 +296,12 @@ __global__ void __maxnreg__(128)
       }
       w = s * Q + qb;
     }
-    // Drain: this producer's last loads have landed.
-    if (lane == 0)
+    // Drain: this producer's last loads have landed (on the long bound,
+    // whatever the call's poll limit: no CTA exits with copies in flight).
+    if (lane == 0 && !a.stall)
       for (long long i = (it > NS ? it - NS : 0); i < it; ++i)
-        if ((int)(i % kProd) == warp) mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), limit, nullptr);
+        if ((int)(i % kProd) == warp)
+          mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), kDefaultSpin, nullptr);
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (converged warp; one lane issues) ----------------
     // Leaf n of this CTA's range uses stage n % NS and TMEM buffer n % kNBuf;
@@ -313,7 +333,7 @@ __global__ void __maxnreg__(128)
     }
     if (elect_one()) tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
     __syncwarp();
-    if (lane == 0) mbar_wait(&bars->fin, 0, limit, nullptr);
+    if (lane == 0) mbar_wait(&bars->fin, 0, kDefaultSpin, nullptr);  // before TMEM is freed (long bound)
   } else {
     // ---------------- epilogue: leaves -> group roots -> pieces ----------------
     grid_dep_wait();  // its stores may overwrite what the previous kernel reads
@@ -344,6 +364,9 @@ __global__ void __maxnreg__(128)
                        b2 = (uint32_t)(((lc + 2) % kNBuf) * BN);
         // The group root: a lone leaf rounded once, l0 + l1, or l0 + (l1 + l2).
         uint32_t root[WORDS];
+        // Leaf dump: this thread's weight row of the tile, tokens 16 c + i.
+        float* const dmp = DUMP ? a.dump + (size_t)(s % a.np) * a.R * a.C * a.L : nullptr;
+        const long long crow = (s / a.np) * BM + row;
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c) {
           uint32_t v0[16];
@@ -352,11 +375,16 @@ __global__ void __maxnreg__(128)
             tmem_ld16(tmem + lane_addr + b1 + 16 * c, v1);
             tmem_ld16(tmem + lane_addr + b2 + 16 * c, v2);
             tmem_wait_ld();
+            if constexpr (DUMP) {
+              dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG + 1, v1);
+              dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG + 2, v2);
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               n12[i] = pack_bf16x2_of(add_f32x2(f32x2(v1[2 * i], v1[2 * i + 1]), f32x2(v2[2 * i], v2[2 * i + 1])));
             tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
             tmem_wait_ld();
+            if constexpr (DUMP) dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG, v0);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               root[8 * c + i] =
@@ -366,12 +394,17 @@ __global__ void __maxnreg__(128)
             tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
             tmem_ld16(tmem + lane_addr + b1 + 16 * c, v1);
             tmem_wait_ld();
+            if constexpr (DUMP) {
+              dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG, v0);
+              dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG + 1, v1);
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               root[8 * c + i] = pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(v1[2 * i], v1[2 * i + 1])));
           } else {
             tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
             tmem_wait_ld();
+            if constexpr (DUMP) dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG, v0);
 #pragma unroll
             for (int i = 0; i < 8; ++i) root[8 * c + i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
           }
@@ -466,6 +499,7 @@ struct TcsTopArgs {
   long long ldo;    // row stride of out0, out1 and h (elements)
   uint16_t* h;      // fused: h = bf16(SiLU(gate)) * up, rounded to BF16; null: plain
   const uint16_t* silu;
+  const int* status;
 };
 
 struct PieceRef {
@@ -680,6 +714,9 @@ __global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
   grid_dep_launch();
   __syncthreads();
   grid_dep_wait();  // the streaming kernel's pieces are complete and visible
+  // A bounded wait of the streaming kernel (or of an earlier launch) ran out:
+  // the pieces are unfinished, so nothing is folded or stored.
+  if (__syncthreads_or(a.status != nullptr && *(volatile int*)a.status != 0)) return;
 #pragma unroll
   for (int g = 0; g < NSEG; ++g) {
     f[g].b = first_cta(a, s0 + g);
@@ -810,7 +847,7 @@ cudaError_t launch_dependent(void (*k)(KArgs...), dim3 grid, int threads, int sm
 }
 
 cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo, uint16_t* h, const uint16_t* silu,
-                       void* scratch, size_t scratch_bytes, int* status, long long spin, cudaStream_t st) {
+                       void* scratch, size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump) {
   if (!plan.direct && (!scratch || scratch_bytes < plan.scratch || ((uintptr_t)scratch & 15u)))
     return cudaErrorInvalidValue;
   if (plan.direct && h) return cudaErrorInvalidValue;
@@ -827,10 +864,12 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
         !tc_make_map(&m[2 * p + 1], q.X, plan.R, plan.K, q.ldx, BN))
       return cudaErrorInvalidValue;
   }
-  static bool attr = false;
-  if (!attr) {
+  static std::once_flag once;
+  static cudaError_t setup_err = cudaSuccess;
+  std::call_once(once, [] {
     cudaError_t e = cudaSuccess;
-    void (*ks[3])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) = {k_tcs<1>, k_tcs<2>, k_tcs<3>};
+    void (*ks[6])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) = {
+        k_tcs<1, false>, k_tcs<2, false>, k_tcs<3, false>, k_tcs<1, true>, k_tcs<2, true>, k_tcs<3, true>};
     for (auto k : ks) {
       // Two CTAs per SM: all of their shared memory, at most 113 KB each.
       if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM);
@@ -843,9 +882,9 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     }
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+    setup_err = e;
+  });
+  if (setup_err != cudaSuccess) return setup_err;
   TcsArgs a{};
   a.R = plan.R;
   a.C = (int)plan.C;
@@ -861,11 +900,15 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   a.out0 = pr[0].out;
   a.out1 = plan.np > 1 ? pr[1].out : nullptr;
   a.ldo = ldo;
-  a.status = status;
-  a.spin = spin;
+  a.status = wt.status;
+  a.spin = wt.spin;
+  a.stall = wt.stall;
+  a.L = plan.G << plan.E;
+  a.dump = dump;
   const int smem = smem_for(plan.E, plan.nstage);
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) =
-      plan.G == 1 ? k_tcs<1> : plan.G == 2 ? k_tcs<2> : k_tcs<3>;
+      dump ? (plan.G == 1 ? k_tcs<1, true> : plan.G == 2 ? k_tcs<2, true> : k_tcs<3, true>)
+           : (plan.G == 1 ? k_tcs<1, false> : plan.G == 2 ? k_tcs<2, false> : k_tcs<3, false>);
   cudaError_t e = launch_dependent(kern, dim3(plan.P), kThreads, smem, st, m[0], m[1], m[2], m[3], a);
   if (e != cudaSuccess || plan.direct) return e;
   TcsTopArgs t{};
@@ -882,6 +925,7 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   t.ldo = ldo;
   t.h = h;
   t.silu = silu;
+  t.status = wt.status;
   const dim3 grid(h ? plan.T : plan.np * plan.T, (plan.R + kTopTok - 1) / kTopTok);
   const int smem_top = top_smem(h != nullptr, plan.E, plan.cap);
   return h ? launch_dependent(k_tcs_top<true>, grid, kTopThreads, smem_top, st, t)
@@ -891,17 +935,17 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
 }  // namespace
 
 cudaError_t launch_tcs(const TcsPlan& plan, const TcsProblem* pr, long long ldo, void* scratch,
-                       size_t scratch_bytes, int* status, long long spin, cudaStream_t st) {
+                       size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump) {
   for (int p = 0; p < plan.np; ++p)
     if (!pr[p].out) return cudaErrorInvalidValue;
-  return tcs_launch(plan, pr, ldo, nullptr, nullptr, scratch, scratch_bytes, status, spin, st);
+  return tcs_launch(plan, pr, ldo, nullptr, nullptr, scratch, scratch_bytes, wt, st, dump);
 }
 
 cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* pr, uint16_t* h, long long ldo,
-                              const uint16_t* silu, void* scratch, size_t scratch_bytes, int* status,
-                              long long spin, cudaStream_t st) {
+                              const uint16_t* silu, void* scratch, size_t scratch_bytes, const Waits& wt,
+                              cudaStream_t st) {
   if (plan.np != 2 || !h || !silu) return cudaErrorInvalidValue;
-  return tcs_launch(plan, pr, ldo, h, silu, scratch, scratch_bytes, status, spin, st);
+  return tcs_launch(plan, pr, ldo, h, silu, scratch, scratch_bytes, wt, st, nullptr);
 }
 
 }  // namespace detffn

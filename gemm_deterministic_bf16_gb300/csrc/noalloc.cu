@@ -21,20 +21,24 @@
 namespace detffn {
 namespace {
 
-// Limits of this entry point.
+// Limits of this entry point: at most 8 tokens, and contraction lengths the
+// weight-streaming decode kernel covers (decode_geometry: 4, 8, 16, 32 or 64
+// leaves of 64, or 12, 24, 48, 96 or 192), i.e. 256 <= H, I <= 12288.
 constexpr long long kNaMaxM = 8;
-constexpr long long kNaMaxH = 8192;
-constexpr long long kNaMaxI = 16384;
+constexpr long long kNaMaxH = 12288;
+constexpr long long kNaMaxI = 12288;
 constexpr long long kNaRows = 2 * kNaMaxI > kNaMaxH ? 2 * kNaMaxI : kNaMaxH;
 
 // Scratch layout (bytes): tickets | status word | block-root planes | h.
+// The tickets and the status word are cleared together at the start of
+// every call.
 constexpr size_t kNaTicketBytes = (size_t)(kNaRows + 1) * sizeof(unsigned);
 constexpr size_t kNaStatusOff = (kNaTicketBytes + 255) / 256 * 256;
 constexpr size_t kNaPartOff = kNaStatusOff + 256;
 constexpr size_t kNaPartBytes = (size_t)64 * kNaRows * sizeof(uint16_t);  // <= 8 blocks x 8 tokens
 constexpr size_t kNaHOff = kNaPartOff + kNaPartBytes;
 constexpr size_t kNaHBytes = (size_t)kNaMaxM * kNaMaxI * sizeof(uint16_t);
-constexpr size_t kNaScratchBytes = kNaHOff + kNaHBytes;  // about 4.4 MiB
+constexpr size_t kNaScratchBytes = kNaHOff + kNaHBytes;  // about 3.3 MiB
 
 static __device__ __align__(256) unsigned char g_na_scratch[kNaScratchBytes];
 static __device__ __align__(256) uint16_t g_na_silu[65536];
@@ -99,8 +103,11 @@ extern "C" detffn_status detffn_forward_decode_noalloc(const void* x, const void
   int* status = reinterpret_cast<int*>(d->scratch + kNaStatusOff);
   uint16_t* part = reinterpret_cast<uint16_t*>(d->scratch + kNaPartOff);
   uint16_t* hh = reinterpret_cast<uint16_t*>(d->scratch + kNaHOff);
-  // The tickets must start at zero; the shared array keeps the last call's bytes.
-  if (cudaMemsetAsync(tickets, 0, kNaTicketBytes, st) != cudaSuccess) return DETFFN_ERR_CUDA;
+  // The tickets and the status word must start at zero; the shared array
+  // keeps the last call's bytes.  (A wait that runs out in the gate/up launch
+  // sets the status word, and the down launch then returns at entry instead
+  // of folding unfinished block roots.)
+  if (cudaMemsetAsync(tickets, 0, kNaStatusOff + sizeof(int), st) != cudaSuccess) return DETFFN_ERR_CUDA;
 
   DecArgs a{};
   a.x = static_cast<const uint16_t*>(x); a.ldx = H;
@@ -120,4 +127,18 @@ extern "C" detffn_status detffn_forward_decode_noalloc(const void* x, const void
   b.silu = d->silu; b.status = status; b.spin_limit = 0;
   if (launch_decode_exact(b, d->sm_count, st) != cudaSuccess) return DETFFN_ERR_CUDA;
   return DETFFN_OK;
+}
+
+extern "C" detffn_status detffn_forward_decode_noalloc_status(void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DETFFN_ERR_CUDA;
+  DevState* d = nullptr;
+  const detffn_status s = na_setup(dev, &d);
+  if (s != DETFFN_OK) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DETFFN_ERR_CUDA;
+  int* status = reinterpret_cast<int*>(d->scratch + kNaStatusOff);
+  int v = 0;
+  if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DETFFN_ERR_CUDA;
+  if (v != 0 && cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return DETFFN_ERR_CUDA;
+  return v == 0 ? DETFFN_OK : (detffn_status)v;
 }

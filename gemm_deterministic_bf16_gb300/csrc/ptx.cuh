@@ -263,6 +263,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Leaf dump (a diagnostic of the tensor kernels): the FP32 leaves of output
+// element (r, c0 + i), i < N, as leaf j of a [R][C][L] array.
+template <int N>
+__device__ __forceinline__ void dump_leaves(float* d, long long r, long long c0, long long R, long long C, int L,
+                                            int j, const uint32_t (&v)[N]) {
+  if (r >= R) return;
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (c0 + i < C) d[((size_t)r * (size_t)C + (size_t)(c0 + i)) * (size_t)L + (size_t)j] = __uint_as_float(v[i]);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace detffn {
 
 // Bottom-group size G and number of upper levels E such that L = G * 2^E with
@@ -25,8 +27,8 @@ struct TcProblem {
 
 // Up to two same-shaped contractions in one launch (their tiles interleave).
 cudaError_t launch_tc_gemms(const TcProblem* problems, int np, long long R, long long C, long long K,
-                            long long ld_r, long long ld_c, int* status, long long spin_limit, int sm_count,
-                            cudaStream_t st);
+                            long long ld_r, long long ld_c, const Waits& wt, int sm_count, cudaStream_t st,
+                            float* dump = nullptr);
 
 // out[r*ld_r + c*ld_c] = T_K(A[r, :], B[c, :]) for r < R, c < C; A and B are
 // K-contiguous BF16 with row strides lda, ldb (elements, multiples of 8) and
@@ -36,8 +38,8 @@ cudaError_t launch_tc_gemms(const TcProblem* problems, int np, long long R, long
 // MN-major by the tensor core.
 cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,
                            long long R, long long C, long long K, uint16_t* out, long long ld_r,
-                           long long ld_c, int* status, long long spin_limit, int sm_count, cudaStream_t st,
-                           bool b_mn = false, bool a_mn = false);
+                           long long ld_c, const Waits& wt, int sm_count, cudaStream_t st,
+                           bool b_mn = false, bool a_mn = false, float* dump = nullptr);
 
 // A 2-D BF16 tensor map over rows x K (row stride ld elements), 128-byte
 // swizzle, boxes of 64 (K) x box_rows.
@@ -76,14 +78,14 @@ struct TcsProblem {
 // One or two same-shaped contractions (plan.np): two launches on `st`, or one
 // in direct mode (scratch unused).
 cudaError_t launch_tcs(const TcsPlan& plan, const TcsProblem* problems, long long ldo, void* scratch,
-                       size_t scratch_bytes, int* status, long long spin, cudaStream_t st);
+                       size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump = nullptr);
 
 // Gate (problems[0]) and up (problems[1]) with the SiLU * up stage boundary
 // fused into the top of the trees: h[r * ldo + c] = bf16(bf16(SiLU(gate)) * up);
 // gate and up are stored only where problems[p].out is non-null.
 cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* problems, uint16_t* h, long long ldo,
-                              const uint16_t* silu, void* scratch, size_t scratch_bytes, int* status,
-                              long long spin, cudaStream_t st);
+                              const uint16_t* silu, void* scratch, size_t scratch_bytes, const Waits& wt,
+                              cudaStream_t st);
 
 // Host check of the few-token kernels' piece decomposition and fold codes
 // over every tile of up to 2^max_levels groups; returns the failed cases.

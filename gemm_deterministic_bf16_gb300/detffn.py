@@ -37,9 +37,12 @@ class DetFFNError(RuntimeError):
         super().__init__(msg)
 
 
+FLAG_TEST_STALL = 1
+
+
 class Options(ctypes.Structure):
     _fields_ = [("leaf_width", ctypes.c_int), ("path", ctypes.c_int),
-                ("shards", ctypes.c_int), ("spin_limit", ctypes.c_longlong)]
+                ("shards", ctypes.c_int), ("flags", ctypes.c_int), ("spin_limit", ctypes.c_longlong)]
 
 
 _LOCK = threading.Lock()
@@ -115,8 +118,8 @@ def handle(device=None):
     return h
 
 
-def _opts(path=PATH_AUTO, shards=1, spin_limit=0):
-    return ctypes.byref(Options(64, path, shards, spin_limit))
+def _opts(path=PATH_AUTO, shards=1, spin_limit=0, flags=0):
+    return ctypes.byref(Options(64, path, shards, flags, spin_limit))
 
 
 def _ptr(t):
@@ -149,9 +152,11 @@ def workspace(op, M, H, I, k=1, path=PATH_AUTO, device=None):
 
 
 def detffn_forward(x, Wg, Wu, Wd, out=None, gate_save=None, up_save=None, ws=None,
-                   path=PATH_AUTO, stream=None):
+                   path=PATH_AUTO, stream=None, spin_limit=0, flags=0):
     """out = down(silu(gate) * up); x [M,H], Wg/Wu [I,H], Wd [H,I].  Pass
-    gate_save/up_save ([M,I]) to keep gate and up (training mode)."""
+    gate_save/up_save ([M,I]) to keep gate and up (training mode).
+    spin_limit and flags go to detffn_options (flags: FLAG_TEST_STALL for
+    tests of the failure path only)."""
     _bf16(x, Wg, Wu, Wd, out, gate_save, up_save)
     M, H = x.shape
     I = Wg.shape[0]
@@ -161,7 +166,8 @@ def detffn_forward(x, Wg, Wu, Wd, out=None, gate_save=None, up_save=None, ws=Non
         ws = workspace(OP_FORWARD, M, H, I, 1, path, x.device)
     _check(lib().detffn_forward(handle(x.device), _ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(out),
                                 _ptr(gate_save), _ptr(up_save), M, H, I, _ptr(ws), ws.numel(),
-                                _stream(x.device, stream), _opts(path)), "detffn_forward")
+                                _stream(x.device, stream), _opts(path, 1, spin_limit, flags)),
+           "detffn_forward")
     return out
 
 
@@ -185,7 +191,7 @@ def detffn_forward_sharded(x, Wg, Wu, Wd, k, out=None, gate_save=None, up_save=N
 
 def detffn_backward(x, Wg, Wu, Wd, gate, up, dOut, dX=None, dWg=None, dWu=None, dWd=None,
                     dh_save=None, dU_save=None, dG_save=None, ws=None, shards=1,
-                    path=PATH_AUTO, stream=None):
+                    path=PATH_AUTO, stream=None, spin_limit=0, flags=0):
     """Returns (dX, dWg, dWu, dWd)."""
     _bf16(x, Wg, Wu, Wd, gate, up, dOut, dX, dWg, dWu, dWd, dh_save, dU_save, dG_save)
     M, H = x.shape
@@ -201,7 +207,7 @@ def detffn_backward(x, Wg, Wu, Wd, gate, up, dOut, dX=None, dWg=None, dWu=None, 
                                  _ptr(gate), _ptr(up), _ptr(dOut), _ptr(dX), _ptr(dWg), _ptr(dWu),
                                  _ptr(dWd), _ptr(dh_save), _ptr(dU_save), _ptr(dG_save), M, H, I,
                                  _ptr(ws), ws.numel(), _stream(x.device, stream),
-                                 _opts(path, shards)), "detffn_backward")
+                                 _opts(path, shards, spin_limit, flags)), "detffn_backward")
     return dX, dWg, dWu, dWd
 
 
@@ -251,7 +257,7 @@ def detffn_rank_tree_reduce(inputs, out=None, stream=None):
     return out
 
 
-def detffn_tree_gemm(A, B, out=None, path=PATH_AUTO, stream=None):
+def detffn_tree_gemm(A, B, out=None, path=PATH_AUTO, stream=None, spin_limit=0, flags=0):
     """out[r, c] = T_K(A[r, :], B[c, :]) for 2-D strided bfloat16 views A [R,K], B [C,K]."""
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
         raise ValueError("bfloat16 operands expected")
@@ -261,7 +267,46 @@ def detffn_tree_gemm(A, B, out=None, path=PATH_AUTO, stream=None):
         out = torch.empty((R, C), dtype=torch.bfloat16, device=A.device)
     _check(lib().detffn_tree_gemm(handle(A.device), _ptr(A), A.stride(0), A.stride(1), _ptr(B),
                                   B.stride(0), B.stride(1), R, C, K, _ptr(out), out.stride(0),
-                                  _stream(A.device, stream), _opts(path)), "detffn_tree_gemm")
+                                  _stream(A.device, stream), _opts(path, 1, spin_limit, flags)),
+           "detffn_tree_gemm")
+    return out
+
+
+def detffn_tree_gemm_leaves(A, B, out=None, leaves=None, stream=None):
+    """The tensor family's contraction of detffn_tree_gemm, plus its FP32
+    leaves: returns (out [R,C] bfloat16, leaves [R,C,L] float32)."""
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise ValueError("bfloat16 operands expected")
+    R, K = A.shape
+    C = B.shape[0]
+    L = (K + 63) // 64
+    if out is None:
+        out = torch.empty((R, C), dtype=torch.bfloat16, device=A.device)
+    if leaves is None:
+        leaves = torch.empty((R, C, L), dtype=torch.float32, device=A.device)
+    L_ = lib()
+    L_.detffn_tree_gemm_leaves.argtypes = [_vp, _vp, _ll, _ll, _vp, _ll, _ll, _ll, _ll, _ll, _vp, _ll,
+                                           _vp, _vp, ctypes.POINTER(Options)]
+    L_.detffn_tree_gemm_leaves.restype = ctypes.c_int
+    _check(L_.detffn_tree_gemm_leaves(handle(A.device), _ptr(A), A.stride(0), A.stride(1), _ptr(B),
+                                      B.stride(0), B.stride(1), R, C, K, _ptr(out), out.stride(0),
+                                      _ptr(leaves), _stream(A.device, stream), _opts(PATH_TENSOR)),
+           "detffn_tree_gemm_leaves")
+    return out, leaves
+
+
+def detffn_cvt_f32_bf16(x, out=None, stream=None):
+    """The kernels' own FP32 -> BF16 rounding applied to a float32 CUDA tensor
+    (returns a bfloat16 tensor of the same shape)."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("contiguous CUDA float32 tensor expected")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    L = lib()
+    L.detffn_cvt_f32_bf16.argtypes = [_vp, _vp, _vp, _ll, _vp]
+    L.detffn_cvt_f32_bf16.restype = ctypes.c_int
+    _check(L.detffn_cvt_f32_bf16(handle(x.device), _ptr(x), _ptr(out), x.numel(),
+                                 _stream(x.device, stream)), "detffn_cvt_f32_bf16")
     return out
 
 
@@ -325,6 +370,17 @@ def detffn_forward_decode_noalloc(x, Wg, Wu, Wd, out=None, stream=None):
                                                M, H, I, _stream(x.device, stream)),
                "detffn_forward_decode_noalloc")
     return out
+
+
+def detffn_forward_decode_noalloc_status(device=None, stream=None):
+    """Status of the last allocation-free decode forward on the device (OK or
+    ERR_TIMEOUT); reading it clears it."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    L = lib()
+    L.detffn_forward_decode_noalloc_status.argtypes = [_vp]
+    L.detffn_forward_decode_noalloc_status.restype = ctypes.c_int
+    with torch.cuda.device(dev):
+        return L.detffn_forward_decode_noalloc_status(_stream(dev, stream))
 
 
 def detffn_selfcheck_pieces(max_levels=8):

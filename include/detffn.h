@@ -74,12 +74,23 @@ typedef enum { DETFFN_F32 = 0, DETFFN_F16 = 1, DETFFN_BF16 = 2 } detffn_dtype;
  * in-leaf order) and applies the same tree to those leaves. */
 typedef enum { DETFFN_PATH_AUTO = 0, DETFFN_PATH_EXACT = 1, DETFFN_PATH_TENSOR = 2 } detffn_path;
 
+/* Option flags.  DETFFN_FLAG_TEST_STALL is for tests of the failure path
+ * only: the call's streaming kernels issue no copies, so the first bounded
+ * wait of every CTA runs out (after spin_limit polls: give a small one), the
+ * CTAs stop with nothing in flight and the call's outputs are left
+ * unfinished; detffn_get_status then returns DETFFN_ERR_TIMEOUT.  The fault
+ * is made by withholding work, never by a bad address or a trap. */
+enum { DETFFN_FLAG_TEST_STALL = 1 };
+
 typedef struct {
     int leaf_width;        /* 64; anything else returns DETFFN_ERR_UNSUPPORTED */
     int path;              /* detffn_path */
     int shards;            /* detffn_backward only: k in {1,2,4,8} TP shards of I for dHidden */
-    long long spin_limit;  /* polls before a bounded in-kernel wait gives up; 0 = default */
-} detffn_options;          /* pass NULL for {64, AUTO, 1, 0} */
+    int flags;             /* 0, or DETFFN_FLAG_TEST_STALL (tests only); other bits: DETFFN_ERR_INVALID_ARG */
+    long long spin_limit;  /* polls before a role's bounded in-kernel wait gives up; 0 = default
+                              (2^26).  Waits that drain a CTA's own copies and tensor-core work
+                              before it exits always use the default. */
+} detffn_options;          /* pass NULL for {64, AUTO, 1, 0, 0} */
 
 typedef struct detffn_handle_s *detffn_handle;
 
@@ -194,6 +205,22 @@ DETFFN_API detffn_status detffn_tree_gemm(detffn_handle h, const void *A, long l
                                void *out, long long o_rs, void *stream,
                                const detffn_options *opts);
 
+/* Leaf dump (a diagnostic of the TENSOR family: it lets a test apply the
+ * canonical tree to the tensor cores' own leaves; RL-Kernel PR #325,
+ * "Design"): the same contraction as
+ * detffn_tree_gemm on the tensor family (same kernels, same plan, same
+ * bits in `out`), which also writes every FP32 leaf to `leaves`, a device
+ * array of R * C * L floats laid out [R][C][L], L = ceil(K / 64).  Applying
+ * the canonical tree to these leaves gives `out` exactly; each leaf is the
+ * tensor core's sum of its 64 (or fewer) products.  K >= 1; EXACT returns
+ * DETFFN_ERR_UNSUPPORTED (its leaves follow the documented LANE8x8 order),
+ * shapes the tensor family does not cover return DETFFN_ERR_UNSUPPORTED.
+ * The dump is slow (scattered 4-byte stores) and meant for tests. */
+DETFFN_API detffn_status detffn_tree_gemm_leaves(detffn_handle h, const void *A, long long a_rs,
+                                      long long a_ks, const void *B, long long b_rs, long long b_ks,
+                                      long long R, long long C, long long K, void *out, long long o_rs,
+                                      void *leaves, void *stream, const detffn_options *opts);
+
 /* Copies the handle's SiLU tables to host memory: silu_bf16[65536] (BF16 bit
  * patterns) and dsilu_f32[65536], indexed by the gate's bit pattern.  Either
  * pointer may be NULL. */
@@ -222,25 +249,43 @@ DETFFN_API detffn_status detffn_profile_read(detffn_handle h, int max, detffn_ke
  * process whose device memory is already owned by a caching allocator's
  * pool, or a runtime that only hands out buffers reserved in advance).
  * It computes exactly what detffn_forward computes on the EXACT path -- the
- * same bits -- for 1 <= M <= 8 tokens, H <= 8192, I <= 16384, where H and I
- * are 64 times 2^d or 3 * 2^d leaves (e.g. 4096 and 12288).  Inputs x [M,H]
- * and the weights must be 16-byte aligned; out [M,H] is written.  Larger or
- * unsupported sizes return DETFFN_ERR_SHAPE, misaligned pointers
- * DETFFN_ERR_ALIGN, and nothing is launched.
- * Its scratch (h, the kernels' block-root planes and tickets, about 4.4 MiB)
- * and its SiLU table are fixed-size arrays inside the library, held by every
- * GPU that loads it until the process exits.  The first call on a device
- * performs a one-time set-up there (it resolves those arrays' device
- * addresses and copies the SiLU table with a synchronous cudaMemcpy); make
- * that first call before any stream capture.  Every call uses the same
- * arrays and clears what must start at zero, so calls that overlap on the
- * GPU (on different streams, or from different host threads) race and must
- * not be issued; calls in order on one stream are fine.  It uses the current
- * device and runs on `stream` (a cudaStream_t). */
+ * same bits -- for 1 <= M <= 8 tokens and H, I in {256, 512, 1024, 2048,
+ * 4096} or {768, 1536, 3072, 6144, 12288} (4 to 64 leaves of 64, a power of
+ * two, or 12 to 192, three times one).  Inputs x [M,H] and the weights must
+ * be 16-byte aligned; out [M,H] is written.  Other sizes return
+ * DETFFN_ERR_SHAPE, misaligned pointers DETFFN_ERR_ALIGN, and nothing is
+ * launched.
+ * Its scratch (h, the kernels' block-root planes and tickets, and a status
+ * word; about 3.3 MiB) and its SiLU table are fixed-size arrays inside the
+ * library, held by every GPU that loads it until the process exits.  The
+ * first call on a device performs a one-time set-up there (it resolves those
+ * arrays' device addresses and copies the SiLU table with a synchronous
+ * cudaMemcpy); make that first call before any stream capture.  Every call
+ * uses the same arrays and first clears what must start at zero (the tickets
+ * and the status word), so calls that overlap on the GPU (on different
+ * streams, or from different host threads) race and must not be issued;
+ * calls in order on one stream are fine.  It uses the current device and runs
+ * on `stream` (a cudaStream_t).  A bounded in-kernel wait that runs out is
+ * reported by detffn_forward_decode_noalloc_status, not by this call. */
 DETFFN_API detffn_status detffn_forward_decode_noalloc(const void *x, const void *Wg,
                                                        const void *Wu, const void *Wd, void *out,
                                                        long long M, long long H, long long I,
                                                        void *stream);
+
+/* Status of the allocation-free decode forward on the current device:
+ * synchronises `stream`, then returns and clears the status word of the
+ * last detffn_forward_decode_noalloc call (DETFFN_OK, or DETFFN_ERR_TIMEOUT
+ * when a bounded wait ran out: its out is then unfinished).  Allocates
+ * nothing; may perform the same one-time set-up as the first call. */
+DETFFN_API detffn_status detffn_forward_decode_noalloc_status(void *stream);
+
+/* Diagnostic: out[i] = the BF16 rounding (to nearest, ties to even) of the
+ * FP32 value in[i], computed on the device with the very conversion every
+ * kernel of the library uses for leaves, nodes and stage boundaries; a test
+ * compares it with an independent rounding rule over all 2^32 patterns.
+ * in: n floats, out: n BF16 (device, 4- and 2-byte aligned, not overlapping). */
+DETFFN_API detffn_status detffn_cvt_f32_bf16(detffn_handle h, const void *in, void *out, long long n,
+                                             void *stream);
 
 /* Diagnostic: counts the BF16 pairs (a, b), over all 2^32 of them, for which
  * the device's packed add.rn.bf16x2 differs from the tree node
@@ -264,7 +309,10 @@ DETFFN_API detffn_status detffn_selfcheck_node_add(detffn_handle h, unsigned lon
 DETFFN_API detffn_status detffn_selfcheck_pieces(int max_levels, unsigned long long *failures);
 
 /* Synchronises `stream`, then returns and clears the handle's device status
- * word (DETFFN_OK or DETFFN_ERR_TIMEOUT from a bounded wait). */
+ * word (DETFFN_OK or DETFFN_ERR_TIMEOUT from a bounded wait).  The word is
+ * sticky: once a wait has run out, every later streaming kernel launched
+ * through the handle returns at entry (leaving its outputs unwritten) until
+ * this call clears it, so no kernel builds on another's unfinished output. */
 DETFFN_API detffn_status detffn_get_status(detffn_handle h, void *stream);
 
 /* The CUDA error behind the calling thread's last DETFFN_ERR_CUDA (a static

@@ -84,6 +84,22 @@ def test_argument_errors_launch_nothing(L):
     bad = ctypes.byref(Options(32, 0, 1, 0))
     n = ctypes.c_size_t()
     assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, bad, ctypes.byref(n)) == 4
+    # Unknown option flag bits and a negative poll limit are argument errors.
+    assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 2, 0)),
+                                   ctypes.byref(n)) == 1
+    assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 0, -5)),
+                                   ctypes.byref(n)) == 1
+    assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 1, 100)),
+                                   ctypes.byref(n)) == 0
+    # Leaf dump and conversion diagnostics: argument errors before any launch.
+    L.detffn_tree_gemm_leaves.argtypes = [ctypes.c_void_p] * 1 + [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_longlong,
+                                          ctypes.c_void_p, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong,
+                                          ctypes.c_longlong, ctypes.c_longlong, ctypes.c_void_p, ctypes.c_longlong,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert L.detffn_tree_gemm_leaves(None, 16, 64, 1, 16, 64, 1, 1, 1, 64, 16, 1, 16, None, None) == 1
+    L.detffn_cvt_f32_bf16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong,
+                                      ctypes.c_void_p]
+    assert L.detffn_cvt_f32_bf16(None, 16, 32, 4, None) == 1
 
 
 def test_header_names_readings():

@@ -6,8 +6,10 @@ it keeps its scratch in fixed arrays inside the library instead of a
 caller-provided workspace.  This file is collected last, so that a run that
 stops at the first failure has already run every other test.  It checks, on
 two calls in a row, that the output equals detffn_forward's on the exact path
-bit for bit (the tolerance of the exact path is 0 mismatching elements), and
-that sizes beyond its limits are refused before anything is launched.
+bit for bit (the tolerance of the exact path is 0 mismatching elements) and
+that the call's status word reports no timeout; that the output equals the
+CPU oracle's; and that sizes beyond its limits are refused before anything
+is launched.
 """
 import numpy as np
 import pytest
@@ -38,6 +40,21 @@ def test_noalloc_matches_forward_twice(G, M, H, I):
         G.detffn_forward_decode_noalloc(t["x"], t["Wg"], t["Wu"], t["Wd"], out=out)
         torch.cuda.synchronize()
         assert mismatches(host(out), ref) == 0
+        # No bounded wait ran out (the call's own status word, read and cleared).
+        assert G.detffn_forward_decode_noalloc_status() == 0
+
+
+def test_noalloc_matches_oracle(G, oracle_mod):
+    """Against the CPU oracle directly: the allocation-free call gives the
+    oracle's bits (its leaves follow the oracle's stated in-leaf order)."""
+    M, H, I = 4, 1024, 3072
+    d = ffn_inputs(M, H, I, seed=77, with_dout=False)
+    t = {n: dev(v) for n, v in d.items()}
+    out = G.detffn_forward_decode_noalloc(t["x"], t["Wg"], t["Wu"], t["Wd"])
+    torch.cuda.synchronize()
+    ref = oracle_mod.ffn_forward(d["x"], d["Wg"], d["Wu"], d["Wd"])
+    assert mismatches(host(out), ref["out"]) == 0
+    assert G.detffn_forward_decode_noalloc_status() == 0
 
 
 def test_noalloc_rejects_sizes_beyond_limits(G):
@@ -47,8 +64,13 @@ def test_noalloc_rejects_sizes_beyond_limits(G):
     with pytest.raises(G.DetFFNError) as e:
         G.detffn_forward_decode_noalloc(x, w, w, wd)   # M = 9 > 8
     assert e.value.status == 2
-    big = torch.zeros(32768, 64, dtype=torch.bfloat16, device="cuda")
+    big = torch.zeros(32768, 256, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(G.DetFFNError) as e:
-        G.detffn_forward_decode_noalloc(x[:1, :64], big, big,
-                                        torch.zeros(64, 32768, dtype=torch.bfloat16, device="cuda"))
-    assert e.value.status == 2                           # I = 32768 > 16384
+        G.detffn_forward_decode_noalloc(x[:1], big, big,
+                                        torch.zeros(256, 32768, dtype=torch.bfloat16, device="cuda"))
+    assert e.value.status == 2                           # I = 32768 > 12288
+    xh = torch.zeros(1, 8192, dtype=torch.bfloat16, device="cuda")
+    wh = torch.zeros(768, 8192, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(G.DetFFNError) as e:
+        G.detffn_forward_decode_noalloc(xh, wh, wh, torch.zeros(8192, 768, dtype=torch.bfloat16, device="cuda"))
+    assert e.value.status == 2                           # H = 8192: 128 leaves, not covered

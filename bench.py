@@ -9,8 +9,8 @@ the M=1 and M=8 forward latencies and the M=32 forward+backward latency.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
---impl reference times the CPU oracle (the only reference this build has) on
-a bounded sample of the same workload.  Under torchrun (N>1) each rank runs
+--impl reference times the CPU oracle (the only reference this build has:
+the pages hold no code) on the same workload, the whole forward per step.  Under torchrun (N>1) each rank runs
 an independent replica (the FFN itself runs on one GPU); rank 0 prints one
 JSON line.
 """
@@ -164,17 +164,21 @@ def max_over_ranks(ws, v):
 _ORACLE_INPUTS = {}
 
 
-def oracle_forward_rows(rows, seed=0):
-    """Times the CPU oracle on `rows` token rows of the M=32 decode forward
-    (rows are independent, so the M=32 latency scales by 32/rows)."""
-    import oracle
+def _oracle_inputs(seed=0):
     from gemm_deterministic_bf16_gb300.inputs import ffn_inputs
     if seed not in _ORACLE_INPUTS:
         _ORACLE_INPUTS[seed] = ffn_inputs(M_DEC, H, I, seed=seed, with_dout=False)
-    d = _ORACLE_INPUTS[seed]
+    return _ORACLE_INPUTS[seed]
+
+
+def oracle_forward_rows(rows, seed=0, nthreads=0):
+    """Times the CPU oracle's forward on the first `rows` token rows of the
+    M=32 decode workload (rows are independent); returns (seconds, out)."""
+    import oracle
+    d = _oracle_inputs(seed)
     t0 = time.perf_counter()
-    oracle.ffn_forward(d["x"][:rows], d["Wg"], d["Wu"], d["Wd"])
-    return time.perf_counter() - t0
+    r = oracle.ffn_forward(d["x"][:rows], d["Wg"], d["Wu"], d["Wd"], nthreads=nthreads)
+    return time.perf_counter() - t0, r["out"]
 
 
 def host_cores():
@@ -184,35 +188,68 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part", "processor\t: 0")) and ":" in ln:
+                    v = ln.split(":", 1)[1].strip()
+                    if v:
+                        return v
+    except OSError:
+        pass
+    return "unknown"
+
+
 def run_reference(args):
+    """The reference arm: the CPU oracle (the only reference the pages allow:
+    they hold no code) running the whole M=32, H=4096, I=12288 forward each
+    step on all host cores."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     import oracle
     oracle.lib()
-    rows = args.ref_rows
     for _ in range(args.warmup):
-        oracle_forward_rows(rows)
-    times = [oracle_forward_rows(rows) for _ in range(args.steps)]
-    us = statistics.median(times) * 1e6 * M_DEC / rows
-    sample = ("oracle (plain C, LANE8x8 leaves, all host threads) on %d of the 32 token rows of "
-              "the M=32, H=4096, I=12288 forward per step, scaled by 32/%d" % (rows, rows))
+        oracle_forward_rows(M_DEC)
+    times = [oracle_forward_rows(M_DEC)[0] for _ in range(args.steps)]
+    us = statistics.median(times) * 1e6
+    sample = ("oracle (plain C, LANE8x8 leaves, all %d host threads): the whole M=32, H=4096, "
+              "I=12288 forward each step (no extrapolation); CPU %s" % (host_cores(), cpu_model()))
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) x, N(0,0.02) weights)",
             "config": {"workload": "decode forward M=32 H=4096 I=12288", "M": M_DEC, "H": H, "I": I},
             "cpu_baseline": {"value": us, "unit": "us", "cores": host_cores(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
 
+def bits_mismatch(a, b):
+    """Elements whose bit patterns differ (two CUDA tensors of one shape)."""
+    import torch
+    ia = a.view(torch.int16) if a.element_size() == 2 else a.view(torch.int32)
+    ib = b.view(torch.int16) if b.element_size() == 2 else b.view(torch.int32)
+    return int((ia != ib).sum().item())
+
+
 def large_training(G, args, ws_n, timed):
     """M=4096 (2 x 2048 tokens) forward and forward+backward on the default
-    (tensor-core) family: TFLOP/s against 6*M*H*I and 18*M*H*I."""
+    (tensor-core) family: TFLOP/s against 6*M*H*I and 18*M*H*I; the weight
+    gradients from c = 2 and 4 token chunks, timed and compared bit for bit
+    with the one-shot backward's."""
     import numpy as np
     import torch
     from gemm_deterministic_bf16_gb300.inputs import ffn_inputs
@@ -236,53 +273,93 @@ def large_training(G, args, ws_n, timed):
     steps = max(3, args.steps // 4)
     fwd_ms = max_over_ranks(ws_n, timed(fwd, steps, 3))
     trn_ms = max_over_ranks(ws_n, timed(train, steps, 3))
-    # Weight gradients with the tokens given as c chunks in logical order (the
-    # same bits as the one-shot backward's).
-    chunked = {}
+    ref = [dWg.clone(), dWu.clone(), dWd.clone()]
+    res = {}
     for c in (2, 4):
         sl = [slice(j * M // c, (j + 1) * M // c) for j in range(c)]
-        xs, gs, us, ds = ([v[q].contiguous() for q in sl] for v in (t["x"], g, u, t["dOut"]))
+        xs, gs, us, ds = ([v[q] for q in sl] for v in (t["x"], g, u, t["dOut"]))
         wsc = G.workspace(G.OP_WGRAD_CHUNKED, M, H, I)
-        chunked["wgrad_chunked_ms_M4096_c%d" % c] = max_over_ranks(ws_n, timed(
-            lambda i: G.detffn_wgrad_chunked(xs, gs, us, ds, t["Wd"], dWg=dWg, dWu=dWu, dWd=dWd, ws=wsc),
+        cw = [e(I, H), e(I, H), e(H, I)]
+        res["wgrad_chunked_ms_M4096_c%d" % c] = max_over_ranks(ws_n, timed(
+            lambda i: G.detffn_wgrad_chunked(xs, gs, us, ds, t["Wd"], dWg=cw[0], dWu=cw[1], dWd=cw[2], ws=wsc),
             steps, 3))
-        del xs, gs, us, ds, wsc
+        res["chunk_mismatches_M4096_c%d" % c] = sum(bits_mismatch(a, b) for a, b in zip(cw, ref))
+        del xs, gs, us, ds, wsc, cw
     G.detffn_profiling(True)
     train(0)
     prof = G.detffn_profile_read()
     G.detffn_profiling(False)
-    res = dict(chunked)
     res.update({"fwd_ms_M4096": fwd_ms, "fwd_tflops_M4096": 6 * M * H * I / (fwd_ms * 1e-3) / 1e12,
-           "fwd_bwd_ms_M4096": trn_ms, "fwd_bwd_tflops_M4096": 18 * M * H * I / (trn_ms * 1e-3) / 1e12,
-           "kernels_M4096": {k: {"launches": v["launches"], "ms": v["ms"],
-                                 "tflops": (v["flops"] / (v["ms"] * 1e-3) / 1e12) if v["flops"] else None,
-                                 "gbs": v["bytes"] / (v["ms"] * 1e-3) / 1e9}
-                             for k, v in prof.items()}})
-    del t, out, g, u, dX, dWg, dWu, dWd, wsf, wsb
+                "fwd_bwd_ms_M4096": trn_ms,
+                "fwd_bwd_tflops_M4096": 18 * M * H * I / (trn_ms * 1e-3) / 1e12,
+                "kernels_M4096": {k: {"launches": v["launches"], "ms": v["ms"],
+                                      "tflops": (v["flops"] / (v["ms"] * 1e-3) / 1e12) if v["flops"] else None,
+                                      "gbs": v["bytes"] / (v["ms"] * 1e-3) / 1e9}
+                                  for k, v in prof.items()}})
+    del t, out, g, u, dX, dWg, dWu, dWd, wsf, wsb, ref
     torch.cuda.empty_cache()
     return res
 
 
-def rank_tree_rows(G, args, ws_n, timed):
-    """The balanced rank tree over n buffers of S bytes: microseconds per call,
-    and for 16 MiB buffers (larger than L2 in total) GB/s of (n+1)*S bytes."""
+L2_BYTES = 129 << 20
+
+
+def rank_tree_rows(G, args):
+    """The balanced rank tree over n in {2, 4, 8} buffers of 4 KiB, 64 KiB,
+    1 MiB and 16 MiB in FP32, FP16 and BF16, plus 16 MiB offset views
+    (+1, +2, +3 elements) with odd tails.  Each row replays a CUDA graph of
+    `reps` calls, cycling over enough buffer sets that a 16 MiB row's sets
+    exceed twice the L2 (so they stream from HBM); the time per call is the
+    kernel's plus the graph's launch gap, free of the host's per-call cost.
+    16 MiB rows report GB/s of (n+1)*S bytes and the fraction of HBM peak."""
     import torch
     pk, _ = peaks()
     rows = {}
-    steps = max(5, args.steps)
-    for dt, name in ((torch.float32, "f32"), (torch.bfloat16, "bf16")):
-        esz = torch.tensor([], dtype=dt).element_size()
-        for S in (4 << 10, 1 << 20, 16 << 20):
-            for n in (2, 4, 8):
-                bufs = [torch.randn(S // esz, device="cuda").to(dt) for _ in range(n)]
-                out = torch.empty_like(bufs[0])
-                us = 1e3 * max_over_ranks(ws_n, timed(lambda i: G.detffn_rank_tree_reduce(bufs, out=out), steps, 3))
-                row = {"us": us}
-                if S >= 16 << 20:
-                    gbs = (n + 1) * S / (us * 1e-6) / 1e9
-                    row.update({"gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"]})
-                rows["%s_n%d_%dKiB" % (name, n, S >> 10)] = row
-                del bufs, out
+    reps = 24
+    cases = [(dt, S, n, 0, 0) for dt in ("f32", "f16", "bf16") for S in (4 << 10, 64 << 10, 1 << 20, 16 << 20)
+             for n in (2, 4, 8)]
+    cases += [(dt, 16 << 20, 8, off, 1) for dt in ("f16", "bf16") for off in (1, 2, 3)]
+    cases += [("f32", 16 << 20, 8, 1, 1)]
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+    for dt, S, n, off, tail in cases:
+        esz = 4 if dt == "f32" else 2
+        count = S // esz - tail
+        nsets = 2
+        if S >= 16 << 20:
+            nsets = max(2, -(-2 * L2_BYTES // ((n + 1) * S)))
+        sets = []
+        for _ in range(nsets):
+            ins = [torch.randn(count + off, device="cuda").to(tdt[dt])[off:] for _ in range(n)]
+            out = torch.empty(count + off, dtype=tdt[dt], device="cuda")[off:]
+            sets.append((ins, out))
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for ins, out in sets:
+                G.detffn_rank_tree_reduce(ins, out=out)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(reps):
+                G.detffn_rank_tree_reduce(sets[i % nsets][0], out=sets[i % nsets][1])
+        graph.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nrep = 4
+        a.record()
+        for _ in range(nrep):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = 1e3 * a.elapsed_time(b) / (nrep * reps)
+        row = {"us": us}
+        if S >= 16 << 20:
+            gbs = (n + 1) * count * esz / (us * 1e-6) / 1e9
+            row.update({"gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "buffer_sets": nsets})
+        name = "%s_n%d_%dKiB" % (dt, n, S >> 10) + ("_off%d_tail" % off if off or tail else "")
+        rows[name] = row
+        del sets, graph
+    torch.cuda.empty_cache()
     return rows
 
 
@@ -313,9 +390,9 @@ def run_ours(args):
         copies.append({k: dev(v) for k, v in d.items()})
     stream = torch.cuda.current_stream()
 
-    def fwd(M, c, out, ws):
+    def fwd(M, c, out, ws, pth=None):
         t = copies[c]
-        G.detffn_forward(t["x"][:M], t["Wg"], t["Wu"], t["Wd"], out=out, ws=ws, path=path)
+        G.detffn_forward(t["x"][:M], t["Wg"], t["Wu"], t["Wd"], out=out, ws=ws, path=path if pth is None else pth)
 
     def timed(fn, steps, warmup):
         for i in range(warmup):
@@ -339,7 +416,9 @@ def run_ours(args):
     ms = max_over_ranks(ws_n, ms)
     us = ms * 1e3
 
-    # Per-kernel durations from events on the launching stream (same loop, profiling on).
+    # Per-op durations from events on the launching stream (the same loop
+    # with per-op event pairs: each op is then timed alone, without the
+    # programmatic-dependent overlap of the chained launches).
     G.detffn_profiling(True)
     for i in range(args.steps):
         fwd(M_DEC, i & 1, outs[M_DEC], wss[M_DEC])
@@ -349,73 +428,69 @@ def run_ours(args):
     top = max(prof.items(), key=lambda kv: kv[1]["ms"])
     pk, how = peaks()
     kname, kv = top
-    per_launch_ms = kv["ms"] / kv["launches"]
-    bytes_per_launch = kv["bytes"] / kv["launches"]
-    achieved = bytes_per_launch / (per_launch_ms * 1e-3) / 1e9
+    op_ms = kv["ms"] / args.steps
+    op_bytes = kv["bytes"] / args.steps
+    achieved = op_bytes / (op_ms * 1e-3) / 1e9
+    step_gbs = fwd_bytes(M_DEC) / (us * 1e-6) / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                 "traffic": traffic_for(kname, "decode_m32"), "peak_source": how,
+                "op_us_alone": op_ms * 1e3, "algorithmic_bytes_per_op": op_bytes,
                 "share": kv["ms"] / sum(v["ms"] for v in prof.values()),
-                "algorithmic_bytes_per_launch": bytes_per_launch}
+                "step_achieved": step_gbs, "step_frac": step_gbs / pk["hbm_gbs"]}
 
-    # Other decode sizes and the M=32 training step (forward with saves + backward).
     extra = {}
+    # Other decode sizes, and each family at every decode size.
     for M in (1, 8):
         extra["fwd_us_M%d" % M] = 1e3 * max_over_ranks(
             ws_n, timed(lambda i, M=M: fwd(M, i & 1, outs[M], wss[M]), args.steps, args.warmup))
         extra["fwd_gbs_M%d" % M] = fwd_bytes(M) / (extra["fwd_us_M%d" % M] * 1e-6) / 1e9
-    gsave = torch.empty(M_DEC, I, dtype=torch.bfloat16, device="cuda")
-    usave = torch.empty_like(gsave)
-    grads = [torch.empty(I, H, dtype=torch.bfloat16, device="cuda") for _ in range(2)] + \
-        [torch.empty(H, I, dtype=torch.bfloat16, device="cuda")]
-    dX = torch.empty(M_DEC, H, dtype=torch.bfloat16, device="cuda")
-    wsb = G.workspace(G.OP_BACKWARD, M_DEC, H, I, 1, path)
-    wsf = G.workspace(G.OP_FORWARD, M_DEC, H, I, 1, path)
-
-    def train_step(i):
-        t = copies[i & 1]
-        G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], out=outs[M_DEC], gate_save=gsave,
-                         up_save=usave, ws=wsf, path=path)
-        G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], gsave, usave, t["dOut"], dX=dX,
-                          dWg=grads[0], dWu=grads[1], dWd=grads[2], ws=wsb, path=path)
-
-    tsteps = max(3, args.steps // 4)
-    extra["fwd_bwd_us_M32"] = 1e3 * max_over_ranks(ws_n, timed(train_step, tsteps, 3))
-    extra["fwd_bwd_gbs_M32"] = 3 * WEIGHT_BYTES / (extra["fwd_bwd_us_M32"] * 1e-6) / 1e9
-
-    # The M=32 forward on the tensor-core family (leaves in the hardware's order).
-    wst = G.workspace(G.OP_FORWARD, M_DEC, H, I, 1, G.PATH_TENSOR)
-
-    def fwd_tc(i):
-        t = copies[i & 1]
-        G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], out=outs[M_DEC], ws=wst, path=G.PATH_TENSOR)
-
-    extra["fwd_us_M32_tensor"] = 1e3 * max_over_ranks(ws_n, timed(fwd_tc, args.steps, args.warmup))
-    extra["fwd_gbs_M32_tensor"] = fwd_bytes(M_DEC) / (extra["fwd_us_M32_tensor"] * 1e-6) / 1e9
-    # Each family at the other decode sizes (AUTO takes one of them by M).
-    for M in (1, 8):
+    for M in (1, 8, 32):
         for name, pth in (("tensor", G.PATH_TENSOR), ("exact", G.PATH_EXACT)):
             wsm = G.workspace(G.OP_FORWARD, M, H, I, 1, pth)
-            us_m = 1e3 * max_over_ranks(ws_n, timed(
-                lambda i, M=M, pth=pth, wsm=wsm: G.detffn_forward(copies[i & 1]["x"][:M], copies[i & 1]["Wg"],
-                                                                  copies[i & 1]["Wu"], copies[i & 1]["Wd"],
-                                                                  out=outs[M], ws=wsm, path=pth),
-                args.steps, args.warmup))
-            extra["fwd_us_M%d_%s" % (M, name)] = us_m
-    # The M=32 training step with the I axis in k=8 shards (tensor-parallel
-    # emulation: shard partials combined by the rank tree; the same bits).
-    wsf8 = G.workspace(G.OP_FORWARD_SHARDED, M_DEC, H, I, 8, path)
-    wsb8 = G.workspace(G.OP_BACKWARD, M_DEC, H, I, 8, path)
+            extra["fwd_us_M%d_%s" % (M, name)] = 1e3 * max_over_ranks(ws_n, timed(
+                lambda i, M=M, pth=pth, wsm=wsm: fwd(M, i & 1, outs[M], wsm, pth), args.steps, args.warmup))
+            del wsm
 
-    def train_step_k8(i):
-        t = copies[i & 1]
-        G.detffn_forward_sharded(t["x"], t["Wg"], t["Wu"], t["Wd"], 8, out=outs[M_DEC], gate_save=gsave,
-                                 up_save=usave, ws=wsf8, path=path)
-        G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], gsave, usave, t["dOut"], dX=dX,
-                          dWg=grads[0], dWu=grads[1], dWd=grads[2], ws=wsb8, shards=8, path=path)
+    # The M=32 training step (forward with saves + backward), unsharded and
+    # with the I axis in k = 2, 4, 8 shards (tensor-parallel emulation: shard
+    # partials combined by the rank tree); the shards' outputs are compared
+    # bit for bit with the unsharded call's.
+    e = lambda *s: torch.empty(s, dtype=torch.bfloat16, device="cuda")  # noqa: E731
+    tsteps = max(3, args.steps // 4)
+    base = None
+    for k in (1, 2, 4, 8):
+        gs, us_, outk, dXk = e(M_DEC, I), e(M_DEC, I), e(M_DEC, H), e(M_DEC, H)
+        grads = [e(I, H), e(I, H), e(H, I)]
+        wsf = G.workspace(G.OP_FORWARD_SHARDED if k > 1 else G.OP_FORWARD, M_DEC, H, I, k, path)
+        wsb = G.workspace(G.OP_BACKWARD, M_DEC, H, I, k, path)
 
-    extra["fwd_bwd_us_M32_k8"] = 1e3 * max_over_ranks(ws_n, timed(train_step_k8, tsteps, 3))
-    extra["rank_tree"] = rank_tree_rows(G, args, ws_n, timed)
+        def train_step(i, k=k, gs=gs, us_=us_, outk=outk, dXk=dXk, grads=grads, wsf=wsf, wsb=wsb):
+            t = copies[i & 1]
+            if k == 1:
+                G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], out=outk, gate_save=gs, up_save=us_, ws=wsf,
+                                 path=path)
+            else:
+                G.detffn_forward_sharded(t["x"], t["Wg"], t["Wu"], t["Wd"], k, out=outk, gate_save=gs,
+                                         up_save=us_, ws=wsf, path=path)
+            G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], gs, us_, t["dOut"], dX=dXk, dWg=grads[0],
+                              dWu=grads[1], dWd=grads[2], ws=wsb, shards=k, path=path)
+
+        key = "fwd_bwd_us_M32" + ("" if k == 1 else "_k%d" % k)
+        extra[key] = 1e3 * max_over_ranks(ws_n, timed(train_step, tsteps, 3))
+        train_step(0)   # copy 0 last, for the comparison
+        torch.cuda.synchronize()
+        res = [outk, dXk] + grads
+        if base is None:
+            base = [r.clone() for r in res]
+            extra["fwd_bwd_gbs_M32"] = 3 * WEIGHT_BYTES / (extra[key] * 1e-6) / 1e9
+        else:
+            extra["shard_mismatches_M32_k%d" % k] = {n: bits_mismatch(a, b) for n, a, b in
+                                                     zip(["out", "dX", "dWg", "dWu", "dWd"], res, base)}
+        del gs, us_, outk, dXk, grads, wsf, wsb, res
+    del base
+    torch.cuda.empty_cache()
+    extra["rank_tree"] = rank_tree_rows(G, args)
     if not args.no_large:
         extra.update(large_training(G, args, ws_n, timed))
 
@@ -435,11 +510,23 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        t = oracle_forward_rows(args.ref_rows)
-        cpu = {"value": t * 1e6 * M_DEC / args.ref_rows, "unit": "us", "cores": host_cores(),
-               "kind": "oracle",
-               "sample": "one oracle forward on %d of the 32 token rows, scaled by 32/%d"
-                         % (args.ref_rows, args.ref_rows)}
+        # The oracle on the same workload: the whole M=32 forward on all host
+        # cores, and one token row on one core (scaled by 32, labelled so).
+        # Its output rows are compared with this run's (the default family).
+        t_all, ref_out = oracle_forward_rows(M_DEC, seed=0)
+        t_one, _ = oracle_forward_rows(1, seed=0, nthreads=1)
+        fwd(M_DEC, 0, outs[M_DEC], wss[M_DEC])
+        got = outs[M_DEC].cpu().view(torch.int16).numpy().view(np.uint16)
+        key = lambda u: np.where(u & 0x8000, -(u.astype(np.int32) & 0x7FFF), u.astype(np.int32))  # noqa: E731
+        dist = np.abs(key(got) - key(ref_out))
+        cpu = {"value": t_all * 1e6, "unit": "us", "cores": host_cores(), "kind": "oracle",
+               "sample": "the whole M=32, H=4096, I=12288 forward, once, on all host cores",
+               "cpu_model": cpu_model(),
+               "single_thread_us_extrapolated": t_one * 1e6 * M_DEC,
+               "single_thread_sample": "one token row on one core, scaled by 32",
+               "gpu_vs_oracle": {"family": args.path, "elements": int(dist.size),
+                                 "mismatches": int(np.count_nonzero(dist)),
+                                 "over_1ulp": int(np.count_nonzero(dist > 1)), "max_ulp": int(dist.max())}}
 
     if rank == 0:
         line = {"metric": METRIC, "value": us, "unit": "us", "n_gpus": ws_n, "steps": args.steps,
@@ -450,7 +537,7 @@ def run_ours(args):
                            "I": I, "path": args.path,
                            "l2": "weights 302 MB > 129 MB L2, two copies alternated per step",
                            "replicas": ws_n},
-                "hbm_gbs": fwd_bytes(M_DEC) / (us * 1e-6) / 1e9,
+                "hbm_gbs": step_gbs,
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": M_DEC * H * 2,
                         "d2h_bytes_per_step": M_DEC * H * 2},
@@ -475,6 +562,16 @@ def run_profile_case(args):
     from gemm_deterministic_bf16_gb300 import build as libbuild
     from gemm_deterministic_bf16_gb300.inputs import ffn_inputs
     libbuild.build()
+    if args.profile_case.startswith("rt"):
+        # Rank tree: n = int(suffix) BF16 buffers of 16 MiB, --steps calls.
+        n = int(args.profile_case[2:])
+        bufs = [torch.randn(8 << 20, device="cuda").to(torch.bfloat16) for _ in range(n)]
+        out = torch.empty_like(bufs[0])
+        for _ in range(args.steps):
+            G.detffn_rank_tree_reduce(bufs, out=out)
+        torch.cuda.synchronize()
+        print("profile case %s done" % args.profile_case)
+        return 0
     kind, M = args.profile_case[:3], int(args.profile_case[3:])
     path = {"auto": G.PATH_AUTO, "exact": G.PATH_EXACT, "tensor": G.PATH_TENSOR}[args.path]
     d = ffn_inputs(M, H, I, seed=0, with_dout=(kind == "trn"))
@@ -499,12 +596,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--path", choices=["auto", "exact", "tensor"], default="auto")
-    ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-large", action="store_true", help="skip the M=4096 training measurement")
     ap.add_argument("--profile-case", default=None,
                     help="fwdM or trnM (e.g. fwd8): run --steps forwards (or training steps) "
-                         "of M tokens only, for profiler captures")
+                         "of M tokens only; rtN: --steps rank-tree calls over N 16 MiB BF16 "
+                         "buffers; for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -188,13 +188,17 @@ void set_waits(detffn_handle h, const Opts& o) {
 
 // The kernel family a call uses.  EXACT: CUDA-core kernels with LANE8x8
 // leaves (bit-identical to the oracle).  TENSOR: tcgen05 leaves.  AUTO takes
-// TENSOR for M > 1 token when the tensor kernels cover every contraction
-// length of the call (H, I, I/k and M leaves of the form 1, 2^d or 3*2^d, and
-// H, I multiples of 8), else EXACT: at one token both stream the weights at
-// the same speed and EXACT gives the oracle's bits.  It never depends on the
-// shard count or the chunking: a shard of I has the same leaf-count form as I.
+// TENSOR whenever the tensor kernels cover every contraction length of the
+// call (H, I, I/k and M leaves of the form 1, 2^d or 3*2^d, and H, I
+// multiples of 8), else EXACT.  A tensor-core leaf of an output element does
+// not depend on the other rows or columns of its tile, nor on which operand
+// sits on the MMA's 128-row side, so on the tensor family a token's result
+// is the same for every token count (one token, a decode batch, a prefill);
+// at one token the tensor family is also the faster one.  The choice never
+// depends on the shard count or the chunking: a shard of I has the same
+// leaf-count form as I.
 enum Family { kExact = 0, kTensor = 1 };
-constexpr long long kAutoExactMaxM = 1;
+constexpr long long kAutoExactMaxM = 0;
 
 bool tc_len_ok(long long K) {
   int G, E;
@@ -453,7 +457,8 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
       if (!tcs_plan_fit(R, C, K, 1, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
       const TcsProblem pr{B.p, ldb, A.p, A.rs, out, b_mn};
       return timed(h, st, "tcs_tree_gemm", bytes, 2.0 * R * C * K,
-                   [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->wt, st, dump)); });
+                   [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->wt, st, dump)); },
+                   p.direct ? 1 : 2);
     }
     return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
       return cu(launch_tc_gemm(A.p, a_mn ? A.ks : A.rs, B.p, ldb, R, C, K, out, o_rs, 1, h->wt, h->sm_count, st,
@@ -485,7 +490,7 @@ detffn_status tree_gemm2(detffn_handle h, Family f, Strided A0, Strided B0, uint
     if (!tcs_plan_fit(R, C, K, 2, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
     const TcsProblem pr[2] = {{B0.p, ldb0, A0.p, A0.rs, out0, b_mn}, {B1.p, ldb1, A1.p, A1.rs, out1, b_mn}};
     return timed(h, st, "tcs_tree_gemm", bytes, 4.0 * R * C * K,
-                 [&] { return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st)); });
+                 [&] { return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st)); }, p.direct ? 1 : 2);
   }
   return timed(h, st, "tc_tree_gemm", bytes, 4.0 * R * C * K, [&] {
     const TcProblem pr[2] = {{A0.p, a_mn ? A0.ks : A0.rs, B0.p, ldb0, out0, b_mn, a_mn},
@@ -717,7 +722,7 @@ detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const u
                                 {BU.p, H, x, H, keep ? up + s * w : nullptr}};
       return timed(h, st, "tcs_gateup", bytes, 4.0 * M * w * H, [&] {
         return cu(launch_tcs_gateup(p, pr, hh + s * w, I, h->d_silu, sc.p, sc.bytes, h->wt, st));
-      });
+      }, 2);
     }
     const double bytes = 2.0 * (2.0 * w * H + (double)M * H + 2.0 * M * w);
     TRY(timed(h, st, "tc_tree_gemm", bytes, 4.0 * M * w * H, [&] {

@@ -61,11 +61,12 @@ typedef enum {
 
 typedef enum { DETFFN_F32 = 0, DETFFN_F16 = 1, DETFFN_BF16 = 2 } detffn_dtype;
 
-/* Kernel family.  AUTO picks TENSOR for M > 1 token when the tensor kernels
- * cover the call's contraction lengths (64-wide leaf counts of the form 1, 2^d
- * or 3*2^d, H and I multiples of 8, 16-byte-aligned tensors), else EXACT; it
- * never depends on the shard count or the chunking, and the bits of a token's
- * result may differ between token counts that pick different families.
+/* Kernel family.  AUTO picks TENSOR when the tensor kernels cover the
+ * call's contraction lengths (64-wide leaf counts of the form 1, 2^d or
+ * 3*2^d, H and I multiples of 8, 16-byte-aligned tensors), else EXACT; it
+ * never depends on the shard count or the chunking.  On the TENSOR family a
+ * token's result does not depend on how many tokens the call has (1, a
+ * decode batch, or a prefill of thousands: the same bits).
  * EXACT runs CUDA-core kernels whose leaves follow the LANE8x8 in-leaf
  * order (8 groups of 8 contiguous positions, each summed in ascending order
  * with fused multiply-adds from +0, then ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)));

@@ -217,14 +217,16 @@ def rank_tree(bufs, dtype):
 # The FFN (PR #325, Design; weights [out, in])
 # --------------------------------------------------------------------------
 
-def ffn_forward(x, Wg, Wu, Wd, lw=LEAF_WIDTH, order=LANE):
+def ffn_forward(x, Wg, Wu, Wd, lw=LEAF_WIDTH, order=LANE, nthreads=0):
     """Forward of the bias-free gated FFN (PR #325, Design / Operator test matrix):
     gate = T(x, Wg), up = T(x, Wu) over K=H; h = rne_bf16(silu_bf16(gate)*up);
-    out = T(h, Wd) over K=I.  Returns dict(gate, up, h, out)."""
-    gate = tree_gemm(x, Wg, lw, order)
-    up = tree_gemm(x, Wu, lw, order)
+    out = T(h, Wd) over K=I.  Returns dict(gate, up, h, out).  ``nthreads``
+    (0 = all host cores) only splits output rows over threads; the result
+    does not depend on it."""
+    gate = tree_gemm(x, Wg, lw, order, nthreads)
+    up = tree_gemm(x, Wu, lw, order, nthreads)
     h = silu_mul(gate, up)
-    out = tree_gemm(h, Wd, lw, order)
+    out = tree_gemm(h, Wd, lw, order, nthreads)
     return dict(gate=gate, up=up, h=h, out=out)
 
 

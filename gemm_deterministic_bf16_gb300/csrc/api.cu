@@ -248,10 +248,11 @@ constexpr int kSizingSms = 152;  // SM count a workspace is sized for when no ha
 // (R, C, K, problems, CTAs, direct), and working it out walks every CTA's
 // range, which costs microseconds of host time per call at decode sizes --
 // comparable to the call's device time.  A small table keeps the recent ones.
-bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bool direct, TcsPlan* p) {
+bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bool direct, TcsPlan* p,
+                     int ns = 1) {
   struct Entry {
     long long R, C, K;
-    int np, ctas;
+    int np, ns, ctas;
     bool direct, ok, used;
     TcsPlan plan;
   };
@@ -262,38 +263,41 @@ bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bo
   {
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& e : table)
-      if (e.used && e.R == R && e.C == C && e.K == K && e.np == np && e.ctas == ctas && e.direct == direct) {
+      if (e.used && e.R == R && e.C == C && e.K == K && e.np == np && e.ns == ns && e.ctas == ctas &&
+          e.direct == direct) {
         if (e.ok) *p = e.plan;
         return e.ok;
       }
   }
   TcsPlan plan{};
-  const bool ok = tcs_plan(R, C, K, np, ctas, direct, &plan);
+  const bool ok = tcs_plan(R, C, K, np, ctas, direct, &plan, ns);
   std::lock_guard<std::mutex> lock(mu);
-  table[next] = Entry{R, C, K, np, ctas, direct, ok, true, plan};
+  table[next] = Entry{R, C, K, np, ns, ctas, direct, ok, true, plan};
   next = (next + 1) % kEntries;
   if (ok) *p = plan;
   return ok;
 }
 
-// Piece-slot bytes of a few-token contraction over C weight rows and K, two CTAs per SM.
-size_t tcs_bytes(long long C, long long K, int np, int sms) {
+// Piece-slot bytes of a few-token contraction over C weight rows and K (ns
+// shards of K each), two CTAs per SM.
+size_t tcs_bytes(long long C, long long K, int np, int sms, int ns = 1) {
   TcsPlan p;
-  return tcs_plan_cached(1, C, K, np, 2 * sms, false, &p) ? p.scratch : 0;
+  return tcs_plan_cached(1, C, K, np, 2 * sms, false, &p, ns) ? p.scratch : 0;
 }
 
 // The plan for the scratch at hand: two CTAs per SM when the slots fit, fewer
 // CTAs when they do not, whole tiles per CTA (no slots) as the last resort.
 // The results are the same for every plan.
-bool tcs_plan_fit(long long R, long long C, long long K, int np, int sms, const TcsScratch& sc, TcsPlan* p) {
+bool tcs_plan_fit(long long R, long long C, long long K, int np, int sms, const TcsScratch& sc, TcsPlan* p,
+                  int ns = 1) {
   if (sc.p) {
     for (int ctas = 2 * sms; ctas >= 1; ctas = ctas * 3 / 4) {
-      if (!tcs_plan_cached(R, C, K, np, ctas, false, p)) return false;
+      if (!tcs_plan_cached(R, C, K, np, ctas, false, p, ns)) return false;
       if (p->scratch <= sc.bytes) return true;
       if (ctas == 1) break;
     }
   }
-  return tcs_plan_cached(R, C, K, np, 2 * sms, true, p);
+  return tcs_plan_cached(R, C, K, np, 2 * sms, true, p, ns);
 }
 
 struct FwdWs {
@@ -316,8 +320,8 @@ FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k, int s
   // Tensor family with few tokens: piece slots for gate/up (all of I: the
   // shards' gate/up slices are computed by one launch) and for down.
   if (M >= 1 && M <= 32) {
-    const long long sw = I / k;
-    const size_t gu = tcs_bytes(I, H, 2, sms), dn = tcs_bytes(H, sw, 1, sms);
+    const long long sw = I / k;  // the down projection's k shards go in one launch
+    const size_t gu = tcs_bytes(I, H, 2, sms), dn = tcs_bytes(H, sw, 1, sms, k);
     w.tcs.bytes = gu > dn ? gu : dn;
     w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
   }
@@ -339,8 +343,8 @@ BwdWs plan_backward(Arena& a, long long M, long long H, long long I, int k, bool
   w.cgs = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
   w.cus = k > 1 ? a.take<uint16_t>((long long)k * M * H) : nullptr;
   if (tensor) {
-    if (M >= 1 && M <= 32) {  // dh over K = H; cg and cu (one launch) over K = I / k
-      const size_t d1 = tcs_bytes(I, H, 1, sms), d2 = tcs_bytes(H, I / k, 2, sms);
+    if (M >= 1 && M <= 32) {  // dh over K = H; cg and cu of all k shards (one launch) over K = I / k each
+      const size_t d1 = tcs_bytes(I, H, 1, sms), d2 = tcs_bytes(H, I / k, 2, sms, k);
       w.tcs.bytes = d1 > d2 ? d1 : d2;
       w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
     }
@@ -497,6 +501,55 @@ detffn_status tree_gemm2(detffn_handle h, Family f, Strided A0, Strided B0, uint
                              {A1.p, a_mn ? A1.ks : A1.rs, B1.p, ldb1, out1, b_mn, a_mn}};
     return cu(launch_tc_gemms(pr, 2, R, C, K, o_rs, 1, h->wt, h->sm_count, st));
   });
+}
+
+// The K shard q of a strided operand: K positions [q * Ksh, (q + 1) * Ksh).
+Strided kslice(const Strided& X, long long q, long long Ksh) { return Strided{X.p + q * Ksh * X.ks, X.rs, X.ks}; }
+
+// k contractions over consecutive K shards of Ksh positions each (the
+// tensor-parallel emulation): shard q's result goes to out + q * oss.  On the
+// few-token tensor kernels all shards (and both problems of the two-problem
+// form) are one launch; otherwise one launch per shard.
+detffn_status tree_gemm_k(detffn_handle h, Family f, Strided A, Strided B, long long R, long long C,
+                          long long Ksh, int k, uint16_t* out, long long o_rs, long long oss, cudaStream_t st,
+                          const TcsScratch& sc) {
+  if (f == kTensor && R <= 32 && k > 1) {
+    const bool b_mn = tc_mn_ok(B);
+    if (!tc_operands_ok(A) || !(b_mn || tc_operands_ok(B))) return DETFFN_ERR_ALIGN;
+    TcsPlan p;
+    if (!tcs_plan_fit(R, C, Ksh, 1, h->sm_count, sc, &p, k)) return DETFFN_ERR_SHAPE;
+    const TcsProblem pr{B.p, b_mn ? B.ks : B.rs, A.p, A.rs, out, b_mn};
+    const double bytes = 2.0 * ((double)R * Ksh * k + (double)C * Ksh * k + (double)R * C * k);
+    return timed(h, st, "tcs_tree_gemm", bytes, 2.0 * R * C * Ksh * k, [&] {
+      return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->wt, st, nullptr, oss));
+    }, p.direct ? 1 : 2);
+  }
+  for (int q = 0; q < k; ++q)
+    TRY(tree_gemm(h, f, kslice(A, q, Ksh), kslice(B, q, Ksh), R, C, Ksh, out + q * oss, o_rs, st, sc));
+  return DETFFN_OK;
+}
+
+detffn_status tree_gemm2_k(detffn_handle h, Family f, Strided A0, Strided B0, uint16_t* out0, Strided A1,
+                           Strided B1, uint16_t* out1, long long R, long long C, long long Ksh, int k,
+                           long long o_rs, long long oss, cudaStream_t st, const TcsScratch& sc) {
+  if (f == kTensor && R <= 32 && k > 1) {
+    const bool b_mn = tc_mn_ok(B0);
+    if (tc_mn_ok(B1) != b_mn) return DETFFN_ERR_ALIGN;
+    if (!tc_operands_ok(A0) || !tc_operands_ok(A1) || !(b_mn || (tc_operands_ok(B0) && tc_operands_ok(B1))))
+      return DETFFN_ERR_ALIGN;
+    TcsPlan p;
+    if (!tcs_plan_fit(R, C, Ksh, 2, h->sm_count, sc, &p, k)) return DETFFN_ERR_SHAPE;
+    const TcsProblem pr[2] = {{B0.p, b_mn ? B0.ks : B0.rs, A0.p, A0.rs, out0, b_mn},
+                              {B1.p, b_mn ? B1.ks : B1.rs, A1.p, A1.rs, out1, b_mn}};
+    const double bytes = 4.0 * ((double)R * Ksh * k + (double)C * Ksh * k + (double)R * C * k);
+    return timed(h, st, "tcs_tree_gemm", bytes, 4.0 * R * C * Ksh * k, [&] {
+      return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st, nullptr, oss));
+    }, p.direct ? 1 : 2);
+  }
+  for (int q = 0; q < k; ++q)
+    TRY(tree_gemm2(h, f, kslice(A0, q, Ksh), kslice(B0, q, Ksh), out0 + q * oss, kslice(A1, q, Ksh),
+                   kslice(B1, q, Ksh), out1 + q * oss, R, C, Ksh, o_rs, st, sc));
+  return DETFFN_OK;
 }
 
 detffn_status silu_mul(detffn_handle h, const uint16_t* g, const uint16_t* u, uint16_t* hh,
@@ -796,9 +849,12 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
     } else {
       // gate/up contract over H, which no shard splits: the shards' slices of
       // gate, up and h are the same bits whether computed slice by slice or
-      // at once, so one launch computes all of them.
-      if (s == 0) TRY(gateup_slice(h, f, X, WG, WU, gate, up, saves, w.h, M, H, I, 0, I, st, sc));
-      TRY(tree_gemm(h, f, Strided{w.h + s * sw, I, 1}, Strided{WD + s * sw, I, 1}, M, H, sw, dst, H, st, sc));
+      // at once, so one launch computes all of them.  The down projection's
+      // shards (consecutive K ranges of I) are one call as well.
+      if (s == 0) {
+        TRY(gateup_slice(h, f, X, WG, WU, gate, up, saves, w.h, M, H, I, 0, I, st, sc));
+        TRY(tree_gemm_k(h, f, Strided{w.h, I, 1}, Strided{WD, I, 1}, M, H, sw, k, dst, H, M * H, st, sc));
+      }
     }
   }
   if (k == 1) return DETFFN_OK;
@@ -922,11 +978,14 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   // column n of Wg (K stride H), read MN-major by the tensor family.
   auto wcol = [&](const uint16_t* W, long long s0) { return Strided{W + s0 * H, 1, H}; };
   const long long sw = I / k;
-  for (long long s = 0; s < k; ++s) {
-    uint16_t* cg = k == 1 ? w.cg : w.cgs + s * M * H;
-    uint16_t* cu = k == 1 ? w.cu : w.cus + s * M * H;
-    TRY(tree_gemm2(h, f, Strided{dG + s * sw, I, 1}, wcol(WG, s * sw), cg, Strided{dU + s * sw, I, 1},
-                   wcol(WU, s * sw), cu, M, H, sw, H, st, w.tcs));
+  if (k == 1) {
+    TRY(tree_gemm2(h, f, Strided{dG, I, 1}, wcol(WG, 0), w.cg, Strided{dU, I, 1}, wcol(WU, 0), w.cu, M, H, I, H,
+                   st, w.tcs));
+  } else {
+    // Shard s contracts K positions [s sw, (s+1) sw) of I; all shards' cg and
+    // cu subtree roots in one call.
+    TRY(tree_gemm2_k(h, f, Strided{dG, I, 1}, wcol(WG, 0), w.cgs, Strided{dU, I, 1}, wcol(WU, 0), w.cus, M, H, sw,
+                     k, H, M * H, st, w.tcs));
   }
   if (k > 1) {
     const void *pg[8], *pu[8];

@@ -100,7 +100,10 @@ struct TcsArgs {
   int R, C;         // tokens (<= 32), weight rows per problem
   int G, E;         // leaves per bottom group, levels above the groups (2^E groups per tile)
   int np, T;        // problems (1 or 2), 128-row tiles per problem
-  long long W;      // groups in all: np * T * 2^E
+  int ns;           // K shards per problem (1..8): shard q contracts K positions [q*ksh, (q+1)*ksh)
+  long long ksh;    // K positions per shard (a multiple of 64)
+  long long oss;    // element offset between the outputs of consecutive shards
+  long long W;      // groups in all: np * ns * T * 2^E
   int cap;          // piece slots per CTA
   int nstage;
   int w_mn;         // weights stored [K][C] (C contiguous): MN-major A tiles
@@ -119,6 +122,17 @@ struct TcsArgs {
 // boundaries only, so every tile's root is formed in one CTA.
 __host__ __device__ __forceinline__ long long range_lo(long long b, long long W, long long P, int Q, bool direct) {
   return direct ? (b * (W / Q) / P) * Q : b * W / P;
+}
+
+// Segment s = one tree per (row tile t, K shard q, problem pb), in that
+// nesting: s = (t * ns + q) * np + pb.
+struct Seg {
+  int t, q, pb;
+};
+__host__ __device__ __forceinline__ Seg seg_of(long long s, int np, int ns) {
+  const long long per = (long long)np * ns;
+  const int rem = (int)(s % per);
+  return Seg{(int)(s / per), rem / np, rem % np};
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
@@ -159,15 +173,16 @@ __device__ __forceinline__ void emit_piece(uint16_t* slots, int& n, int cap, int
 namespace detffn {
 namespace {
 
-// The weight tile of leaf j, row tile t: 128 rows x 64 K, K-major (one box)
-// or, for weights stored [K][C], MN-major (two boxes of 64 rows x 64 K).
-__device__ __forceinline__ void load_w(unsigned char* dst, const CUtensorMap* mW, int j, int t, uint64_t* bar,
+// The weight tile of the leaf at K position k, row tile t: 128 rows x 64 K,
+// K-major (one box) or, for weights stored [K][C], MN-major (two boxes of
+// 64 rows x 64 K).
+__device__ __forceinline__ void load_w(unsigned char* dst, const CUtensorMap* mW, int k, int t, uint64_t* bar,
                                        uint64_t pol, int mn) {
   if (mn) {
-    tma_load_2d_hint(dst, mW, t * BM, j * BK, bar, pol);
-    tma_load_2d_hint(dst + A_BYTES / 2, mW, t * BM + BM / 2, j * BK, bar, pol);
+    tma_load_2d_hint(dst, mW, t * BM, k, bar, pol);
+    tma_load_2d_hint(dst + A_BYTES / 2, mW, t * BM + BM / 2, k, bar, pol);
   } else {
-    tma_load_2d_hint(dst, mW, j * BK, t * BM, bar, pol);
+    tma_load_2d_hint(dst, mW, k, t * BM, bar, pol);
   }
 }
 
@@ -245,13 +260,14 @@ __global__ void __maxnreg__(128)
         const long long s = w / Q;
         const int qa = (int)(w - s * Q);
         const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
-        const int t = (int)(s / a.np), pb = (int)(s % a.np);
-        const CUtensorMap* mW = pb ? &tmW2 : &tmW;
+        const Seg g = seg_of(s, a.np, a.ns);
+        const int k0 = (int)(g.q * a.ksh);
+        const CUtensorMap* mW = g.pb ? &tmW2 : &tmW;
         for (int j = qa * GG; j < qb * GG && it < NS; ++j, ++it) {
           if ((int)(it % kProd) != warp) continue;
           if (elect_one()) {
             mbar_arrive_expect_tx(&bars->full[it], (uint32_t)STAGE);
-            load_w(stages + it * STAGE, mW, j, t, &bars->full[it], pol, a.w_mn);
+            load_w(stages + it * STAGE, mW, k0 + j * BK, g.t, &bars->full[it], pol, a.w_mn);
           }
           __syncwarp();
         }
@@ -267,9 +283,10 @@ __global__ void __maxnreg__(128)
       const long long s = w / Q;
       const int qa = (int)(w - s * Q);
       const int qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
-      const int t = (int)(s / a.np), pb = (int)(s % a.np);
-      const CUtensorMap* mW = pb ? &tmW2 : &tmW;
-      const CUtensorMap* mX = pb ? &tmX2 : &tmX;
+      const Seg g = seg_of(s, a.np, a.ns);
+      const int k0 = (int)(g.q * a.ksh);
+      const CUtensorMap* mW = g.pb ? &tmW2 : &tmW;
+      const CUtensorMap* mX = g.pb ? &tmX2 : &tmX;
       for (int j = qa * GG; j < qb * GG; ++j, ++it, rs.next(NS)) {
         const bool reuse = it >= NS;  // (the first NS weight tiles are already on their way)
         const int vb = rv.slot;
@@ -288,9 +305,9 @@ __global__ void __maxnreg__(128)
         if (!a.stall && elect_one()) {
           if (reuse) {
             mbar_arrive_expect_tx(&bars->full[st], (uint32_t)STAGE);
-            load_w(dst, mW, j, t, &bars->full[st], pol, a.w_mn);
+            load_w(dst, mW, k0 + j * BK, g.t, &bars->full[st], pol, a.w_mn);
           }
-          tma_load_2d(dst + A_BYTES, mX, j * BK, 0, &bars->full[st]);
+          tma_load_2d(dst + A_BYTES, mX, k0 + j * BK, 0, &bars->full[st]);
         }
         __syncwarp();
       }
@@ -365,8 +382,9 @@ __global__ void __maxnreg__(128)
         // The group root: a lone leaf rounded once, l0 + l1, or l0 + (l1 + l2).
         uint32_t root[WORDS];
         // Leaf dump: this thread's weight row of the tile, tokens 16 c + i.
-        float* const dmp = DUMP ? a.dump + (size_t)(s % a.np) * a.R * a.C * a.L : nullptr;
-        const long long crow = (s / a.np) * BM + row;
+        const Seg sg = seg_of(s, a.np, a.ns);
+        float* const dmp = DUMP ? a.dump + (size_t)sg.pb * a.R * a.C * a.L : nullptr;
+        const long long crow = (long long)sg.t * BM + row;
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c) {
           uint32_t v0[16];
@@ -426,8 +444,8 @@ __global__ void __maxnreg__(128)
           if (live) {
             if (m == a.E) {  // the whole tile: its root
               if (direct) {
-                const long long c = (long long)(s / a.np) * BM + row;
-                uint16_t* o = (s % a.np) ? a.out1 : a.out0;
+                const long long c = (long long)sg.t * BM + row;
+                uint16_t* o = (sg.pb ? a.out1 : a.out0) + sg.q * a.oss;
                 if (c < a.C)
 #pragma unroll
                   for (int i = 0; i < BN; ++i)
@@ -490,7 +508,8 @@ namespace detffn {
 namespace {
 
 struct TcsTopArgs {
-  int R, C, E, np;
+  int R, C, E, np, ns;  // ns: K shards per problem (segments as in the streaming kernel)
+  long long oss;        // element offset between consecutive shards' outputs
   long long W;
   int P, cap;
   const uint16_t* slots;
@@ -733,10 +752,10 @@ __global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
   }
   const int r0 = kTopTok * quad;
   if constexpr (!FUSED) {
-    const int t = (int)(s0 / a.np), pb = (int)(s0 % a.np);
+    const Seg sg = seg_of(s0, a.np, a.ns);
     put_tile(tiles, row, f[0].root);
     __syncthreads();
-    store_tile(tiles, pb ? a.out1 : a.out0, a.ldo, a.R, r0, (long long)t * BM, a.C);
+    store_tile(tiles, (sg.pb ? a.out1 : a.out0) + sg.q * a.oss, a.ldo, a.R, r0, (long long)sg.t * BM, a.C);
   } else {
     const int t = blockIdx.x;
     const uint32_t gw[4] = {f[0].root.x, f[0].root.y, f[0].root.z, f[0].root.w};
@@ -764,8 +783,9 @@ __global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
 
 namespace detffn {
 
-bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* p) {
+bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* p, int ns) {
   if (R < 1 || R > BN || C < 1 || K < 1 || np < 1 || np > 2 || max_ctas < 1) return false;
+  if (ns < 1 || ns > kTcsMaxShards || (ns > 1 && K % BK != 0)) return false;
   const long long L = (K + BK - 1) / BK;
   int G;
   long long q;
@@ -791,11 +811,12 @@ bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool 
   r.G = G;
   r.E = E;
   r.np = np;
+  r.ns = ns;
   r.T = (int)((C + BM - 1) / BM);
   const int Q = 1 << E;
-  r.W = (long long)np * r.T * Q;
+  r.W = (long long)np * ns * r.T * Q;
   r.direct = direct;
-  const long long units = direct ? (long long)np * r.T : r.W;
+  const long long units = direct ? (long long)np * ns * r.T : r.W;
   r.P = (int)(max_ctas < units ? max_ctas : units);
   r.nstage = stages_for(E);
   if (r.nstage < 2) return false;
@@ -847,7 +868,10 @@ cudaError_t launch_dependent(void (*k)(KArgs...), dim3 grid, int threads, int sm
 }
 
 cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo, uint16_t* h, const uint16_t* silu,
-                       void* scratch, size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump) {
+                       void* scratch, size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump,
+                       long long oss) {
+  if (plan.ns > 1 && (h || dump)) return cudaErrorInvalidValue;
+  const long long Ktot = plan.K * plan.ns;  // the maps span every shard's K range
   if (!plan.direct && (!scratch || scratch_bytes < plan.scratch || ((uintptr_t)scratch & 15u)))
     return cudaErrorInvalidValue;
   if (plan.direct && h) return cudaErrorInvalidValue;
@@ -858,10 +882,10 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   CUtensorMap m[4];
   for (int p = 0; p < 2; ++p) {
     const TcsProblem& q = pr[p < plan.np ? p : 0];
-    const bool wmap = q.w_mn ? tc_make_map(&m[2 * p], q.W, plan.K, plan.C, q.ldw, BK)
-                             : tc_make_map(&m[2 * p], q.W, plan.C, plan.K, q.ldw, BM);
+    const bool wmap = q.w_mn ? tc_make_map(&m[2 * p], q.W, Ktot, plan.C, q.ldw, BK)
+                             : tc_make_map(&m[2 * p], q.W, plan.C, Ktot, q.ldw, BM);
     if (!wmap ||
-        !tc_make_map(&m[2 * p + 1], q.X, plan.R, plan.K, q.ldx, BN))
+        !tc_make_map(&m[2 * p + 1], q.X, plan.R, Ktot, q.ldx, BN))
       return cudaErrorInvalidValue;
   }
   static std::once_flag once;
@@ -891,6 +915,9 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   a.G = plan.G;
   a.E = plan.E;
   a.np = plan.np;
+  a.ns = plan.ns;
+  a.ksh = plan.K;
+  a.oss = oss;
   a.T = plan.T;
   a.W = plan.W;
   a.cap = plan.cap;
@@ -916,6 +943,8 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   t.C = (int)plan.C;
   t.E = plan.E;
   t.np = plan.np;
+  t.ns = plan.ns;
+  t.oss = oss;
   t.W = plan.W;
   t.P = plan.P;
   t.cap = plan.cap;
@@ -926,7 +955,7 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   t.h = h;
   t.silu = silu;
   t.status = wt.status;
-  const dim3 grid(h ? plan.T : plan.np * plan.T, (plan.R + kTopTok - 1) / kTopTok);
+  const dim3 grid(h ? plan.T : plan.np * plan.ns * plan.T, (plan.R + kTopTok - 1) / kTopTok);
   const int smem_top = top_smem(h != nullptr, plan.E, plan.cap);
   return h ? launch_dependent(k_tcs_top<true>, grid, kTopThreads, smem_top, st, t)
            : launch_dependent(k_tcs_top<false>, grid, kTopThreads, smem_top, st, t);
@@ -935,17 +964,17 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
 }  // namespace
 
 cudaError_t launch_tcs(const TcsPlan& plan, const TcsProblem* pr, long long ldo, void* scratch,
-                       size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump) {
+                       size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump, long long oss) {
   for (int p = 0; p < plan.np; ++p)
     if (!pr[p].out) return cudaErrorInvalidValue;
-  return tcs_launch(plan, pr, ldo, nullptr, nullptr, scratch, scratch_bytes, wt, st, dump);
+  return tcs_launch(plan, pr, ldo, nullptr, nullptr, scratch, scratch_bytes, wt, st, dump, oss);
 }
 
 cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* pr, uint16_t* h, long long ldo,
                               const uint16_t* silu, void* scratch, size_t scratch_bytes, const Waits& wt,
                               cudaStream_t st) {
   if (plan.np != 2 || !h || !silu) return cudaErrorInvalidValue;
-  return tcs_launch(plan, pr, ldo, h, silu, scratch, scratch_bytes, wt, st, nullptr);
+  return tcs_launch(plan, pr, ldo, h, silu, scratch, scratch_bytes, wt, st, nullptr, 0);
 }
 
 }  // namespace detffn

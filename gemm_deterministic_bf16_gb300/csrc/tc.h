@@ -51,11 +51,12 @@ bool tc_make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long
 // the work split evenly over two CTAs per SM (balanced K ranges whose partial
 // subtrees a second kernel folds into the canonical tree).
 // ---------------------------------------------------------------------------
-constexpr int kTcsMaxLv = 8;  // at most 2^8 bottom groups (K <= 3 * 256 * 64)
+constexpr int kTcsMaxLv = 8;      // at most 2^8 bottom groups (K <= 3 * 256 * 64)
+constexpr int kTcsMaxShards = 8;  // K shards per problem in one launch
 
 struct TcsPlan {
-  int R = 0, G = 0, E = 0, T = 0, np = 0, P = 0, cap = 0, nstage = 0, top_smem = 0;
-  long long C = 0, K = 0, W = 0;
+  int R = 0, G = 0, E = 0, T = 0, np = 0, ns = 1, P = 0, cap = 0, nstage = 0, top_smem = 0;
+  long long C = 0, K = 0, W = 0;    // K: the contraction length of one shard
   bool direct = false;  // whole tiles per CTA, roots stored directly (no scratch, no top kernel)
   size_t scratch = 0;   // bytes of piece slots the launch needs
 };
@@ -63,8 +64,12 @@ struct TcsPlan {
 // Plans a launch on at most max_ctas CTAs (two per SM is the design point).
 // False when the shape is not covered (R > 32, or K's leaf count not 1, 2^d or
 // 3 * 2^d with at most 2^8 bottom groups).  The results never depend on the
-// plan: only the split of each tree into pieces does.
-bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* plan);
+// plan: only the split of each tree into pieces does.  With ns > 1, each
+// problem is ns contractions over consecutive K ranges of K positions each
+// (K a multiple of 64): shard q reads K positions [q K, (q+1) K) of the
+// operands and writes its own output (out + q * oss), one tree each.
+bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* plan,
+              int ns = 1);
 
 struct TcsProblem {
   const uint16_t* W;  // [C, K] weights, row stride ldw (multiple of 8), 16-byte aligned;
@@ -78,7 +83,8 @@ struct TcsProblem {
 // One or two same-shaped contractions (plan.np): two launches on `st`, or one
 // in direct mode (scratch unused).
 cudaError_t launch_tcs(const TcsPlan& plan, const TcsProblem* problems, long long ldo, void* scratch,
-                       size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump = nullptr);
+                       size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump = nullptr,
+                       long long oss = 0);
 
 // Gate (problems[0]) and up (problems[1]) with the SiLU * up stage boundary
 // fused into the top of the trees: h[r * ldo + c] = bf16(bf16(SiLU(gate)) * up);

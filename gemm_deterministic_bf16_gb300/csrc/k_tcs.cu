@@ -121,6 +121,17 @@ struct TcsArgs {
   float* dump;      // leaf dump (DUMP instances): [np][R][C][L] FP32 leaves
 };
 
+// What the tile fold needs from the launch's arguments, copied at the fold
+// (taking the address of the kernel's parameter block would move it to local
+// memory for the whole kernel, the streaming loops included).
+struct FoldArgs {
+  int R, C, E, np, ns, UG, cap, fold_ch, fused;
+  long long W, oss, ldo;
+  const uint16_t* slots;
+  uint16_t *out0, *out1, *h;
+  const uint16_t* silu;
+};
+
 // Segment s = one tree per (row tile t, K shard q, problem pb), in that
 // nesting: s = (t * ns + q) * np + pb.
 struct Seg {
@@ -253,7 +264,7 @@ static_assert(sizeof(PieceRef) == kPieceRefBytes, "piece list entries: shared-me
 // Lists, in order, the pieces of segment s that CTAs [b_base, min(b_base +
 // 32, b_end)) wrote (P CTAs in all): one lane per CTA, placed by a warp
 // scan.  Returns the count.
-__device__ int list_pieces(const TcsArgs& a, long long s, long long b_base, long long b_end, long long P,
+__device__ int list_pieces(const FoldArgs& a, long long s, long long b_base, long long b_end, long long P,
                            PieceRef* list, int lane) {
   const int Q = 1 << a.E;
   const long long ws = s * Q, we = ws + Q;
@@ -309,7 +320,7 @@ __device__ __forceinline__ uint4 add4(uint4 l, uint4 r) {
 // thread's row of the root: 32 tokens as 4 x 16 bytes.  Shared memory (the
 // idle stage area): stack [E][4][BM] and staged pieces [fold_ch][4][BM]
 // (16 bytes each, this thread's row only), then the list.
-__device__ __noinline__ void fold_segment(const TcsArgs& a, long long s, unsigned char* fsm, Bars* bars, int row, int ew,
+__device__ __noinline__ void fold_segment(const FoldArgs& a, long long s, unsigned char* fsm, Bars* bars, int row, int ew,
                              int lane, uint4 (&root)[4]) {
   const int Q = 1 << a.E;
   const long long P = gridDim.x;
@@ -377,7 +388,7 @@ __device__ __forceinline__ void words_of(const uint4 (&r)[4], uint32_t (&v)[WORD
 
 // The last CTA to arrive on fold unit u: folds its segments' pieces and
 // stores the result (the root, or h for gate and up).
-__device__ __noinline__ void fold_unit(const TcsArgs& a, long long u, unsigned char* fsm, Bars* bars, int row, int ew, int lane) {
+__device__ __noinline__ void fold_unit(const FoldArgs& a, long long u, unsigned char* fsm, Bars* bars, int row, int ew, int lane) {
   const int spu = a.fused ? 2 : 1;
   uint4 r0[4];
   uint32_t v0[WORDS];
@@ -722,7 +733,9 @@ __global__ void __maxnreg__(128)
         epi_sync();
         if (bars->fold_last) {
           __threadfence();
-          fold_unit(a, u, smem, bars, row, warp - kEpi0, lane);
+          const FoldArgs fa{a.R,   a.C,   a.E,     a.np,  a.ns,  a.UG,   a.cap,  a.fold_ch, a.fused,
+                            a.W,   a.oss, a.ldo,   a.slots, a.out0, a.out1, a.h, a.silu};
+          fold_unit(fa, u, smem, bars, row, warp - kEpi0, lane);
         }
       }
     }

@@ -25,9 +25,6 @@ struct detffn_handle_s {
   float* d_dsilu = nullptr;     // [65536] FP32 SiLU' by gate bit pattern
   int* d_status = nullptr;      // device status word (bounded waits)
   Waits wt;                     // the current call's wait settings (status word, poll limit, test stall)
-  // Few-token scratch regions zeroed once (their fold-unit tickets start at
-  // zero and the kernels leave them at zero): (address, bytes), most recent last.
-  std::vector<std::pair<void*, size_t>> zeroed;
   std::vector<uint16_t> h_silu;
   std::vector<float> h_dsilu;
   // Measurement: event pairs around launches while profiling is on.
@@ -246,31 +243,17 @@ struct TcsScratch {
 };
 constexpr int kSizingSms = 152;  // SM count a workspace is sized for when no handle is given
 
-// The few-token kernels' fold-unit tickets live in the caller's workspace:
-// they must read as zero (or as a stale launch epoch) when a launch starts,
-// and every launch that completes leaves them at zero.  A workspace region
-// this handle has not seen before is zeroed once, on the call's stream.
-detffn_status tcs_scratch_ready(detffn_handle h, const TcsScratch& sc, cudaStream_t st) {
-  if (!sc.p || !sc.bytes) return DETFFN_OK;
-  for (const auto& z : h->zeroed)
-    if (z.first == sc.p && z.second >= sc.bytes) return DETFFN_OK;
-  if (cudaMemsetAsync(sc.p, 0, sc.bytes, st) != cudaSuccess) return DETFFN_ERR_CUDA;
-  if (h->zeroed.size() >= 16) h->zeroed.erase(h->zeroed.begin());
-  h->zeroed.emplace_back(sc.p, sc.bytes);
-  return DETFFN_OK;
-}
-
 // Plans are validated and worked out once per signature (as the transport
 // collectives do, RL-Kernel PR #356, "Design"): a plan depends only on
 // (R, C, K, problems, CTAs, direct), and working it out walks every CTA's
 // range, which costs microseconds of host time per call at decode sizes --
 // comparable to the call's device time.  A small table keeps the recent ones.
 bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bool direct, TcsPlan* p,
-                     int ns = 1, bool fused = false) {
+                     int ns = 1) {
   struct Entry {
     long long R, C, K;
     int np, ns, ctas;
-    bool direct, fused, ok, used;
+    bool direct, ok, used;
     TcsPlan plan;
   };
   constexpr int kEntries = 32;
@@ -281,15 +264,15 @@ bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bo
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& e : table)
       if (e.used && e.R == R && e.C == C && e.K == K && e.np == np && e.ns == ns && e.ctas == ctas &&
-          e.direct == direct && e.fused == fused) {
+          e.direct == direct) {
         if (e.ok) *p = e.plan;
         return e.ok;
       }
   }
   TcsPlan plan{};
-  const bool ok = tcs_plan(R, C, K, np, ctas, direct, &plan, ns, fused);
+  const bool ok = tcs_plan(R, C, K, np, ctas, direct, &plan, ns);
   std::lock_guard<std::mutex> lock(mu);
-  table[next] = Entry{R, C, K, np, ns, ctas, direct, fused, ok, true, plan};
+  table[next] = Entry{R, C, K, np, ns, ctas, direct, ok, true, plan};
   next = (next + 1) % kEntries;
   if (ok) *p = plan;
   return ok;
@@ -297,24 +280,24 @@ bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bo
 
 // Piece-slot bytes of a few-token contraction over C weight rows and K (ns
 // shards of K each), two CTAs per SM.
-size_t tcs_bytes(long long C, long long K, int np, int sms, int ns = 1, bool fused = false) {
+size_t tcs_bytes(long long C, long long K, int np, int sms, int ns = 1) {
   TcsPlan p;
-  return tcs_plan_cached(1, C, K, np, 2 * sms, false, &p, ns, fused) ? p.scratch : 0;
+  return tcs_plan_cached(1, C, K, np, 2 * sms, false, &p, ns) ? p.scratch : 0;
 }
 
 // The plan for the scratch at hand: two CTAs per SM when the slots fit, fewer
 // CTAs when they do not, whole tiles per CTA (no slots) as the last resort.
 // The results are the same for every plan.
 bool tcs_plan_fit(long long R, long long C, long long K, int np, int sms, const TcsScratch& sc, TcsPlan* p,
-                  int ns = 1, bool fused = false) {
+                  int ns = 1) {
   if (sc.p) {
     for (int ctas = 2 * sms; ctas >= 1; ctas = ctas * 3 / 4) {
-      if (!tcs_plan_cached(R, C, K, np, ctas, false, p, ns, fused)) break;
+      if (!tcs_plan_cached(R, C, K, np, ctas, false, p, ns)) return false;
       if (p->scratch <= sc.bytes) return true;
       if (ctas == 1) break;
     }
   }
-  return tcs_plan_cached(R, C, K, np, 2 * sms, true, p, ns, fused);
+  return tcs_plan_cached(R, C, K, np, 2 * sms, true, p, ns);
 }
 
 struct FwdWs {
@@ -338,7 +321,7 @@ FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k, int s
   // shards' gate/up slices are computed by one launch) and for down.
   if (M >= 1 && M <= 32) {
     const long long sw = I / k;  // the down projection's k shards go in one launch
-    const size_t gu = tcs_bytes(I, H, 2, sms, 1, true), dn = tcs_bytes(H, sw, 1, sms, k);
+    const size_t gu = tcs_bytes(I, H, 2, sms), dn = tcs_bytes(H, sw, 1, sms, k);
     w.tcs.bytes = gu > dn ? gu : dn;
     w.tcs.p = a.take<unsigned char>((long long)w.tcs.bytes);
   }
@@ -477,10 +460,9 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
       TcsPlan p;
       if (!tcs_plan_fit(R, C, K, 1, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
       const TcsProblem pr{B.p, ldb, A.p, A.rs, out, b_mn};
-      if (!p.direct) TRY(tcs_scratch_ready(h, sc, st));
       return timed(h, st, "tcs_tree_gemm", bytes, 2.0 * R * C * K,
                    [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->wt, st, dump)); },
-                   1);
+                   p.direct ? 1 : 2);
     }
     return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
       return cu(launch_tc_gemm(A.p, a_mn ? A.ks : A.rs, B.p, ldb, R, C, K, out, o_rs, 1, h->wt, h->sm_count, st,
@@ -511,9 +493,8 @@ detffn_status tree_gemm2(detffn_handle h, Family f, Strided A0, Strided B0, uint
     TcsPlan p;
     if (!tcs_plan_fit(R, C, K, 2, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
     const TcsProblem pr[2] = {{B0.p, ldb0, A0.p, A0.rs, out0, b_mn}, {B1.p, ldb1, A1.p, A1.rs, out1, b_mn}};
-    if (!p.direct) TRY(tcs_scratch_ready(h, sc, st));
     return timed(h, st, "tcs_tree_gemm", bytes, 4.0 * R * C * K,
-                 [&] { return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st)); });
+                 [&] { return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st)); }, p.direct ? 1 : 2);
   }
   return timed(h, st, "tc_tree_gemm", bytes, 4.0 * R * C * K, [&] {
     const TcProblem pr[2] = {{A0.p, a_mn ? A0.ks : A0.rs, B0.p, ldb0, out0, b_mn, a_mn},
@@ -539,10 +520,9 @@ detffn_status tree_gemm_k(detffn_handle h, Family f, Strided A, Strided B, long 
     if (!tcs_plan_fit(R, C, Ksh, 1, h->sm_count, sc, &p, k)) return DETFFN_ERR_SHAPE;
     const TcsProblem pr{B.p, b_mn ? B.ks : B.rs, A.p, A.rs, out, b_mn};
     const double bytes = 2.0 * ((double)R * Ksh * k + (double)C * Ksh * k + (double)R * C * k);
-    if (!p.direct) TRY(tcs_scratch_ready(h, sc, st));
     return timed(h, st, "tcs_tree_gemm", bytes, 2.0 * R * C * Ksh * k, [&] {
       return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->wt, st, nullptr, oss));
-    });
+    }, p.direct ? 1 : 2);
   }
   for (int q = 0; q < k; ++q)
     TRY(tree_gemm(h, f, kslice(A, q, Ksh), kslice(B, q, Ksh), R, C, Ksh, out + q * oss, o_rs, st, sc));
@@ -562,10 +542,9 @@ detffn_status tree_gemm2_k(detffn_handle h, Family f, Strided A0, Strided B0, ui
     const TcsProblem pr[2] = {{B0.p, b_mn ? B0.ks : B0.rs, A0.p, A0.rs, out0, b_mn},
                               {B1.p, b_mn ? B1.ks : B1.rs, A1.p, A1.rs, out1, b_mn}};
     const double bytes = 4.0 * ((double)R * Ksh * k + (double)C * Ksh * k + (double)R * C * k);
-    if (!p.direct) TRY(tcs_scratch_ready(h, sc, st));
     return timed(h, st, "tcs_tree_gemm", bytes, 4.0 * R * C * Ksh * k, [&] {
       return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st, nullptr, oss));
-    });
+    }, p.direct ? 1 : 2);
   }
   for (int q = 0; q < k; ++q)
     TRY(tree_gemm2(h, f, kslice(A0, q, Ksh), kslice(B0, q, Ksh), out0 + q * oss, kslice(A1, q, Ksh),
@@ -790,14 +769,13 @@ detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const u
       // Few tokens: the top of both trees fused with SiLU * up; gate and up
       // are stored only when the caller keeps them.
       TcsPlan p;
-      if (!tcs_plan_fit(M, w, H, 2, h->sm_count, sc, &p, 1, true) || p.direct) return DETFFN_ERR_WORKSPACE;
+      if (!tcs_plan_fit(M, w, H, 2, h->sm_count, sc, &p) || p.direct) return DETFFN_ERR_WORKSPACE;
       const double bytes = 2.0 * (2.0 * w * H + (double)M * H + (keep ? 3.0 : 1.0) * M * w);
       const TcsProblem pr[2] = {{BG.p, H, x, H, keep ? gate + s * w : nullptr},
                                 {BU.p, H, x, H, keep ? up + s * w : nullptr}};
-      if (!p.direct) TRY(tcs_scratch_ready(h, sc, st));
       return timed(h, st, "tcs_gateup", bytes, 4.0 * M * w * H, [&] {
         return cu(launch_tcs_gateup(p, pr, hh + s * w, I, h->d_silu, sc.p, sc.bytes, h->wt, st));
-      });
+      }, 2);
     }
     const double bytes = 2.0 * (2.0 * w * H + (double)M * H + 2.0 * M * w);
     TRY(timed(h, st, "tc_tree_gemm", bytes, 4.0 * M * w * H, [&] {

@@ -13,11 +13,10 @@
 // CTA streams the same number of bytes to within one group.  Where a range
 // covers only part of a tile, the CTA folds that part into its maximal
 // aligned subtrees -- nodes of the canonical tree -- and writes them as
-// "pieces".  The CTAs that share a tile take a ticket once their ranges are
-// done; the last of them folds the tile's pieces, left to right, into the
-// root (and, for gate and up, applies SiLU * up).  A tile that lies inside
-// one CTA's range is finished by that CTA directly.  Nothing waits on
-// another CTA.  Without scratch ("direct" mode) CTAs take whole tiles.
+// "pieces"; a second kernel folds each tile's pieces, left to right, into the
+// root.  A whole tile is one piece, its root.  Nothing in the streaming
+// kernel waits on another CTA.  Without scratch ("direct" mode) CTAs take
+// whole tiles and store the roots themselves.
 //
 // Streaming.  Two CTAs per SM.  In each, two producer warps issue the TMA
 // loads of alternate leaves, one warp issues the MMAs (4 x K=16 per 64-wide
@@ -29,8 +28,6 @@
 // stops, drains its own copies and MMAs (bounded) and frees its TMEM.
 #include <cuda.h>
 
-#include <atomic>
-#include <chrono>
 #include <mutex>
 #include <utility>
 
@@ -62,12 +59,21 @@ constexpr int BAR_BYTES = 512;
 constexpr int MAX_SMEM = 113 * 1024;
 constexpr int MAX_STAGES = 8;
 constexpr int PIECE = BM * BN;    // elements of one piece: [row][token], 64 bytes per row
-// The tile fold at the end of a CTA's range reuses the stage and stack-level
-// shared memory (idle by then): a stack of E levels and a few staged pieces,
-// each [4 quarters][128 rows] x 16 bytes, and the piece list (8 bytes per entry).
-constexpr int kFoldRowBytes = BM * BN * 2;  // one level or one staged piece: 8 KB
-constexpr int kPieceRefBytes = 8;           // sizeof(PieceRef), checked where it is defined
-constexpr int kMaxFoldChunk = 8;
+constexpr int kTopTok = 8;        // top kernel: tokens per CTA (one 16-byte quarter of a piece row; grid.y covers the rest)
+constexpr int kTopThreads = BM;   // one thread per row
+// Pieces per segment staged in shared memory at a time: fused gate/up CTAs
+// (two segments, a few pieces each at decode sizes) and plain CTAs (one
+// segment, up to a few dozen pieces).
+__host__ __device__ constexpr int top_chunk(bool fused) { return fused ? 8 : 32; }
+// Dynamic shared memory of a top CTA: staged pieces, the fold stacks (E
+// levels), the output tiles and the piece lists (16 bytes per row and piece
+// or level).
+constexpr int kPieceRefBytes = 8;  // sizeof(PieceRef), checked where it is defined
+__host__ __device__ inline int top_smem(bool fused, int E, int cap) {
+  const int nseg = fused ? 2 : 1;
+  return nseg * top_chunk(fused) * BM * 16 + nseg * E * BM * 16 + 3 * kTopTok * (BM + 8) * 2 +
+         2 * (32 * cap + 1) * kPieceRefBytes;
+}
 
 static_assert(kTcsMaxLv >= REG_LV, "stack levels");
 static_assert(MAX_STAGES <= kNBuf, "stage reuse is read off the leaf barriers");
@@ -87,8 +93,6 @@ struct Bars {
   uint64_t full[MAX_STAGES], accf[kNBuf], acce[kNBuf], fin;
   uint32_t tmem_slot;
   int abort;
-  int fold_last;  // the tile fold: this CTA arrived last on the unit's ticket
-  int fold_n;     // the tile fold: entries of the current piece list
 };
 static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block");
 
@@ -104,15 +108,8 @@ struct TcsArgs {
   int nstage;
   int w_mn;         // weights stored [K][C] (C contiguous): MN-major A tiles
   uint16_t* slots;  // [gridDim.x][cap][BM][BN]; null: direct mode
-  unsigned long long* tick;  // per fold unit: (launch epoch << 32) | arrivals; 0 after the fold
-  unsigned epoch;   // this launch's ticket epoch (stale tickets of an aborted launch read as 0)
-  int fused;        // gate (problem 0) and up (problem 1) with h = bf16(bf16(SiLU(gate)) * up)
-  int UG;           // groups per fold unit: 2^E (one tree), or 2^(E+1) when fused (gate and up of a tile)
-  int fold_ch;      // pieces staged at a time by the tile fold
-  uint16_t* out0;   // roots go to out_p[r * ldo + c] (+ shard * oss); fused: gate, or null
-  uint16_t* out1;   // fused: up, or null
-  uint16_t* h;      // fused: h[r * ldo + c]
-  const uint16_t* silu;
+  uint16_t* out0;   // direct mode: roots go to out_p[r * ldo + c]
+  uint16_t* out1;
   long long ldo;
   int* status;
   long long spin;
@@ -121,16 +118,11 @@ struct TcsArgs {
   float* dump;      // leaf dump (DUMP instances): [np][R][C][L] FP32 leaves
 };
 
-// What the tile fold needs from the launch's arguments, copied at the fold
-// (taking the address of the kernel's parameter block would move it to local
-// memory for the whole kernel, the streaming loops included).
-struct FoldArgs {
-  int R, C, E, np, ns, UG, cap, fold_ch, fused;
-  long long W, oss, ldo;
-  const uint16_t* slots;
-  uint16_t *out0, *out1, *h;
-  const uint16_t* silu;
-};
+// First group of CTA b's range.  Direct mode deals whole tiles: segment
+// boundaries only, so every tile's root is formed in one CTA.
+__host__ __device__ __forceinline__ long long range_lo(long long b, long long W, long long P, int Q, bool direct) {
+  return direct ? (b * (W / Q) / P) * Q : b * W / P;
+}
 
 // Segment s = one tree per (row tile t, K shard q, problem pb), in that
 // nesting: s = (t * ns + q) * np + pb.
@@ -164,66 +156,6 @@ __device__ __forceinline__ void dump_tokens(float* d, long long crow, int t0, in
     if (t0 + i < R) d[((size_t)(t0 + i) * (size_t)C + (size_t)crow) * (size_t)L + (size_t)j] = __uint_as_float(v[i]);
 }
 
-// The 4 epilogue warps' own barrier (the producers and the MMA warp do not
-// take part).
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); }
-// True in every epilogue thread if p holds in any of them (the same barrier).
-__device__ __forceinline__ bool epi_any(bool p) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, 1, %2, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)p), "n"(kEpiWarps * 32)
-      : "memory");
-  return r != 0;
-}
-
-// Token i of a row held as packed BF16 pairs (word i / 2, low half first) to
-// o[i * ldo + c], for i < R and c < C.
-__device__ __forceinline__ void store_words(const uint32_t (&v)[WORDS], uint16_t* o, long long ldo, int R, long long c,
-                                            long long C) {
-  if (c >= C) return;
-#pragma unroll
-  for (int i = 0; i < BN; ++i)
-    if (i < R) o[i * ldo + c] = (uint16_t)(v[i >> 1] >> (16 * (i & 1)));
-}
-
-// The fused stage boundary of one row: h = bf16(bf16(SiLU(gate)) * up) for
-// every token, plus gate and up where they are kept.
-template <class Args>
-__device__ __forceinline__ void store_fused(const uint32_t (&g)[WORDS], const uint32_t (&u)[WORDS], const Args& a,
-                                           long long c) {
-  if (c >= a.C) return;
-#pragma unroll
-  for (int i = 0; i < BN; ++i) {
-    if (i < a.R) {
-      const uint16_t gb = (uint16_t)(g[i >> 1] >> (16 * (i & 1))), ub = (uint16_t)(u[i >> 1] >> (16 * (i & 1)));
-      a.h[i * a.ldo + c] = f2bf(__fmul_rn(bf2f(__ldg(a.silu + gb)), bf2f(ub)));
-      if (a.out0) a.out0[i * a.ldo + c] = gb;
-      if (a.out1) a.out1[i * a.ldo + c] = ub;
-    }
-  }
-}
-
-// Arrival of one CTA on a fold unit's ticket; true for the last of the `need`
-// CTAs that share the unit (which then resets the ticket).  A ticket left by
-// a launch that stopped early carries another epoch and counts as 0.
-__device__ __forceinline__ bool arrive_unit(unsigned long long* t, unsigned epoch, unsigned need) {
-  unsigned long long old = atomicAdd(t, 0ull);
-  for (;;) {
-    const unsigned cnt = ((unsigned)(old >> 32) == epoch) ? (unsigned)old : 0u;
-    const unsigned long long nv = ((unsigned long long)epoch << 32) | (unsigned long long)(cnt + 1);
-    const unsigned long long prev = atomicCAS(t, old, nv);
-    if (prev == old) {
-      if (cnt + 1 < need) return false;
-      atomicExch(t, 0ull);
-      return true;
-    }
-    old = prev;
-  }
-}
-
 // Writes one row (all tokens) of the CTA's next piece: the row's 64 bytes
 // at [row], so that the top kernel reads a quarter row with one 16-byte load.
 __device__ __forceinline__ void emit_piece(uint16_t* slots, int& n, int cap, int row, const uint32_t (&v)[WORDS]) {
@@ -254,159 +186,6 @@ __device__ __forceinline__ void load_w(unsigned char* dst, const CUtensorMap* mW
   }
 }
 
-struct PieceRef {
-  int slot;  // b * cap + j
-  int at;    // level m (bits 0..7), left siblings it merges with (bits 8..15), and whether the
-             // result is the root (bit 16): the fold, the same for every element, worked out once
-};
-static_assert(sizeof(PieceRef) == kPieceRefBytes, "piece list entries: shared-memory sizes assume 8 bytes");
-
-// Lists, in order, the pieces of segment s that CTAs [b_base, min(b_base +
-// 32, b_end)) wrote (P CTAs in all): one lane per CTA, placed by a warp
-// scan.  Returns the count.
-__device__ int list_pieces(const FoldArgs& a, long long s, long long b_base, long long b_end, long long P,
-                           PieceRef* list, int lane) {
-  const int Q = 1 << a.E;
-  const long long ws = s * Q, we = ws + Q;
-  const long long b = b_base + lane;
-  int cnt = 0;
-  long long lo = 0, hi = 0;
-  if (b < b_end) {
-    const long long blo = b * a.W / P, bhi = (b + 1) * a.W / P;
-    lo = blo > ws ? blo : ws;
-    hi = bhi < we ? bhi : we;
-    if (lo < hi) cnt = count_pieces((int)(lo - ws), (int)(hi - ws));
-  }
-  int incl = cnt;
-  for (int d = 1; d < 32; d <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += t;
-  }
-  if (cnt > 0) {
-    int j = slot_base(b, s, a.W, P, Q, a.UG);
-    int pos = incl - cnt;
-    const PieceSplit p = piece_split((int)(lo - ws), (int)(hi - ws));
-    if (p.one) {
-      list[pos].slot = (int)(b * a.cap + j);
-      list[pos].at = fold_code(p.x, hibit((unsigned)(p.y - p.x)), a.E);
-    } else {
-      int at = p.x;
-#pragma unroll 1
-      for (unsigned rem = (unsigned)(p.z - p.x); rem; ++pos, ++j) {  // ascending sizes
-        const unsigned bit = rem & (0u - rem);
-        list[pos].slot = (int)(b * a.cap + j);
-        list[pos].at = fold_code(at, hibit(bit), a.E);
-        at += (int)bit;
-        rem -= bit;
-      }
-#pragma unroll 1
-      for (unsigned rem = (unsigned)(p.y - p.z); rem; ++pos, ++j) {  // descending sizes
-        const unsigned bit = 1u << hibit(rem);
-        list[pos].slot = (int)(b * a.cap + j);
-        list[pos].at = fold_code(at, hibit(bit), a.E);
-        at += (int)bit;
-        rem -= bit;
-      }
-    }
-  }
-  return __shfl_sync(0xffffffffu, incl, 31);
-}
-
-__device__ __forceinline__ uint4 add4(uint4 l, uint4 r) {
-  return make_uint4(add_bf16x2(l.x, r.x), add_bf16x2(l.y, r.y), add_bf16x2(l.z, r.z), add_bf16x2(l.w, r.w));
-}
-
-// Folds segment s's pieces (all CTAs that share it, in order) into this
-// thread's row of the root: 32 tokens as 4 x 16 bytes.  Shared memory (the
-// idle stage area): stack [E][4][BM] and staged pieces [fold_ch][4][BM]
-// (16 bytes each, this thread's row only), then the list.
-__device__ __noinline__ void fold_segment(const FoldArgs& a, long long s, unsigned char* fsm, Bars* bars, int row, int ew,
-                             int lane, uint4 (&root)[4]) {
-  const int Q = 1 << a.E;
-  const long long P = gridDim.x;
-  uint4* stk = reinterpret_cast<uint4*>(fsm);
-  uint4* buf = stk + (size_t)a.E * 4 * BM;
-  PieceRef* list = reinterpret_cast<PieceRef*>(buf + (size_t)a.fold_ch * 4 * BM);
-  const long long b_last = cta_of((s + 1) * Q - 1, a.W, P);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) root[i] = make_uint4(0, 0, 0, 0);
-#pragma unroll 1
-  for (long long b0 = cta_of(s * Q, a.W, P); b0 <= b_last; b0 += 32) {
-    epi_sync();  // the previous batch's list is no longer read
-    if (ew == 0) {
-      const int n = list_pieces(a, s, b0, b_last + 1, P, list, lane);
-      if (lane == 0) bars->fold_n = n;
-    }
-    epi_sync();
-    const int n = bars->fold_n;
-#pragma unroll 1
-    for (int k0 = 0; k0 < n; k0 += a.fold_ch) {
-      const int kend = n < k0 + a.fold_ch ? n : k0 + a.fold_ch;
-#pragma unroll 1
-      for (int k = k0; k < kend; ++k) {
-        const uint16_t* src = a.slots + (size_t)list[k].slot * PIECE + (size_t)row * BN;
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd)
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(buf + ((k - k0) * 4 + qd) * BM + row)),
-                       "l"(src + 8 * qd)
-                       : "memory");
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      asm volatile("cp.async.wait_all;" ::: "memory");
-#pragma unroll 1
-      for (int k = k0; k < kend; ++k) {
-        const int code = list[k].at;
-        const int m = code & 0xFF, kk = (code >> 8) & 0xFF;
-        uint4 cur[4];
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) cur[qd] = buf[((k - k0) * 4 + qd) * BM + row];
-#pragma unroll 1
-        for (int i = 0; i < kk; ++i)
-#pragma unroll
-          for (int qd = 0; qd < 4; ++qd) cur[qd] = add4(stk[((m + i) * 4 + qd) * BM + row], cur[qd]);
-        if (code >> 16) {
-#pragma unroll
-          for (int qd = 0; qd < 4; ++qd) root[qd] = cur[qd];
-        } else {
-#pragma unroll
-          for (int qd = 0; qd < 4; ++qd) stk[((m + kk) * 4 + qd) * BM + row] = cur[qd];
-        }
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void words_of(const uint4 (&r)[4], uint32_t (&v)[WORDS]) {
-#pragma unroll
-  for (int qd = 0; qd < 4; ++qd) {
-    v[4 * qd] = r[qd].x;
-    v[4 * qd + 1] = r[qd].y;
-    v[4 * qd + 2] = r[qd].z;
-    v[4 * qd + 3] = r[qd].w;
-  }
-}
-
-// The last CTA to arrive on fold unit u: folds its segments' pieces and
-// stores the result (the root, or h for gate and up).
-__device__ __noinline__ void fold_unit(const FoldArgs& a, long long u, unsigned char* fsm, Bars* bars, int row, int ew, int lane) {
-  const int spu = a.fused ? 2 : 1;
-  uint4 r0[4];
-  uint32_t v0[WORDS];
-  fold_segment(a, u * spu, fsm, bars, row, ew, lane, r0);
-  words_of(r0, v0);
-  const Seg sg = seg_of(u * spu, a.np, a.ns);
-  const long long c = (long long)sg.t * BM + row;
-  if (!a.fused) {
-    store_words(v0, (sg.pb ? a.out1 : a.out0) + sg.q * a.oss, a.ldo, a.R, c, a.C);
-    return;
-  }
-  uint4 r1[4];
-  uint32_t v1[WORDS];
-  fold_segment(a, u * spu + 1, fsm, bars, row, ew, lane, r1);
-  words_of(r1, v1);
-  store_fused(v0, v1, a, c);
-}
-
 // The streaming kernel.  Each role walks the CTA's groups in the same order:
 // segment (tile, problem) after segment, groups qa..qb-1 of each.
 // 128 registers: registers are granted per 4 warps, so a CTA of 7 warps holds
@@ -427,8 +206,8 @@ __global__ void __maxnreg__(128)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Q = 1 << a.E;
   const bool direct = a.slots == nullptr;
-  const long long w0 = range_lo(blockIdx.x, a.W, gridDim.x, a.UG, direct);
-  const long long w1 = range_lo(blockIdx.x + 1ll, a.W, gridDim.x, a.UG, direct);
+  const long long w0 = range_lo(blockIdx.x, a.W, gridDim.x, Q, direct);
+  const long long w1 = range_lo(blockIdx.x + 1ll, a.W, gridDim.x, Q, direct);
   const long long limit = a.spin > 0 ? a.spin : kDefaultSpin;
   // A wait of an earlier launch ran out (the status word is set until the
   // caller reads it): its outputs, which may be this launch's inputs, are
@@ -544,7 +323,12 @@ __global__ void __maxnreg__(128)
     // ---------------- MMA issuer (converged warp; one lane issues) ----------------
     // Leaf n of this CTA's range uses stage n % NS and TMEM buffer n % kNBuf;
     // one commit per leaf (its "full accumulator" barrier, read by the
-    // epilogue and the producers).
+    // epilogue and the producers).  No stage can fill before the previous
+    // kernel has completed (the token tiles wait for it), so this warp waits
+    // for it too, in the hardware, instead of polling barriers meanwhile:
+    // the previous kernel's last CTAs may share this SM, and the polls would
+    // take their shared-memory and issue bandwidth.
+    grid_dep_wait();
     const uint32_t idesc = idesc_bf16(BM, BN) | (a.w_mn ? kIdescTransA : 0u);
     const uint32_t astep = a.w_mn ? 128u : 2u;  // K = 16 step in descriptor units
     const long long nleaf = (w1 - w0) * GG;
@@ -664,11 +448,13 @@ __global__ void __maxnreg__(128)
         for (int m = 0; m <= kTcsMaxLv; ++m) {
           if (live) {
             if (m == a.E) {  // the whole tile: its root
-              const long long u = s * Q / a.UG;
-              if (direct || (!a.fused && u * a.UG >= w0 && (u + 1) * a.UG <= w1)) {
-                // A one-tree unit inside this range: store its root here.
-                store_words(root, (sg.pb ? a.out1 : a.out0) + sg.q * a.oss, a.ldo, a.R, (long long)sg.t * BM + row,
-                            a.C);
+              if (direct) {
+                const long long c = (long long)sg.t * BM + row;
+                uint16_t* o = (sg.pb ? a.out1 : a.out0) + sg.q * a.oss;
+                if (c < a.C)
+#pragma unroll
+                  for (int i = 0; i < BN; ++i)
+                    if (i < a.R) o[i * a.ldo + c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
               } else {
                 emit_piece(myslots, np_out, a.cap, row, root);
               }
@@ -710,35 +496,6 @@ __global__ void __maxnreg__(128)
         }
       w = s * Q + qb;
     }
-    // The fold units that hold pieces of this range (one-tree units at its
-    // two ends that other CTAs share; every fused unit): arrive on their
-    // tickets; the last CTA to arrive folds the unit's pieces.  (The stages
-    // and stack levels are idle now: every leaf has been consumed.)  Every
-    // epilogue warp gets here exactly once, also after a wait ran out, and
-    // they decide together: a warp that stopped early must not leave the
-    // others waiting at the fold's barriers.
-    const bool all_ok = !epi_any(!ok);
-    if (all_ok && !direct) {
-      const long long ua = w0 / a.UG, ub = (w1 - 1) / a.UG;
-      const long long step = a.fused ? 1 : (ub > ua ? ub - ua : 1);
-      for (long long u = ua; u <= ub; u += step) {
-        if (!a.fused && u * a.UG >= w0 && (u + 1) * a.UG <= w1) continue;  // stored directly
-        __threadfence();  // this thread's pieces are visible before the ticket
-        epi_sync();
-        if (warp == kEpi0 && lane == 0) {
-          const unsigned need =
-              (unsigned)(cta_of((u + 1) * a.UG - 1, a.W, gridDim.x) - cta_of(u * a.UG, a.W, gridDim.x) + 1);
-          bars->fold_last = arrive_unit(a.tick + u, a.epoch, need) ? 1 : 0;
-        }
-        epi_sync();
-        if (bars->fold_last) {
-          __threadfence();
-          const FoldArgs fa{a.R,   a.C,   a.E,     a.np,  a.ns,  a.UG,   a.cap,  a.fold_ch, a.fused,
-                            a.W,   a.oss, a.ldo,   a.slots, a.out0, a.out1, a.h, a.silu};
-          fold_unit(fa, u, smem, bars, row, warp - kEpi0, lane);
-        }
-      }
-    }
   }
 
   tc_fence_before();
@@ -755,16 +512,285 @@ __global__ void __maxnreg__(128)
 namespace detffn {
 namespace {
 
+struct TcsTopArgs {
+  int R, C, E, np, ns;  // ns: K shards per problem (segments as in the streaming kernel)
+  long long oss;        // element offset between consecutive shards' outputs
+  long long W;
+  int P, cap;
+  const uint16_t* slots;
+  uint16_t* out0;   // problem 0 result (gate when fused), or null when fused and not kept
+  uint16_t* out1;   // problem 1 result (up when fused), or null
+  long long ldo;    // row stride of out0, out1 and h (elements)
+  uint16_t* h;      // fused: h = bf16(SiLU(gate)) * up, rounded to BF16; null: plain
+  const uint16_t* silu;
+  const int* status;
+};
+
+struct PieceRef {
+  int slot;  // b * cap + j
+  int at;    // level m (bits 0..7), left siblings it merges with (bits 8..15), and whether the
+             // result is the root (bit 16): the fold, the same for every element, worked out once
+};
+static_assert(sizeof(PieceRef) == kPieceRefBytes, "piece list entries: shared-memory sizes assume 8 bytes");
+
+// Lists, in order, the pieces of segment s that CTAs [b_base, b_base + 32)
+// wrote: one lane per CTA, placed by a warp scan.  Returns the count.
+__device__ int list_pieces(const TcsTopArgs& a, long long s, long long b_base, PieceRef* list, int lane) {
+  const int Q = 1 << a.E;
+  const long long ws = s * Q, we = ws + Q;
+  const long long b = b_base + lane;
+  int cnt = 0;
+  long long lo = 0, hi = 0, blo = 0;
+  if (b < a.P) {
+    blo = b * a.W / a.P;
+    const long long bhi = (b + 1) * a.W / a.P;
+    lo = blo > ws ? blo : ws;
+    hi = bhi < we ? bhi : we;
+    if (lo < hi) cnt = count_pieces((int)(lo - ws), (int)(hi - ws));
+  }
+  int incl = cnt;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += t;
+  }
+  if (cnt > 0) {
+    // Pieces CTA b wrote for its earlier segments: its first (partial) one and whole ones.
+    const long long s0 = blo / Q;
+    int j = 0;
+    if (s0 < s) j = count_pieces((int)(blo - s0 * Q), Q) + (int)(s - s0 - 1);
+    int pos = incl - cnt;
+    const PieceSplit p = piece_split((int)(lo - ws), (int)(hi - ws));
+    if (p.one) {
+      list[pos].slot = (int)(b * a.cap + j);
+      list[pos].at = fold_code(p.x, hibit((unsigned)(p.y - p.x)), a.E);
+    } else {
+      int at = p.x;
+#pragma unroll 1
+      for (unsigned rem = (unsigned)(p.z - p.x); rem; ++pos, ++j) {  // ascending sizes
+        const unsigned bit = rem & (0u - rem);
+        list[pos].slot = (int)(b * a.cap + j);
+        list[pos].at = fold_code(at, hibit(bit), a.E);
+        at += (int)bit;
+        rem -= bit;
+      }
+#pragma unroll 1
+      for (unsigned rem = (unsigned)(p.y - p.z); rem; ++pos, ++j) {  // descending sizes
+        const unsigned bit = 1u << hibit(rem);
+        list[pos].slot = (int)(b * a.cap + j);
+        list[pos].at = fold_code(at, hibit(bit), a.E);
+        at += (int)bit;
+        rem -= bit;
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// Fold state of one segment for this thread's (row, 8 tokens): the pieces,
+// left to right, meet their left siblings on a stack in this thread's column
+// of shared memory.
+struct Fold {
+  uint4* stk;     // level l at stk[l * BM]
+  uint4 root;
+  long long b;    // first CTA of the current list batch
+  int n;          // pieces in the current list batch
+};
+
+__device__ __forceinline__ uint4 add4(uint4 l, uint4 r) {
+  return make_uint4(add_bf16x2(l.x, r.x), add_bf16x2(l.y, r.y), add_bf16x2(l.z, r.z), add_bf16x2(l.w, r.w));
+}
+
+// The first CTA whose range holds a group of segment s.
+__device__ __forceinline__ long long first_cta(const TcsTopArgs& a, long long s) {
+  const long long ws = s * (1ll << a.E);
+  long long b = ws * a.P / a.W;
+  if ((b + 1) * a.W / a.P <= ws) ++b;  // CTA b ends where segment s begins
+  return b;
+}
+__device__ __forceinline__ bool more_ctas(const TcsTopArgs& a, long long s, long long b) {
+  return b < a.P && b * a.W / a.P < (s + 1) * (1ll << a.E);
+}
+
+// Folds one piece (its fold code from the list) into the stack.
+__device__ __forceinline__ void fold_piece(int code, uint4 cur, Fold& f) {
+  const int m = code & 0xFF, k = (code >> 8) & 0xFF;
+#pragma unroll 1
+  for (int i = 0; i < k; ++i) cur = add4(f.stk[(m + i) * BM], cur);
+  if (code >> 16) f.root = cur;
+  else f.stk[(m + k) * BM] = cur;
+}
+
+// Copies (cp.async, 16 bytes per thread: 8 tokens of one row) this
+// thread's part of pieces k0 .. min(k0 + CH, n) - 1 of the list into its
+// column of buf.
+template <int CH>
+__device__ __forceinline__ void stage_pieces(const TcsTopArgs& a, const PieceRef* list, int k0, int n, int row,
+                                             int quad, uint4* buf) {
+  const int kend = n < k0 + CH ? n : k0 + CH;
+#pragma unroll 1
+  for (int k = k0; k < kend; ++k) {
+    const uint16_t* src = a.slots + (size_t)list[k].slot * PIECE + row * BN + quad * kTopTok;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(buf + (k - k0) * BM + row)), "l"(src)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void staged_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <int CH>
+__device__ __forceinline__ void fold_staged(const TcsTopArgs& a, const PieceRef* list, int k0, int n,
+                                            const uint4* buf, Fold& f) {
+  const int kend = n < k0 + CH ? n : k0 + CH;
+#pragma unroll 1
+  for (int k = k0; k < kend; ++k) fold_piece(list[k].at, buf[(k - k0) * BM + threadIdx.x], f);
+}
+
+// Everything of segment s after its first CH pieces (already staged and
+// folded by the caller): the rest of that list, then further list batches.
+template <int CH>
+__device__ void fold_rest(const TcsTopArgs& a, long long s, PieceRef* list, int row, int quad, bool active,
+                          uint4* buf, Fold& f) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int k0 = CH; k0 < f.n; k0 += CH) {
+    if (active) {
+      stage_pieces<CH>(a, list, k0, f.n, row, quad, buf);
+      staged_wait();
+      fold_staged<CH>(a, list, k0, f.n, buf, f);
+    }
+  }
+#pragma unroll 1
+  for (f.b += 32; more_ctas(a, s, f.b); f.b += 32) {
+    __syncthreads();  // the previous batch's list is no longer read
+    if (warp == 0) {
+      const int n = list_pieces(a, s, f.b, list, lane);
+      if (lane == 0) list[32 * a.cap].slot = n;
+    }
+    __syncthreads();
+    f.n = list[32 * a.cap].slot;
+#pragma unroll 1
+    for (int k0 = 0; k0 < f.n; k0 += CH) {
+      if (active) {
+        stage_pieces<CH>(a, list, k0, f.n, row, quad, buf);
+        staged_wait();
+        fold_staged<CH>(a, list, k0, f.n, buf, f);
+      }
+    }
+  }
+}
+
+// Writes a [kTopTok tokens][128 rows] tile held in shared memory to
+// out[r * ldo + c] for r in [r0, min(r0 + kTopTok, R)), c in [c0, min(c0 + 128, C)).
+__device__ __forceinline__ void store_tile(const uint16_t* tile, uint16_t* out, long long ldo, int R, int r0,
+                                           long long c0, long long C) {
+  static_assert(kTopTok * BM == 8 * kTopThreads, "one 16-byte store per thread");
+  const int tok = threadIdx.x >> 4, c8 = (threadIdx.x & 15) * 8;
+  if (r0 + tok >= R) return;
+  const long long c = c0 + c8;
+  uint16_t* o = out + (r0 + tok) * ldo + c;
+  const uint16_t* src = tile + tok * (BM + 8) + c8;
+  if (c + 8 <= C && ((uintptr_t)o & 15u) == 0) {
+    *reinterpret_cast<uint4*>(o) = *reinterpret_cast<const uint4*>(src);
+  } else {
+    for (int i = 0; i < 8; ++i)
+      if (c + i < C) o[i] = src[i];
+  }
+}
+
+// Token t of this thread's 8 (word t / 2 of v, low half first) to tile[t][row].
+__device__ __forceinline__ void put_tile(uint16_t* tile, int row, uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    tile[(2 * i) * (BM + 8) + row] = (uint16_t)(w[i] & 0xFFFFu);
+    tile[(2 * i + 1) * (BM + 8) + row] = (uint16_t)(w[i] >> 16);
+  }
+}
+
+// Plain (FUSED false): CTA (s, y) folds segment s for tokens
+// kTopTok * y .. kTopTok * y + kTopTok - 1.  Fused (np == 2): CTA (t, y) folds
+// gate (segment 2t) and up (segment 2t+1) and forms h = bf16(SiLU(gate)) * up,
+// rounded to BF16.  Each thread owns one row and 8 tokens (a 16-byte quarter
+// of a piece row); the pieces are staged in shared memory (up to CH per
+// segment in flight) and folded from there.  Launched as a programmatic
+// dependent of the streaming kernel: the piece lists (arithmetic only) are
+// built before waiting for its results.
+template <bool FUSED>
+__global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
+  constexpr int NSEG = FUSED ? 2 : 1;
+  constexpr int CH = top_chunk(FUSED);
+  extern __shared__ __align__(16) unsigned char top_sm[];
+  uint4* bufs = reinterpret_cast<uint4*>(top_sm);        // NSEG x [CH][BM]
+  uint4* stacks = bufs + NSEG * CH * BM;                  // NSEG x [E][BM]
+  uint16_t* tiles = reinterpret_cast<uint16_t*>(stacks + NSEG * a.E * BM);  // 3 x [kTopTok][BM + 8]
+  PieceRef* lists = reinterpret_cast<PieceRef*>(tiles + 3 * kTopTok * (BM + 8));
+  const int row = threadIdx.x, quad = blockIdx.y;
+  const bool active = kTopTok * quad < a.R;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long s0 = FUSED ? 2ll * blockIdx.x : (long long)blockIdx.x;
+  const int stride = 32 * a.cap + 1;  // list entries per segment (the last holds the count)
+  Fold f[NSEG];
+  if (warp < NSEG) {
+    PieceRef* list = lists + warp * stride;
+    const int n = list_pieces(a, s0 + warp, first_cta(a, s0 + warp), list, lane);
+    if (lane == 0) list[32 * a.cap].slot = n;
+  }
+  grid_dep_launch();
+  __syncthreads();
+  grid_dep_wait();  // the streaming kernel's pieces are complete and visible
+  // A bounded wait of the streaming kernel (or of an earlier launch) ran out:
+  // the pieces are unfinished, so nothing is folded or stored.
+  if (__syncthreads_or(a.status != nullptr && *(volatile int*)a.status != 0)) return;
+#pragma unroll
+  for (int g = 0; g < NSEG; ++g) {
+    f[g].b = first_cta(a, s0 + g);
+    f[g].n = lists[g * stride + 32 * a.cap].slot;
+    f[g].root = make_uint4(0, 0, 0, 0);
+    f[g].stk = stacks + (g * a.E) * BM + row;
+    if (active) stage_pieces<CH>(a, lists + g * stride, 0, f[g].n, row, quad, bufs + g * CH * BM);
+  }
+  staged_wait();
+#pragma unroll
+  for (int g = 0; g < NSEG; ++g) {
+    if (active) fold_staged<CH>(a, lists + g * stride, 0, f[g].n, bufs + g * CH * BM, f[g]);
+    fold_rest<CH>(a, s0 + g, lists + g * stride, row, quad, active, bufs + g * CH * BM, f[g]);
+  }
+  const int r0 = kTopTok * quad;
+  if constexpr (!FUSED) {
+    const Seg sg = seg_of(s0, a.np, a.ns);
+    put_tile(tiles, row, f[0].root);
+    __syncthreads();
+    store_tile(tiles, (sg.pb ? a.out1 : a.out0) + sg.q * a.oss, a.ldo, a.R, r0, (long long)sg.t * BM, a.C);
+  } else {
+    const int t = blockIdx.x;
+    const uint32_t gw[4] = {f[0].root.x, f[0].root.y, f[0].root.z, f[0].root.w};
+    const uint32_t uw[4] = {f[1].root.x, f[1].root.y, f[1].root.z, f[1].root.w};
+    uint32_t hw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float h0 = __fmul_rn(bf2f(__ldg(a.silu + (gw[i] & 0xFFFFu))), __uint_as_float(uw[i] << 16));
+      const float h1 = __fmul_rn(bf2f(__ldg(a.silu + (gw[i] >> 16))), __uint_as_float(uw[i] & 0xFFFF0000u));
+      hw[i] = (uint32_t)f2bf(h0) | ((uint32_t)f2bf(h1) << 16);
+    }
+    constexpr int TILE = kTopTok * (BM + 8);
+    put_tile(tiles, row, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    if (a.out0) put_tile(tiles + TILE, row, f[0].root);
+    if (a.out1) put_tile(tiles + 2 * TILE, row, f[1].root);
+    __syncthreads();
+    store_tile(tiles, a.h, a.ldo, a.R, r0, (long long)t * BM, a.C);
+    if (a.out0) store_tile(tiles + TILE, a.out0, a.ldo, a.R, r0, (long long)t * BM, a.C);
+    if (a.out1) store_tile(tiles + 2 * TILE, a.out1, a.ldo, a.R, r0, (long long)t * BM, a.C);
+  }
+}
+
 }  // namespace
 }  // namespace detffn
 
 namespace detffn {
 
-bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* p, int ns,
-              bool fused) {
+bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* p, int ns) {
   if (R < 1 || R > BN || C < 1 || K < 1 || np < 1 || np > 2 || max_ctas < 1) return false;
   if (ns < 1 || ns > kTcsMaxShards || (ns > 1 && K % BK != 0)) return false;
-  if (fused && (np != 2 || ns != 1)) return false;
   const long long L = (K + BK - 1) / BK;
   int G;
   long long q;
@@ -791,40 +817,36 @@ bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool 
   r.E = E;
   r.np = np;
   r.ns = ns;
-  r.fused = fused;
   r.T = (int)((C + BM - 1) / BM);
   const int Q = 1 << E;
-  r.UG = fused ? 2 * Q : Q;
   r.W = (long long)np * ns * r.T * Q;
   r.direct = direct;
-  const long long units = r.W / r.UG;
-  r.P = (int)(max_ctas < (direct ? units : r.W) ? max_ctas : (direct ? units : r.W));
+  const long long units = direct ? (long long)np * ns * r.T : r.W;
+  r.P = (int)(max_ctas < units ? max_ctas : units);
   r.nstage = stages_for(E);
   if (r.nstage < 2) return false;
   if (direct) {
     *p = r;
     return true;
   }
-  // Piece slots per CTA: the most pieces any CTA writes (only the fold units
-  // at the two ends of its range can be shared with other CTAs).
+  // Piece slots per CTA: the most pieces any CTA's range produces.
   int cap = 1;
   for (long long b = 0; b < r.P; ++b) {
-    const long long bhi = (b + 1) * r.W / r.P;
-    const int n = slot_base(b, (bhi - 1) / Q + 1, r.W, r.P, Q, r.UG);
+    const long long w0 = b * r.W / r.P, w1 = (b + 1) * r.W / r.P;
+    int n = 0;
+    for (long long w = w0; w < w1;) {
+      const long long s = w / Q;
+      const int qa = (int)(w - s * Q), qb = (int)((w1 - s * Q) < Q ? (w1 - s * Q) : Q);
+      n += count_pieces(qa, qb);
+      w = s * Q + qb;
+    }
     if (n > cap) cap = n;
   }
   r.cap = cap;
-  // The tile fold reuses the stages and stack levels: the fold stack (E
-  // levels), at least one staged piece and a list of up to 32 CTAs' pieces.
-  const int lv = E > REG_LV ? E - REG_LV : 0;
-  const long long avail = (long long)r.nstage * STAGE + (long long)lv * LV_BYTES;
-  const long long list_bytes = (32ll * cap) * kPieceRefBytes;
-  const long long ch = (avail - (long long)E * kFoldRowBytes - list_bytes) / kFoldRowBytes;
-  if (ch < 1) return false;
-  r.fold_ch = (int)(ch < kMaxFoldChunk ? ch : kMaxFoldChunk);
-  const size_t slots = (size_t)r.P * cap * PIECE * 2;
-  r.tick_off = (slots + 255) & ~(size_t)255;
-  r.scratch = r.tick_off + (size_t)units * sizeof(unsigned long long);
+  // Top kernel: staged pieces, output tiles, piece lists (the larger of its two modes).
+  r.top_smem = top_smem(false, E, cap) > top_smem(true, E, cap) ? top_smem(false, E, cap) : top_smem(true, E, cap);
+  if (r.top_smem > 200 * 1024) return false;
+  r.scratch = (size_t)r.P * cap * PIECE * 2;
   *p = r;
   return true;
 }
@@ -854,10 +876,10 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
                        void* scratch, size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump,
                        long long oss) {
   if (plan.ns > 1 && (h || dump)) return cudaErrorInvalidValue;
-  if ((h != nullptr) != plan.fused || (h && !silu) || (plan.fused && plan.direct)) return cudaErrorInvalidValue;
   const long long Ktot = plan.K * plan.ns;  // the maps span every shard's K range
-  if (!plan.direct && (!scratch || scratch_bytes < plan.scratch || ((uintptr_t)scratch & 255u)))
+  if (!plan.direct && (!scratch || scratch_bytes < plan.scratch || ((uintptr_t)scratch & 15u)))
     return cudaErrorInvalidValue;
+  if (plan.direct && h) return cudaErrorInvalidValue;
   for (int p = 0; p < plan.np; ++p)
     if ((pr[p].ldw % 8) || (pr[p].ldx % 8) || ((uintptr_t)pr[p].W & 15u) || ((uintptr_t)pr[p].X & 15u) ||
         pr[p].w_mn != pr[0].w_mn)
@@ -883,6 +905,12 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     }
+    void (*tops[2])(TcsTopArgs) = {k_tcs_top<false>, k_tcs_top<true>};
+    for (auto k : tops) {
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    }
     setup_err = e;
   });
   if (setup_err != cudaSuccess) return setup_err;
@@ -901,19 +929,6 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   a.nstage = plan.nstage;
   a.w_mn = pr[0].w_mn ? 1 : 0;
   a.slots = plan.direct ? nullptr : static_cast<uint16_t*>(scratch);
-  a.tick = plan.direct ? nullptr
-                       : reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(scratch) + plan.tick_off);
-  // Launch epochs: consecutive per process from a start that varies between
-  // processes; 0 is never used (a zeroed ticket is always read as empty).
-  static std::atomic<unsigned> epochs{(unsigned)std::chrono::steady_clock::now().time_since_epoch().count() | 1u};
-  unsigned ep = epochs.fetch_add(1u);
-  if (ep == 0) ep = epochs.fetch_add(1u);
-  a.epoch = ep;
-  a.fused = plan.fused ? 1 : 0;
-  a.UG = plan.UG;
-  a.fold_ch = plan.fold_ch;
-  a.h = h;
-  a.silu = silu;
   a.out0 = pr[0].out;
   a.out1 = plan.np > 1 ? pr[1].out : nullptr;
   a.ldo = ldo;
@@ -926,7 +941,29 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) =
       dump ? (plan.G == 1 ? k_tcs<1, true> : plan.G == 2 ? k_tcs<2, true> : k_tcs<3, true>)
            : (plan.G == 1 ? k_tcs<1, false> : plan.G == 2 ? k_tcs<2, false> : k_tcs<3, false>);
-  return launch_dependent(kern, dim3(plan.P), kThreads, smem, st, m[0], m[1], m[2], m[3], a);
+  cudaError_t e = launch_dependent(kern, dim3(plan.P), kThreads, smem, st, m[0], m[1], m[2], m[3], a);
+  if (e != cudaSuccess || plan.direct) return e;
+  TcsTopArgs t{};
+  t.R = plan.R;
+  t.C = (int)plan.C;
+  t.E = plan.E;
+  t.np = plan.np;
+  t.ns = plan.ns;
+  t.oss = oss;
+  t.W = plan.W;
+  t.P = plan.P;
+  t.cap = plan.cap;
+  t.slots = static_cast<const uint16_t*>(scratch);
+  t.out0 = pr[0].out;
+  t.out1 = plan.np > 1 ? pr[1].out : nullptr;
+  t.ldo = ldo;
+  t.h = h;
+  t.silu = silu;
+  t.status = wt.status;
+  const dim3 grid(h ? plan.T : plan.np * plan.ns * plan.T, (plan.R + kTopTok - 1) / kTopTok);
+  const int smem_top = top_smem(h != nullptr, plan.E, plan.cap);
+  return h ? launch_dependent(k_tcs_top<true>, grid, kTopThreads, smem_top, st, t)
+           : launch_dependent(k_tcs_top<false>, grid, kTopThreads, smem_top, st, t);
 }
 
 }  // namespace

@@ -55,12 +55,10 @@ constexpr int kTcsMaxLv = 8;      // at most 2^8 bottom groups (K <= 3 * 256 * 6
 constexpr int kTcsMaxShards = 8;  // K shards per problem in one launch
 
 struct TcsPlan {
-  int R = 0, G = 0, E = 0, T = 0, np = 0, ns = 1, P = 0, cap = 0, nstage = 0, UG = 0, fold_ch = 0;
+  int R = 0, G = 0, E = 0, T = 0, np = 0, ns = 1, P = 0, cap = 0, nstage = 0, top_smem = 0;
   long long C = 0, K = 0, W = 0;    // K: the contraction length of one shard
-  bool direct = false;  // whole fold units per CTA, results stored directly (no scratch)
-  bool fused = false;   // gate and up with SiLU * up (a fold unit is a tile's gate and up trees)
-  size_t tick_off = 0;  // byte offset of the fold units' tickets in the scratch
-  size_t scratch = 0;   // bytes of piece slots and tickets the launch needs
+  bool direct = false;  // whole tiles per CTA, roots stored directly (no scratch, no top kernel)
+  size_t scratch = 0;   // bytes of piece slots the launch needs
 };
 
 // Plans a launch on at most max_ctas CTAs (two per SM is the design point).
@@ -71,7 +69,7 @@ struct TcsPlan {
 // (K a multiple of 64): shard q reads K positions [q K, (q+1) K) of the
 // operands and writes its own output (out + q * oss), one tree each.
 bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* plan,
-              int ns = 1, bool fused = false);
+              int ns = 1);
 
 struct TcsProblem {
   const uint16_t* W;  // [C, K] weights, row stride ldw (multiple of 8), 16-byte aligned;
@@ -82,15 +80,15 @@ struct TcsProblem {
   bool w_mn = false;  // weights read MN-major (no transposed copy needed)
 };
 
-// One or two same-shaped contractions (plan.np), one launch on `st`.
+// One or two same-shaped contractions (plan.np): two launches on `st`, or one
+// in direct mode (scratch unused).
 cudaError_t launch_tcs(const TcsPlan& plan, const TcsProblem* problems, long long ldo, void* scratch,
                        size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump = nullptr,
                        long long oss = 0);
 
 // Gate (problems[0]) and up (problems[1]) with the SiLU * up stage boundary
 // fused into the top of the trees: h[r * ldo + c] = bf16(bf16(SiLU(gate)) * up);
-// gate and up are stored only where problems[p].out is non-null.  The plan
-// must have been made with fused = true.
+// gate and up are stored only where problems[p].out is non-null.
 cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* problems, uint16_t* h, long long ldo,
                               const uint16_t* silu, void* scratch, size_t scratch_bytes, const Waits& wt,
                               cudaStream_t st);

@@ -823,6 +823,15 @@ bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool 
   r.direct = direct;
   const long long units = direct ? (long long)np * ns * r.T : r.W;
   r.P = (int)(max_ctas < units ? max_ctas : units);
+  if (!direct) {
+    // Equal, aligned ranges: the smallest power of two B of groups per CTA
+    // with W / B <= max_ctas.  When B divides a tile's 2^E groups, every
+    // range is one aligned block -- one piece, a node of the canonical tree
+    // -- so a tile's fold takes 2^E / B pieces (or its root, for B = 2^E).
+    long long B = 1;
+    while (r.W / B > max_ctas) B <<= 1;
+    if (B <= Q) r.P = (int)(r.W / B);
+  }
   r.nstage = stages_for(E);
   if (r.nstage < 2) return false;
   if (direct) {

@@ -275,6 +275,19 @@ def large_training(G, args, ws_n, timed):
     trn_ms = max_over_ranks(ws_n, timed(train, steps, 3))
     ref = [dWg.clone(), dWu.clone(), dWd.clone()]
     res = {}
+    # Backward with the I axis in k = 2 shards, one stream and two-stream
+    # dHidden (the gate contribution's rank tree beside the up shards).
+    dX1 = dX.clone()
+    wsk = G.workspace(G.OP_BACKWARD, M, H, I, 2)
+    dXk = e(M, H)
+    for name, fl in (("", 0), ("_overlap", G.FLAG_OVERLAP_DHIDDEN)):
+        def bwd_k(i, fl=fl):
+            G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], g, u, t["dOut"], dX=dXk, dWg=dWg, dWu=dWu,
+                              dWd=dWd, ws=wsk, shards=2, flags=fl)
+        res["bwd_ms_M4096_k2" + name] = max_over_ranks(ws_n, timed(bwd_k, steps, 3))
+        torch.cuda.synchronize()
+        res["dX_mismatches_M4096_k2" + name] = bits_mismatch(dXk, dX1)
+    del wsk, dXk, dX1
     for c in (2, 4):
         sl = [slice(j * M // c, (j + 1) * M // c) for j in range(c)]
         xs, gs, us, ds = ([v[q] for q in sl] for v in (t["x"], g, u, t["dOut"]))
@@ -465,7 +478,7 @@ def run_ours(args):
         wsf = G.workspace(G.OP_FORWARD_SHARDED if k > 1 else G.OP_FORWARD, M_DEC, H, I, k, path)
         wsb = G.workspace(G.OP_BACKWARD, M_DEC, H, I, k, path)
 
-        def train_step(i, k=k, gs=gs, us_=us_, outk=outk, dXk=dXk, grads=grads, wsf=wsf, wsb=wsb):
+        def train_step(i, k=k, gs=gs, us_=us_, outk=outk, dXk=dXk, grads=grads, wsf=wsf, wsb=wsb, flags=0):
             t = copies[i & 1]
             if k == 1:
                 G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], out=outk, gate_save=gs, up_save=us_, ws=wsf,
@@ -474,9 +487,19 @@ def run_ours(args):
                 G.detffn_forward_sharded(t["x"], t["Wg"], t["Wu"], t["Wd"], k, out=outk, gate_save=gs,
                                          up_save=us_, ws=wsf, path=path)
             G.detffn_backward(t["x"], t["Wg"], t["Wu"], t["Wd"], gs, us_, t["dOut"], dX=dXk, dWg=grads[0],
-                              dWu=grads[1], dWd=grads[2], ws=wsb, shards=k, path=path)
+                              dWu=grads[1], dWd=grads[2], ws=wsb, shards=k, path=path, flags=flags)
 
         key = "fwd_bwd_us_M32" + ("" if k == 1 else "_k%d" % k)
+        if k > 1:
+            # The same step with the gate contribution's rank tree on a second
+            # stream (two-stream dHidden); its results are compared below too.
+            ov = lambda i, ts=train_step: ts(i, flags=G.FLAG_OVERLAP_DHIDDEN)  # noqa: E731
+            extra[key + "_overlap"] = 1e3 * max_over_ranks(ws_n, timed(ov, tsteps, 3))
+            ov(0)
+            torch.cuda.synchronize()
+            extra["overlap_mismatches_M32_k%d" % k] = {
+                n: bits_mismatch(a, b) for n, a, b in zip(["out", "dX", "dWg", "dWu", "dWd"], [outk, dXk] + grads,
+                                                          base)}
         extra[key] = 1e3 * max_over_ranks(ws_n, timed(train_step, tsteps, 3))
         train_step(0)   # copy 0 last, for the comparison
         torch.cuda.synchronize()

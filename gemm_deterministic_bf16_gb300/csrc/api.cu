@@ -25,6 +25,11 @@ struct detffn_handle_s {
   float* d_dsilu = nullptr;     // [65536] FP32 SiLU' by gate bit pattern
   int* d_status = nullptr;      // device status word (bounded waits)
   Waits wt;                     // the current call's wait settings (status word, poll limit, test stall)
+  int flags = 0;                // the current call's option flags
+  // A second stream and two events (made at creation) for the overlapped
+  // dHidden reduction (DETFFN_FLAG_OVERLAP_DHIDDEN).
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   std::vector<uint16_t> h_silu;
   std::vector<float> h_dsilu;
   // Measurement: event pairs around launches while profiling is on.
@@ -169,7 +174,7 @@ detffn_status read_opts(const detffn_options* o, Opts* out) {
     if (!(o->shards == 0 || o->shards == 1 || o->shards == 2 || o->shards == 4 || o->shards == 8))
       return DETFFN_ERR_INVALID_ARG;
     if (o->spin_limit < 0) return DETFFN_ERR_INVALID_ARG;
-    if (o->flags & ~DETFFN_FLAG_TEST_STALL) return DETFFN_ERR_INVALID_ARG;
+    if (o->flags & ~(DETFFN_FLAG_TEST_STALL | DETFFN_FLAG_OVERLAP_DHIDDEN)) return DETFFN_ERR_INVALID_ARG;
     r.path = o->path;
     r.shards = o->shards ? o->shards : 1;
     r.flags = o->flags;
@@ -184,6 +189,7 @@ void set_waits(detffn_handle h, const Opts& o) {
   h->wt.status = h->d_status;
   h->wt.spin = o.spin_limit;
   h->wt.stall = (o.flags & DETFFN_FLAG_TEST_STALL) ? 1 : 0;
+  h->flags = o.flags;
 }
 
 // The kernel family a call uses.  EXACT: CUDA-core kernels with LANE8x8
@@ -673,6 +679,9 @@ detffn_status detffn_create(detffn_handle* out, int device) {
     if (cudaMalloc(&h->d_silu, 65536 * sizeof(uint16_t)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaMalloc(&h->d_dsilu, 65536 * sizeof(float)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+    if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaMemcpy(h->d_silu, h->h_silu.data(), 65536 * sizeof(uint16_t), cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemcpy(h->d_dsilu, h->h_dsilu.data(), 65536 * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
@@ -694,6 +703,9 @@ detffn_status detffn_destroy(detffn_handle h) {
   if (h->d_silu) cudaFree(h->d_silu);
   if (h->d_dsilu) cudaFree(h->d_dsilu);
   if (h->d_status) cudaFree(h->d_status);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->side) cudaStreamDestroy(h->side);
   for (auto& r : h->recs) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -981,13 +993,38 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   if (k == 1) {
     TRY(tree_gemm2(h, f, Strided{dG, I, 1}, wcol(WG, 0), w.cg, Strided{dU, I, 1}, wcol(WU, 0), w.cu, M, H, I, H,
                    st, w.tcs));
+  } else if (h->flags & DETFFN_FLAG_OVERLAP_DHIDDEN) {
+    // Two streams (PR #325, "Communication overlap assessment"): the gate
+    // contribution's shard roots, then their rank tree on the handle's second
+    // stream while the up contribution's shards are computed here; the final
+    // gate-then-up addition waits for both.  Same kernels, same trees, same
+    // order of every addition: the same bits as one stream.
+    const void *pg[8], *pu[8];
+    for (int s = 0; s < k; ++s) {
+      pg[s] = w.cgs + (long long)s * M * H;
+      pu[s] = w.cus + (long long)s * M * H;
+    }
+    TRY(tree_gemm_k(h, f, Strided{dG, I, 1}, wcol(WG, 0), M, H, sw, k, w.cgs, H, M * H, st, w.tcs));
+    TRYCU(cudaEventRecord(h->ev_fork, st));
+    TRYCU(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+    // Once forked, the side stream is joined back whatever fails in between,
+    // so that nothing of this call is left running behind `stream`.
+    detffn_status side_st = rank_tree_bf16(h, pg, k, w.cg, M * H, h->side);
+    const detffn_status rec = cu(cudaEventRecord(h->ev_join, h->side));
+    detffn_status main_st = tree_gemm_k(h, f, Strided{dU, I, 1}, wcol(WU, 0), M, H, sw, k, w.cus, H, M * H, st, w.tcs);
+    if (main_st == DETFFN_OK) main_st = rank_tree_bf16(h, pu, k, w.cu, M * H, st);
+    if (rec == DETFFN_OK) TRYCU(cudaStreamWaitEvent(st, h->ev_join, 0));
+    else TRYCU(cudaStreamSynchronize(h->side));
+    TRY(side_st);
+    TRY(rec);
+    TRY(main_st);
   } else {
     // Shard s contracts K positions [s sw, (s+1) sw) of I; all shards' cg and
     // cu subtree roots in one call.
     TRY(tree_gemm2_k(h, f, Strided{dG, I, 1}, wcol(WG, 0), w.cgs, Strided{dU, I, 1}, wcol(WU, 0), w.cus, M, H, sw,
                      k, H, M * H, st, w.tcs));
   }
-  if (k > 1) {
+  if (k > 1 && !(h->flags & DETFFN_FLAG_OVERLAP_DHIDDEN)) {
     const void *pg[8], *pu[8];
     for (int s = 0; s < k; ++s) {
       pg[s] = w.cgs + (long long)s * M * H;

@@ -38,6 +38,7 @@ class DetFFNError(RuntimeError):
 
 
 FLAG_TEST_STALL = 1
+FLAG_OVERLAP_DHIDDEN = 2
 
 
 class Options(ctypes.Structure):

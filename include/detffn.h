@@ -81,13 +81,19 @@ typedef enum { DETFFN_PATH_AUTO = 0, DETFFN_PATH_EXACT = 1, DETFFN_PATH_TENSOR =
  * CTAs stop with nothing in flight and the call's outputs are left
  * unfinished; detffn_get_status then returns DETFFN_ERR_TIMEOUT.  The fault
  * is made by withholding work, never by a bad address or a trap. */
-enum { DETFFN_FLAG_TEST_STALL = 1 };
+enum { DETFFN_FLAG_TEST_STALL = 1, DETFFN_FLAG_OVERLAP_DHIDDEN = 2 };
+/* DETFFN_FLAG_OVERLAP_DHIDDEN (detffn_backward with options->shards = k > 1;
+ * PR #325, "Communication overlap assessment"): the rank tree of the gate
+ * contribution's shard roots runs on a second stream of the handle while the
+ * up contribution's shards are computed on `stream`; the gate-then-up
+ * addition waits for both.  The bits are those of the one-stream call.
+ * Without shards it changes nothing. */
 
 typedef struct {
     int leaf_width;        /* 64; anything else returns DETFFN_ERR_UNSUPPORTED */
     int path;              /* detffn_path */
     int shards;            /* detffn_backward only: k in {1,2,4,8} TP shards of I for dHidden */
-    int flags;             /* 0, or DETFFN_FLAG_TEST_STALL (tests only); other bits: DETFFN_ERR_INVALID_ARG */
+    int flags;             /* DETFFN_FLAG_* bits (0: none); other bits: DETFFN_ERR_INVALID_ARG */
     long long spin_limit;  /* polls before a role's bounded in-kernel wait gives up; 0 = default
                               (2^26).  Waits that drain a CTA's own copies and tensor-core work
                               before it exits always use the default. */

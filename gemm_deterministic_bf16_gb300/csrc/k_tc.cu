@@ -47,13 +47,26 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kMaxAccBufs = 16;  // TMEM leaf buffers: 512 columns / BN (at most 16)
-constexpr int kEpiWarp0 = 4;  // warp 0: producer, warps 1-3: MMA, warps 4..11: epilogue
-// MMA-issuing warps 1 .. kIssuers.  Issuer q takes leaves q, q + kIssuers,
-// ...: each leaf costs its issuing thread a commit and two barrier waits of
-// a few hundred cycles of latency, more than the 4 MMAs of a 128 x 128 leaf
-// keep the tensor pipe busy, so one issuer alone leaves the pipe idle
-// between leaves.
-constexpr int kIssuers = kEpiWarp0 - 1;
+constexpr int kEpiWarp0 = 4;  // warps 0-3: TMA producers and MMA issuers, warps 4..11: epilogue
+// Roles of warps 0-3.  Each leaf costs the threads that load it and issue
+// its MMAs a few dependent barrier operations of a hundred-odd cycles of
+// latency each, more than the 4 MMAs of a 128 x 128 leaf keep the tensor
+// pipe busy, so the work is spread over several warps.  Every barrier is
+// waited on by parity, which is only sound while no waiter can fall two
+// phases behind; the two layouts below keep that true by construction:
+//   paired (bottom groups of two leaves): leaves 4k, 4k+1 go to issuer 0
+//     (warp 1) and leaves 4k+2, 4k+3 to issuer 1 (warp 2), one group at a
+//     time, so that each TMEM buffer -- and with four stages each stage --
+//     has one issuer; with an even number of stages the loads are split by
+//     leaf parity between warp 0 and warp 3, each owning its stages (with
+//     an odd number, warp 0 loads every leaf and warp 3 idles);
+//   single (groups of one or three leaves): warp 0 loads every leaf, and
+//   issuer q (warp 1 + q) takes leaves q, q + 3, ...
+template <int GG> struct Roles {
+  static constexpr bool PAIRED = GG == 2;
+  static constexpr int ISSUERS = PAIRED ? 2 : 3;
+  static constexpr int UNIT = PAIRED ? 2 : 1;  // consecutive leaves an issuer takes at a time
+};
 // Registers per thread: at launch (384 threads), and after the split between
 // warpgroup 0 (producer and issuers) and the epilogue's two warpgroups.  The
 // split hands over exactly what the launch holds; the host refuses to launch
@@ -175,6 +188,113 @@ __device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int 
   return stk + (((m - T::REG_LV) * T::HALVES + half) * T::WORDS + w) * BM + row;
 }
 
+// The epilogue's view of one CTA's pipeline.
+struct EpiCtx {
+  uint32_t tmem, lane_addr;
+  int col0, lane;
+  Bars* bars;
+  long long limit;
+  volatile int* abort_flag;
+  uint32_t lc;  // leaves consumed (NBUF is a power of two)
+  bool ok;
+};
+
+// Bottom group qg of tile (pb, tm, tn), whose leaves are the next GG in
+// TMEM: wait for the commits of its leaves (of the second alone in the
+// paired layout, where one issuer committed both), read them in column
+// chunks, hand this thread's group root words to emit(w, word) as they are
+// formed, and return the buffers to the MMA issuers.  False when a wait ran
+// out.
+template <int BN, int GG, bool DUMP, class Emit>
+__device__ __forceinline__ bool group_root(EpiCtx& e, const TcArgs& a, Emit&& emit, int pb, long long r, int tn,
+                                         int qg) {
+  using T = TcGeo<BN>;
+  if constexpr (GG == 2) {  // one issuer committed both leaves, the second last
+    const uint32_t last = e.lc + 1;
+    if (!wait_or_abort(&e.bars->accf[last % T::NBUF], (last / T::NBUF) & 1u, e.limit, e.abort_flag, a.status))
+      e.ok = false;
+  } else {
+    for (int g = 0; g < GG; ++g)
+      if (!wait_or_abort(&e.bars->accf[(e.lc + g) % T::NBUF], ((e.lc + g) / T::NBUF) & 1u, e.limit, e.abort_flag,
+                         a.status))
+        e.ok = false;
+  }
+  if (__any_sync(0xffffffffu, !e.ok)) {
+    e.ok = false;
+    return false;
+  }
+  tc_fence_after();
+  const uint32_t b0 = (uint32_t)((e.lc % T::NBUF) * BN), b1 = (uint32_t)(((e.lc + 1) % T::NBUF) * BN),
+                 b2 = (uint32_t)(((e.lc + 2) % T::NBUF) * BN);
+  constexpr int CW = GG >= 3 ? 16 : 32;  // columns per chunk (registers: GG x CW)
+  constexpr int WC = CW / 2;             // packed words per chunk
+  if constexpr (GG == 1) {
+    // A lone leaf (one-leaf trees: weight gradients over few tokens):
+    // all columns read with one wait, each rounded once.
+    static_assert(T::COLS % 32 == 0, "columns per thread");
+#pragma unroll
+    for (int c = 0; c < T::COLS / 32; c += 2) {
+      uint32_t va[32], vb[32];
+      tmem_ld32(e.tmem + e.lane_addr + b0 + (uint32_t)(e.col0 + 32 * c), va);
+      if (c + 1 < T::COLS / 32) tmem_ld32(e.tmem + e.lane_addr + b0 + (uint32_t)(e.col0 + 32 * c + 32), vb);
+      tmem_wait_ld();
+      if constexpr (DUMP) {
+        float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
+        const long long cc = (long long)tn * BN + e.col0 + 32 * c;
+        dump_leaves(d, r, cc, a.R, a.C, a.L, qg, va);
+        if (c + 1 < T::COLS / 32) dump_leaves(d, r, cc + 32, a.R, a.C, a.L, qg, vb);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) emit(16 * c + i, pack_bf16x2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1])));
+      if (c + 1 < T::COLS / 32)
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          emit(16 * c + 16 + i, pack_bf16x2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1])));
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < T::COLS / CW; ++c) {
+      uint32_t v0[CW], v1[CW], v2[GG >= 3 ? CW : 1];
+      const uint32_t col = (uint32_t)(e.col0 + CW * c);
+      if constexpr (GG >= 3) {
+        tmem_ld16(e.tmem + e.lane_addr + b0 + col, v0);
+        tmem_ld16(e.tmem + e.lane_addr + b1 + col, v1);
+        tmem_ld16(e.tmem + e.lane_addr + b2 + col, v2);
+      } else {
+        tmem_ld32(e.tmem + e.lane_addr + b0 + col, v0);
+        tmem_ld32(e.tmem + e.lane_addr + b1 + col, v1);
+      }
+      tmem_wait_ld();
+      if constexpr (DUMP) {
+        float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
+        const long long cc = (long long)tn * BN + col;
+        dump_leaves(d, r, cc, a.R, a.C, a.L, qg * GG, v0);
+        dump_leaves(d, r, cc, a.R, a.C, a.L, qg * GG + 1, v1);
+        if constexpr (GG >= 3) dump_leaves(d, r, cc, a.R, a.C, a.L, qg * GG + 2, v2);
+      }
+#pragma unroll
+      for (int i = 0; i < WC; ++i) {
+        // Pairs of adjacent columns, added two at a time (add.rn.f32x2).
+        uint64_t xy = f32x2(v0[2 * i], v0[2 * i + 1]);
+        if constexpr (GG == 2) {
+          xy = add_f32x2(xy, f32x2(v1[2 * i], v1[2 * i + 1]));
+        } else {
+          const uint32_t n12 = pack_bf16x2_of(add_f32x2(f32x2(v1[2 * i], v1[2 * i + 1]), f32x2(v2[2 * i], v2[2 * i + 1])));
+          xy = add_f32x2(xy, f32x2(n12 << 16, n12 & 0xFFFF0000u));
+        }
+        emit(c * WC + i, pack_bf16x2_of(xy));
+      }
+    }
+  }
+  // The leaves are in registers: return the TMEM buffers.
+  tc_fence_before();
+  __syncwarp();
+  if (e.lane == 0)
+    for (int g = 0; g < GG; ++g) mbar_arrive(&e.bars->acce[(e.lc + g) % T::NBUF]);
+  e.lc += GG;
+  return true;
+}
+
 template <int BN, int GG, bool DUMP>
 __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -208,7 +328,7 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
       mbar_init(&bars->accf[b], 1);
       mbar_init(&bars->acce[b], T::EPI_WARPS);
     }
-    mbar_init(&bars->fin, kIssuers);
+    mbar_init(&bars->fin, Roles<GG>::ISSUERS);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -228,108 +348,125 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
-  if (warp < kEpiWarp0) regs_dec<kRegsLow>();
-  else regs_inc<kRegsHigh>();
 
-  if (warp == 0) {
-    // ---------------- TMA producer (converged warp; one lane issues) ----------------
-    // Stage it % NS is free once the MMAs of leaf it - NS have completed,
-    // which the leaf's own "full accumulator" barrier reports (NS <= NBUF,
-    // so that barrier cannot have moved on by a second phase).
-    long long it = 0;
-    Ring rs;  // stage of load it
-    Ring rv;  // TMEM buffer of leaf it - NS
-    bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const int pb = u % a.np, v = u / a.np;
-      const int t = v;
-      const int tm = t % a.num_m, tn = t / a.num_m;
-      const CUtensorMap* mA = pb ? &tmA2 : &tmA;
-      const CUtensorMap* mB = pb ? &tmB2 : &tmB;
-      for (int j = 0; j < a.L; ++j, ++it, rs.next(NS)) {
-        const int s = rs.slot;
-        if (it >= NS) {
-          const bool w = wait_or_abort(&bars->accf[rv.slot], rv.phase, limit, abort_flag, a.status);
-          if (!__all_sync(0xffffffffu, w)) {
-            ok = false;
-            break;
+  using RL = Roles<GG>;
+  const int nprod = (RL::PAIRED && NS % 2 == 0) ? 2 : 1;
+  if (warp < kEpiWarp0) {
+    // Warpgroup 0 hands most of its registers to the epilogue's two
+    // warpgroups (the register budget of each role is set in its own
+    // branch, so that the compiler allocates each role's code for it).
+    regs_dec<kRegsLow>();
+    if (warp == 0 || (RL::PAIRED && warp == 3)) {
+      // ---------------- TMA producers (converged warps; one lane issues) ----------------
+      // Producer p loads the leaves it with it % nprod == p.  Stage it % NS is
+      // free once the MMAs of leaf it - NS (the same producer's) have
+      // completed, which the leaf's own "full accumulator" barrier reports
+      // (NS <= NBUF, and leaf it - NS + NBUF is not loaded before leaf it, so
+      // that barrier cannot have moved on by a second phase).
+      const int p = warp == 0 ? 0 : 1;
+      long long it = 0;
+      Ring rs;  // stage of load it
+      Ring rv;  // TMEM buffer of leaf it - NS
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok && p < nprod; u += gridDim.x) {
+        const int pb = u % a.np, v = u / a.np;
+        const int t = v;
+        const int tm = t % a.num_m, tn = t / a.num_m;
+        const CUtensorMap* mA = pb ? &tmA2 : &tmA;
+        const CUtensorMap* mB = pb ? &tmB2 : &tmB;
+        for (int j = 0; j < a.L; ++j, ++it, rs.next(NS)) {
+          const int s = rs.slot;
+          const bool own = (int)(it & (nprod - 1)) == p;
+          if (it >= NS) {
+            if (own) {
+              const bool w = wait_or_abort(&bars->accf[rv.slot], rv.phase, limit, abort_flag, a.status);
+              if (!__all_sync(0xffffffffu, w)) {
+                ok = false;
+                break;
+              }
+            }
+            rv.next(T::NBUF);
           }
-          rv.next(T::NBUF);
+          if (own && !a.stall && elect_one()) {
+            unsigned char* st = stages + s * T::STAGE;
+            mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
+            const int x = j * BK;
+            if (a.a_mn) {  // two boxes of 64 (R) x 64 (K)
+              tma_load_2d(st, mA, tm * BM, x, &bars->full[s]);
+              tma_load_2d(st + T::A_BYTES / 2, mA, tm * BM + BM / 2, x, &bars->full[s]);
+            } else {
+              tma_load_2d(st, mA, x, tm * BM, &bars->full[s]);
+            }
+            if (a.b_mn) {  // two boxes of 64 (C) x 64 (K)
+              tma_load_2d(st + T::A_BYTES, mB, tn * BN, x, &bars->full[s]);
+              tma_load_2d(st + T::A_BYTES + T::B_BYTES / 2, mB, tn * BN + BN / 2, x, &bars->full[s]);
+            } else {
+              tma_load_2d(st + T::A_BYTES, mB, x, tn * BN, &bars->full[s]);
+            }
+          }
+          __syncwarp();
         }
-        if (!a.stall && elect_one()) {
-          unsigned char* st = stages + s * T::STAGE;
-          mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
-          const int x = j * BK;
-          if (a.a_mn) {  // two boxes of 64 (R) x 64 (K)
-            tma_load_2d(st, mA, tm * BM, x, &bars->full[s]);
-            tma_load_2d(st + T::A_BYTES / 2, mA, tm * BM + BM / 2, x, &bars->full[s]);
-          } else {
-            tma_load_2d(st, mA, x, tm * BM, &bars->full[s]);
-          }
-          if (a.b_mn) {  // two boxes of 64 (C) x 64 (K)
-            tma_load_2d(st + T::A_BYTES, mB, tn * BN, x, &bars->full[s]);
-            tma_load_2d(st + T::A_BYTES + T::B_BYTES / 2, mB, tn * BN + BN / 2, x, &bars->full[s]);
-          } else {
-            tma_load_2d(st + T::A_BYTES, mB, x, tn * BN, &bars->full[s]);
-          }
+      }
+      // Drain: the last loads issued into each stage have landed (on the long
+      // bound, whatever the call's poll limit: no CTA exits with copies in
+      // flight).
+      if (lane == 0 && !a.stall)
+        for (long long i = (it > NS ? it - NS : 0); i < it; ++i)
+          if ((int)(i & (nprod - 1)) == p) mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), kDefaultSpin, nullptr);
+    } else if (warp >= 1 && warp <= RL::ISSUERS) {
+      const int q = warp - 1;  // issuer index
+      // ---------------- MMA issuers (converged warps; one lane each issues) ----------------
+      // Leaf n uses stage n % NS and TMEM buffer n % NBUF, with one commit per
+      // leaf (its "full accumulator" barrier, which the producer reads).
+      // Issuer q takes UNIT consecutive leaves at a time (units q, q + ISSUERS,
+      // ...).  In the paired layout a unit is a bottom group, so the commit of
+      // its second leaf also covers its first (a commit tracks all of its
+      // thread's earlier MMAs) and the epilogue waits once per group.  Leaves
+      // are independent accumulations, so the issuers' MMAs may reach the
+      // tensor pipe in any order.
+      static_assert(T::NBUF >= 3, "a group of up to 3 leaves in flight");
+      const uint32_t idesc = idesc_bf16(BM, BN) | (a.b_mn ? kIdescTransB : 0u) | (a.a_mn ? kIdescTransA : 0u);
+      const uint32_t bstep = a.b_mn ? 128u : 2u;  // K = 16 step in descriptor units
+      const uint32_t astep = a.a_mn ? 128u : 2u;
+      const int mine = blockIdx.x < units ? (units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+      const long long nunit = (long long)mine * (a.L / RL::UNIT);
+      Ring rs, rb;  // pipeline stage; TMEM leaf buffer
+      rs.adv(q * RL::UNIT, NS);
+      rb.adv(q * RL::UNIT, T::NBUF);
+      bool ok = true;
+      for (long long gi = q; gi < nunit && ok; gi += RL::ISSUERS) {
+       for (int gl = 0; gl < RL::UNIT; ++gl) {
+        const int s = rs.slot, b = rb.slot;
+        const bool w = wait_or_abort(&bars->acce[b], rb.phase ^ 1u, limit, abort_flag, a.status) &&
+                       wait_or_abort(&bars->full[s], rs.phase, limit, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t da = a.a_mn ? smem_desc_sw128_mn(stages + s * T::STAGE) : smem_desc_sw128(stages + s * T::STAGE);
+        const uint64_t db = a.b_mn ? smem_desc_sw128_mn(stages + s * T::STAGE + T::A_BYTES)
+                                   : smem_desc_sw128(stages + s * T::STAGE + T::A_BYTES);
+        if (elect_one()) {
+  #pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
+            tc_mma_bf16(tmem + (uint32_t)(b * BN), da + astep * kk, db + bstep * kk, idesc, kk > 0 ? 1u : 0u);
+          tc_commit(&bars->accf[b]);
         }
         __syncwarp();
-      }
-    }
-    // Drain: the last loads issued into each stage have landed (on the long
-    // bound, whatever the call's poll limit: no CTA exits with copies in
-    // flight).
-    if (lane == 0 && !a.stall)
-      for (long long i = (it > NS ? it - NS : 0); i < it; ++i)
-        mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), kDefaultSpin, nullptr);
-  } else if (warp < kEpiWarp0) {
-    const int q = warp - 1;  // issuer index
-    // ---------------- MMA issuers (converged warps; one lane each issues) ----------------
-    // Leaf n uses stage n % NS and TMEM buffer n % NBUF; one commit per leaf
-    // (its "full accumulator" barrier) tells both the epilogue and the
-    // producer.  Leaves are independent accumulations, so the issuers' MMAs
-    // may reach the tensor pipe in any order.
-    static_assert(T::NBUF >= 3, "a group of up to 3 leaves in flight");
-    const uint32_t idesc = idesc_bf16(BM, BN) | (a.b_mn ? kIdescTransB : 0u) | (a.a_mn ? kIdescTransA : 0u);
-    const uint32_t bstep = a.b_mn ? 128u : 2u;  // K = 16 step in descriptor units
-    const uint32_t astep = a.a_mn ? 128u : 2u;
-    const int mine = blockIdx.x < units ? (units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-    const long long nleaf = (long long)mine * a.L;
-    Ring rs, rb;  // pipeline stage; TMEM leaf buffer
-    for (int i = 0; i < q; ++i) {
-      rs.next(NS);
-      rb.next(T::NBUF);
-    }
-    bool ok = true;
-    for (long long n = q; n < nleaf && ok; n += kIssuers) {
-      const int s = rs.slot, b = rb.slot;
-      const bool w = wait_or_abort(&bars->acce[b], rb.phase ^ 1u, limit, abort_flag, a.status) &&
-                     wait_or_abort(&bars->full[s], rs.phase, limit, abort_flag, a.status);
-      if (!__all_sync(0xffffffffu, w)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint64_t da = a.a_mn ? smem_desc_sw128_mn(stages + s * T::STAGE) : smem_desc_sw128(stages + s * T::STAGE);
-      const uint64_t db = a.b_mn ? smem_desc_sw128_mn(stages + s * T::STAGE + T::A_BYTES)
-                                 : smem_desc_sw128(stages + s * T::STAGE + T::A_BYTES);
-      if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)  // a fresh FP32 accumulation per leaf
-          tc_mma_bf16(tmem + (uint32_t)(b * BN), da + astep * kk, db + bstep * kk, idesc, kk > 0 ? 1u : 0u);
-        tc_commit(&bars->accf[b]);
-      }
-      __syncwarp();
-      for (int i = 0; i < kIssuers; ++i) {
         rs.next(NS);
         rb.next(T::NBUF);
+       }
+       rs.adv((RL::ISSUERS - 1) * RL::UNIT, NS);
+       rb.adv((RL::ISSUERS - 1) * RL::UNIT, T::NBUF);
       }
+      if (elect_one()) tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
+      __syncwarp();
+      // Every issuer's MMAs have completed before TMEM is freed (long bound).
+      if (q == 0 && lane == 0) mbar_wait(&bars->fin, 0, kDefaultSpin, nullptr);
     }
-    if (elect_one()) tc_commit(&bars->fin);  // arrives when every MMA issued above has completed
-    __syncwarp();
-    // Every issuer's MMAs have completed before TMEM is freed (long bound).
-    if (q == 0 && lane == 0) mbar_wait(&bars->fin, 0, kDefaultSpin, nullptr);
   } else {
+    regs_inc<kRegsHigh>();
     // ---------------- epilogue: leaves -> tree ----------------
     const int ew = warp - kEpiWarp0;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
@@ -338,137 +475,91 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     const int col0 = half * T::COLS;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const int Q = 1 << a.E;
-    uint32_t lc = 0;  // leaves consumed (NBUF is a power of two)
-    int stg_n = 0;    // tiles staged for a TMA store
-    bool ok = true;
-    uint32_t reg_lv[T::REG_LV][T::WORDS];
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const int pb = u % a.np, v = u / a.np;
-      const int t = v;
-      const int tm = t % a.num_m, tn = t / a.num_m;
-      uint16_t* const outp = pb ? a.out2 : a.out;
-      const long long r = (long long)tm * BM + row;
-      for (int q = 0; q < Q; ++q) {
-        for (int g = 0; g < GG; ++g)
-          if (!wait_or_abort(&bars->accf[(lc + g) % T::NBUF], (uint32_t)(((lc + g) / T::NBUF) & 1),
-                             limit, abort_flag, a.status))
-            ok = false;
-        if (__any_sync(0xffffffffu, !ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t b0 = (uint32_t)((lc % T::NBUF) * BN), b1 = (uint32_t)(((lc + 1) % T::NBUF) * BN),
-                       b2 = (uint32_t)(((lc + 2) % T::NBUF) * BN);
-        // Phase 1: read the group's leaves from TMEM in column chunks of 32
-        // and form the group roots.
-        constexpr int CW = 32;
-        constexpr int WC = CW / 2;  // packed words per chunk
-        uint32_t root[T::WORDS];
-        if constexpr (GG == 1) {
-          // A lone leaf (one-leaf trees: weight gradients over few tokens):
-          // all columns read with one wait, each rounded once.
-          static_assert(T::COLS % 32 == 0, "columns per thread");
-#pragma unroll
-          for (int c = 0; c < T::COLS / 32; c += 2) {
-            uint32_t va[32], vb[32];
-            tmem_ld32(tmem + lane_addr + b0 + (uint32_t)(col0 + 32 * c), va);
-            if (c + 1 < T::COLS / 32) tmem_ld32(tmem + lane_addr + b0 + (uint32_t)(col0 + 32 * c + 32), vb);
-            tmem_wait_ld();
-            if constexpr (DUMP) {
-              float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
-              const long long cc = (long long)tn * BN + col0 + 32 * c;
-              dump_leaves(d, r, cc, a.R, a.C, a.L, q, va);
-              if (c + 1 < T::COLS / 32) dump_leaves(d, r, cc + 32, a.R, a.C, a.L, q, vb);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) root[16 * c + i] = pack_bf16x2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]));
-            if (c + 1 < T::COLS / 32)
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                root[16 * c + 16 + i] = pack_bf16x2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1]));
-          }
-        } else
-#pragma unroll
-        for (int c = 0; c < T::COLS / CW; ++c) {
-          uint32_t v0[CW], v1[GG >= 2 ? CW : 1], v2[GG >= 3 ? CW : 1];
-          const uint32_t col = (uint32_t)(col0 + CW * c);
-          tmem_ld32(tmem + lane_addr + b0 + col, v0);
-          if constexpr (GG >= 2) tmem_ld32(tmem + lane_addr + b1 + col, v1);
-          if constexpr (GG >= 3) tmem_ld32(tmem + lane_addr + b2 + col, v2);
-          tmem_wait_ld();
-          if constexpr (DUMP) {
-            float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
-            const long long cc = (long long)tn * BN + col;
-            dump_leaves(d, r, cc, a.R, a.C, a.L, q * GG, v0);
-            if constexpr (GG >= 2) dump_leaves(d, r, cc, a.R, a.C, a.L, q * GG + 1, v1);
-            if constexpr (GG >= 3) dump_leaves(d, r, cc, a.R, a.C, a.L, q * GG + 2, v2);
-          }
-#pragma unroll
-          for (int i = 0; i < WC; ++i) {
-            // Pairs of adjacent columns, added two at a time (add.rn.f32x2).
-            uint64_t xy = f32x2(v0[2 * i], v0[2 * i + 1]);
-            if constexpr (GG == 2) {
-              xy = add_f32x2(xy, f32x2(v1[2 * i], v1[2 * i + 1]));
-            } else if constexpr (GG == 3) {
-              const uint32_t n12 = pack_bf16x2_of(add_f32x2(f32x2(v1[2 * i], v1[2 * i + 1]), f32x2(v2[2 * i], v2[2 * i + 1])));
-              xy = add_f32x2(xy, f32x2(n12 << 16, n12 & 0xFFFF0000u));
-            }
-            root[c * WC + i] = pack_bf16x2_of(xy);  // a lone leaf (GG == 1) is rounded once
-          }
-        }
-        // The leaves are in registers: return the TMEM buffers to the MMA warp.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-          for (int g = 0; g < GG; ++g) mbar_arrive(&bars->acce[(lc + g) % T::NBUF]);
-        lc += GG;
+    EpiCtx e{tmem, lane_addr, col0, lane, bars, limit, abort_flag, 0u, true};
+    int stg_n = 0;  // tiles staged for a TMA store
+    bool& ok = e.ok;
 
-        // Phase 2: fold the roots into the stack (an elementwise binary counter).
-        int l = 0;
-#pragma unroll
-        for (int m = 0; m < kMaxLv; ++m) {
-          if (m >= a.E || !((q >> m) & 1)) break;
-#pragma unroll
-          for (int w = 0; w < T::WORDS; ++w) {
-            const uint32_t left = (m < T::REG_LV) ? reg_lv[m < T::REG_LV ? m : 0][w]
-                                                  : *stk_at<BN>(stk, m, half, w, row);
-            root[w] = node2(left, root[w]);
+
+    if constexpr (GG >= 2) {
+      // Blocks of four bottom groups (or the one or two groups of a shorter
+      // tree), whose level-0 and level-1 nodes stay in fixed registers; the
+      // binary counter above them (levels >= 2) lives in shared memory.
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int pb = u % a.np, t = u / a.np;
+        const int tm = t % a.num_m, tn = t / a.num_m;
+        uint16_t* const outp = pb ? a.out2 : a.out;
+        const long long r = (long long)tm * BM + row;
+        for (int q = 0; q < Q; q += 4) {
+          // n0: the root of group q, then of q+2, then the node over q..q+3;
+          // n1: the node over groups q, q+1.
+          uint32_t n0[T::WORDS], n1[T::WORDS];
+          if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q)) break;
+          if (Q == 1) {
+            if (r < a.R) store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, n0);
+            continue;
           }
-          l = m + 1;
-        }
-        if (q != Q - 1) {
+          if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n1[w] = node2(n0[w], g); }, pb, r, tn, q + 1))
+            break;
+          if (Q == 2) {
+            if (r < a.R) store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, n1);
+            continue;
+          }
+          if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q + 2)) break;
+          if (!group_root<BN, GG, DUMP>(
+                  e, a, [&](int w, uint32_t g) { n0[w] = node2(n1[w], node2(n0[w], g)); }, pb, r, tn, q + 3))
+            break;
+          uint32_t(&root)[T::WORDS] = n0;
+          const int qq = q + 3;
+          int l = 2;
 #pragma unroll
-          for (int m = 0; m < kMaxLv; ++m)
-            if (m == l) {
+          for (int m = 2; m < kMaxLv; ++m) {
+            if (m >= a.E || !((qq >> m) & 1)) break;
 #pragma unroll
-              for (int w = 0; w < T::WORDS; ++w) {
-                if (m < T::REG_LV) reg_lv[m < T::REG_LV ? m : 0][w] = root[w];
-                else *stk_at<BN>(stk, m, half, w, row) = root[w];
+            for (int w = 0; w < T::WORDS; ++w) root[w] = node2(*stk_at<BN>(stk, m, half, w, row), root[w]);
+            l = m + 1;
+          }
+          if (qq != Q - 1) {
+#pragma unroll
+            for (int m = 2; m < kMaxLv; ++m)
+              if (m == l) {
+#pragma unroll
+                for (int w = 0; w < T::WORDS; ++w) *stk_at<BN>(stk, m, half, w, row) = root[w];
               }
-            }
-        } else if (GG == 1 && a.o_tma) {
+          } else if (r < a.R) {
+            store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
+          }
+        }
+      }
+    } else {
+      // One-leaf trees (the weight gradients over at most 64 tokens): the
+      // leaf, rounded once, is the output.
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int pb = u % a.np, t = u / a.np;
+        const int tm = t % a.num_m, tn = t / a.num_m;
+        uint16_t* const outp = pb ? a.out2 : a.out;
+        const long long r = (long long)tm * BM + row;
+        uint32_t root[T::WORDS];
+        if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { root[w] = g; }, pb, r, tn, 0)) break;
+        if (a.o_tma) {
           // Row-major output: this warp's 32 rows x COLS columns go to shared
           // memory in the swizzled layout of a TMA box and leave as one bulk
           // tensor store (clipped at the output's edges); two buffers per
           // warp, so that staging the next tile overlaps this store.
-          if constexpr (GG == 1) {
-            unsigned char* buf = stg_all + (ew * 2 + (stg_n & 1)) * T::STG_BUF;
-            if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
-            __syncwarp();
+          unsigned char* buf = stg_all + (ew * 2 + (stg_n & 1)) * T::STG_BUF;
+          if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+          __syncwarp();
 #pragma unroll
-            for (int v = 0; v < T::COLS / 8; ++v)  // 16-byte chunk v of row `lane` at chunk v ^ (lane % 8)
-              *reinterpret_cast<uint4*>(buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
-                  make_uint4(root[4 * v], root[4 * v + 1], root[4 * v + 2], root[4 * v + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            const int ox = tn * BN + col0, oy = tm * BM + quarter * 32;
-            if (lane == 0 && ox < a.C && oy < a.R) {  // (a box wholly past the edge is skipped)
-              tma_store_2d(pb ? &tmO2 : &tmO, buf, ox, oy);
-              bulk_commit();
-            }
-            ++stg_n;
+          for (int v = 0; v < T::COLS / 8; ++v)  // 16-byte chunk v of row `lane` at chunk v ^ (lane % 8)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
+                make_uint4(root[4 * v], root[4 * v + 1], root[4 * v + 2], root[4 * v + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int ox = tn * BN + col0, oy = tm * BM + quarter * 32;
+          if (lane == 0 && ox < a.C && oy < a.R) {  // (a box wholly past the edge is skipped)
+            tma_store_2d(pb ? &tmO2 : &tmO, buf, ox, oy);
+            bulk_commit();
           }
+          ++stg_n;
         } else if (r < a.R) {
           store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
         }

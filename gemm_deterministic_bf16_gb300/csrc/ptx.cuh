@@ -83,6 +83,14 @@ struct Ring {
       phase ^= 1u;
     }
   }
+  // k increments at once.
+  __device__ __forceinline__ void adv(int k, int n) {
+    slot += k;
+    while (slot >= n) {
+      slot -= n;
+      phase ^= 1u;
+    }
+  }
 };
 
 // 1-D bulk copy global -> shared, completing `bytes` of transaction on `bar`.

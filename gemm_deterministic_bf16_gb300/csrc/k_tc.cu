@@ -153,7 +153,7 @@ struct TcArgs {
   int num_m, num_n;
   int np;           // problems in this launch (1 or 2; the second uses tmA2/tmB2 and out2)
   int b_mn;         // B stored [K][C] (C contiguous): MN-major B tiles (BN = 128 only)
-  int o_tma;        // one-leaf trees: outputs leave through TMA stores (maps tmO, tmO2)
+  int o_tma;        // row-major outputs may leave through TMA stores (maps tmO, tmO2)
   int a_mn;         // A stored [K][R] (R contiguous): MN-major A tiles
   uint16_t* out;
   uint16_t* out2;
@@ -181,11 +181,14 @@ __device__ __forceinline__ void store_cols(uint16_t* base, long long row_off, lo
   }
 }
 
-// Stack level m >= REG_LV lives in shared memory as [level][half][word][row].
+// Stack level m >= REG_LV lives in shared memory as [level][epilogue
+// warp][word][lane]: each warp's share of a level is its own 4 KB block
+// (1024-byte aligned), which at the end of a tile doubles as the staging
+// buffer of the warp's TMA output store.
 template <int BN>
-__device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int half, int w, int row) {
+__device__ __forceinline__ uint32_t* stk_at(uint32_t* stk, int m, int ew, int w, int lane) {
   using T = TcGeo<BN>;
-  return stk + (((m - T::REG_LV) * T::HALVES + half) * T::WORDS + w) * BM + row;
+  return stk + (((m - T::REG_LV) * T::EPI_WARPS + ew) * T::WORDS + w) * 32 + lane;
 }
 
 // The epilogue's view of one CTA's pipeline.
@@ -214,7 +217,8 @@ __device__ __forceinline__ bool group_root(EpiCtx& e, const TcArgs& a, Emit&& em
     if (!wait_or_abort(&e.bars->accf[last % T::NBUF], (last / T::NBUF) & 1u, e.limit, e.abort_flag, a.status))
       e.ok = false;
   } else {
-    for (int g = 0; g < GG; ++g)
+    // (Three-leaf groups: the first two slots here, the third further down.)
+    for (int g = 0; g < (GG == 3 ? 2 : GG); ++g)
       if (!wait_or_abort(&e.bars->accf[(e.lc + g) % T::NBUF], ((e.lc + g) / T::NBUF) & 1u, e.limit, e.abort_flag,
                          a.status))
         e.ok = false;
@@ -226,8 +230,8 @@ __device__ __forceinline__ bool group_root(EpiCtx& e, const TcArgs& a, Emit&& em
   tc_fence_after();
   const uint32_t b0 = (uint32_t)((e.lc % T::NBUF) * BN), b1 = (uint32_t)(((e.lc + 1) % T::NBUF) * BN),
                  b2 = (uint32_t)(((e.lc + 2) % T::NBUF) * BN);
-  constexpr int CW = GG >= 3 ? 16 : 32;  // columns per chunk (registers: GG x CW)
-  constexpr int WC = CW / 2;             // packed words per chunk
+  constexpr int CW = 32;     // columns per chunk
+  constexpr int WC = CW / 2;  // packed words per chunk
   if constexpr (GG == 1) {
     // A lone leaf (one-leaf trees: weight gradients over few tokens):
     // all columns read with one wait, each rounded once.
@@ -251,38 +255,76 @@ __device__ __forceinline__ bool group_root(EpiCtx& e, const TcArgs& a, Emit&& em
         for (int i = 0; i < 16; ++i)
           emit(16 * c + 16 + i, pack_bf16x2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1])));
     }
-  } else {
+  } else if constexpr (GG == 2) {
 #pragma unroll
     for (int c = 0; c < T::COLS / CW; ++c) {
-      uint32_t v0[CW], v1[CW], v2[GG >= 3 ? CW : 1];
+      uint32_t v0[CW], v1[CW];
       const uint32_t col = (uint32_t)(e.col0 + CW * c);
-      if constexpr (GG >= 3) {
-        tmem_ld16(e.tmem + e.lane_addr + b0 + col, v0);
-        tmem_ld16(e.tmem + e.lane_addr + b1 + col, v1);
-        tmem_ld16(e.tmem + e.lane_addr + b2 + col, v2);
-      } else {
-        tmem_ld32(e.tmem + e.lane_addr + b0 + col, v0);
-        tmem_ld32(e.tmem + e.lane_addr + b1 + col, v1);
-      }
+      tmem_ld32(e.tmem + e.lane_addr + b0 + col, v0);
+      tmem_ld32(e.tmem + e.lane_addr + b1 + col, v1);
       tmem_wait_ld();
       if constexpr (DUMP) {
         float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
         const long long cc = (long long)tn * BN + col;
         dump_leaves(d, r, cc, a.R, a.C, a.L, qg * GG, v0);
         dump_leaves(d, r, cc, a.R, a.C, a.L, qg * GG + 1, v1);
-        if constexpr (GG >= 3) dump_leaves(d, r, cc, a.R, a.C, a.L, qg * GG + 2, v2);
+      }
+#pragma unroll
+      for (int i = 0; i < WC; ++i)  // pairs of adjacent columns, added two at a time (add.rn.f32x2)
+        emit(c * WC + i, pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(v1[2 * i], v1[2 * i + 1]))));
+    }
+  } else {
+    // Three leaves, loaded and issued in the order leaf 1, leaf 2, leaf 0
+    // (slots 0, 1, 2): the node over leaves 1 and 2 is formed first and their
+    // two buffers go back to the issuers before leaf 0 is read, so that the
+    // next group's first two leaves can start while this one finishes.
+    constexpr int CH = 16;  // columns per chunk in the first pass
+    uint32_t n12[T::WORDS];
+#pragma unroll
+    for (int c = 0; c < T::COLS / CH; ++c) {
+      uint32_t v1[CH], v2[CH];
+      const uint32_t col = (uint32_t)(e.col0 + CH * c);
+      tmem_ld16(e.tmem + e.lane_addr + b0 + col, v1);
+      tmem_ld16(e.tmem + e.lane_addr + b1 + col, v2);
+      tmem_wait_ld();
+      if constexpr (DUMP) {
+        float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
+        const long long cc = (long long)tn * BN + col;
+        dump_leaves(d, r, cc, a.R, a.C, a.L, qg * GG + 1, v1);
+        dump_leaves(d, r, cc, a.R, a.C, a.L, qg * GG + 2, v2);
+      }
+#pragma unroll
+      for (int i = 0; i < CH / 2; ++i)
+        n12[c * (CH / 2) + i] = pack_bf16x2_of(add_f32x2(f32x2(v1[2 * i], v1[2 * i + 1]), f32x2(v2[2 * i], v2[2 * i + 1])));
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (e.lane == 0) {
+      mbar_arrive(&e.bars->acce[e.lc % T::NBUF]);
+      mbar_arrive(&e.bars->acce[(e.lc + 1) % T::NBUF]);
+    }
+    const uint32_t l0 = e.lc + 2;
+    if (!wait_or_abort(&e.bars->accf[l0 % T::NBUF], (l0 / T::NBUF) & 1u, e.limit, e.abort_flag, a.status))
+      e.ok = false;
+    if (__any_sync(0xffffffffu, !e.ok)) {
+      e.ok = false;
+      return false;
+    }
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < T::COLS / CW; ++c) {
+      uint32_t v0[CW];
+      const uint32_t col = (uint32_t)(e.col0 + CW * c);
+      tmem_ld32(e.tmem + e.lane_addr + b2 + col, v0);
+      tmem_wait_ld();
+      if constexpr (DUMP) {
+        float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
+        dump_leaves(d, r, (long long)tn * BN + col, a.R, a.C, a.L, qg * GG, v0);
       }
 #pragma unroll
       for (int i = 0; i < WC; ++i) {
-        // Pairs of adjacent columns, added two at a time (add.rn.f32x2).
-        uint64_t xy = f32x2(v0[2 * i], v0[2 * i + 1]);
-        if constexpr (GG == 2) {
-          xy = add_f32x2(xy, f32x2(v1[2 * i], v1[2 * i + 1]));
-        } else {
-          const uint32_t n12 = pack_bf16x2_of(add_f32x2(f32x2(v1[2 * i], v1[2 * i + 1]), f32x2(v2[2 * i], v2[2 * i + 1])));
-          xy = add_f32x2(xy, f32x2(n12 << 16, n12 & 0xFFFF0000u));
-        }
-        emit(c * WC + i, pack_bf16x2_of(xy));
+        const uint32_t nn = n12[c * WC + i];
+        emit(c * WC + i, pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(nn << 16, nn & 0xFFFF0000u))));
       }
     }
   }
@@ -290,7 +332,7 @@ __device__ __forceinline__ bool group_root(EpiCtx& e, const TcArgs& a, Emit&& em
   tc_fence_before();
   __syncwarp();
   if (e.lane == 0)
-    for (int g = 0; g < GG; ++g) mbar_arrive(&e.bars->acce[(e.lc + g) % T::NBUF]);
+    for (int g = (GG == 3 ? 2 : 0); g < GG; ++g) mbar_arrive(&e.bars->acce[(e.lc + g) % T::NBUF]);
   e.lc += GG;
   return true;
 }
@@ -374,7 +416,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
         const int tm = t % a.num_m, tn = t / a.num_m;
         const CUtensorMap* mA = pb ? &tmA2 : &tmA;
         const CUtensorMap* mB = pb ? &tmB2 : &tmB;
-        for (int j = 0; j < a.L; ++j, ++it, rs.next(NS)) {
+        int j3 = 0;  // j % 3
+        for (int j = 0; j < a.L; ++j, ++it, rs.next(NS), j3 = (j3 == 2 ? 0 : j3 + 1)) {
           const int s = rs.slot;
           const bool own = (int)(it & (nprod - 1)) == p;
           if (it >= NS) {
@@ -390,7 +433,9 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
           if (own && !a.stall && elect_one()) {
             unsigned char* st = stages + s * T::STAGE;
             mbar_arrive_expect_tx(&bars->full[s], (uint32_t)T::STAGE);
-            const int x = j * BK;
+            // Three-leaf groups are loaded leaf 1, leaf 2, leaf 0 (see the
+            // epilogue): slot j3 = j % 3 of a group holds leaf (j3 + 1) % 3.
+            const int x = (GG == 3 ? (j3 == 2 ? j - 2 : j + 1) : j) * BK;
             if (a.a_mn) {  // two boxes of 64 (R) x 64 (K)
               tma_load_2d(st, mA, tm * BM, x, &bars->full[s]);
               tma_load_2d(st + T::A_BYTES / 2, mA, tm * BM + BM / 2, x, &bars->full[s]);
@@ -489,44 +534,74 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
         const int tm = t % a.num_m, tn = t / a.num_m;
         uint16_t* const outp = pb ? a.out2 : a.out;
         const long long r = (long long)tm * BM + row;
-        for (int q = 0; q < Q; q += 4) {
-          // n0: the root of group q, then of q+2, then the node over q..q+3;
-          // n1: the node over groups q, q+1.
-          uint32_t n0[T::WORDS], n1[T::WORDS];
-          if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q)) break;
-          if (Q == 1) {
-            if (r < a.R) store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, n0);
-            continue;
+        for (int q = 0; q < Q && ok; q += 4) {
+          // One copy of the group reader in a loop that is not unrolled (the
+          // epilogue's speed is bound by instruction fetch, so its code is
+          // kept small): cur takes the group's root and then the node over
+          // the groups read so far in this block; n0 keeps the root of group
+          // q (then q+2), n1 the node over groups q, q+1.
+          uint32_t n0[T::WORDS], n1[T::WORDS], cur[T::WORDS];
+#pragma unroll 1
+          for (int k = 0; k < 4 && k < Q; ++k) {
+            if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { cur[w] = g; }, pb, r, tn, q + k)) break;
+            if (k & 1) {
+#pragma unroll
+              for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n0[w], cur[w]);
+            }
+            if (k == 3) {
+#pragma unroll
+              for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n1[w], cur[w]);
+            } else if (k == 1) {
+#pragma unroll
+              for (int w = 0; w < T::WORDS; ++w) n1[w] = cur[w];
+            } else {
+#pragma unroll
+              for (int w = 0; w < T::WORDS; ++w) n0[w] = cur[w];
+            }
           }
-          if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n1[w] = node2(n0[w], g); }, pb, r, tn, q + 1))
-            break;
-          if (Q == 2) {
-            if (r < a.R) store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, n1);
-            continue;
-          }
-          if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q + 2)) break;
-          if (!group_root<BN, GG, DUMP>(
-                  e, a, [&](int w, uint32_t g) { n0[w] = node2(n1[w], node2(n0[w], g)); }, pb, r, tn, q + 3))
-            break;
-          uint32_t(&root)[T::WORDS] = n0;
-          const int qq = q + 3;
+          if (!ok) break;
+          const int qq = q + (Q < 4 ? Q : 4) - 1;  // the last group of this block
+          // The binary counter above the register levels: fold the stored
+          // nodes of levels 2, 3, ... while the group index has those bits.
           int l = 2;
+#pragma unroll 1
+          for (int m = 2; m < a.E && ((qq >> m) & 1); ++m) {
+            const uint32_t* src = stk_at<BN>(stk, m, ew, 0, lane);
 #pragma unroll
-          for (int m = 2; m < kMaxLv; ++m) {
-            if (m >= a.E || !((qq >> m) & 1)) break;
-#pragma unroll
-            for (int w = 0; w < T::WORDS; ++w) root[w] = node2(*stk_at<BN>(stk, m, half, w, row), root[w]);
+            for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(src[w * 32], cur[w]);
             l = m + 1;
           }
           if (qq != Q - 1) {
+            if (l == 2 && stg_n) {  // this warp's last output store has read its level-2 block
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+              stg_n = 0;
+            }
+            uint32_t* dst = stk_at<BN>(stk, l, ew, 0, lane);
 #pragma unroll
-            for (int m = 2; m < kMaxLv; ++m)
-              if (m == l) {
+            for (int w = 0; w < T::WORDS; ++w) dst[w * 32] = cur[w];
+          } else if (a.o_tma && a.E >= 3) {
+            // Every stored level has just been folded: the warp's level-2
+            // block stages its 32 rows x COLS columns in the swizzled layout
+            // of a TMA box, which leaves as one bulk tensor store (clipped
+            // at the output's edges) -- coalesced, where a row per thread is
+            // not.
+            unsigned char* buf = reinterpret_cast<unsigned char*>(stk_at<BN>(stk, 2, ew, 0, 0));
+            __syncwarp();  // all lanes' reads of the level are done
 #pragma unroll
-                for (int w = 0; w < T::WORDS; ++w) *stk_at<BN>(stk, m, half, w, row) = root[w];
-              }
+            for (int v = 0; v < T::COLS / 8; ++v)  // 16-byte chunk v of row `lane` at chunk v ^ (lane % 8)
+              *reinterpret_cast<uint4*>(buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
+                  make_uint4(cur[4 * v], cur[4 * v + 1], cur[4 * v + 2], cur[4 * v + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int ox = tn * BN + col0, oy = tm * BM + quarter * 32;
+            if (lane == 0 && ox < a.C && oy < a.R) {  // (a box wholly past the edge is skipped)
+              tma_store_2d(pb ? &tmO2 : &tmO, buf, ox, oy);
+              bulk_commit();
+            }
+            stg_n = 1;
           } else if (r < a.R) {
-            store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, root);
+            store_cols(outp, r * a.ld_r, (long long)tn * BN + col0, a.ld_c, a.C, cur);
           }
         }
       }
@@ -714,12 +789,15 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   a.dump = dump;
   a.nstage = TcGeo<bn>::stages_for(a.G, a.E);
   if (a.nstage > TcGeo<bn>::NBUF) a.nstage = TcGeo<bn>::NBUF;  // stage reuse is read off the leaf barriers
-  if (a.nstage < 2) return cudaErrorInvalidValue;
+  // At least three stages: with fewer, an issuer could wait on a stage barrier
+  // two phases behind (every tree shape the kernel takes leaves room for three).
+  if (a.nstage < 3) return cudaErrorInvalidValue;
   CUtensorMap m[6];
-  // One-leaf trees with row-major outputs store through TMA: boxes of 32 rows
-  // x 64 columns (one epilogue warp's share of a tile), 128-byte swizzle.
+  // Row-major outputs store through TMA (one-leaf trees, and trees with a
+  // shared-memory stack level): boxes of 32 rows x 64 columns (one epilogue
+  // warp's share of a tile), 128-byte swizzle.
   a.o_tma = 0;
-  if (G == 1 && ld_c == 1 && ld_r % 8 == 0) {
+  if (ld_c == 1 && ld_r % 8 == 0) {
     bool okm = true;
     for (int p = 0; p < 2 && okm; ++p) {
       const uint16_t* o = pr[p < np ? p : 0].out;

@@ -482,8 +482,14 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
       for (long long gi = q; gi < nunit && ok; gi += RL::ISSUERS) {
        for (int gl = 0; gl < RL::UNIT; ++gl) {
         const int s = rs.slot, b = rb.slot;
-        const bool w = wait_or_abort(&bars->acce[b], rb.phase ^ 1u, limit, abort_flag, a.status) &&
-                       wait_or_abort(&bars->full[s], rs.phase, limit, abort_flag, a.status);
+        // The buffer must have been returned by the epilogue.  In the paired
+        // layout the epilogue returns a pair's two buffers in order (each
+        // warp arrives on the first, then the second), so the second one's
+        // return, awaited before the first leaf, covers both.
+        bool w = true;
+        if (!RL::PAIRED || gl == 0)
+          w = wait_or_abort(&bars->acce[RL::PAIRED ? b + 1 : b], rb.phase ^ 1u, limit, abort_flag, a.status);
+        w = w && wait_or_abort(&bars->full[s], rs.phase, limit, abort_flag, a.status);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;

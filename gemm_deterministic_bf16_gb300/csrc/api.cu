@@ -565,9 +565,9 @@ detffn_status silu_mul(detffn_handle h, const uint16_t* g, const uint16_t* u, ui
 }
 
 detffn_status silu_bwd(detffn_handle h, const uint16_t* dh, const uint16_t* g, const uint16_t* u,
-                       uint16_t* dU, uint16_t* dG, long long n, cudaStream_t st) {
-  return timed(h, st, "silu_bwd", 10.0 * n, 0.0, [&] {
-    return cu(launch_silu_bwd(dh, g, u, dU, dG, n, h->d_silu, h->d_dsilu, st));
+                       uint16_t* dU, uint16_t* dG, uint16_t* hh, long long n, cudaStream_t st) {
+  return timed(h, st, "silu_bwd", (hh ? 12.0 : 10.0) * n, 0.0, [&] {
+    return cu(launch_silu_bwd(dh, g, u, dU, dG, hh, n, h->d_silu, h->d_dsilu, st));
   });
 }
 
@@ -896,16 +896,17 @@ extern "C" detffn_status detffn_forward_sharded(detffn_handle h, const void* x, 
 
 namespace {
 
-// Row-wise backward stages for rows [r0, r0+rows): dh, then dU and dG.
+// Row-wise backward stages for rows [r0, r0+rows): dh, then dU and dG (and h
+// again, for the down projection's weight gradient, in the same pass).
 detffn_status rowwise_bwd(detffn_handle h, Family f, const uint16_t* dOut, const uint16_t* Wd,
                           const uint16_t* gate, const uint16_t* up,
-                          uint16_t* dh, uint16_t* dU, uint16_t* dG, long long rows, long long H,
+                          uint16_t* dh, uint16_t* dU, uint16_t* dG, uint16_t* hh, long long rows, long long H,
                           long long I, cudaStream_t st, const TcsScratch& sc) {
   // dh[m, i] = T_{n<H}(dOut[m, n], Wd[n, i]): B row i is column i of Wd (K stride I),
   // (read MN-major by the tensor family).
   const Strided B{Wd, 1, I};
   TRY(tree_gemm(h, f, Strided{dOut, H, 1}, B, rows, I, H, dh, I, st, sc));
-  return silu_bwd(h, dh, gate, up, dU, dG, rows * I, st);
+  return silu_bwd(h, dh, gate, up, dU, dG, hh, rows * I, st);
 }
 
 // Weight gradients over K = M tokens from row-major [M, .] stage tensors (the
@@ -916,9 +917,10 @@ detffn_status wgrads(detffn_handle h, Family f, const uint16_t* x, const uint16_
                      cudaStream_t st) {
   // dWd[n, i] = T_m(dOut[m, n], h[m, i])
   TRY(tree_gemm(h, f, Strided{dOut, 1, H}, Strided{hh, 1, I}, H, I, M, dWd, I, st));
-  // dWg[i, n] = T_m(dG[m, i], x[m, n]); dWu likewise with dU.
-  TRY(tree_gemm(h, f, Strided{dG, 1, I}, Strided{x, 1, H}, I, H, M, dWg, H, st));
-  return tree_gemm(h, f, Strided{dU, 1, I}, Strided{x, 1, H}, I, H, M, dWu, H, st);
+  // dWg[i, n] = T_m(dG[m, i], x[m, n]); dWu likewise with dU (one launch of
+  // the tensor family for both).
+  return tree_gemm2(h, f, Strided{dG, 1, I}, Strided{x, 1, H}, dWg, Strided{dU, 1, I}, Strided{x, 1, H}, dWu, I, H,
+                    M, H, st, TcsScratch());
 }
 
 }  // namespace
@@ -983,7 +985,7 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
   const uint16_t* U = (const uint16_t*)up;
   const uint16_t* WG = (const uint16_t*)Wg;
   const uint16_t* WU = (const uint16_t*)Wu;
-  TRY(rowwise_bwd(h, f, (const uint16_t*)dOut, (const uint16_t*)Wd, G, U, dh, dU, dG, M, H, I, st,
+  TRY(rowwise_bwd(h, f, (const uint16_t*)dOut, (const uint16_t*)Wd, G, U, dh, dU, dG, w.h, M, H, I, st,
                   w.tcs));
   // dHidden: cg = T_i(dG[m, i], Wg[i, n]), cu = T_i(dU[m, i], Wu[i, n]); the two
   // trees stay separate until the final gate-then-up addition.  B row n is
@@ -1034,7 +1036,6 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
     TRY(rank_tree_bf16(h, pu, k, w.cu, M * H, st));
   }
   TRY(add_bf16(h, w.cg, w.cu, (uint16_t*)dX, M * H, st));
-  TRY(silu_mul(h, G, U, w.h, M, I, I, st));
   return wgrads(h, f, (const uint16_t*)x, (const uint16_t*)dOut, w.h, dU, dG, (uint16_t*)dWg,
                 (uint16_t*)dWu, (uint16_t*)dWd, M, H, I, st);
 }
@@ -1097,8 +1098,7 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
     TRYCU(cudaMemcpyAsync(w.g + r0 * I, gate_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
     TRYCU(cudaMemcpyAsync(w.u + r0 * I, up_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
     TRY(rowwise_bwd(h, f, w.dO + r0 * H, (const uint16_t*)Wd, w.g + r0 * I, w.u + r0 * I,
-                    w.dh + r0 * I, w.dU + r0 * I, w.dG + r0 * I, t, H, I, st, w.tcs));
-    TRY(silu_mul(h, w.g + r0 * I, w.u + r0 * I, w.h + r0 * I, t, I, I, st));
+                    w.dh + r0 * I, w.dU + r0 * I, w.dG + r0 * I, w.h + r0 * I, t, H, I, st, w.tcs));
     r0 += t;
   }
   return wgrads(h, f, w.x, w.dO, w.h, w.dU, w.dG, (uint16_t*)dWg, (uint16_t*)dWu, (uint16_t*)dWd,

@@ -69,9 +69,11 @@ cudaError_t launch_tree_gemm_exact(Strided A, Strided B, long long R, long long 
 cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* h, long long rows,
                             long long cols, long long ld, const uint16_t* silu_tab,
                             cudaStream_t st);
-// dU = rne(dh*a), dG = rne(rne_f32(rne(dh*u) * dsilu[g])).
+// dU = rne(dh*a), dG = rne(rne_f32(rne(dh*u) * dsilu[g])), and, where hh is
+// not null, hh = rne(a*u) (the forward's h, for the down projection's weight
+// gradient).
 cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u,
-                            uint16_t* dU, uint16_t* dG, long long n, const uint16_t* silu_tab,
+                            uint16_t* dU, uint16_t* dG, uint16_t* hh, long long n, const uint16_t* silu_tab,
                             const float* dsilu_tab, cudaStream_t st);
 // out = rne(a + b).
 cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out, long long n,

@@ -34,18 +34,22 @@ __global__ void k_silu_mul(const uint16_t* __restrict__ g, const uint16_t* __res
   }
 }
 
+// The backward stages, and (hh not null) the forward's h again, which the
+// weight gradient of the down projection reads.
 __global__ void k_silu_bwd(const uint16_t* __restrict__ dh, const uint16_t* __restrict__ g,
                            const uint16_t* __restrict__ u, uint16_t* __restrict__ dU,
-                           uint16_t* __restrict__ dG, long long n,
+                           uint16_t* __restrict__ dG, uint16_t* __restrict__ hh, long long n,
                            const uint16_t* __restrict__ silu, const float* __restrict__ dsilu) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const uint16_t gi = g[i];
     const float d = bf2f(dh[i]);
     const float a = bf2f(__ldg(silu + gi));
+    const float uu = bf2f(u[i]);
     dU[i] = f2bf(__fmul_rn(d, a));
-    const float dA = bf2f(f2bf(__fmul_rn(d, bf2f(u[i]))));
+    const float dA = bf2f(f2bf(__fmul_rn(d, uu)));
     dG[i] = f2bf(__fmul_rn(dA, __ldg(dsilu + gi)));
+    if (hh) hh[i] = f2bf(__fmul_rn(a, uu));
   }
 }
 
@@ -87,7 +91,7 @@ __device__ __forceinline__ void silu_bwd2(uint32_t dh2, uint32_t g2, uint32_t u2
 }
 
 __global__ void k_silu_bwd_v8(const uint4* __restrict__ dh, const uint4* __restrict__ g, const uint4* __restrict__ u,
-                              uint4* __restrict__ dU, uint4* __restrict__ dG, long long nv,
+                              uint4* __restrict__ dU, uint4* __restrict__ dG, uint4* __restrict__ hh, long long nv,
                               const uint16_t* __restrict__ silu, const float* __restrict__ dsilu) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nv;
        i += (long long)gridDim.x * blockDim.x) {
@@ -99,6 +103,9 @@ __global__ void k_silu_bwd_v8(const uint4* __restrict__ dh, const uint4* __restr
     silu_bwd2(dv.w, gv.w, uv.w, silu, dsilu, a.w, b.w);
     dU[i] = a;
     dG[i] = b;
+    if (hh)
+      hh[i] = make_uint4(silu_mul2(gv.x, uv.x, silu), silu_mul2(gv.y, uv.y, silu), silu_mul2(gv.z, uv.z, silu),
+                         silu_mul2(gv.w, uv.w, silu));
   }
 }
 
@@ -261,15 +268,17 @@ cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* h, l
 }
 
 cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u,
-                            uint16_t* dU, uint16_t* dG, long long n, const uint16_t* silu_tab,
+                            uint16_t* dU, uint16_t* dG, uint16_t* hh, long long n, const uint16_t* silu_tab,
                             const float* dsilu_tab, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  const bool a16 = (((uintptr_t)dh | (uintptr_t)g | (uintptr_t)u | (uintptr_t)dU | (uintptr_t)dG) & 15u) == 0;
+  const bool a16 =
+      (((uintptr_t)dh | (uintptr_t)g | (uintptr_t)u | (uintptr_t)dU | (uintptr_t)dG | (uintptr_t)hh) & 15u) == 0;
   if (a16 && n % 8 == 0)
     k_silu_bwd_v8<<<grid_for(n / 8, 4096), kThreads, 0, st>>>((const uint4*)dh, (const uint4*)g, (const uint4*)u,
-                                                               (uint4*)dU, (uint4*)dG, n / 8, silu_tab, dsilu_tab);
+                                                               (uint4*)dU, (uint4*)dG, (uint4*)hh, n / 8, silu_tab,
+                                                               dsilu_tab);
   else
-    k_silu_bwd<<<grid_for(n, 4096), kThreads, 0, st>>>(dh, g, u, dU, dG, n, silu_tab, dsilu_tab);
+    k_silu_bwd<<<grid_for(n, 4096), kThreads, 0, st>>>(dh, g, u, dU, dG, hh, n, silu_tab, dsilu_tab);
   return cudaGetLastError();
 }
 

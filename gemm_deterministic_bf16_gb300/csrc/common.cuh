@@ -15,6 +15,33 @@
 
 namespace detffn {
 
+// Programmatic dependent launch.  grid_dep_wait blocks until the grid this
+// one was launched after has completed and its memory is visible (it returns
+// at once when there was no such launch); grid_dep_launch lets the next grid
+// on the stream start launching (its CTAs then wait in grid_dep_wait).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// A launch that may begin while the previous kernel on the stream finishes
+// (programmatic dependent launch); the kernel waits in grid_dep_wait before
+// touching global memory, and lets its own successor launch with
+// grid_dep_launch (which takes effect once every one of its CTAs has run it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*k)(KArgs...), dim3 grid, int threads, int smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
+
 constexpr int kLeaf = 64;        // leaf width (K positions per FP32 leaf)
 constexpr int kMaxDepth = 24;    // stack entries; enough for < 2^22 leaves
 constexpr long long kMaxK = 1ll << 27;

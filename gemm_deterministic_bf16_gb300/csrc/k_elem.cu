@@ -25,6 +25,8 @@ constexpr int kThreads = 256;
 __global__ void k_silu_mul(const uint16_t* __restrict__ g, const uint16_t* __restrict__ u,
                            uint16_t* __restrict__ h, long long rows, long long cols, long long ld,
                            const uint16_t* __restrict__ silu) {
+  grid_dep_wait();  // the inputs may be the previous kernel's outputs
+  grid_dep_launch();
   const long long n = rows * cols;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
        t += (long long)gridDim.x * blockDim.x) {
@@ -40,6 +42,8 @@ __global__ void k_silu_bwd(const uint16_t* __restrict__ dh, const uint16_t* __re
                            const uint16_t* __restrict__ u, uint16_t* __restrict__ dU,
                            uint16_t* __restrict__ dG, uint16_t* __restrict__ hh, long long n,
                            const uint16_t* __restrict__ silu, const float* __restrict__ dsilu) {
+  grid_dep_wait();  // the inputs may be the previous kernel's outputs
+  grid_dep_launch();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const uint16_t gi = g[i];
@@ -64,6 +68,8 @@ __device__ __forceinline__ uint32_t silu_mul2(uint32_t g2, uint32_t u2, const ui
 
 __global__ void k_silu_mul_v8(const uint4* __restrict__ g, const uint4* __restrict__ u, uint4* __restrict__ h,
                               long long rows, long long cv, long long ldv, const uint16_t* __restrict__ silu) {
+  grid_dep_wait();  // the inputs may be the previous kernel's outputs
+  grid_dep_launch();
   const long long n = rows * cv;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
        t += (long long)gridDim.x * blockDim.x) {
@@ -93,6 +99,8 @@ __device__ __forceinline__ void silu_bwd2(uint32_t dh2, uint32_t g2, uint32_t u2
 __global__ void k_silu_bwd_v8(const uint4* __restrict__ dh, const uint4* __restrict__ g, const uint4* __restrict__ u,
                               uint4* __restrict__ dU, uint4* __restrict__ dG, uint4* __restrict__ hh, long long nv,
                               const uint16_t* __restrict__ silu, const float* __restrict__ dsilu) {
+  grid_dep_wait();  // the inputs may be the previous kernel's outputs
+  grid_dep_launch();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nv;
        i += (long long)gridDim.x * blockDim.x) {
     const uint4 dv = __ldg(dh + i), gv = __ldg(g + i), uv = __ldg(u + i);
@@ -111,6 +119,8 @@ __global__ void k_silu_bwd_v8(const uint4* __restrict__ dh, const uint4* __restr
 
 __global__ void k_add_bf16(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
                            uint16_t* __restrict__ out, long long n) {
+  grid_dep_wait();  // the inputs may be the previous kernel's outputs
+  grid_dep_launch();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
     out[i] = f2bf(__fadd_rn(bf2f(a[i]), bf2f(b[i])));
@@ -167,6 +177,8 @@ __device__ __forceinline__ float rank_tree(const float* v) {
 // VEC = bytes moved per input per step (16, 4 or the element size).
 template <int DT, int N, int VEC>
 __global__ void __launch_bounds__(kThreads) k_rank_tree(Bufs B, long long count) {
+  grid_dep_wait();  // the inputs may be the previous kernel's outputs
+  grid_dep_launch();
   constexpr int E = Elt<DT>::kBytes;
   constexpr int PER = VEC / E;  // elements per step
   constexpr bool kScalar = (VEC == E);
@@ -229,10 +241,9 @@ cudaError_t launch_rt_n(const Bufs& B, long long count, int align_all, int sm_co
   const long long cap = (long long)sm_count * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (vec == 16) k_rank_tree<DT, N, 16><<<(unsigned)blocks, kThreads, 0, st>>>(B, count);
-  else if (vec == 4) k_rank_tree<DT, N, 4><<<(unsigned)blocks, kThreads, 0, st>>>(B, count);
-  else k_rank_tree<DT, N, E><<<(unsigned)blocks, kThreads, 0, st>>>(B, count);
-  return cudaGetLastError();
+  if (vec == 16) return launch_dependent(k_rank_tree<DT, N, 16>, dim3((unsigned)blocks), kThreads, 0, st, B, count);
+  if (vec == 4) return launch_dependent(k_rank_tree<DT, N, 4>, dim3((unsigned)blocks), kThreads, 0, st, B, count);
+  return launch_dependent(k_rank_tree<DT, N, E>, dim3((unsigned)blocks), kThreads, 0, st, B, count);
 }
 
 template <int DT>
@@ -260,11 +271,10 @@ cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* h, l
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   const bool a16 = (((uintptr_t)g | (uintptr_t)u | (uintptr_t)h) & 15u) == 0;
   if (a16 && cols % 8 == 0 && ld % 8 == 0)
-    k_silu_mul_v8<<<grid_for(rows * cols / 8, 4096), kThreads, 0, st>>>(
-        (const uint4*)g, (const uint4*)u, (uint4*)h, rows, cols / 8, ld / 8, silu_tab);
-  else
-    k_silu_mul<<<grid_for(rows * cols, 4096), kThreads, 0, st>>>(g, u, h, rows, cols, ld, silu_tab);
-  return cudaGetLastError();
+    return launch_dependent(k_silu_mul_v8, dim3(grid_for(rows * cols / 8, 4096)), kThreads, 0, st, (const uint4*)g,
+                            (const uint4*)u, (uint4*)h, rows, cols / 8, ld / 8, silu_tab);
+  return launch_dependent(k_silu_mul, dim3(grid_for(rows * cols, 4096)), kThreads, 0, st, g, u, h, rows, cols, ld,
+                          silu_tab);
 }
 
 cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u,
@@ -274,19 +284,17 @@ cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_
   const bool a16 =
       (((uintptr_t)dh | (uintptr_t)g | (uintptr_t)u | (uintptr_t)dU | (uintptr_t)dG | (uintptr_t)hh) & 15u) == 0;
   if (a16 && n % 8 == 0)
-    k_silu_bwd_v8<<<grid_for(n / 8, 4096), kThreads, 0, st>>>((const uint4*)dh, (const uint4*)g, (const uint4*)u,
-                                                               (uint4*)dU, (uint4*)dG, (uint4*)hh, n / 8, silu_tab,
-                                                               dsilu_tab);
-  else
-    k_silu_bwd<<<grid_for(n, 4096), kThreads, 0, st>>>(dh, g, u, dU, dG, hh, n, silu_tab, dsilu_tab);
-  return cudaGetLastError();
+    return launch_dependent(k_silu_bwd_v8, dim3(grid_for(n / 8, 4096)), kThreads, 0, st, (const uint4*)dh,
+                            (const uint4*)g, (const uint4*)u, (uint4*)dU, (uint4*)dG, (uint4*)hh, n / 8, silu_tab,
+                            dsilu_tab);
+  return launch_dependent(k_silu_bwd, dim3(grid_for(n, 4096)), kThreads, 0, st, dh, g, u, dU, dG, hh, n, silu_tab,
+                          dsilu_tab);
 }
 
 cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out, long long n,
                             cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  k_add_bf16<<<grid_for(n, 4096), kThreads, 0, st>>>(a, b, out, n);
-  return cudaGetLastError();
+  return launch_dependent(k_add_bf16, dim3(grid_for(n, 4096)), kThreads, 0, st, a, b, out, n);
 }
 
 cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long count, int dtype,

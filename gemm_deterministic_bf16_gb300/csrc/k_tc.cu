@@ -360,6 +360,12 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
   // A wait of an earlier launch ran out (the status word is set until the
   // caller reads it): its outputs, which may be this launch's inputs, are
   // unfinished, so this launch does nothing.
+  // Programmatic dependent launch: the previous kernel on the stream (whose
+  // outputs may be this one's inputs, or whose inputs this one may
+  // overwrite) has completed past this wait; the next may begin launching
+  // (its CTAs cannot share an SM with this kernel's, and wait in turn).
+  grid_dep_launch();
+  grid_dep_wait();
   if (__syncthreads_or(a.status != nullptr && *(volatile int*)a.status != 0)) return;
 
   if (threadIdx.x == 0) {
@@ -711,8 +717,8 @@ cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cuda
   const int slots = sm_count;
   const int grid = units < slots ? units : slots;
   const int smem = TcGeo<BN>::smem_for(a.G, a.E, a.nstage);
-  k_tc<BN, GG, DUMP><<<grid, TcGeo<BN>::THREADS, smem, st>>>(m[0], m[1], m[2], m[3], m[4], m[5], a);
-  return cudaGetLastError();
+  return launch_dependent(k_tc<BN, GG, DUMP>, dim3(grid), TcGeo<BN>::THREADS, smem, st, m[0], m[1], m[2], m[3], m[4],
+                          m[5], a);
 }
 
 template <int BN>

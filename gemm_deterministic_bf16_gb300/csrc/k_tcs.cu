@@ -862,25 +862,6 @@ bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool 
 
 namespace {
 
-// A launch that may begin while the previous kernel on the stream finishes
-// (programmatic dependent launch); the kernels wait in grid_dep_wait before
-// touching global memory.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*k)(KArgs...), dim3 grid, int threads, int smem, cudaStream_t st,
-                             Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
-}
-
 cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo, uint16_t* h, const uint16_t* silu,
                        void* scratch, size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump,
                        long long oss) {

@@ -105,12 +105,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 constexpr long long kDefaultSpin = 1ll << 26;  // polls; far beyond any legitimate wait
 
-// Programmatic dependent launch.  grid_dep_wait blocks until the grid this
-// one was launched after has completed and its memory is visible (it returns
-// at once when there was no such launch); grid_dep_launch lets the next grid
-// on the stream start launching (its CTAs then wait in grid_dep_wait).
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 }  // namespace detffn
 

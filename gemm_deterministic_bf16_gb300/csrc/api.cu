@@ -1032,10 +1032,14 @@ extern "C" detffn_status detffn_backward(detffn_handle h, const void* x, const v
       pg[s] = w.cgs + (long long)s * M * H;
       pu[s] = w.cus + (long long)s * M * H;
     }
-    TRY(rank_tree_bf16(h, pg, k, w.cg, M * H, st));
-    TRY(rank_tree_bf16(h, pu, k, w.cu, M * H, st));
+    // Both rank trees and the gate-then-up addition in one pass (the same
+    // arithmetic as the two trees and then the addition).
+    TRY(timed(h, st, "rank_tree_add", 2.0 * (2 * k + 1) * M * H, 0.0, [&] {
+      return cu(launch_rank_tree_add_bf16(pg, pu, k, dX, M * H, h->sm_count, st));
+    }));
+  } else {
+    TRY(add_bf16(h, w.cg, w.cu, (uint16_t*)dX, M * H, st));
   }
-  TRY(add_bf16(h, w.cg, w.cu, (uint16_t*)dX, M * H, st));
   return wgrads(h, f, (const uint16_t*)x, (const uint16_t*)dOut, w.h, dU, dG, (uint16_t*)dWg,
                 (uint16_t*)dWu, (uint16_t*)dWd, M, H, I, st);
 }

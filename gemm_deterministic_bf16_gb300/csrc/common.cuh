@@ -102,6 +102,9 @@ cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* h, l
 cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u,
                             uint16_t* dU, uint16_t* dG, uint16_t* hh, long long n, const uint16_t* silu_tab,
                             const float* dsilu_tab, cudaStream_t st);
+// out = rne_bf16(T(g[0..n)) + T(u[0..n))), T the BF16 rank tree (n in {2,4,8}).
+cudaError_t launch_rank_tree_add_bf16(const void* const* g, const void* const* u, int n, void* out, long long count,
+                                      int sm_count, cudaStream_t st);
 // out = rne(a + b).
 cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out, long long n,
                             cudaStream_t st);

@@ -229,6 +229,74 @@ __global__ void __launch_bounds__(kThreads) k_rank_tree(Bufs B, long long count)
   }
 }
 
+// dX = rne_bf16(T(g) + T(u)) where T is the rank tree over the shard
+// partials of the gate contribution (g[0..N)) and of the up contribution
+// (u[0..N)): both trees and the gate-then-up addition in one pass (the same
+// arithmetic as two rank-tree passes and the addition).
+struct Bufs2 {
+  const unsigned char* g[8];
+  const unsigned char* u[8];
+  unsigned char* out;
+};
+
+template <int N, bool VEC16>
+__global__ void __launch_bounds__(kThreads) k_rank_tree_add(Bufs2 B, long long count) {
+  grid_dep_wait();  // the inputs may be the previous kernel's outputs
+  grid_dep_launch();
+  using EB = Elt<DETFFN_BF16>;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long t0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long nvec = VEC16 ? count / 8 : 0;
+  for (long long v = t0; v < nvec; v += stride) {
+    uint32_t wg[N][4], wu[N][4];
+#pragma unroll
+    for (int s = 0; s < N; ++s) {
+      const uint4 a = __ldcs(reinterpret_cast<const uint4*>(B.g[s]) + v);
+      const uint4 b = __ldcs(reinterpret_cast<const uint4*>(B.u[s]) + v);
+      wg[s][0] = a.x; wg[s][1] = a.y; wg[s][2] = a.z; wg[s][3] = a.w;
+      wu[s][0] = b.x; wu[s][1] = b.y; wu[s][2] = b.z; wu[s][3] = b.w;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t r = 0;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float xg[N], xu[N];
+#pragma unroll
+        for (int s = 0; s < N; ++s) {
+          xg[s] = EB::from_bits((wg[s][q] >> (16 * hf)) & 0xFFFFu);
+          xu[s] = EB::from_bits((wu[s][q] >> (16 * hf)) & 0xFFFFu);
+        }
+        const float sum = __fadd_rn(rank_tree<DETFFN_BF16, N>(xg), rank_tree<DETFFN_BF16, N>(xu));
+        r |= (EB::to_bits(sum) & 0xFFFFu) << (16 * hf);
+      }
+      o[q] = r;
+    }
+    reinterpret_cast<uint4*>(B.out)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  for (long long i = nvec * 8 + t0; i < count; i += stride) {
+    float xg[N], xu[N];
+#pragma unroll
+    for (int s = 0; s < N; ++s) {
+      xg[s] = EB::ld(B.g[s], i);
+      xu[s] = EB::ld(B.u[s], i);
+    }
+    EB::st(B.out, i, __fadd_rn(rank_tree<DETFFN_BF16, N>(xg), rank_tree<DETFFN_BF16, N>(xu)));
+  }
+}
+
+template <int N>
+cudaError_t launch_rta_n(const Bufs2& B, long long count, bool v16, int sm_count, cudaStream_t st) {
+  const long long work = v16 ? count / 8 + count % 8 : count;
+  long long blocks = (work + kThreads - 1) / kThreads;
+  const long long cap = (long long)sm_count * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (v16) return launch_dependent(k_rank_tree_add<N, true>, dim3((unsigned)blocks), kThreads, 0, st, B, count);
+  return launch_dependent(k_rank_tree_add<N, false>, dim3((unsigned)blocks), kThreads, 0, st, B, count);
+}
+
 template <int DT, int N>
 cudaError_t launch_rt_n(const Bufs& B, long long count, int align_all, int sm_count, cudaStream_t st) {
   constexpr int E = Elt<DT>::kBytes;
@@ -264,6 +332,27 @@ unsigned grid_for(long long n, int cap_blocks) {
 }
 
 }  // namespace
+
+cudaError_t launch_rank_tree_add_bf16(const void* const* g, const void* const* u, int n, void* out, long long count,
+                                      int sm_count, cudaStream_t st) {
+  if (count <= 0) return cudaSuccess;
+  if (!g || !u || !out || !(n == 2 || n == 4 || n == 8)) return cudaErrorInvalidValue;
+  Bufs2 B{};
+  uintptr_t al = (uintptr_t)out;
+  for (int s = 0; s < n; ++s) {
+    if (!g[s] || !u[s]) return cudaErrorInvalidValue;
+    B.g[s] = static_cast<const unsigned char*>(g[s]);
+    B.u[s] = static_cast<const unsigned char*>(u[s]);
+    al |= (uintptr_t)g[s] | (uintptr_t)u[s];
+  }
+  B.out = static_cast<unsigned char*>(out);
+  const bool v16 = (al & 15u) == 0;
+  switch (n) {
+    case 2: return launch_rta_n<2>(B, count, v16, sm_count, st);
+    case 4: return launch_rta_n<4>(B, count, v16, sm_count, st);
+    default: return launch_rta_n<8>(B, count, v16, sm_count, st);
+  }
+}
 
 cudaError_t launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* h, long long rows,
                             long long cols, long long ld, const uint16_t* silu_tab,

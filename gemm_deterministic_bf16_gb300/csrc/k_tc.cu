@@ -151,6 +151,7 @@ struct TcArgs {
   int L, G, E;      // leaves, bottom group size, levels above the groups
   int nstage;
   int num_m, num_n;
+  int gm;           // tile order: blocks of gm row tiles, row tile fastest within a block
   int np;           // problems in this launch (1 or 2; the second uses tmA2/tmB2 and out2)
   int b_mn;         // B stored [K][C] (C contiguous): MN-major B tiles (BN = 128 only)
   int o_tma;        // row-major outputs may leave through TMA stores (maps tmO, tmO2)
@@ -163,6 +164,19 @@ struct TcArgs {
   int stall;        // test only: the producer issues no loads
   float* dump;      // leaf dump (DUMP instances): [np][R][C][L] FP32 leaves
 };
+
+// Output tile of unit index t.  The tiles are taken in blocks of gm row
+// tiles, row tile fastest within a block: the CTAs at work at one time then
+// share a block of A rows (kept in L2 while the block sweeps the columns)
+// and a few column tiles of B, so that neither operand is re-read from DRAM
+// once per wave of tiles when A is larger than L2 can keep.
+__device__ __forceinline__ void tile_of(int t, const TcArgs& a, int& tm, int& tn) {
+  const int per = a.gm * a.num_n;
+  const int mb = t / per, idx = t - mb * per;
+  const int rows = min(a.gm, a.num_m - mb * a.gm);
+  tm = mb * a.gm + idx % rows;
+  tn = idx / rows;
+}
 
 // Writes the COLS columns of one row held as packed BF16 pairs: element i goes
 // to base[row_off + (c0 + i) * ld_c] for c0 + i < C.
@@ -419,7 +433,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
       for (int u = blockIdx.x; u < units && ok && p < nprod; u += gridDim.x) {
         const int pb = u % a.np, v = u / a.np;
         const int t = v;
-        const int tm = t % a.num_m, tn = t / a.num_m;
+        int tm, tn;
+        tile_of(t, a, tm, tn);
         const CUtensorMap* mA = pb ? &tmA2 : &tmA;
         const CUtensorMap* mB = pb ? &tmB2 : &tmB;
         int j3 = 0;  // j % 3
@@ -543,7 +558,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
       // binary counter above them (levels >= 2) lives in shared memory.
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const int pb = u % a.np, t = u / a.np;
-        const int tm = t % a.num_m, tn = t / a.num_m;
+        int tm, tn;
+        tile_of(t, a, tm, tn);
         uint16_t* const outp = pb ? a.out2 : a.out;
         const long long r = (long long)tm * BM + row;
         for (int q = 0; q < Q && ok; q += 4) {
@@ -622,7 +638,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
       // leaf, rounded once, is the output.
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const int pb = u % a.np, t = u / a.np;
-        const int tm = t % a.num_m, tn = t / a.num_m;
+        int tm, tn;
+        tile_of(t, a, tm, tn);
         uint16_t* const outp = pb ? a.out2 : a.out;
         const long long r = (long long)tm * BM + row;
         uint32_t root[T::WORDS];
@@ -789,6 +806,16 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   if (np > 1 && (pr[1].b_mn != pr[0].b_mn || pr[1].a_mn != pr[0].a_mn)) return cudaErrorInvalidValue;
   a.num_m = (int)((R + BM - 1) / BM);
   a.num_n = (int)((C + bn - 1) / bn);
+  // Row blocks: all row tiles when A is small enough for L2 to keep whole
+  // (then B is read once); otherwise as many row tiles as 48 MB of A holds.
+  {
+    const bool shared_a = np > 1 && pr[1].A == pr[0].A && pr[1].lda == pr[0].lda;
+    const double row_bytes = (double)BM * (double)K * 2.0 * (shared_a ? 1 : np);
+    const double keep = 48.0 * (1 << 20);
+    int gm = a.num_m;
+    if (row_bytes * a.num_m > keep) gm = (int)(keep / row_bytes);
+    a.gm = gm < 1 ? 1 : (gm > a.num_m ? a.num_m : gm);
+  }
   a.E = E;
   a.L = (int)L;
   a.out = pr[0].out;

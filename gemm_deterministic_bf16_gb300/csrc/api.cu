@@ -1091,22 +1091,71 @@ extern "C" detffn_status detffn_wgrad_chunked(detffn_handle h, int n_chunks,
   }
   Arena a(ws);
   ChunkWs w = plan_chunked(a, M, H, I, f == kTensor, h->sm_count);
-  // Gather the chunks in logical token order, then run the row-wise stages
-  // chunk by chunk on their own rows.
+  // The row-wise stages (dh, dU, dG and h) run chunk by chunk on each
+  // chunk's own rows, reading gate and up where the caller keeps them (a
+  // copy first only where a chunk is not 16-byte aligned, which the tensor
+  // kernels' TMA needs); x and dOut are gathered in logical token order for
+  // the weight gradients, whose K axis is the tokens.
+  // On the tensor family the weight gradients read x and dOut chunk by chunk
+  // as one K axis (a tensor map per chunk), without gathering them, when
+  // every chunk but the last holds a multiple of 64 tokens (no leaf spans
+  // two chunks), there are at most 8 non-empty chunks and all are 16-byte
+  // aligned; otherwise they are gathered in logical order first.
+  TcKChunks kx, kd;
+  bool virt = f == kTensor && H % 8 == 0 && M > 64;
+  for (int c = 0; c < n_chunks && virt; ++c) {
+    const long long t = chunk_tokens[c];
+    if (t == 0) continue;
+    if (kx.n == kMaxKChunks || !aligned16(x_chunks[c]) || !aligned16(dOut_chunks[c])) {
+      virt = false;
+      break;
+    }
+    kx.base[kx.n] = (const uint16_t*)x_chunks[c];
+    kd.base[kd.n] = (const uint16_t*)dOut_chunks[c];
+    kx.tokens[kx.n++] = t;
+    kd.tokens[kd.n++] = t;
+  }
+  for (int c = 0; c + 1 < kx.n && virt; ++c)
+    if (kx.tokens[c] % kLeaf) virt = false;
   long long r0 = 0;
   for (int c = 0; c < n_chunks; ++c) {
     const long long t = chunk_tokens[c];
     if (t == 0) continue;
-    TRYCU(cudaMemcpyAsync(w.x + r0 * H, x_chunks[c], (size_t)(2 * t * H), cudaMemcpyDeviceToDevice, st));
-    TRYCU(cudaMemcpyAsync(w.dO + r0 * H, dOut_chunks[c], (size_t)(2 * t * H), cudaMemcpyDeviceToDevice, st));
-    TRYCU(cudaMemcpyAsync(w.g + r0 * I, gate_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
-    TRYCU(cudaMemcpyAsync(w.u + r0 * I, up_chunks[c], (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
-    TRY(rowwise_bwd(h, f, w.dO + r0 * H, (const uint16_t*)Wd, w.g + r0 * I, w.u + r0 * I,
-                    w.dh + r0 * I, w.dU + r0 * I, w.dG + r0 * I, w.h + r0 * I, t, H, I, st, w.tcs));
+    if (!virt) {
+      TRYCU(cudaMemcpyAsync(w.x + r0 * H, x_chunks[c], (size_t)(2 * t * H), cudaMemcpyDeviceToDevice, st));
+      TRYCU(cudaMemcpyAsync(w.dO + r0 * H, dOut_chunks[c], (size_t)(2 * t * H), cudaMemcpyDeviceToDevice, st));
+    }
+    const uint16_t* dOc = virt ? (const uint16_t*)dOut_chunks[c] : w.dO + r0 * H;
+    const uint16_t* gc = (const uint16_t*)gate_chunks[c];
+    const uint16_t* uc = (const uint16_t*)up_chunks[c];
+    if (!aligned16(gc) || !aligned16(uc)) {
+      TRYCU(cudaMemcpyAsync(w.g + r0 * I, gc, (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
+      TRYCU(cudaMemcpyAsync(w.u + r0 * I, uc, (size_t)(2 * t * I), cudaMemcpyDeviceToDevice, st));
+      gc = w.g + r0 * I;
+      uc = w.u + r0 * I;
+    }
+    TRY(rowwise_bwd(h, f, dOc, (const uint16_t*)Wd, gc, uc, w.dh + r0 * I, w.dU + r0 * I,
+                    w.dG + r0 * I, w.h + r0 * I, t, H, I, st, w.tcs));
     r0 += t;
   }
-  return wgrads(h, f, w.x, w.dO, w.h, w.dU, w.dG, (uint16_t*)dWg, (uint16_t*)dWu, (uint16_t*)dWd,
-                M, H, I, st);
+  if (!virt)
+    return wgrads(h, f, w.x, w.dO, w.h, w.dU, w.dG, (uint16_t*)dWg, (uint16_t*)dWu, (uint16_t*)dWd, M, H, I,
+                  st);
+  // dWd[n, i] = T_m(dOut[m, n], h[m, i]): A = dOut, MN-major, in chunks.
+  kd.op = 1;
+  const double bd = 2.0 * ((double)H * M + (double)I * M + (double)H * I);
+  TRY(timed(h, st, "tc_tree_gemm", bd, 2.0 * H * I * M, [&] {
+    const TcProblem pd{kd.base[0], H, w.h, I, (uint16_t*)dWd, true, true};
+    return cu(launch_tc_gemms(&pd, 1, H, I, M, I, 1, h->wt, h->sm_count, st, nullptr, &kd));
+  }));
+  // dWg[i, n] = T_m(dG[m, i], x[m, n]), dWu likewise: B = x, MN-major, in chunks.
+  kx.op = 2;
+  const double bg = 4.0 * ((double)I * M + (double)H * M + (double)I * H);
+  return timed(h, st, "tc_tree_gemm", bg, 4.0 * I * H * M, [&] {
+    const TcProblem pg[2] = {{w.dG, I, kx.base[0], H, (uint16_t*)dWg, true, true},
+                             {w.dU, I, kx.base[0], H, (uint16_t*)dWu, true, true}};
+    return cu(launch_tc_gemms(pg, 2, I, H, M, H, 1, h->wt, h->sm_count, st, nullptr, &kx));
+  });
 }
 
 extern "C" detffn_status detffn_rank_tree_reduce(const void* const* inputs, int n, void* out,

@@ -163,6 +163,14 @@ struct TcArgs {
   long long spin;
   int stall;        // test only: the producer issues no loads
   float* dump;      // leaf dump (DUMP instances): [np][R][C][L] FP32 leaves
+  int kc_op;        // K axis in chunks (0: no; 1: operand A, 2: operand B), read through the chunk maps
+  int kc_n;
+  int kc_leaf[kMaxKChunks];  // first leaf of chunk c
+};
+
+// The tensor maps of a chunked operand, one per chunk.
+struct KChunkMaps {
+  CUtensorMap m[kMaxKChunks];
 };
 
 // Output tile of unit index t.  The tiles are taken in blocks of gm row
@@ -355,7 +363,8 @@ template <int BN, int GG, bool DUMP>
 __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-         const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2, const TcArgs a) {
+         const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2, const TcArgs a,
+         const __grid_constant__ KChunkMaps kcm) {
   using T = TcGeo<BN>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -457,17 +466,34 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
             // Three-leaf groups are loaded leaf 1, leaf 2, leaf 0 (see the
             // epilogue): slot j3 = j % 3 of a group holds leaf (j3 + 1) % 3.
             const int x = (GG == 3 ? (j3 == 2 ? j - 2 : j + 1) : j) * BK;
+            // A chunked K axis: the leaf's chunk (a leaf never spans two) and
+            // the K coordinate within it.
+            const CUtensorMap* lA = mA;
+            const CUtensorMap* lB = mB;
+            int xa = x, xb = x;
+            if (a.kc_op) {
+              int c = 0;
+              while (c + 1 < a.kc_n && a.kc_leaf[c + 1] * BK <= x) ++c;
+              const int xc = x - a.kc_leaf[c] * BK;
+              if (a.kc_op == 1) {
+                lA = &kcm.m[c];
+                xa = xc;
+              } else {
+                lB = &kcm.m[c];
+                xb = xc;
+              }
+            }
             if (a.a_mn) {  // two boxes of 64 (R) x 64 (K)
-              tma_load_2d(st, mA, tm * BM, x, &bars->full[s]);
-              tma_load_2d(st + T::A_BYTES / 2, mA, tm * BM + BM / 2, x, &bars->full[s]);
+              tma_load_2d(st, lA, tm * BM, xa, &bars->full[s]);
+              tma_load_2d(st + T::A_BYTES / 2, lA, tm * BM + BM / 2, xa, &bars->full[s]);
             } else {
-              tma_load_2d(st, mA, x, tm * BM, &bars->full[s]);
+              tma_load_2d(st, lA, xa, tm * BM, &bars->full[s]);
             }
             if (a.b_mn) {  // two boxes of 64 (C) x 64 (K)
-              tma_load_2d(st + T::A_BYTES, mB, tn * BN, x, &bars->full[s]);
-              tma_load_2d(st + T::A_BYTES + T::B_BYTES / 2, mB, tn * BN + BN / 2, x, &bars->full[s]);
+              tma_load_2d(st + T::A_BYTES, lB, tn * BN, xb, &bars->full[s]);
+              tma_load_2d(st + T::A_BYTES + T::B_BYTES / 2, lB, tn * BN + BN / 2, xb, &bars->full[s]);
             } else {
-              tma_load_2d(st + T::A_BYTES, mB, x, tn * BN, &bars->full[s]);
+              tma_load_2d(st + T::A_BYTES, lB, xb, tn * BN, &bars->full[s]);
             }
           }
           __syncwarp();
@@ -716,7 +742,7 @@ bool tc_make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long
 namespace {
 
 template <int BN, int GG, bool DUMP>
-cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cudaStream_t st) {
+cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, const KChunkMaps& kcm, int sm_count, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t setup_err = cudaSuccess;
   std::call_once(once, [] {
@@ -735,23 +761,23 @@ cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, int sm_count, cuda
   const int grid = units < slots ? units : slots;
   const int smem = TcGeo<BN>::smem_for(a.G, a.E, a.nstage);
   return launch_dependent(k_tc<BN, GG, DUMP>, dim3(grid), TcGeo<BN>::THREADS, smem, st, m[0], m[1], m[2], m[3], m[4],
-                          m[5], a);
+                          m[5], a, kcm);
 }
 
 template <int BN>
-cudaError_t launch_bn(const CUtensorMap* m, const TcArgs& a, int sm_count, cudaStream_t st) {
+cudaError_t launch_bn(const CUtensorMap* m, const TcArgs& a, const KChunkMaps& kcm, int sm_count, cudaStream_t st) {
   if (a.dump) {
     switch (a.G) {
-      case 1: return launch_bng<BN, 1, true>(m, a, sm_count, st);
-      case 2: return launch_bng<BN, 2, true>(m, a, sm_count, st);
-      case 3: return launch_bng<BN, 3, true>(m, a, sm_count, st);
+      case 1: return launch_bng<BN, 1, true>(m, a, kcm, sm_count, st);
+      case 2: return launch_bng<BN, 2, true>(m, a, kcm, sm_count, st);
+      case 3: return launch_bng<BN, 3, true>(m, a, kcm, sm_count, st);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (a.G) {
-    case 1: return launch_bng<BN, 1, false>(m, a, sm_count, st);
-    case 2: return launch_bng<BN, 2, false>(m, a, sm_count, st);
-    case 3: return launch_bng<BN, 3, false>(m, a, sm_count, st);
+    case 1: return launch_bng<BN, 1, false>(m, a, kcm, sm_count, st);
+    case 2: return launch_bng<BN, 2, false>(m, a, kcm, sm_count, st);
+    case 3: return launch_bng<BN, 3, false>(m, a, kcm, sm_count, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -785,7 +811,7 @@ bool tc_tree_shape(long long L, int* G, int* E) {
 
 cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long C, long long K,
                             long long ld_r, long long ld_c, const Waits& wt, int sm_count, cudaStream_t st,
-                            float* dump) {
+                            float* dump, const TcKChunks* kc) {
   constexpr int bn = 128;
   if (R <= 0 || C <= 0) return cudaSuccess;
   if (np < 1 || np > 2) return cudaErrorInvalidValue;
@@ -853,7 +879,31 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
     if (!amap || !bmap)
       return cudaErrorInvalidValue;
   }
-  return launch_bn<bn>(m, a, sm_count, st);
+  // A chunked K axis: one map per chunk, each over the chunk's own tokens
+  // (rows), so that TMA zero-fills the tail of the last leaf exactly as the
+  // map of a gathered operand would.
+  KChunkMaps kcm{};
+  a.kc_op = 0;
+  a.kc_n = 0;
+  if (kc && kc->op) {
+    if (kc->n < 1 || kc->n > kMaxKChunks || (kc->op == 1 && !a.a_mn) || (kc->op == 2 && !a.b_mn) ||
+        (kc->op != 1 && kc->op != 2))
+      return cudaErrorInvalidValue;
+    const long long ld = kc->op == 1 ? pr[0].lda : pr[0].ldb;
+    const long long inner = kc->op == 1 ? R : C;
+    long long start = 0;
+    for (int c = 0; c < kc->n; ++c) {
+      const long long t = kc->tokens[c];
+      if (t < 1 || ((uintptr_t)kc->base[c] & 15u) || (c + 1 < kc->n && t % BK)) return cudaErrorInvalidValue;
+      a.kc_leaf[c] = (int)(start / BK);
+      if (!tc_make_map(&kcm.m[c], kc->base[c], t, inner, ld, BK)) return cudaErrorInvalidValue;
+      start += t;
+    }
+    if (start != K) return cudaErrorInvalidValue;
+    a.kc_op = kc->op;
+    a.kc_n = kc->n;
+  }
+  return launch_bn<bn>(m, a, kcm, sm_count, st);
 }
 
 cudaError_t launch_tc_gemm(const uint16_t* A, long long lda, const uint16_t* B, long long ldb,

@@ -25,10 +25,24 @@ struct TcProblem {
   bool a_mn = false;  // A given as [K, R] (R contiguous, row stride lda), read MN-major
 };
 
+// A contraction whose K axis (the tokens, for the weight gradients) is given
+// in chunks of one operand: chunk c holds tokens [sum of earlier chunks,
+// + tokens[c]) at base[c] (same row stride as the operand, 16-byte aligned),
+// read through a tensor map of its own -- one virtual K axis, no gather copy.
+// Every chunk but the last holds a multiple of 64 tokens (a leaf never spans
+// two chunks); op 1: operand A (read MN-major), op 2: operand B (MN-major).
+constexpr int kMaxKChunks = 8;
+struct TcKChunks {
+  int op = 0;
+  int n = 0;
+  const uint16_t* base[kMaxKChunks] = {};
+  long long tokens[kMaxKChunks] = {};
+};
+
 // Up to two same-shaped contractions in one launch (their tiles interleave).
 cudaError_t launch_tc_gemms(const TcProblem* problems, int np, long long R, long long C, long long K,
                             long long ld_r, long long ld_c, const Waits& wt, int sm_count, cudaStream_t st,
-                            float* dump = nullptr);
+                            float* dump = nullptr, const TcKChunks* kc = nullptr);
 
 // out[r*ld_r + c*ld_c] = T_K(A[r, :], B[c, :]) for r < R, c < C; A and B are
 // K-contiguous BF16 with row strides lda, ldb (elements, multiples of 8) and

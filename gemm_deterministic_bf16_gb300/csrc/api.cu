@@ -777,6 +777,17 @@ detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const u
     // gate and up in one launch (their tiles interleave over the SMs).
     const Strided BG{Wg + s * w * H, H, 1}, BU{Wu + s * w * H, H, 1};
     if (!tc_operands_ok(X) || !tc_operands_ok(BG) || !tc_operands_ok(BU)) return DETFFN_ERR_ALIGN;
+    if (M <= 32 && w % 64 == 0) {
+      // Few tokens, whole tiles: 64 rows of Wg over the same 64 rows of Wu
+      // per CTA, which forms both trees' roots and h itself (one launch, no
+      // pieces); gate and up are stored only when the caller keeps them.
+      const double bytes = 2.0 * (2.0 * w * H + (double)M * H + (keep ? 3.0 : 1.0) * M * w);
+      return timed(h, st, "tcs_gateup", bytes, 4.0 * M * w * H, [&] {
+        return cu(launch_tcs_gateup_stacked(M, w, H, BG.p, BU.p, H, x, H, keep ? gate + s * w : nullptr,
+                                            keep ? up + s * w : nullptr, hh + s * w, I, h->d_silu, h->sm_count,
+                                            h->wt, st));
+      });
+    }
     if (M <= 32) {
       // Few tokens: the top of both trees fused with SiLU * up; gate and up
       // are stored only when the caller keeps them.

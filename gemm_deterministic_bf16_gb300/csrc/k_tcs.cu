@@ -78,19 +78,23 @@ __host__ __device__ inline int top_smem(bool fused, int E, int cap) {
 static_assert(kTcsMaxLv >= REG_LV, "stack levels");
 static_assert(MAX_STAGES <= kNBuf, "stage reuse is read off the leaf barriers");
 
-__host__ __device__ inline int stages_for(int E) {
+// Stacked gate/up (see the streaming kernel): the up half of a tile's roots
+// passes to the gate half through shared memory, 64 rows x WORDS words.
+constexpr int XCH_BYTES = 64 * WORDS * 4;
+__host__ __device__ inline int stages_for(int E, bool stacked = false) {
   const int lv = E > REG_LV ? E - REG_LV : 0;
-  int n = (MAX_SMEM - 1024 - BAR_BYTES - lv * LV_BYTES) / STAGE;
+  int n = (MAX_SMEM - 1024 - BAR_BYTES - lv * LV_BYTES - (stacked ? XCH_BYTES : 0)) / STAGE;
   if (n > MAX_STAGES) n = MAX_STAGES;
   return n & ~1;  // even: stage s is always filled by producer s % 2
 }
-__host__ __device__ inline int smem_for(int E, int ns) {
+__host__ __device__ inline int smem_for(int E, int ns, bool stacked = false) {
   const int lv = E > REG_LV ? E - REG_LV : 0;
-  return 1024 + ns * STAGE + lv * LV_BYTES + BAR_BYTES;
+  return 1024 + ns * STAGE + lv * LV_BYTES + BAR_BYTES + (stacked ? XCH_BYTES : 0);
 }
 
 struct Bars {
   uint64_t full[MAX_STAGES], accf[kNBuf], acce[kNBuf], fin;
+  uint64_t xfull, xempty;  // stacked gate/up: the up half's roots are in the exchange buffer / have been read
   uint32_t tmem_slot;
   int abort;
 };
@@ -116,6 +120,15 @@ struct TcsArgs {
   int stall;        // test only: the producers issue no loads
   int L;            // leaves per tree (G * 2^E)
   float* dump;      // leaf dump (DUMP instances): [np][R][C][L] FP32 leaves
+  // Stacked gate/up (direct mode, one problem): a tile's 128 MMA rows are 64
+  // rows of Wg (map tmW) over the same 64 rows of Wu (map tmW2), so that one
+  // CTA holds both roots of every (row, token) of its tiles and writes
+  // h = bf16(bf16(SiLU(gate)) * up) itself (gate and up too, to out0 / out1
+  // where not null), with no pieces and no second kernel.  C counts the rows
+  // of each weight; tiles are 64 rows.
+  int stacked;
+  uint16_t* hout;
+  const uint16_t* silu;
 };
 
 // First group of CTA b's range.  Direct mode deals whole tiles: segment
@@ -177,8 +190,11 @@ namespace {
 // K-major (one box) or, for weights stored [K][C], MN-major (two boxes of
 // 64 rows x 64 K).
 __device__ __forceinline__ void load_w(unsigned char* dst, const CUtensorMap* mW, int k, int t, uint64_t* bar,
-                                       uint64_t pol, int mn) {
-  if (mn) {
+                                       uint64_t pol, int mn, const CUtensorMap* mW2 = nullptr) {
+  if (mW2) {  // stacked: 64 rows of each weight (two boxes of 64 rows x 64 K)
+    tma_load_2d_hint(dst, mW, k, t * (BM / 2), bar, pol);
+    tma_load_2d_hint(dst + A_BYTES / 2, mW2, k, t * (BM / 2), bar, pol);
+  } else if (mn) {
     tma_load_2d_hint(dst, mW, t * BM, k, bar, pol);
     tma_load_2d_hint(dst + A_BYTES / 2, mW, t * BM + BM / 2, k, bar, pol);
   } else {
@@ -201,6 +217,7 @@ __global__ void __maxnreg__(128)
   unsigned char* stages = smem;
   uint32_t* stk = reinterpret_cast<uint32_t*>(smem + NS * STAGE);
   Bars* bars = reinterpret_cast<Bars*>(smem + NS * STAGE + slv * LV_BYTES);
+  uint32_t* xch = reinterpret_cast<uint32_t*>(smem + NS * STAGE + slv * LV_BYTES + BAR_BYTES);  // [word][64 rows]
   volatile int* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -223,6 +240,8 @@ __global__ void __maxnreg__(128)
       mbar_init(&bars->acce[b], kEpiWarps);
     }
     mbar_init(&bars->fin, 1);
+    mbar_init(&bars->xfull, 2);   // the two warps of the up half (lanes 64..127)
+    mbar_init(&bars->xempty, 2);  // the two warps of the gate half (lanes 0..63)
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -267,7 +286,7 @@ __global__ void __maxnreg__(128)
           if ((int)(it % kProd) != warp) continue;
           if (elect_one()) {
             mbar_arrive_expect_tx(&bars->full[it], (uint32_t)STAGE);
-            load_w(stages + it * STAGE, mW, k0 + j * BK, g.t, &bars->full[it], pol, a.w_mn);
+            load_w(stages + it * STAGE, mW, k0 + j * BK, g.t, &bars->full[it], pol, a.w_mn, a.stacked ? &tmW2 : nullptr);
           }
           __syncwarp();
         }
@@ -305,7 +324,7 @@ __global__ void __maxnreg__(128)
         if (!a.stall && elect_one()) {
           if (reuse) {
             mbar_arrive_expect_tx(&bars->full[st], (uint32_t)STAGE);
-            load_w(dst, mW, k0 + j * BK, g.t, &bars->full[st], pol, a.w_mn);
+            load_w(dst, mW, k0 + j * BK, g.t, &bars->full[st], pol, a.w_mn, a.stacked ? &tmW2 : nullptr);
           }
           tma_load_2d(dst + A_BYTES, mX, k0 + j * BK, 0, &bars->full[st]);
         }
@@ -365,6 +384,7 @@ __global__ void __maxnreg__(128)
     uint16_t* const myslots = direct ? nullptr : a.slots + (size_t)blockIdx.x * a.cap * PIECE;
     uint32_t lc = 0;  // leaves consumed (kNBuf is a power of two)
     int np_out = 0;  // pieces written
+    uint32_t xk = 0;  // stacked: tiles exchanged (the phase of xfull / xempty)
     bool ok = true;
     uint32_t reg_lv[REG_LV][WORDS];
     for (long long w = w0; w < w1 && ok;) {
@@ -444,20 +464,13 @@ __global__ void __maxnreg__(128)
         // child waits on the stack for its right sibling.
         int at = q;
         bool live = true;
+        bool tile_root = false;
 #pragma unroll
         for (int m = 0; m <= kTcsMaxLv; ++m) {
           if (live) {
-            if (m == a.E) {  // the whole tile: its root
-              if (direct) {
-                const long long c = (long long)sg.t * BM + row;
-                uint16_t* o = (sg.pb ? a.out1 : a.out0) + sg.q * a.oss;
-                if (c < a.C)
-#pragma unroll
-                  for (int i = 0; i < BN; ++i)
-                    if (i < a.R) o[i * a.ldo + c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
-              } else {
-                emit_piece(myslots, np_out, a.cap, row, root);
-              }
+            if (m == a.E) {  // the whole tile: its root (stored below, outside the unrolled loop)
+              if (direct) tile_root = true;
+              else emit_piece(myslots, np_out, a.cap, row, root);
               live = false;
             } else if (((at >> m) & 1) && at - (1 << m) >= qa) {
 #pragma unroll
@@ -480,6 +493,54 @@ __global__ void __maxnreg__(128)
               pend |= 1u << m;
               live = false;
             }
+          }
+        }
+        if (tile_root) {
+          if (a.stacked) {
+            // Rows 0..63 hold gate, rows 64..127 up, of weight rows
+            // 64 t + (row mod 64): the up half hands its roots over in
+            // shared memory, the gate half forms h.  Every wait is bounded.
+            const long long c = (long long)sg.t * (BM / 2) + (row & (BM / 2 - 1));
+            const uint32_t ph = xk & 1u;
+            if (row >= BM / 2) {
+              if (!wait_or_abort(&bars->xempty, ph ^ 1u, limit, abort_flag, a.status)) ok = false;
+              if (ok) {
+  #pragma unroll
+                for (int i = 0; i < WORDS; ++i) xch[i * (BM / 2) + (row - BM / 2)] = root[i];
+                if (a.out1 && c < a.C)
+  #pragma unroll
+                  for (int i = 0; i < BN; ++i)
+                    if (i < a.R) a.out1[i * a.ldo + c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->xfull);
+          } else {
+              if (!wait_or_abort(&bars->xfull, ph, limit, abort_flag, a.status)) ok = false;
+              if (ok && c < a.C) {
+  #pragma unroll
+                for (int i = 0; i < WORDS; ++i) {
+                  const uint32_t g2 = root[i], u2 = xch[i * (BM / 2) + row];
+                  const float h0 = __fmul_rn(bf2f(__ldg(a.silu + (g2 & 0xFFFFu))), __uint_as_float(u2 << 16));
+                  const float h1 = __fmul_rn(bf2f(__ldg(a.silu + (g2 >> 16))), __uint_as_float(u2 & 0xFFFF0000u));
+                  if (2 * i < a.R) a.hout[(2 * i) * a.ldo + c] = f2bf(h0);
+                  if (2 * i + 1 < a.R) a.hout[(2 * i + 1) * a.ldo + c] = f2bf(h1);
+                  if (a.out0) {
+                    if (2 * i < a.R) a.out0[(2 * i) * a.ldo + c] = (uint16_t)(g2 & 0xFFFFu);
+                    if (2 * i + 1 < a.R) a.out0[(2 * i + 1) * a.ldo + c] = (uint16_t)(g2 >> 16);
+                  }
+                }
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->xempty);
+          }
+          ++xk;
+          } else {
+          const long long c = (long long)sg.t * BM + row;
+          uint16_t* o = (sg.pb ? a.out1 : a.out0) + sg.q * a.oss;
+          if (c < a.C)
+#pragma unroll
+            for (int i = 0; i < BN; ++i)
+              if (i < a.R) o[i * a.ldo + c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
           }
         }
       }
@@ -862,6 +923,31 @@ bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool 
 
 namespace {
 
+// One-time kernel attributes (shared memory limits and carve-out).
+cudaError_t tcs_setup() {
+  static std::once_flag once;
+  static cudaError_t setup_err = cudaSuccess;
+  std::call_once(once, [] {
+    cudaError_t e = cudaSuccess;
+    void (*ks[6])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) = {
+        k_tcs<1, false>, k_tcs<2, false>, k_tcs<3, false>, k_tcs<1, true>, k_tcs<2, true>, k_tcs<3, true>};
+    for (auto k : ks) {
+      // Two CTAs per SM: all of their shared memory, at most 113 KB each.
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    }
+    void (*tops[2])(TcsTopArgs) = {k_tcs_top<false>, k_tcs_top<true>};
+    for (auto k : tops) {
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    }
+    setup_err = e;
+  });
+  return setup_err;
+}
+
 cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo, uint16_t* h, const uint16_t* silu,
                        void* scratch, size_t scratch_bytes, const Waits& wt, cudaStream_t st, float* dump,
                        long long oss) {
@@ -883,26 +969,7 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
         !tc_make_map(&m[2 * p + 1], q.X, plan.R, Ktot, q.ldx, BN))
       return cudaErrorInvalidValue;
   }
-  static std::once_flag once;
-  static cudaError_t setup_err = cudaSuccess;
-  std::call_once(once, [] {
-    cudaError_t e = cudaSuccess;
-    void (*ks[6])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) = {
-        k_tcs<1, false>, k_tcs<2, false>, k_tcs<3, false>, k_tcs<1, true>, k_tcs<2, true>, k_tcs<3, true>};
-    for (auto k : ks) {
-      // Two CTAs per SM: all of their shared memory, at most 113 KB each.
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    }
-    void (*tops[2])(TcsTopArgs) = {k_tcs_top<false>, k_tcs_top<true>};
-    for (auto k : tops) {
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    }
-    setup_err = e;
-  });
+  const cudaError_t setup_err = tcs_setup();
   if (setup_err != cudaSuccess) return setup_err;
   TcsArgs a{};
   a.R = plan.R;
@@ -963,6 +1030,52 @@ cudaError_t launch_tcs(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   for (int p = 0; p < plan.np; ++p)
     if (!pr[p].out) return cudaErrorInvalidValue;
   return tcs_launch(plan, pr, ldo, nullptr, nullptr, scratch, scratch_bytes, wt, st, dump, oss);
+}
+
+cudaError_t launch_tcs_gateup_stacked(long long R, long long C, long long K, const uint16_t* Wg, const uint16_t* Wu,
+                                      long long ldw, const uint16_t* X, long long ldx, uint16_t* gate, uint16_t* up,
+                                      uint16_t* h, long long ldo, const uint16_t* silu, int sm_count, const Waits& wt,
+                                      cudaStream_t st) {
+  if (R < 1 || R > BN || C < 1 || C % (BM / 2) || !h || !silu || (ldw % 8) || (ldx % 8) ||
+      (((uintptr_t)Wg | (uintptr_t)Wu | (uintptr_t)X) & 15u))
+    return cudaErrorInvalidValue;
+  TcsPlan plan;
+  // Tiles of 64 rows of each weight = 128 MMA rows: the plan of 2C rows.
+  if (!tcs_plan(R, 2 * C, K, 1, 2 * sm_count, true, &plan, 1)) return cudaErrorInvalidValue;
+  plan.nstage = stages_for(plan.E, true);
+  if (plan.nstage < 2) return cudaErrorInvalidValue;
+  CUtensorMap m[4];
+  if (!tc_make_map(&m[0], Wg, C, K, ldw, BM / 2) || !tc_make_map(&m[2], Wu, C, K, ldw, BM / 2) ||
+      !tc_make_map(&m[1], X, R, K, ldx, BN))
+    return cudaErrorInvalidValue;
+  m[3] = m[1];
+  const cudaError_t setup_err = tcs_setup();
+  if (setup_err != cudaSuccess) return setup_err;
+  TcsArgs a{};
+  a.R = (int)R;
+  a.C = (int)C;
+  a.G = plan.G;
+  a.E = plan.E;
+  a.np = 1;
+  a.ns = 1;
+  a.ksh = K;
+  a.T = plan.T;
+  a.W = plan.W;
+  a.nstage = plan.nstage;
+  a.out0 = gate;
+  a.out1 = up;
+  a.ldo = ldo;
+  a.status = wt.status;
+  a.spin = wt.spin;
+  a.stall = wt.stall;
+  a.L = plan.G << plan.E;
+  a.stacked = 1;
+  a.hout = h;
+  a.silu = silu;
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) =
+      plan.G == 1 ? k_tcs<1, false> : plan.G == 2 ? k_tcs<2, false> : k_tcs<3, false>;
+  return launch_dependent(kern, dim3(plan.P), kThreads, smem_for(plan.E, plan.nstage, true), st, m[0], m[1], m[2],
+                          m[3], a);
 }
 
 cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* pr, uint16_t* h, long long ldo,

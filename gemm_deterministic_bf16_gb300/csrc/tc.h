@@ -107,6 +107,15 @@ cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* problems, u
                               const uint16_t* silu, void* scratch, size_t scratch_bytes, const Waits& wt,
                               cudaStream_t st);
 
+// Gate and up of R <= 32 tokens with h = bf16(bf16(SiLU(gate)) * up) in one
+// launch and no scratch: every CTA takes whole tiles of 64 rows of Wg over the
+// same 64 rows of Wu (the MMA's 128 rows) and writes h, and gate and up where
+// not null, itself.  C (rows of each weight) a multiple of 64.
+cudaError_t launch_tcs_gateup_stacked(long long R, long long C, long long K, const uint16_t* Wg, const uint16_t* Wu,
+                                      long long ldw, const uint16_t* X, long long ldx, uint16_t* gate, uint16_t* up,
+                                      uint16_t* h, long long ldo, const uint16_t* silu, int sm_count, const Waits& wt,
+                                      cudaStream_t st);
+
 // Host check of the few-token kernels' piece decomposition and fold codes
 // over every tile of up to 2^max_levels groups; returns the failed cases.
 unsigned long long tcs_selfcheck_pieces(int max_levels);

@@ -11,6 +11,7 @@ from .detffn import (  # noqa: F401
     PATH_EXACT, PATH_TENSOR, DetFFNError, detffn_backward, detffn_forward,
     detffn_forward_sharded, detffn_get_status, detffn_rank_tree_reduce, detffn_silu_tables,
     detffn_cvt_f32_bf16, detffn_forward_decode_noalloc, detffn_forward_decode_noalloc_status,
+    detffn_forward_decode_noalloc_test_waits,
     detffn_profile_read, detffn_profiling, detffn_selfcheck_node_add, detffn_selfcheck_pieces,
     detffn_tree_gemm, detffn_tree_gemm_leaves,
     detffn_wgrad_chunked,

@@ -13,6 +13,7 @@
 // Host code may not use the arrays' names as device addresses (on the host
 // they are stand-ins), so a one-time set-up per device looks up their device
 // addresses with cudaGetSymbolAddress, with that device current.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -51,6 +52,10 @@ struct DevState {
 };
 constexpr int kNaMaxDevices = 64;
 std::mutex g_na_mu;
+// Test settings of the failure path (detffn_forward_decode_noalloc_test_waits):
+// 0 and 0, the normal path, unless a test set them.
+std::atomic<long long> g_na_test_spin{0};
+std::atomic<int> g_na_test_stall{0};
 DevState g_na_dev[kNaMaxDevices];
 
 // Once per device, with that device current: resolve the arrays' device
@@ -115,7 +120,7 @@ extern "C" detffn_status detffn_forward_decode_noalloc(const void* x, const void
   a.N = I; a.K = H; a.M = (int)M;
   a.part = part; a.cnt = tickets;
   a.out = hh; a.ldo = I;
-  a.silu = d->silu; a.status = status; a.spin_limit = 0;
+  a.silu = d->silu; a.status = status; a.spin_limit = g_na_test_spin.load(); a.stall = g_na_test_stall.load();
   if (launch_decode_exact(a, d->sm_count, st) != cudaSuccess) return DETFFN_ERR_CUDA;
 
   DecArgs b{};
@@ -124,7 +129,7 @@ extern "C" detffn_status detffn_forward_decode_noalloc(const void* x, const void
   b.N = H; b.K = I; b.M = (int)M;
   b.part = part; b.cnt = tickets;
   b.out = static_cast<uint16_t*>(out); b.ldo = H;
-  b.silu = d->silu; b.status = status; b.spin_limit = 0;
+  b.silu = d->silu; b.status = status; b.spin_limit = g_na_test_spin.load(); b.stall = g_na_test_stall.load();
   if (launch_decode_exact(b, d->sm_count, st) != cudaSuccess) return DETFFN_ERR_CUDA;
   return DETFFN_OK;
 }
@@ -141,4 +146,11 @@ extern "C" detffn_status detffn_forward_decode_noalloc_status(void* stream) {
   if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DETFFN_ERR_CUDA;
   if (v != 0 && cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return DETFFN_ERR_CUDA;
   return v == 0 ? DETFFN_OK : (detffn_status)v;
+}
+
+extern "C" detffn_status detffn_forward_decode_noalloc_test_waits(long long spin_limit, int stall) {
+  if (spin_limit < 0 || (stall != 0 && stall != 1)) return DETFFN_ERR_INVALID_ARG;
+  g_na_test_spin.store(spin_limit);
+  g_na_test_stall.store(stall);
+  return DETFFN_OK;
 }

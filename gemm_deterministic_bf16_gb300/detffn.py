@@ -384,6 +384,15 @@ def detffn_forward_decode_noalloc_status(device=None, stream=None):
         return L.detffn_forward_decode_noalloc_status(_stream(dev, stream))
 
 
+def detffn_forward_decode_noalloc_test_waits(spin_limit=0, stall=0):
+    """Test-only settings of the allocation-free decode forward's bounded
+    waits: (0, 0) is the normal path; stall=1 makes its waits run out."""
+    L = lib()
+    L.detffn_forward_decode_noalloc_test_waits.argtypes = [_ll, ctypes.c_int]
+    L.detffn_forward_decode_noalloc_test_waits.restype = ctypes.c_int
+    _check(L.detffn_forward_decode_noalloc_test_waits(spin_limit, stall), "detffn_forward_decode_noalloc_test_waits")
+
+
 def detffn_selfcheck_pieces(max_levels=8):
     """Failed cases of the host check of the few-token kernels' piece
     decomposition and fold codes (no GPU needed)."""

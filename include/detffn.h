@@ -286,6 +286,14 @@ DETFFN_API detffn_status detffn_forward_decode_noalloc(const void *x, const void
  * nothing; may perform the same one-time set-up as the first call. */
 DETFFN_API detffn_status detffn_forward_decode_noalloc_status(void *stream);
 
+/* For tests of the failure path only: later detffn_forward_decode_noalloc
+ * calls in this process poll their bounded waits at most spin_limit times
+ * (0: the default bound) and, with stall = 1, issue no copies, so that their
+ * first wait runs out and the status word reports DETFFN_ERR_TIMEOUT without
+ * any fault.  (0, 0), the state at load, is the normal path.  A negative
+ * spin_limit or another stall value: DETFFN_ERR_INVALID_ARG. */
+DETFFN_API detffn_status detffn_forward_decode_noalloc_test_waits(long long spin_limit, int stall);
+
 /* Diagnostic: out[i] = the BF16 rounding (to nearest, ties to even) of the
  * FP32 value in[i], computed on the device with the very conversion every
  * kernel of the library uses for leaves, nodes and stage boundaries; a test

@@ -8,8 +8,9 @@ stops at the first failure has already run every other test.  It checks, on
 two calls in a row, that the output equals detffn_forward's on the exact path
 bit for bit (the tolerance of the exact path is 0 mismatching elements) and
 that the call's status word reports no timeout; that the output equals the
-CPU oracle's; and that sizes beyond its limits are refused before anything
-is launched.
+CPU oracle's; that a bounded wait that runs out (a test setting, no fault)
+is reported by the call's status word; and that sizes beyond its limits are
+refused before anything is launched.
 """
 import numpy as np
 import pytest
@@ -55,6 +56,35 @@ def test_noalloc_matches_oracle(G, oracle_mod):
     ref = oracle_mod.ffn_forward(d["x"], d["Wg"], d["Wu"], d["Wd"])
     assert mismatches(host(out), ref["out"]) == 0
     assert G.detffn_forward_decode_noalloc_status() == 0
+
+
+def test_noalloc_reports_a_wait_that_ran_out(G):
+    """The failure path, without any fault: with the test setting that makes
+    the kernels issue no copies and a short poll limit, the first wait of the
+    gate/up launch runs out; the call's status word reports DETFFN_ERR_TIMEOUT
+    (the down launch returns at entry, leaving out untouched), reading it
+    clears it, and the next normal call is bit-identical to detffn_forward."""
+    M, H, I = 2, 1024, 3072
+    d = ffn_inputs(M, H, I, seed=81, with_dout=False)
+    t = {n: dev(v) for n, v in d.items()}
+    ref = host(G.detffn_forward(t["x"], t["Wg"], t["Wu"], t["Wd"], path=G.PATH_EXACT))
+    out = torch.zeros(M, H, dtype=torch.bfloat16, device="cuda")
+    assert G.detffn_forward_decode_noalloc_status() == 0
+    G.detffn_forward_decode_noalloc_test_waits(spin_limit=4096, stall=1)
+    try:
+        G.detffn_forward_decode_noalloc(t["x"], t["Wg"], t["Wu"], t["Wd"], out=out)
+        torch.cuda.synchronize()
+        assert G.detffn_forward_decode_noalloc_status() == 7           # DETFFN_ERR_TIMEOUT
+        assert G.detffn_forward_decode_noalloc_status() == 0           # read and cleared
+        assert not torch.any(out.view(torch.int16) != 0).item()        # the down launch did nothing
+    finally:
+        G.detffn_forward_decode_noalloc_test_waits(0, 0)
+    G.detffn_forward_decode_noalloc(t["x"], t["Wg"], t["Wu"], t["Wd"], out=out)
+    torch.cuda.synchronize()
+    assert G.detffn_forward_decode_noalloc_status() == 0
+    assert mismatches(host(out), ref) == 0
+    with pytest.raises(G.DetFFNError):
+        G.detffn_forward_decode_noalloc_test_waits(spin_limit=-1)
 
 
 def test_noalloc_rejects_sizes_beyond_limits(G):

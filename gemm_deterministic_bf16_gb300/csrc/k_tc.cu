@@ -359,7 +359,7 @@ __device__ __forceinline__ bool group_root(EpiCtx& e, const TcArgs& a, Emit&& em
   return true;
 }
 
-template <int BN, int GG, bool DUMP>
+template <int BN, int GG, bool DUMP, bool KC>
 __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
             const CUtensorMap* lA = mA;
             const CUtensorMap* lB = mB;
             int xa = x, xb = x;
-            if (a.kc_op) {
+            if constexpr (KC) {  // (a separate instance: the branch costs the producer loop a few %)
               int c = 0;
               while (c + 1 < a.kc_n && a.kc_leaf[c + 1] * BK <= x) ++c;
               const int xc = x - a.kc_leaf[c] * BK;
@@ -741,18 +741,18 @@ bool tc_make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long
 
 namespace {
 
-template <int BN, int GG, bool DUMP>
+template <int BN, int GG, bool DUMP, bool KC>
 cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, const KChunkMaps& kcm, int sm_count, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t setup_err = cudaSuccess;
   std::call_once(once, [] {
-    setup_err = cudaFuncSetAttribute(k_tc<BN, GG, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    setup_err = cudaFuncSetAttribute(k_tc<BN, GG, DUMP, KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      TcGeo<BN>::MAX_SMEM);
     if (setup_err != cudaSuccess) return;
     // The in-kernel register split (setmaxnreg) hands over exactly the
     // launch's registers; with any other count it could not complete.
     cudaFuncAttributes fa;
-    setup_err = cudaFuncGetAttributes(&fa, k_tc<BN, GG, DUMP>);
+    setup_err = cudaFuncGetAttributes(&fa, k_tc<BN, GG, DUMP, KC>);
     if (setup_err == cudaSuccess && fa.numRegs != kRegsLaunch) setup_err = cudaErrorInvalidConfiguration;
   });
   if (setup_err != cudaSuccess) return setup_err;
@@ -760,7 +760,7 @@ cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, const KChunkMaps& 
   const int slots = sm_count;
   const int grid = units < slots ? units : slots;
   const int smem = TcGeo<BN>::smem_for(a.G, a.E, a.nstage);
-  return launch_dependent(k_tc<BN, GG, DUMP>, dim3(grid), TcGeo<BN>::THREADS, smem, st, m[0], m[1], m[2], m[3], m[4],
+  return launch_dependent(k_tc<BN, GG, DUMP, KC>, dim3(grid), TcGeo<BN>::THREADS, smem, st, m[0], m[1], m[2], m[3], m[4],
                           m[5], a, kcm);
 }
 
@@ -768,16 +768,19 @@ template <int BN>
 cudaError_t launch_bn(const CUtensorMap* m, const TcArgs& a, const KChunkMaps& kcm, int sm_count, cudaStream_t st) {
   if (a.dump) {
     switch (a.G) {
-      case 1: return launch_bng<BN, 1, true>(m, a, kcm, sm_count, st);
-      case 2: return launch_bng<BN, 2, true>(m, a, kcm, sm_count, st);
-      case 3: return launch_bng<BN, 3, true>(m, a, kcm, sm_count, st);
+      case 1: return launch_bng<BN, 1, true, false>(m, a, kcm, sm_count, st);
+      case 2: return launch_bng<BN, 2, true, false>(m, a, kcm, sm_count, st);
+      case 3: return launch_bng<BN, 3, true, false>(m, a, kcm, sm_count, st);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (a.G) {
-    case 1: return launch_bng<BN, 1, false>(m, a, kcm, sm_count, st);
-    case 2: return launch_bng<BN, 2, false>(m, a, kcm, sm_count, st);
-    case 3: return launch_bng<BN, 3, false>(m, a, kcm, sm_count, st);
+    case 1: return a.kc_op ? launch_bng<BN, 1, false, true>(m, a, kcm, sm_count, st)
+                      : launch_bng<BN, 1, false, false>(m, a, kcm, sm_count, st);
+    case 2: return a.kc_op ? launch_bng<BN, 2, false, true>(m, a, kcm, sm_count, st)
+                      : launch_bng<BN, 2, false, false>(m, a, kcm, sm_count, st);
+    case 3: return a.kc_op ? launch_bng<BN, 3, false, true>(m, a, kcm, sm_count, st)
+                      : launch_bng<BN, 3, false, false>(m, a, kcm, sm_count, st);
     default: return cudaErrorInvalidValue;
   }
 }

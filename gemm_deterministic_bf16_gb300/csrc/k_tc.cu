@@ -74,6 +74,7 @@ template <int GG> struct Roles {
 constexpr int kRegsLaunch = 168, kRegsLow = 56, kRegsHigh = 224;
 static_assert(128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch, "register split");
 constexpr int kMaxLv = 6;  // up to Q = 64 bottom groups
+constexpr int kLayRuntime = 4;  // operand layouts read at run time (leaf-dump instances)
 
 // One CTA per SM, 8 epilogue warps (two per TMEM lane quarter, BN/2 columns
 // each), 512/BN leaf buffers.
@@ -359,13 +360,17 @@ __device__ __forceinline__ bool group_root(EpiCtx& e, const TcArgs& a, Emit&& em
   return true;
 }
 
-template <int BN, int GG, bool DUMP, bool KC>
+template <int BN, int GG, bool DUMP, bool KC, int LAY>
 __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
          const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2, const TcArgs a,
          const __grid_constant__ KChunkMaps kcm) {
   using T = TcGeo<BN>;
+  // Operand layouts: fixed by the instance (LAY = a_mn + 2 b_mn) except in
+  // the leaf-dump instances (LAY = kLayRuntime), which read them from a.
+  const bool amn = LAY == kLayRuntime ? a.a_mn != 0 : (LAY & 1) != 0;
+  const bool bmn = LAY == kLayRuntime ? a.b_mn != 0 : (LAY & 2) != 0;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int NS = a.nstage;
@@ -483,13 +488,13 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
                 xb = xc;
               }
             }
-            if (a.a_mn) {  // two boxes of 64 (R) x 64 (K)
+            if (amn) {  // two boxes of 64 (R) x 64 (K)
               tma_load_2d(st, lA, tm * BM, xa, &bars->full[s]);
               tma_load_2d(st + T::A_BYTES / 2, lA, tm * BM + BM / 2, xa, &bars->full[s]);
             } else {
               tma_load_2d(st, lA, xa, tm * BM, &bars->full[s]);
             }
-            if (a.b_mn) {  // two boxes of 64 (C) x 64 (K)
+            if (bmn) {  // two boxes of 64 (C) x 64 (K)
               tma_load_2d(st + T::A_BYTES, lB, tn * BN, xb, &bars->full[s]);
               tma_load_2d(st + T::A_BYTES + T::B_BYTES / 2, lB, tn * BN + BN / 2, xb, &bars->full[s]);
             } else {
@@ -517,9 +522,9 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
       // are independent accumulations, so the issuers' MMAs may reach the
       // tensor pipe in any order.
       static_assert(T::NBUF >= 3, "a group of up to 3 leaves in flight");
-      const uint32_t idesc = idesc_bf16(BM, BN) | (a.b_mn ? kIdescTransB : 0u) | (a.a_mn ? kIdescTransA : 0u);
-      const uint32_t bstep = a.b_mn ? 128u : 2u;  // K = 16 step in descriptor units
-      const uint32_t astep = a.a_mn ? 128u : 2u;
+      const uint32_t idesc = idesc_bf16(BM, BN) | (bmn ? kIdescTransB : 0u) | (amn ? kIdescTransA : 0u);
+      const uint32_t bstep = bmn ? 128u : 2u;  // K = 16 step in descriptor units
+      const uint32_t astep = amn ? 128u : 2u;
       const int mine = blockIdx.x < units ? (units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
       const long long nunit = (long long)mine * (a.L / RL::UNIT);
       Ring rs, rb;  // pipeline stage; TMEM leaf buffer
@@ -542,8 +547,8 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t da = a.a_mn ? smem_desc_sw128_mn(stages + s * T::STAGE) : smem_desc_sw128(stages + s * T::STAGE);
-        const uint64_t db = a.b_mn ? smem_desc_sw128_mn(stages + s * T::STAGE + T::A_BYTES)
+        const uint64_t da = amn ? smem_desc_sw128_mn(stages + s * T::STAGE) : smem_desc_sw128(stages + s * T::STAGE);
+        const uint64_t db = bmn ? smem_desc_sw128_mn(stages + s * T::STAGE + T::A_BYTES)
                                    : smem_desc_sw128(stages + s * T::STAGE + T::A_BYTES);
         if (elect_one()) {
   #pragma unroll
@@ -741,18 +746,18 @@ bool tc_make_map(CUtensorMap* m, const uint16_t* base, long long rows, long long
 
 namespace {
 
-template <int BN, int GG, bool DUMP, bool KC>
+template <int BN, int GG, bool DUMP, bool KC, int LAY>
 cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, const KChunkMaps& kcm, int sm_count, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t setup_err = cudaSuccess;
   std::call_once(once, [] {
-    setup_err = cudaFuncSetAttribute(k_tc<BN, GG, DUMP, KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    setup_err = cudaFuncSetAttribute(k_tc<BN, GG, DUMP, KC, LAY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      TcGeo<BN>::MAX_SMEM);
     if (setup_err != cudaSuccess) return;
     // The in-kernel register split (setmaxnreg) hands over exactly the
     // launch's registers; with any other count it could not complete.
     cudaFuncAttributes fa;
-    setup_err = cudaFuncGetAttributes(&fa, k_tc<BN, GG, DUMP, KC>);
+    setup_err = cudaFuncGetAttributes(&fa, k_tc<BN, GG, DUMP, KC, LAY>);
     if (setup_err == cudaSuccess && fa.numRegs != kRegsLaunch) setup_err = cudaErrorInvalidConfiguration;
   });
   if (setup_err != cudaSuccess) return setup_err;
@@ -760,27 +765,35 @@ cudaError_t launch_bng(const CUtensorMap* m, const TcArgs& a, const KChunkMaps& 
   const int slots = sm_count;
   const int grid = units < slots ? units : slots;
   const int smem = TcGeo<BN>::smem_for(a.G, a.E, a.nstage);
-  return launch_dependent(k_tc<BN, GG, DUMP, KC>, dim3(grid), TcGeo<BN>::THREADS, smem, st, m[0], m[1], m[2], m[3], m[4],
+  return launch_dependent(k_tc<BN, GG, DUMP, KC, LAY>, dim3(grid), TcGeo<BN>::THREADS, smem, st, m[0], m[1], m[2], m[3], m[4],
                           m[5], a, kcm);
+}
+
+template <int BN, int GG>
+cudaError_t launch_lay(const CUtensorMap* m, const TcArgs& a, const KChunkMaps& kcm, int sm_count, cudaStream_t st) {
+  if (a.kc_op) return launch_bng<BN, GG, false, true, 3>(m, a, kcm, sm_count, st);  // chunked: both MN-major
+  switch (a.a_mn + 2 * a.b_mn) {
+    case 0: return launch_bng<BN, GG, false, false, 0>(m, a, kcm, sm_count, st);
+    case 1: return launch_bng<BN, GG, false, false, 1>(m, a, kcm, sm_count, st);
+    case 2: return launch_bng<BN, GG, false, false, 2>(m, a, kcm, sm_count, st);
+    default: return launch_bng<BN, GG, false, false, 3>(m, a, kcm, sm_count, st);
+  }
 }
 
 template <int BN>
 cudaError_t launch_bn(const CUtensorMap* m, const TcArgs& a, const KChunkMaps& kcm, int sm_count, cudaStream_t st) {
   if (a.dump) {
     switch (a.G) {
-      case 1: return launch_bng<BN, 1, true, false>(m, a, kcm, sm_count, st);
-      case 2: return launch_bng<BN, 2, true, false>(m, a, kcm, sm_count, st);
-      case 3: return launch_bng<BN, 3, true, false>(m, a, kcm, sm_count, st);
+      case 1: return launch_bng<BN, 1, true, false, kLayRuntime>(m, a, kcm, sm_count, st);
+      case 2: return launch_bng<BN, 2, true, false, kLayRuntime>(m, a, kcm, sm_count, st);
+      case 3: return launch_bng<BN, 3, true, false, kLayRuntime>(m, a, kcm, sm_count, st);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (a.G) {
-    case 1: return a.kc_op ? launch_bng<BN, 1, false, true>(m, a, kcm, sm_count, st)
-                      : launch_bng<BN, 1, false, false>(m, a, kcm, sm_count, st);
-    case 2: return a.kc_op ? launch_bng<BN, 2, false, true>(m, a, kcm, sm_count, st)
-                      : launch_bng<BN, 2, false, false>(m, a, kcm, sm_count, st);
-    case 3: return a.kc_op ? launch_bng<BN, 3, false, true>(m, a, kcm, sm_count, st)
-                      : launch_bng<BN, 3, false, false>(m, a, kcm, sm_count, st);
+    case 1: return launch_lay<BN, 1>(m, a, kcm, sm_count, st);
+    case 2: return launch_lay<BN, 2>(m, a, kcm, sm_count, st);
+    case 3: return launch_lay<BN, 3>(m, a, kcm, sm_count, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -889,7 +902,9 @@ cudaError_t launch_tc_gemms(const TcProblem* pr, int np, long long R, long long 
   a.kc_op = 0;
   a.kc_n = 0;
   if (kc && kc->op) {
-    if (kc->n < 1 || kc->n > kMaxKChunks || (kc->op == 1 && !a.a_mn) || (kc->op == 2 && !a.b_mn) ||
+    // (The chunked instance reads both operands MN-major, as the weight
+    // gradients give them.)
+    if (kc->n < 1 || kc->n > kMaxKChunks || !a.a_mn || !a.b_mn ||
         (kc->op != 1 && kc->op != 2))
       return cudaErrorInvalidValue;
     const long long ld = kc->op == 1 ? pr[0].lda : pr[0].ldb;

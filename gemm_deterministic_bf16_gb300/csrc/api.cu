@@ -24,6 +24,7 @@ struct detffn_handle_s {
   uint16_t* d_silu = nullptr;   // [65536] BF16 SiLU by gate bit pattern
   float* d_dsilu = nullptr;     // [65536] FP32 SiLU' by gate bit pattern
   int* d_status = nullptr;      // device status word (bounded waits)
+  int* d_tickets = nullptr;     // tree tickets of the few-token kernels (kTcsTickets words, zero between calls)
   Waits wt;                     // the current call's wait settings (status word, poll limit, test stall)
   int flags = 0;                // the current call's option flags
   // A second stream and two events (made at creation) for the overlapped
@@ -187,6 +188,7 @@ detffn_status read_opts(const detffn_options* o, Opts* out) {
 // The wait settings the launches of one call take from its options.
 void set_waits(detffn_handle h, const Opts& o) {
   h->wt.status = h->d_status;
+  h->wt.tickets = h->d_tickets;
   h->wt.spin = o.spin_limit;
   h->wt.stall = (o.flags & DETFFN_FLAG_TEST_STALL) ? 1 : 0;
   h->flags = o.flags;
@@ -468,7 +470,7 @@ detffn_status tree_gemm(detffn_handle h, Family f, Strided A, Strided B, long lo
       const TcsProblem pr{B.p, ldb, A.p, A.rs, out, b_mn};
       return timed(h, st, "tcs_tree_gemm", bytes, 2.0 * R * C * K,
                    [&] { return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->wt, st, dump)); },
-                   p.direct ? 1 : 2);
+                   p.launches(dump == nullptr));
     }
     return timed(h, st, "tc_tree_gemm", bytes, 2.0 * R * C * K, [&] {
       return cu(launch_tc_gemm(A.p, a_mn ? A.ks : A.rs, B.p, ldb, R, C, K, out, o_rs, 1, h->wt, h->sm_count, st,
@@ -500,7 +502,7 @@ detffn_status tree_gemm2(detffn_handle h, Family f, Strided A0, Strided B0, uint
     if (!tcs_plan_fit(R, C, K, 2, h->sm_count, sc, &p)) return DETFFN_ERR_SHAPE;
     const TcsProblem pr[2] = {{B0.p, ldb0, A0.p, A0.rs, out0, b_mn}, {B1.p, ldb1, A1.p, A1.rs, out1, b_mn}};
     return timed(h, st, "tcs_tree_gemm", bytes, 4.0 * R * C * K,
-                 [&] { return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st)); }, p.direct ? 1 : 2);
+                 [&] { return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st)); }, p.launches(true));
   }
   return timed(h, st, "tc_tree_gemm", bytes, 4.0 * R * C * K, [&] {
     const TcProblem pr[2] = {{A0.p, a_mn ? A0.ks : A0.rs, B0.p, ldb0, out0, b_mn, a_mn},
@@ -528,7 +530,7 @@ detffn_status tree_gemm_k(detffn_handle h, Family f, Strided A, Strided B, long 
     const double bytes = 2.0 * ((double)R * Ksh * k + (double)C * Ksh * k + (double)R * C * k);
     return timed(h, st, "tcs_tree_gemm", bytes, 2.0 * R * C * Ksh * k, [&] {
       return cu(launch_tcs(p, &pr, o_rs, sc.p, sc.bytes, h->wt, st, nullptr, oss));
-    }, p.direct ? 1 : 2);
+    }, p.launches(true));
   }
   for (int q = 0; q < k; ++q)
     TRY(tree_gemm(h, f, kslice(A, q, Ksh), kslice(B, q, Ksh), R, C, Ksh, out + q * oss, o_rs, st, sc));
@@ -550,7 +552,7 @@ detffn_status tree_gemm2_k(detffn_handle h, Family f, Strided A0, Strided B0, ui
     const double bytes = 4.0 * ((double)R * Ksh * k + (double)C * Ksh * k + (double)R * C * k);
     return timed(h, st, "tcs_tree_gemm", bytes, 4.0 * R * C * Ksh * k, [&] {
       return cu(launch_tcs(p, pr, o_rs, sc.p, sc.bytes, h->wt, st, nullptr, oss));
-    }, p.direct ? 1 : 2);
+    }, p.launches(true));
   }
   for (int q = 0; q < k; ++q)
     TRY(tree_gemm2(h, f, kslice(A0, q, Ksh), kslice(B0, q, Ksh), out0 + q * oss, kslice(A1, q, Ksh),
@@ -679,12 +681,14 @@ detffn_status detffn_create(detffn_handle* out, int device) {
     if (cudaMalloc(&h->d_silu, 65536 * sizeof(uint16_t)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaMalloc(&h->d_dsilu, 65536 * sizeof(float)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+    if (cudaMalloc(&h->d_tickets, kTcsTickets * sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaMemcpy(h->d_silu, h->h_silu.data(), 65536 * sizeof(uint16_t), cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemcpy(h->d_dsilu, h->h_dsilu.data(), 65536 * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+        cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(h->d_tickets, 0, kTcsTickets * sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
   } while (0);
   cudaSetDevice(prev);
   if (st != DETFFN_OK) {
@@ -703,6 +707,7 @@ detffn_status detffn_destroy(detffn_handle h) {
   if (h->d_silu) cudaFree(h->d_silu);
   if (h->d_dsilu) cudaFree(h->d_dsilu);
   if (h->d_status) cudaFree(h->d_status);
+  if (h->d_tickets) cudaFree(h->d_tickets);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->side) cudaStreamDestroy(h->side);
@@ -753,6 +758,9 @@ detffn_status detffn_get_status(detffn_handle h, void* stream) {
   int v = 0;
   TRYCU(cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost));
   TRYCU(cudaMemset(h->d_status, 0, sizeof(int)));
+  // A launch that stopped on a timeout may have left trees with some of
+  // their tickets taken: start the next call from zero.
+  if (v != 0) TRYCU(cudaMemset(h->d_tickets, 0, kTcsTickets * sizeof(int)));
   return (detffn_status)v;
 }
 

@@ -81,6 +81,10 @@ struct Waits {
   int* status = nullptr;
   long long spin = 0;
   int stall = 0;
+  // The handle's tree tickets (kTcsTickets words, zero between launches):
+  // the few-token kernel's CTAs count their finished pieces of a tree there,
+  // and the last one folds them.  Null: a separate top-of-tree kernel does.
+  int* tickets = nullptr;
 };
 
 struct Strided {

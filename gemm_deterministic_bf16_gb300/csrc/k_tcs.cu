@@ -14,9 +14,12 @@
 // covers only part of a tile, the CTA folds that part into its maximal
 // aligned subtrees -- nodes of the canonical tree -- and writes them as
 // "pieces"; a second kernel folds each tile's pieces, left to right, into the
-// root.  A whole tile is one piece, its root.  Nothing in the streaming
-// kernel waits on another CTA.  Without scratch ("direct" mode) CTAs take
-// whole tiles and store the roots themselves.
+// root.  A whole tile is one piece, its root.  Where every range is one
+// aligned block and a tile has at most 8 of them ("folded trees"), no second
+// kernel runs: each CTA takes a ticket of its tile once its piece is
+// written, and the tile's last CTA folds the pieces and stores the root.
+// Nothing in the streaming kernel waits on another CTA.  Without scratch
+// ("direct" mode) CTAs take whole tiles and store the roots themselves.
 //
 // Streaming.  Two CTAs per SM.  In each, two producer warps issue the TMA
 // loads of alternate leaves, one warp issues the MMAs (4 x K=16 per 64-wide
@@ -97,6 +100,7 @@ struct Bars {
   uint64_t xfull, xempty;  // stacked gate/up: the up half's roots are in the exchange buffer / have been read
   uint32_t tmem_slot;
   int abort;
+  int last;  // folded trees: this CTA took its tree's last ticket
 };
 static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block");
 
@@ -129,6 +133,12 @@ struct TcsArgs {
   int stacked;
   uint16_t* hout;
   const uint16_t* silu;
+  // Folded trees (aligned ranges, fold_n > 0): CTA b's range is one aligned
+  // block of tree b / fold_n, its one piece in slot b * cap; the tree's last
+  // CTA to finish (tickets[tree], counted up and reset to zero by that CTA)
+  // folds the fold_n pieces into the root and stores it as in direct mode.
+  int fold_n;
+  int* tickets;
 };
 
 // First group of CTA b's range.  Direct mode deals whole tiles: segment
@@ -169,6 +179,9 @@ __device__ __forceinline__ void dump_tokens(float* d, long long crow, int t0, in
     if (t0 + i < R) d[((size_t)(t0 + i) * (size_t)C + (size_t)crow) * (size_t)L + (size_t)j] = __uint_as_float(v[i]);
 }
 
+// Barrier of the four epilogue warps alone (the other roles do not take part).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory"); }
+
 // Writes one row (all tokens) of the CTA's next piece: the row's 64 bytes
 // at [row], so that the top kernel reads a quarter row with one 16-byte load.
 __device__ __forceinline__ void emit_piece(uint16_t* slots, int& n, int cap, int row, const uint32_t (&v)[WORDS]) {
@@ -200,6 +213,57 @@ __device__ __forceinline__ void load_w(unsigned char* dst, const CUtensorMap* mW
   } else {
     tma_load_2d_hint(dst, mW, k, t * BM, bar, pol);
   }
+}
+
+// The fold of a tree's pieces by its last CTA.  src: the tree's first
+// piece (n pieces, n a power of two, at most 8, pstride 16-byte units apart;
+// the aligned blocks of the tree, left to right).  Each epilogue warp copies
+// its 32 rows of every piece (2 KB per piece, contiguous) into shared memory
+// at buf in one batch of copies, rows of 64 bytes whose four 16-byte
+// quarters are rotated by bits 1-2 of the row, so that both the copies and
+// the per-row reads below are free of bank conflicts.  Then each thread folds
+// its row, a quarter at a time: the balanced tree over the n pieces.  Token
+// i < R of the root goes to o[i * ldo]; o is null beyond the weight rows.
+__device__ __forceinline__ void fold_pieces(const uint4* src, long long pstride, int n, unsigned char* buf, int ew,
+                                            int lane, uint16_t* o, long long ldo, int R) {
+  const int row = ew * 32 + lane;
+  const uint32_t b0 = smem_u32(buf);
+#pragma unroll 1
+  for (int j = 0; j < n; ++j)
+#pragma unroll
+    for (int i = 0; i < WORDS / 4; ++i) {
+      const int u = i * 32 + lane, r = ew * 32 + (u >> 2), q = u & 3;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                       b0 + (uint32_t)((j * BM + r) * 64 + ((q ^ ((r >> 1) & 3)) * 16))),
+                   "l"(src + j * pstride + ew * 128 + u)
+                   : "memory");
+    }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+  __syncwarp();  // the warp's rows were copied by all its lanes
+  uint32_t root[WORDS];
+#pragma unroll
+  for (int q = 0; q < WORDS / 4; ++q) {
+    const unsigned char* at = buf + row * 64 + ((q ^ ((row >> 1) & 3)) * 16);
+    uint4 v[kTcsFoldMax];
+#pragma unroll
+    for (int j = 0; j < kTcsFoldMax; ++j)
+      if (j < n) v[j] = *reinterpret_cast<const uint4*>(at + j * BM * 64);
+#pragma unroll
+    for (int w = 2; w <= kTcsFoldMax; w *= 2)  // level by level: node j of the next level = v[2j] + v[2j+1]
+#pragma unroll
+      for (int j = 0; j < kTcsFoldMax / w; ++j)
+        if (j < n / w)
+          v[j] = make_uint4(add_bf16x2(v[2 * j].x, v[2 * j + 1].x), add_bf16x2(v[2 * j].y, v[2 * j + 1].y),
+                            add_bf16x2(v[2 * j].z, v[2 * j + 1].z), add_bf16x2(v[2 * j].w, v[2 * j + 1].w));
+    root[4 * q] = v[0].x;
+    root[4 * q + 1] = v[0].y;
+    root[4 * q + 2] = v[0].z;
+    root[4 * q + 3] = v[0].w;
+  }
+  if (o)
+#pragma unroll
+    for (int i = 0; i < BN; ++i)
+      if (i < R) o[i * ldo] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
 }
 
 // The streaming kernel.  Each role walks the CTA's groups in the same order:
@@ -377,9 +441,9 @@ __global__ void __maxnreg__(128)
     if (lane == 0) mbar_wait(&bars->fin, 0, kDefaultSpin, nullptr);  // before TMEM is freed (long bound)
   } else {
     // ---------------- epilogue: leaves -> group roots -> pieces ----------------
-    grid_dep_wait();  // its stores may overwrite what the previous kernel reads
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;
+    grid_dep_wait();  // its stores may overwrite what the previous kernel reads
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     uint16_t* const myslots = direct ? nullptr : a.slots + (size_t)blockIdx.x * a.cap * PIECE;
     uint32_t lc = 0;  // leaves consumed (kNBuf is a power of two)
@@ -556,6 +620,39 @@ __global__ void __maxnreg__(128)
           emit_piece(myslots, np_out, a.cap, row, v);
         }
       w = s * Q + qb;
+    }
+    if (a.fold_n > 0) {
+      // Folded trees: this CTA's piece is written; the tree's last CTA folds
+      // all of them.  Every epilogue warp reaches the two barriers, whatever
+      // happened: a warp that stopped early has set the abort flag, and a
+      // CTA that stopped takes no ticket (its tree stays unfinished, which
+      // the status word reports).  One thread orders the CTA's piece rows
+      // (after the barrier) before its ticket, and the last CTA's reads after
+      // the tickets of the others, with device-scope fences.
+      const int fold_tree = (int)(w0 / Q);  // fewer than kTcsTickets trees
+      epi_sync();
+      if (threadIdx.x == kEpi0 * 32) {
+        int last = 0;
+        if (!*abort_flag) {
+          __threadfence();
+          last = atomicAdd(a.tickets + fold_tree, 1) == a.fold_n - 1;
+          if (last) {
+            a.tickets[fold_tree] = 0;  // no other CTA of this launch takes it again
+            __threadfence();
+          }
+        }
+        bars->last = last;
+      }
+      epi_sync();
+      if (bars->last) {
+        // The pipeline stages are idle now (every load has landed and every
+        // MMA has completed); the plan checks that they hold fold_n pieces.
+        const int per = a.np * a.ns, rem = fold_tree % per;
+        const int c = (fold_tree / per) * BM + row;
+        fold_pieces(reinterpret_cast<const uint4*>(a.slots + (size_t)fold_tree * a.fold_n * a.cap * PIECE),
+                    (long long)a.cap * (PIECE / 8), a.fold_n, stages, quarter, lane,
+                    c < a.C ? ((rem % a.np) ? a.out1 : a.out0) + (rem / a.np) * a.oss + c : nullptr, a.ldo, a.R);
+      }
     }
   }
 
@@ -891,10 +988,14 @@ bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool 
     // -- so a tile's fold takes 2^E / B pieces (or its root, for B = 2^E).
     long long B = 1;
     while (r.W / B > max_ctas) B <<= 1;
-    if (B <= Q) r.P = (int)(r.W / B);
+    if (B <= Q) {
+      r.P = (int)(r.W / B);
+      if (Q / B <= kTcsFoldMax && r.W / Q <= kTcsTickets) r.fold_n = (int)(Q / B);
+    }
   }
   r.nstage = stages_for(E);
   if (r.nstage < 2) return false;
+  if (r.fold_n * PIECE * 2 > r.nstage * STAGE) r.fold_n = 0;  // the last CTA stages the pieces there
   if (direct) {
     *p = r;
     return true;
@@ -994,12 +1095,17 @@ cudaError_t tcs_launch(const TcsPlan& plan, const TcsProblem* pr, long long ldo,
   a.stall = wt.stall;
   a.L = plan.G << plan.E;
   a.dump = dump;
+  // Folded trees: the plain form (no h, no leaf dump) of aligned ranges, with
+  // the handle's tickets.
+  const bool fold = plan.fold_n > 0 && !h && !dump && wt.tickets;
+  a.fold_n = fold ? plan.fold_n : 0;
+  a.tickets = fold ? wt.tickets : nullptr;
   const int smem = smem_for(plan.E, plan.nstage);
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcsArgs) =
       dump ? (plan.G == 1 ? k_tcs<1, true> : plan.G == 2 ? k_tcs<2, true> : k_tcs<3, true>)
            : (plan.G == 1 ? k_tcs<1, false> : plan.G == 2 ? k_tcs<2, false> : k_tcs<3, false>);
   cudaError_t e = launch_dependent(kern, dim3(plan.P), kThreads, smem, st, m[0], m[1], m[2], m[3], a);
-  if (e != cudaSuccess || plan.direct) return e;
+  if (e != cudaSuccess || plan.direct || fold) return e;
   TcsTopArgs t{};
   t.R = plan.R;
   t.C = (int)plan.C;

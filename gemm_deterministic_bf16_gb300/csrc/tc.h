@@ -73,7 +73,15 @@ struct TcsPlan {
   long long C = 0, K = 0, W = 0;    // K: the contraction length of one shard
   bool direct = false;  // whole tiles per CTA, roots stored directly (no scratch, no top kernel)
   size_t scratch = 0;   // bytes of piece slots the launch needs
+  // Aligned ranges of at most kTcsFoldMax pieces per tree: each CTA's range is
+  // one aligned block (one piece), fold_n of them per tree, and the last CTA
+  // of a tree to finish folds them (no top kernel).  0: a top kernel folds.
+  int fold_n = 0;
+  // Kernels a launch takes: one, or the streaming kernel and its top kernel.
+  int launches(bool plain) const { return direct || (plain && fold_n > 0) ? 1 : 2; }
 };
+constexpr int kTcsFoldMax = 8;    // pieces per tree the last CTA folds
+constexpr int kTcsTickets = 1024; // tree tickets per handle (a fused launch has at most 2 x SMs trees)
 
 // Plans a launch on at most max_ctas CTAs (two per SM is the design point).
 // False when the shape is not covered (R > 32, or K's leaf count not 1, 2^d or

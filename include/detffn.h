@@ -110,9 +110,14 @@ enum {
 };
 
 /* Creates a handle bound to CUDA device `device`: builds the SiLU tables
- * (correctly rounded BF16 SiLU and FP32 SiLU' for all 2^16 gate values) and a
- * device status word.  *out is set only on success.  The handle may be used
- * from one host thread at a time. */
+ * (correctly rounded BF16 SiLU and FP32 SiLU' for all 2^16 gate values), a
+ * device status word and the tree tickets of the few-token kernels (4 KiB:
+ * where a tree's K range is split over several CTAs, the last of them to
+ * finish folds their subtree roots into the root).  *out is set only on
+ * success.  The handle may be used from one host thread at a time, and its
+ * calls must run in order on the GPU (one stream, or streams ordered by
+ * events): calls through one handle that overlap on the GPU share the status
+ * word and the tickets and must not be issued. */
 DETFFN_API detffn_status detffn_create(detffn_handle *out, int device);
 
 /* Frees the handle's device memory; waits for nothing.  NULL is accepted. */
@@ -327,7 +332,9 @@ DETFFN_API detffn_status detffn_selfcheck_pieces(int max_levels, unsigned long l
  * word (DETFFN_OK or DETFFN_ERR_TIMEOUT from a bounded wait).  The word is
  * sticky: once a wait has run out, every later streaming kernel launched
  * through the handle returns at entry (leaving its outputs unwritten) until
- * this call clears it, so no kernel builds on another's unfinished output. */
+ * this call clears it, so no kernel builds on another's unfinished output.
+ * On DETFFN_ERR_TIMEOUT it also clears the tree tickets (a stopped launch
+ * may have left some taken), so that the next call starts clean. */
 DETFFN_API detffn_status detffn_get_status(detffn_handle h, void *stream);
 
 /* The CUDA error behind the calling thread's last DETFFN_ERR_CUDA (a static

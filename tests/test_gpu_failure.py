@@ -39,7 +39,8 @@ def G():
 
 
 @pytest.mark.parametrize("path,M,H,I", [(1, 8, 1024, 3072),      # exact weight streaming (k_decode)
-                                        (2, 8, 1024, 3072),      # few-token tensor kernels (k_tcs)
+                                        (2, 8, 1024, 3072),      # few-token tensor kernels (k_tcs), top kernel
+                                        (2, 8, 1024, 1536),      # k_tcs, trees folded by their last CTA
                                         (2, 256, 512, 1536)])    # many-token tensor kernel (k_tc)
 def test_stalled_wait_times_out_and_recovers(G, path, M, H, I):
     d = ffn_inputs(M, H, I, seed=90 + M, with_dout=False)

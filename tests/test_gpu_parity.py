@@ -94,7 +94,12 @@ def _rand(shape, seed, scale=1.0):
     return to_bf16_bits((scale * rng.standard_normal(shape)).astype(np.float32))
 
 
+# Few-token shapes cover both ways of finishing a tree split over several
+# CTAs: its last CTA folds the pieces (2, 4, 8 per tree at the first three;
+# one, the tree itself, at (4, 24576, 128); 4 at (16, 8192, 1536)), or a top
+# kernel does (32 pieces at (1, 1024, 4096)).
 @pytest.mark.parametrize("R,C,K", [(32, 12288, 4096), (32, 4096, 12288), (8, 3072, 768), (1, 1024, 4096),
+                                   (4, 24576, 128), (16, 8192, 1536),
                                    (256, 256, 4096), (256, 128, 12288), (200, 296, 40), (130, 72, 64),
                                    (96, 384, 128)])
 def test_leaf_dump_replay_and_bound(G, oracle_mod, R, C, K):

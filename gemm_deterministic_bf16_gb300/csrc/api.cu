@@ -257,11 +257,11 @@ constexpr int kSizingSms = 152;  // SM count a workspace is sized for when no ha
 // range, which costs microseconds of host time per call at decode sizes --
 // comparable to the call's device time.  A small table keeps the recent ones.
 bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bool direct, TcsPlan* p,
-                     int ns = 1) {
+                     int ns = 1, bool whole_ok = true) {
   struct Entry {
     long long R, C, K;
     int np, ns, ctas;
-    bool direct, ok, used;
+    bool direct, whole_ok, ok, used;
     TcsPlan plan;
   };
   constexpr int kEntries = 32;
@@ -272,15 +272,15 @@ bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bo
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& e : table)
       if (e.used && e.R == R && e.C == C && e.K == K && e.np == np && e.ns == ns && e.ctas == ctas &&
-          e.direct == direct) {
+          e.direct == direct && e.whole_ok == whole_ok) {
         if (e.ok) *p = e.plan;
         return e.ok;
       }
   }
   TcsPlan plan{};
-  const bool ok = tcs_plan(R, C, K, np, ctas, direct, &plan, ns);
+  const bool ok = tcs_plan(R, C, K, np, ctas, direct, &plan, ns, whole_ok);
   std::lock_guard<std::mutex> lock(mu);
-  table[next] = Entry{R, C, K, np, ns, ctas, direct, ok, true, plan};
+  table[next] = Entry{R, C, K, np, ns, ctas, direct, whole_ok, ok, true, plan};
   next = (next + 1) % kEntries;
   if (ok) *p = plan;
   return ok;
@@ -289,18 +289,18 @@ bool tcs_plan_cached(long long R, long long C, long long K, int np, int ctas, bo
 // Piece-slot bytes of a few-token contraction over C weight rows and K (ns
 // shards of K each), two CTAs per SM.
 size_t tcs_bytes(long long C, long long K, int np, int sms, int ns = 1) {
-  TcsPlan p;
-  return tcs_plan_cached(1, C, K, np, 2 * sms, false, &p, ns) ? p.scratch : 0;
+  TcsPlan p;  // sized for plans without whole-tile ranges (they need the most)
+  return tcs_plan_cached(1, C, K, np, 2 * sms, false, &p, ns, false) ? p.scratch : 0;
 }
 
 // The plan for the scratch at hand: two CTAs per SM when the slots fit, fewer
 // CTAs when they do not, whole tiles per CTA (no slots) as the last resort.
 // The results are the same for every plan.
 bool tcs_plan_fit(long long R, long long C, long long K, int np, int sms, const TcsScratch& sc, TcsPlan* p,
-                  int ns = 1) {
+                  int ns = 1, bool whole_ok = true) {
   if (sc.p) {
     for (int ctas = 2 * sms; ctas >= 1; ctas = ctas * 3 / 4) {
-      if (!tcs_plan_cached(R, C, K, np, ctas, false, p, ns)) return false;
+      if (!tcs_plan_cached(R, C, K, np, ctas, false, p, ns, whole_ok)) return false;
       if (p->scratch <= sc.bytes) return true;
       if (ctas == 1) break;
     }
@@ -800,7 +800,7 @@ detffn_status gateup_slice(detffn_handle h, Family f, const uint16_t* x, const u
       // Few tokens: the top of both trees fused with SiLU * up; gate and up
       // are stored only when the caller keeps them.
       TcsPlan p;
-      if (!tcs_plan_fit(M, w, H, 2, h->sm_count, sc, &p) || p.direct) return DETFFN_ERR_WORKSPACE;
+      if (!tcs_plan_fit(M, w, H, 2, h->sm_count, sc, &p, 1, false) || p.direct) return DETFFN_ERR_WORKSPACE;
       const double bytes = 2.0 * (2.0 * w * H + (double)M * H + (keep ? 3.0 : 1.0) * M * w);
       const TcsProblem pr[2] = {{BG.p, H, x, H, keep ? gate + s * w : nullptr},
                                 {BU.p, H, x, H, keep ? up + s * w : nullptr}};

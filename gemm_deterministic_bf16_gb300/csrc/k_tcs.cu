@@ -946,7 +946,8 @@ __global__ void __launch_bounds__(kTopThreads) k_tcs_top(const TcsTopArgs a) {
 
 namespace detffn {
 
-bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* p, int ns) {
+bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* p, int ns,
+              bool whole_ok) {
   if (R < 1 || R > BN || C < 1 || K < 1 || np < 1 || np > 2 || max_ctas < 1) return false;
   if (ns < 1 || ns > kTcsMaxShards || (ns > 1 && K % BK != 0)) return false;
   const long long L = (K + BK - 1) / BK;
@@ -978,21 +979,25 @@ bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool 
   r.T = (int)((C + BM - 1) / BM);
   const int Q = 1 << E;
   r.W = (long long)np * ns * r.T * Q;
-  r.direct = direct;
   const long long units = direct ? (long long)np * ns * r.T : r.W;
   r.P = (int)(max_ctas < units ? max_ctas : units);
   if (!direct) {
     // Equal, aligned ranges: the smallest power of two B of groups per CTA
     // with W / B <= max_ctas.  When B divides a tile's 2^E groups, every
     // range is one aligned block -- one piece, a node of the canonical tree
-    // -- so a tile's fold takes 2^E / B pieces (or its root, for B = 2^E).
+    // -- so a tile's fold takes 2^E / B pieces.  When B is a multiple of
+    // 2^E, every range is B / 2^E whole tiles: direct, and balanced.
     long long B = 1;
     while (r.W / B > max_ctas) B <<= 1;
-    if (B <= Q) {
+    if (B >= Q && whole_ok) {
+      direct = true;
+      r.P = (int)(r.W / B);
+    } else if (B <= Q) {
       r.P = (int)(r.W / B);
       if (Q / B <= kTcsFoldMax && r.W / Q <= kTcsTickets) r.fold_n = (int)(Q / B);
     }
   }
+  r.direct = direct;
   r.nstage = stages_for(E);
   if (r.nstage < 2) return false;
   if (r.fold_n * PIECE * 2 > r.nstage * STAGE) r.fold_n = 0;  // the last CTA stages the pieces there

@@ -90,8 +90,12 @@ constexpr int kTcsTickets = 1024; // tree tickets per handle (a fused launch has
 // problem is ns contractions over consecutive K ranges of K positions each
 // (K a multiple of 64): shard q reads K positions [q K, (q+1) K) of the
 // operands and writes its own output (out + q * oss), one tree each.
+// Without direct, the CTAs take equal aligned blocks of 2^b groups, for the
+// smallest 2^b that needs at most max_ctas CTAs; where a block holds whole
+// trees (2^b >= a tree's groups) and whole_ok is set, the plan is direct with
+// that many trees per CTA: balanced, and no pieces at all.
 bool tcs_plan(long long R, long long C, long long K, int np, int max_ctas, bool direct, TcsPlan* plan,
-              int ns = 1);
+              int ns = 1, bool whole_ok = true);
 
 struct TcsProblem {
   const uint16_t* W;  // [C, K] weights, row stride ldw (multiple of 8), 16-byte aligned;

@@ -94,12 +94,13 @@ def _rand(shape, seed, scale=1.0):
     return to_bf16_bits((scale * rng.standard_normal(shape)).astype(np.float32))
 
 
-# Few-token shapes cover both ways of finishing a tree split over several
-# CTAs: its last CTA folds the pieces (2, 4, 8 per tree at the first three;
-# one, the tree itself, at (4, 24576, 128); 4 at (16, 8192, 1536)), or a top
-# kernel does (32 pieces at (1, 1024, 4096)).
+# Few-token shapes cover the three ways a tree's root is formed: its last
+# CTA folds the pieces of a tree split over several CTAs (2, 4, 8 per tree at
+# the first three; 4 at (16, 8192, 1536)), a top kernel does (32 pieces at
+# (1, 1024, 4096)), or each CTA takes whole trees (two each at
+# (4, 40960, 128)).
 @pytest.mark.parametrize("R,C,K", [(32, 12288, 4096), (32, 4096, 12288), (8, 3072, 768), (1, 1024, 4096),
-                                   (4, 24576, 128), (16, 8192, 1536),
+                                   (4, 40960, 128), (16, 8192, 1536),
                                    (256, 256, 4096), (256, 128, 12288), (200, 296, 40), (130, 72, 64),
                                    (96, 384, 128)])
 def test_leaf_dump_replay_and_bound(G, oracle_mod, R, C, K):

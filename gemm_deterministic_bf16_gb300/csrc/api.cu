@@ -18,13 +18,16 @@
 
 using namespace detffn;
 
+constexpr int kTicketWords = kTcsTickets + 2 * kTcsRanges;
+
 struct detffn_handle_s {
   int device = 0;
   int sm_count = 0;
   uint16_t* d_silu = nullptr;   // [65536] BF16 SiLU by gate bit pattern
   float* d_dsilu = nullptr;     // [65536] FP32 SiLU' by gate bit pattern
   int* d_status = nullptr;      // device status word (bounded waits)
-  int* d_tickets = nullptr;     // tree tickets of the few-token kernels (kTcsTickets words, zero between calls)
+  int* d_tickets = nullptr;     // tree tickets of the few-token kernels (kTcsTickets words) and the fused
+                                // forward's range counters (2 x kTcsRanges words), zero between calls
   Waits wt;                     // the current call's wait settings (status word, poll limit, test stall)
   int flags = 0;                // the current call's option flags
   // A second stream and two events (made at creation) for the overlapped
@@ -175,7 +178,8 @@ detffn_status read_opts(const detffn_options* o, Opts* out) {
     if (!(o->shards == 0 || o->shards == 1 || o->shards == 2 || o->shards == 4 || o->shards == 8))
       return DETFFN_ERR_INVALID_ARG;
     if (o->spin_limit < 0) return DETFFN_ERR_INVALID_ARG;
-    if (o->flags & ~(DETFFN_FLAG_TEST_STALL | DETFFN_FLAG_OVERLAP_DHIDDEN)) return DETFFN_ERR_INVALID_ARG;
+    if (o->flags & ~(DETFFN_FLAG_TEST_STALL | DETFFN_FLAG_OVERLAP_DHIDDEN | DETFFN_FLAG_SPLIT_FORWARD))
+      return DETFFN_ERR_INVALID_ARG;
     r.path = o->path;
     r.shards = o->shards ? o->shards : 1;
     r.flags = o->flags;
@@ -681,14 +685,14 @@ detffn_status detffn_create(detffn_handle* out, int device) {
     if (cudaMalloc(&h->d_silu, 65536 * sizeof(uint16_t)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaMalloc(&h->d_dsilu, 65536 * sizeof(float)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
-    if (cudaMalloc(&h->d_tickets, kTcsTickets * sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+    if (cudaMalloc(&h->d_tickets, kTicketWords * sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
     if (cudaMemcpy(h->d_silu, h->h_silu.data(), 65536 * sizeof(uint16_t), cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemcpy(h->d_dsilu, h->h_dsilu.data(), 65536 * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess ||
-        cudaMemset(h->d_tickets, 0, kTcsTickets * sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
+        cudaMemset(h->d_tickets, 0, kTicketWords * sizeof(int)) != cudaSuccess) { st = DETFFN_ERR_CUDA; break; }
   } while (0);
   cudaSetDevice(prev);
   if (st != DETFFN_OK) {
@@ -760,7 +764,7 @@ detffn_status detffn_get_status(detffn_handle h, void* stream) {
   TRYCU(cudaMemset(h->d_status, 0, sizeof(int)));
   // A launch that stopped on a timeout may have left trees with some of
   // their tickets taken: start the next call from zero.
-  if (v != 0) TRYCU(cudaMemset(h->d_tickets, 0, kTcsTickets * sizeof(int)));
+  if (v != 0) TRYCU(cudaMemset(h->d_tickets, 0, kTicketWords * sizeof(int)));
   return (detffn_status)v;
 }
 
@@ -882,7 +886,17 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
       // gate, up and h are the same bits whether computed slice by slice or
       // at once, so one launch computes all of them.  The down projection's
       // shards (consecutive K ranges of I) are one call as well.
-      if (s == 0) {
+      size_t need = 0;
+      if (s == 0 && k == 1 && f == kTensor && !(o.flags & DETFFN_FLAG_SPLIT_FORWARD) && sc.p &&
+          tcs_forward_fused_covers(M, H, I, h->sm_count, &need) && need <= sc.bytes) {
+        // One launch: gate/up, SiLU * up and down (the same bits as below).
+        const double bytes = 2.0 * (3.0 * I * H + (double)M * H * 2 + (saves ? 3.0 : 1.0) * M * I);
+        TRY(timed(h, st, "tcs_forward", bytes, 6.0 * M * I * H, [&] {
+          return cu(launch_tcs_forward_fused(M, H, I, X, WG, WU, WD, w.h, saves ? gate : nullptr,
+                                             saves ? up : nullptr, dst, h->d_silu, sc.p, sc.bytes, h->sm_count,
+                                             h->wt, st));
+        }));
+      } else if (s == 0) {
         TRY(gateup_slice(h, f, X, WG, WU, gate, up, saves, w.h, M, H, I, 0, I, st, sc));
         TRY(tree_gemm_k(h, f, Strided{w.h, I, 1}, Strided{WD, I, 1}, M, H, sw, k, dst, H, M * H, st, sc));
       }

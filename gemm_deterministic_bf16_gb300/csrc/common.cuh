@@ -56,6 +56,20 @@ __device__ __forceinline__ uint16_t f2bf(float v) {
 // Tree node: one FP32 add (round to nearest even), then round to BF16.
 __device__ __forceinline__ float node(float l, float r) { return bf2f(f2bf(__fadd_rn(l, r))); }
 
+// The backward stages of one element, with BF16 at every stage boundary:
+// dU = bf16(dh * SiLU(g)), dG = bf16(bf16(dh * u) * SiLU'(g)), and the
+// forward's h = bf16(SiLU(g) * u) again, from the correctly rounded tables
+// (SiLU in BF16, SiLU' in FP32, indexed by the bits of g).
+struct SiluBwd1 {
+  uint16_t dU, dG, h;
+};
+__device__ __forceinline__ SiluBwd1 silu_bwd1(uint16_t dh, uint16_t g, uint16_t u, const uint16_t* __restrict__ silu,
+                                              const float* __restrict__ dsilu) {
+  const float d = bf2f(dh), a = bf2f(__ldg(silu + g)), uu = bf2f(u);
+  const float dA = bf2f(f2bf(__fmul_rn(d, uu)));
+  return SiluBwd1{f2bf(__fmul_rn(d, a)), f2bf(__fmul_rn(dA, __ldg(dsilu + g))), f2bf(__fmul_rn(a, uu))};
+}
+
 // Number of internal nodes that end at leaf j in the midpoint tree over L
 // leaves, i.e. how many combines follow the push of leaf j in a left-to-right
 // post-order evaluation.

@@ -46,14 +46,10 @@ __global__ void k_silu_bwd(const uint16_t* __restrict__ dh, const uint16_t* __re
   grid_dep_launch();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
-    const uint16_t gi = g[i];
-    const float d = bf2f(dh[i]);
-    const float a = bf2f(__ldg(silu + gi));
-    const float uu = bf2f(u[i]);
-    dU[i] = f2bf(__fmul_rn(d, a));
-    const float dA = bf2f(f2bf(__fmul_rn(d, uu)));
-    dG[i] = f2bf(__fmul_rn(dA, __ldg(dsilu + gi)));
-    if (hh) hh[i] = f2bf(__fmul_rn(a, uu));
+    const SiluBwd1 r = silu_bwd1(dh[i], g[i], u[i], silu, dsilu);
+    dU[i] = r.dU;
+    dG[i] = r.dG;
+    if (hh) hh[i] = r.h;
   }
 }
 
@@ -83,17 +79,10 @@ __global__ void k_silu_mul_v8(const uint4* __restrict__ g, const uint4* __restri
 
 __device__ __forceinline__ void silu_bwd2(uint32_t dh2, uint32_t g2, uint32_t u2, const uint16_t* __restrict__ silu,
                                           const float* __restrict__ dsilu, uint32_t& dU2, uint32_t& dG2) {
-  uint32_t du[2], dg[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const uint16_t gi = (uint16_t)(g2 >> (16 * k));
-    const float d = bf2f((uint16_t)(dh2 >> (16 * k)));
-    du[k] = f2bf(__fmul_rn(d, bf2f(__ldg(silu + gi))));
-    const float dA = bf2f(f2bf(__fmul_rn(d, bf2f((uint16_t)(u2 >> (16 * k))))));
-    dg[k] = f2bf(__fmul_rn(dA, __ldg(dsilu + gi)));
-  }
-  dU2 = du[0] | (du[1] << 16);
-  dG2 = dg[0] | (dg[1] << 16);
+  const SiluBwd1 lo = silu_bwd1((uint16_t)dh2, (uint16_t)g2, (uint16_t)u2, silu, dsilu);
+  const SiluBwd1 hi = silu_bwd1((uint16_t)(dh2 >> 16), (uint16_t)(g2 >> 16), (uint16_t)(u2 >> 16), silu, dsilu);
+  dU2 = (uint32_t)lo.dU | ((uint32_t)hi.dU << 16);
+  dG2 = (uint32_t)lo.dG | ((uint32_t)hi.dG << 16);
 }
 
 __global__ void k_silu_bwd_v8(const uint4* __restrict__ dh, const uint4* __restrict__ g, const uint4* __restrict__ u,

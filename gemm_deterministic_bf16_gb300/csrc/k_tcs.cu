@@ -101,6 +101,7 @@ struct Bars {
   uint32_t tmem_slot;
   int abort;
   int last;  // folded trees: this CTA took its tree's last ticket
+  int go;    // fused forward: the down block runs (nothing stopped before it)
 };
 static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block");
 
@@ -215,6 +216,106 @@ __device__ __forceinline__ void load_w(unsigned char* dst, const CUtensorMap* mW
   }
 }
 
+// The root of one bottom group, this thread's row and all tokens, from its
+// GG leaves in TMEM buffers lc .. lc + GG - 1 (taddr: the TMEM base plus
+// the warp's lane quarter): a lone leaf rounded once, l0 + l1, or
+// l0 + (l1 + l2).  DUMP: the leaves also go to the leaf dump, as leaves
+// j0 .. j0 + GG - 1 of weight row crow.
+template <int GG, bool DUMP>
+__device__ __forceinline__ void group_root(uint32_t taddr, uint32_t lc, uint32_t (&root)[WORDS], float* dmp,
+                                           long long crow, int R, int C, int L, int j0) {
+  const uint32_t b0 = (uint32_t)((lc % kNBuf) * BN), b1 = (uint32_t)(((lc + 1) % kNBuf) * BN),
+                 b2 = (uint32_t)(((lc + 2) % kNBuf) * BN);
+#pragma unroll
+  for (int c = 0; c < BN / 16; ++c) {
+    uint32_t v0[16];
+    if constexpr (GG == 3) {
+      uint32_t v1[16], v2[16], n12[8];
+      tmem_ld16(taddr + b1 + 16 * c, v1);
+      tmem_ld16(taddr + b2 + 16 * c, v2);
+      tmem_wait_ld();
+      if constexpr (DUMP) {
+        dump_tokens(dmp, crow, 16 * c, R, C, L, j0 + 1, v1);
+        dump_tokens(dmp, crow, 16 * c, R, C, L, j0 + 2, v2);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        n12[i] = pack_bf16x2_of(add_f32x2(f32x2(v1[2 * i], v1[2 * i + 1]), f32x2(v2[2 * i], v2[2 * i + 1])));
+      tmem_ld16(taddr + b0 + 16 * c, v0);
+      tmem_wait_ld();
+      if constexpr (DUMP) dump_tokens(dmp, crow, 16 * c, R, C, L, j0, v0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        root[8 * c + i] =
+            pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(n12[i] << 16, n12[i] & 0xFFFF0000u)));
+    } else if constexpr (GG == 2) {
+      uint32_t v1[16];
+      tmem_ld16(taddr + b0 + 16 * c, v0);
+      tmem_ld16(taddr + b1 + 16 * c, v1);
+      tmem_wait_ld();
+      if constexpr (DUMP) {
+        dump_tokens(dmp, crow, 16 * c, R, C, L, j0, v0);
+        dump_tokens(dmp, crow, 16 * c, R, C, L, j0 + 1, v1);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        root[8 * c + i] = pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(v1[2 * i], v1[2 * i + 1])));
+    } else {
+      tmem_ld16(taddr + b0 + 16 * c, v0);
+      tmem_wait_ld();
+      if constexpr (DUMP) dump_tokens(dmp, crow, 16 * c, R, C, L, j0, v0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) root[8 * c + i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+    }
+  }
+}
+
+// Stacked gate/up, the tile's root (see TcsArgs): rows 0..63 hold gate,
+// rows 64..127 up, of weight rows 64 t + (row mod 64).  The up half hands its
+// roots over in shared memory (xch) and stores up where kept; the gate half
+// forms h = bf16(bf16(SiLU(gate)) * up) and stores it, and gate where kept.
+// xk counts the CTA's exchanges (the phase of xfull / xempty).  Every wait is
+// bounded; false when one ran out.
+__device__ __forceinline__ bool stacked_store(const TcsArgs& a, Bars* bars, uint32_t* xch, uint32_t xk, long long t,
+                                              int row, int lane, const uint32_t (&root)[WORDS], long long limit,
+                                              volatile int* abort_flag) {
+  const long long c = t * (BM / 2) + (row & (BM / 2 - 1));
+  const uint32_t ph = xk & 1u;
+  bool ok = true;
+  if (row >= BM / 2) {
+    if (!wait_or_abort(&bars->xempty, ph ^ 1u, limit, abort_flag, a.status)) ok = false;
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < WORDS; ++i) xch[i * (BM / 2) + (row - BM / 2)] = root[i];
+      if (a.out1 && c < a.C)
+#pragma unroll
+        for (int i = 0; i < BN; ++i)
+          if (i < a.R) a.out1[i * a.ldo + c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->xfull);
+  } else {
+    if (!wait_or_abort(&bars->xfull, ph, limit, abort_flag, a.status)) ok = false;
+    if (ok && c < a.C) {
+#pragma unroll
+      for (int i = 0; i < WORDS; ++i) {
+        const uint32_t g2 = root[i], u2 = xch[i * (BM / 2) + row];
+        const float h0 = __fmul_rn(bf2f(__ldg(a.silu + (g2 & 0xFFFFu))), __uint_as_float(u2 << 16));
+        const float h1 = __fmul_rn(bf2f(__ldg(a.silu + (g2 >> 16))), __uint_as_float(u2 & 0xFFFF0000u));
+        if (2 * i < a.R) a.hout[(2 * i) * a.ldo + c] = f2bf(h0);
+        if (2 * i + 1 < a.R) a.hout[(2 * i + 1) * a.ldo + c] = f2bf(h1);
+        if (a.out0) {
+          if (2 * i < a.R) a.out0[(2 * i) * a.ldo + c] = (uint16_t)(g2 & 0xFFFFu);
+          if (2 * i + 1 < a.R) a.out0[(2 * i + 1) * a.ldo + c] = (uint16_t)(g2 >> 16);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->xempty);
+  }
+  return ok;
+}
+
 // The fold of a tree's pieces by its last CTA.  src: the tree's first
 // piece (n pieces, n a power of two, at most 8, pstride 16-byte units apart;
 // the aligned blocks of the tree, left to right).  Each epilogue warp copies
@@ -264,6 +365,42 @@ __device__ __forceinline__ void fold_pieces(const uint4* src, long long pstride,
 #pragma unroll
     for (int i = 0; i < BN; ++i)
       if (i < R) o[i * ldo] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
+}
+
+// Folded trees, after this CTA's piece of tree `tree` is written: the
+// CTA takes the tree's ticket, and the last of its CTAs folds the tree's
+// fold_n pieces (slots tree * fold_n .. tree * fold_n + fold_n - 1) into the
+// root and stores it.  Every epilogue warp reaches the two barriers, whatever
+// happened: a warp that stopped early has set the abort flag, and a CTA that
+// stopped takes no ticket (its tree stays unfinished, which the status word
+// reports).  One thread orders the CTA's piece rows (after the barrier)
+// before its ticket, and the last CTA's reads after the tickets of the
+// others, with device-scope fences.  The pipeline stages must be idle (every
+// load landed and every MMA completed) and hold fold_n pieces.
+__device__ __forceinline__ void finish_tree(const TcsArgs& a, int tree, unsigned char* stages, Bars* bars,
+                                            volatile int* abort_flag, int quarter, int lane) {
+  epi_sync();
+  if (threadIdx.x == kEpi0 * 32) {
+    int last = 0;
+    if (!*abort_flag) {
+      __threadfence();
+      last = atomicAdd(a.tickets + tree, 1) == a.fold_n - 1;
+      if (last) {
+        a.tickets[tree] = 0;  // no other CTA of this launch takes it again
+        __threadfence();
+      }
+    }
+    bars->last = last;
+  }
+  epi_sync();
+  if (bars->last) {
+    const int row = quarter * 32 + lane;
+    const int per = a.np * a.ns, rem = tree % per;
+    const int c = (tree / per) * BM + row;
+    fold_pieces(reinterpret_cast<const uint4*>(a.slots + (size_t)tree * a.fold_n * a.cap * PIECE),
+                (long long)a.cap * (PIECE / 8), a.fold_n, stages, quarter, lane,
+                c < a.C ? ((rem % a.np) ? a.out1 : a.out0) + (rem / a.np) * a.oss + c : nullptr, a.ldo, a.R);
+  }
 }
 
 // The streaming kernel.  Each role walks the CTA's groups in the same order:
@@ -466,56 +603,12 @@ __global__ void __maxnreg__(128)
           break;
         }
         tc_fence_after();
-        const uint32_t b0 = (uint32_t)((lc % kNBuf) * BN), b1 = (uint32_t)(((lc + 1) % kNBuf) * BN),
-                       b2 = (uint32_t)(((lc + 2) % kNBuf) * BN);
-        // The group root: a lone leaf rounded once, l0 + l1, or l0 + (l1 + l2).
+        // The group root; leaf dump: this thread's weight row of the tile.
         uint32_t root[WORDS];
-        // Leaf dump: this thread's weight row of the tile, tokens 16 c + i.
         const Seg sg = seg_of(s, a.np, a.ns);
-        float* const dmp = DUMP ? a.dump + (size_t)sg.pb * a.R * a.C * a.L : nullptr;
-        const long long crow = (long long)sg.t * BM + row;
-#pragma unroll
-        for (int c = 0; c < BN / 16; ++c) {
-          uint32_t v0[16];
-          if constexpr (GG == 3) {
-            uint32_t v1[16], v2[16], n12[8];
-            tmem_ld16(tmem + lane_addr + b1 + 16 * c, v1);
-            tmem_ld16(tmem + lane_addr + b2 + 16 * c, v2);
-            tmem_wait_ld();
-            if constexpr (DUMP) {
-              dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG + 1, v1);
-              dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG + 2, v2);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              n12[i] = pack_bf16x2_of(add_f32x2(f32x2(v1[2 * i], v1[2 * i + 1]), f32x2(v2[2 * i], v2[2 * i + 1])));
-            tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
-            tmem_wait_ld();
-            if constexpr (DUMP) dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG, v0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              root[8 * c + i] =
-                  pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(n12[i] << 16, n12[i] & 0xFFFF0000u)));
-          } else if constexpr (GG == 2) {
-            uint32_t v1[16];
-            tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
-            tmem_ld16(tmem + lane_addr + b1 + 16 * c, v1);
-            tmem_wait_ld();
-            if constexpr (DUMP) {
-              dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG, v0);
-              dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG + 1, v1);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              root[8 * c + i] = pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(v1[2 * i], v1[2 * i + 1])));
-          } else {
-            tmem_ld16(tmem + lane_addr + b0 + 16 * c, v0);
-            tmem_wait_ld();
-            if constexpr (DUMP) dump_tokens(dmp, crow, 16 * c, a.R, a.C, a.L, q * GG, v0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) root[8 * c + i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
-          }
-        }
+        group_root<GG, DUMP>(tmem + lane_addr, lc, root,
+                             DUMP ? a.dump + (size_t)sg.pb * a.R * a.C * a.L : nullptr,
+                             (long long)sg.t * BM + row, a.R, a.C, a.L, q * GG);
         // The leaves are in registers: return the TMEM buffers to the MMA warp.
         tc_fence_before();
         __syncwarp();
@@ -561,50 +654,15 @@ __global__ void __maxnreg__(128)
         }
         if (tile_root) {
           if (a.stacked) {
-            // Rows 0..63 hold gate, rows 64..127 up, of weight rows
-            // 64 t + (row mod 64): the up half hands its roots over in
-            // shared memory, the gate half forms h.  Every wait is bounded.
-            const long long c = (long long)sg.t * (BM / 2) + (row & (BM / 2 - 1));
-            const uint32_t ph = xk & 1u;
-            if (row >= BM / 2) {
-              if (!wait_or_abort(&bars->xempty, ph ^ 1u, limit, abort_flag, a.status)) ok = false;
-              if (ok) {
-  #pragma unroll
-                for (int i = 0; i < WORDS; ++i) xch[i * (BM / 2) + (row - BM / 2)] = root[i];
-                if (a.out1 && c < a.C)
-  #pragma unroll
-                  for (int i = 0; i < BN; ++i)
-                    if (i < a.R) a.out1[i * a.ldo + c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
-              }
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars->xfull);
+            if (!stacked_store(a, bars, xch, xk, sg.t, row, lane, root, limit, abort_flag)) ok = false;
+            ++xk;
           } else {
-              if (!wait_or_abort(&bars->xfull, ph, limit, abort_flag, a.status)) ok = false;
-              if (ok && c < a.C) {
-  #pragma unroll
-                for (int i = 0; i < WORDS; ++i) {
-                  const uint32_t g2 = root[i], u2 = xch[i * (BM / 2) + row];
-                  const float h0 = __fmul_rn(bf2f(__ldg(a.silu + (g2 & 0xFFFFu))), __uint_as_float(u2 << 16));
-                  const float h1 = __fmul_rn(bf2f(__ldg(a.silu + (g2 >> 16))), __uint_as_float(u2 & 0xFFFF0000u));
-                  if (2 * i < a.R) a.hout[(2 * i) * a.ldo + c] = f2bf(h0);
-                  if (2 * i + 1 < a.R) a.hout[(2 * i + 1) * a.ldo + c] = f2bf(h1);
-                  if (a.out0) {
-                    if (2 * i < a.R) a.out0[(2 * i) * a.ldo + c] = (uint16_t)(g2 & 0xFFFFu);
-                    if (2 * i + 1 < a.R) a.out0[(2 * i + 1) * a.ldo + c] = (uint16_t)(g2 >> 16);
-                  }
-                }
-              }
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars->xempty);
-          }
-          ++xk;
-          } else {
-          const long long c = (long long)sg.t * BM + row;
-          uint16_t* o = (sg.pb ? a.out1 : a.out0) + sg.q * a.oss;
-          if (c < a.C)
+            const long long c = (long long)sg.t * BM + row;
+            uint16_t* o = (sg.pb ? a.out1 : a.out0) + sg.q * a.oss;
+            if (c < a.C)
 #pragma unroll
-            for (int i = 0; i < BN; ++i)
-              if (i < a.R) o[i * a.ldo + c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
+              for (int i = 0; i < BN; ++i)
+                if (i < a.R) o[i * a.ldo + c] = (uint16_t)(root[i >> 1] >> (16 * (i & 1)));
           }
         }
       }
@@ -621,38 +679,354 @@ __global__ void __maxnreg__(128)
         }
       w = s * Q + qb;
     }
-    if (a.fold_n > 0) {
-      // Folded trees: this CTA's piece is written; the tree's last CTA folds
-      // all of them.  Every epilogue warp reaches the two barriers, whatever
-      // happened: a warp that stopped early has set the abort flag, and a
-      // CTA that stopped takes no ticket (its tree stays unfinished, which
-      // the status word reports).  One thread orders the CTA's piece rows
-      // (after the barrier) before its ticket, and the last CTA's reads after
-      // the tickets of the others, with device-scope fences.
-      const int fold_tree = (int)(w0 / Q);  // fewer than kTcsTickets trees
-      epi_sync();
-      if (threadIdx.x == kEpi0 * 32) {
-        int last = 0;
-        if (!*abort_flag) {
-          __threadfence();
-          last = atomicAdd(a.tickets + fold_tree, 1) == a.fold_n - 1;
-          if (last) {
-            a.tickets[fold_tree] = 0;  // no other CTA of this launch takes it again
-            __threadfence();
+    // Folded trees: this CTA's piece is written; the tree's last CTA folds
+    // all of them (every epilogue warp takes part, whatever happened).
+    if (a.fold_n > 0) finish_tree(a, (int)(w0 / Q), stages, bars, abort_flag, quarter, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Fused decode forward: one launch for gate/up, SiLU * up and down.
+// ---------------------------------------------------------------------------
+// Unit A is one stacked gate/up tile (64 rows of Wg over the same 64 rows of
+// Wu, the whole K = H; the gate half writes h, as in the stacked kernel),
+// unit B one aligned block of groups of a down-projection tree (one piece;
+// the tree's last CTA folds, as with folded trees).  CTA b takes tile b
+// (b < nA) and then block (b - nA) mod P (when below nB).  A block's K range
+// of I is h's columns of per_range consecutive tiles; before its first token
+// tile each producer warp of the block waits until those tiles have been
+// counted in ready[range] (each tile's gate half counts itself once its h is
+// stored), and the last of the range's waiters resets both counters.  No unit
+// A waits on a unit B, so every wait ends once the tiles it needs run.
+// Pending levels of a unit's fold kept in registers (the rest in shared
+// memory): two, so that the epilogue fits its 128 registers.
+constexpr int kFwdRegLv = 2;
+__host__ __device__ inline int fwd_smem_levels(int eA, int eB) {
+  const int e = eA > eB ? eA : eB;
+  return e > kFwdRegLv ? e - kFwdRegLv : 0;
+}
+
+struct FwdArgs {
+  TcsArgs A, B;    // unit A geometry (stacked, direct), unit B geometry (folded trees)
+  int slv;         // pending levels in shared memory (fwd_smem_levels of both units)
+  int nA, nB;      // gate/up tiles, down blocks
+  int bG;          // groups per down block
+  int per_range;   // gate/up tiles per down range (= bG * leaves per group)
+  int waiters;     // producer warps that wait on one range (two per down tree)
+  int* ready;      // [kTcsRanges] tiles counted, then [kTcsRanges] waiters passed
+};
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Group root v (group q of a complete aligned block of 2^e groups, counted
+// from the block's start) into the block's pending stack (levels below RL in
+// registers, the rest in this thread's column of stk); true when v is then
+// the block's root.
+template <int RL>
+__device__ __forceinline__ bool fold_push(uint32_t (&v)[WORDS], int q, int e, uint32_t (&reg_lv)[RL][WORDS],
+                                          uint32_t* stk, int row) {
+  bool root = false, live = true;
+#pragma unroll
+  for (int m = 0; m <= kTcsMaxLv; ++m) {
+    if (live) {
+      if (m == e) {
+        root = true;
+        live = false;
+      } else if ((q >> m) & 1) {
+#pragma unroll
+        for (int i = 0; i < WORDS; ++i) {
+          const uint32_t left = m < RL ? reg_lv[m < RL ? m : 0][i] : stk[((m - RL) * WORDS + i) * BM + row];
+          v[i] = add_bf16x2(left, v[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < WORDS; ++i) {
+          if (m < RL) reg_lv[m < RL ? m : 0][i] = v[i];
+          else stk[((m - RL) * WORDS + i) * BM + row] = v[i];
+        }
+        live = false;
+      }
+    }
+  }
+  return root;
+}
+
+// The epilogue's walk over one unit: 2^e groups of G leaves each (TMEM
+// buffers from lc on), folded into the unit's root (root is the working
+// value: each group's root, pushed or merged, and the unit's root at the
+// end).  False when a wait ran out (root unfinished).
+template <int G>
+__device__ __forceinline__ bool unit_root(uint32_t taddr, uint32_t& lc, int e, uint32_t (&root)[WORDS], uint32_t* stk,
+                                          int row, int lane, Bars* bars, long long limit, volatile int* abort_flag,
+                                          int* status) {
+  uint32_t reg_lv[kFwdRegLv][WORDS];
+  bool ok = true;
+#pragma unroll 1
+  for (int q = 0; q < (1 << e); ++q) {
+    for (int g = 0; g < G; ++g)
+      if (!wait_or_abort(&bars->accf[(lc + g) % kNBuf], (uint32_t)(((lc + g) / kNBuf) & 1), limit, abort_flag,
+                         status))
+        ok = false;
+    if (__any_sync(0xffffffffu, !ok)) return false;
+    tc_fence_after();
+    group_root<G, false>(taddr, lc, root, nullptr, 0, 0, 0, 0, 0);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0)
+      for (int g = 0; g < G; ++g) mbar_arrive(&bars->acce[(lc + g) % kNBuf]);
+    lc += G;
+    fold_push<kFwdRegLv>(root, q, e, reg_lv, stk, row);  // after the last group, root is the unit's root
+  }
+  return true;
+}
+
+template <int GA, int GB>
+__global__ void __maxnreg__(128)
+    k_tcs_fwd(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ CUtensorMap tmWu,
+              const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmWd,
+              const __grid_constant__ CUtensorMap tmH, const __grid_constant__ FwdArgs f) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const TcsArgs& A = f.A;
+  const TcsArgs& B = f.B;
+  const int NS = A.nstage;
+  const int slv = f.slv;
+  unsigned char* stages = smem;
+  uint32_t* stk = reinterpret_cast<uint32_t*>(smem + NS * STAGE);
+  Bars* bars = reinterpret_cast<Bars*>(smem + NS * STAGE + slv * LV_BYTES);
+  uint32_t* xch = reinterpret_cast<uint32_t*>(smem + NS * STAGE + slv * LV_BYTES + BAR_BYTES);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = (int)gridDim.x;
+  const bool hasA = (int)blockIdx.x < f.nA;
+  int jB = ((int)blockIdx.x - f.nA) % P;
+  if (jB < 0) jB += P;
+  const bool hasB = jB < f.nB;
+  const int nLA = hasA ? (GA << A.E) : 0;  // leaves of unit A (the whole K = H)
+  const int nLB = hasB ? f.bG * GB : 0;     // leaves of unit B
+  const int treeB = hasB ? jB / B.fold_n : 0, rangeB = hasB ? jB % B.fold_n : 0;
+  const int kB0 = rangeB * f.bG * GB;       // unit B's first leaf along K = I
+  const long long limit = A.spin > 0 ? A.spin : kDefaultSpin;
+  if (__syncthreads_or(A.status != nullptr && *(volatile int*)A.status != 0)) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&bars->full[s], 1);
+    for (int b = 0; b < kNBuf; ++b) {
+      mbar_init(&bars->accf[b], 1);
+      mbar_init(&bars->acce[b], kEpiWarps);
+    }
+    mbar_init(&bars->fin, 1);
+    mbar_init(&bars->xfull, 2);
+    mbar_init(&bars->xempty, 2);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp < kProd && lane == 0) {
+    if (warp == 0) {
+      prefetch_tmap(&tmWg);
+      prefetch_tmap(&tmWu);
+      prefetch_tmap(&tmWd);
+    } else {
+      prefetch_tmap(&tmX);
+      prefetch_tmap(&tmH);
+    }
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  grid_dep_launch();
+
+  if (warp < kProd) {
+    // ---------------- TMA producers: leaf it goes to producer it % kProd ----------------
+    // Leaves 0 .. nLA-1 are unit A's (K positions 64 it of H), then unit B's
+    // (K positions 64 (kB0 + it - nLA) of I).
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    const long long nL = nLA + nLB;
+    auto load_weights = [&](long long it, unsigned char* dst, uint64_t* bar) {
+      if (it < nLA) load_w(dst, &tmWg, (int)(it * BK), (int)blockIdx.x, bar, pol, 0, &tmWu);
+      else load_w(dst, &tmWd, (int)((kB0 + it - nLA) * BK), treeB, bar, pol, 0);
+    };
+    // Before the previous kernel has finished: weight tiles of the first NS leaves.
+    if (!A.stall)
+      for (long long it = warp; it < nL && it < NS; it += kProd) {
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bars->full[it], (uint32_t)STAGE);
+          load_weights(it, stages + it * STAGE, &bars->full[it]);
+        }
+        __syncwarp();
+      }
+    grid_dep_wait();
+    // Leaf i uses stage i % NS, free once leaf i - NS has been committed.
+    // This warp's leaves below wmax have their weight tiles issued, those
+    // below xdone their token tiles too.
+    bool ok = true;
+    long long wmax = warp, xdone = warp;
+    for (long long i = warp; i < nL && i < NS; i += kProd) wmax = i + kProd;  // the prefetch above
+    auto stage_free = [&](long long i) -> bool {
+      if (i < NS) return true;
+      const long long v = i - NS;
+      const bool wok = wait_or_abort(&bars->accf[v % kNBuf], (uint32_t)((v / kNBuf) & 1), limit, abort_flag, A.status);
+      return __all_sync(0xffffffffu, wok) != 0;
+    };
+    auto issue_w = [&](long long i) {
+      if (!A.stall && elect_one()) {
+        mbar_arrive_expect_tx(&bars->full[i % NS], (uint32_t)STAGE);
+        load_weights(i, stages + (i % NS) * STAGE, &bars->full[i % NS]);
+      }
+      __syncwarp();
+      wmax = i + kProd;
+    };
+    auto issue_x = [&](long long i) {
+      if (!A.stall && elect_one()) {
+        unsigned char* dst = stages + (i % NS) * STAGE + A_BYTES;
+        if (i < nLA) tma_load_2d(dst, &tmX, (int)(i * BK), 0, &bars->full[i % NS]);
+        else tma_load_2d(dst, &tmH, (int)((kB0 + i - nLA) * BK), 0, &bars->full[i % NS]);
+      }
+      __syncwarp();
+      xdone = i + kProd;
+    };
+    bool waited = false;
+    for (long long it = warp; it < nL && ok; it += kProd) {
+      if (it >= nLA && !waited) {
+        // Unit B: first the weight tiles of its leaves within one ring of its
+        // start (their stages free up as unit A drains), then the wait for
+        // h's columns, which are per_range gate/up tiles of this launch.
+        for (long long j = it; j < nL && j < nLA + NS && ok; j += kProd)
+          if (j >= wmax) {
+            if (stage_free(j)) issue_w(j);
+            else ok = false;
+          }
+        if (!ok) break;
+        bool rok = true;
+        if (lane == 0) {
+          long long i = 0;
+          for (; i < limit; ++i) {
+            if (ld_acquire(f.ready + rangeB) >= f.per_range) break;
+            if ((i & 255) == 255 && *abort_flag) {
+              i = limit;
+              break;
+            }
+            __nanosleep(64);
+          }
+          if (i >= limit) {
+            rok = false;
+            *abort_flag = 1;
+            if (A.status) atomicExch(A.status, (int)DETFFN_ERR_TIMEOUT);
+          } else {
+            fence_proxy_async_global();  // the TMA loads below read what generic stores wrote
+            if (atomicAdd(f.ready + kTcsRanges + rangeB, 1) == f.waiters - 1) {
+              f.ready[rangeB] = 0;  // every waiter of this launch has passed
+              f.ready[kTcsRanges + rangeB] = 0;
+            }
           }
         }
-        bars->last = last;
+        waited = true;
+        if (!__shfl_sync(0xffffffffu, rok, 0)) {
+          ok = false;
+          break;
+        }
       }
+      if (it >= wmax) {
+        if (!stage_free(it)) {
+          ok = false;
+          break;
+        }
+        issue_w(it);
+      }
+      issue_x(it);
+    }
+    // After a stop, the stages whose weight tiles went out without their
+    // token tiles get those too (in-bounds reads), so that each completes.
+    // Then drain: this producer's loads have landed (long bound).
+    if (!A.stall) {
+      for (long long i = xdone; i < wmax; i += kProd) issue_x(i);
+      if (lane == 0)
+        for (long long i = (wmax > NS ? wmax - NS : 0); i < wmax; ++i)
+          if ((int)(i % kProd) == warp) mbar_wait(&bars->full[i % NS], (uint32_t)((i / NS) & 1), kDefaultSpin, nullptr);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer: every leaf of both units, in order ----------------
+    grid_dep_wait();
+    const uint32_t idesc = idesc_bf16(BM, BN);
+    const long long nleaf = nLA + nLB;
+    Ring rs, rb;
+    bool ok = true;
+    for (long long n = 0; n < nleaf && ok; ++n, rs.next(NS), rb.next(kNBuf)) {
+      const int st = rs.slot, b = rb.slot;
+      const bool wok = wait_or_abort(&bars->acce[b], rb.phase ^ 1u, limit, abort_flag, A.status) &&
+                       wait_or_abort(&bars->full[st], rs.phase, limit, abort_flag, A.status);
+      if (!__all_sync(0xffffffffu, wok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t da = smem_desc_sw128(stages + st * STAGE);
+      const uint64_t db = smem_desc_sw128(stages + st * STAGE + A_BYTES);
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma_bf16(tmem + (uint32_t)(b * BN), da + 2u * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+        tc_commit(&bars->accf[b]);
+      }
+      __syncwarp();
+    }
+    if (elect_one()) tc_commit(&bars->fin);
+    __syncwarp();
+    if (lane == 0) mbar_wait(&bars->fin, 0, kDefaultSpin, nullptr);
+  } else {
+    // ---------------- epilogue ----------------
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    grid_dep_wait();
+    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint32_t lc = 0;
+    uint32_t root[WORDS];
+    if (hasA) {
+      // The tile's root, then h (and the saves) through the stacked exchange.
+      bool ok = unit_root<GA>(taddr, lc, A.E, root, stk, row, lane, bars, limit, abort_flag, A.status);
+      if (ok) ok = stacked_store(A, bars, xch, 0, blockIdx.x, row, lane, root, limit, abort_flag);
+      // The gate half (rows 0..63, two warps) stored h: count the tile in
+      // its range once both warps are done (both always reach the barrier).
+      if (row < BM / 2) {
+        asm volatile("bar.sync 2, %0;" ::"n"(BM / 2) : "memory");
+        if (row == 0 && !*abort_flag) {
+          fence_proxy_async_global();
+          __threadfence();
+          atomicAdd(f.ready + (int)blockIdx.x / f.per_range, 1);
+        }
+      }
+    }
+    if (hasB) {
+      // Unit B runs unless something stopped (one decision for all four warps).
       epi_sync();
-      if (bars->last) {
-        // The pipeline stages are idle now (every load has landed and every
-        // MMA has completed); the plan checks that they hold fold_n pieces.
-        const int per = a.np * a.ns, rem = fold_tree % per;
-        const int c = (fold_tree / per) * BM + row;
-        fold_pieces(reinterpret_cast<const uint4*>(a.slots + (size_t)fold_tree * a.fold_n * a.cap * PIECE),
-                    (long long)a.cap * (PIECE / 8), a.fold_n, stages, quarter, lane,
-                    c < a.C ? ((rem % a.np) ? a.out1 : a.out0) + (rem / a.np) * a.oss + c : nullptr, a.ldo, a.R);
+      if (threadIdx.x == kEpi0 * 32) bars->go = !*abort_flag;
+      epi_sync();
+      if (bars->go &&
+          unit_root<GB>(taddr, lc, B.E - hibit((unsigned)B.fold_n), root, stk, row, lane, bars, limit, abort_flag,
+                        B.status)) {
+        int n = 0;
+        emit_piece(B.slots + (size_t)jB * B.cap * PIECE, n, B.cap, row, root);
       }
+      finish_tree(B, treeB, stages, bars, abort_flag, quarter, lane);
     }
   }
 
@@ -1043,6 +1417,13 @@ cudaError_t tcs_setup() {
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     }
+    void (*fws[4])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, FwdArgs) = {
+        k_tcs_fwd<2, 2>, k_tcs_fwd<2, 3>, k_tcs_fwd<3, 2>, k_tcs_fwd<3, 3>};
+    for (auto k : fws) {
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    }
     void (*tops[2])(TcsTopArgs) = {k_tcs_top<false>, k_tcs_top<true>};
     for (auto k : tops) {
       if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
@@ -1187,6 +1568,118 @@ cudaError_t launch_tcs_gateup_stacked(long long R, long long C, long long K, con
       plan.G == 1 ? k_tcs<1, false> : plan.G == 2 ? k_tcs<2, false> : k_tcs<3, false>;
   return launch_dependent(kern, dim3(plan.P), kThreads, smem_for(plan.E, plan.nstage, true), st, m[0], m[1], m[2],
                           m[3], a);
+}
+
+namespace {
+
+// The two plans of the fused forward and its launch geometry; false when the
+// shape is not covered.
+struct FusedPlan {
+  TcsPlan a, b;
+  int P, nA, nB, bG, nstage, slv;
+};
+bool fused_plan(long long R, long long H, long long I, int sm_count, FusedPlan* fp) {
+  if (R < 1 || R > BN || H < 1 || I < 1 || I % (BM / 2) || H % 8) return false;
+  FusedPlan p;
+  p.P = 2 * sm_count;
+  // Unit A: stacked tiles (64 rows of each weight = 128 MMA rows) over K = H.
+  if (!tcs_plan(R, 2 * I, H, 1, p.P, true, &p.a, 1)) return false;
+  // Unit B: the down projection's aligned blocks, folded by the trees' last CTAs.
+  if (!tcs_plan(R, H, I, 1, p.P, false, &p.b, 1, false) || p.b.fold_n < 2 || p.b.direct) return false;
+  if (p.a.T > p.P || p.b.P > p.P || (p.a.G != 2 && p.a.G != 3) || (p.b.G != 2 && p.b.G != 3)) return false;
+  p.nA = p.a.T;
+  p.nB = p.b.P;
+  p.bG = (int)(p.b.W / p.b.P);
+  if (p.b.fold_n > kTcsRanges || p.b.cap != 1 || p.b.W / (1ll << p.b.E) > kTcsTickets) return false;
+  // The down's K range of one block is bG * G leaves: that many 64-column tiles of h.
+  if ((long long)p.bG * p.b.G * 64 * p.b.fold_n != I) return false;
+  p.slv = fwd_smem_levels(p.a.E, p.b.E - hibit((unsigned)p.b.fold_n));
+  p.nstage = (MAX_SMEM - 1024 - BAR_BYTES - p.slv * LV_BYTES - XCH_BYTES) / STAGE;
+  if (p.nstage > MAX_STAGES) p.nstage = MAX_STAGES;
+  p.nstage &= ~1;
+  if (p.nstage < 2 || p.b.fold_n * PIECE * 2 > p.nstage * STAGE) return false;
+  *fp = p;
+  return true;
+}
+
+}  // namespace
+
+bool tcs_forward_fused_covers(long long R, long long H, long long I, int sm_count, size_t* scratch) {
+  FusedPlan p;
+  if (!fused_plan(R, H, I, sm_count, &p)) return false;
+  if (scratch) *scratch = p.b.scratch;
+  return true;
+}
+
+cudaError_t launch_tcs_forward_fused(long long R, long long H, long long I, const uint16_t* x, const uint16_t* Wg,
+                                     const uint16_t* Wu, const uint16_t* Wd, uint16_t* h, uint16_t* gate,
+                                     uint16_t* up, uint16_t* out, const uint16_t* silu, void* scratch,
+                                     size_t scratch_bytes, int sm_count, const Waits& wt, cudaStream_t st) {
+  FusedPlan p;
+  if (!fused_plan(R, H, I, sm_count, &p)) return cudaErrorNotSupported;
+  if (!x || !Wg || !Wu || !Wd || !h || !out || !silu || !wt.tickets || !scratch || scratch_bytes < p.b.scratch ||
+      (((uintptr_t)x | (uintptr_t)Wg | (uintptr_t)Wu | (uintptr_t)Wd | (uintptr_t)h | (uintptr_t)scratch) & 15u))
+    return cudaErrorInvalidValue;
+  CUtensorMap m[5];
+  if (!tc_make_map(&m[0], Wg, I, H, H, BM / 2) || !tc_make_map(&m[1], Wu, I, H, H, BM / 2) ||
+      !tc_make_map(&m[2], x, R, H, H, BN) || !tc_make_map(&m[3], Wd, H, I, I, BM) || !tc_make_map(&m[4], h, R, I, I, BN))
+    return cudaErrorInvalidValue;
+  const cudaError_t setup_err = tcs_setup();
+  if (setup_err != cudaSuccess) return setup_err;
+  FwdArgs f{};
+  TcsArgs& A = f.A;
+  A.R = (int)R;
+  A.C = (int)I;
+  A.G = p.a.G;
+  A.E = p.a.E;
+  A.np = 1;
+  A.ns = 1;
+  A.ksh = H;
+  A.T = p.a.T;
+  A.W = p.a.W;
+  A.nstage = p.nstage;
+  A.out0 = gate;
+  A.out1 = up;
+  A.ldo = I;
+  A.status = wt.status;
+  A.spin = wt.spin;
+  A.stall = wt.stall;
+  A.L = p.a.G << p.a.E;
+  A.stacked = 1;
+  A.hout = h;
+  A.silu = silu;
+  TcsArgs& B = f.B;
+  B.R = (int)R;
+  B.C = (int)H;
+  B.G = p.b.G;
+  B.E = p.b.E;
+  B.np = 1;
+  B.ns = 1;
+  B.ksh = I;
+  B.T = p.b.T;
+  B.W = p.b.W;
+  B.cap = p.b.cap;
+  B.nstage = p.nstage;
+  B.slots = static_cast<uint16_t*>(scratch);
+  B.out0 = out;
+  B.ldo = H;
+  B.status = wt.status;
+  B.spin = wt.spin;
+  B.stall = wt.stall;
+  B.L = p.b.G << p.b.E;
+  B.fold_n = p.b.fold_n;
+  B.tickets = wt.tickets;
+  f.nA = p.nA;
+  f.nB = p.nB;
+  f.bG = p.bG;
+  f.per_range = p.bG * p.b.G;
+  f.waiters = 2 * p.b.T;
+  f.ready = wt.tickets + kTcsTickets;
+  f.slv = p.slv;
+  const int smem = 1024 + p.nstage * STAGE + p.slv * LV_BYTES + BAR_BYTES + XCH_BYTES;
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, FwdArgs) =
+      p.a.G == 2 ? (p.b.G == 2 ? k_tcs_fwd<2, 2> : k_tcs_fwd<2, 3>) : (p.b.G == 2 ? k_tcs_fwd<3, 2> : k_tcs_fwd<3, 3>);
+  return launch_dependent(kern, dim3(p.P), kThreads, smem, st, m[0], m[1], m[2], m[3], m[4], f);
 }
 
 cudaError_t launch_tcs_gateup(const TcsPlan& plan, const TcsProblem* pr, uint16_t* h, long long ldo,

@@ -82,6 +82,7 @@ struct TcsPlan {
 };
 constexpr int kTcsFoldMax = 8;    // pieces per tree the last CTA folds
 constexpr int kTcsTickets = 1024; // tree tickets per handle (a fused launch has at most 2 x SMs trees)
+constexpr int kTcsRanges = 64;    // fused decode forward: range counters per handle (two words each)
 
 // Plans a launch on at most max_ctas CTAs (two per SM is the design point).
 // False when the shape is not covered (R > 32, or K's leaf count not 1, 2^d or
@@ -127,6 +128,21 @@ cudaError_t launch_tcs_gateup_stacked(long long R, long long C, long long K, con
                                       long long ldw, const uint16_t* X, long long ldx, uint16_t* gate, uint16_t* up,
                                       uint16_t* h, long long ldo, const uint16_t* silu, int sm_count, const Waits& wt,
                                       cudaStream_t st);
+
+// The whole decode forward of R <= 32 tokens in one launch: x [R, H], Wg,
+// Wu [I, H], Wd [H, I] (rows of H and I elements, 16-byte aligned), h [R, I]
+// written (and gate, up where not null), out [R, H].  Stacked gate/up tiles
+// and the down projection's folded trees, as launch_tcs_gateup_stacked and
+// launch_tcs compute them (the same bits); a down block starts once the
+// gate/up tiles of its K range are done.  Needs the tickets and range
+// counters of `wt` and plan scratch bytes at `scratch`.  Returns
+// cudaErrorNotSupported, launching nothing, for shapes it does not cover
+// (tcs_forward_fused_covers false).
+bool tcs_forward_fused_covers(long long R, long long H, long long I, int sm_count, size_t* scratch);
+cudaError_t launch_tcs_forward_fused(long long R, long long H, long long I, const uint16_t* x, const uint16_t* Wg,
+                                     const uint16_t* Wu, const uint16_t* Wd, uint16_t* h, uint16_t* gate,
+                                     uint16_t* up, uint16_t* out, const uint16_t* silu, void* scratch,
+                                     size_t scratch_bytes, int sm_count, const Waits& wt, cudaStream_t st);
 
 // Host check of the few-token kernels' piece decomposition and fold codes
 // over every tile of up to 2^max_levels groups; returns the failed cases.

@@ -39,6 +39,7 @@ class DetFFNError(RuntimeError):
 
 FLAG_TEST_STALL = 1
 FLAG_OVERLAP_DHIDDEN = 2
+FLAG_SPLIT_FORWARD = 4
 
 
 class Options(ctypes.Structure):

@@ -81,13 +81,19 @@ typedef enum { DETFFN_PATH_AUTO = 0, DETFFN_PATH_EXACT = 1, DETFFN_PATH_TENSOR =
  * CTAs stop with nothing in flight and the call's outputs are left
  * unfinished; detffn_get_status then returns DETFFN_ERR_TIMEOUT.  The fault
  * is made by withholding work, never by a bad address or a trap. */
-enum { DETFFN_FLAG_TEST_STALL = 1, DETFFN_FLAG_OVERLAP_DHIDDEN = 2 };
+enum { DETFFN_FLAG_TEST_STALL = 1, DETFFN_FLAG_OVERLAP_DHIDDEN = 2, DETFFN_FLAG_SPLIT_FORWARD = 4 };
 /* DETFFN_FLAG_OVERLAP_DHIDDEN (detffn_backward with options->shards = k > 1;
  * PR #325, "Communication overlap assessment"): the rank tree of the gate
  * contribution's shard roots runs on a second stream of the handle while the
  * up contribution's shards are computed on `stream`; the gate-then-up
  * addition waits for both.  The bits are those of the one-stream call.
- * Without shards it changes nothing. */
+ * Without shards it changes nothing.
+ * DETFFN_FLAG_SPLIT_FORWARD (detffn_forward): on the tensor family with at
+ * most 32 tokens the forward is one launch (PR #325, "Communication overlap
+ * assessment": the gate/up to down dependency taken per K range of the down
+ * projection, inside the launch) wherever the shape allows; this flag asks
+ * for the two-launch form instead (gate/up with SiLU * up, then down).  The
+ * bits are the same. */
 
 typedef struct {
     int leaf_width;        /* 64; anything else returns DETFFN_ERR_UNSUPPORTED */

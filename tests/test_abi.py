@@ -85,7 +85,7 @@ def test_argument_errors_launch_nothing(L):
     n = ctypes.c_size_t()
     assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, bad, ctypes.byref(n)) == 4
     # Unknown option flag bits and a negative poll limit are argument errors.
-    for fl in (4, 8, 1 << 30, -1):
+    for fl in (8, 16, 1 << 30, -1):
         assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, fl, 0)),
                                        ctypes.byref(n)) == 1
     assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 2, 0)),

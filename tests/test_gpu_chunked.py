@@ -29,8 +29,8 @@ _CASES = {}
 
 def _case(G, M):
     """Inputs, forward saves and the one-shot backward's weight gradients at
-    M tokens (H = 256, I = 512): 384 tokens are a tree of 6 leaves (bottom
-    groups of three), 512 tokens one of 8 leaves (pairs)."""
+    M tokens (H = 256, I = 512): 32 tokens are one leaf, 384 tokens a tree of
+    6 leaves (bottom groups of three), 512 tokens one of 8 leaves (pairs)."""
     if M not in _CASES:
         H, I = 256, 512
         d = ffn_inputs(M, H, I, seed=23 + M)
@@ -51,7 +51,9 @@ def _misaligned(v):
     return out
 
 
-@pytest.mark.parametrize("M,sizes", [(384, [128, 256]), (384, [64] * 6), (384, [64, 320]), (384, [192, 192]),
+# M = 32: the few-token kernels for dh, whole and in chunks of 16, 8 and 24.
+@pytest.mark.parametrize("M,sizes", [(32, [32]), (32, [16, 16]), (32, [8, 24]),
+                                     (384, [128, 256]), (384, [64] * 6), (384, [64, 320]), (384, [192, 192]),
                                      (384, [0, 384, 0]), (384, [100, 284]), (384, [32] * 12), (384, [1, 63, 320]),
                                      (512, [256, 256]), (512, [64] * 8), (512, [448, 64]), (512, [200, 312])])
 @pytest.mark.parametrize("aligned", [True, False])

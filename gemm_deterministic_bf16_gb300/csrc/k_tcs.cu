@@ -1578,7 +1578,7 @@ struct FusedPlan {
   TcsPlan a, b;
   int P, nA, nB, bG, nstage, slv;
 };
-bool fused_plan(long long R, long long H, long long I, int sm_count, FusedPlan* fp) {
+bool fused_plan_uncached(long long R, long long H, long long I, int sm_count, FusedPlan* fp) {
   if (R < 1 || R > BN || H < 1 || I < 1 || I % (BM / 2) || H % 8) return false;
   FusedPlan p;
   p.P = 2 * sm_count;
@@ -1600,6 +1600,37 @@ bool fused_plan(long long R, long long H, long long I, int sm_count, FusedPlan* 
   if (p.nstage < 2 || p.b.fold_n * PIECE * 2 > p.nstage * STAGE) return false;
   *fp = p;
   return true;
+}
+
+// The plan of a (R, H, I, SM count): worked out once (two few-token plans
+// walk every CTA's range) and kept in a small table, as the call's other
+// plans are.
+bool fused_plan(long long R, long long H, long long I, int sm_count, FusedPlan* fp) {
+  struct Entry {
+    long long R, H, I;
+    int sms;
+    bool ok, used;
+    FusedPlan plan;
+  };
+  constexpr int kEntries = 16;
+  static Entry table[kEntries];
+  static int next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : table)
+      if (e.used && e.R == R && e.H == H && e.I == I && e.sms == sm_count) {
+        if (e.ok) *fp = e.plan;
+        return e.ok;
+      }
+  }
+  FusedPlan p{};
+  const bool ok = fused_plan_uncached(R, H, I, sm_count, &p);
+  std::lock_guard<std::mutex> lock(mu);
+  table[next] = Entry{R, H, I, sm_count, ok, true, p};
+  next = (next + 1) % kEntries;
+  if (ok) *fp = p;
+  return ok;
 }
 
 }  // namespace

@@ -88,8 +88,9 @@ def test_argument_errors_launch_nothing(L):
     for fl in (8, 16, 1 << 30, -1):
         assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, fl, 0)),
                                        ctypes.byref(n)) == 1
-    assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 2, 0)),
-                                   ctypes.byref(n)) == 0
+    for fl in (2, 4, 6):  # the dHidden overlap and the two-launch forward are valid flags
+        assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, fl, 0)),
+                                       ctypes.byref(n)) == 0
     assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 0, -5)),
                                    ctypes.byref(n)) == 1
     assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 1, 100)),

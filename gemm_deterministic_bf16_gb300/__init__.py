@@ -12,7 +12,8 @@ from .detffn import (  # noqa: F401
     detffn_forward_sharded, detffn_get_status, detffn_rank_tree_reduce, detffn_silu_tables,
     detffn_cvt_f32_bf16, detffn_forward_decode_noalloc, detffn_forward_decode_noalloc_status,
     detffn_forward_decode_noalloc_test_waits,
-    detffn_profile_read, detffn_profiling, detffn_selfcheck_node_add, detffn_selfcheck_pieces,
+    detffn_profile_read, detffn_profiling, detffn_selfcheck_fused_schedule, detffn_selfcheck_node_add,
+    detffn_selfcheck_pieces,
     detffn_tree_gemm, detffn_tree_gemm_leaves,
     detffn_wgrad_chunked,
     detffn_workspace_size, workspace,

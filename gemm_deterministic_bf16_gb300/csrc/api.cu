@@ -1300,6 +1300,12 @@ extern "C" detffn_status detffn_profile_read(detffn_handle h, int max, detffn_ke
   return DETFFN_OK;
 }
 
+extern "C" detffn_status detffn_selfcheck_fused_schedule(unsigned long long* cases, unsigned long long* failures) {
+  if (!cases || !failures) return DETFFN_ERR_INVALID_ARG;
+  *failures = tcs_selfcheck_fused_schedule(cases);
+  return DETFFN_OK;
+}
+
 extern "C" detffn_status detffn_selfcheck_pieces(int max_levels, unsigned long long* failures) {
   if (!failures || max_levels < 0 || max_levels > kTcsMaxLv) return DETFFN_ERR_INVALID_ARG;
   *failures = tcs_selfcheck_pieces(max_levels);

@@ -812,12 +812,11 @@ __global__ void __maxnreg__(128)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = (int)gridDim.x;
   const bool hasA = (int)blockIdx.x < f.nA;
-  int jB = ((int)blockIdx.x - f.nA) % P;
-  if (jB < 0) jB += P;
+  const int jB = fwd_block_of((int)blockIdx.x, f.nA, P);
   const bool hasB = jB < f.nB;
   const int nLA = hasA ? (GA << A.E) : 0;  // leaves of unit A (the whole K = H)
   const int nLB = hasB ? f.bG * GB : 0;     // leaves of unit B
-  const int treeB = hasB ? jB / B.fold_n : 0, rangeB = hasB ? jB % B.fold_n : 0;
+  const int treeB = hasB ? fwd_tree_of(jB, B.fold_n) : 0, rangeB = hasB ? fwd_range_of(jB, B.fold_n) : 0;
   const int kB0 = rangeB * f.bG * GB;       // unit B's first leaf along K = I
   const long long limit = A.spin > 0 ? A.spin : kDefaultSpin;
   if (__syncthreads_or(A.status != nullptr && *(volatile int*)A.status != 0)) return;
@@ -1011,7 +1010,7 @@ __global__ void __maxnreg__(128)
         if (row == 0 && !*abort_flag) {
           fence_proxy_async_global();
           __threadfence();
-          atomicAdd(f.ready + (int)blockIdx.x / f.per_range, 1);
+          atomicAdd(f.ready + fwd_tile_range((int)blockIdx.x, f.per_range), 1);
         }
       }
     }
@@ -1634,6 +1633,29 @@ bool fused_plan(long long R, long long H, long long I, int sm_count, FusedPlan* 
 }
 
 }  // namespace
+
+bool tcs_forward_fused_info(long long R, long long H, long long I, int sm_count, TcsFusedInfo* info) {
+  FusedPlan p;
+  if (!fused_plan(R, H, I, sm_count, &p)) return false;
+  TcsFusedInfo r;
+  r.P = p.P;
+  r.nA = p.nA;
+  r.nB = p.nB;
+  r.bG = p.bG;
+  r.GA = p.a.G;
+  r.GB = p.b.G;
+  r.EA = p.a.E;
+  r.EB = p.b.E;
+  r.fold_n = p.b.fold_n;
+  r.trees = p.b.T;
+  r.per_range = p.bG * p.b.G;
+  r.waiters = 2 * p.b.T;
+  r.nstage = p.nstage;
+  r.smem = 1024 + p.nstage * STAGE + p.slv * LV_BYTES + BAR_BYTES + XCH_BYTES;
+  r.scratch = p.b.scratch;
+  *info = r;
+  return true;
+}
 
 bool tcs_forward_fused_covers(long long R, long long H, long long I, int sm_count, size_t* scratch) {
   FusedPlan p;

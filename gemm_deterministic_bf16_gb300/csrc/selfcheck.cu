@@ -99,4 +99,55 @@ unsigned long long tcs_selfcheck_pieces(int max_levels) {
   return bad;
 }
 
+// Host check of the one-launch forward's schedule (see fwd_block_of): for
+// every covered (H, I, SMs) of a grid of shapes, each down block runs on
+// exactly one CTA, no CTA holds more than one tile or block, the tiles that
+// count into a range are exactly those whose 64 columns of h make up the K
+// range its blocks read, each range has one block per tree (so its waiters
+// are two per tree), the trees' blocks tile their K axis, and the fold of a
+// tree's pieces fits the pipeline stages.  Returns the failed cases.
+unsigned long long tcs_selfcheck_fused_schedule(unsigned long long* cases) {
+  static const long long dims[] = {256, 512, 768, 1024, 1536, 2048, 3072, 4096, 6144, 8192, 12288};
+  static const int sms_list[] = {1, 2, 8, 16, 66, 76, 132, 148, 152, 160};
+  unsigned long long bad = 0, n = 0;
+  for (long long H : dims)
+    for (long long I : dims)
+      for (int sms : sms_list) {
+        TcsFusedInfo f;
+        if (!tcs_forward_fused_info(8, H, I, sms, &f)) continue;
+        ++n;
+        bool ok = f.nA * 64LL == I && f.fold_n >= 2 && f.fold_n * f.trees == f.nB && f.nA <= f.P && f.nB <= f.P &&
+                  (long long)f.fold_n * f.bG * f.GB * 64 == I && ((long long)f.bG * f.fold_n == (1LL << f.EB)) &&
+                  f.per_range == f.bG * f.GB && f.waiters == 2 * f.trees && f.GB >= 2 &&
+                  f.fold_n * 128 * 32 * 2 <= f.nstage * (128 * 64 * 2 + 32 * 64 * 2) && f.smem <= 113 * 1024 &&
+                  f.scratch >= (size_t)f.nB * 128 * 32 * 2;
+        std::vector<int> blocks_seen(f.nB, 0), range_tiles(f.fold_n, 0), range_blocks(f.fold_n, 0);
+        for (int b = 0; b < f.P && ok; ++b) {
+          const int j = fwd_block_of(b, f.nA, f.P);
+          if (j < f.nB) {
+            ++blocks_seen[j];
+            const int tree = fwd_tree_of(j, f.fold_n), range = fwd_range_of(j, f.fold_n);
+            if (tree >= f.trees || range >= f.fold_n) ok = false;
+            else ++range_blocks[range];
+            // The block's K range of I, in 64-column leaves, and the tiles counted into its range.
+            const long long k0 = (long long)range * f.bG * f.GB, k1 = k0 + (long long)f.bG * f.GB;
+            for (int t = 0; t < f.nA && ok; ++t) {
+              const bool counted = fwd_tile_range(t, f.per_range) == range, inside = t >= k0 && t < k1;
+              if (counted != inside) ok = false;
+            }
+          }
+        }
+        for (int t = 0; t < f.nA && ok; ++t) {
+          const int r = fwd_tile_range(t, f.per_range);
+          if (r >= f.fold_n) ok = false;
+          else ++range_tiles[r];
+        }
+        for (int j = 0; j < f.nB && ok; ++j) ok = blocks_seen[j] == 1;
+        for (int r = 0; r < f.fold_n && ok; ++r) ok = range_tiles[r] == f.per_range && 2 * range_blocks[r] == f.waiters;
+        if (!ok) ++bad;
+      }
+  if (cases) *cases = n;
+  return bad;
+}
+
 }  // namespace detffn

@@ -139,6 +139,32 @@ cudaError_t launch_tcs_gateup_stacked(long long R, long long C, long long K, con
 // cudaErrorNotSupported, launching nothing, for shapes it does not cover
 // (tcs_forward_fused_covers false).
 bool tcs_forward_fused_covers(long long R, long long H, long long I, int sm_count, size_t* scratch);
+
+// The one-launch forward's unit schedule, shared by the kernel and the host
+// check: CTA b of P takes gate/up tile b when b < nA, then down block
+// j = fwd_block_of(b) when j < nB; block j is aligned block fwd_range_of(j)
+// of down tree fwd_tree_of(j) (fold_n blocks per tree); gate/up tile t
+// (64 columns of h) counts into range fwd_tile_range(t).
+__host__ __device__ inline int fwd_block_of(int b, int nA, int P) {
+  const int j = (b - nA) % P;
+  return j < 0 ? j + P : j;
+}
+__host__ __device__ inline int fwd_tree_of(int j, int fold_n) { return j / fold_n; }
+__host__ __device__ inline int fwd_range_of(int j, int fold_n) { return j % fold_n; }
+__host__ __device__ inline int fwd_tile_range(int t, int per_range) { return t / per_range; }
+
+// The one-launch forward's geometry for (R, H, I, SMs), for host checks.
+struct TcsFusedInfo {
+  int P, nA, nB, bG, GA, GB, EA, EB, fold_n, trees, per_range, waiters, nstage, smem;
+  size_t scratch;
+};
+bool tcs_forward_fused_info(long long R, long long H, long long I, int sm_count, TcsFusedInfo* info);
+
+// Host check of the one-launch forward's schedule over a set of shapes and
+// SM counts (every down block on one CTA, each range counting exactly the
+// gate/up tiles of its K range, waiter counts, shared-memory room); returns
+// the failed cases and sets *cases to the shapes it covered.
+unsigned long long tcs_selfcheck_fused_schedule(unsigned long long* cases);
 cudaError_t launch_tcs_forward_fused(long long R, long long H, long long I, const uint16_t* x, const uint16_t* Wg,
                                      const uint16_t* Wu, const uint16_t* Wd, uint16_t* h, uint16_t* gate,
                                      uint16_t* up, uint16_t* out, const uint16_t* silu, void* scratch,

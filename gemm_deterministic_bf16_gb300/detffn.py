@@ -394,6 +394,17 @@ def detffn_forward_decode_noalloc_test_waits(spin_limit=0, stall=0):
     _check(L.detffn_forward_decode_noalloc_test_waits(spin_limit, stall), "detffn_forward_decode_noalloc_test_waits")
 
 
+def detffn_selfcheck_fused_schedule():
+    """(shapes covered, failed cases) of the host check of the one-launch
+    forward's schedule (no GPU needed)."""
+    L = lib()
+    L.detffn_selfcheck_fused_schedule.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)] * 2
+    L.detffn_selfcheck_fused_schedule.restype = ctypes.c_int
+    c, n = ctypes.c_ulonglong(), ctypes.c_ulonglong()
+    _check(L.detffn_selfcheck_fused_schedule(ctypes.byref(c), ctypes.byref(n)), "detffn_selfcheck_fused_schedule")
+    return c.value, n.value
+
+
 def detffn_selfcheck_pieces(max_levels=8):
     """Failed cases of the host check of the few-token kernels' piece
     decomposition and fold codes (no GPU needed)."""

@@ -334,6 +334,17 @@ DETFFN_API detffn_status detffn_selfcheck_node_add(detffn_handle h, unsigned lon
  * pointer or max_levels outside [0, 8]. */
 DETFFN_API detffn_status detffn_selfcheck_pieces(int max_levels, unsigned long long *failures);
 
+/* Host check (no GPU needed) of the one-launch decode forward's schedule
+ * (see DETFFN_FLAG_SPLIT_FORWARD) over a grid of shapes (H, I in
+ * {256, ..., 12288}) and SM counts: each down-projection block runs on
+ * exactly one CTA, each range of I counts exactly the gate/up tiles whose
+ * columns of h its blocks read, the waiter counts match, the blocks tile each
+ * tree's K axis, and the fold fits the pipeline stages.  Writes the shapes
+ * covered to *cases and the failed ones to *failures; DETFFN_ERR_INVALID_ARG
+ * for a null pointer. */
+DETFFN_API detffn_status detffn_selfcheck_fused_schedule(unsigned long long *cases,
+                                                         unsigned long long *failures);
+
 /* Synchronises `stream`, then returns and clears the handle's device status
  * word (DETFFN_OK or DETFFN_ERR_TIMEOUT from a bounded wait).  The word is
  * sticky: once a wait has run out, every later streaming kernel launched

@@ -128,3 +128,19 @@ def test_piece_decomposition_and_fold_selfcheck():
     L.detffn_selfcheck_pieces.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_ulonglong)]
     assert L.detffn_selfcheck_pieces(9, ctypes.byref(n)) != 0          # out of range: an argument error
     assert L.detffn_selfcheck_pieces(8, None) != 0
+
+
+def test_fused_forward_schedule_selfcheck():
+    """The one-launch decode forward's schedule, checked on the host over a
+    grid of shapes and SM counts: every down block on one CTA, each range of
+    I counting exactly the gate/up tiles its blocks read, the waiter counts,
+    and the fold's room in the pipeline stages.  The benchmark shape (H = 4096,
+    I = 12288) is among the covered ones.  No GPU is needed."""
+    from gemm_deterministic_bf16_gb300 import build, detffn
+    build.build()
+    cases, failures = detffn.detffn_selfcheck_fused_schedule()
+    assert failures == 0
+    assert cases >= 50, cases
+    L = detffn.lib()
+    L.detffn_selfcheck_fused_schedule.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert L.detffn_selfcheck_fused_schedule(None, None) != 0

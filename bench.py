@@ -404,9 +404,10 @@ def run_ours(args):
         copies.append({k: dev(v) for k, v in d.items()})
     stream = torch.cuda.current_stream()
 
-    def fwd(M, c, out, ws, pth=None):
+    def fwd(M, c, out, ws, pth=None, flags=0):
         t = copies[c]
-        G.detffn_forward(t["x"][:M], t["Wg"], t["Wu"], t["Wd"], out=out, ws=ws, path=path if pth is None else pth)
+        G.detffn_forward(t["x"][:M], t["Wg"], t["Wu"], t["Wd"], out=out, ws=ws, path=path if pth is None else pth,
+                         flags=flags)
 
     def timed(fn, steps, warmup):
         for i in range(warmup):
@@ -473,6 +474,10 @@ def run_ours(args):
             extra["fwd_us_M%d_%s" % (M, name)] = 1e3 * max_over_ranks(ws_n, timed(
                 lambda i, M=M, pth=pth, wsm=wsm: fwd(M, i & 1, outs[M], wsm, pth), args.steps, args.warmup))
             del wsm
+        # The tensor family's two-launch form of the same forward (same bits).
+        extra["fwd_us_M%d_two_launch" % M] = 1e3 * max_over_ranks(ws_n, timed(
+            lambda i, M=M: fwd(M, i & 1, outs[M], wss[M], G.PATH_TENSOR, G.FLAG_SPLIT_FORWARD), args.steps,
+            args.warmup))
 
     # The M=32 training step (forward with saves + backward), unsharded and
     # with the I axis in k = 2, 4, 8 shards (tensor-parallel emulation: shard

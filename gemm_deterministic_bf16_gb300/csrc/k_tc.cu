@@ -88,7 +88,7 @@ template <int BN> struct TcGeo {
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int COLS = BN / HALVES;  // columns per epilogue thread
   static constexpr int WORDS = COLS / 2;    // packed BF16 pairs per stack level per thread
-  static constexpr int REG_LV = 2;                        // stack levels kept in registers
+  static constexpr int REG_LV = 3;                        // stack levels kept in registers
   static constexpr int LV_BYTES = BM * BN * 2;            // one shared-memory stack level
   static constexpr int BAR_BYTES = 512;
   // Output staging for one-leaf trees (G = 1: the weight gradients over few
@@ -585,14 +585,17 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
 
     if constexpr (GG >= 2) {
       // Blocks of four bottom groups (or the one or two groups of a shorter
-      // tree), whose level-0 and level-1 nodes stay in fixed registers; the
-      // binary counter above them (levels >= 2) lives in shared memory.
+      // tree), whose level-0 and level-1 nodes stay in fixed registers, as
+      // does the pending level-2 node (n2); the binary counter above them
+      // (levels >= 3) lives in shared memory, which leaves a 64-group tree
+      // room for four pipeline stages.
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const int pb = u % a.np, t = u / a.np;
         int tm, tn;
         tile_of(t, a, tm, tn);
         uint16_t* const outp = pb ? a.out2 : a.out;
         const long long r = (long long)tm * BM + row;
+        uint32_t n2[T::WORDS];  // the pending level-2 node (left child over four groups)
         for (int q = 0; q < Q && ok; q += 4) {
           // One copy of the group reader in a loop that is not unrolled (the
           // epilogue's speed is bound by instruction fetch, so its code is
@@ -620,32 +623,43 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
           }
           if (!ok) break;
           const int qq = q + (Q < 4 ? Q : 4) - 1;  // the last group of this block
-          // The binary counter above the register levels: fold the stored
-          // nodes of levels 2, 3, ... while the group index has those bits.
+          // The binary counter above the block: fold the pending level-2 node
+          // and then the stored nodes of levels 3, 4, ... while the group
+          // index has those bits.
           int l = 2;
-#pragma unroll 1
-          for (int m = 2; m < a.E && ((qq >> m) & 1); ++m) {
-            const uint32_t* src = stk_at<BN>(stk, m, ew, 0, lane);
+          if (a.E > 2 && ((qq >> 2) & 1)) {
 #pragma unroll
-            for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(src[w * 32], cur[w]);
-            l = m + 1;
+            for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n2[w], cur[w]);
+            l = 3;
+#pragma unroll 1
+            for (int m = 3; m < a.E && ((qq >> m) & 1); ++m) {
+              const uint32_t* src = stk_at<BN>(stk, m, ew, 0, lane);
+#pragma unroll
+              for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(src[w * 32], cur[w]);
+              l = m + 1;
+            }
           }
           if (qq != Q - 1) {
-            if (l == 2 && stg_n) {  // this warp's last output store has read its level-2 block
-              if (lane == 0) bulk_wait_read<0>();
-              __syncwarp();
-              stg_n = 0;
-            }
-            uint32_t* dst = stk_at<BN>(stk, l, ew, 0, lane);
+            if (l == 2) {
 #pragma unroll
-            for (int w = 0; w < T::WORDS; ++w) dst[w * 32] = cur[w];
-          } else if (a.o_tma && a.E >= 3) {
-            // Every stored level has just been folded: the warp's level-2
+              for (int w = 0; w < T::WORDS; ++w) n2[w] = cur[w];
+            } else {
+              if (l == 3 && stg_n) {  // this warp's last output store has read its level-3 block
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+                stg_n = 0;
+              }
+              uint32_t* dst = stk_at<BN>(stk, l, ew, 0, lane);
+#pragma unroll
+              for (int w = 0; w < T::WORDS; ++w) dst[w * 32] = cur[w];
+            }
+          } else if (a.o_tma && a.E >= 4) {
+            // Every stored level has just been folded: the warp's level-3
             // block stages its 32 rows x COLS columns in the swizzled layout
             // of a TMA box, which leaves as one bulk tensor store (clipped
             // at the output's edges) -- coalesced, where a row per thread is
             // not.
-            unsigned char* buf = reinterpret_cast<unsigned char*>(stk_at<BN>(stk, 2, ew, 0, 0));
+            unsigned char* buf = reinterpret_cast<unsigned char*>(stk_at<BN>(stk, 3, ew, 0, 0));
             __syncwarp();  // all lanes' reads of the level are done
 #pragma unroll
             for (int v = 0; v < T::COLS / 8; ++v)  // 16-byte chunk v of row `lane` at chunk v ^ (lane % 8)

@@ -217,15 +217,15 @@ __device__ __forceinline__ void load_w(unsigned char* dst, const CUtensorMap* mW
 }
 
 // The root of one bottom group, this thread's row and all tokens, from its
-// GG leaves in TMEM buffers lc .. lc + GG - 1 (taddr: the TMEM base plus
-// the warp's lane quarter): a lone leaf rounded once, l0 + l1, or
+// GG leaves in TMEM buffers lc .. lc + GG - 1 of NB (taddr: the TMEM base
+// plus the warp's lane quarter): a lone leaf rounded once, l0 + l1, or
 // l0 + (l1 + l2).  DUMP: the leaves also go to the leaf dump, as leaves
 // j0 .. j0 + GG - 1 of weight row crow.
-template <int GG, bool DUMP>
+template <int GG, bool DUMP, int NB = kNBuf>
 __device__ __forceinline__ void group_root(uint32_t taddr, uint32_t lc, uint32_t (&root)[WORDS], float* dmp,
                                            long long crow, int R, int C, int L, int j0) {
-  const uint32_t b0 = (uint32_t)((lc % kNBuf) * BN), b1 = (uint32_t)(((lc + 1) % kNBuf) * BN),
-                 b2 = (uint32_t)(((lc + 2) % kNBuf) * BN);
+  const uint32_t b0 = (uint32_t)((lc % NB) * BN), b1 = (uint32_t)(((lc + 1) % NB) * BN),
+                 b2 = (uint32_t)(((lc + 2) % NB) * BN);
 #pragma unroll
   for (int c = 0; c < BN / 16; ++c) {
     uint32_t v0[16];
@@ -705,17 +705,17 @@ __global__ void __maxnreg__(128)
 // counted in ready[range] (each tile's gate half counts itself once its h is
 // stored), and the last of the range's waiters resets both counters.  No unit
 // A waits on a unit B, so every wait ends once the tiles it needs run.
-// Pending levels of a unit's fold kept in registers (the rest in shared
-// memory): two, so that the epilogue fits its 128 registers.
+// Pending levels of a unit's fold kept in registers: two, so that the
+// epilogue fits its 128 registers.  The levels above them live in TMEM,
+// 16 columns each, after kFwdNBuf leaf buffers (six, not eight: the room
+// that the shared-memory stack would take goes to a fifth pipeline stage).
 constexpr int kFwdRegLv = 2;
-__host__ __device__ inline int fwd_smem_levels(int eA, int eB) {
-  const int e = eA > eB ? eA : eB;
-  return e > kFwdRegLv ? e - kFwdRegLv : 0;
-}
+constexpr int kFwdNBuf = 6;
+constexpr int kFwdStackCol = kFwdNBuf * BN;
+constexpr int kFwdMaxLevels = (kTmemCols - kFwdStackCol) / WORDS + kFwdRegLv;  // deepest unit fold
 
 struct FwdArgs {
   TcsArgs A, B;    // unit A geometry (stacked, direct), unit B geometry (folded trees)
-  int slv;         // pending levels in shared memory (fwd_smem_levels of both units)
   int nA, nB;      // gate/up tiles, down blocks
   int bG;          // groups per down block
   int per_range;   // gate/up tiles per down range (= bG * leaves per group)
@@ -732,11 +732,11 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 
 // Group root v (group q of a complete aligned block of 2^e groups, counted
 // from the block's start) into the block's pending stack (levels below RL in
-// registers, the rest in this thread's column of stk); true when v is then
-// the block's root.
+// registers, level m >= RL in TMEM columns tstk + WORDS (m - RL) of this
+// thread's lane); true when v is then the block's root.
 template <int RL>
 __device__ __forceinline__ bool fold_push(uint32_t (&v)[WORDS], int q, int e, uint32_t (&reg_lv)[RL][WORDS],
-                                          uint32_t* stk, int row) {
+                                          uint32_t tstk) {
   bool root = false, live = true;
 #pragma unroll
   for (int m = 0; m <= kTcsMaxLv; ++m) {
@@ -745,16 +745,23 @@ __device__ __forceinline__ bool fold_push(uint32_t (&v)[WORDS], int q, int e, ui
         root = true;
         live = false;
       } else if ((q >> m) & 1) {
+        if (m < RL) {
 #pragma unroll
-        for (int i = 0; i < WORDS; ++i) {
-          const uint32_t left = m < RL ? reg_lv[m < RL ? m : 0][i] : stk[((m - RL) * WORDS + i) * BM + row];
-          v[i] = add_bf16x2(left, v[i]);
+          for (int i = 0; i < WORDS; ++i) v[i] = add_bf16x2(reg_lv[m < RL ? m : 0][i], v[i]);
+        } else {
+          uint32_t left[WORDS];
+          tmem_ld16(tstk + (uint32_t)(WORDS * (m - RL)), left);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < WORDS; ++i) v[i] = add_bf16x2(left[i], v[i]);
         }
       } else {
+        if (m < RL) {
 #pragma unroll
-        for (int i = 0; i < WORDS; ++i) {
-          if (m < RL) reg_lv[m < RL ? m : 0][i] = v[i];
-          else stk[((m - RL) * WORDS + i) * BM + row] = v[i];
+          for (int i = 0; i < WORDS; ++i) reg_lv[m < RL ? m : 0][i] = v[i];
+        } else {
+          tmem_st16(tstk + (uint32_t)(WORDS * (m - RL)), v);
+          tmem_wait_st();
         }
         live = false;
       }
@@ -768,26 +775,26 @@ __device__ __forceinline__ bool fold_push(uint32_t (&v)[WORDS], int q, int e, ui
 // value: each group's root, pushed or merged, and the unit's root at the
 // end).  False when a wait ran out (root unfinished).
 template <int G>
-__device__ __forceinline__ bool unit_root(uint32_t taddr, uint32_t& lc, int e, uint32_t (&root)[WORDS], uint32_t* stk,
-                                          int row, int lane, Bars* bars, long long limit, volatile int* abort_flag,
-                                          int* status) {
+__device__ __forceinline__ bool unit_root(uint32_t taddr, uint32_t& lc, int e, uint32_t (&root)[WORDS], int lane,
+                                          Bars* bars, long long limit, volatile int* abort_flag, int* status) {
   uint32_t reg_lv[kFwdRegLv][WORDS];
   bool ok = true;
 #pragma unroll 1
   for (int q = 0; q < (1 << e); ++q) {
     for (int g = 0; g < G; ++g)
-      if (!wait_or_abort(&bars->accf[(lc + g) % kNBuf], (uint32_t)(((lc + g) / kNBuf) & 1), limit, abort_flag,
+      if (!wait_or_abort(&bars->accf[(lc + g) % kFwdNBuf], (uint32_t)(((lc + g) / kFwdNBuf) & 1), limit, abort_flag,
                          status))
         ok = false;
     if (__any_sync(0xffffffffu, !ok)) return false;
     tc_fence_after();
-    group_root<G, false>(taddr, lc, root, nullptr, 0, 0, 0, 0, 0);
+    group_root<G, false, kFwdNBuf>(taddr, lc, root, nullptr, 0, 0, 0, 0, 0);
     tc_fence_before();
     __syncwarp();
     if (lane == 0)
-      for (int g = 0; g < G; ++g) mbar_arrive(&bars->acce[(lc + g) % kNBuf]);
+      for (int g = 0; g < G; ++g) mbar_arrive(&bars->acce[(lc + g) % kFwdNBuf]);
     lc += G;
-    fold_push<kFwdRegLv>(root, q, e, reg_lv, stk, row);  // after the last group, root is the unit's root
+    // After the last group, root is the unit's root.
+    fold_push<kFwdRegLv>(root, q, e, reg_lv, taddr + (uint32_t)kFwdStackCol);
   }
   return true;
 }
@@ -802,11 +809,9 @@ __global__ void __maxnreg__(128)
   const TcsArgs& A = f.A;
   const TcsArgs& B = f.B;
   const int NS = A.nstage;
-  const int slv = f.slv;
   unsigned char* stages = smem;
-  uint32_t* stk = reinterpret_cast<uint32_t*>(smem + NS * STAGE);
-  Bars* bars = reinterpret_cast<Bars*>(smem + NS * STAGE + slv * LV_BYTES);
-  uint32_t* xch = reinterpret_cast<uint32_t*>(smem + NS * STAGE + slv * LV_BYTES + BAR_BYTES);
+  Bars* bars = reinterpret_cast<Bars*>(smem + NS * STAGE);
+  uint32_t* xch = reinterpret_cast<uint32_t*>(smem + NS * STAGE + BAR_BYTES);
   volatile int* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -883,7 +888,8 @@ __global__ void __maxnreg__(128)
     auto stage_free = [&](long long i) -> bool {
       if (i < NS) return true;
       const long long v = i - NS;
-      const bool wok = wait_or_abort(&bars->accf[v % kNBuf], (uint32_t)((v / kNBuf) & 1), limit, abort_flag, A.status);
+      const bool wok =
+          wait_or_abort(&bars->accf[v % kFwdNBuf], (uint32_t)((v / kFwdNBuf) & 1), limit, abort_flag, A.status);
       return __all_sync(0xffffffffu, wok) != 0;
     };
     auto issue_w = [&](long long i) {
@@ -969,7 +975,7 @@ __global__ void __maxnreg__(128)
     const long long nleaf = nLA + nLB;
     Ring rs, rb;
     bool ok = true;
-    for (long long n = 0; n < nleaf && ok; ++n, rs.next(NS), rb.next(kNBuf)) {
+    for (long long n = 0; n < nleaf && ok; ++n, rs.next(NS), rb.next(kFwdNBuf)) {
       const int st = rs.slot, b = rb.slot;
       const bool wok = wait_or_abort(&bars->acce[b], rb.phase ^ 1u, limit, abort_flag, A.status) &&
                        wait_or_abort(&bars->full[st], rs.phase, limit, abort_flag, A.status);
@@ -1001,7 +1007,7 @@ __global__ void __maxnreg__(128)
     uint32_t root[WORDS];
     if (hasA) {
       // The tile's root, then h (and the saves) through the stacked exchange.
-      bool ok = unit_root<GA>(taddr, lc, A.E, root, stk, row, lane, bars, limit, abort_flag, A.status);
+      bool ok = unit_root<GA>(taddr, lc, A.E, root, lane, bars, limit, abort_flag, A.status);
       if (ok) ok = stacked_store(A, bars, xch, 0, blockIdx.x, row, lane, root, limit, abort_flag);
       // The gate half (rows 0..63, two warps) stored h: count the tile in
       // its range once both warps are done (both always reach the barrier).
@@ -1020,8 +1026,7 @@ __global__ void __maxnreg__(128)
       if (threadIdx.x == kEpi0 * 32) bars->go = !*abort_flag;
       epi_sync();
       if (bars->go &&
-          unit_root<GB>(taddr, lc, B.E - hibit((unsigned)B.fold_n), root, stk, row, lane, bars, limit, abort_flag,
-                        B.status)) {
+          unit_root<GB>(taddr, lc, B.E - hibit((unsigned)B.fold_n), root, lane, bars, limit, abort_flag, B.status)) {
         int n = 0;
         emit_piece(B.slots + (size_t)jB * B.cap * PIECE, n, B.cap, row, root);
       }
@@ -1575,7 +1580,7 @@ namespace {
 // shape is not covered.
 struct FusedPlan {
   TcsPlan a, b;
-  int P, nA, nB, bG, nstage, slv;
+  int P, nA, nB, bG, nstage;
 };
 bool fused_plan_uncached(long long R, long long H, long long I, int sm_count, FusedPlan* fp) {
   if (R < 1 || R > BN || H < 1 || I < 1 || I % (BM / 2) || H % 8) return false;
@@ -1592,10 +1597,14 @@ bool fused_plan_uncached(long long R, long long H, long long I, int sm_count, Fu
   if (p.b.fold_n > kTcsRanges || p.b.cap != 1 || p.b.W / (1ll << p.b.E) > kTcsTickets) return false;
   // The down's K range of one block is bG * G leaves: that many 64-column tiles of h.
   if ((long long)p.bG * p.b.G * 64 * p.b.fold_n != I) return false;
-  p.slv = fwd_smem_levels(p.a.E, p.b.E - hibit((unsigned)p.b.fold_n));
-  p.nstage = (MAX_SMEM - 1024 - BAR_BYTES - p.slv * LV_BYTES - XCH_BYTES) / STAGE;
+  // The units' pending fold levels above the register ones live in TMEM.
+  const int eB = p.b.E - hibit((unsigned)p.b.fold_n);
+  if (p.a.E > kFwdMaxLevels || eB > kFwdMaxLevels) return false;
+  // Stages: all the shared memory two CTAs per SM allow, at most one per
+  // TMEM leaf buffer (a stage is reused once its leaf has been committed).
+  p.nstage = (MAX_SMEM - 1024 - BAR_BYTES - XCH_BYTES) / STAGE;
   if (p.nstage > MAX_STAGES) p.nstage = MAX_STAGES;
-  p.nstage &= ~1;
+  if (p.nstage > kFwdNBuf) p.nstage = kFwdNBuf;
   if (p.nstage < 2 || p.b.fold_n * PIECE * 2 > p.nstage * STAGE) return false;
   *fp = p;
   return true;
@@ -1651,7 +1660,7 @@ bool tcs_forward_fused_info(long long R, long long H, long long I, int sm_count,
   r.per_range = p.bG * p.b.G;
   r.waiters = 2 * p.b.T;
   r.nstage = p.nstage;
-  r.smem = 1024 + p.nstage * STAGE + p.slv * LV_BYTES + BAR_BYTES + XCH_BYTES;
+  r.smem = 1024 + p.nstage * STAGE + BAR_BYTES + XCH_BYTES;
   r.scratch = p.b.scratch;
   *info = r;
   return true;
@@ -1728,8 +1737,7 @@ cudaError_t launch_tcs_forward_fused(long long R, long long H, long long I, cons
   f.per_range = p.bG * p.b.G;
   f.waiters = 2 * p.b.T;
   f.ready = wt.tickets + kTcsTickets;
-  f.slv = p.slv;
-  const int smem = 1024 + p.nstage * STAGE + p.slv * LV_BYTES + BAR_BYTES + XCH_BYTES;
+  const int smem = 1024 + p.nstage * STAGE + BAR_BYTES + XCH_BYTES;
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, FwdArgs) =
       p.a.G == 2 ? (p.b.G == 2 ? k_tcs_fwd<2, 2> : k_tcs_fwd<2, 3>) : (p.b.G == 2 ? k_tcs_fwd<3, 2> : k_tcs_fwd<3, 3>);
   return launch_dependent(kern, dim3(p.P), kThreads, smem, st, m[0], m[1], m[2], m[3], m[4], f);

@@ -7,7 +7,7 @@ the first call does, and raises if the library is missing -- there is no CPU
 fallback.
 """
 from .detffn import (  # noqa: F401
-    BF16, F16, F32, FLAG_OVERLAP_DHIDDEN, FLAG_SPLIT_FORWARD, FLAG_TEST_STALL, OP_BACKWARD, OP_FORWARD, OP_FORWARD_SHARDED, OP_WGRAD_CHUNKED, PATH_AUTO,
+    BF16, F16, F32, FLAG_HOST_IO, FLAG_OVERLAP_DHIDDEN, FLAG_SPLIT_FORWARD, FLAG_TEST_STALL, OP_BACKWARD, OP_FORWARD, OP_FORWARD_SHARDED, OP_WGRAD_CHUNKED, PATH_AUTO,
     PATH_EXACT, PATH_TENSOR, DetFFNError, detffn_backward, detffn_forward,
     detffn_forward_sharded, detffn_get_status, detffn_rank_tree_reduce, detffn_silu_tables,
     detffn_cvt_f32_bf16, detffn_forward_decode_noalloc, detffn_forward_decode_noalloc_status,

@@ -170,7 +170,9 @@ struct Opts {
   long long spin_limit = 0;
 };
 
-detffn_status read_opts(const detffn_options* o, Opts* out) {
+// host_io_ok: the call takes DETFFN_FLAG_HOST_IO (the forward calls and
+// their workspace sizes); elsewhere the flag is an invalid argument.
+detffn_status read_opts(const detffn_options* o, Opts* out, bool host_io_ok = false) {
   Opts r;
   if (o) {
     if (o->leaf_width != 0 && o->leaf_width != kLeaf) return DETFFN_ERR_UNSUPPORTED;
@@ -178,8 +180,10 @@ detffn_status read_opts(const detffn_options* o, Opts* out) {
     if (!(o->shards == 0 || o->shards == 1 || o->shards == 2 || o->shards == 4 || o->shards == 8))
       return DETFFN_ERR_INVALID_ARG;
     if (o->spin_limit < 0) return DETFFN_ERR_INVALID_ARG;
-    if (o->flags & ~(DETFFN_FLAG_TEST_STALL | DETFFN_FLAG_OVERLAP_DHIDDEN | DETFFN_FLAG_SPLIT_FORWARD))
+    if (o->flags & ~(DETFFN_FLAG_TEST_STALL | DETFFN_FLAG_OVERLAP_DHIDDEN | DETFFN_FLAG_SPLIT_FORWARD |
+                     DETFFN_FLAG_HOST_IO))
       return DETFFN_ERR_INVALID_ARG;
+    if ((o->flags & DETFFN_FLAG_HOST_IO) && !host_io_ok) return DETFFN_ERR_INVALID_ARG;
     r.path = o->path;
     r.shards = o->shards ? o->shards : 1;
     r.flags = o->flags;
@@ -314,14 +318,17 @@ bool tcs_plan_fit(long long R, long long C, long long K, int np, int sms, const 
 
 struct FwdWs {
   uint16_t *gate, *up, *h, *parts, *dec_part;
+  uint16_t *x_stage, *out_stage;  // DETFFN_FLAG_HOST_IO: device copies of x and out
   unsigned* dec_cnt;
   TcsScratch tcs;
 };
 // Decode scratch: block-root planes (at most 8 blocks x 8 tokens x rows) and
 // one ticket per row tile (at most one tile per row).
 constexpr long long kDecPlanes = 64;
-FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k, int sms) {
+FwdWs plan_forward(Arena& a, long long M, long long H, long long I, int k, int sms, bool host_io = false) {
   FwdWs w;
+  w.x_stage = host_io ? a.take<uint16_t>(M * H) : nullptr;
+  w.out_stage = host_io ? a.take<uint16_t>(M * H) : nullptr;
   w.gate = a.take<uint16_t>(M * I);
   w.up = a.take<uint16_t>(M * I);
   w.h = a.take<uint16_t>(M * I);
@@ -385,11 +392,12 @@ ChunkWs plan_chunked(Arena& a, long long M, long long H, long long I, bool tenso
   return w;
 }
 
-size_t ws_bytes_for(int op, long long M, long long H, long long I, int k, bool tensor, int sms) {
+size_t ws_bytes_for(int op, long long M, long long H, long long I, int k, bool tensor, int sms,
+                    bool host_io = false) {
   Arena a(nullptr);
   switch (op) {
-    case DETFFN_OP_FORWARD: plan_forward(a, M, H, I, 1, sms); break;
-    case DETFFN_OP_FORWARD_SHARDED: plan_forward(a, M, H, I, k, sms); break;
+    case DETFFN_OP_FORWARD: plan_forward(a, M, H, I, 1, sms, host_io); break;
+    case DETFFN_OP_FORWARD_SHARDED: plan_forward(a, M, H, I, k, sms, host_io); break;
     case DETFFN_OP_BACKWARD: plan_backward(a, M, H, I, k, tensor, sms); break;
     case DETFFN_OP_WGRAD_CHUNKED: plan_chunked(a, M, H, I, tensor, sms); break;
     default: return 0;
@@ -728,15 +736,17 @@ detffn_status detffn_workspace_size(detffn_handle h, int op, long long M, long l
                                     int k, const detffn_options* opts, size_t* bytes) {
   if (!bytes) return DETFFN_ERR_INVALID_ARG;
   Opts o;
-  TRY(read_opts(opts, &o));
+  TRY(read_opts(opts, &o, true));
   TRY(check_sizes(M, H, I));
   if (op < DETFFN_OP_FORWARD || op > DETFFN_OP_WGRAD_CHUNKED) return DETFFN_ERR_INVALID_ARG;
+  const bool host_io = (o.flags & DETFFN_FLAG_HOST_IO) != 0;
+  if (host_io && op != DETFFN_OP_FORWARD && op != DETFFN_OP_FORWARD_SHARDED) return DETFFN_ERR_INVALID_ARG;
   if (op == DETFFN_OP_BACKWARD && k <= 1) k = o.shards;
   if (!(k == 1 || k == 2 || k == 4 || k == 8)) return DETFFN_ERR_INVALID_ARG;
   Family f;
   const bool bwd = op == DETFFN_OP_BACKWARD || op == DETFFN_OP_WGRAD_CHUNKED;
   TRY(pick_family(o, M, H, I, bwd, &f));
-  *bytes = ws_bytes_for(op, M, H, I, k, f == kTensor, h ? h->sm_count : kSizingSms);
+  *bytes = ws_bytes_for(op, M, H, I, k, f == kTensor, h ? h->sm_count : kSizingSms, host_io);
   return DETFFN_OK;
 }
 
@@ -771,6 +781,19 @@ detffn_status detffn_get_status(detffn_handle h, void* stream) {
 }  // extern "C"
 
 namespace {
+
+// The device-visible address of a page-locked host buffer of this process
+// (DETFFN_FLAG_HOST_IO); anything else is an invalid argument.
+detffn_status host_buffer(const void* p, void** dev) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // (clears the sticky-free error of the query)
+    return DETFFN_ERR_INVALID_ARG;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return DETFFN_ERR_INVALID_ARG;
+  *dev = at.devicePointer;
+  return DETFFN_OK;
+}
 
 detffn_status check_ffn_ptrs(const void* x, const void* Wg, const void* Wu, const void* Wd) {
   if (!x || !Wg || !Wu || !Wd) return DETFFN_ERR_INVALID_ARG;
@@ -830,10 +853,11 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
                            void* stream, const detffn_options* opts) {
   if (!h || !out) return DETFFN_ERR_INVALID_ARG;
   Opts o;
-  TRY(read_opts(opts, &o));
+  TRY(read_opts(opts, &o, true));
   set_waits(h, o);
   TRY(check_sizes(M, H, I));
   TRY(check_ffn_ptrs(x, Wg, Wu, Wd));
+  const bool host_io = (o.flags & DETFFN_FLAG_HOST_IO) != 0;
   if (!aligned2(out) || !aligned2(gate_save) || !aligned2(up_save)) return DETFFN_ERR_ALIGN;
   if ((gate_save == nullptr) != (up_save == nullptr)) return DETFFN_ERR_INVALID_ARG;
   if (!(k == 1 || k == 2 || k == 4 || k == 8)) return DETFFN_ERR_INVALID_ARG;
@@ -851,17 +875,31 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
   }
   Family f;
   TRY(pick_family(o, M, H, I, false, &f));
-  if (f == kTensor && (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))) {
+  if (f == kTensor && ((!host_io && !aligned16(x)) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd))) {
     if (o.path == DETFFN_PATH_TENSOR) return DETFFN_ERR_ALIGN;
     f = kExact;
   }
   TRY(check_ws(ws, ws_bytes,
-               ws_bytes_for(k > 1 ? DETFFN_OP_FORWARD_SHARDED : DETFFN_OP_FORWARD, M, H, I, k, false, h->sm_count)));
+               ws_bytes_for(k > 1 ? DETFFN_OP_FORWARD_SHARDED : DETFFN_OP_FORWARD, M, H, I, k, false, h->sm_count,
+                            host_io)));
   if (M == 0) return DETFFN_OK;
   TRYCU(cudaSetDevice(h->device));
   cudaStream_t st = (cudaStream_t)stream;
   Arena a(ws);
-  FwdWs w = plan_forward(a, M, H, I, k, h->sm_count);
+  FwdWs w = plan_forward(a, M, H, I, k, h->sm_count, host_io);
+  void* out_host = nullptr;  // DETFFN_FLAG_HOST_IO: where out goes back to
+  if (host_io) {
+    // x comes in over the host link to its staged copy, which the kernels
+    // read; out is formed in its staged copy and goes back at the end.
+    void* x_host = nullptr;
+    TRY(host_buffer(x, &x_host));
+    TRY(host_buffer(out, &out_host));
+    TRY(timed(h, st, "host_copy", 2.0 * M * H, 0.0, [&] {
+      return cu(launch_copy(x_host, w.x_stage, 2 * M * H, h->sm_count, st));
+    }));
+    x = w.x_stage;
+    out = w.out_stage;
+  }
   uint16_t* gate = gate_save ? (uint16_t*)gate_save : w.gate;
   uint16_t* up = up_save ? (uint16_t*)up_save : w.up;
   const uint16_t* X = (const uint16_t*)x;
@@ -902,10 +940,15 @@ detffn_status forward_impl(detffn_handle h, const void* x, const void* Wg, const
       }
     }
   }
-  if (k == 1) return DETFFN_OK;
-  const void* parts[8];
-  for (int s = 0; s < k; ++s) parts[s] = w.parts + (long long)s * M * H;
-  return rank_tree_bf16(h, parts, k, out, M * H, st);
+  if (k > 1) {
+    const void* parts[8];
+    for (int s = 0; s < k; ++s) parts[s] = w.parts + (long long)s * M * H;
+    TRY(rank_tree_bf16(h, parts, k, out, M * H, st));
+  }
+  if (!host_io) return DETFFN_OK;
+  return timed(h, st, "host_copy", 2.0 * M * H, 0.0, [&] {
+    return cu(launch_copy(out, out_host, 2 * M * H, h->sm_count, st));
+  });
 }
 
 }  // namespace

@@ -123,6 +123,10 @@ cudaError_t launch_silu_bwd(const uint16_t* dh, const uint16_t* g, const uint16_
 // out = rne_bf16(T(g[0..n)) + T(u[0..n))), T the BF16 rank tree (n in {2,4,8}).
 cudaError_t launch_rank_tree_add_bf16(const void* const* g, const void* const* u, int n, void* out, long long count,
                                       int sm_count, cudaStream_t st);
+// dst[0 .. bytes) = src[0 .. bytes) (bytes even) by a kernel of plain loads
+// and stores: either side may be page-locked host memory (its device-visible
+// address), which the GPU then reads or writes over the host link.
+cudaError_t launch_copy(const void* src, void* dst, long long bytes, int sm_count, cudaStream_t st);
 // out = rne(a + b).
 cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out, long long n,
                             cudaStream_t st);

@@ -115,6 +115,18 @@ __global__ void k_add_bf16(const uint16_t* __restrict__ a, const uint16_t* __res
     out[i] = f2bf(__fadd_rn(bf2f(a[i]), bf2f(b[i])));
 }
 
+// Plain copy, 16 bytes (or 2 bytes) a thread per step: every thread's loads
+// are independent, so a copy over the host link keeps as many requests in
+// flight as it has threads.
+template <class V>
+__global__ void k_copy(const V* __restrict__ src, V* __restrict__ dst, long long n) {
+  grid_dep_wait();  // the source may be the previous kernel's output
+  grid_dep_launch();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 // ----------------------------- rank tree ---------------------------------
 
 struct Bufs {
@@ -373,6 +385,22 @@ cudaError_t launch_add_bf16(const uint16_t* a, const uint16_t* b, uint16_t* out,
                             cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   return launch_dependent(k_add_bf16, dim3(grid_for(n, 4096)), kThreads, 0, st, a, b, out, n);
+}
+
+cudaError_t launch_copy(const void* src, void* dst, long long bytes, int sm_count, cudaStream_t st) {
+  if (bytes <= 0) return cudaSuccess;
+  if ((bytes & 1) != 0) return cudaErrorInvalidValue;
+  const long long cap = 8ll * (sm_count > 0 ? sm_count : 1);  // blocks: one wave of small CTAs at most
+  if ((((uintptr_t)src | (uintptr_t)dst | (uintptr_t)bytes) & 15u) == 0) {
+    const long long n = bytes / 16;
+    const long long g = (n + kThreads - 1) / kThreads;
+    return launch_dependent(k_copy<uint4>, dim3((unsigned)(g < cap ? g : cap)), kThreads, 0, st,
+                            static_cast<const uint4*>(src), static_cast<uint4*>(dst), n);
+  }
+  const long long n = bytes / 2;
+  const long long g = (n + kThreads - 1) / kThreads;
+  return launch_dependent(k_copy<uint16_t>, dim3((unsigned)(g < cap ? g : cap)), kThreads, 0, st,
+                          static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), n);
 }
 
 cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long count, int dtype,

@@ -40,6 +40,7 @@ class DetFFNError(RuntimeError):
 FLAG_TEST_STALL = 1
 FLAG_OVERLAP_DHIDDEN = 2
 FLAG_SPLIT_FORWARD = 4
+FLAG_HOST_IO = 8
 
 
 class Options(ctypes.Structure):
@@ -140,16 +141,37 @@ def _bf16(*ts):
                 raise ValueError("expected contiguous CUDA bfloat16 tensors")
 
 
-def detffn_workspace_size(op, M, H, I, k=1, path=PATH_AUTO, device=None):
+def _bf16_host(*ts):
+    for t in ts:
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError("FLAG_HOST_IO: expected contiguous pinned (page-locked) CPU bfloat16 tensors")
+
+
+def _io(x, out, M, H, device, flags):
+    """x and out of a forward: device tensors, or pinned host tensors under
+    FLAG_HOST_IO (out allocated where it is None)."""
+    if flags & FLAG_HOST_IO:
+        if out is None:
+            out = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
+        _bf16_host(x, out)
+    else:
+        if out is None:
+            out = torch.empty((M, H), dtype=torch.bfloat16, device=device)
+        _bf16(x, out)
+    return out
+
+
+def detffn_workspace_size(op, M, H, I, k=1, path=PATH_AUTO, device=None, flags=0):
     n = ctypes.c_size_t()
-    _check(lib().detffn_workspace_size(handle(device), op, M, H, I, k, _opts(path, 1),
+    _check(lib().detffn_workspace_size(handle(device), op, M, H, I, k, _opts(path, 1, 0, flags),
                                        ctypes.byref(n)), "detffn_workspace_size")
     return n.value
 
 
-def workspace(op, M, H, I, k=1, path=PATH_AUTO, device=None):
-    """A caller-owned scratch buffer of the size the call needs."""
-    n = detffn_workspace_size(op, M, H, I, k, path, device)
+def workspace(op, M, H, I, k=1, path=PATH_AUTO, device=None, flags=0):
+    """A caller-owned scratch buffer of the size the call needs (flags:
+    FLAG_HOST_IO for forwards on host buffers)."""
+    n = detffn_workspace_size(op, M, H, I, k, path, device, flags)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
 
 
@@ -158,36 +180,38 @@ def detffn_forward(x, Wg, Wu, Wd, out=None, gate_save=None, up_save=None, ws=Non
     """out = down(silu(gate) * up); x [M,H], Wg/Wu [I,H], Wd [H,I].  Pass
     gate_save/up_save ([M,I]) to keep gate and up (training mode).
     spin_limit and flags go to detffn_options (flags: FLAG_TEST_STALL for
-    tests of the failure path only)."""
-    _bf16(x, Wg, Wu, Wd, out, gate_save, up_save)
+    tests of the failure path only; FLAG_HOST_IO: x and out are pinned CPU
+    tensors, moved by the call itself; out is complete once the stream has
+    passed the call)."""
+    _bf16(Wg, Wu, Wd, gate_save, up_save)
     M, H = x.shape
     I = Wg.shape[0]
-    if out is None:
-        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    dev = Wg.device
+    out = _io(x, out, M, H, dev, flags)
     if ws is None:
-        ws = workspace(OP_FORWARD, M, H, I, 1, path, x.device)
-    _check(lib().detffn_forward(handle(x.device), _ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(out),
+        ws = workspace(OP_FORWARD, M, H, I, 1, path, dev, flags & FLAG_HOST_IO)
+    _check(lib().detffn_forward(handle(dev), _ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(out),
                                 _ptr(gate_save), _ptr(up_save), M, H, I, _ptr(ws), ws.numel(),
-                                _stream(x.device, stream), _opts(path, 1, spin_limit, flags)),
+                                _stream(dev, stream), _opts(path, 1, spin_limit, flags)),
            "detffn_forward")
     return out
 
 
 def detffn_forward_sharded(x, Wg, Wu, Wd, k, out=None, gate_save=None, up_save=None, ws=None,
-                           path=PATH_AUTO, stream=None):
+                           path=PATH_AUTO, stream=None, flags=0):
     """Forward with k in {1,2,4,8} tensor-parallel shards of I emulated on one
-    GPU; the same bits as detffn_forward."""
-    _bf16(x, Wg, Wu, Wd, out, gate_save, up_save)
+    GPU; the same bits as detffn_forward (flags as there)."""
+    _bf16(Wg, Wu, Wd, gate_save, up_save)
     M, H = x.shape
     I = Wg.shape[0]
-    if out is None:
-        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    dev = Wg.device
+    out = _io(x, out, M, H, dev, flags)
     if ws is None:
-        ws = workspace(OP_FORWARD_SHARDED, M, H, I, k, path, x.device)
-    _check(lib().detffn_forward_sharded(handle(x.device), _ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd),
+        ws = workspace(OP_FORWARD_SHARDED, M, H, I, k, path, dev, flags & FLAG_HOST_IO)
+    _check(lib().detffn_forward_sharded(handle(dev), _ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd),
                                         _ptr(out), _ptr(gate_save), _ptr(up_save), M, H, I, k,
-                                        _ptr(ws), ws.numel(), _stream(x.device, stream),
-                                        _opts(path)), "detffn_forward_sharded")
+                                        _ptr(ws), ws.numel(), _stream(dev, stream),
+                                        _opts(path, 1, 0, flags)), "detffn_forward_sharded")
     return out
 
 

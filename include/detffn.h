@@ -81,7 +81,12 @@ typedef enum { DETFFN_PATH_AUTO = 0, DETFFN_PATH_EXACT = 1, DETFFN_PATH_TENSOR =
  * CTAs stop with nothing in flight and the call's outputs are left
  * unfinished; detffn_get_status then returns DETFFN_ERR_TIMEOUT.  The fault
  * is made by withholding work, never by a bad address or a trap. */
-enum { DETFFN_FLAG_TEST_STALL = 1, DETFFN_FLAG_OVERLAP_DHIDDEN = 2, DETFFN_FLAG_SPLIT_FORWARD = 4 };
+enum {
+    DETFFN_FLAG_TEST_STALL = 1,
+    DETFFN_FLAG_OVERLAP_DHIDDEN = 2,
+    DETFFN_FLAG_SPLIT_FORWARD = 4,
+    DETFFN_FLAG_HOST_IO = 8
+};
 /* DETFFN_FLAG_OVERLAP_DHIDDEN (detffn_backward with options->shards = k > 1;
  * PR #325, "Communication overlap assessment"): the rank tree of the gate
  * contribution's shard roots runs on a second stream of the handle while the
@@ -93,7 +98,18 @@ enum { DETFFN_FLAG_TEST_STALL = 1, DETFFN_FLAG_OVERLAP_DHIDDEN = 2, DETFFN_FLAG_
  * assessment": the gate/up to down dependency taken per K range of the down
  * projection, inside the launch) wherever the shape allows; this flag asks
  * for the two-launch form instead (gate/up with SiLU * up, then down).  The
- * bits are the same. */
+ * bits are the same.
+ * DETFFN_FLAG_HOST_IO (detffn_forward, detffn_forward_sharded, and
+ * detffn_workspace_size for their ops): x and out are page-locked host
+ * buffers of this process (cudaHostAlloc, or registered with
+ * cudaHostRegister); the weights, gate_save, up_save and ws stay device
+ * memory.  The call reads x over the host link into the workspace and writes
+ * out back to the host buffer with its own copy kernels, on `stream` and in
+ * stream order (no host synchronization inside the call: out is complete
+ * once the stream has reached the end of the call).  The workspace must be
+ * sized with the flag (it holds the two staged copies).  x or out not
+ * page-locked host memory: DETFFN_ERR_INVALID_ARG.  The bits are those of
+ * the call on device buffers.  Other calls: DETFFN_ERR_INVALID_ARG. */
 
 typedef struct {
     int leaf_width;        /* 64; anything else returns DETFFN_ERR_UNSUPPORTED */

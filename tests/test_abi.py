@@ -85,12 +85,26 @@ def test_argument_errors_launch_nothing(L):
     n = ctypes.c_size_t()
     assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, bad, ctypes.byref(n)) == 4
     # Unknown option flag bits and a negative poll limit are argument errors.
-    for fl in (8, 16, 1 << 30, -1):
+    for fl in (16, 32, 1 << 30, -1):
         assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, fl, 0)),
                                        ctypes.byref(n)) == 1
-    for fl in (2, 4, 6):  # the dHidden overlap and the two-launch forward are valid flags
+    for fl in (2, 4, 6, 8):  # dHidden overlap, two-launch forward, host buffers: valid flags
         assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, fl, 0)),
                                        ctypes.byref(n)) == 0
+    # Host buffers (flag 8): the forward's workspace holds the staged x and
+    # out (two 256-byte-aligned blocks of M*H BF16 here); the backward and
+    # the chunked weight gradients do not take the flag.
+    plain, hio = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 0, 0)),
+                                   ctypes.byref(plain)) == 0
+    assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 8, 0)),
+                                   ctypes.byref(hio)) == 0
+    assert hio.value == plain.value + 512
+    assert L.detffn_workspace_size(None, 1, 1, 64, 128, 2, ctypes.byref(Options(64, 0, 1, 8, 0)),
+                                   ctypes.byref(hio)) == 0
+    for op in (2, 3):
+        assert L.detffn_workspace_size(None, op, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 8, 0)),
+                                       ctypes.byref(n)) == 1
     assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 0, -5)),
                                    ctypes.byref(n)) == 1
     assert L.detffn_workspace_size(None, 0, 1, 64, 64, 1, ctypes.byref(Options(64, 0, 1, 1, 100)),

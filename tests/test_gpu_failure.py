@@ -89,7 +89,7 @@ def test_unknown_flag_is_rejected(G):
     w = torch.zeros(768, 256, dtype=torch.bfloat16, device="cuda")
     wd = torch.zeros(256, 768, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(G.DetFFNError) as e:
-        G.detffn_forward(x, w, w, wd, flags=8)
+        G.detffn_forward(x, w, w, wd, flags=16)
     assert e.value.status == 1
     with pytest.raises(G.DetFFNError) as e:
         G.detffn_forward(x, w, w, wd, spin_limit=-1)

@@ -176,14 +176,19 @@ __device__ __forceinline__ float rank_tree(const float* v) {
 }
 
 // VEC = bytes moved per input per step (16, 4 or the element size).
+// Elements [0, head) are taken one at a time and the vector steps start at
+// element head, through Bv (the buffers advanced by head elements: where
+// every buffer sits the same number of bytes past a VEC-byte boundary, head
+// elements bring them all onto the next one); the tail after the last whole
+// vector, one at a time as well.
 template <int DT, int N, int VEC>
-__global__ void __launch_bounds__(kThreads) k_rank_tree(Bufs B, long long count) {
+__global__ void __launch_bounds__(kThreads) k_rank_tree(Bufs B, Bufs Bv, long long count, long long head) {
   grid_dep_wait();  // the inputs may be the previous kernel's outputs
   grid_dep_launch();
   constexpr int E = Elt<DT>::kBytes;
   constexpr int PER = VEC / E;  // elements per step
   constexpr bool kScalar = (VEC == E);
-  const long long nvec = kScalar ? 0 : count / PER;
+  const long long nvec = kScalar ? 0 : (count - head) / PER;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long t0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   for (long long v = t0; v < nvec; v += stride) {
@@ -191,10 +196,10 @@ __global__ void __launch_bounds__(kThreads) k_rank_tree(Bufs B, long long count)
 #pragma unroll
     for (int s = 0; s < N; ++s) {
       if (VEC == 16) {
-        const uint4 q = __ldcs(reinterpret_cast<const uint4*>(B.in[s]) + v);
+        const uint4 q = __ldcs(reinterpret_cast<const uint4*>(Bv.in[s]) + v);
         w[s][0] = q.x; w[s][1] = q.y; w[s][2] = q.z; w[s][3] = q.w;
       } else {
-        w[s][0] = reinterpret_cast<const uint32_t*>(B.in[s])[v];
+        w[s][0] = reinterpret_cast<const uint32_t*>(Bv.in[s])[v];
       }
     }
     uint32_t o[VEC / 4 > 0 ? VEC / 4 : 1];
@@ -217,12 +222,18 @@ __global__ void __launch_bounds__(kThreads) k_rank_tree(Bufs B, long long count)
       }
     }
     if (VEC == 16)
-      reinterpret_cast<uint4*>(B.out)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+      reinterpret_cast<uint4*>(Bv.out)[v] = make_uint4(o[0], o[1], o[2], o[3]);
     else
-      reinterpret_cast<uint32_t*>(B.out)[v] = o[0];
+      reinterpret_cast<uint32_t*>(Bv.out)[v] = o[0];
   }
-  // Scalar tail (all of it when PER == 1).
-  for (long long i = nvec * PER + t0; i < count; i += stride) {
+  // Scalar head and tail (all of it when PER == 1).
+  for (long long i = t0; i < head; i += stride) {
+    float x[N];
+#pragma unroll
+    for (int s = 0; s < N; ++s) x[s] = Elt<DT>::ld(B.in[s], i);
+    Elt<DT>::st(B.out, i, rank_tree<DT, N>(x));
+  }
+  for (long long i = head + nvec * PER + t0; i < count; i += stride) {
     float x[N];
 #pragma unroll
     for (int s = 0; s < N; ++s) x[s] = Elt<DT>::ld(B.in[s], i);
@@ -299,7 +310,8 @@ cudaError_t launch_rta_n(const Bufs2& B, long long count, bool v16, int sm_count
 }
 
 template <int DT, int N>
-cudaError_t launch_rt_n(const Bufs& B, long long count, int align_all, int sm_count, cudaStream_t st) {
+cudaError_t launch_rt_n(const Bufs& B, long long count, long long head, int align_all, int sm_count,
+                        cudaStream_t st) {
   constexpr int E = Elt<DT>::kBytes;
   int vec = E;
   if (align_all % 16 == 0) vec = 16;
@@ -310,18 +322,38 @@ cudaError_t launch_rt_n(const Bufs& B, long long count, int align_all, int sm_co
   const long long cap = (long long)sm_count * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (vec == 16) return launch_dependent(k_rank_tree<DT, N, 16>, dim3((unsigned)blocks), kThreads, 0, st, B, count);
-  if (vec == 4) return launch_dependent(k_rank_tree<DT, N, 4>, dim3((unsigned)blocks), kThreads, 0, st, B, count);
-  return launch_dependent(k_rank_tree<DT, N, E>, dim3((unsigned)blocks), kThreads, 0, st, B, count);
+  Bufs Bv = B;
+  for (int s = 0; s < N; ++s) Bv.in[s] = B.in[s] + head * E;
+  Bv.out = B.out + head * E;
+  if (vec == 16) return launch_dependent(k_rank_tree<DT, N, 16>, dim3((unsigned)blocks), kThreads, 0, st, B, Bv, count, head);
+  if (vec == 4) return launch_dependent(k_rank_tree<DT, N, 4>, dim3((unsigned)blocks), kThreads, 0, st, B, Bv, count, head);
+  return launch_dependent(k_rank_tree<DT, N, E>, dim3((unsigned)blocks), kThreads, 0, st, B, B, count, 0ll);
 }
 
 template <int DT>
-cudaError_t launch_rt_dt(const Bufs& B, int n, long long count, int align_all, int sm_count, cudaStream_t st) {
+cudaError_t launch_rt_dt(const Bufs& B, int n, long long count, int sm_count, cudaStream_t st) {
+  // Where every buffer sits the same number of bytes past a 16-byte
+  // boundary, the first `head` elements bring them all onto the next one.
+  constexpr int E = Elt<DT>::kBytes;
+  const uintptr_t r = (uintptr_t)B.out & 15u;
+  bool same = true;
+  for (int s = 0; s < n; ++s) same = same && ((uintptr_t)B.in[s] & 15u) == r;
+  long long head = 0;
+  if (same && r != 0 && r % E == 0) {
+    head = (long long)((16 - r) / E);
+    if (head > count) head = count;
+  }
+  // Largest power of two (<= 16) dividing every address from element head on.
+  uintptr_t acc = (uintptr_t)(B.out + head * E);
+  for (int s = 0; s < n; ++s) acc |= (uintptr_t)(B.in[s] + head * E);
+  int align_all = 16;
+  while (align_all > 1 && (acc % (uintptr_t)align_all) != 0) align_all >>= 1;
+  if (align_all < 4) head = 0;  // no common boundary: element by element from the start
   switch (n) {
-    case 1: return launch_rt_n<DT, 1>(B, count, align_all, sm_count, st);
-    case 2: return launch_rt_n<DT, 2>(B, count, align_all, sm_count, st);
-    case 4: return launch_rt_n<DT, 4>(B, count, align_all, sm_count, st);
-    case 8: return launch_rt_n<DT, 8>(B, count, align_all, sm_count, st);
+    case 1: return launch_rt_n<DT, 1>(B, count, head, align_all, sm_count, st);
+    case 2: return launch_rt_n<DT, 2>(B, count, head, align_all, sm_count, st);
+    case 4: return launch_rt_n<DT, 4>(B, count, head, align_all, sm_count, st);
+    case 8: return launch_rt_n<DT, 8>(B, count, head, align_all, sm_count, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -407,19 +439,12 @@ cudaError_t launch_rank_tree(const void* const* in, int n, void* out, long long 
                              int sm_count, cudaStream_t st) {
   if (count <= 0) return cudaSuccess;
   Bufs B{};
-  uintptr_t acc = (uintptr_t)out;
-  for (int s = 0; s < n; ++s) {
-    B.in[s] = static_cast<const unsigned char*>(in[s]);
-    acc |= (uintptr_t)in[s];
-  }
+  for (int s = 0; s < n; ++s) B.in[s] = static_cast<const unsigned char*>(in[s]);
   B.out = static_cast<unsigned char*>(out);
-  // Largest power of two (<= 16) dividing every address.
-  int align_all = 16;
-  while (align_all > 1 && (acc % (uintptr_t)align_all) != 0) align_all >>= 1;
   switch (dtype) {
-    case DETFFN_F32: return launch_rt_dt<DETFFN_F32>(B, n, count, align_all, sm_count, st);
-    case DETFFN_F16: return launch_rt_dt<DETFFN_F16>(B, n, count, align_all, sm_count, st);
-    case DETFFN_BF16: return launch_rt_dt<DETFFN_BF16>(B, n, count, align_all, sm_count, st);
+    case DETFFN_F32: return launch_rt_dt<DETFFN_F32>(B, n, count, sm_count, st);
+    case DETFFN_F16: return launch_rt_dt<DETFFN_F16>(B, n, count, sm_count, st);
+    case DETFFN_BF16: return launch_rt_dt<DETFFN_BF16>(B, n, count, sm_count, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -59,6 +59,26 @@ def test_offset_views_and_tails(G, oracle_mod, dt, offset):
     assert not host(out_base[:offset]).any() and not host(out_base[offset + count:]).any()
 
 
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("offsets,count", [((1, 1, 1, 1, 0), 4093), ((2, 3, 2), 70001), ((3, 3, 3), 3),
+                                           ((1, 1, 1, 1, 1), 9), ((0, 1, 2, 3, 3), 1027)])
+def test_mixed_offsets_and_short_heads(G, oracle_mod, dt, offsets, count):
+    """Buffers at different offsets from the 16-byte grid (no common boundary:
+    element by element or 4-byte steps), and counts shorter than the head
+    that a common offset would take one element at a time."""
+    tdt, esz, odt = DT[dt]
+    n = len(offsets) - 1  # input offsets, then the output's
+    bufs = rank_tree_inputs(n, count + 8, dt, seed=count)
+    ins = [_to_dev(b, tdt)[o:o + count] for b, o in zip(bufs, offsets)]
+    oo = offsets[-1]
+    out_base = torch.zeros(count + 8, dtype=tdt, device="cuda")
+    out = out_base[oo:oo + count]
+    G.detffn_rank_tree_reduce(ins, out=out)
+    ref = oracle_mod.rank_tree([b[o:o + count] for b, o in zip(bufs, offsets)], odt)
+    assert mismatches(host(out), ref) == 0
+    assert not host(out_base[:oo]).any() and not host(out_base[oo + count:]).any()
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_in_place(G, oracle_mod, dt):
     tdt, esz, odt = DT[dt]

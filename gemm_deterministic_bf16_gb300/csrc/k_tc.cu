@@ -597,28 +597,50 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
         const long long r = (long long)tm * BM + row;
         uint32_t n2[T::WORDS];  // the pending level-2 node (left child over four groups)
         for (int q = 0; q < Q && ok; q += 4) {
-          // One copy of the group reader in a loop that is not unrolled (the
-          // epilogue's speed is bound by instruction fetch, so its code is
-          // kept small): cur takes the group's root and then the node over
-          // the groups read so far in this block; n0 keeps the root of group
-          // q (then q+2), n1 the node over groups q, q+1.
           uint32_t n0[T::WORDS], n1[T::WORDS], cur[T::WORDS];
-#pragma unroll 1
-          for (int k = 0; k < 4 && k < Q; ++k) {
-            if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { cur[w] = g; }, pb, r, tn, q + k)) break;
-            if (k & 1) {
-#pragma unroll
-              for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n0[w], cur[w]);
-            }
-            if (k == 3) {
-#pragma unroll
-              for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n1[w], cur[w]);
-            } else if (k == 1) {
-#pragma unroll
-              for (int w = 0; w < T::WORDS; ++w) n1[w] = cur[w];
+          if constexpr (GG == 2) {
+            // The block's four group readers hand each root word straight to
+            // the node it enters, so that no node is copied: n0 takes the
+            // root of group q (then of q+2), n1 the node over groups q, q+1,
+            // and cur the node over the block (over all of a shorter tree's
+            // one or two groups).
+            if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q)) break;
+            if (Q >= 2 &&
+                !group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n1[w] = node2(n0[w], g); }, pb, r, tn, q + 1))
+              break;
+            if (Q >= 4) {
+              if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q + 2)) break;
+              if (!group_root<BN, GG, DUMP>(
+                      e, a, [&](int w, uint32_t g) { cur[w] = node2(n1[w], node2(n0[w], g)); }, pb, r, tn, q + 3))
+                break;
             } else {
 #pragma unroll
-              for (int w = 0; w < T::WORDS; ++w) n0[w] = cur[w];
+              for (int w = 0; w < T::WORDS; ++w) cur[w] = Q == 2 ? n1[w] : n0[w];
+            }
+          } else {
+            // Three-leaf groups hold a partial node of their own (registers
+            // for four copies of the reader are not there): one copy of the
+            // group reader in a loop that is not unrolled; cur takes the
+            // group's root and then the node over the groups read so far in
+            // this block; n0 keeps the root of group q (then q+2), n1 the
+            // node over groups q, q+1.
+#pragma unroll 1
+            for (int k = 0; k < 4 && k < Q; ++k) {
+              if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { cur[w] = g; }, pb, r, tn, q + k)) break;
+              if (k & 1) {
+#pragma unroll
+                for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n0[w], cur[w]);
+              }
+              if (k == 3) {
+#pragma unroll
+                for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n1[w], cur[w]);
+              } else if (k == 1) {
+#pragma unroll
+                for (int w = 0; w < T::WORDS; ++w) n1[w] = cur[w];
+              } else {
+#pragma unroll
+                for (int w = 0; w < T::WORDS; ++w) n0[w] = cur[w];
+              }
             }
           }
           if (!ok) break;

@@ -335,19 +335,20 @@ __device__ __forceinline__ bool group_root(EpiCtx& e, const TcArgs& a, Emit&& em
     }
     tc_fence_after();
 #pragma unroll
-    for (int c = 0; c < T::COLS / CW; ++c) {
-      uint32_t v0[CW];
-      const uint32_t col = (uint32_t)(e.col0 + CW * c);
-      tmem_ld32(e.tmem + e.lane_addr + b2 + col, v0);
+    for (int c = 0; c < T::COLS / CH; ++c) {  // (chunks of 16 columns: the caller's nodes are live here)
+      uint32_t v0[CH];
+      const uint32_t col = (uint32_t)(e.col0 + CH * c);
+      tmem_ld16(e.tmem + e.lane_addr + b2 + col, v0);
       tmem_wait_ld();
       if constexpr (DUMP) {
         float* d = a.dump + (size_t)pb * a.R * a.C * a.L;
         dump_leaves(d, r, (long long)tn * BN + col, a.R, a.C, a.L, qg * GG, v0);
       }
 #pragma unroll
-      for (int i = 0; i < WC; ++i) {
-        const uint32_t nn = n12[c * WC + i];
-        emit(c * WC + i, pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(nn << 16, nn & 0xFFFF0000u))));
+      for (int i = 0; i < CH / 2; ++i) {
+        const uint32_t nn = n12[c * (CH / 2) + i];
+        emit(c * (CH / 2) + i,
+             pack_bf16x2_of(add_f32x2(f32x2(v0[2 * i], v0[2 * i + 1]), f32x2(nn << 16, nn & 0xFFFF0000u))));
       }
     }
   }
@@ -619,27 +620,28 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
             }
           } else {
             // Three-leaf groups hold a partial node of their own (registers
-            // for four copies of the reader are not there): one copy of the
-            // group reader in a loop that is not unrolled; cur takes the
-            // group's root and then the node over the groups read so far in
-            // this block; n0 keeps the root of group q (then q+2), n1 the
-            // node over groups q, q+1.
+            // for four copies of the reader are not there): two copies, for
+            // the even and the odd group of each pair, in a loop over the
+            // block's pairs; the even one's root goes to n0, the odd one
+            // forms the pair's node in cur, which becomes n1 (first pair) or
+            // the node over the block (second pair).
 #pragma unroll 1
-            for (int k = 0; k < 4 && k < Q; ++k) {
-              if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { cur[w] = g; }, pb, r, tn, q + k)) break;
-              if (k & 1) {
+            for (int k = 0; k < 4 && k < Q; k += 2) {
+              if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q + k)) break;
+              if (Q == 1) {
 #pragma unroll
-                for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n0[w], cur[w]);
+                for (int w = 0; w < T::WORDS; ++w) cur[w] = n0[w];
+                break;
               }
-              if (k == 3) {
+              if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { cur[w] = node2(n0[w], g); }, pb, r, tn,
+                                            q + k + 1))
+                break;
+              if (k == 2) {
 #pragma unroll
                 for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n1[w], cur[w]);
-              } else if (k == 1) {
+              } else if (Q >= 4) {
 #pragma unroll
                 for (int w = 0; w < T::WORDS; ++w) n1[w] = cur[w];
-              } else {
-#pragma unroll
-                for (int w = 0; w < T::WORDS; ++w) n0[w] = cur[w];
               }
             }
           }

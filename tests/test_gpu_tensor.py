@@ -41,7 +41,9 @@ def _ints(shape, seed):
 
 @pytest.mark.parametrize("R,C,K", [(128, 128, 64), (256, 128, 128), (128, 256, 256), (200, 300, 104),
                                    (130, 129, 192), (256, 256, 768), (128, 128, 4096),
-                                   (256, 128, 12288), (384, 384, 3072)])
+                                   (256, 128, 12288), (384, 384, 3072),
+                                   # block folds of short trees: three-leaf groups Q = 2, two-leaf Q = 4
+                                   (200, 136, 384), (130, 200, 512)])
 def test_tc_integer_inputs_bit_exact(G, oracle_mod, R, C, K):
     A, B = _ints((R, K), R + K), _ints((C, K), C + 7 * K)
     got = host(G.detffn_tree_gemm(dev(A), dev(B), path=TENSOR))

@@ -599,50 +599,31 @@ __global__ void __launch_bounds__(TcGeo<BN>::THREADS, 1)
         uint32_t n2[T::WORDS];  // the pending level-2 node (left child over four groups)
         for (int q = 0; q < Q && ok; q += 4) {
           uint32_t n0[T::WORDS], n1[T::WORDS], cur[T::WORDS];
-          if constexpr (GG == 2) {
-            // The block's four group readers hand each root word straight to
-            // the node it enters, so that no node is copied: n0 takes the
-            // root of group q (then of q+2), n1 the node over groups q, q+1,
-            // and cur the node over the block (over all of a shorter tree's
-            // one or two groups).
-            if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q)) break;
-            if (Q >= 2 &&
-                !group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n1[w] = node2(n0[w], g); }, pb, r, tn, q + 1))
-              break;
-            if (Q >= 4) {
-              if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q + 2)) break;
-              if (!group_root<BN, GG, DUMP>(
-                      e, a, [&](int w, uint32_t g) { cur[w] = node2(n1[w], node2(n0[w], g)); }, pb, r, tn, q + 3))
-                break;
-            } else {
-#pragma unroll
-              for (int w = 0; w < T::WORDS; ++w) cur[w] = Q == 2 ? n1[w] : n0[w];
-            }
-          } else {
-            // Three-leaf groups hold a partial node of their own (registers
-            // for four copies of the reader are not there): two copies, for
-            // the even and the odd group of each pair, in a loop over the
-            // block's pairs; the even one's root goes to n0, the odd one
-            // forms the pair's node in cur, which becomes n1 (first pair) or
-            // the node over the block (second pair).
+          // Two copies of the group reader, for the even and the odd group of
+          // each pair, in a loop over the block's pairs; each hands its root
+          // words straight to the node they enter: the even one's root goes
+          // to n0, the odd one forms the pair's node in cur, which becomes n1
+          // (first pair) or is folded with n1 into the node over the block
+          // (second pair).  (Two copies run faster than one copy with a
+          // per-group branch and node copies, and than four copies, whose
+          // code no longer stays in the instruction cache.)
 #pragma unroll 1
-            for (int k = 0; k < 4 && k < Q; k += 2) {
-              if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q + k)) break;
-              if (Q == 1) {
+          for (int k = 0; k < 4 && k < Q; k += 2) {
+            if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { n0[w] = g; }, pb, r, tn, q + k)) break;
+            if (Q == 1) {
 #pragma unroll
-                for (int w = 0; w < T::WORDS; ++w) cur[w] = n0[w];
-                break;
-              }
-              if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { cur[w] = node2(n0[w], g); }, pb, r, tn,
-                                            q + k + 1))
-                break;
-              if (k == 2) {
+              for (int w = 0; w < T::WORDS; ++w) cur[w] = n0[w];
+              break;
+            }
+            if (!group_root<BN, GG, DUMP>(e, a, [&](int w, uint32_t g) { cur[w] = node2(n0[w], g); }, pb, r, tn,
+                                          q + k + 1))
+              break;
+            if (k == 2) {
 #pragma unroll
-                for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n1[w], cur[w]);
-              } else if (Q >= 4) {
+              for (int w = 0; w < T::WORDS; ++w) cur[w] = node2(n1[w], cur[w]);
+            } else if (Q >= 4) {
 #pragma unroll
-                for (int w = 0; w < T::WORDS; ++w) n1[w] = cur[w];
-              }
+              for (int w = 0; w < T::WORDS; ++w) n1[w] = cur[w];
             }
           }
           if (!ok) break;
